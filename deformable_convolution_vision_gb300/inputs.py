@@ -1,0 +1,124 @@
+"""Seeded synthetic inputs for the deformable convolution workloads.
+
+This module draws random tensors and nothing else: it holds none of the
+operator's arithmetic, so the CUDA path and the oracle can both be fed from
+it without sharing any of the method.
+
+Shapes and value distributions are those of the five workloads the library
+is measured on (a tiny fp32 case, a decoder 3x3, the BiRefNet-style ASPP 7x7
+at 256x256 that the "birefnet-lite-1024-webgpu patch_deform.py" page sizes
+at 392 MB of gathered fp16, a batched backbone 3x3 and a non-square 5x5
+boundary case), plus the three kernel sizes of the self-test on the page
+"litert-community/Idol ... deform_conv.py" (x [1,64,33,40] ~ N(0,1),
+offsets N(0,1)*4, mask U(0,2), weight N(0,1)*0.05, no bias).
+
+Every tensor is generated in logical NCHW / OIHW order in fp32 on the CPU,
+then x and weight are rounded to the compute dtype.  Offsets, mask and bias
+stay fp32.
+"""
+
+from dataclasses import dataclass, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    C: int
+    H: int
+    W: int
+    O: int
+    kh: int
+    kw: int
+    pad: int
+    dtype: str            # "f32" or "bf16": dtype of x, weight and out
+    offset_std: float
+    mask: str             # "sigmoid", "uniform", "uniform_zero10", "uniform2", "none"
+    weight_std: float     # 0 -> 1/sqrt(kh*kw*C)
+    bias_std: float       # 0 -> no bias
+    seed: int
+
+    @property
+    def Ho(self):
+        return self.H + 2 * self.pad - self.kh + 1
+
+    @property
+    def Wo(self):
+        return self.W + 2 * self.pad - self.kw + 1
+
+    @property
+    def taps(self):
+        return self.kh * self.kw
+
+    @property
+    def pixels(self):
+        """Output pixels P = B * Ho * Wo."""
+        return self.B * self.Ho * self.Wo
+
+    @property
+    def flops(self):
+        """Effective FLOPs of the contraction, 2 * B*Ho*Wo * O * kh*kw * C."""
+        return 2 * self.pixels * self.O * self.taps * self.C
+
+    def with_(self, **kw):
+        return replace(self, **kw)
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("tiny", 1, 4, 8, 8, 3, 3, 3, 1, "f32", 1.5, "sigmoid", 0.0, 0.1, 0),
+        Workload("decoder3x3", 1, 64, 128, 128, 64, 3, 3, 1, "bf16", 2.0, "sigmoid", 0.0, 0.1, 1),
+        Workload("aspp7x7", 1, 64, 256, 256, 64, 7, 7, 3, "bf16", 3.0, "sigmoid", 0.0, 0.1, 2),
+        Workload("backbone3x3", 8, 256, 64, 64, 256, 3, 3, 1, "bf16", 1.0, "sigmoid", 0.0, 0.1, 3),
+        Workload("boundary5x5", 2, 128, 160, 224, 128, 5, 5, 2, "bf16", 8.0, "uniform_zero10", 0.0, 0.1, 4),
+        # the page's self-test shapes (ks, pad) = (1, 0), (3, 1), (7, 3)
+        Workload("selftest1x1", 1, 64, 33, 40, 256, 1, 1, 0, "f32", 4.0, "uniform2", 0.05, 0.0, 0),
+        Workload("selftest3x3", 1, 64, 33, 40, 256, 3, 3, 1, "f32", 4.0, "uniform2", 0.05, 0.0, 0),
+        Workload("selftest7x7", 1, 64, 33, 40, 256, 7, 7, 3, "f32", 4.0, "uniform2", 0.05, 0.0, 0),
+    ]
+}
+
+# The five measured workloads, in order.
+MAIN = ["tiny", "decoder3x3", "aspp7x7", "backbone3x3", "boundary5x5"]
+
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def make_inputs(wl: Workload, seed=None):
+    """Return a dict of CPU tensors for workload ``wl``.
+
+    x [B,C,H,W] and weight [O,C,kh,kw] are in the compute dtype;
+    offset [B,2*kh*kw,Ho,Wo], mask [B,kh*kw,Ho,Wo] (or None) and bias [O]
+    (or None) are fp32.
+    """
+    g = torch.Generator().manual_seed(wl.seed if seed is None else seed)
+    k = wl.taps
+    x = torch.randn(wl.B, wl.C, wl.H, wl.W, generator=g)
+    offset = torch.randn(wl.B, 2 * k, wl.Ho, wl.Wo, generator=g) * wl.offset_std
+    if wl.mask == "sigmoid":
+        mask = torch.sigmoid(torch.randn(wl.B, k, wl.Ho, wl.Wo, generator=g))
+    elif wl.mask == "uniform":
+        mask = torch.rand(wl.B, k, wl.Ho, wl.Wo, generator=g)
+    elif wl.mask == "uniform2":
+        mask = torch.rand(wl.B, k, wl.Ho, wl.Wo, generator=g) * 2
+    elif wl.mask == "uniform_zero10":
+        mask = torch.rand(wl.B, k, wl.Ho, wl.Wo, generator=g)
+        drop = torch.rand(wl.B, k, wl.Ho, wl.Wo, generator=g) < 0.1
+        mask = torch.where(drop, torch.zeros_like(mask), mask)
+    elif wl.mask == "none":
+        mask = None
+    else:
+        raise ValueError(f"unknown mask kind {wl.mask!r}")
+    wstd = wl.weight_std if wl.weight_std > 0 else 1.0 / (k * wl.C) ** 0.5
+    weight = torch.randn(wl.O, wl.C, wl.kh, wl.kw, generator=g) * wstd
+    bias = torch.randn(wl.O, generator=g) * wl.bias_std if wl.bias_std > 0 else None
+    dt = TORCH_DTYPE[wl.dtype]
+    return {
+        "x": x.to(dt),
+        "offset": offset.float().contiguous(),
+        "mask": None if mask is None else mask.float().contiguous(),
+        "weight": weight.to(dt),
+        "bias": None if bias is None else bias.float().contiguous(),
+    }

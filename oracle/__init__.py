@@ -1,0 +1,139 @@
+"""Oracle for the modulated deformable convolution forward pass.
+
+TEST INFRASTRUCTURE ONLY.  The plain C definition in ``dcn_oracle.c`` is
+what the CUDA path is checked against.  Only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this
+package; the product library never loads it, and it shares no code with the
+CUDA sources.
+
+The arithmetic follows the page "litert-community/Idol ... deform_conv.py"
+(module docstring and the four-corner loop of ``deform_conv2d_gather``):
+bilinear samples at (h - pad + i + dy_k, w - pad + j + dx_k), corners
+outside the image count as 0, each sample scaled by mask_k, contracted over
+(tap, channel) with the weight, plus bias.  Accumulation is fp64; the
+sampling coordinate is fp32 (the page builds its grid in the input dtype,
+fp32 for the fp32 offsets).
+
+All arrays cross this boundary in logical NCHW order:
+x [B,C,H,W] fp32, offset [B,2k,Ho,Wo] fp32, mask [B,k,Ho,Wo] fp32 or None,
+weight [O,C,kh,kw] fp32, bias [O] fp32 or None; results are fp64.
+"""
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "dcn_oracle.c")
+LIBRARY = os.path.join(_HERE, "libdcn_oracle.so")
+
+# -ffp-contract=off: no fused multiply-add, so x86 and Arm hosts give the
+# same bits.  No -ffast-math: floor, comparisons and NaN must follow IEEE.
+CFLAGS = ["-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off"]
+
+
+def compile_oracle(source=SOURCE, output=LIBRARY):
+    """Compile the oracle's C source into a shared library (gcc)."""
+    cmd = ["gcc", *CFLAGS, source, "-o", output, "-lm"]
+    subprocess.run(cmd, check=True)
+    return output
+
+
+def _stale(source, output):
+    return (not os.path.exists(output)
+            or os.path.getmtime(output) < os.path.getmtime(source))
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, path=LIBRARY, source=SOURCE):
+        if path == LIBRARY and _stale(source, path):
+            compile_oracle(source, path)
+        self.path = path
+        lib = ctypes.CDLL(path)
+        f = ctypes.c_void_p
+        i = ctypes.c_int
+        lib.oracle_dcn_forward.argtypes = [f, f, f, f, f, f] + [i] * 9
+        lib.oracle_dcn_forward.restype = i
+        lib.oracle_dcn_forward_points.argtypes = [f, f, f, f, f, f, i, f] + [i] * 9
+        lib.oracle_dcn_forward_points.restype = i
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = i
+        self._lib = lib
+
+    def max_threads(self):
+        return int(self._lib.oracle_max_threads())
+
+    @staticmethod
+    def _f32(a):
+        if a is None:
+            return None
+        if hasattr(a, "detach"):  # torch tensor
+            a = a.detach().to("cpu").float().numpy()
+        return np.ascontiguousarray(a, dtype=np.float32)
+
+    @staticmethod
+    def _ptr(a):
+        return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+    def _prepare(self, x, offset, mask, weight, bias, pad):
+        x, offset, mask, weight, bias = (self._f32(t) for t in (x, offset, mask, weight, bias))
+        B, C, H, W = x.shape
+        O, C2, kh, kw = weight.shape
+        if C2 != C:
+            raise ValueError("weight channel count does not match x")
+        Ho, Wo = H + 2 * pad - kh + 1, W + 2 * pad - kw + 1
+        if offset.shape != (B, 2 * kh * kw, Ho, Wo):
+            raise ValueError(f"offset shape {offset.shape} != {(B, 2 * kh * kw, Ho, Wo)}")
+        if mask is not None and mask.shape != (B, kh * kw, Ho, Wo):
+            raise ValueError(f"mask shape {mask.shape} != {(B, kh * kw, Ho, Wo)}")
+        if bias is not None and bias.shape != (O,):
+            raise ValueError("bias must have shape [O]")
+        return (x, offset, mask, weight, bias), (B, C, H, W, O, kh, kw, pad), (Ho, Wo)
+
+    def forward(self, x, offset, mask, weight, bias, pad, nthreads=0):
+        """Whole output [B, O, Ho, Wo] in fp64."""
+        arrs, dims, (Ho, Wo) = self._prepare(x, offset, mask, weight, bias, pad)
+        B, O = dims[0], dims[4]
+        out = np.empty((B, O, Ho, Wo), dtype=np.float64)
+        rc = self._lib.oracle_dcn_forward(*(self._ptr(a) for a in arrs), self._ptr(out),
+                                          *dims, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_dcn_forward rejected its arguments")
+        return out
+
+    def forward_points(self, x, offset, mask, weight, bias, pad, points, nthreads=0):
+        """Selected pixels: points is an int array [n, 3] of (b, h, w);
+        returns [n, O] fp64."""
+        arrs, dims, _ = self._prepare(x, offset, mask, weight, bias, pad)
+        pts = np.ascontiguousarray(points, dtype=np.int32).reshape(-1, 3)
+        n = pts.shape[0]
+        out = np.empty((n, dims[4]), dtype=np.float64)
+        rc = self._lib.oracle_dcn_forward_points(*(self._ptr(a) for a in arrs),
+                                                 self._ptr(pts), n, self._ptr(out),
+                                                 *dims, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_dcn_forward_points rejected its arguments")
+        return out
+
+
+_default = None
+
+
+def get():
+    """The oracle built from this directory's source (compiled on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def forward(*args, **kwargs):
+    return get().forward(*args, **kwargs)
+
+
+def forward_points(*args, **kwargs):
+    return get().forward_points(*args, **kwargs)
