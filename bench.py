@@ -1,0 +1,389 @@
+"""Benchmark of the deformable convolution forward pass on GB300.
+
+One step = one full forward pass (weight pack + fused sampling/contraction/
+epilogue kernel) over the 7x7, C = O = 64, 256 x 256 ASPP workload, inputs
+already resident in device memory.  L2 is flushed (a 256 MiB write, twice
+the 129 MB L2) before every step, outside the timed events.  Every step is
+timed with CUDA events on the stream the kernels run on; ms_per_step is
+the mean, the maximum over ranks when several run (weak scaling: every rank
+runs the same workload, no collective on the data path).
+
+Prints one JSON line.  --impl reference times the CPU oracle instead.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "deform-conv fwd effective TFLOP/s & out-pixels/s on 1 GB300; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+MAIN_KERNEL = "dcn_tc_kernel"
+TC_SOURCES = ["dcn_tc.cu", "dcn_device.cuh", "dcn_sampling.cuh", "dcn_kernels.h"]
+
+
+# ----------------------------------------------------------- host helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def reduce_max(value, world):
+    """Maximum of a float over all ranks (identity for one rank)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, max_seconds):
+    """Weak scaling: every rank processes units_per_rank; the job's rate is
+    all units over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured (MEASURED_PEAKS.json)"
+    return dict(FALLBACK_PEAKS), "fallback (profiling recipe)"
+
+
+def algorithmic_bytes(wl):
+    """x, offset, mask, weight, bias and out, each moved once."""
+    es = 2 if wl.dtype == "bf16" else 4
+    return (wl.B * wl.H * wl.W * wl.C * es + wl.B * 2 * wl.taps * wl.Ho * wl.Wo * 4
+            + (wl.B * wl.taps * wl.Ho * wl.Wo * 4 if wl.mask != "none" else 0)
+            + wl.O * wl.C * wl.taps * es + (wl.O * 4 if wl.bias_std > 0 else 0)
+            + wl.pixels * wl.O * es)
+
+
+def tc_source_hash():
+    h = hashlib.sha256()
+    for name in TC_SOURCES:
+        with open(os.path.join(ROOT, "deformable_convolution_vision_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(workload):
+    """DRAM bytes per launch of the main kernel from the committed ncu
+    summary, or None if none was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        d = json.load(fh)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != tc_source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.device_index), "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, r[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def time_oracle(wl, inp, seconds, seed=0):
+    """Run the oracle on batches of random output pixels (all O channels each)
+    until `seconds` have passed.  Returns (pixels, elapsed s, threads)."""
+    import numpy as np
+    import oracle
+    orc = oracle.get()
+    threads = orc.max_threads()
+    rng = np.random.default_rng(seed)
+    batch = max(threads * 4, 16)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        flat = rng.integers(0, wl.pixels, size=batch)
+        pts = np.stack([flat // (wl.Ho * wl.Wo), (flat // wl.Wo) % wl.Ho, flat % wl.Wo], 1)
+        orc.forward_points(inp["x"], inp["offset"], inp["mask"], inp["weight"], inp["bias"],
+                           wl.pad, pts)
+        done += batch
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done, el, threads
+
+
+def cpu_baseline(wl, inp, seconds):
+    px, el, threads = time_oracle(wl, inp, seconds)
+    flops = 2.0 * px * wl.O * wl.taps * wl.C
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{px} random output pixels x all {wl.O} channels of {wl.name} "
+                      f"({el:.1f} s, fp64 C oracle, OpenMP over pixels)",
+            "out_pixels_per_s": px / el}
+
+
+# ------------------------------------------------------------------- arms
+
+def run_reference(args, wl, rank, world):
+    """The oracle, timed on the host cores: each step is a bounded sample."""
+    if rank != 0:
+        return
+    from deformable_convolution_vision_gb300.inputs import make_inputs
+    inp = make_inputs(wl)
+    per_step = args.reference_step_seconds
+    for _ in range(args.warmup):
+        time_oracle(wl, inp, per_step * 0.25)
+    steps = []
+    for k in range(args.steps):
+        px, el, threads = time_oracle(wl, inp, per_step, seed=k + 1)
+        steps.append((px, el))
+    px = sum(s[0] for s in steps)
+    el = sum(s[1] for s in steps)
+    flops = 2.0 * px * wl.O * wl.taps * wl.C
+    value = flops / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(wl, "no GPU: host caches only"),
+        "out_pixels_per_s": px / el,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{px} random output pixels x all {wl.O} channels over "
+                                   f"{args.steps} steps of ~{per_step} s"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(wl, l2):
+    return {"workload": f"{wl.name}: B={wl.B} C={wl.C} O={wl.O} H={wl.H} W={wl.W} "
+                        f"{wl.kh}x{wl.kw} pad={wl.pad} {wl.dtype} offsets~N(0,{wl.offset_std}) "
+                        f"mask {wl.mask}",
+            "B": wl.B, "C": wl.C, "O": wl.O, "H": wl.H, "W": wl.W, "kh": wl.kh, "kw": wl.kw,
+            "pad": wl.pad, "out_pixels": wl.pixels, "flops_per_step": wl.flops, "l2": l2}
+
+
+def run_ours(args, wl, rank, local_rank, world):
+    import torch
+    import deformable_convolution_vision_gb300 as dcn
+    from deformable_convolution_vision_gb300.inputs import make_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = make_inputs(wl)
+    x = inp["x"].to(dev).contiguous(memory_format=torch.channels_last)
+    off = inp["offset"].to(dev)
+    m = None if inp["mask"] is None else inp["mask"].to(dev)
+    w = inp["weight"].to(dev).contiguous()
+    b = None if inp["bias"] is None else inp["bias"].to(dev)
+    out = torch.empty((wl.B, wl.O, wl.Ho, wl.Wo), dtype=x.dtype, device=dev,
+                      memory_format=torch.channels_last)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    code = dcn.DCN_BF16 if wl.dtype == "bf16" else dcn.DCN_F32
+    dims = (wl.B, wl.C, wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad, code)
+    h = dcn.Handle()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dcn.dcn_pack_weight(h.h, w, wl.O, wl.C, wl.kh, wl.kw, code, stream)
+        dcn.dcn_forward_packed(h.h, x, off, m, b, out, *dims, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    if dcn.dcn_sync_status(h.h, stream) != 0:
+        raise RuntimeError("device status set during warm-up")
+    path_taken = dcn.dcn_last_path(h.h)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        dcn.dcn_pack_weight(h.h, w, wl.O, wl.C, wl.kh, wl.kw, code, stream)
+        ev[k][1].record(stream)
+        dcn.dcn_forward_packed(h.h, x, off, m, b, out, *dims, stream)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    if dcn.dcn_sync_status(h.h, stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    main_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    pack_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ms = statistics.fmean(step_ms)
+    ms_max = reduce_max(ms, world)
+    main_mean = statistics.fmean(main_ms)
+
+    # end to end through the host-buffer entry point: pinned host inputs in,
+    # pinned host output back, copies inside the timed region
+    hx = inp["x"].permute(0, 2, 3, 1).contiguous().pin_memory()
+    hoff = inp["offset"].pin_memory()
+    hm = None if inp["mask"] is None else inp["mask"].pin_memory()
+    hw = inp["weight"].contiguous().pin_memory()
+    hb = None if inp["bias"] is None else inp["bias"].pin_memory()
+    hout = torch.empty((wl.B, wl.Ho, wl.Wo, wl.O), dtype=x.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hoff, hm, hw, hb) if t is not None)
+    d2h = hout.numel() * hout.element_size()
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(max(args.warmup, 3)):
+        dcn.dcn_forward_host(h.h, hx, hoff, hm, hw, hb, hout, *dims, stream)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        dcn.dcn_forward_host(h.h, hx, hoff, hm, hw, hb, hout, *dims, stream)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_max = reduce_max(e2e_s, world)
+    h.close()
+
+    if rank != 0:
+        return
+    pk, pk_src = peaks()
+    achieved = wl.flops / (main_mean * 1e-3) / 1e12
+    value = whole_job_rate(wl.flops, world, ms_max * 1e-3) / 1e12
+    t_tc = wl.flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = algorithmic_bytes(wl) / (pk["hbm_gbs"] * 1e9)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic",
+        "config": config_dict(wl, f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write), "
+                                  f"outside the timed events"),
+        "out_pixels_per_s": whole_job_rate(wl.pixels, world, ms_max * 1e-3),
+        "roofline_frac_step": max(t_tc, t_hbm) / (ms_max * 1e-3),
+        "step_ms": {"mean": ms, "min": min(step_ms), "median": statistics.median(step_ms),
+                    "pack_mean": statistics.fmean(pack_ms), "main_mean": main_mean,
+                    "main_min": min(main_ms)},
+        "roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "achieved": achieved,
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / pk["bf16_tflops"], "traffic": dram_traffic(wl.name),
+                     "kernel": MAIN_KERNEL if path_taken == dcn.DCN_PATH_TC else "dcn_simt_kernel",
+                     "peak_source": pk_src + ", bf16 dense burst",
+                     "t_tensor_us": t_tc * 1e6, "t_hbm_us": t_hbm * 1e6,
+                     "algorithmic_bytes": algorithmic_bytes(wl)},
+        "e2e": {"value": whole_job_rate(wl.flops, world, e2e_max) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_max * 1e3, "api": "dcn_forward_host (pinned host buffers)"},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+        "wall_s_timed_region": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="aspp7x7")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-step-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from deformable_convolution_vision_gb300.inputs import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only
+        run_reference(args, wl, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, wl, rank, local_rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,108 @@
+"""GB300 (sm_103a) modulated deformable convolution, forward pass.
+
+torchvision ``deform_conv2d`` semantics with stride 1, dilation 1, one
+offset group and one weight group, computed by hand-written CUDA kernels
+behind the C ABI declared in ``include/dcn.h``.  This package is the thin
+Python side: ``binding`` maps the C entry points one to one, and
+``deform_conv2d`` below shapes PyTorch tensors into one call.
+"""
+
+from . import binding
+from .binding import (DCN_BF16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC, DcnError,
+                      dcn_create, dcn_destroy, dcn_forward, dcn_forward_host, dcn_forward_packed,
+                      dcn_last_path, dcn_pack_weight, dcn_selftest_timeout, dcn_set_path,
+                      dcn_status_string, dcn_sync_status)
+
+__all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF16",
+           "DCN_PATH_AUTO", "DCN_PATH_SIMT", "DCN_PATH_TC", "dcn_create", "dcn_destroy",
+           "dcn_forward", "dcn_forward_host", "dcn_forward_packed", "dcn_pack_weight",
+           "dcn_set_path", "dcn_last_path", "dcn_sync_status", "dcn_selftest_timeout",
+           "dcn_status_string"]
+
+
+class Handle:
+    """Owns one ``dcn_handle_t`` (workspace + status word) on the current device."""
+
+    def __init__(self, path=DCN_PATH_AUTO):
+        self.h = dcn_create()
+        if path != DCN_PATH_AUTO:
+            dcn_set_path(self.h, path)
+
+    def close(self):
+        if self.h is not None:
+            dcn_destroy(self.h)
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return DCN_F32
+    if t.dtype == torch.bfloat16:
+        return DCN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def deform_conv2d(x, offset, weight, bias=None, padding=0, mask=None, handle=None, out=None,
+                  stream=None):
+    """Modulated deformable convolution forward on CUDA tensors.
+
+    x       [B, C, H, W] float32/bfloat16, channels_last memory format
+    offset  [B, 2*kh*kw, Ho, Wo] float32, contiguous (dy, dx per tap)
+    weight  [O, C, kh, kw] same dtype as x, contiguous
+    bias    [O] float32 or None
+    mask    [B, kh*kw, Ho, Wo] float32 or None
+    Returns out [B, O, Ho, Wo] in x's dtype, channels_last memory format.
+    Layouts are checked, never converted.
+    """
+    import torch
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    if not x.is_contiguous(memory_format=torch.channels_last):
+        raise ValueError("x must be channels_last contiguous")
+    for name, t in (("offset", offset), ("weight", weight), ("bias", bias), ("mask", mask)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if offset.dtype != torch.float32 or (mask is not None and mask.dtype != torch.float32) or \
+            (bias is not None and bias.dtype != torch.float32):
+        raise TypeError("offset, mask and bias must be float32")
+    if weight.dtype != x.dtype:
+        raise TypeError("weight must have x's dtype")
+    B, C, H, W = x.shape
+    O, C2, kh, kw = weight.shape
+    if C2 != C:
+        raise ValueError("weight and x disagree on C")
+    pad = int(padding)
+    Ho, Wo = H + 2 * pad - kh + 1, W + 2 * pad - kw + 1
+    if tuple(offset.shape) != (B, 2 * kh * kw, Ho, Wo):
+        raise ValueError(f"offset must be {(B, 2 * kh * kw, Ho, Wo)}")
+    if mask is not None and tuple(mask.shape) != (B, kh * kw, Ho, Wo):
+        raise ValueError(f"mask must be {(B, kh * kw, Ho, Wo)}")
+    if out is None:
+        out = torch.empty((B, O, Ho, Wo), dtype=x.dtype, device=x.device,
+                          memory_format=torch.channels_last)
+    own = handle is None
+    h = Handle() if own else handle
+    try:
+        dcn_forward(h.h, x, offset, mask, weight, bias, out, B, C, H, W, O, kh, kw, pad,
+                    _dtype_code(x), stream)
+        if own:
+            st = dcn_sync_status(h.h, stream)
+            if st != 0:
+                raise DcnError(st, "deform_conv2d")
+    finally:
+        if own:
+            h.close()
+    return out

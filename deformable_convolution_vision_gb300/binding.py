@@ -1,0 +1,144 @@
+"""ctypes binding of ``libdcn.so`` with the C ABI's names.
+
+Argument marshalling only: tensors become device (or host) pointers, the
+stream becomes a ``cudaStream_t``; every step of the forward pass runs in
+the library's CUDA kernels.  There is no fallback: if the library is not
+built, every call raises.
+"""
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libdcn.so")
+
+DCN_F32, DCN_BF16 = 0, 1
+DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC = 0, 1, 2
+STATUS = {0: "DCN_OK", 1: "DCN_ERR_INVALID_ARG", 2: "DCN_ERR_UNSUPPORTED", 3: "DCN_ERR_CUDA",
+          4: "DCN_ERR_NO_DEVICE", 5: "DCN_ERR_OOM", 6: "DCN_ERR_TIMEOUT"}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_forward_packed",
+           "dcn_forward_host", "dcn_set_path", "dcn_last_path", "dcn_sync_status",
+           "dcn_selftest_timeout", "dcn_status_string"]
+
+
+class DcnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+_lib = None
+
+
+def load():
+    """Load libdcn.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIBRARY):
+        raise RuntimeError(f"{LIBRARY} is not built; run deformable_convolution_vision_gb300.build.build()")
+    lib = ctypes.CDLL(LIBRARY)
+    P, I, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+    fwd = [P, P, P, P, P, P, P] + [I] * 9 + [P]
+    sig = {
+        "dcn_create": ([ctypes.POINTER(P)], I),
+        "dcn_destroy": ([P], I),
+        "dcn_forward": (fwd, I),
+        "dcn_pack_weight": ([P, P, I, I, I, I, I, P], I),
+        "dcn_forward_packed": ([P, P, P, P, P, P] + [I] * 9 + [P], I),
+        "dcn_forward_host": (fwd, I),
+        "dcn_set_path": ([P, I], I),
+        "dcn_last_path": ([P], I),
+        "dcn_sync_status": ([P, P], I),
+        "dcn_selftest_timeout": ([P, LL, P], I),
+        "dcn_status_string": ([I], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    """Pointer of a tensor (or an int address, or None)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status, where):
+    if status != 0:
+        raise DcnError(status, where)
+
+
+def dcn_status_string(status):
+    return load().dcn_status_string(status).decode()
+
+
+def dcn_create():
+    h = ctypes.c_void_p()
+    _check(load().dcn_create(ctypes.byref(h)), "dcn_create")
+    return h
+
+
+def dcn_destroy(h):
+    _check(load().dcn_destroy(h), "dcn_destroy")
+
+
+def dcn_forward(h, x, offset, mask, weight, bias, out, B, C, H, W, O, kh, kw, pad, dtype,
+                stream=None):
+    _check(load().dcn_forward(h, _ptr(x), _ptr(offset), _ptr(mask), _ptr(weight), _ptr(bias),
+                              _ptr(out), B, C, H, W, O, kh, kw, pad, dtype, _stream(stream)),
+           "dcn_forward")
+
+
+def dcn_pack_weight(h, weight, O, C, kh, kw, dtype, stream=None):
+    _check(load().dcn_pack_weight(h, _ptr(weight), O, C, kh, kw, dtype, _stream(stream)),
+           "dcn_pack_weight")
+
+
+def dcn_forward_packed(h, x, offset, mask, bias, out, B, C, H, W, O, kh, kw, pad, dtype,
+                       stream=None):
+    _check(load().dcn_forward_packed(h, _ptr(x), _ptr(offset), _ptr(mask), _ptr(bias), _ptr(out),
+                                     B, C, H, W, O, kh, kw, pad, dtype, _stream(stream)),
+           "dcn_forward_packed")
+
+
+def dcn_forward_host(h, x, offset, mask, weight, bias, out, B, C, H, W, O, kh, kw, pad, dtype,
+                     stream=None):
+    _check(load().dcn_forward_host(h, _ptr(x), _ptr(offset), _ptr(mask), _ptr(weight), _ptr(bias),
+                                   _ptr(out), B, C, H, W, O, kh, kw, pad, dtype, _stream(stream)),
+           "dcn_forward_host")
+
+
+def dcn_set_path(h, path):
+    _check(load().dcn_set_path(h, path), "dcn_set_path")
+
+
+def dcn_last_path(h):
+    return load().dcn_last_path(h)
+
+
+def dcn_sync_status(h, stream=None):
+    """Returns the status code (0 = OK) instead of raising, so callers can
+    inspect DCN_ERR_TIMEOUT."""
+    return load().dcn_sync_status(h, _stream(stream))
+
+
+def dcn_selftest_timeout(h, timeout_ns, stream=None):
+    _check(load().dcn_selftest_timeout(h, int(timeout_ns), _stream(stream)), "dcn_selftest_timeout")

@@ -1,0 +1,341 @@
+// C ABI of the deformable convolution forward pass: argument checks,
+// handle/workspace management and kernel selection.  Every entry point
+// validates before launching (the entry-check-then-launch pattern of the
+// "StyleGAN2 upfirdn2d" tutorial page, its C++ entry section) and reports a
+// status code instead of throwing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "dcn.h"
+#include "dcn_kernels.h"
+
+struct dcn_handle_s {
+    int device = 0;
+    int sm_count = 0;
+    int path = DCN_PATH_AUTO;
+    int last_path = -1;
+
+    // packed weight [O][kh*kw*C]
+    void *wpack = nullptr;
+    size_t wpack_cap = 0;
+    int pk_O = 0, pk_C = 0, pk_kh = 0, pk_kw = 0, pk_dtype = -1;
+
+    unsigned *status = nullptr;  // device status word
+
+    // device staging for dcn_forward_host: x, offset, mask, weight, bias, out
+    void *stage[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    size_t stage_cap[6] = {0, 0, 0, 0, 0, 0};
+
+    PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;
+};
+
+namespace {
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
+constexpr long long kIndexLimit = (1ll << 31) - 1;
+
+inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+inline bool aligned(const void *p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+inline size_t esize(int dtype) { return dtype == DCN_F32 ? 4 : 2; }
+
+dcn_status_t check_dims(int B, int C, int H, int W, int O, int kh, int kw, int pad, int dtype) {
+    if (dtype != DCN_F32 && dtype != DCN_BF16) return DCN_ERR_INVALID_ARG;
+    if (B <= 0 || C <= 0 || H <= 0 || W <= 0 || O <= 0 || kh <= 0 || kw <= 0 || pad < 0)
+        return DCN_ERR_INVALID_ARG;
+    const long long Ho = static_cast<long long>(H) + 2ll * pad - kh + 1;
+    const long long Wo = static_cast<long long>(W) + 2ll * pad - kw + 1;
+    if (Ho <= 0 || Wo <= 0) return DCN_ERR_INVALID_ARG;
+    const long long taps = static_cast<long long>(kh) * kw;
+    if (taps > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H * W * C > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * 2 * taps * Ho * Wo > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * Ho * Wo * O > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(O) * C * taps > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    return DCN_OK;
+}
+
+// Grow a device buffer in stream order.
+dcn_status_t ensure(void **buf, size_t *cap, size_t bytes, cudaStream_t s) {
+    if (*cap >= bytes && *buf) return DCN_OK;
+    if (*buf) {
+        if (cudaFreeAsync(*buf, s) != cudaSuccess) return DCN_ERR_CUDA;
+        *buf = nullptr;
+        *cap = 0;
+    }
+    if (cudaMallocAsync(buf, bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        *buf = nullptr;
+        return DCN_ERR_OOM;
+    }
+    *cap = bytes;
+    return DCN_OK;
+}
+
+dcn_status_t pack_impl(dcn_handle_t h, const void *weight, int O, int C, int kh, int kw,
+                       int dtype, cudaStream_t s) {
+    const size_t bytes = static_cast<size_t>(O) * C * kh * kw * esize(dtype);
+    dcn_status_t st = ensure(&h->wpack, &h->wpack_cap, bytes, s);
+    if (st != DCN_OK) return st;
+    if (dcn::launch_pack_weight(weight, h->wpack, O, C, kh, kw, dtype, s) != cudaSuccess)
+        return DCN_ERR_CUDA;
+    h->pk_O = O; h->pk_C = C; h->pk_kh = kh; h->pk_kw = kw; h->pk_dtype = dtype;
+    return DCN_OK;
+}
+
+dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *offset,
+                                 const float *mask, const float *bias, void *out,
+                                 int B, int C, int H, int W, int O, int kh, int kw, int pad,
+                                 int dtype, cudaStream_t s) {
+    if (h->pk_O != O || h->pk_C != C || h->pk_kh != kh || h->pk_kw != kw || h->pk_dtype != dtype)
+        return DCN_ERR_INVALID_ARG;
+
+    dcn::Params p;
+    p.x = x; p.offset = offset; p.mask = mask; p.wpack = h->wpack; p.bias = bias; p.out = out;
+    p.B = B; p.C = C; p.H = H; p.W = W; p.O = O; p.kh = kh; p.kw = kw; p.pad = pad;
+    p.Ho = H + 2 * pad - kh + 1;
+    p.Wo = W + 2 * pad - kw + 1;
+    p.P = B * p.Ho * p.Wo;
+    p.K = kh * kw * C;
+    p.status = h->status;
+    p.timeout_ns = kWaitLimitNs;
+
+    const bool tc_ok = dtype == DCN_BF16 && dcn::tc_supported(C, O) &&
+                       aligned(x, 16) && aligned(out, 16) && aligned(h->wpack, 16);
+    int path = h->path;
+    if (path == DCN_PATH_AUTO) path = tc_ok ? DCN_PATH_TC : DCN_PATH_SIMT;
+    if (path == DCN_PATH_TC && !tc_ok) return DCN_ERR_UNSUPPORTED;
+
+    cudaError_t e;
+    if (path == DCN_PATH_TC) {
+        CUtensorMap map;
+        std::memset(&map, 0, sizeof(map));
+        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(O)};
+        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p.K) * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(O)};
+        const cuuint32_t estride[2] = {1, 1};
+        CUresult r = h->encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->wpack, gdim,
+                                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return DCN_ERR_CUDA;
+        e = dcn::launch_tc(p, map, s);
+    } else {
+        e = dcn::launch_simt(p, dtype, s);
+    }
+    if (e != cudaSuccess) return DCN_ERR_CUDA;
+    h->last_path = path;
+    return DCN_OK;
+}
+
+dcn_status_t check_forward_ptrs(const void *x, const float *offset, const float *mask,
+                                const void *weight, const float *bias, void *out, int dtype,
+                                bool need_weight) {
+    if (!x || !offset || !out || (need_weight && !weight)) return DCN_ERR_INVALID_ARG;
+    const size_t es = esize(dtype);
+    if (!aligned(x, es) || !aligned(out, es) || (weight && !aligned(weight, es)))
+        return DCN_ERR_INVALID_ARG;
+    if (!aligned(offset, 4) || (mask && !aligned(mask, 4)) || (bias && !aligned(bias, 4)))
+        return DCN_ERR_INVALID_ARG;
+    return DCN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dcn_status_t dcn_create(dcn_handle_t *out_handle) {
+    if (!out_handle) return DCN_ERR_INVALID_ARG;
+    *out_handle = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+        cudaGetLastError();
+        return DCN_ERR_NO_DEVICE;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DCN_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return DCN_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return DCN_ERR_UNSUPPORTED;
+
+    dcn_handle_t h = new (std::nothrow) dcn_handle_s();
+    if (!h) return DCN_ERR_OOM;
+    h->device = dev;
+    h->sm_count = prop.multiProcessorCount;
+
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        delete h;
+        return DCN_ERR_CUDA;
+    }
+    h->encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+
+    if (cudaMalloc(&h->status, sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return DCN_ERR_OOM;
+    }
+    if (cudaMemset(h->status, 0, sizeof(unsigned)) != cudaSuccess) {
+        cudaFree(h->status);
+        delete h;
+        return DCN_ERR_CUDA;
+    }
+    *out_handle = h;
+    return DCN_OK;
+}
+
+dcn_status_t dcn_destroy(dcn_handle_t h) {
+    if (!h) return DCN_OK;
+    dcn_status_t st = DCN_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess) st = DCN_ERR_CUDA;
+    if (h->wpack) cudaFree(h->wpack);
+    if (h->status) cudaFree(h->status);
+    for (int i = 0; i < 6; ++i)
+        if (h->stage[i]) cudaFree(h->stage[i]);
+    delete h;
+    return st;
+}
+
+dcn_status_t dcn_pack_weight(dcn_handle_t h, const void *weight, int O, int C, int kh, int kw,
+                             int dtype, void *stream) {
+    if (!h || !weight) return DCN_ERR_INVALID_ARG;
+    if (dtype != DCN_F32 && dtype != DCN_BF16) return DCN_ERR_INVALID_ARG;
+    if (O <= 0 || C <= 0 || kh <= 0 || kw <= 0) return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(O) * C * kh * kw > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (!aligned(weight, esize(dtype))) return DCN_ERR_INVALID_ARG;
+    return pack_impl(h, weight, O, C, kh, kw, dtype, as_stream(stream));
+}
+
+dcn_status_t dcn_forward_packed(dcn_handle_t h, const void *x, const float *offset,
+                                const float *mask, const float *bias, void *out,
+                                int B, int C, int H, int W, int O, int kh, int kw, int pad,
+                                int dtype, void *stream) {
+    if (!h) return DCN_ERR_INVALID_ARG;
+    dcn_status_t st = check_dims(B, C, H, W, O, kh, kw, pad, dtype);
+    if (st != DCN_OK) return st;
+    st = check_forward_ptrs(x, offset, mask, nullptr, bias, out, dtype, false);
+    if (st != DCN_OK) return st;
+    return forward_packed_impl(h, x, offset, mask, bias, out, B, C, H, W, O, kh, kw, pad, dtype,
+                               as_stream(stream));
+}
+
+dcn_status_t dcn_forward(dcn_handle_t h, const void *x, const float *offset, const float *mask,
+                         const void *weight, const float *bias, void *out,
+                         int B, int C, int H, int W, int O, int kh, int kw, int pad,
+                         int dtype, void *stream) {
+    if (!h) return DCN_ERR_INVALID_ARG;
+    dcn_status_t st = check_dims(B, C, H, W, O, kh, kw, pad, dtype);
+    if (st != DCN_OK) return st;
+    st = check_forward_ptrs(x, offset, mask, weight, bias, out, dtype, true);
+    if (st != DCN_OK) return st;
+    // a forced tensor-core path that cannot run this shape launches nothing
+    if (h->path == DCN_PATH_TC &&
+        !(dtype == DCN_BF16 && dcn::tc_supported(C, O) && aligned(x, 16) && aligned(out, 16)))
+        return DCN_ERR_UNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    st = pack_impl(h, weight, O, C, kh, kw, dtype, s);
+    if (st != DCN_OK) return st;
+    return forward_packed_impl(h, x, offset, mask, bias, out, B, C, H, W, O, kh, kw, pad, dtype, s);
+}
+
+dcn_status_t dcn_sync_status(dcn_handle_t h, void *stream) {
+    if (!h) return DCN_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DCN_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, h->status, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DCN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DCN_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemsetAsync(h->status, 0, sizeof(unsigned), s) != cudaSuccess) return DCN_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return DCN_ERR_CUDA;
+        return DCN_ERR_TIMEOUT;
+    }
+    return DCN_OK;
+}
+
+dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset,
+                              const float *mask, const void *weight, const float *bias, void *out,
+                              int B, int C, int H, int W, int O, int kh, int kw, int pad,
+                              int dtype, void *stream) {
+    if (!h) return DCN_ERR_INVALID_ARG;
+    dcn_status_t st = check_dims(B, C, H, W, O, kh, kw, pad, dtype);
+    if (st != DCN_OK) return st;
+    st = check_forward_ptrs(x, offset, mask, weight, bias, out, dtype, true);
+    if (st != DCN_OK) return st;
+    const size_t es = esize(dtype);
+    const size_t Ho = static_cast<size_t>(H) + 2 * pad - kh + 1;
+    const size_t Wo = static_cast<size_t>(W) + 2 * pad - kw + 1;
+    const size_t taps = static_cast<size_t>(kh) * kw;
+    const size_t bytes[6] = {
+        static_cast<size_t>(B) * H * W * C * es,
+        static_cast<size_t>(B) * 2 * taps * Ho * Wo * 4,
+        mask ? static_cast<size_t>(B) * taps * Ho * Wo * 4 : 0,
+        static_cast<size_t>(O) * C * taps * es,
+        bias ? static_cast<size_t>(O) * 4 : 0,
+        static_cast<size_t>(B) * Ho * Wo * O * es,
+    };
+    const void *src[5] = {x, offset, mask, weight, bias};
+    cudaStream_t s = as_stream(stream);
+    for (int i = 0; i < 6; ++i) {
+        if (bytes[i] == 0) continue;
+        // round up so every staging buffer starts 256-byte aligned and is reusable
+        st = ensure(&h->stage[i], &h->stage_cap[i], (bytes[i] + 255) & ~static_cast<size_t>(255), s);
+        if (st != DCN_OK) return st;
+    }
+    for (int i = 0; i < 5; ++i) {
+        if (bytes[i] == 0) continue;
+        if (cudaMemcpyAsync(h->stage[i], src[i], bytes[i], cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return DCN_ERR_CUDA;
+    }
+    st = dcn_forward(h, h->stage[0], static_cast<const float *>(h->stage[1]),
+                     mask ? static_cast<const float *>(h->stage[2]) : nullptr, h->stage[3],
+                     bias ? static_cast<const float *>(h->stage[4]) : nullptr, h->stage[5],
+                     B, C, H, W, O, kh, kw, pad, dtype, stream);
+    if (st != DCN_OK) return st;
+    if (cudaMemcpyAsync(out, h->stage[5], bytes[5], cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DCN_ERR_CUDA;
+    return dcn_sync_status(h, stream);
+}
+
+dcn_status_t dcn_set_path(dcn_handle_t h, int path) {
+    if (!h || path < DCN_PATH_AUTO || path > DCN_PATH_TC) return DCN_ERR_INVALID_ARG;
+    h->path = path;
+    return DCN_OK;
+}
+
+int dcn_last_path(dcn_handle_t h) { return h ? h->last_path : -1; }
+
+dcn_status_t dcn_selftest_timeout(dcn_handle_t h, long long timeout_ns, void *stream) {
+    if (!h || timeout_ns <= 0 || timeout_ns > 10000000000ll) return DCN_ERR_INVALID_ARG;
+    if (dcn::launch_selftest_timeout(h->status, static_cast<unsigned long long>(timeout_ns),
+                                     as_stream(stream)) != cudaSuccess)
+        return DCN_ERR_CUDA;
+    return DCN_OK;
+}
+
+const char *dcn_status_string(dcn_status_t s) {
+    switch (s) {
+        case DCN_OK: return "DCN_OK";
+        case DCN_ERR_INVALID_ARG: return "DCN_ERR_INVALID_ARG";
+        case DCN_ERR_UNSUPPORTED: return "DCN_ERR_UNSUPPORTED";
+        case DCN_ERR_CUDA: return "DCN_ERR_CUDA";
+        case DCN_ERR_NO_DEVICE: return "DCN_ERR_NO_DEVICE";
+        case DCN_ERR_OOM: return "DCN_ERR_OOM";
+        case DCN_ERR_TIMEOUT: return "DCN_ERR_TIMEOUT";
+    }
+    return "DCN_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,42 @@
+// Internal interface between the C ABI (dcn_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dcn {
+
+// Everything a forward kernel needs, passed by value.  Device pointers.
+struct Params {
+    const void *x;        // [B, H, W, C] channels-last
+    const float *offset;  // [B, 2*kh*kw, Ho, Wo]
+    const float *mask;    // [B, kh*kw, Ho, Wo] or nullptr
+    const void *wpack;    // [O][kh*kw*C], tap-major / channel-minor
+    const float *bias;    // [O] or nullptr
+    void *out;            // [B, Ho, Wo, O] channels-last
+    int B, C, H, W, O, kh, kw, pad, Ho, Wo;
+    int P;                // B * Ho * Wo output pixels
+    int K;                // kh * kw * C
+    unsigned *status;     // device status word (timeout bit)
+    unsigned long long timeout_ns;  // bound of every barrier wait
+};
+
+enum Dtype { kF32 = 0, kBF16 = 1 };
+
+// S0: weight [O, C, kh, kw] -> packed [O][(i*kw + j)*C + c].
+cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int C, int kh, int kw,
+                               int dtype, cudaStream_t stream);
+
+// CUDA-core fused sample + contraction + epilogue (fp32 or bf16 operands).
+cudaError_t launch_simt(const Params &p, int dtype, cudaStream_t stream);
+
+// tcgen05 fused implicit GEMM (bf16 operands).  `wmap` is a 2-D tensor map
+// over the packed bf16 weight, box {64, O}, 128-byte swizzle.
+bool tc_supported(int C, int O);
+cudaError_t launch_tc(const Params &p, const CUtensorMap &wmap, cudaStream_t stream);
+
+// One-thread kernel whose barrier wait runs out after timeout_ns.
+cudaError_t launch_selftest_timeout(unsigned *status, unsigned long long timeout_ns,
+                                    cudaStream_t stream);
+
+}  // namespace dcn

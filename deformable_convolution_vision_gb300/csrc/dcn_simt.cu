@@ -1,0 +1,207 @@
+// Weight packing (S0) and the CUDA-core fused forward kernel.
+//
+// The CUDA-core kernel is the path for fp32 operands (no TF32 anywhere: the
+// "deformops 3.0.1" page, section "Deformable convolution", keeps TF32 out
+// of the contraction) and for bf16 shapes outside the tensor-core kernel's
+// envelope.  It is an implicit GEMM on FFMA: per tap, the CTA computes the
+// four corner weights of its 64 pixels once, then for each chunk of 16
+// channels samples a [16 x 64] operand tile into shared memory, stages the
+// matching [16 x 64] weight tile, and accumulates a 4 x 4 register tile per
+// thread.  The sampled tile is never written to global memory.
+#include <cuda_bf16.h>
+
+#include "dcn_kernels.h"
+#include "dcn_sampling.cuh"
+
+namespace dcn {
+
+namespace {
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// S0: out[o][(i*kw + j)*C + c] = w[o][c][i][j].  One thread per packed
+// element, so the writes are coalesced; the weight is small (<= a few MB).
+template <typename T>
+__global__ void pack_weight_kernel(const T *__restrict__ w, T *__restrict__ wp,
+                                   int O, int C, int kh, int kw) {
+    const long long K = static_cast<long long>(kh) * kw * C;
+    const long long n = K * O;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < n;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int o = static_cast<int>(e / K);
+        const int kk = static_cast<int>(e - static_cast<long long>(o) * K);
+        const int tap = kk / C;
+        const int c = kk - tap * C;
+        const int i = tap / kw;
+        const int j = tap - i * kw;
+        wp[e] = w[((static_cast<long long>(o) * C + c) * kh + i) * kw + j];
+    }
+}
+
+constexpr int SIMT_BM = 64;    // output pixels per CTA
+constexpr int SIMT_BN = 64;    // output channels per CTA
+constexpr int SIMT_BK = 16;    // channels per inner step
+constexpr int SIMT_THREADS = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(SIMT_THREADS)
+dcn_simt_kernel(Params p) {
+    __shared__ float As[SIMT_BK][SIMT_BM + 4];
+    __shared__ float Bs[SIMT_BK][SIMT_BN + 4];
+    __shared__ float4 cw_s[SIMT_BM];
+    __shared__ int4 ci_s[SIMT_BM];
+
+    const T *__restrict__ x = static_cast<const T *>(p.x);
+    const T *__restrict__ wp = static_cast<const T *>(p.wpack);
+    const int tid = threadIdx.x;
+    const int pix0 = blockIdx.x * SIMT_BM;
+    const int o0 = blockIdx.y * SIMT_BN;
+    const int ty = tid / 16;   // pixel group: pixels ty*4 .. ty*4+3
+    const int tx = tid % 16;   // channel group: outputs tx*4 .. tx*4+3
+    const int HoWo = p.Ho * p.Wo;
+    const int taps = p.kh * p.kw;
+
+    // the pixel whose corner weights this thread computes (tid < SIMT_BM)
+    const int my_pix = pix0 + tid;
+    int my_b = 0, my_h = 0, my_w = 0;
+    if (tid < SIMT_BM && my_pix < p.P) {
+        my_b = my_pix / HoWo;
+        const int rem = my_pix - my_b * HoWo;
+        my_h = rem / p.Wo;
+        my_w = rem - my_h * p.Wo;
+    }
+
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+
+    for (int tap = 0; tap < taps; ++tap) {
+        const int i = tap / p.kw;
+        const int j = tap - i * p.kw;
+        __syncthreads();  // the previous tap's corner table is no longer read
+        if (tid < SIMT_BM) {
+            TapCorners t;
+            if (my_pix < p.P) {
+                const size_t hw = static_cast<size_t>(my_h) * p.Wo + my_w;
+                const size_t ob = static_cast<size_t>(my_b) * 2 * taps * HoWo + hw;
+                const float dy = p.offset[ob + static_cast<size_t>(2 * tap) * HoWo];
+                const float dx = p.offset[ob + static_cast<size_t>(2 * tap + 1) * HoWo];
+                const float m = p.mask
+                    ? p.mask[(static_cast<size_t>(my_b) * taps + tap) * HoWo + hw] : 1.0f;
+                tap_corners(dy, dx, m, my_h, my_w, i, j, p.pad, my_b, p.H, p.W, p.C, t);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) { t.w[q] = 0.0f; t.idx[q] = 0; }
+            }
+            cw_s[tid] = make_float4(t.w[0], t.w[1], t.w[2], t.w[3]);
+            ci_s[tid] = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
+        }
+        __syncthreads();
+
+        for (int c0 = 0; c0 < p.C; c0 += SIMT_BK) {
+            // sampled operand: 16 channels x 64 pixels; consecutive threads
+            // take consecutive channels of one pixel (coalesced in NHWC)
+#pragma unroll
+            for (int e = 0; e < (SIMT_BK * SIMT_BM) / SIMT_THREADS; ++e) {
+                const int idx = tid + e * SIMT_THREADS;
+                const int kk = idx % SIMT_BK;
+                const int pp = idx / SIMT_BK;
+                const int c = c0 + kk;
+                float v = 0.0f;
+                if (c < p.C) {
+                    const float4 cw = cw_s[pp];
+                    const int4 ci = ci_s[pp];
+                    if (cw.x != 0.0f) v += cw.x * to_f32<T>(x[ci.x + c]);
+                    if (cw.y != 0.0f) v += cw.y * to_f32<T>(x[ci.y + c]);
+                    if (cw.z != 0.0f) v += cw.z * to_f32<T>(x[ci.z + c]);
+                    if (cw.w != 0.0f) v += cw.w * to_f32<T>(x[ci.w + c]);
+                }
+                As[kk][pp] = v;
+            }
+            // weight tile: 16 channels x 64 outputs, contiguous along K
+#pragma unroll
+            for (int e = 0; e < (SIMT_BK * SIMT_BN) / SIMT_THREADS; ++e) {
+                const int idx = tid + e * SIMT_THREADS;
+                const int kk = idx % SIMT_BK;
+                const int oo = idx / SIMT_BK;
+                const int c = c0 + kk;
+                const int o = o0 + oo;
+                float v = 0.0f;
+                if (c < p.C && o < p.O)
+                    v = to_f32<T>(wp[static_cast<size_t>(o) * p.K + static_cast<size_t>(tap) * p.C + c]);
+                Bs[kk][oo] = v;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int kk = 0; kk < SIMT_BK; ++kk) {
+                float a[4], b[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) a[r] = As[kk][ty * 4 + r];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) b[r] = Bs[kk][tx * 4 + r];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(a[r], b[s], acc[r][s]);
+            }
+            __syncthreads();
+        }
+    }
+
+    // S5 epilogue: bias in fp32, cast, channels-last store
+    T *__restrict__ out = static_cast<T *>(p.out);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int pix = pix0 + ty * 4 + r;
+        if (pix >= p.P) continue;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const int o = o0 + tx * 4 + s;
+            if (o >= p.O) continue;
+            const float bv = p.bias ? p.bias[o] : 0.0f;
+            out[static_cast<size_t>(pix) * p.O + o] = from_f32<T>(acc[r][s] + bv);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int C, int kh, int kw,
+                               int dtype, cudaStream_t stream) {
+    const long long n = static_cast<long long>(O) * C * kh * kw;
+    const int threads = 256;
+    const long long want = (n + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < 4096 ? want : 4096);
+    if (dtype == kF32) {
+        pack_weight_kernel<float><<<blocks, threads, 0, stream>>>(
+            static_cast<const float *>(weight), static_cast<float *>(wpack), O, C, kh, kw);
+    } else {
+        pack_weight_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(weight), static_cast<__nv_bfloat16 *>(wpack),
+            O, C, kh, kw);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_simt(const Params &p, int dtype, cudaStream_t stream) {
+    dim3 grid((p.P + SIMT_BM - 1) / SIMT_BM, (p.O + SIMT_BN - 1) / SIMT_BN);
+    if (dtype == kF32)
+        dcn_simt_kernel<float><<<grid, SIMT_THREADS, 0, stream>>>(p);
+    else
+        dcn_simt_kernel<__nv_bfloat16><<<grid, SIMT_THREADS, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace dcn

@@ -1,0 +1,160 @@
+/*
+ * dcn.h -- C ABI of the GB300 (sm_103a) modulated deformable convolution
+ * forward pass.
+ *
+ * The operation (page "litert-community/Idol ... deform_conv.py", module
+ * docstring and the four-corner loop of deform_conv2d_gather; page
+ * "deformops 3.0.1", section "Deformable convolution"): torchvision
+ * deform_conv2d with stride 1, dilation 1, one offset group and one weight
+ * group.  For image b, output channel o and output pixel (h, w):
+ *
+ *   out[b,h,w,o] = bias[o] + sum_{i,j,c} weight[o,c,i,j] * m * S(b,c,py,px)
+ *   k = i*kw + j,  dy = offset[b,2k,h,w],  dx = offset[b,2k+1,h,w],
+ *   m = mask[b,k,h,w] (1 without a mask),
+ *   py = (h - pad + i) + dy,  px = (w - pad + j) + dx   (fp32),
+ *   S  = bilinear sample of channel c at (py, px); each of the four corners
+ *        that falls outside [0,H-1] x [0,W-1] contributes 0.
+ *
+ *   Ho = H + 2*pad - kh + 1,  Wo = W + 2*pad - kw + 1.
+ *
+ * Layouts (dense, no padding between rows; all pointers are DEVICE pointers
+ * unless the function name ends in _host):
+ *   x      [B, H, W, C]       channels-last, element type `dtype`
+ *   offset [B, 2*kh*kw, Ho, Wo] fp32; channel 2k holds dy_k, 2k+1 holds dx_k
+ *   mask   [B, kh*kw, Ho, Wo] fp32, or NULL for "all ones" (DCN v1)
+ *   weight [O, C, kh, kw]     element type `dtype` (torchvision layout)
+ *   bias   [O]                fp32, or NULL for zero
+ *   out    [B, Ho, Wo, O]     channels-last, element type `dtype`
+ *
+ * Numerics: sampling coordinates, corner weights and the interpolation are
+ * fp32; the contraction accumulates in fp32 for both dtypes (no TF32).  The
+ * bf16 path rounds each interpolated sample to bf16 before the tensor-core
+ * contraction and rounds the fp32 result (after bias) to bf16 at the end.
+ *
+ * Ownership: the caller owns every tensor and the stream.  A handle owns a
+ * small device workspace (the packed weight, a status word and, for
+ * dcn_forward_host, device staging buffers) that grows on demand, in stream
+ * order, and is released by dcn_destroy.  Calls that share a handle must be
+ * ordered on one stream; use one handle per stream for concurrent streams.
+ *
+ * Errors: every function validates its arguments before launching anything
+ * and returns a dcn_status_t; a failed check launches nothing.  Launches are
+ * asynchronous; a device-side failure (a bounded wait that ran out) sets the
+ * handle's status word, which dcn_sync_status reports.
+ */
+#ifndef DCN_H
+#define DCN_H
+
+#if defined(__GNUC__)
+#define DCN_API __attribute__((visibility("default")))
+#else
+#define DCN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dcn_handle_s *dcn_handle_t;
+
+/* Element type of x, weight and out. */
+typedef enum {
+    DCN_F32 = 0,   /* fp32 operands, CUDA-core FFMA path */
+    DCN_BF16 = 1   /* bf16 operands, tcgen05 tensor-core path where the shape allows */
+} dcn_dtype_t;
+
+typedef enum {
+    DCN_OK = 0,
+    DCN_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, misaligned pointer, size overflow */
+    DCN_ERR_UNSUPPORTED = 2,  /* a forced path that cannot run this shape, or a device that is not sm_103 */
+    DCN_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    DCN_ERR_NO_DEVICE = 4,    /* no CUDA device is visible */
+    DCN_ERR_OOM = 5,          /* workspace allocation failed */
+    DCN_ERR_TIMEOUT = 6       /* a device-side bounded wait ran out (reported by dcn_sync_status) */
+} dcn_status_t;
+
+/* Kernel selection for bf16.  AUTO takes the tcgen05 path when
+ * C % 64 == 0, O % 16 == 0, 16 <= O <= 256 and x/out are 16-byte aligned,
+ * and the CUDA-core path otherwise.  fp32 always takes the CUDA-core path. */
+typedef enum {
+    DCN_PATH_AUTO = 0,
+    DCN_PATH_SIMT = 1,   /* CUDA-core fused sample + FFMA contraction */
+    DCN_PATH_TC = 2      /* tcgen05 fused implicit GEMM (bf16 only) */
+} dcn_path_t;
+
+/* Create a handle on the current CUDA device.  Returns DCN_ERR_NO_DEVICE
+ * without a device and DCN_ERR_UNSUPPORTED on a device other than compute
+ * capability 10.3.  *out_handle is NULL on failure. */
+DCN_API dcn_status_t dcn_create(dcn_handle_t *out_handle);
+
+/* Release the handle and its workspace.  Synchronises the device first.
+ * NULL is accepted and ignored. */
+DCN_API dcn_status_t dcn_destroy(dcn_handle_t h);
+
+/* Full forward pass on `stream` (a cudaStream_t; NULL = legacy default
+ * stream): packs the weight into the handle's workspace, then runs the
+ * fused sampling + contraction + epilogue kernel.  Asynchronous.
+ * x, weight and out must be aligned to their element size, offset, mask
+ * and bias to 4 bytes.  Sizes: every dimension > 0, pad >= 0, Ho > 0,
+ * Wo > 0, and each of B*H*W*C, B*2*kh*kw*Ho*Wo, B*Ho*Wo*O, O*C*kh*kw
+ * below 2^31. */
+DCN_API dcn_status_t dcn_forward(dcn_handle_t h,
+                         const void *x, const float *offset, const float *mask,
+                         const void *weight, const float *bias, void *out,
+                         int B, int C, int H, int W, int O,
+                         int kh, int kw, int pad, int dtype, void *stream);
+
+/* The two halves of dcn_forward, for callers that reuse one weight.
+ * dcn_pack_weight reorders weight [O,C,kh,kw] into the handle's workspace
+ * as [O][(i*kw + j)*C + c] (tap-major, channel-minor).
+ * dcn_forward_packed then runs the fused kernel with that packed weight;
+ * it returns DCN_ERR_INVALID_ARG if (O, C, kh, kw, dtype) differ from the
+ * last dcn_pack_weight on this handle.  Both are asynchronous on `stream`. */
+DCN_API dcn_status_t dcn_pack_weight(dcn_handle_t h, const void *weight,
+                             int O, int C, int kh, int kw, int dtype, void *stream);
+DCN_API dcn_status_t dcn_forward_packed(dcn_handle_t h,
+                                const void *x, const float *offset, const float *mask,
+                                const float *bias, void *out,
+                                int B, int C, int H, int W, int O,
+                                int kh, int kw, int pad, int dtype, void *stream);
+
+/* dcn_forward with HOST buffers (same layouts): copies every input to
+ * device staging buffers owned by the handle, runs the forward pass,
+ * copies out back and synchronises `stream`.  Pinned host memory gives
+ * asynchronous copies; pageable memory works but is slower.  Returns the
+ * device status as dcn_sync_status would. */
+DCN_API dcn_status_t dcn_forward_host(dcn_handle_t h,
+                              const void *x, const float *offset, const float *mask,
+                              const void *weight, const float *bias, void *out,
+                              int B, int C, int H, int W, int O,
+                              int kh, int kw, int pad, int dtype, void *stream);
+
+/* Choose the kernel path for later calls on this handle (dcn_path_t).
+ * A forced path that cannot run a given shape makes that call return
+ * DCN_ERR_UNSUPPORTED. */
+DCN_API dcn_status_t dcn_set_path(dcn_handle_t h, int path);
+
+/* The path (dcn_path_t, never AUTO) taken by the last successful forward
+ * call on this handle, or -1 before the first. */
+DCN_API int dcn_last_path(dcn_handle_t h);
+
+/* Synchronise `stream` and report the handle's device status word:
+ * DCN_OK, DCN_ERR_TIMEOUT if a kernel's bounded wait ran out (the word is
+ * cleared after it is read), or DCN_ERR_CUDA if the synchronisation failed. */
+DCN_API dcn_status_t dcn_sync_status(dcn_handle_t h, void *stream);
+
+/* Launch a one-thread kernel that waits on a barrier nothing arrives on,
+ * with a bound of timeout_ns nanoseconds; it then sets the status word
+ * exactly as a stalled forward kernel would and returns.  Lets a caller
+ * check the timeout path without stalling a real kernel.  timeout_ns must
+ * be in (0, 10^10]. */
+DCN_API dcn_status_t dcn_selftest_timeout(dcn_handle_t h, long long timeout_ns, void *stream);
+
+/* Static, human-readable name of a status code. */
+DCN_API const char *dcn_status_string(dcn_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCN_H */

@@ -1,0 +1,126 @@
+"""C-ABI behaviour on a GB300: argument errors, forced paths, the packed
+weight halves, the host-buffer entry point and the bounded-wait status."""
+
+import numpy as np
+import pytest
+import torch
+
+import deformable_convolution_vision_gb300 as dcn
+from deformable_convolution_vision_gb300 import binding
+from deformable_convolution_vision_gb300.inputs import WORKLOADS, make_inputs
+from tests.helpers import TOL, compare_full, oracle_full, to_device
+
+pytestmark = pytest.mark.gpu
+
+E = binding.STATUS_CODE
+
+
+@pytest.fixture
+def handle():
+    with dcn.Handle() as h:
+        yield h
+
+
+def _args(d, wl):
+    return [d["x"].data_ptr(), d["offset"].data_ptr(),
+            None if d["mask"] is None else d["mask"].data_ptr(), d["weight"].data_ptr(),
+            None if d["bias"] is None else d["bias"].data_ptr()]
+
+
+def test_argument_errors(handle):
+    lib = binding.load()
+    wl = WORKLOADS["tiny"]
+    d = to_device(make_inputs(wl))
+    out = torch.empty(wl.B * wl.Ho * wl.Wo * wl.O, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    x, off, m, w, b = _args(d, wl)
+    ok = [wl.B, wl.C, wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad, 0]
+
+    def call(xx=x, oo=off, ww=w, out_p=out.data_ptr(), dims=ok):
+        return lib.dcn_forward(handle.h, xx, oo, m, ww, b, out_p, *dims, s)
+
+    assert call() == E["DCN_OK"]
+    assert call(xx=None) == E["DCN_ERR_INVALID_ARG"]
+    assert call(oo=None) == E["DCN_ERR_INVALID_ARG"]
+    assert call(ww=None) == E["DCN_ERR_INVALID_ARG"]
+    assert call(out_p=None) == E["DCN_ERR_INVALID_ARG"]
+    assert call(xx=x + 2) == E["DCN_ERR_INVALID_ARG"]           # misaligned fp32
+    for bad in ([0] + ok[1:], ok[:1] + [-1] + ok[2:], ok[:7] + [-1, 0], ok[:8] + [7],
+                [1, 4, 2, 2, 3, 5, 5, 0, 0],                       # Ho <= 0
+                [1 << 16, 1 << 16, 1, 1, 1, 1, 1, 0, 0]):          # B*H*W*C >= 2^31
+        assert call(dims=bad) == E["DCN_ERR_INVALID_ARG"], bad
+    assert dcn.dcn_sync_status(handle.h) == 0
+
+
+def test_forced_tc_path_rejects_unsupported_shapes(handle):
+    dcn.dcn_set_path(handle.h, dcn.DCN_PATH_TC)
+    wl = WORKLOADS["tiny"]  # fp32: no tensor-core path
+    inp = make_inputs(wl)
+    d = to_device(inp)
+    out = torch.empty((wl.B, wl.O, wl.Ho, wl.Wo), device="cuda", memory_format=torch.channels_last)
+    with pytest.raises(dcn.DcnError) as e:
+        dcn.dcn_forward(handle.h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"], out,
+                        wl.B, wl.C, wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad, dcn.DCN_F32)
+    assert e.value.status == E["DCN_ERR_UNSUPPORTED"]
+    wl2 = WORKLOADS["decoder3x3"].with_(C=48, H=16, W=16)  # C % 64 != 0
+    d2 = to_device(make_inputs(wl2))
+    out2 = torch.empty((1, wl2.O, wl2.Ho, wl2.Wo), dtype=torch.bfloat16, device="cuda",
+                       memory_format=torch.channels_last)
+    with pytest.raises(dcn.DcnError) as e:
+        dcn.dcn_forward(handle.h, d2["x"], d2["offset"], d2["mask"], d2["weight"], d2["bias"],
+                        out2, 1, 48, 16, 16, wl2.O, 3, 3, 1, dcn.DCN_BF16)
+    assert e.value.status == E["DCN_ERR_UNSUPPORTED"]
+    assert dcn.dcn_sync_status(handle.h) == 0
+
+
+def test_packed_halves_match_forward(handle):
+    wl = WORKLOADS["decoder3x3"].with_(H=48, W=40)
+    inp = make_inputs(wl)
+    d = to_device(inp)
+    shape = (wl.B, wl.O, wl.Ho, wl.Wo)
+    a = torch.empty(shape, dtype=torch.bfloat16, device="cuda", memory_format=torch.channels_last)
+    b = torch.empty_like(a)
+    dims = (wl.B, wl.C, wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad, dcn.DCN_BF16)
+    dcn.dcn_forward(handle.h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"], a, *dims)
+    dcn.dcn_pack_weight(handle.h, d["weight"], wl.O, wl.C, wl.kh, wl.kw, dcn.DCN_BF16)
+    dcn.dcn_forward_packed(handle.h, d["x"], d["offset"], d["mask"], d["bias"], b, *dims)
+    assert dcn.dcn_sync_status(handle.h) == 0
+    assert torch.equal(a, b)
+    # a packed weight of another shape is refused
+    with pytest.raises(dcn.DcnError) as e:
+        dcn.dcn_forward_packed(handle.h, d["x"], d["offset"], d["mask"], d["bias"], b,
+                               wl.B, wl.C, wl.H, wl.W, wl.O, 5, 5, 2, dcn.DCN_BF16)
+    assert e.value.status == E["DCN_ERR_INVALID_ARG"]
+
+
+@pytest.mark.parametrize("name", ["tiny", "decoder3x3"])
+def test_host_entry_point_matches_device(handle, name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    # host buffers in the ABI layouts, pinned
+    x = inp["x"].permute(0, 2, 3, 1).contiguous().pin_memory()
+    off = inp["offset"].pin_memory()
+    m = inp["mask"].pin_memory()
+    w = inp["weight"].contiguous().pin_memory()
+    bias = inp["bias"].pin_memory()
+    out = torch.empty((wl.B, wl.Ho, wl.Wo, wl.O), dtype=x.dtype).pin_memory()
+    code = dcn.DCN_F32 if wl.dtype == "f32" else dcn.DCN_BF16
+    dcn.dcn_forward_host(handle.h, x, off, m, w, bias, out, wl.B, wl.C, wl.H, wl.W, wl.O,
+                         wl.kh, wl.kw, wl.pad, code)
+    d = to_device(inp)
+    ref = dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], wl.pad, d["mask"])
+    assert torch.equal(out, ref.permute(0, 2, 3, 1).cpu())
+    assert compare_full(out.permute(0, 3, 1, 2), oracle_full(inp, wl.pad)) <= TOL[wl.dtype]
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(handle):
+    dcn.dcn_selftest_timeout(handle.h, 20_000_000)  # 20 ms
+    assert dcn.dcn_sync_status(handle.h) == E["DCN_ERR_TIMEOUT"]
+    assert dcn.dcn_sync_status(handle.h) == 0       # the word is cleared once read
+    wl = WORKLOADS["tiny"]
+    inp = make_inputs(wl)
+    d = to_device(inp)
+    out = dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], wl.pad, d["mask"],
+                            handle=handle)
+    assert dcn.dcn_sync_status(handle.h) == 0
+    assert compare_full(out, oracle_full(inp, wl.pad)) <= TOL["f32"]

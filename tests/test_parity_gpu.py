@@ -1,0 +1,159 @@
+"""CUDA path vs the oracle on seeded inputs (GB300).
+
+Small and ragged shapes are compared element by element over the whole
+output; the full-size workloads are compared on sampled pixels (every
+output channel of ~300 pixels, including image corners and 128-pixel tile
+boundaries), which the oracle computes one by one.  The bar is the one the
+spec tolerance sets: max|gpu - ref| / max|ref| <= 1e-4 for fp32 and
+<= 2e-2 for bf16 operands with fp32 accumulation.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deformable_convolution_vision_gb300 import (DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC, Handle,
+                                                 dcn_last_path)
+from deformable_convolution_vision_gb300.inputs import MAIN, WORKLOADS, Workload, make_inputs
+from tests.helpers import (TOL, compare_full, compare_points, oracle_full, run_cuda,
+                           sample_points)
+
+pytestmark = pytest.mark.gpu
+
+# full-output comparison when the oracle's work stays small
+FULL_LIMIT = 4e9
+
+
+def _oracle_cost(wl):
+    return wl.pixels * wl.O * wl.taps * wl.C * 4
+
+
+def check(wl, path=DCN_PATH_AUTO, inp=None, expect_path=None, n_points=256):
+    inp = make_inputs(wl) if inp is None else inp
+    with Handle(path) as h:
+        out = run_cuda(inp, wl.pad, handle=h)
+        taken = dcn_last_path(h.h)
+    if expect_path is not None:
+        assert taken == expect_path, f"{wl.name}: path {taken}, expected {expect_path}"
+    if _oracle_cost(wl) <= FULL_LIMIT:
+        err = compare_full(out, oracle_full(inp, wl.pad))
+    else:
+        pts = sample_points(wl.B, wl.Ho, wl.Wo, n_points, seed=wl.seed)
+        ref = oracle.forward_points(inp["x"], inp["offset"], inp["mask"], inp["weight"],
+                                    inp["bias"], wl.pad, pts)
+        err = compare_points(out, ref, pts)
+    assert err <= TOL[wl.dtype], f"{wl.name} path {taken}: rel err {err:.3e} > {TOL[wl.dtype]}"
+    return err, out
+
+
+@pytest.mark.parametrize("name", MAIN)
+def test_workload(name):
+    wl = WORKLOADS[name]
+    expect = DCN_PATH_SIMT if wl.dtype == "f32" else DCN_PATH_TC
+    check(wl, expect_path=expect)
+
+
+@pytest.mark.parametrize("ks", [1, 3, 7])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_page_selftest_shapes(ks, dtype):
+    wl = WORKLOADS[f"selftest{ks}x{ks}"].with_(dtype=dtype)
+    check(wl, expect_path=DCN_PATH_SIMT if dtype == "f32" else DCN_PATH_TC)
+
+
+@pytest.mark.parametrize("path", [DCN_PATH_SIMT, DCN_PATH_TC])
+def test_both_bf16_paths(path):
+    check(WORKLOADS["decoder3x3"], path=path, expect_path=path)
+
+
+# ragged tile counts, non-square kernels, small maps, no mask / no bias
+TC_SHAPES = [
+    Workload("tc_ragged_a", 1, 64, 13, 11, 48, 3, 3, 1, "bf16", 2.0, "sigmoid", 0.0, 0.1, 11),
+    Workload("tc_ragged_b", 3, 128, 7, 9, 16, 5, 5, 2, "bf16", 3.0, "uniform", 0.0, 0.1, 12),
+    Workload("tc_one_tile", 2, 192, 10, 10, 256, 3, 3, 0, "bf16", 1.5, "sigmoid", 0.0, 0.1, 13),
+    Workload("tc_one_pixel", 1, 64, 1, 1, 32, 3, 3, 1, "bf16", 0.7, "sigmoid", 0.0, 0.1, 14),
+    Workload("tc_no_mask_bias", 1, 64, 40, 37, 64, 7, 7, 3, "bf16", 5.0, "none", 0.0, 0.0, 15),
+    Workload("tc_rect_kernel", 1, 64, 12, 20, 64, 3, 5, 2, "bf16", 2.0, "sigmoid", 0.0, 0.1, 16),
+    Workload("tc_o_112", 2, 64, 9, 30, 112, 3, 3, 1, "bf16", 2.0, "uniform_zero10", 0.0, 0.1, 17),
+]
+
+SIMT_SHAPES = [
+    Workload("simt_odd", 2, 3, 9, 7, 5, 3, 3, 1, "f32", 2.0, "sigmoid", 0.0, 0.1, 21),
+    Workload("simt_wide", 1, 17, 11, 13, 70, 5, 3, 2, "f32", 3.0, "uniform", 0.0, 0.1, 22),
+    Workload("simt_no_mask", 1, 33, 6, 5, 8, 2, 2, 0, "f32", 1.0, "none", 0.0, 0.0, 23),
+    Workload("simt_bf16_odd", 2, 24, 10, 9, 40, 3, 3, 1, "bf16", 2.0, "sigmoid", 0.0, 0.1, 24),
+    Workload("simt_pad_big", 1, 8, 4, 5, 9, 3, 3, 3, "f32", 1.0, "sigmoid", 0.0, 0.1, 25),
+]
+
+
+@pytest.mark.parametrize("wl", TC_SHAPES, ids=lambda w: w.name)
+def test_tc_shapes(wl):
+    check(wl, expect_path=DCN_PATH_TC)
+
+
+@pytest.mark.parametrize("wl", SIMT_SHAPES, ids=lambda w: w.name)
+def test_simt_shapes(wl):
+    check(wl, expect_path=DCN_PATH_SIMT)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_samples_outside_give_bias(dtype):
+    wl = WORKLOADS["decoder3x3"].with_(H=32, W=32, dtype=dtype, seed=30)
+    inp = make_inputs(wl)
+    inp["offset"][:, 0::2] = -(wl.H + 5.0)
+    out = run_cuda(inp, wl.pad).float().cpu()
+    exp = inp["bias"].to(torch.bfloat16 if dtype == "bf16" else torch.float32).float()
+    assert torch.equal(out, exp.view(1, -1, 1, 1).expand_as(out))
+
+
+def test_mask_zero_gives_bias():
+    wl = WORKLOADS["decoder3x3"].with_(H=24, W=40, seed=31)
+    inp = make_inputs(wl)
+    inp["mask"].zero_()
+    out = run_cuda(inp, wl.pad).float().cpu()
+    exp = inp["bias"].to(torch.bfloat16).float()
+    assert torch.equal(out, exp.view(1, -1, 1, 1).expand_as(out))
+
+
+def test_nonfinite_offsets_do_not_fault():
+    """The pages leave non-finite offsets open; the kernels clamp the sampling
+    coordinate, so such taps contribute nothing and nothing is read out of
+    bounds."""
+    wl = WORKLOADS["decoder3x3"].with_(H=16, W=16, seed=32)
+    inp = make_inputs(wl)
+    inp["offset"][:, 0, :4] = float("nan")
+    inp["offset"][:, 3, 4:8] = float("inf")
+    inp["offset"][:, 5, 8:12] = -float("inf")
+    inp["offset"][:, 7, 12:] = 3e38
+    out = run_cuda(inp, wl.pad)
+    ref = oracle_full(inp, wl.pad)
+    assert compare_full(out, ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("name", ["decoder3x3", "tiny"])
+def test_deterministic(name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    a = run_cuda(inp, wl.pad)
+    b = run_cuda(inp, wl.pad)
+    assert torch.equal(a, b)
+
+
+def test_output_guard_bands_untouched():
+    """Only the output's own bytes are written: canaries on both sides stay."""
+    import deformable_convolution_vision_gb300 as dcn
+    from tests.helpers import to_device
+    wl = TC_SHAPES[0]
+    inp = make_inputs(wl)
+    d = to_device(inp)
+    n = wl.pixels * wl.O
+    guard = 4096
+    buf = torch.full((guard + n + guard,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out_view = buf[guard:guard + n]
+    with Handle() as h:
+        dcn.dcn_forward(h.h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"], out_view,
+                        wl.B, wl.C, wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad, 1)
+        assert dcn.dcn_sync_status(h.h) == 0
+    assert torch.all(buf[:guard] == 7.0) and torch.all(buf[guard + n:] == 7.0)
+    out = out_view.view(wl.B, wl.Ho, wl.Wo, wl.O).permute(0, 3, 1, 2)
+    assert compare_full(out, oracle_full(inp, wl.pad)) <= TOL["bf16"]
