@@ -20,7 +20,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_forward_packed",
            "dcn_forward_host", "dcn_set_path", "dcn_last_path", "dcn_sync_status",
-           "dcn_selftest_timeout", "dcn_status_string"]
+           "dcn_selftest_timeout", "dcn_status_string", "dcn_forward_noalloc"]
 
 
 class DcnError(RuntimeError):
@@ -54,6 +54,7 @@ def load():
         "dcn_sync_status": ([P, P], I),
         "dcn_selftest_timeout": ([P, LL, P], I),
         "dcn_status_string": ([I], ctypes.c_char_p),
+        "dcn_forward_noalloc": ([P, P, P, P, P, P] + [I] * 9 + [P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -142,3 +143,12 @@ def dcn_sync_status(h, stream=None):
 
 def dcn_selftest_timeout(h, timeout_ns, stream=None):
     _check(load().dcn_selftest_timeout(h, int(timeout_ns), _stream(stream)), "dcn_selftest_timeout")
+
+
+def dcn_forward_noalloc(x, offset, mask, weight, bias, out, B, C, H, W, O, kh, kw, pad, dtype,
+                        stream=None):
+    """The allocation-free forward pass (no handle; fixed scratch)."""
+    _check(load().dcn_forward_noalloc(_ptr(x), _ptr(offset), _ptr(mask), _ptr(weight), _ptr(bias),
+                                      _ptr(out), B, C, H, W, O, kh, kw, pad, dtype,
+                                      _stream(stream)),
+           "dcn_forward_noalloc")

@@ -150,6 +150,41 @@ DCN_API dcn_status_t dcn_sync_status(dcn_handle_t h, void *stream);
  * be in (0, 10^10]. */
 DCN_API dcn_status_t dcn_selftest_timeout(dcn_handle_t h, long long timeout_ns, void *stream);
 
+/* Largest packed weight (O*C*kh*kw elements times the element size, in
+ * bytes) that dcn_forward_noalloc accepts: 8 MiB. */
+#define DCN_NOALLOC_MAX_WEIGHT_BYTES 8388608ull
+
+/* dcn_forward without any device allocation.  The pages have no
+ * counterpart: this exists for callers that must not let a library
+ * allocate device memory -- plugin hosts and inference engines that own
+ * all device memory and forbid allocations behind their back, processes
+ * whose device-memory budget is fixed at start-up, and latency-critical
+ * loops where cudaMalloc/cudaFree can synchronise the device and stall
+ * other streams.
+ *
+ * It takes no handle and calls no cudaMalloc, cudaFree or other allocating
+ * routine.  Its scratch (the packed weight and a status word) lives in
+ * fixed device arrays built into the library, which every GPU that loads
+ * the library holds until the process exits.  Same arguments, layouts,
+ * kernels and results as dcn_forward; asynchronous on `stream`.
+ *
+ * - The packed weight must fit DCN_NOALLOC_MAX_WEIGHT_BYTES; larger
+ *   weights return DCN_ERR_UNSUPPORTED and launch nothing.  Other argument
+ *   errors return DCN_ERR_INVALID_ARG as for dcn_forward.
+ * - The first call on each device looks up the scratch arrays' device
+ *   addresses (cudaGetSymbolAddress) with that device current; make that
+ *   first call before any stream capture.
+ * - Every call on a device shares the same scratch, which keeps the last
+ *   call's contents: calls whose work overlaps on the GPU (on different
+ *   streams, or from different threads) race and may corrupt each other's
+ *   results.  Order them on one stream.
+ * - The status word is cleared at the start of each call; a device-side
+ *   wait that runs out is not reported back by this entry point. */
+DCN_API dcn_status_t dcn_forward_noalloc(const void *x, const float *offset, const float *mask,
+                                         const void *weight, const float *bias, void *out,
+                                         int B, int C, int H, int W, int O,
+                                         int kh, int kw, int pad, int dtype, void *stream);
+
 /* Static, human-readable name of a status code. */
 DCN_API const char *dcn_status_string(dcn_status_t s);
 
