@@ -52,6 +52,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but lets the hardware suspend the thread for up to
+// `hint_ns` while the phase is incomplete instead of returning at once:
+// threads that only wait (the MMA issuer, the TMA producer) then stop
+// competing for issue slots with the threads doing work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait that sleeps (up to hint_ns per try) instead of spinning.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
+                                                unsigned *status, uint64_t limit_ns,
+                                                uint32_t hint_ns = 20000u) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
 // Wait until the phase with the given parity has completed, for at most
 // `limit_ns` nanoseconds of global time.  On running out it sets the
 // timeout bit in *status and returns false; it never traps or spins
@@ -73,6 +102,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 // async-proxy reads (tcgen05.mma operands).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Vector shared-memory accesses (one instruction each).
+__device__ __forceinline__ int4 lds_v4_s32(uint32_t addr) {
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void lds_v2_u64(uint32_t addr, uint64_t &a, uint64_t &b) {
+    asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
+__device__ __forceinline__ void sts_v4_b32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                           uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // --------------------------------------------------------------------- TMA
@@ -177,9 +222,34 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 // ------------------------------------------------------------------ numbers
 
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Packed fp32 pairs (two lanes of one 64-bit register) for the sm_100-family
+// f32x2 FMA pipe: each op is exactly two independent fp32 operations.
+__device__ __forceinline__ uint64_t f2_make(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// Round a packed fp32 pair to a bf16x2 word (lo in the low half).
+__device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return pack_bf16x2(lo, hi);
 }
 
 // The two bf16 halves of a 32-bit word as fp32 (exact).

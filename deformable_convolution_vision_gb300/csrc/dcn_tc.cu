@@ -8,8 +8,9 @@
 // sizes at 392 MB for the 7x7, C = 64, 256 x 256 layer, exists here only as
 // one 128 x 64 tile per pipeline stage in shared memory.
 //
-// One CTA computes a tile of 128 consecutive output pixels (flattened
-// b, h, w) x all O output channels:
+// One CTA computes a tile of 8 x 16 output pixels of one image (a compact
+// 2-D tile keeps each tap's sampled footprint small, so more corner reads
+// hit L1) x all O output channels:
 //   warp 0      TMA producer: the packed-weight K-block [O x 64] of each
 //               stage, 128-byte swizzle; also allocates/frees TMEM.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=O,
@@ -17,12 +18,17 @@
 //               each stage back to its "empty" barrier.
 //   warps 2..9  samplers: per (pixel, tap) the corner weights and
 //               addresses (S1, S2), then for 8 channels per lane the four
-//               16-byte corner loads, the fp32 bilinear combine, a bf16
+//               16-byte corner loads, the fp32 bilinear combine (packed
+//               f32x2 FMAs: exactly the fp32 result), a bf16
 //               round and one 16-byte store into the swizzled A stage (S3).
 //               After the last K-block they run the epilogue (S5): TMEM ->
 //               registers, + bias in fp32, bf16 round, channels-last store.
 // K-blocks run tap-major with 64 channels each, so a tap's corner geometry
-// is computed once and reused for all of its channel blocks.
+// is computed once and reused for all of its channel blocks.  The geometry
+// is computed for two taps at a time by all 32 lanes of a sampler warp into
+// a ring of four per-warp tables, with its inputs fetched taps ahead.  Each
+// lane issues all sixteen corner loads of a stage before it waits for the
+// stage to be free.
 // Every barrier wait is bounded; a wait that runs out sets the status word
 // and the kernel winds down without trapping.
 #include <cuda_bf16.h>
@@ -42,6 +48,18 @@ constexpr int TC_THREADS = 32 * (2 + TC_SAMPLER_WARPS);
 constexpr int TC_ROWS_PER_WARP = TC_BM / TC_SAMPLER_WARPS;   // 16
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;                // 16 KB
 constexpr int TC_MMA_K = 16;
+constexpr int TC_TILE_W = 16;                                 // tile = 8 x 16 output pixels
+constexpr int TC_TILE_H = TC_BM / TC_TILE_W;                  // one tile row per sampler warp
+constexpr int TC_ITEMS = TC_ROWS_PER_WARP / 4;                // 16-byte items per lane per stage
+// per-warp corner table of one tap: for each of the warp's 16 rows the four
+// corner weights, each duplicated into an fp32 pair for the f32x2 pipe
+// (32 bytes), then the four corner indices (16 bytes)
+constexpr int TC_TABLE_W_BYTES = TC_ROWS_PER_WARP * 32;
+constexpr int TC_TABLE_BUF_BYTES = TC_TABLE_W_BYTES + TC_ROWS_PER_WARP * 16;
+constexpr int TC_TABLE_BUFS = 4;                              // taps t .. t+3 in flight
+constexpr int TC_TABLE_WARP_BYTES = TC_TABLE_BUFS * TC_TABLE_BUF_BYTES;
+static_assert(TC_TILE_H == TC_SAMPLER_WARPS, "one tile row per sampler warp");
+static_assert(TC_ROWS_PER_WARP == TC_TILE_W, "a warp's rows are one tile row");
 
 struct TcLayout {
     int stages;
@@ -61,7 +79,7 @@ __host__ __device__ inline TcLayout tc_layout(int O, int stages) {
     // full[stages], empty[stages], accum_full, tmem slot (8 bytes each)
     L.table_off = L.bar_off + (2 * stages + 2) * 8;
     L.table_off = (L.table_off + 15) & ~15;
-    L.total = L.table_off + TC_SAMPLER_WARPS * TC_ROWS_PER_WARP * 32;
+    L.total = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_WARP_BYTES;
     return L;
 }
 
@@ -85,7 +103,13 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int tile0 = blockIdx.x * TC_BM;
+    // tile -> (image, first output row, first output column)
+    const int tiles_x = (p.Wo + TC_TILE_W - 1) / TC_TILE_W;
+    const int tiles_y = (p.Ho + TC_TILE_H - 1) / TC_TILE_H;
+    const int tb = blockIdx.x / (tiles_x * tiles_y);
+    const int trem = blockIdx.x - tb * tiles_x * tiles_y;
+    const int th0 = (trem / tiles_x) * TC_TILE_H;
+    const int tw0 = (trem % tiles_x) * TC_TILE_W;
     const int ncb = p.C / TC_BK;
     const int taps = p.kh * p.kw;
     const int nkb = taps * ncb;
@@ -116,7 +140,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % stages;
                 const uint32_t r = kb / stages;
-                if (!mbar_wait(empty0 + 8 * s, (r & 1) ^ 1, p.status, p.timeout_ns)) break;
+                if (!mbar_wait_sleep(empty0 + 8 * s, (r & 1) ^ 1, p.status, p.timeout_ns)) break;
                 const uint32_t b_dst = smem_u32(smem + s * L.stage_bytes + TC_A_BYTES);
                 mbar_arrive_expect_tx(full0 + 8 * s, L.b_bytes);
                 tma_load_2d(b_dst, &wmap, full0 + 8 * s, kb * TC_BK, 0);
@@ -127,7 +151,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             const int first = issued > stages ? issued - stages : 0;
             for (int kb = first; kb < issued; ++kb) {
                 const int s = kb % stages;
-                mbar_wait(full0 + 8 * s, (kb / stages) & 1, p.status, p.timeout_ns);
+                mbar_wait_sleep(full0 + 8 * s, (kb / stages) & 1, p.status, p.timeout_ns);
             }
         }
     } else if (warp == 1) {
@@ -137,7 +161,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % stages;
                 const uint32_t r = kb / stages;
-                if (!mbar_wait(full0 + 8 * s, r & 1, p.status, p.timeout_ns)) break;
+                if (!mbar_wait_sleep(full0 + 8 * s, r & 1, p.status, p.timeout_ns)) break;
                 tc_fence_after_sync();
                 const uint32_t a_addr = smem_u32(smem + s * L.stage_bytes);
                 const uint32_t b_addr = a_addr + TC_A_BYTES;
@@ -153,129 +177,167 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             }
             mma_commit(accum_bar);
             // the MMAs must be complete before TMEM is released
-            mbar_wait(accum_bar, 0, p.status, p.timeout_ns);
+            mbar_wait_sleep(accum_bar, 0, p.status, p.timeout_ns);
         }
     } else {
         // ------------------------------------------------ samplers
-        const int sw = warp - 2;
+        const int sw = warp - 2;   // this warp's tile row (16 pixels)
         const __nv_bfloat16 *__restrict__ x = static_cast<const __nv_bfloat16 *>(p.x);
-        float4 *cw_tab = reinterpret_cast<float4 *>(smem + L.table_off) + sw * TC_ROWS_PER_WARP * 2;
-        int4 *ci_tab = reinterpret_cast<int4 *>(cw_tab + TC_ROWS_PER_WARP);
+        uint8_t *table = smem + L.table_off + sw * TC_TABLE_WARP_BYTES;
+        const uint32_t table_s = smem_u32(table);
+        const uint32_t stage0_s = smem_u32(smem);
         const int HoWo = p.Ho * p.Wo;
 
-        // lanes 0..15 own the geometry of rows sw*16 + lane
-        const int my_row = sw * TC_ROWS_PER_WARP + (lane & 15);
-        const int my_pix = tile0 + my_row;
-        const bool my_valid = (lane < 16) && (my_pix < p.P);
-        int my_b = 0, my_h = 0, my_w = 0;
-        if (my_valid) {
-            my_b = my_pix / HoWo;
-            const int rem = my_pix - my_b * HoWo;
-            my_h = rem / p.Wo;
-            my_w = rem - my_h * p.Wo;
-        }
-        const size_t my_hw = static_cast<size_t>(my_h) * p.Wo + my_w;
-        const float *off_base = p.offset + static_cast<size_t>(my_b) * 2 * taps * HoWo + my_hw;
-        const float *mask_base = p.mask ? p.mask + static_cast<size_t>(my_b) * taps * HoWo + my_hw
-                                        : nullptr;
+        // Geometry: lane l computes pixel (th0 + sw, tw0 + l % 16); lanes
+        // 0..15 take the even tap of a pair, lanes 16..31 the odd one.
+        const int my_h = th0 + sw;
+        const int my_w = tw0 + (lane & 15);
+        const int my_half = lane >> 4;
+        const bool my_valid = (my_h < p.Ho) && (my_w < p.Wo);
+        const int my_hw = my_valid ? my_h * p.Wo + my_w : 0;
+
+        // raw inputs (dy, dx, mask) of this lane's next tap, loaded about two
+        // taps ahead of their use so their latency hides behind the gathers
+        float n_dy = 0.0f, n_dx = 0.0f, n_m = 0.0f;
+        auto load_raw = [&](int pair_tap) {
+            const int tap = pair_tap + my_half;
+            if (my_valid && tap < taps) {
+                const float *o = p.offset + (static_cast<size_t>(tb) * 2 * taps + 2 * tap) * HoWo + my_hw;
+                n_dy = __ldg(o);
+                n_dx = __ldg(o + HoWo);
+                n_m = p.mask ? __ldg(p.mask + (static_cast<size_t>(tb) * taps + tap) * HoWo + my_hw)
+                             : 1.0f;
+            }
+        };
+        // corner tables of taps pair_tap and pair_tap + 1 (ring slots tap % 4)
+        auto tabulate = [&](int pair_tap) {
+            const int tap = pair_tap + my_half;
+            TapCorners t;
+            if (my_valid && tap < taps) {
+                const int i = tap / p.kw;
+                const int j = tap - i * p.kw;
+                tap_corners(n_dy, n_dx, n_m, my_h, my_w, i, j, p.pad, tb, p.H, p.W, p.C, t);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) { t.w[q] = 0.0f; t.idx[q] = 0; }
+            }
+            uint8_t *slot = table + (tap & (TC_TABLE_BUFS - 1)) * TC_TABLE_BUF_BYTES;
+            float4 *wdst = reinterpret_cast<float4 *>(slot + (lane & 15) * 32);
+            wdst[0] = make_float4(t.w[0], t.w[0], t.w[1], t.w[1]);
+            wdst[1] = make_float4(t.w[2], t.w[2], t.w[3], t.w[3]);
+            *reinterpret_cast<int4 *>(slot + TC_TABLE_W_BYTES + (lane & 15) * 16) =
+                make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
+        };
 
         const int chunk = lane & 7;     // 8 channels = 16 bytes
         const int rsub = lane >> 3;     // 0..3
+        // this lane's row offsets inside a table slot and inside an A stage
+        const uint32_t w_off = rsub * 32;
+        const uint32_t i_off = TC_TABLE_W_BYTES + rsub * 16;
         bool ok = true;
 
+        // Issue the four 16-byte corner loads of item `it` (rows it*4 + rsub)
+        // from a table slot.  Corners outside the image read a clamped
+        // in-image address and carry weight 0.
+        auto issue = [&](uint32_t slot, const __nv_bfloat16 *xc, int it, uint4 (&v)[4]) {
+            const int4 ci = lds_v4_s32(slot + i_off + it * 64);
+            v[0] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.x));
+            v[1] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.y));
+            v[2] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.z));
+            v[3] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.w));
+        };
+
+        load_raw(0);
+        tabulate(0);
+        if (taps > 2) load_raw(2);
+        __syncwarp();
+
+        // Stage, phase, tap and channel block advance by counters (no
+        // divisions).  Each lane issues all sixteen corner loads of a stage
+        // before it waits for the stage to be free.
+        int s = 0;
+        uint32_t phase = 0;
+        int tap = 0, cb = 0;
+
         for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % stages;
-            const uint32_t r = kb / stages;
-            const int tap = kb / ncb;
-            const int cb = kb - tap * ncb;
-            if (cb == 0) {
-                __syncwarp();
-                if (lane < 16) {
-                    TapCorners t;
-                    if (my_valid) {
-                        const int i = tap / p.kw;
-                        const int j = tap - i * p.kw;
-                        const float dy = __ldg(off_base + static_cast<size_t>(2 * tap) * HoWo);
-                        const float dx = __ldg(off_base + static_cast<size_t>(2 * tap + 1) * HoWo);
-                        const float m = mask_base ? __ldg(mask_base + static_cast<size_t>(tap) * HoWo) : 1.0f;
-                        tap_corners(dy, dx, m, my_h, my_w, i, j, p.pad, my_b, p.H, p.W, p.C, t);
-                    } else {
+            const uint32_t cur_slot = table_s + (tap & (TC_TABLE_BUFS - 1)) * TC_TABLE_BUF_BYTES;
+            const __nv_bfloat16 *xc = x + cb * TC_BK + chunk * 8;
+            uint4 v[TC_ITEMS][4];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) { t.w[q] = 0.0f; t.idx[q] = 0; }
-                    }
-                    cw_tab[lane] = make_float4(t.w[0], t.w[1], t.w[2], t.w[3]);
-                    ci_tab[lane] = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
-                }
-                __syncwarp();
-            }
+            for (int it = 0; it < TC_ITEMS; ++it) issue(cur_slot, xc, it, v[it]);
+
             // every lane waits; the warp leaves the loop together if any lane ran out
-            const bool got = mbar_wait(empty0 + 8 * s, (r & 1) ^ 1, p.status, p.timeout_ns);
+            const bool got = mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns, 2000u);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
 
-            uint8_t *a_stage = smem + s * L.stage_bytes;
-            const __nv_bfloat16 *xc = x + cb * TC_BK + chunk * 8;
+            const uint32_t a_stage = stage0_s + s * L.stage_bytes;
 #pragma unroll
-            for (int it = 0; it < TC_ROWS_PER_WARP / 4; ++it) {
-                const int rl = it * 4 + rsub;
-                const int row = sw * TC_ROWS_PER_WARP + rl;
-                const float4 cw = cw_tab[rl];
-                const int4 ci = ci_tab[rl];
-                uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0, v2 = v0, v3 = v0;
-                if (cw.x != 0.0f) v0 = __ldg(reinterpret_cast<const uint4 *>(xc + ci.x));
-                if (cw.y != 0.0f) v1 = __ldg(reinterpret_cast<const uint4 *>(xc + ci.y));
-                if (cw.z != 0.0f) v2 = __ldg(reinterpret_cast<const uint4 *>(xc + ci.z));
-                if (cw.w != 0.0f) v3 = __ldg(reinterpret_cast<const uint4 *>(xc + ci.w));
-                const uint32_t *w0 = reinterpret_cast<const uint32_t *>(&v0);
-                const uint32_t *w1 = reinterpret_cast<const uint32_t *>(&v1);
-                const uint32_t *w2 = reinterpret_cast<const uint32_t *>(&v2);
-                const uint32_t *w3 = reinterpret_cast<const uint32_t *>(&v3);
+            for (int it = 0; it < TC_ITEMS; ++it) {
+                const int row = sw * TC_ROWS_PER_WARP + it * 4 + rsub;
+                uint64_t c0, c1, c2, c3;   // {w_q, w_q} pairs
+                lds_v2_u64(cur_slot + w_off + it * 128, c0, c1);
+                lds_v2_u64(cur_slot + w_off + it * 128 + 16, c2, c3);
+                const uint32_t *w0 = reinterpret_cast<const uint32_t *>(&v[it][0]);
+                const uint32_t *w1 = reinterpret_cast<const uint32_t *>(&v[it][1]);
+                const uint32_t *w2 = reinterpret_cast<const uint32_t *>(&v[it][2]);
+                const uint32_t *w3 = reinterpret_cast<const uint32_t *>(&v[it][3]);
                 uint32_t packed[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    float lo = cw.x * bf16_lo(w0[q]);
-                    float hi = cw.x * bf16_hi(w0[q]);
-                    lo = fmaf(cw.y, bf16_lo(w1[q]), lo);
-                    hi = fmaf(cw.y, bf16_hi(w1[q]), hi);
-                    lo = fmaf(cw.z, bf16_lo(w2[q]), lo);
-                    hi = fmaf(cw.z, bf16_hi(w2[q]), hi);
-                    lo = fmaf(cw.w, bf16_lo(w3[q]), lo);
-                    hi = fmaf(cw.w, bf16_hi(w3[q]), hi);
-                    packed[q] = pack_bf16x2(lo, hi);
+                    // channels 2q, 2q+1: w0*x00 + w1*x01 + w2*x10 + w3*x11 in fp32
+                    uint64_t acc = f2_mul(c0, f2_make(bf16_lo(w0[q]), bf16_hi(w0[q])));
+                    acc = f2_fma(c1, f2_make(bf16_lo(w1[q]), bf16_hi(w1[q])), acc);
+                    acc = f2_fma(c2, f2_make(bf16_lo(w2[q]), bf16_hi(w2[q])), acc);
+                    acc = f2_fma(c3, f2_make(bf16_lo(w3[q]), bf16_hi(w3[q])), acc);
+                    packed[q] = f2_to_bf16x2(acc);
                 }
                 // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r % 8)
-                uint8_t *dst = a_stage + row * 128 + ((chunk ^ (row & 7)) << 4);
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                sts_v4_b32(a_stage + row * 128 + ((chunk ^ (row & 7)) << 4),
+                           packed[0], packed[1], packed[2], packed[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(full0 + 8 * s);
+
+            if (cb == ncb - 1 && (tap & 1) == 0 && tap + 2 < taps) {
+                // ring slots of taps tap - 2 and tap - 1 are no longer read:
+                // fill them for taps tap + 2, tap + 3, and fetch the pair after
+                tabulate(tap + 2);
+                if (tap + 4 < taps) load_raw(tap + 4);
+                __syncwarp();
+            }
+            if (++cb == ncb) { cb = 0; ++tap; }
+            if (++s == stages) { s = 0; phase ^= 1; }
         }
 
         // ------------------------------------------------ epilogue (S5)
-        if (ok) ok = mbar_wait(accum_bar, 0, p.status, p.timeout_ns);
+        if (ok) ok = mbar_wait_sleep(accum_bar, 0, p.status, p.timeout_ns);
         __syncwarp();
         tc_fence_after_sync();
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         const int half = (warp - 2) >> 2;       // two warps per quarter split the columns
-        const int row = q * 32 + lane;
-        const int pix = tile0 + row;
+        const int row = q * 32 + lane;          // tile row = pixel within the tile
+        const int oh = th0 + row / TC_TILE_W;
+        const int ow = tw0 + row % TC_TILE_W;
+        const bool pix_valid = oh < p.Ho && ow < p.Wo;
+        const size_t pix = (static_cast<size_t>(tb) * p.Ho + oh) * p.Wo + ow;
         const int nch = p.O / 16;
         const int ch_begin = half == 0 ? 0 : nch / 2;
         const int ch_end = half == 0 ? nch / 2 : nch;
         __nv_bfloat16 *__restrict__ out = static_cast<__nv_bfloat16 *>(p.out);
         for (int ch = ch_begin; ch < ch_end; ++ch) {
-            float v[16];
-            tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ch * 16, v);
-            if (ok && pix < p.P) {
+            float vv[16];
+            tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ch * 16, vv);
+            if (ok && pix_valid) {
                 uint32_t packed[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int o = ch * 16 + 2 * e;
                     const float b0 = p.bias ? __ldg(p.bias + o) : 0.0f;
                     const float b1 = p.bias ? __ldg(p.bias + o + 1) : 0.0f;
-                    packed[e] = pack_bf16x2(v[2 * e] + b0, v[2 * e + 1] + b1);
+                    packed[e] = pack_bf16x2(vv[2 * e] + b0, vv[2 * e + 1] + b1);
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(out + static_cast<size_t>(pix) * p.O + ch * 16);
+                uint4 *dst = reinterpret_cast<uint4 *>(out + pix * p.O + ch * 16);
                 dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                 dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
             }
@@ -312,7 +374,7 @@ cudaError_t launch_tc(const Params &p, const CUtensorMap &wmap, cudaStream_t str
         if (e != cudaSuccess) return e;
         g_max_smem_set = smem;
     }
-    const int tiles = (p.P + TC_BM - 1) / TC_BM;
+    const int tiles = p.B * ((p.Ho + TC_TILE_H - 1) / TC_TILE_H) * ((p.Wo + TC_TILE_W - 1) / TC_TILE_W);
     dcn_tc_kernel<<<tiles, TC_THREADS, smem, stream>>>(wmap, p, stages);
     return cudaGetLastError();
 }
