@@ -8,13 +8,15 @@ Python side: ``binding`` maps the C entry points one to one, and
 """
 
 from . import binding
-from .binding import (DCN_BF16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC, DcnError,
-                      dcn_create, dcn_destroy, dcn_forward, dcn_forward_host, dcn_forward_packed,
-                      dcn_last_path, dcn_pack_weight, dcn_selftest_timeout, dcn_set_path,
-                      dcn_status_string, dcn_sync_status)
+from .binding import (DCN_BF16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
+                      DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, DcnError, dcn_create, dcn_destroy,
+                      dcn_forward, dcn_forward_host, dcn_forward_packed, dcn_last_path,
+                      dcn_pack_weight, dcn_selftest_timeout, dcn_set_path,
+                      dcn_set_sample_precision, dcn_status_string, dcn_sync_status)
 
 __all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF16",
-           "DCN_PATH_AUTO", "DCN_PATH_SIMT", "DCN_PATH_TC", "dcn_create", "dcn_destroy",
+           "DCN_PATH_AUTO", "DCN_PATH_SIMT", "DCN_PATH_TC", "DCN_SAMPLE_INPUT_DTYPE",
+           "DCN_SAMPLE_F32", "dcn_set_sample_precision", "dcn_create", "dcn_destroy",
            "dcn_forward", "dcn_forward_host", "dcn_forward_packed", "dcn_pack_weight",
            "dcn_set_path", "dcn_last_path", "dcn_sync_status", "dcn_selftest_timeout",
            "dcn_status_string"]
@@ -23,10 +25,12 @@ __all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF1
 class Handle:
     """Owns one ``dcn_handle_t`` (workspace + status word) on the current device."""
 
-    def __init__(self, path=DCN_PATH_AUTO):
+    def __init__(self, path=DCN_PATH_AUTO, sample=DCN_SAMPLE_INPUT_DTYPE):
         self.h = dcn_create()
         if path != DCN_PATH_AUTO:
             dcn_set_path(self.h, path)
+        if sample != DCN_SAMPLE_INPUT_DTYPE:
+            dcn_set_sample_precision(self.h, sample)
 
     def close(self):
         if self.h is not None:

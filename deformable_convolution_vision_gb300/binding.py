@@ -14,13 +14,15 @@ LIBRARY = os.path.join(_HERE, "libdcn.so")
 
 DCN_F32, DCN_BF16 = 0, 1
 DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC = 0, 1, 2
+DCN_SAMPLE_INPUT_DTYPE, DCN_SAMPLE_F32 = 0, 1
 STATUS = {0: "DCN_OK", 1: "DCN_ERR_INVALID_ARG", 2: "DCN_ERR_UNSUPPORTED", 3: "DCN_ERR_CUDA",
           4: "DCN_ERR_NO_DEVICE", 5: "DCN_ERR_OOM", 6: "DCN_ERR_TIMEOUT"}
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_forward_packed",
            "dcn_forward_host", "dcn_set_path", "dcn_last_path", "dcn_sync_status",
-           "dcn_selftest_timeout", "dcn_status_string", "dcn_forward_noalloc"]
+           "dcn_selftest_timeout", "dcn_status_string", "dcn_forward_noalloc",
+           "dcn_set_sample_precision"]
 
 
 class DcnError(RuntimeError):
@@ -50,6 +52,7 @@ def load():
         "dcn_forward_packed": ([P, P, P, P, P, P] + [I] * 9 + [P], I),
         "dcn_forward_host": (fwd, I),
         "dcn_set_path": ([P, I], I),
+        "dcn_set_sample_precision": ([P, I], I),
         "dcn_last_path": ([P], I),
         "dcn_sync_status": ([P, P], I),
         "dcn_selftest_timeout": ([P, LL, P], I),
@@ -129,6 +132,10 @@ def dcn_forward_host(h, x, offset, mask, weight, bias, out, B, C, H, W, O, kh, k
 
 def dcn_set_path(h, path):
     _check(load().dcn_set_path(h, path), "dcn_set_path")
+
+
+def dcn_set_sample_precision(h, mode):
+    _check(load().dcn_set_sample_precision(h, mode), "dcn_set_sample_precision")
 
 
 def dcn_last_path(h):

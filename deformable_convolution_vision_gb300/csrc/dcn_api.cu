@@ -19,6 +19,7 @@ struct dcn_handle_s {
     int sm_count = 0;
     int path = DCN_PATH_AUTO;
     int last_path = -1;
+    int sample = DCN_SAMPLE_INPUT_DTYPE;
 
     // packed weight [O][kh*kw*C]
     void *wpack = nullptr;
@@ -107,6 +108,7 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
     p.K = kh * kw * C;
     p.status = h->status;
     p.timeout_ns = kWaitLimitNs;
+    p.sample_f32 = h->sample == DCN_SAMPLE_F32 ? 1 : 0;
 
     const bool tc_ok = dtype == DCN_BF16 && dcn::tc_supported(C, O) &&
                        aligned(x, 16) && aligned(out, 16) && aligned(h->wpack, 16);
@@ -316,6 +318,12 @@ dcn_status_t dcn_set_path(dcn_handle_t h, int path) {
 }
 
 int dcn_last_path(dcn_handle_t h) { return h ? h->last_path : -1; }
+
+dcn_status_t dcn_set_sample_precision(dcn_handle_t h, int mode) {
+    if (!h || (mode != DCN_SAMPLE_INPUT_DTYPE && mode != DCN_SAMPLE_F32)) return DCN_ERR_INVALID_ARG;
+    h->sample = mode;
+    return DCN_OK;
+}
 
 dcn_status_t dcn_selftest_timeout(dcn_handle_t h, long long timeout_ns, void *stream) {
     if (!h || timeout_ns <= 0 || timeout_ns > 10000000000ll) return DCN_ERR_INVALID_ARG;

@@ -252,6 +252,23 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t v) {
     return pack_bf16x2(lo, hi);
 }
 
+// bf16x2 arithmetic on 32-bit words (low half = first element); each op
+// rounds once, to nearest even.
+__device__ __forceinline__ uint32_t bf16x2_splat(float v) {
+    __nv_bfloat162 r = __float2bfloat162_rn(v);
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // The two bf16 halves of a 32-bit word as fp32 (exact).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -19,6 +19,7 @@ struct Params {
     int K;                // kh * kw * C
     unsigned *status;     // device status word (timeout bit)
     unsigned long long timeout_ns;  // bound of every barrier wait
+    int sample_f32;       // tensor-core path: 1 = fp32 bilinear combine, 0 = bf16
 };
 
 enum Dtype { kF32 = 0, kBF16 = 1 };

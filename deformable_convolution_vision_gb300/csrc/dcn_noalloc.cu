@@ -124,6 +124,7 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.K = kh * kw * C;
     p.status = s->status;
     p.timeout_ns = kWaitLimitNs;
+    p.sample_f32 = 0;
 
     const bool tc = dtype == DCN_BF16 && dcn::tc_supported(C, O) && is_aligned(x, 16) &&
                     is_aligned(out, 16);

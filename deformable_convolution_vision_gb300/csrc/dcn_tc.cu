@@ -18,8 +18,9 @@
 //               each stage back to its "empty" barrier.
 //   warps 2..9  samplers: per (pixel, tap) the corner weights and
 //               addresses (S1, S2), then for 8 channels per lane the four
-//               16-byte corner loads, the fp32 bilinear combine (packed
-//               f32x2 FMAs: exactly the fp32 result), a bf16
+//               16-byte corner loads, the bilinear combine (by default in
+//               the input dtype, bf16, as packed bf16x2 FMAs; optionally in
+//               fp32 with packed f32x2 FMAs), a bf16
 //               round and one 16-byte store into the swizzled A stage (S3).
 //               After the last K-block they run the epilogue (S5): TMEM ->
 //               registers, + bias in fp32, bf16 round, channels-last store.
@@ -51,11 +52,16 @@ constexpr int TC_MMA_K = 16;
 constexpr int TC_TILE_W = 16;                                 // tile = 8 x 16 output pixels
 constexpr int TC_TILE_H = TC_BM / TC_TILE_W;                  // one tile row per sampler warp
 constexpr int TC_ITEMS = TC_ROWS_PER_WARP / 4;                // 16-byte items per lane per stage
-// per-warp corner table of one tap: for each of the warp's 16 rows the four
-// corner weights, each duplicated into an fp32 pair for the f32x2 pipe
-// (32 bytes), then the four corner indices (16 bytes)
-constexpr int TC_TABLE_W_BYTES = TC_ROWS_PER_WARP * 32;
-constexpr int TC_TABLE_BUF_BYTES = TC_TABLE_W_BYTES + TC_ROWS_PER_WARP * 16;
+// per-warp corner table of one tap, three arrays of 16-byte rows (one row
+// per pixel of the warp's tile row, so both the writes and the reads are
+// free of bank conflicts): corner weights {w0,w0,w1,w1} and {w2,w2,w3,w3},
+// each duplicated into fp32 pairs for the f32x2 pipe, then the four corner
+// indices
+constexpr int TC_TABLE_ARRAY_BYTES = TC_ROWS_PER_WARP * 16;
+constexpr int TC_TABLE_W01 = 0;
+constexpr int TC_TABLE_W23 = TC_TABLE_ARRAY_BYTES;
+constexpr int TC_TABLE_IDX = 2 * TC_TABLE_ARRAY_BYTES;
+constexpr int TC_TABLE_BUF_BYTES = 3 * TC_TABLE_ARRAY_BYTES;
 constexpr int TC_TABLE_BUFS = 4;                              // taps t .. t+3 in flight
 constexpr int TC_TABLE_WARP_BYTES = TC_TABLE_BUFS * TC_TABLE_BUF_BYTES;
 static_assert(TC_TILE_H == TC_SAMPLER_WARPS, "one tile row per sampler warp");
@@ -89,6 +95,7 @@ __host__ __device__ inline int tmem_cols_for(int O) {
     return n;
 }
 
+template <bool kSampleF32>
 __global__ void __launch_bounds__(TC_THREADS, 2)
 dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     extern __shared__ uint8_t smem_raw[];
@@ -222,25 +229,31 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 for (int q = 0; q < 4; ++q) { t.w[q] = 0.0f; t.idx[q] = 0; }
             }
             uint8_t *slot = table + (tap & (TC_TABLE_BUFS - 1)) * TC_TABLE_BUF_BYTES;
-            float4 *wdst = reinterpret_cast<float4 *>(slot + (lane & 15) * 32);
-            wdst[0] = make_float4(t.w[0], t.w[0], t.w[1], t.w[1]);
-            wdst[1] = make_float4(t.w[2], t.w[2], t.w[3], t.w[3]);
-            *reinterpret_cast<int4 *>(slot + TC_TABLE_W_BYTES + (lane & 15) * 16) =
+            const int rowb = (lane & 15) * 16;
+            if constexpr (kSampleF32) {
+                *reinterpret_cast<float4 *>(slot + TC_TABLE_W01 + rowb) = make_float4(t.w[0], t.w[0], t.w[1], t.w[1]);
+                *reinterpret_cast<float4 *>(slot + TC_TABLE_W23 + rowb) = make_float4(t.w[2], t.w[2], t.w[3], t.w[3]);
+            } else {
+                // the weights rounded to bf16, each duplicated into a bf16x2 pair
+                *reinterpret_cast<uint4 *>(slot + TC_TABLE_W01 + rowb) =
+                    make_uint4(bf16x2_splat(t.w[0]), bf16x2_splat(t.w[1]), bf16x2_splat(t.w[2]),
+                               bf16x2_splat(t.w[3]));
+            }
+            *reinterpret_cast<int4 *>(slot + TC_TABLE_IDX + rowb) =
                 make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
         };
 
         const int chunk = lane & 7;     // 8 channels = 16 bytes
         const int rsub = lane >> 3;     // 0..3
         // this lane's row offsets inside a table slot and inside an A stage
-        const uint32_t w_off = rsub * 32;
-        const uint32_t i_off = TC_TABLE_W_BYTES + rsub * 16;
+        const uint32_t r_off = rsub * 16;
         bool ok = true;
 
         // Issue the four 16-byte corner loads of item `it` (rows it*4 + rsub)
         // from a table slot.  Corners outside the image read a clamped
         // in-image address and carry weight 0.
         auto issue = [&](uint32_t slot, const __nv_bfloat16 *xc, int it, uint4 (&v)[4]) {
-            const int4 ci = lds_v4_s32(slot + i_off + it * 64);
+            const int4 ci = lds_v4_s32(slot + TC_TABLE_IDX + r_off + it * 64);
             v[0] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.x));
             v[1] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.y));
             v[2] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.z));
@@ -274,22 +287,36 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
 #pragma unroll
             for (int it = 0; it < TC_ITEMS; ++it) {
                 const int row = sw * TC_ROWS_PER_WARP + it * 4 + rsub;
-                uint64_t c0, c1, c2, c3;   // {w_q, w_q} pairs
-                lds_v2_u64(cur_slot + w_off + it * 128, c0, c1);
-                lds_v2_u64(cur_slot + w_off + it * 128 + 16, c2, c3);
                 const uint32_t *w0 = reinterpret_cast<const uint32_t *>(&v[it][0]);
                 const uint32_t *w1 = reinterpret_cast<const uint32_t *>(&v[it][1]);
                 const uint32_t *w2 = reinterpret_cast<const uint32_t *>(&v[it][2]);
                 const uint32_t *w3 = reinterpret_cast<const uint32_t *>(&v[it][3]);
                 uint32_t packed[4];
+                if constexpr (kSampleF32) {
+                    uint64_t c0, c1, c2, c3;   // {w_q, w_q} fp32 pairs
+                    lds_v2_u64(cur_slot + TC_TABLE_W01 + r_off + it * 64, c0, c1);
+                    lds_v2_u64(cur_slot + TC_TABLE_W23 + r_off + it * 64, c2, c3);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    // channels 2q, 2q+1: w0*x00 + w1*x01 + w2*x10 + w3*x11 in fp32
-                    uint64_t acc = f2_mul(c0, f2_make(bf16_lo(w0[q]), bf16_hi(w0[q])));
-                    acc = f2_fma(c1, f2_make(bf16_lo(w1[q]), bf16_hi(w1[q])), acc);
-                    acc = f2_fma(c2, f2_make(bf16_lo(w2[q]), bf16_hi(w2[q])), acc);
-                    acc = f2_fma(c3, f2_make(bf16_lo(w3[q]), bf16_hi(w3[q])), acc);
-                    packed[q] = f2_to_bf16x2(acc);
+                    for (int q = 0; q < 4; ++q) {
+                        // channels 2q, 2q+1: w0*x00 + w1*x01 + w2*x10 + w3*x11 in fp32
+                        uint64_t acc = f2_mul(c0, f2_make(bf16_lo(w0[q]), bf16_hi(w0[q])));
+                        acc = f2_fma(c1, f2_make(bf16_lo(w1[q]), bf16_hi(w1[q])), acc);
+                        acc = f2_fma(c2, f2_make(bf16_lo(w2[q]), bf16_hi(w2[q])), acc);
+                        acc = f2_fma(c3, f2_make(bf16_lo(w3[q]), bf16_hi(w3[q])), acc);
+                        packed[q] = f2_to_bf16x2(acc);
+                    }
+                } else {
+                    // the same sum in the input dtype: bf16 weights, one bf16
+                    // rounding per fused multiply-add, two channels per op
+                    const int4 cw = lds_v4_s32(cur_slot + TC_TABLE_W01 + r_off + it * 64);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t acc = bf16x2_mul(cw.x, w0[q]);
+                        acc = bf16x2_fma(cw.y, w1[q], acc);
+                        acc = bf16x2_fma(cw.z, w2[q], acc);
+                        acc = bf16x2_fma(cw.w, w3[q], acc);
+                        packed[q] = acc;
+                    }
                 }
                 // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r % 8)
                 sts_v4_b32(a_stage + row * 128 + ((chunk ^ (row & 7)) << 4),
@@ -354,6 +381,15 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
 }
 
 int g_max_smem_set = 0;
+int g_max_smem_set_f32 = 0;
+constexpr int kMaxSmemPerSm = 228 * 1024;   // largest shared-memory carveout of an SM
+
+// Shared memory one CTA may use.  Two CTAs fit an SM at 113 KB each; a
+// smaller budget leaves more of the SM's 256 KB L1/shared array as L1 cache
+// for the corner gathers, at the cost of pipeline depth.
+#ifndef DCN_TC_SMEM_BUDGET
+#define DCN_TC_SMEM_BUDGET (113 * 1024)
+#endif
 
 }  // namespace
 
@@ -364,18 +400,28 @@ bool tc_supported(int C, int O) {
 cudaError_t launch_tc(const Params &p, const CUtensorMap &wmap, cudaStream_t stream) {
     // Two CTAs per SM when the stages allow it, so one CTA's epilogue
     // overlaps the other's main loop.
-    const int per_cta_budget = 113 * 1024;
+    const int per_cta_budget = DCN_TC_SMEM_BUDGET;
     int stages = (per_cta_budget - 1024 - tc_layout(p.O, 0).total) / tc_layout(p.O, 1).stage_bytes;
     stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
     const TcLayout L = tc_layout(p.O, stages);
     const int smem = L.total + 1024;  // slack for 1024-byte alignment
-    if (smem > g_max_smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(dcn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kernel = p.sample_f32 ? dcn_tc_kernel<true> : dcn_tc_kernel<false>;
+    int &smem_set = p.sample_f32 ? g_max_smem_set_f32 : g_max_smem_set;
+    if (smem != smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        g_max_smem_set = smem;
+        // Ask for just enough shared memory for two resident CTAs (plus the
+        // 1 KB the system reserves per CTA); the rest of the SM's L1/shared
+        // array stays L1 cache, which serves the corner gathers.
+        const int needed = 2 * (smem + 1024);
+        int pct = (needed * 100 + kMaxSmemPerSm - 1) / kMaxSmemPerSm;
+        pct = pct > 100 ? 100 : pct;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
     }
     const int tiles = p.B * ((p.Ho + TC_TILE_H - 1) / TC_TILE_H) * ((p.Wo + TC_TILE_W - 1) / TC_TILE_W);
-    dcn_tc_kernel<<<tiles, TC_THREADS, smem, stream>>>(wmap, p, stages);
+    kernel<<<tiles, TC_THREADS, smem, stream>>>(wmap, p, stages);
     return cudaGetLastError();
 }
 

@@ -26,10 +26,15 @@
  *   bias   [O]                fp32, or NULL for zero
  *   out    [B, Ho, Wo, O]     channels-last, element type `dtype`
  *
- * Numerics: sampling coordinates, corner weights and the interpolation are
- * fp32; the contraction accumulates in fp32 for both dtypes (no TF32).  The
- * bf16 path rounds each interpolated sample to bf16 before the tensor-core
- * contraction and rounds the fp32 result (after bias) to bf16 at the end.
+ * Numerics: sampling coordinates and corner weights are fp32.  The bilinear
+ * combine of the four corners runs in the input dtype by default, as the
+ * page's own gather decomposition does (its corner weights and sums are in
+ * x.dtype): for bf16 the weights are rounded to bf16 and each fused
+ * multiply-add rounds once to bf16; dcn_set_sample_precision selects an
+ * fp32 combine instead.  The contraction accumulates in fp32 for both
+ * dtypes (no TF32).  The bf16 path rounds each interpolated sample to bf16
+ * before the tensor-core contraction and rounds the fp32 result (after
+ * bias) to bf16 at the end.
  *
  * Ownership: the caller owns every tensor and the stream.  A handle owns a
  * small device workspace (the packed weight, a status word and, for
@@ -128,6 +133,16 @@ DCN_API dcn_status_t dcn_forward_host(dcn_handle_t h,
                               const void *weight, const float *bias, void *out,
                               int B, int C, int H, int W, int O,
                               int kh, int kw, int pad, int dtype, void *stream);
+
+/* Precision of the bilinear combine on the bf16 tensor-core path. */
+typedef enum {
+    DCN_SAMPLE_INPUT_DTYPE = 0,  /* default: bf16 weights and bf16 fused multiply-adds */
+    DCN_SAMPLE_F32 = 1           /* fp32 weights and fp32 sums, then one bf16 rounding */
+} dcn_sample_t;
+
+/* Choose the combine precision (dcn_sample_t) for later calls on this
+ * handle.  The fp32 operand path always combines in fp32. */
+DCN_API dcn_status_t dcn_set_sample_precision(dcn_handle_t h, int mode);
 
 /* Choose the kernel path for later calls on this handle (dcn_path_t).
  * A forced path that cannot run a given shape makes that call return

@@ -13,7 +13,8 @@ import pytest
 import torch
 
 import oracle
-from deformable_convolution_vision_gb300 import (DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC, Handle,
+from deformable_convolution_vision_gb300 import (DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
+                                                 DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, Handle,
                                                  dcn_last_path)
 from deformable_convolution_vision_gb300.inputs import MAIN, WORKLOADS, Workload, make_inputs
 from tests.helpers import (TOL, compare_full, compare_points, oracle_full, run_cuda,
@@ -29,9 +30,10 @@ def _oracle_cost(wl):
     return wl.pixels * wl.O * wl.taps * wl.C * 4
 
 
-def check(wl, path=DCN_PATH_AUTO, inp=None, expect_path=None, n_points=256):
+def check(wl, path=DCN_PATH_AUTO, inp=None, expect_path=None, n_points=256,
+          sample=DCN_SAMPLE_INPUT_DTYPE):
     inp = make_inputs(wl) if inp is None else inp
-    with Handle(path) as h:
+    with Handle(path, sample) as h:
         out = run_cuda(inp, wl.pad, handle=h)
         taken = dcn_last_path(h.h)
     if expect_path is not None:
@@ -47,11 +49,12 @@ def check(wl, path=DCN_PATH_AUTO, inp=None, expect_path=None, n_points=256):
     return err, out
 
 
+@pytest.mark.parametrize("sample", [DCN_SAMPLE_INPUT_DTYPE, DCN_SAMPLE_F32])
 @pytest.mark.parametrize("name", MAIN)
-def test_workload(name):
+def test_workload(name, sample):
     wl = WORKLOADS[name]
     expect = DCN_PATH_SIMT if wl.dtype == "f32" else DCN_PATH_TC
-    check(wl, expect_path=expect)
+    check(wl, expect_path=expect, sample=sample)
 
 
 @pytest.mark.parametrize("ks", [1, 3, 7])
@@ -86,9 +89,10 @@ SIMT_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("sample", [DCN_SAMPLE_INPUT_DTYPE, DCN_SAMPLE_F32])
 @pytest.mark.parametrize("wl", TC_SHAPES, ids=lambda w: w.name)
-def test_tc_shapes(wl):
-    check(wl, expect_path=DCN_PATH_TC)
+def test_tc_shapes(wl, sample):
+    check(wl, expect_path=DCN_PATH_TC, sample=sample)
 
 
 @pytest.mark.parametrize("wl", SIMT_SHAPES, ids=lambda w: w.name)
