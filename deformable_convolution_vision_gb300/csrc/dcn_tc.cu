@@ -44,28 +44,29 @@ namespace {
 
 constexpr int TC_BM = 128;               // output pixels per tile (MMA M)
 constexpr int TC_BK = 64;                // channels per K-block (128 bytes)
-constexpr int TC_SAMPLER_WARPS = 8;
-constexpr int TC_THREADS = 32 * (2 + TC_SAMPLER_WARPS);
-constexpr int TC_ROWS_PER_WARP = TC_BM / TC_SAMPLER_WARPS;   // 16
-constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;                // 16 KB
 constexpr int TC_MMA_K = 16;
 constexpr int TC_TILE_W = 16;                                 // tile = 8 x 16 output pixels
-constexpr int TC_TILE_H = TC_BM / TC_TILE_W;                  // one tile row per sampler warp
+constexpr int TC_TILE_H = TC_BM / TC_TILE_W;
+constexpr int TC_SAMPLER_WARPS = 16;
+constexpr int TC_ROWS_PER_WARP = TC_BM / TC_SAMPLER_WARPS;    // 8 pixels: half a tile row
 constexpr int TC_ITEMS = TC_ROWS_PER_WARP / 4;                // 16-byte items per lane per stage
-// per-warp corner table of one tap, three arrays of 16-byte rows (one row
-// per pixel of the warp's tile row, so both the writes and the reads are
-// free of bank conflicts): corner weights {w0,w0,w1,w1} and {w2,w2,w3,w3},
-// each duplicated into fp32 pairs for the f32x2 pipe, then the four corner
-// indices
+constexpr int TC_THREADS = 32 * (2 + TC_SAMPLER_WARPS);
+constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;                 // 16 KB
+constexpr int TC_TAP_GROUP = 32 / TC_ROWS_PER_WARP;           // taps tabulated together (one per 8 lanes)
+constexpr int TC_TABLE_BUFS = 2 * TC_TAP_GROUP;               // ring: one group in use, one ahead
+static_assert(TC_ROWS_PER_WARP * 2 == TC_TILE_W, "two sampler warps per tile row");
+static_assert((TC_TABLE_BUFS & (TC_TABLE_BUFS - 1)) == 0, "ring size is a power of two");
+
+// Per-warp corner table of one tap: arrays of 16-byte rows, one row per
+// pixel of the warp (conflict-free writes and broadcast reads).  The fp32
+// combine keeps the weights as duplicated fp32 pairs {w0,w0,w1,w1},
+// {w2,w2,w3,w3}; the bf16 combine as four bf16x2 pairs.  Then the four
+// corner indices.
 constexpr int TC_TABLE_ARRAY_BYTES = TC_ROWS_PER_WARP * 16;
 constexpr int TC_TABLE_W01 = 0;
-constexpr int TC_TABLE_W23 = TC_TABLE_ARRAY_BYTES;
-constexpr int TC_TABLE_IDX = 2 * TC_TABLE_ARRAY_BYTES;
-constexpr int TC_TABLE_BUF_BYTES = 3 * TC_TABLE_ARRAY_BYTES;
-constexpr int TC_TABLE_BUFS = 4;                              // taps t .. t+3 in flight
-constexpr int TC_TABLE_WARP_BYTES = TC_TABLE_BUFS * TC_TABLE_BUF_BYTES;
-static_assert(TC_TILE_H == TC_SAMPLER_WARPS, "one tile row per sampler warp");
-static_assert(TC_ROWS_PER_WARP == TC_TILE_W, "a warp's rows are one tile row");
+constexpr int TC_TABLE_W23 = TC_TABLE_ARRAY_BYTES;            // fp32 combine only
+__host__ __device__ constexpr int table_buf_bytes(bool f32) { return (f32 ? 3 : 2) * TC_TABLE_ARRAY_BYTES; }
+__host__ __device__ constexpr int table_idx_off(bool f32) { return (f32 ? 2 : 1) * TC_TABLE_ARRAY_BYTES; }
 
 struct TcLayout {
     int stages;
@@ -76,7 +77,7 @@ struct TcLayout {
     int total;         // bytes used from the 1024-aligned base
 };
 
-__host__ __device__ inline TcLayout tc_layout(int O, int stages) {
+__host__ __device__ inline TcLayout tc_layout(int O, int stages, bool f32) {
     TcLayout L;
     L.stages = stages;
     L.b_bytes = O * TC_BK * 2;
@@ -85,7 +86,7 @@ __host__ __device__ inline TcLayout tc_layout(int O, int stages) {
     // full[stages], empty[stages], accum_full, tmem slot (8 bytes each)
     L.table_off = L.bar_off + (2 * stages + 2) * 8;
     L.table_off = (L.table_off + 15) & ~15;
-    L.total = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_WARP_BYTES;
+    L.total = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_BUFS * table_buf_bytes(f32);
     return L;
 }
 
@@ -96,12 +97,14 @@ __host__ __device__ inline int tmem_cols_for(int O) {
 }
 
 template <bool kSampleF32>
-__global__ void __launch_bounds__(TC_THREADS, 2)
+__global__ void __launch_bounds__(TC_THREADS, 1)
 dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
+    constexpr int kBuf = table_buf_bytes(kSampleF32);
+    constexpr int kIdx = table_idx_off(kSampleF32);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const TcLayout L = tc_layout(p.O, stages);
+    const TcLayout L = tc_layout(p.O, stages, kSampleF32);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + stages);
@@ -188,26 +191,30 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         }
     } else {
         // ------------------------------------------------ samplers
-        const int sw = warp - 2;   // this warp's tile row (16 pixels)
+        const int sw = warp - 2;                         // sampler warp 0..15
+        const int trow = sw >> 1;                        // its tile row
+        const int tcol0 = (sw & 1) * TC_ROWS_PER_WARP;   // its first tile column
+        const int row_base = trow * TC_TILE_W + tcol0;   // its first A row
         const __nv_bfloat16 *__restrict__ x = static_cast<const __nv_bfloat16 *>(p.x);
-        uint8_t *table = smem + L.table_off + sw * TC_TABLE_WARP_BYTES;
+        uint8_t *table = smem + L.table_off + sw * TC_TABLE_BUFS * kBuf;
         const uint32_t table_s = smem_u32(table);
         const uint32_t stage0_s = smem_u32(smem);
         const int HoWo = p.Ho * p.Wo;
 
-        // Geometry: lane l computes pixel (th0 + sw, tw0 + l % 16); lanes
-        // 0..15 take the even tap of a pair, lanes 16..31 the odd one.
-        const int my_h = th0 + sw;
-        const int my_w = tw0 + (lane & 15);
-        const int my_half = lane >> 4;
+        // Geometry: lane l computes pixel (th0 + trow, tw0 + tcol0 + l % 8)
+        // for tap group_tap + l / 8 (four taps per pass, all lanes busy).
+        const int my_g = lane >> 3;
+        const int my_px = lane & 7;
+        const int my_h = th0 + trow;
+        const int my_w = tw0 + tcol0 + my_px;
         const bool my_valid = (my_h < p.Ho) && (my_w < p.Wo);
         const int my_hw = my_valid ? my_h * p.Wo + my_w : 0;
 
-        // raw inputs (dy, dx, mask) of this lane's next tap, loaded about two
-        // taps ahead of their use so their latency hides behind the gathers
+        // raw inputs (dy, dx, mask) of this lane's next tap, fetched a whole
+        // tap group ahead of their use so their latency hides behind gathers
         float n_dy = 0.0f, n_dx = 0.0f, n_m = 0.0f;
-        auto load_raw = [&](int pair_tap) {
-            const int tap = pair_tap + my_half;
+        auto load_raw = [&](int group_tap) {
+            const int tap = group_tap + my_g;
             if (my_valid && tap < taps) {
                 const float *o = p.offset + (static_cast<size_t>(tb) * 2 * taps + 2 * tap) * HoWo + my_hw;
                 n_dy = __ldg(o);
@@ -216,9 +223,9 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                              : 1.0f;
             }
         };
-        // corner tables of taps pair_tap and pair_tap + 1 (ring slots tap % 4)
-        auto tabulate = [&](int pair_tap) {
-            const int tap = pair_tap + my_half;
+        // corner tables of taps group_tap .. group_tap + 3 (ring slot tap % 8)
+        auto tabulate = [&](int group_tap) {
+            const int tap = group_tap + my_g;
             TapCorners t;
             if (my_valid && tap < taps) {
                 const int i = tap / p.kw;
@@ -228,8 +235,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) { t.w[q] = 0.0f; t.idx[q] = 0; }
             }
-            uint8_t *slot = table + (tap & (TC_TABLE_BUFS - 1)) * TC_TABLE_BUF_BYTES;
-            const int rowb = (lane & 15) * 16;
+            uint8_t *slot = table + (tap & (TC_TABLE_BUFS - 1)) * kBuf;
+            const int rowb = my_px * 16;
             if constexpr (kSampleF32) {
                 *reinterpret_cast<float4 *>(slot + TC_TABLE_W01 + rowb) = make_float4(t.w[0], t.w[0], t.w[1], t.w[1]);
                 *reinterpret_cast<float4 *>(slot + TC_TABLE_W23 + rowb) = make_float4(t.w[2], t.w[2], t.w[3], t.w[3]);
@@ -239,21 +246,19 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     make_uint4(bf16x2_splat(t.w[0]), bf16x2_splat(t.w[1]), bf16x2_splat(t.w[2]),
                                bf16x2_splat(t.w[3]));
             }
-            *reinterpret_cast<int4 *>(slot + TC_TABLE_IDX + rowb) =
-                make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
+            *reinterpret_cast<int4 *>(slot + kIdx + rowb) = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
         };
 
         const int chunk = lane & 7;     // 8 channels = 16 bytes
         const int rsub = lane >> 3;     // 0..3
-        // this lane's row offsets inside a table slot and inside an A stage
         const uint32_t r_off = rsub * 16;
         bool ok = true;
 
-        // Issue the four 16-byte corner loads of item `it` (rows it*4 + rsub)
-        // from a table slot.  Corners outside the image read a clamped
-        // in-image address and carry weight 0.
+        // Issue the four 16-byte corner loads of item `it` (warp rows
+        // it*4 + rsub) from a table slot.  Corners outside the image read a
+        // clamped in-image address and carry weight 0.
         auto issue = [&](uint32_t slot, const __nv_bfloat16 *xc, int it, uint4 (&v)[4]) {
-            const int4 ci = lds_v4_s32(slot + TC_TABLE_IDX + r_off + it * 64);
+            const int4 ci = lds_v4_s32(slot + kIdx + r_off + it * 64);
             v[0] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.x));
             v[1] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.y));
             v[2] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.z));
@@ -262,22 +267,29 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
 
         load_raw(0);
         tabulate(0);
-        if (taps > 2) load_raw(2);
+        if (taps > TC_TAP_GROUP) load_raw(TC_TAP_GROUP);
         __syncwarp();
 
-        // Stage, phase, tap and channel block advance by counters (no
-        // divisions).  Each lane issues all sixteen corner loads of a stage
-        // before it waits for the stage to be free.
+        // Rolling pipeline: the corner loads of K-block kb + 1 go out item by
+        // item as the items of K-block kb are combined, so each lane always
+        // has loads in flight.  Stage, phase, tap and channel block advance
+        // by counters (no divisions).
+        uint4 v[TC_ITEMS][4];
+        {
+            const __nv_bfloat16 *xc0 = x + chunk * 8;
+#pragma unroll
+            for (int it = 0; it < TC_ITEMS; ++it) issue(table_s, xc0, it, v[it]);
+        }
         int s = 0;
         uint32_t phase = 0;
         int tap = 0, cb = 0;
+        int n_tap = ncb == 1 ? 1 : 0, n_cb = ncb == 1 ? 0 : 1;   // K-block kb + 1
 
         for (int kb = 0; kb < nkb; ++kb) {
-            const uint32_t cur_slot = table_s + (tap & (TC_TABLE_BUFS - 1)) * TC_TABLE_BUF_BYTES;
-            const __nv_bfloat16 *xc = x + cb * TC_BK + chunk * 8;
-            uint4 v[TC_ITEMS][4];
-#pragma unroll
-            for (int it = 0; it < TC_ITEMS; ++it) issue(cur_slot, xc, it, v[it]);
+            const bool has_next = kb + 1 < nkb;
+            const uint32_t cur_slot = table_s + (tap & (TC_TABLE_BUFS - 1)) * kBuf;
+            const uint32_t nxt_slot = table_s + (n_tap & (TC_TABLE_BUFS - 1)) * kBuf;
+            const __nv_bfloat16 *nxc = x + n_cb * TC_BK + chunk * 8;
 
             // every lane waits; the warp leaves the loop together if any lane ran out
             const bool got = mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns, 2000u);
@@ -286,7 +298,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             const uint32_t a_stage = stage0_s + s * L.stage_bytes;
 #pragma unroll
             for (int it = 0; it < TC_ITEMS; ++it) {
-                const int row = sw * TC_ROWS_PER_WARP + it * 4 + rsub;
+                const int row = row_base + it * 4 + rsub;
                 const uint32_t *w0 = reinterpret_cast<const uint32_t *>(&v[it][0]);
                 const uint32_t *w1 = reinterpret_cast<const uint32_t *>(&v[it][1]);
                 const uint32_t *w2 = reinterpret_cast<const uint32_t *>(&v[it][2]);
@@ -318,6 +330,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                         packed[q] = acc;
                     }
                 }
+                if (has_next) issue(nxt_slot, nxc, it, v[it]);
                 // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r % 8)
                 sts_v4_b32(a_stage + row * 128 + ((chunk ^ (row & 7)) << 4),
                            packed[0], packed[1], packed[2], packed[3]);
@@ -326,14 +339,16 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             __syncwarp();
             if (lane == 0) mbar_arrive(full0 + 8 * s);
 
-            if (cb == ncb - 1 && (tap & 1) == 0 && tap + 2 < taps) {
-                // ring slots of taps tap - 2 and tap - 1 are no longer read:
-                // fill them for taps tap + 2, tap + 3, and fetch the pair after
-                tabulate(tap + 2);
-                if (tap + 4 < taps) load_raw(tap + 4);
+            if (cb == ncb - 1 && (tap & (TC_TAP_GROUP - 1)) == 0 && tap + TC_TAP_GROUP < taps) {
+                // the ring slots of taps tap - 4 .. tap - 1 are no longer read:
+                // fill them for taps tap + 4 .. tap + 7 and fetch the group after
+                tabulate(tap + TC_TAP_GROUP);
+                if (tap + 2 * TC_TAP_GROUP < taps) load_raw(tap + 2 * TC_TAP_GROUP);
                 __syncwarp();
             }
-            if (++cb == ncb) { cb = 0; ++tap; }
+            tap = n_tap;
+            cb = n_cb;
+            if (++n_cb == ncb) { n_cb = 0; ++n_tap; }
             if (++s == stages) { s = 0; phase ^= 1; }
         }
 
@@ -342,15 +357,15 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         __syncwarp();
         tc_fence_after_sync();
         const int q = warp & 3;                 // TMEM lane quarter of this warp
-        const int half = (warp - 2) >> 2;       // two warps per quarter split the columns
-        const int row = q * 32 + lane;          // tile row = pixel within the tile
+        const int part = (warp - 2) >> 2;       // four warps per quarter split the columns
+        const int row = q * 32 + lane;          // A row = pixel within the tile
         const int oh = th0 + row / TC_TILE_W;
         const int ow = tw0 + row % TC_TILE_W;
         const bool pix_valid = oh < p.Ho && ow < p.Wo;
         const size_t pix = (static_cast<size_t>(tb) * p.Ho + oh) * p.Wo + ow;
         const int nch = p.O / 16;
-        const int ch_begin = half == 0 ? 0 : nch / 2;
-        const int ch_end = half == 0 ? nch / 2 : nch;
+        const int ch_begin = part * nch / 4;
+        const int ch_end = (part + 1) * nch / 4;
         __nv_bfloat16 *__restrict__ out = static_cast<__nv_bfloat16 *>(p.out);
         for (int ch = ch_begin; ch < ch_end; ++ch) {
             float vv[16];
@@ -382,13 +397,23 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
 
 int g_max_smem_set = 0;
 int g_max_smem_set_f32 = 0;
-constexpr int kMaxSmemPerSm = 228 * 1024;   // largest shared-memory carveout of an SM
 
-// Shared memory one CTA may use.  Two CTAs fit an SM at 113 KB each; a
-// smaller budget leaves more of the SM's 256 KB L1/shared array as L1 cache
-// for the corner gathers, at the cost of pipeline depth.
+// Carveout preference (percent of the 228 KB maximum) that selects the
+// smallest supported shared-memory size holding `needed` bytes; the driver
+// rounds a percentage up to the next supported size.
+int carveout_percent(int needed) {
+    static const int kSizesKb[] = {0, 8, 16, 32, 64, 100, 132, 164, 196, 228};
+    for (int kb : kSizesKb) {
+        if (kb * 1024 >= needed) return kb == 0 ? 0 : (kb * 100) / 228;
+    }
+    return 100;
+}
+
+// Shared memory the CTA may use (stages + tables + alignment).  The SM's
+// L1/shared array is 256 KB; at 131 KB the 132 KB carveout leaves 124 KB of
+// L1 for the corner gathers.
 #ifndef DCN_TC_SMEM_BUDGET
-#define DCN_TC_SMEM_BUDGET (113 * 1024)
+#define DCN_TC_SMEM_BUDGET (131 * 1024)
 #endif
 
 }  // namespace
@@ -398,24 +423,23 @@ bool tc_supported(int C, int O) {
 }
 
 cudaError_t launch_tc(const Params &p, const CUtensorMap &wmap, cudaStream_t stream) {
-    // Two CTAs per SM when the stages allow it, so one CTA's epilogue
-    // overlaps the other's main loop.
-    const int per_cta_budget = DCN_TC_SMEM_BUDGET;
-    int stages = (per_cta_budget - 1024 - tc_layout(p.O, 0).total) / tc_layout(p.O, 1).stage_bytes;
+    // One CTA per SM.  Its shared memory is kept small so that most of the
+    // SM's L1/shared array stays L1 cache, which holds a good part of the
+    // tile's corner footprint across taps.
+    const bool f32 = p.sample_f32 != 0;
+    const int fixed = tc_layout(p.O, 0, f32).total + 1024;
+    int stages = (DCN_TC_SMEM_BUDGET - fixed) / tc_layout(p.O, 1, f32).stage_bytes;
     stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-    const TcLayout L = tc_layout(p.O, stages);
+    const TcLayout L = tc_layout(p.O, stages, f32);
     const int smem = L.total + 1024;  // slack for 1024-byte alignment
-    auto kernel = p.sample_f32 ? dcn_tc_kernel<true> : dcn_tc_kernel<false>;
-    int &smem_set = p.sample_f32 ? g_max_smem_set_f32 : g_max_smem_set;
+    auto kernel = f32 ? dcn_tc_kernel<true> : dcn_tc_kernel<false>;
+    int &smem_set = f32 ? g_max_smem_set_f32 : g_max_smem_set;
     if (smem != smem_set) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        // Ask for just enough shared memory for two resident CTAs (plus the
-        // 1 KB the system reserves per CTA); the rest of the SM's L1/shared
-        // array stays L1 cache, which serves the corner gathers.
-        const int needed = 2 * (smem + 1024);
-        int pct = (needed * 100 + kMaxSmemPerSm - 1) / kMaxSmemPerSm;
-        pct = pct > 100 ? 100 : pct;
+        // ask for just enough shared memory for the one resident CTA (plus
+        // the 1 KB the system reserves per CTA); the rest stays L1
+        const int pct = carveout_percent(smem + 1024);
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
         if (e != cudaSuccess) return e;
         smem_set = smem;
