@@ -111,7 +111,7 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
     p.sample_f32 = h->sample == DCN_SAMPLE_F32 ? 1 : 0;
 
     const bool tc_ok = dtype == DCN_BF16 && dcn::tc_supported(C, O) &&
-                       aligned(x, 16) && aligned(out, 16) && aligned(h->wpack, 16);
+                       aligned(x, 32) && aligned(out, 16) && aligned(h->wpack, 16);
     int path = h->path;
     if (path == DCN_PATH_AUTO) path = tc_ok ? DCN_PATH_TC : DCN_PATH_SIMT;
     if (path == DCN_PATH_TC && !tc_ok) return DCN_ERR_UNSUPPORTED;
@@ -243,7 +243,7 @@ dcn_status_t dcn_forward(dcn_handle_t h, const void *x, const float *offset, con
     if (st != DCN_OK) return st;
     // a forced tensor-core path that cannot run this shape launches nothing
     if (h->path == DCN_PATH_TC &&
-        !(dtype == DCN_BF16 && dcn::tc_supported(C, O) && aligned(x, 16) && aligned(out, 16)))
+        !(dtype == DCN_BF16 && dcn::tc_supported(C, O) && aligned(x, 32) && aligned(out, 16)))
         return DCN_ERR_UNSUPPORTED;
     cudaStream_t s = as_stream(stream);
     st = pack_impl(h, weight, O, C, kh, kw, dtype, s);

@@ -104,6 +104,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 256-bit read-only global load (sm_100 family); `p` must be 32-byte aligned.
+struct u32x8 { uint32_t w[8]; };
+__device__ __forceinline__ u32x8 ldg_v8(const void *p) {
+    u32x8 v;
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
+                   "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+    return v;
+}
+
 // Vector shared-memory accesses (one instruction each).
 __device__ __forceinline__ int4 lds_v4_s32(uint32_t addr) {
     int4 v;
@@ -117,7 +128,7 @@ __device__ __forceinline__ void lds_v2_u64(uint32_t addr, uint64_t &a, uint64_t 
 __device__ __forceinline__ void sts_v4_b32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                            uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                 :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+                 :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
 // --------------------------------------------------------------------- TMA

@@ -126,7 +126,7 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.timeout_ns = kWaitLimitNs;
     p.sample_f32 = 0;
 
-    const bool tc = dtype == DCN_BF16 && dcn::tc_supported(C, O) && is_aligned(x, 16) &&
+    const bool tc = dtype == DCN_BF16 && dcn::tc_supported(C, O) && is_aligned(x, 32) &&
                     is_aligned(out, 16);
     cudaError_t e;
     if (tc) {

@@ -16,7 +16,7 @@
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=O,
 //               K=16) x 4 per K-block, accumulating in TMEM, and commits
 //               each stage back to its "empty" barrier.
-//   warps 2..9  samplers: per (pixel, tap) the corner weights and
+//   warps 2..17 samplers: per (pixel, tap) the corner weights and
 //               addresses (S1, S2), then for 8 channels per lane the four
 //               16-byte corner loads, the bilinear combine (by default in
 //               the input dtype, bf16, as packed bf16x2 FMAs; optionally in
@@ -49,7 +49,6 @@ constexpr int TC_TILE_W = 16;                                 // tile = 8 x 16 o
 constexpr int TC_TILE_H = TC_BM / TC_TILE_W;
 constexpr int TC_SAMPLER_WARPS = 16;
 constexpr int TC_ROWS_PER_WARP = TC_BM / TC_SAMPLER_WARPS;    // 8 pixels: half a tile row
-constexpr int TC_ITEMS = TC_ROWS_PER_WARP / 4;                // 16-byte items per lane per stage
 constexpr int TC_THREADS = 32 * (2 + TC_SAMPLER_WARPS);
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;                 // 16 KB
 constexpr int TC_TAP_GROUP = 32 / TC_ROWS_PER_WARP;           // taps tabulated together (one per 8 lanes)
@@ -249,20 +248,27 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             *reinterpret_cast<int4 *>(slot + kIdx + rowb) = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
         };
 
-        const int chunk = lane & 7;     // 8 channels = 16 bytes
-        const int rsub = lane >> 3;     // 0..3
+        // Gather mapping: lane l handles 16 channels (32 bytes: quarter
+        // l % 4 of the 128-byte K-block row) of warp row l / 4.
+        const int quart = lane & 3;
+        const int rsub = lane >> 2;     // 0..7
+        const int arow = row_base + rsub;
         const uint32_t r_off = rsub * 16;
+        // its two 16-byte chunks in an A stage (128-byte swizzle: chunk c of
+        // row r lives at chunk c ^ (r % 8))
+        const uint32_t sts0 = arow * 128 + (((2 * quart) ^ (arow & 7)) << 4);
+        const uint32_t sts1 = arow * 128 + (((2 * quart + 1) ^ (arow & 7)) << 4);
         bool ok = true;
 
-        // Issue the four 16-byte corner loads of item `it` (warp rows
-        // it*4 + rsub) from a table slot.  Corners outside the image read a
-        // clamped in-image address and carry weight 0.
-        auto issue = [&](uint32_t slot, const __nv_bfloat16 *xc, int it, uint4 (&v)[4]) {
-            const int4 ci = lds_v4_s32(slot + kIdx + r_off + it * 64);
-            v[0] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.x));
-            v[1] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.y));
-            v[2] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.z));
-            v[3] = __ldg(reinterpret_cast<const uint4 *>(xc + ci.w));
+        // Issue the four 32-byte corner loads of this lane's item from a
+        // table slot.  Corners outside the image read a clamped in-image
+        // address and carry weight 0.
+        auto issue = [&](uint32_t slot, const __nv_bfloat16 *xc, u32x8 (&v)[4]) {
+            const int4 ci = lds_v4_s32(slot + kIdx + r_off);
+            v[0] = ldg_v8(xc + ci.x);
+            v[1] = ldg_v8(xc + ci.y);
+            v[2] = ldg_v8(xc + ci.z);
+            v[3] = ldg_v8(xc + ci.w);
         };
 
         load_raw(0);
@@ -270,71 +276,57 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         if (taps > TC_TAP_GROUP) load_raw(TC_TAP_GROUP);
         __syncwarp();
 
-        // Rolling pipeline: the corner loads of K-block kb + 1 go out item by
-        // item as the items of K-block kb are combined, so each lane always
-        // has loads in flight.  Stage, phase, tap and channel block advance
-        // by counters (no divisions).
-        uint4 v[TC_ITEMS][4];
-        {
-            const __nv_bfloat16 *xc0 = x + chunk * 8;
-#pragma unroll
-            for (int it = 0; it < TC_ITEMS; ++it) issue(table_s, xc0, it, v[it]);
-        }
+        // Rolling pipeline: the corner loads of K-block kb + 1 go out as
+        // K-block kb is combined, so each lane always has loads in flight.
+        // Stage, phase, tap and channel block advance by counters (no
+        // divisions).
+        u32x8 v[4];
+        issue(table_s, x + quart * 16, v);
         int s = 0;
         uint32_t phase = 0;
         int tap = 0, cb = 0;
         int n_tap = ncb == 1 ? 1 : 0, n_cb = ncb == 1 ? 0 : 1;   // K-block kb + 1
+        uint32_t a_stage = stage0_s;
 
         for (int kb = 0; kb < nkb; ++kb) {
             const bool has_next = kb + 1 < nkb;
             const uint32_t cur_slot = table_s + (tap & (TC_TABLE_BUFS - 1)) * kBuf;
-            const uint32_t nxt_slot = table_s + (n_tap & (TC_TABLE_BUFS - 1)) * kBuf;
-            const __nv_bfloat16 *nxc = x + n_cb * TC_BK + chunk * 8;
 
             // every lane waits; the warp leaves the loop together if any lane ran out
             const bool got = mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns, 2000u);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
 
-            const uint32_t a_stage = stage0_s + s * L.stage_bytes;
+            uint32_t packed[8];
+            if constexpr (kSampleF32) {
+                uint64_t c0, c1, c2, c3;   // {w_q, w_q} fp32 pairs
+                lds_v2_u64(cur_slot + TC_TABLE_W01 + r_off, c0, c1);
+                lds_v2_u64(cur_slot + TC_TABLE_W23 + r_off, c2, c3);
 #pragma unroll
-            for (int it = 0; it < TC_ITEMS; ++it) {
-                const int row = row_base + it * 4 + rsub;
-                const uint32_t *w0 = reinterpret_cast<const uint32_t *>(&v[it][0]);
-                const uint32_t *w1 = reinterpret_cast<const uint32_t *>(&v[it][1]);
-                const uint32_t *w2 = reinterpret_cast<const uint32_t *>(&v[it][2]);
-                const uint32_t *w3 = reinterpret_cast<const uint32_t *>(&v[it][3]);
-                uint32_t packed[4];
-                if constexpr (kSampleF32) {
-                    uint64_t c0, c1, c2, c3;   // {w_q, w_q} fp32 pairs
-                    lds_v2_u64(cur_slot + TC_TABLE_W01 + r_off + it * 64, c0, c1);
-                    lds_v2_u64(cur_slot + TC_TABLE_W23 + r_off + it * 64, c2, c3);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        // channels 2q, 2q+1: w0*x00 + w1*x01 + w2*x10 + w3*x11 in fp32
-                        uint64_t acc = f2_mul(c0, f2_make(bf16_lo(w0[q]), bf16_hi(w0[q])));
-                        acc = f2_fma(c1, f2_make(bf16_lo(w1[q]), bf16_hi(w1[q])), acc);
-                        acc = f2_fma(c2, f2_make(bf16_lo(w2[q]), bf16_hi(w2[q])), acc);
-                        acc = f2_fma(c3, f2_make(bf16_lo(w3[q]), bf16_hi(w3[q])), acc);
-                        packed[q] = f2_to_bf16x2(acc);
-                    }
-                } else {
-                    // the same sum in the input dtype: bf16 weights, one bf16
-                    // rounding per fused multiply-add, two channels per op
-                    const int4 cw = lds_v4_s32(cur_slot + TC_TABLE_W01 + r_off + it * 64);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t acc = bf16x2_mul(cw.x, w0[q]);
-                        acc = bf16x2_fma(cw.y, w1[q], acc);
-                        acc = bf16x2_fma(cw.z, w2[q], acc);
-                        acc = bf16x2_fma(cw.w, w3[q], acc);
-                        packed[q] = acc;
-                    }
+                for (int q = 0; q < 8; ++q) {
+                    // channels 2q, 2q+1: w0*x00 + w1*x01 + w2*x10 + w3*x11 in fp32
+                    uint64_t acc = f2_mul(c0, f2_make(bf16_lo(v[0].w[q]), bf16_hi(v[0].w[q])));
+                    acc = f2_fma(c1, f2_make(bf16_lo(v[1].w[q]), bf16_hi(v[1].w[q])), acc);
+                    acc = f2_fma(c2, f2_make(bf16_lo(v[2].w[q]), bf16_hi(v[2].w[q])), acc);
+                    acc = f2_fma(c3, f2_make(bf16_lo(v[3].w[q]), bf16_hi(v[3].w[q])), acc);
+                    packed[q] = f2_to_bf16x2(acc);
                 }
-                if (has_next) issue(nxt_slot, nxc, it, v[it]);
-                // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r % 8)
-                sts_v4_b32(a_stage + row * 128 + ((chunk ^ (row & 7)) << 4),
-                           packed[0], packed[1], packed[2], packed[3]);
+            } else {
+                // the same sum in the input dtype: bf16 weights, one bf16
+                // rounding per fused multiply-add, two channels per op
+                const int4 cw = lds_v4_s32(cur_slot + TC_TABLE_W01 + r_off);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t acc = bf16x2_mul(cw.x, v[0].w[q]);
+                    acc = bf16x2_fma(cw.y, v[1].w[q], acc);
+                    acc = bf16x2_fma(cw.z, v[2].w[q], acc);
+                    acc = bf16x2_fma(cw.w, v[3].w[q], acc);
+                    packed[q] = acc;
+                }
             }
+            if (has_next)
+                issue(table_s + (n_tap & (TC_TABLE_BUFS - 1)) * kBuf, x + n_cb * TC_BK + quart * 16, v);
+            sts_v4_b32(a_stage + sts0, packed[0], packed[1], packed[2], packed[3]);
+            sts_v4_b32(a_stage + sts1, packed[4], packed[5], packed[6], packed[7]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(full0 + 8 * s);
@@ -349,7 +341,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             tap = n_tap;
             cb = n_cb;
             if (++n_cb == ncb) { n_cb = 0; ++n_tap; }
-            if (++s == stages) { s = 0; phase ^= 1; }
+            a_stage += L.stage_bytes;
+            if (++s == stages) { s = 0; phase ^= 1; a_stage = stage0_s; }
         }
 
         // ------------------------------------------------ epilogue (S5)

@@ -79,8 +79,9 @@ typedef enum {
 } dcn_status_t;
 
 /* Kernel selection for bf16.  AUTO takes the tcgen05 path when
- * C % 64 == 0, O % 16 == 0, 16 <= O <= 256 and x/out are 16-byte aligned,
- * and the CUDA-core path otherwise.  fp32 always takes the CUDA-core path. */
+ * C % 64 == 0, O % 16 == 0, 16 <= O <= 256, x is 32-byte aligned and out is
+ * 16-byte aligned, and the CUDA-core path otherwise.  fp32 always takes the
+ * CUDA-core path. */
 typedef enum {
     DCN_PATH_AUTO = 0,
     DCN_PATH_SIMT = 1,   /* CUDA-core fused sample + FFMA contraction */
