@@ -34,30 +34,32 @@ __device__ __forceinline__ void tap_corners(float dy, float dx, float m,
     const float fx = floorf(px);
     const float ly = py - fy;
     const float lx = px - fx;
-    const float hy = 1.0f - ly;
-    const float hx = 1.0f - lx;
     const int y0 = static_cast<int>(fy);
     const int x0 = static_cast<int>(fx);
-    const int y1 = y0 + 1;
-    const int x1 = x0 + 1;
-    const bool vy0 = (y0 >= 0) && (y0 <= H - 1);
-    const bool vy1 = (y1 >= 0) && (y1 <= H - 1);
-    const bool vx0 = (x0 >= 0) && (x0 <= W - 1);
-    const bool vx1 = (x1 >= 0) && (x1 <= W - 1);
-    t.w[0] = (vy0 && vx0) ? hy * hx * m : 0.0f;
-    t.w[1] = (vy0 && vx1) ? hy * lx * m : 0.0f;
-    t.w[2] = (vy1 && vx0) ? ly * hx * m : 0.0f;
-    t.w[3] = (vy1 && vx1) ? ly * lx * m : 0.0f;
+    // a corner row / column is inside when 0 <= index < H (W)
+    const bool vy0 = static_cast<unsigned>(y0) < static_cast<unsigned>(H);
+    const bool vy1 = static_cast<unsigned>(y0 + 1) < static_cast<unsigned>(H);
+    const bool vx0 = static_cast<unsigned>(x0) < static_cast<unsigned>(W);
+    const bool vx1 = static_cast<unsigned>(x0 + 1) < static_cast<unsigned>(W);
+    // row weights carry the mask; a corner outside gets weight 0
+    const float wy0 = vy0 ? (1.0f - ly) * m : 0.0f;
+    const float wy1 = vy1 ? ly * m : 0.0f;
+    const float wx0 = vx0 ? 1.0f - lx : 0.0f;
+    const float wx1 = vx1 ? lx : 0.0f;
+    t.w[0] = wy0 * wx0;
+    t.w[1] = wy0 * wx1;
+    t.w[2] = wy1 * wx0;
+    t.w[3] = wy1 * wx1;
+    // clamped corner addresses: the top-left one, then steps of one column
+    // and one row that are 0 where the clamp folds both corners together
     const int yc0 = min(max(y0, 0), H - 1);
-    const int yc1 = min(max(y1, 0), H - 1);
     const int xc0 = min(max(x0, 0), W - 1);
-    const int xc1 = min(max(x1, 0), W - 1);
-    const int row0 = (b * H + yc0) * W;
-    const int row1 = (b * H + yc1) * W;
-    t.idx[0] = (row0 + xc0) * C;
-    t.idx[1] = (row0 + xc1) * C;
-    t.idx[2] = (row1 + xc0) * C;
-    t.idx[3] = (row1 + xc1) * C;
+    const int dxc = (x0 + 1 >= 1 && x0 + 1 <= W - 1) ? C : 0;      // xc1 - xc0, times C
+    const int dyc = (y0 + 1 >= 1 && y0 + 1 <= H - 1) ? W * C : 0;  // yc1 - yc0, times W*C
+    t.idx[0] = ((b * H + yc0) * W + xc0) * C;
+    t.idx[1] = t.idx[0] + dxc;
+    t.idx[2] = t.idx[0] + dyc;
+    t.idx[3] = t.idx[2] + dxc;
 }
 
 }  // namespace dcn

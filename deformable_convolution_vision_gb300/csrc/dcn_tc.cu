@@ -222,14 +222,16 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                              : 1.0f;
             }
         };
+        // kernel row and column (ti, tj) of this lane's tap, advanced by four
+        // taps per tabulation instead of divided out each time
+        int ti = my_g / p.kw;
+        int tj = my_g - ti * p.kw;
         // corner tables of taps group_tap .. group_tap + 3 (ring slot tap % 8)
         auto tabulate = [&](int group_tap) {
             const int tap = group_tap + my_g;
             TapCorners t;
             if (my_valid && tap < taps) {
-                const int i = tap / p.kw;
-                const int j = tap - i * p.kw;
-                tap_corners(n_dy, n_dx, n_m, my_h, my_w, i, j, p.pad, tb, p.H, p.W, p.C, t);
+                tap_corners(n_dy, n_dx, n_m, my_h, my_w, ti, tj, p.pad, tb, p.H, p.W, p.C, t);
             } else {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) { t.w[q] = 0.0f; t.idx[q] = 0; }
@@ -246,6 +248,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                                bf16x2_splat(t.w[3]));
             }
             *reinterpret_cast<int4 *>(slot + kIdx + rowb) = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
+            tj += TC_TAP_GROUP;
+            while (tj >= p.kw) { tj -= p.kw; ++ti; }
         };
 
         // Gather mapping: lane l handles 16 channels (32 bytes: quarter
