@@ -28,6 +28,14 @@ struct dcn_handle_s {
 
     unsigned *status = nullptr;  // device status word
 
+    // stream-K workspace of the tensor-core kernel: one fp32 partial tile
+    // and one flag word per SM, and the flag value of the next launch
+    void *partial = nullptr;
+    size_t partial_cap = 0;
+    void *flags = nullptr;
+    size_t flags_cap = 0;
+    unsigned epoch = 0;
+
     // device staging for dcn_forward_host: x, offset, mask, weight, bias, out
     void *stage[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     size_t stage_cap[6] = {0, 0, 0, 0, 0, 0};
@@ -109,6 +117,11 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
     p.status = h->status;
     p.timeout_ns = kWaitLimitNs;
     p.sample_f32 = h->sample == DCN_SAMPLE_F32 ? 1 : 0;
+    p.partial = nullptr;
+    p.flags = nullptr;
+    p.epoch = 0;
+    p.sm_count = h->sm_count;
+    p.units_per_cta = 0;
 
     const bool tc_ok = dtype == DCN_BF16 && dcn::tc_supported(C, O) &&
                        aligned(x, 32) && aligned(out, 16) && aligned(h->wpack, 16);
@@ -129,6 +142,25 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
                                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return DCN_ERR_CUDA;
+        // stream-K workspace: a [O/16][128][16] fp32 tile per SM, plus flags
+        const size_t part_bytes = static_cast<size_t>(h->sm_count) * 128 * O * sizeof(float);
+        const size_t flag_bytes = static_cast<size_t>(h->sm_count + 1) * sizeof(unsigned);
+        dcn_status_t st = ensure(&h->partial, &h->partial_cap, part_bytes, s);
+        if (st != DCN_OK) return st;
+        if (h->flags_cap < flag_bytes || !h->flags) {
+            st = ensure(&h->flags, &h->flags_cap, flag_bytes, s);
+            if (st != DCN_OK) return st;
+            if (cudaMemsetAsync(h->flags, 0, h->flags_cap, s) != cudaSuccess) return DCN_ERR_CUDA;
+            h->epoch = 0;
+        }
+        if (++h->epoch == 0) {
+            // flag values wrapped: clear the flags and start again at 1
+            if (cudaMemsetAsync(h->flags, 0, h->flags_cap, s) != cudaSuccess) return DCN_ERR_CUDA;
+            h->epoch = 1;
+        }
+        p.partial = static_cast<float *>(h->partial);
+        p.flags = static_cast<unsigned *>(h->flags);
+        p.epoch = h->epoch;
         e = dcn::launch_tc(p, map, s);
     } else {
         e = dcn::launch_simt(p, dtype, s);
@@ -202,6 +234,8 @@ dcn_status_t dcn_destroy(dcn_handle_t h) {
     dcn_status_t st = DCN_OK;
     if (cudaDeviceSynchronize() != cudaSuccess) st = DCN_ERR_CUDA;
     if (h->wpack) cudaFree(h->wpack);
+    if (h->partial) cudaFree(h->partial);
+    if (h->flags) cudaFree(h->flags);
     if (h->status) cudaFree(h->status);
     for (int i = 0; i < 6; ++i)
         if (h->stage[i]) cudaFree(h->stage[i]);

@@ -131,6 +131,11 @@ __device__ __forceinline__ void sts_v4_b32(uint32_t addr, uint32_t a, uint32_t b
                  :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
+// Barrier over `count` threads (a multiple of 32) of the CTA, id 1..15.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {

@@ -20,6 +20,12 @@ struct Params {
     unsigned *status;     // device status word (timeout bit)
     unsigned long long timeout_ns;  // bound of every barrier wait
     int sample_f32;       // tensor-core path: 1 = fp32 bilinear combine, 0 = bf16
+    // tensor-core path, stream-K scheduling (partial == nullptr: one tile per CTA)
+    float *partial;       // fp32 partial tiles, one [O/16][128][16] slot per CTA
+    unsigned *flags;      // one word per CTA: set to `epoch` once its partial is stored
+    unsigned epoch;       // this launch's flag value (never 0)
+    int sm_count;         // SMs of the device
+    int units_per_cta;    // set by the launcher
 };
 
 enum Dtype { kF32 = 0, kBF16 = 1 };

@@ -125,6 +125,11 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.status = s->status;
     p.timeout_ns = kWaitLimitNs;
     p.sample_f32 = 0;
+    p.partial = nullptr;   // no stream-K workspace: one tile per CTA
+    p.flags = nullptr;
+    p.epoch = 0;
+    p.sm_count = 0;
+    p.units_per_cta = 0;
 
     const bool tc = dtype == DCN_BF16 && dcn::tc_supported(C, O) && is_aligned(x, 32) &&
                     is_aligned(out, 16);

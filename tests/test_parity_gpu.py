@@ -78,6 +78,12 @@ TC_SHAPES = [
     Workload("tc_no_mask_bias", 1, 64, 40, 37, 64, 7, 7, 3, "bf16", 5.0, "none", 0.0, 0.0, 15),
     Workload("tc_rect_kernel", 1, 64, 12, 20, 64, 3, 5, 2, "bf16", 2.0, "sigmoid", 0.0, 0.1, 16),
     Workload("tc_o_112", 2, 64, 9, 30, 112, 3, 3, 1, "bf16", 2.0, "uniform_zero10", 0.0, 0.1, 17),
+    # more 8x16 tiles than a GB300 has SMs: the persistent stream-K schedule,
+    # with tiles split between CTAs (one and two channel blocks per tap, and
+    # a 5x5 kernel whose CTA runs start in the middle of a group of taps)
+    Workload("tc_streamk_3x3", 3, 64, 64, 128, 64, 3, 3, 1, "bf16", 2.0, "sigmoid", 0.0, 0.1, 18),
+    Workload("tc_streamk_c128", 2, 128, 64, 160, 32, 3, 3, 1, "bf16", 1.5, "sigmoid", 0.0, 0.1, 19),
+    Workload("tc_streamk_5x5", 1, 64, 96, 208, 32, 5, 5, 2, "bf16", 4.0, "uniform_zero10", 0.0, 0.1, 20),
 ]
 
 SIMT_SHAPES = [
