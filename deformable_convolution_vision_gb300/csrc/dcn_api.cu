@@ -94,7 +94,8 @@ dcn_status_t pack_impl(dcn_handle_t h, const void *weight, int O, int C, int kh,
     const size_t bytes = static_cast<size_t>(O) * C * kh * kw * esize(dtype);
     dcn_status_t st = ensure(&h->wpack, &h->wpack_cap, bytes, s);
     if (st != DCN_OK) return st;
-    if (dcn::launch_pack_weight(weight, h->wpack, O, C, kh, kw, dtype, s) != cudaSuccess)
+    const int perm = dcn::tc_pack_permuted(dtype, C, O) ? 1 : 0;
+    if (dcn::launch_pack_weight(weight, h->wpack, O, C, kh, kw, dtype, perm, s) != cudaSuccess)
         return DCN_ERR_CUDA;
     h->pk_O = O; h->pk_C = C; h->pk_kh = kh; h->pk_kw = kw; h->pk_dtype = dtype;
     return DCN_OK;
@@ -122,6 +123,7 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
     p.epoch = 0;
     p.sm_count = h->sm_count;
     p.units_per_cta = 0;
+    p.wperm = dcn::tc_pack_permuted(dtype, C, O) ? 1 : 0;   // as pack_impl packed it
 
     const bool tc_ok = dtype == DCN_BF16 && dcn::tc_supported(C, O) &&
                        aligned(x, 32) && aligned(out, 16) && aligned(h->wpack, 16);

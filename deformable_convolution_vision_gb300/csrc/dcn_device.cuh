@@ -131,6 +131,22 @@ __device__ __forceinline__ void sts_v4_b32(uint32_t addr, uint32_t a, uint32_t b
                  :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
+// Asynchronous 4-byte global -> shared copy; with valid == false nothing
+// is read and the destination is zero-filled.  The thread's copies are
+// complete after cp_async_wait_all.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+                 :: "r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Barrier over `count` threads (a multiple of 32) of the CTA, id 1..15.
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
@@ -211,6 +227,38 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.  A occupies TMEM
+// lanes 0..M-1 (row m in lane m) and K/2 columns from a_tmem, two bf16 per
+// 32-bit column, the even k in the low half.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Store 16 lanes x 32 columns from a warp (shape 16x256b, four repeats of
+// 8 columns).  Thread t writes, in repeat r, r[4r], r[4r+1] to lane
+// taddr.lane + t/4, columns 8r + 2(t%4) + {0, 1}, and r[4r+2], r[4r+3] to
+// lane taddr.lane + 8 + t/4, the same columns.
+__device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+           "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+           "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// This thread's earlier tcgen05.st have completed.
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Arrive once on the mbarrier when every tcgen05 operation this thread has

@@ -112,7 +112,8 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     // the status word keeps the previous call's value: start this call at zero
     if (cudaMemsetAsync(s->status, 0, sizeof(unsigned), cs) != cudaSuccess) return DCN_ERR_CUDA;
-    if (dcn::launch_pack_weight(weight, s->wpack, O, C, kh, kw, dtype, cs) != cudaSuccess)
+    const int perm = dcn::tc_pack_permuted(dtype, C, O) ? 1 : 0;
+    if (dcn::launch_pack_weight(weight, s->wpack, O, C, kh, kw, dtype, perm, cs) != cudaSuccess)
         return DCN_ERR_CUDA;
 
     dcn::Params p;
@@ -130,6 +131,7 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.epoch = 0;
     p.sm_count = 0;
     p.units_per_cta = 0;
+    p.wperm = perm;
 
     const bool tc = dtype == DCN_BF16 && dcn::tc_supported(C, O) && is_aligned(x, 32) &&
                     is_aligned(out, 16);

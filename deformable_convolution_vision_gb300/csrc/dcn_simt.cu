@@ -29,11 +29,13 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
-// S0: out[o][(i*kw + j)*C + c] = w[o][c][i][j].  One thread per packed
-// element, so the writes are coalesced; the weight is small (<= a few MB).
+// S0: out[o][(i*kw + j)*C + c] = w[o][c'][i][j] with c' = c, or with
+// c' = tc_channel_perm(c) for the tensor-core operand order.  One thread per
+// packed element, so the writes are coalesced; the weight is small (<= a
+// few MB).
 template <typename T>
 __global__ void pack_weight_kernel(const T *__restrict__ w, T *__restrict__ wp,
-                                   int O, int C, int kh, int kw) {
+                                   int O, int C, int kh, int kw, int perm) {
     const long long K = static_cast<long long>(kh) * kw * C;
     const long long n = K * O;
     for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < n;
@@ -41,7 +43,8 @@ __global__ void pack_weight_kernel(const T *__restrict__ w, T *__restrict__ wp,
         const int o = static_cast<int>(e / K);
         const int kk = static_cast<int>(e - static_cast<long long>(o) * K);
         const int tap = kk / C;
-        const int c = kk - tap * C;
+        const int cp = kk - tap * C;
+        const int c = perm ? tc_channel_perm(cp) : cp;
         const int i = tap / kw;
         const int j = tap - i * kw;
         wp[e] = w[((static_cast<long long>(o) * C + c) * kh + i) * kw + j];
@@ -139,8 +142,10 @@ dcn_simt_kernel(Params p) {
                 const int c = c0 + kk;
                 const int o = o0 + oo;
                 float v = 0.0f;
-                if (c < p.C && o < p.O)
-                    v = to_f32<T>(wp[static_cast<size_t>(o) * p.K + static_cast<size_t>(tap) * p.C + c]);
+                if (c < p.C && o < p.O) {
+                    const int cp = p.wperm ? tc_channel_perm(c) : c;   // packed position of c
+                    v = to_f32<T>(wp[static_cast<size_t>(o) * p.K + static_cast<size_t>(tap) * p.C + cp]);
+                }
                 Bs[kk][oo] = v;
             }
             __syncthreads();
@@ -179,18 +184,19 @@ dcn_simt_kernel(Params p) {
 }  // namespace
 
 cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int C, int kh, int kw,
-                               int dtype, cudaStream_t stream) {
+                               int dtype, int perm, cudaStream_t stream) {
+    if (perm && C % 64 != 0) return cudaErrorInvalidValue;
     const long long n = static_cast<long long>(O) * C * kh * kw;
     const int threads = 256;
     const long long want = (n + threads - 1) / threads;
     const int blocks = static_cast<int>(want < 4096 ? want : 4096);
     if (dtype == kF32) {
         pack_weight_kernel<float><<<blocks, threads, 0, stream>>>(
-            static_cast<const float *>(weight), static_cast<float *>(wpack), O, C, kh, kw);
+            static_cast<const float *>(weight), static_cast<float *>(wpack), O, C, kh, kw, perm);
     } else {
         pack_weight_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(weight), static_cast<__nv_bfloat16 *>(wpack),
-            O, C, kh, kw);
+            O, C, kh, kw, perm);
     }
     return cudaGetLastError();
 }

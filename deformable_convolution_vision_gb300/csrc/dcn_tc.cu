@@ -2,34 +2,46 @@
 // accumulation) for sm_103a.
 //
 // The contraction out[p, o] = sum_K A[p, K] * Wp[o, K] with K = (tap, c) is
-// a dense GEMM whose A operand is never materialised: the im2col column
-// buffer that page "deformops 3.0.1" (section "Deformable convolution")
-// avoids, and that the "birefnet-lite-1024-webgpu patch_deform.py" page
-// sizes at 392 MB for the 7x7, C = 64, 256 x 256 layer, exists here only as
-// one 128 x 64 tile per pipeline stage in shared memory.
+// a dense GEMM whose A operand is never materialised in memory: the im2col
+// column buffer that page "deformops 3.0.1" (section "Deformable
+// convolution") avoids, and that the "birefnet-lite-1024-webgpu
+// patch_deform.py" page sizes at 392 MB for the 7x7, C = 64, 256 x 256
+// layer, exists here only as one 128 x 64 tile per pipeline stage, in
+// tensor memory.
 //
-// One CTA computes a tile of 8 x 16 output pixels of one image (a compact
-// 2-D tile keeps each tap's sampled footprint small, so more corner reads
-// hit L1) x all O output channels:
+// A tile is 8 x 16 output pixels of one image (a compact 2-D tile keeps each
+// tap's sampled footprint small, so more corner reads hit L1) x all O
+// output channels.  One CTA per SM:
 //   warp 0      TMA producer: the packed-weight K-block [O x 64] of each
-//               stage, 128-byte swizzle; also allocates/frees TMEM.
+//               stage into shared memory, 128-byte swizzle; also
+//               allocates/frees TMEM.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=O,
-//               K=16) x 4 per K-block, accumulating in TMEM, and commits
-//               each stage back to its "empty" barrier.
-//   warps 2..17 samplers: per (pixel, tap) the corner weights and
-//               addresses (S1, S2), then for 8 channels per lane the four
-//               16-byte corner loads, the bilinear combine (by default in
+//               K=16, A from TMEM, B from shared memory) x 4 per K-block,
+//               accumulating in TMEM, and commits each stage back to its
+//               "empty" barrier.
+//   warps 2..17 samplers, two teams of eight that take alternate K-blocks.
+//               A sampler warp owns one tile row (16 pixels, TMEM lanes
+//               32q + 16h .. +15 of its lane quarter q).  Per (pixel, tap)
+//               it computes the corner weights and addresses (S1, S2); per
+//               K-block each lane gathers 16 channels of two pixels: eight
+//               32-byte corner loads, the bilinear combine (by default in
 //               the input dtype, bf16, as packed bf16x2 FMAs; optionally in
-//               fp32 with packed f32x2 FMAs), a bf16
-//               round and one 16-byte store into the swizzled A stage (S3).
-//               After the last K-block they run the epilogue (S5): TMEM ->
-//               registers, + bias in fp32, bf16 round, channels-last store.
+//               fp32 with packed f32x2 FMAs) and one 16x256b store of both
+//               pixels' rows into the stage's TMEM columns (S3).  After a
+//               tile's last K-block all sixteen run the epilogue (S5): TMEM
+//               -> registers, + bias in fp32, bf16 round, channels-last
+//               store.
 // K-blocks run tap-major with 64 channels each, so a tap's corner geometry
 // is computed once and reused for all of its channel blocks.  The geometry
-// is computed for two taps at a time by all 32 lanes of a sampler warp into
-// a ring of four per-warp tables, with its inputs fetched taps ahead.  Each
-// lane issues all sixteen corner loads of a stage before it waits for the
-// stage to be free.
+// of two taps at a time is computed by all 32 lanes of a warp into a ring
+// of four per-warp tables, with its inputs fetched a group ahead.  Each
+// lane issues the corner loads of its next K-block before it stores the
+// current one.
+//
+// With more tiles than SMs the launch is persistent and stream-K: every
+// CTA takes an equal run of (tile, K-block) units; a tile split between two
+// CTAs is finished by the first, which adds the second's fp32 partial.
+//
 // Every barrier wait is bounded; a wait that runs out sets the status word
 // and the kernel winds down without trapping.
 #include <cuda_bf16.h>
@@ -43,25 +55,35 @@ namespace dcn {
 namespace {
 
 constexpr int TC_BM = 128;               // output pixels per tile (MMA M)
-constexpr int TC_BK = 64;                // channels per K-block (128 bytes)
+constexpr int TC_BK = 64;                // channels per K-block
 constexpr int TC_MMA_K = 16;
 constexpr int TC_TILE_W = 16;                                 // tile = 8 x 16 output pixels
 constexpr int TC_TILE_H = TC_BM / TC_TILE_W;
-constexpr int TC_SAMPLER_WARPS = 16;
-constexpr int TC_ROWS_PER_WARP = TC_BM / TC_SAMPLER_WARPS;    // 8 pixels: half a tile row
-constexpr int TC_THREADS = 32 * (2 + TC_SAMPLER_WARPS);
-constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;                 // 16 KB
-constexpr int TC_TAP_GROUP = 32 / TC_ROWS_PER_WARP;           // taps tabulated together (one per 8 lanes)
-constexpr int TC_TABLE_BUFS = 2 * TC_TAP_GROUP;               // ring: one group in use, one ahead
-static_assert(TC_ROWS_PER_WARP * 2 == TC_TILE_W, "two sampler warps per tile row");
-static_assert((TC_TABLE_BUFS & (TC_TABLE_BUFS - 1)) == 0, "ring size is a power of two");
+// Sampler teams: a team of eight warps covers the 128 rows of a K-block;
+// with two teams each takes every other K-block (more warps to hide
+// latency, fewer registers per thread).
+#ifndef DCN_TC_TEAMS
+#define DCN_TC_TEAMS 2
+#endif
+constexpr int TC_TEAMS = DCN_TC_TEAMS;
+static_assert(TC_TEAMS == 1 || TC_TEAMS == 2, "one or two sampler teams");
+constexpr int TC_TEAM_WARPS = 8;
+constexpr int TC_SAMPLER_WARPS = TC_TEAM_WARPS * TC_TEAMS;
+constexpr int TC_EPI_PARTS = TC_SAMPLER_WARPS / 4;            // epilogue column parts per lane quarter
+constexpr int TC_CTRL_WARPS = 2;                              // TMA producer, MMA issuer
+constexpr int TC_THREADS = 32 * (TC_CTRL_WARPS + TC_SAMPLER_WARPS);
+constexpr int TC_A_COLS = TC_BK / 2;                          // TMEM columns of one A stage
+constexpr int TC_TAP_GROUP = 32 / TC_TILE_W;                  // taps tabulated together (one per 16 lanes)
+constexpr int TC_TABLE_SLOTS = 2 * TC_TAP_GROUP;              // ring: one group in use, one ahead
+static_assert(TC_TEAM_WARPS * TC_TILE_W == TC_BM, "a team covers the tile");
+static_assert(TC_TABLE_SLOTS == 4, "ring index arithmetic assumes four slots");
 
 // Per-warp corner table of one tap: arrays of 16-byte rows, one row per
-// pixel of the warp (conflict-free writes and broadcast reads).  The fp32
-// combine keeps the weights as duplicated fp32 pairs {w0,w0,w1,w1},
-// {w2,w2,w3,w3}; the bf16 combine as four bf16x2 pairs.  Then the four
-// corner indices.
-constexpr int TC_TABLE_ARRAY_BYTES = TC_ROWS_PER_WARP * 16;
+// pixel of the warp's tile row (conflict-free writes, broadcast reads).
+// The fp32 combine keeps the weights as duplicated fp32 pairs
+// {w0,w0,w1,w1}, {w2,w2,w3,w3}; the bf16 combine as four bf16x2 pairs.
+// Then the four corner indices.
+constexpr int TC_TABLE_ARRAY_BYTES = TC_TILE_W * 16;
 constexpr int TC_TABLE_W01 = 0;
 constexpr int TC_TABLE_W23 = TC_TABLE_ARRAY_BYTES;            // fp32 combine only
 __host__ __device__ constexpr int table_buf_bytes(bool f32) { return (f32 ? 3 : 2) * TC_TABLE_ARRAY_BYTES; }
@@ -69,10 +91,10 @@ __host__ __device__ constexpr int table_idx_off(bool f32) { return (f32 ? 2 : 1)
 
 struct TcLayout {
     int stages;
-    int b_bytes;       // O * 128
-    int stage_bytes;   // A + B
+    int b_bytes;       // O * 128: one weight K-block
     int bar_off;       // barriers after the stages
     int table_off;     // per-warp corner tables
+    int raw_off;       // per-warp raw geometry inputs (dy, dx, mask) [3][32] fp32
     int total;         // bytes used from the 1024-aligned base
 };
 
@@ -80,18 +102,22 @@ __host__ __device__ inline TcLayout tc_layout(int O, int stages, bool f32) {
     TcLayout L;
     L.stages = stages;
     L.b_bytes = O * TC_BK * 2;
-    L.stage_bytes = TC_A_BYTES + L.b_bytes;
-    L.bar_off = stages * L.stage_bytes;
+    L.bar_off = stages * L.b_bytes;
     // full[stages], empty[stages], accum_full, tmem slot (8 bytes each)
     L.table_off = L.bar_off + (2 * stages + 2) * 8;
     L.table_off = (L.table_off + 15) & ~15;
-    L.total = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_BUFS * table_buf_bytes(f32);
+    L.raw_off = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_SLOTS * table_buf_bytes(f32);
+    L.total = L.raw_off + TC_SAMPLER_WARPS * 3 * 32 * 4;
     return L;
 }
 
-__host__ __device__ inline int tmem_cols_for(int O) {
+// TMEM columns: the fp32 accumulator [128 x O] from column 0, then the A
+// stages, TC_A_COLS columns each.
+__host__ __device__ inline int tmem_acc_cols(int O) { return (O + 31) & ~31; }
+__host__ __device__ inline int tmem_cols_for(int O, int stages) {
+    const int need = tmem_acc_cols(O) + stages * TC_A_COLS;
     int n = 32;
-    while (n < O) n <<= 1;
+    while (n < need) n <<= 1;
     return n;
 }
 
@@ -140,7 +166,9 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     const uint32_t accum_bar = smem_u32(bars + 2 * stages);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 1);
 
-    const int warp = threadIdx.x / 32;
+    // the warp index, broadcast so that the compiler treats everything
+    // derived from it as warp-uniform (uniform registers)
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
     const int lane = threadIdx.x % 32;
     const int tiles_x = (p.Wo + TC_TILE_W - 1) / TC_TILE_W;
     const int tiles_y = (p.Ho + TC_TILE_H - 1) / TC_TILE_H;
@@ -150,11 +178,12 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     const int total = p.B * tiles_x * tiles_y * nkb;
     const int u_begin = blockIdx.x * p.units_per_cta;
     const int u_end = min(u_begin + p.units_per_cta, total);
-    const int tmem_cols = tmem_cols_for(p.O);
+    const int tmem_cols = tmem_cols_for(p.O, stages);
+    const uint32_t a_col0 = tmem_acc_cols(p.O);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
-            mbar_init(full0 + 8 * s, 1 + TC_SAMPLER_WARPS);
+            mbar_init(full0 + 8 * s, 1 + TC_TEAM_WARPS);
             mbar_init(empty0 + 8 * s, 1);
         }
         mbar_init(accum_bar, 1);
@@ -179,7 +208,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             int kb = u_begin % nkb;
             for (int u = u_begin; u < u_end; ++u) {
                 if (!mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns)) break;
-                const uint32_t b_dst = smem_u32(smem + s * L.stage_bytes + TC_A_BYTES);
+                const uint32_t b_dst = smem_u32(smem + s * L.b_bytes);
                 mbar_arrive_expect_tx(full0 + 8 * s, L.b_bytes);
                 tma_load_2d(b_dst, &wmap, full0 + 8 * s, kb * TC_BK, 0);
                 ++issued;
@@ -206,15 +235,14 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait_sleep(full0 + 8 * s, phase, p.status, p.timeout_ns)) { live = false; break; }
                     tc_fence_after_sync();
-                    const uint32_t a_addr = smem_u32(smem + s * L.stage_bytes);
-                    const uint32_t b_addr = a_addr + TC_A_BYTES;
-                    const uint64_t adesc = smem_desc_sw128(a_addr);
-                    const uint64_t bdesc = smem_desc_sw128(b_addr);
+                    const uint32_t a_tmem = tmem_base + a_col0 + s * TC_A_COLS;
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + s * L.b_bytes));
 #pragma unroll
                     for (int ks = 0; ks < TC_BK / TC_MMA_K; ++ks) {
-                        // advance the start address by 32 bytes per K=16 step; the
-                        // segment's first MMA overwrites the accumulator
-                        mma_bf16_ss(tmem_base, adesc + 2 * ks, bdesc + 2 * ks, idesc,
+                        // K=16 steps: 8 TMEM columns of A, 32 bytes of the
+                        // swizzled B rows; the segment's first MMA
+                        // overwrites the accumulator
+                        mma_bf16_ts(tmem_base, a_tmem + ks * (TC_MMA_K / 2), bdesc + 2 * ks, idesc,
                                     (kb > sg.kb0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(empty0 + 8 * s);
@@ -229,37 +257,37 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         }
     } else {
         // ------------------------------------------------ samplers
-        const int sw = warp - 2;                         // sampler warp 0..15
-        const int trow = sw >> 1;                        // its tile row
-        const int tcol0 = (sw & 1) * TC_ROWS_PER_WARP;   // its first tile column
-        const int row_base = trow * TC_TILE_W + tcol0;   // its first A row
+        const int sw = warp - TC_CTRL_WARPS;             // sampler warp 0 .. TC_SAMPLER_WARPS - 1
+        const int team = sw / TC_TEAM_WARPS;             // takes units u_begin + team + TC_TEAMS * i
+        const int q = warp & 3;                          // TMEM lane quarter this warp may access
+        const int half = (sw % TC_TEAM_WARPS) / 4;       // which 16 lanes of the quarter
+        const int trow = 2 * q + half;                   // its tile row = A rows 16 trow .. +15
         const __nv_bfloat16 *__restrict__ x = static_cast<const __nv_bfloat16 *>(p.x);
-        uint8_t *table = smem + L.table_off + sw * TC_TABLE_BUFS * kBuf;
+        uint8_t *table = smem + L.table_off + sw * TC_TABLE_SLOTS * kBuf;
         const uint32_t table_s = smem_u32(table);
-        const uint32_t stage0_s = smem_u32(smem);
+        const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * 3 * 32 * 4) + lane * 4;
+        const uint32_t a_lane = static_cast<uint32_t>(16 * trow) << 16;
         const int HoWo = p.Ho * p.Wo;
-        const int my_g = lane >> 3;     // geometry: tap offset within a group of four
-        const int my_px = lane & 7;     // geometry: pixel of the warp
+        const int my_g = lane >> 4;     // geometry: tap of the group
+        const int my_px = lane & 15;    // geometry: pixel (tile column)
         const int quart = lane & 3;     // gather: 16 channels of the 64-channel K-block
-        const int rsub = lane >> 2;     // gather: warp row 0..7
-        const int arow = row_base + rsub;
-        const uint32_t r_off = rsub * 16;
-        // the lane's two 16-byte chunks in an A stage (128-byte swizzle: chunk
-        // c of row r lives at chunk c ^ (r % 8))
-        const uint32_t sts0 = arow * 128 + (((2 * quart) ^ (arow & 7)) << 4);
-        const uint32_t sts1 = arow * 128 + (((2 * quart + 1) ^ (arow & 7)) << 4);
+        const int rsub = lane >> 2;     // gather: pixels rsub and rsub + 8 of the row
+        const uint32_t r_off0 = rsub * 16;
+        const uint32_t r_off1 = (rsub + 8) * 16;
+        // the sequence of taps a warp visits: every tap, or with two teams
+        // and one channel block per tap (alternate K-blocks = alternate
+        // taps) every other one
+        const int tap_shift = (TC_TEAMS == 2 && ncb == 1) ? 1 : 0;
         // epilogue: TMEM lane quarter, column part, A row of this thread
-        const int q = warp & 3;
-        const int part = sw >> 2;
+        const int part = sw >> 2;                        // 0 .. TC_EPI_PARTS - 1
         const int erow = q * 32 + lane;
         const int nch = p.O / 16;
-        const int ch_begin = part * nch / 4;
-        const int ch_end = (part + 1) * nch / 4;
+        const int ch_begin = part * nch / TC_EPI_PARTS;
+        const int ch_end = (part + 1) * nch / TC_EPI_PARTS;
         const size_t part_floats = static_cast<size_t>(nch) * TC_BM * 16;   // one partial tile
         bool ok = true;
-        int s = 0;
+        int s = team;                   // this warp's stages: team, team + TC_TEAMS, ...
         uint32_t phase = 0;
-        uint32_t a_stage = stage0_s;
         int segs = 0;
 
         Segment sg;
@@ -270,143 +298,188 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             const int trem = sg.tile - tb * tiles_x * tiles_y;
             const int th0 = (trem / tiles_x) * TC_TILE_H;
             const int tw0 = (trem % tiles_x) * TC_TILE_W;
-            const int my_h = th0 + trow;
-            const int my_w = tw0 + tcol0 + my_px;
-            const bool my_valid = (my_h < p.Ho) && (my_w < p.Wo);
-            const int my_hw = my_valid ? my_h * p.Wo + my_w : 0;
-            const int t0 = sg.kb0 / ncb;                 // first tap of the segment
-            const int g0 = t0 & ~(TC_TAP_GROUP - 1);     // its group of four taps
+            // this warp's K-blocks: every TC_TEAMS-th from the first of its team
+            const int seg_u0 = sg.tile * nkb + sg.kb0;
+            const int kb_first = sg.kb0 + (team - (seg_u0 - u_begin) % TC_TEAMS + TC_TEAMS) % TC_TEAMS;
 
-            // raw inputs (dy, dx, mask) of this lane's next tap, fetched a whole
-            // tap group ahead of their use so their latency hides behind gathers
-            float n_dy = 0.0f, n_dx = 0.0f, n_m = 0.0f;
-            auto load_raw = [&](int group_tap) {
-                const int tap = group_tap + my_g;
-                if (my_valid && tap < taps) {
-                    const float *o = p.offset + (static_cast<size_t>(tb) * 2 * taps + 2 * tap) * HoWo + my_hw;
-                    n_dy = __ldg(o);
-                    n_dx = __ldg(o + HoWo);
-                    n_m = p.mask ? __ldg(p.mask + (static_cast<size_t>(tb) * taps + tap) * HoWo + my_hw)
-                                 : 1.0f;
-                }
-            };
-            // kernel row and column (ti, tj) of this lane's tap, advanced by
-            // four taps per tabulation instead of divided out each time
-            int ti = (g0 + my_g) / p.kw;
-            int tj = (g0 + my_g) - ti * p.kw;
-            // corner tables of taps group_tap .. group_tap + 3 (ring slot tap % 8)
-            auto tabulate = [&](int group_tap) {
-                const int tap = group_tap + my_g;
-                TapCorners t;
-                if (my_valid && tap < taps) {
-                    tap_corners(n_dy, n_dx, n_m, my_h, my_w, ti, tj, p.pad, tb, p.H, p.W, p.C, t);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) { t.w[k] = 0.0f; t.idx[k] = 0; }
-                }
-                uint8_t *slot = table + (tap & (TC_TABLE_BUFS - 1)) * kBuf;
-                const int rowb = my_px * 16;
-                if constexpr (kSampleF32) {
-                    *reinterpret_cast<float4 *>(slot + TC_TABLE_W01 + rowb) = make_float4(t.w[0], t.w[0], t.w[1], t.w[1]);
-                    *reinterpret_cast<float4 *>(slot + TC_TABLE_W23 + rowb) = make_float4(t.w[2], t.w[2], t.w[3], t.w[3]);
-                } else {
-                    // the weights rounded to bf16, each duplicated into a bf16x2 pair
-                    *reinterpret_cast<uint4 *>(slot + TC_TABLE_W01 + rowb) =
-                        make_uint4(bf16x2_splat(t.w[0]), bf16x2_splat(t.w[1]), bf16x2_splat(t.w[2]),
-                                   bf16x2_splat(t.w[3]));
-                }
-                *reinterpret_cast<int4 *>(slot + kIdx + rowb) = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
-                tj += TC_TAP_GROUP;
-                while (tj >= p.kw) { tj -= p.kw; ++ti; }
-            };
-            // the four 32-byte corner loads of this lane's item from a table
-            // slot; corners outside the image read a clamped in-image address
-            // and carry weight 0
-            auto issue = [&](uint32_t slot, const __nv_bfloat16 *xc, u32x8 (&v)[4]) {
-                const int4 ci = lds_v4_s32(slot + kIdx + r_off);
-                v[0] = ldg_v8(xc + ci.x);
-                v[1] = ldg_v8(xc + ci.y);
-                v[2] = ldg_v8(xc + ci.z);
-                v[3] = ldg_v8(xc + ci.w);
-            };
+            if (kb_first < sg.kb1) {
+                const int my_h = th0 + trow;
+                const int my_w = tw0 + my_px;
+                const bool my_valid = (my_h < p.Ho) && (my_w < p.Wo);
+                const int my_hw = my_valid ? my_h * p.Wo + my_w : 0;
+                const int t_first = kb_first / ncb;
+                const int tap_par = tap_shift ? (t_first & 1) : 0;
+                // position of a tap in the warp's sequence, and back
+                auto seq_of = [&](int tap) { return tap >> tap_shift; };
+                auto tap_of = [&](int sq) { return (sq << tap_shift) + tap_par; };
+                const int sq0 = seq_of(t_first);
+                const int g0 = sq0 & ~(TC_TAP_GROUP - 1);    // its group of two
 
-            // Tables of the first two tap groups.  (The group after a group
-            // that starts inside the segment is tabulated when that group's
-            // first tap ends; a segment that starts mid-group never sees that
-            // tap end, so its second group is tabulated here.)  Slots of the
-            // previous segment are free: this warp finished reading them.
-            load_raw(g0);
-            tabulate(g0);
-            if (g0 + TC_TAP_GROUP < taps) load_raw(g0 + TC_TAP_GROUP);
-            if (t0 != g0 && g0 + TC_TAP_GROUP < taps) {
-                tabulate(g0 + TC_TAP_GROUP);
-                if (g0 + 2 * TC_TAP_GROUP < taps) load_raw(g0 + 2 * TC_TAP_GROUP);
-            }
-            __syncwarp();
-
-            // Rolling pipeline: the corner loads of K-block kb + 1 go out as
-            // K-block kb is combined, so each lane always has loads in flight.
-            u32x8 v[4];
-            int tap = t0, cb = sg.kb0 - t0 * ncb;
-            int n_tap = tap, n_cb = cb;
-            if (++n_cb == ncb) { n_cb = 0; ++n_tap; }
-            issue(table_s + (tap & (TC_TABLE_BUFS - 1)) * kBuf, x + cb * TC_BK + quart * 16, v);
-
-            for (int kb = sg.kb0; ok && kb < sg.kb1; ++kb) {
-                const bool has_next = kb + 1 < sg.kb1;
-                const uint32_t cur_slot = table_s + (tap & (TC_TABLE_BUFS - 1)) * kBuf;
-
-                // every lane waits; the warp leaves the loop together if any lane ran out
-                const bool got = mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns, 2000u);
-                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-
-                uint32_t packed[8];
-                if constexpr (kSampleF32) {
-                    uint64_t c0, c1, c2, c3;   // {w_q, w_q} fp32 pairs
-                    lds_v2_u64(cur_slot + TC_TABLE_W01 + r_off, c0, c1);
-                    lds_v2_u64(cur_slot + TC_TABLE_W23 + r_off, c2, c3);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        // channels 2k, 2k+1: w0*x00 + w1*x01 + w2*x10 + w3*x11 in fp32
-                        uint64_t acc = f2_mul(c0, f2_make(bf16_lo(v[0].w[k]), bf16_hi(v[0].w[k])));
-                        acc = f2_fma(c1, f2_make(bf16_lo(v[1].w[k]), bf16_hi(v[1].w[k])), acc);
-                        acc = f2_fma(c2, f2_make(bf16_lo(v[2].w[k]), bf16_hi(v[2].w[k])), acc);
-                        acc = f2_fma(c3, f2_make(bf16_lo(v[3].w[k]), bf16_hi(v[3].w[k])), acc);
-                        packed[k] = f2_to_bf16x2(acc);
+                // raw inputs (dy, dx, mask) of this lane's next tap, copied a
+                // whole group ahead of their use into the warp's raw slot
+                // (asynchronously: no registers held while in flight)
+                auto load_raw = [&](int group_sq) {
+                    const int tap = tap_of(group_sq + my_g);
+                    const bool valid = my_valid && tap < taps;
+                    const float *o = valid
+                        ? p.offset + (static_cast<size_t>(tb) * 2 * taps + 2 * tap) * HoWo + my_hw
+                        : p.offset;
+                    cp_async_4(raw_s, o, valid);
+                    cp_async_4(raw_s + 128, valid ? o + HoWo : o, valid);
+                    if (p.mask) {
+                        const float *mp = valid
+                            ? p.mask + (static_cast<size_t>(tb) * taps + tap) * HoWo + my_hw
+                            : p.mask;
+                        cp_async_4(raw_s + 256, mp, valid);
                     }
-                } else {
-                    // the same sum in the input dtype: bf16 weights, one bf16
-                    // rounding per fused multiply-add, two channels per op
-                    const int4 cw = lds_v4_s32(cur_slot + TC_TABLE_W01 + r_off);
+                };
+                // kernel row and column (ti, tj) of this lane's tap, advanced
+                // by a group per tabulation instead of divided out each time
+                const int step = TC_TAP_GROUP << tap_shift;
+                int ti = tap_of(g0 + my_g) / p.kw;
+                int tj = tap_of(g0 + my_g) - ti * p.kw;
+                // corner tables of the group's two taps (ring slot sq % 4)
+                auto tabulate = [&](int group_sq) {
+                    const int sq = group_sq + my_g;
+                    const int tap = tap_of(sq);
+                    TapCorners t;
+                    cp_async_wait_all();
+                    if (my_valid && tap < taps) {
+                        const float dy = lds_f32(raw_s);
+                        const float dx = lds_f32(raw_s + 128);
+                        const float m = p.mask ? lds_f32(raw_s + 256) : 1.0f;
+                        tap_corners(dy, dx, m, my_h, my_w, ti, tj, p.pad, tb, p.H, p.W, p.C, t);
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        uint32_t acc = bf16x2_mul(cw.x, v[0].w[k]);
-                        acc = bf16x2_fma(cw.y, v[1].w[k], acc);
-                        acc = bf16x2_fma(cw.z, v[2].w[k], acc);
-                        acc = bf16x2_fma(cw.w, v[3].w[k], acc);
-                        packed[k] = acc;
+                        for (int k = 0; k < 4; ++k) { t.w[k] = 0.0f; t.idx[k] = 0; }
                     }
+                    uint8_t *slot = table + (sq & (TC_TABLE_SLOTS - 1)) * kBuf;
+                    const int rowb = my_px * 16;
+                    if constexpr (kSampleF32) {
+                        *reinterpret_cast<float4 *>(slot + TC_TABLE_W01 + rowb) = make_float4(t.w[0], t.w[0], t.w[1], t.w[1]);
+                        *reinterpret_cast<float4 *>(slot + TC_TABLE_W23 + rowb) = make_float4(t.w[2], t.w[2], t.w[3], t.w[3]);
+                    } else {
+                        // the weights rounded to bf16, each duplicated into a bf16x2 pair
+                        *reinterpret_cast<uint4 *>(slot + TC_TABLE_W01 + rowb) =
+                            make_uint4(bf16x2_splat(t.w[0]), bf16x2_splat(t.w[1]), bf16x2_splat(t.w[2]),
+                                       bf16x2_splat(t.w[3]));
+                    }
+                    *reinterpret_cast<int4 *>(slot + kIdx + rowb) = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
+                    tj += step;
+                    while (tj >= p.kw) { tj -= p.kw; ++ti; }
+                };
+                // the four 32-byte corner loads of one of this lane's two pixels
+                // from a table slot; corners outside the image read a clamped
+                // in-image address and carry weight 0
+                auto issue_px = [&](int px, uint32_t slot, const __nv_bfloat16 *xc, u32x8 (&v)[8]) {
+                    const int4 ci = lds_v4_s32(slot + kIdx + (px ? r_off1 : r_off0));
+                    v[4 * px + 0] = ldg_v8(xc + ci.x);
+                    v[4 * px + 1] = ldg_v8(xc + ci.y);
+                    v[4 * px + 2] = ldg_v8(xc + ci.z);
+                    v[4 * px + 3] = ldg_v8(xc + ci.w);
+                };
+
+                // Tables of the first two groups.  (The group after a group
+                // whose first tap ends inside the segment is tabulated when
+                // that tap ends; a warp that starts on a group's second tap
+                // never sees the first end, so its next group is tabulated
+                // here.)  Slots of the previous segment are free: this warp
+                // finished reading them.
+                load_raw(g0);
+                tabulate(g0);
+                if (tap_of(g0 + TC_TAP_GROUP) < taps) load_raw(g0 + TC_TAP_GROUP);
+                if (sq0 != g0 && tap_of(g0 + TC_TAP_GROUP) < taps) {
+                    tabulate(g0 + TC_TAP_GROUP);
+                    if (tap_of(g0 + 2 * TC_TAP_GROUP) < taps) load_raw(g0 + 2 * TC_TAP_GROUP);
                 }
-                if (has_next)
-                    issue(table_s + (n_tap & (TC_TABLE_BUFS - 1)) * kBuf, x + n_cb * TC_BK + quart * 16, v);
-                sts_v4_b32(a_stage + sts0, packed[0], packed[1], packed[2], packed[3]);
-                sts_v4_b32(a_stage + sts1, packed[4], packed[5], packed[6], packed[7]);
-                fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full0 + 8 * s);
 
-                if (cb == ncb - 1 && (tap & (TC_TAP_GROUP - 1)) == 0 && tap + TC_TAP_GROUP < taps) {
-                    // the ring slots of taps tap - 4 .. tap - 1 are no longer read:
-                    // fill them for taps tap + 4 .. tap + 7 and fetch the group after
-                    tabulate(tap + TC_TAP_GROUP);
-                    if (tap + 2 * TC_TAP_GROUP < taps) load_raw(tap + 2 * TC_TAP_GROUP);
-                    __syncwarp();
+                // Rolling pipeline: the corner loads of a pixel's next K-block
+                // go out as soon as its current ones are combined.
+                u32x8 v[8];
+                int tap = t_first, cb = kb_first - t_first * ncb;
+                {
+                    const uint32_t slot = table_s + (seq_of(tap) & (TC_TABLE_SLOTS - 1)) * kBuf;
+                    issue_px(0, slot, x + cb * TC_BK + quart * 16, v);
+                    issue_px(1, slot, x + cb * TC_BK + quart * 16, v);
                 }
-                tap = n_tap;
-                cb = n_cb;
-                if (++n_cb == ncb) { n_cb = 0; ++n_tap; }
-                a_stage += L.stage_bytes;
-                if (++s == stages) { s = 0; phase ^= 1; a_stage = stage0_s; }
+
+                for (int kb = kb_first; ok && kb < sg.kb1; kb += TC_TEAMS) {
+                    const bool has_next = kb + TC_TEAMS < sg.kb1;
+                    int n_tap = tap, n_cb = cb + TC_TEAMS;
+                    while (n_cb >= ncb) { n_cb -= ncb; ++n_tap; }
+                    const int sq = seq_of(tap);
+                    const uint32_t cur_slot = table_s + (sq & (TC_TABLE_SLOTS - 1)) * kBuf;
+
+                    // every lane waits; the warp leaves the loop together if any lane ran out
+                    const bool got = mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns, 2000u);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    // TMEM writes after the MMAs that read this stage
+                    tc_fence_after_sync();
+
+                    // The stage row of both pixels, 16 words in the order of one
+                    // 16x256b.x4 store: w[4k], w[4k+1] are words 2k, 2k+1 (channels
+                    // 4k .. 4k+3 of the lane's 16) of the first pixel, w[4k+2],
+                    // w[4k+3] those of the second.
+                    uint32_t w[16];
+#pragma unroll
+                    for (int px = 0; px < 2; ++px) {
+                        const uint32_t ro = px ? r_off1 : r_off0;
+                        const u32x8 *vp = v + 4 * px;
+                        if constexpr (kSampleF32) {
+                            uint64_t c0, c1, c2, c3;   // {w_q, w_q} fp32 pairs
+                            lds_v2_u64(cur_slot + TC_TABLE_W01 + ro, c0, c1);
+                            lds_v2_u64(cur_slot + TC_TABLE_W23 + ro, c2, c3);
+#pragma unroll
+                            for (int m = 0; m < 8; ++m) {
+                                // channels 2m, 2m+1: w0*x00 + w1*x01 + w2*x10 + w3*x11 in fp32
+                                uint64_t acc = f2_mul(c0, f2_make(bf16_lo(vp[0].w[m]), bf16_hi(vp[0].w[m])));
+                                acc = f2_fma(c1, f2_make(bf16_lo(vp[1].w[m]), bf16_hi(vp[1].w[m])), acc);
+                                acc = f2_fma(c2, f2_make(bf16_lo(vp[2].w[m]), bf16_hi(vp[2].w[m])), acc);
+                                acc = f2_fma(c3, f2_make(bf16_lo(vp[3].w[m]), bf16_hi(vp[3].w[m])), acc);
+                                w[4 * (m >> 1) + 2 * px + (m & 1)] = f2_to_bf16x2(acc);
+                            }
+                        } else {
+                            // the same sum in the input dtype: bf16 weights, one bf16
+                            // rounding per fused multiply-add, two channels per op
+                            const int4 cw = lds_v4_s32(cur_slot + TC_TABLE_W01 + ro);
+#pragma unroll
+                            for (int m = 0; m < 8; ++m) {
+                                uint32_t acc = bf16x2_mul(cw.x, vp[0].w[m]);
+                                acc = bf16x2_fma(cw.y, vp[1].w[m], acc);
+                                acc = bf16x2_fma(cw.z, vp[2].w[m], acc);
+                                acc = bf16x2_fma(cw.w, vp[3].w[m], acc);
+                                w[4 * (m >> 1) + 2 * px + (m & 1)] = acc;
+                            }
+                        }
+                    }
+                    tmem_st_16x256b_x4(tmem_base + a_lane + a_col0 + s * TC_A_COLS, w);
+
+                    // The corner data is consumed.  If the first tap of a group
+                    // is done, the slots of the previous group are no longer
+                    // read: fill them with the next group and fetch the one
+                    // after.  The next K-block's tap is in the current group, so
+                    // its slot is untouched.  Then the next K-block's loads.
+                    if (has_next && n_tap != tap && (sq & (TC_TAP_GROUP - 1)) == 0 &&
+                        tap_of(sq + TC_TAP_GROUP) < taps) {
+                        tabulate(sq + TC_TAP_GROUP);
+                        if (tap_of(sq + 2 * TC_TAP_GROUP) < taps) load_raw(sq + 2 * TC_TAP_GROUP);
+                    }
+                    if (has_next) {
+                        const uint32_t n_slot = table_s + (seq_of(n_tap) & (TC_TABLE_SLOTS - 1)) * kBuf;
+                        issue_px(0, n_slot, x + n_cb * TC_BK + quart * 16, v);
+                        issue_px(1, n_slot, x + n_cb * TC_BK + quart * 16, v);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full0 + 8 * s);
+
+                    tap = n_tap;
+                    cb = n_cb;
+                    s += TC_TEAMS;
+                    if (s >= stages) { s -= stages; phase ^= 1; }
+                }
             }
 
             // ---- epilogue (S5) of the segment
@@ -418,13 +491,14 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             const int ow = tw0 + erow % TC_TILE_W;
             const bool pix_valid = oh < p.Ho && ow < p.Wo;
             const size_t pix = (static_cast<size_t>(tb) * p.Ho + oh) * p.Wo + ow;
+            const uint32_t acc_lane = static_cast<uint32_t>(q * 32) << 16;
             if (sg.kb0 > 0) {
                 // The tile's other K-blocks belong to the CTA before this one:
                 // leave the fp32 partial for it and raise this CTA's flag.
                 float *dst = p.partial + static_cast<size_t>(blockIdx.x) * part_floats;
                 for (int ch = ch_begin; ch < ch_end; ++ch) {
                     float vv[16];
-                    tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ch * 16, vv);
+                    tmem_ld16(tmem_base + acc_lane + ch * 16, vv);
                     float4 *d4 = reinterpret_cast<float4 *>(dst + (static_cast<size_t>(ch) * TC_BM + erow) * 16);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
@@ -451,7 +525,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 __nv_bfloat16 *__restrict__ out = static_cast<__nv_bfloat16 *>(p.out);
                 for (int ch = ch_begin; ch < ch_end; ++ch) {
                     float vv[16];
-                    tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ch * 16, vv);
+                    tmem_ld16(tmem_base + acc_lane + ch * 16, vv);
                     if (merge && ok) {
                         const float *sp = src + (static_cast<size_t>(ch) * TC_BM + erow) * 16;
 #pragma unroll
@@ -504,11 +578,15 @@ int carveout_percent(int needed) {
     return 100;
 }
 
-// Shared memory the CTA may use (stages + tables + alignment).  The SM's
-// L1/shared array is 256 KB; at 131 KB the 132 KB carveout leaves 124 KB of
-// L1 for the corner gathers.
+// Shared memory the CTA may use (weight stages + tables + alignment + the
+// 1 KB the system reserves).  The SM's L1/shared array is 256 KB; within
+// 100 KB the carveout leaves 156 KB of L1 for the corner gathers.  Wide
+// weights (large O) may take up to the second budget to keep four stages.
 #ifndef DCN_TC_SMEM_BUDGET
-#define DCN_TC_SMEM_BUDGET (131 * 1024)
+#define DCN_TC_SMEM_BUDGET (100 * 1024)
+#endif
+#ifndef DCN_TC_SMEM_WIDE_BUDGET
+#define DCN_TC_SMEM_WIDE_BUDGET (164 * 1024)
 #endif
 
 }  // namespace
@@ -523,9 +601,15 @@ cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t 
     // tile's corner footprint across taps.
     Params p = p_in;
     const bool f32 = p.sample_f32 != 0;
-    const int fixed = tc_layout(p.O, 0, f32).total + 1024;
-    int stages = (DCN_TC_SMEM_BUDGET - fixed) / tc_layout(p.O, 1, f32).stage_bytes;
-    stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+    // A multiple of TC_TEAMS stages (with two teams each owns every other
+    // one), as many as fit the budget and TMEM, at most 8.
+    auto smem_for = [&](int st) { return tc_layout(p.O, st, f32).total + 1024 + 1024; };
+    auto tmem_fits = [&](int st) { return tmem_acc_cols(p.O) + st * TC_A_COLS <= 512; };
+    int stages = 2;
+    for (int st = 8; st > 2; st -= TC_TEAMS) {
+        if (tmem_fits(st) && smem_for(st) <= DCN_TC_SMEM_BUDGET) { stages = st; break; }
+    }
+    if (stages < 4 && tmem_fits(4) && smem_for(4) <= DCN_TC_SMEM_WIDE_BUDGET) stages = 4;
     const TcLayout L = tc_layout(p.O, stages, f32);
     const int smem = L.total + 1024;  // slack for 1024-byte alignment
     auto kernel = f32 ? dcn_tc_kernel<true> : dcn_tc_kernel<false>;

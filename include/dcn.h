@@ -112,7 +112,10 @@ DCN_API dcn_status_t dcn_forward(dcn_handle_t h,
 
 /* The two halves of dcn_forward, for callers that reuse one weight.
  * dcn_pack_weight reorders weight [O,C,kh,kw] into the handle's workspace
- * as [O][(i*kw + j)*C + c] (tap-major, channel-minor).
+ * as [O][(i*kw + j)*C + c] (tap-major, channel-minor).  For bf16 shapes
+ * the tensor-core kernel accepts, the channels inside each 64-channel
+ * block are in that kernel's operand order instead; the workspace is
+ * private to the handle and either kernel reads it correctly.
  * dcn_forward_packed then runs the fused kernel with that packed weight;
  * it returns DCN_ERR_INVALID_ARG if (O, C, kh, kw, dtype) differ from the
  * last dcn_pack_weight on this handle.  Both are asynchronous on `stream`. */
