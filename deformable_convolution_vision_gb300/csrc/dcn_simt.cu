@@ -30,24 +30,23 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 
 // S0: out[o][(i*kw + j)*C + c] = w[o][c'][i][j] with c' = c, or with
-// c' = tc_channel_perm(c) for the tensor-core operand order.  One thread per
-// packed element, so the writes are coalesced; the weight is small (<= a
-// few MB).
+// c' = tc_channel_perm(c) for the tensor-core operand order.  One thread
+// per packed position of a row, looping over the rows o of its grid row, so
+// the writes are coalesced; the row arithmetic is 32-bit (K < 2^31 is
+// checked by the caller).  The weight is small: the copy costs a few
+// microseconds, mostly launch and DRAM latency.
 template <typename T>
 __global__ void pack_weight_kernel(const T *__restrict__ w, T *__restrict__ wp,
                                    int O, int C, int kh, int kw, int perm) {
-    const long long K = static_cast<long long>(kh) * kw * C;
-    const long long n = K * O;
-    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < n;
-         e += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int o = static_cast<int>(e / K);
-        const int kk = static_cast<int>(e - static_cast<long long>(o) * K);
-        const int tap = kk / C;
-        const int cp = kk - tap * C;
-        const int c = perm ? tc_channel_perm(cp) : cp;
-        const int i = tap / kw;
-        const int j = tap - i * kw;
-        wp[e] = w[((static_cast<long long>(o) * C + c) * kh + i) * kw + j];
+    const int K = kh * kw * C;
+    const int kk = blockIdx.x * blockDim.x + threadIdx.x;
+    if (kk >= K) return;
+    const int tap = kk / C;
+    const int cp = kk - tap * C;
+    const int c = perm ? tc_channel_perm(cp) : cp;
+    for (int o = blockIdx.y; o < O; o += gridDim.y) {
+        const size_t row = static_cast<size_t>(o) * K;
+        wp[row + kk] = w[row + static_cast<size_t>(c) * (kh * kw) + tap];
     }
 }
 
@@ -186,15 +185,14 @@ dcn_simt_kernel(Params p) {
 cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int C, int kh, int kw,
                                int dtype, int perm, cudaStream_t stream) {
     if (perm && C % 64 != 0) return cudaErrorInvalidValue;
-    const long long n = static_cast<long long>(O) * C * kh * kw;
+    const int K = kh * kw * C;
     const int threads = 256;
-    const long long want = (n + threads - 1) / threads;
-    const int blocks = static_cast<int>(want < 4096 ? want : 4096);
+    const dim3 grid((K + threads - 1) / threads, O < 65535 ? O : 65535);
     if (dtype == kF32) {
-        pack_weight_kernel<float><<<blocks, threads, 0, stream>>>(
+        pack_weight_kernel<float><<<grid, threads, 0, stream>>>(
             static_cast<const float *>(weight), static_cast<float *>(wpack), O, C, kh, kw, perm);
     } else {
-        pack_weight_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(
+        pack_weight_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(weight), static_cast<__nv_bfloat16 *>(wpack),
             O, C, kh, kw, perm);
     }

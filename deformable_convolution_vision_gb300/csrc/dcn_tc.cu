@@ -103,19 +103,24 @@ __host__ __device__ inline TcLayout tc_layout(int O, int stages, bool f32) {
     L.stages = stages;
     L.b_bytes = O * TC_BK * 2;
     L.bar_off = stages * L.b_bytes;
-    // full[stages], empty[stages], accum_full, tmem slot (8 bytes each)
-    L.table_off = L.bar_off + (2 * stages + 2) * 8;
+    // full[stages], empty[stages], acc_full[2], acc_free[2], tmem slot (8 bytes each)
+    L.table_off = L.bar_off + (2 * stages + 5) * 8;
     L.table_off = (L.table_off + 15) & ~15;
     L.raw_off = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_SLOTS * table_buf_bytes(f32);
     L.total = L.raw_off + TC_SAMPLER_WARPS * 3 * 32 * 4;
     return L;
 }
 
-// TMEM columns: the fp32 accumulator [128 x O] from column 0, then the A
-// stages, TC_A_COLS columns each.
+// TMEM columns: the fp32 accumulator [128 x O] from column 0, twice when
+// both copies and the A stages fit the 512 columns (a tile's epilogue then
+// overlaps the next tile's K-blocks), then the A stages, TC_A_COLS columns
+// each.
 __host__ __device__ inline int tmem_acc_cols(int O) { return (O + 31) & ~31; }
+__host__ __device__ inline int tmem_acc_bufs(int O, int stages) {
+    return 2 * tmem_acc_cols(O) + stages * TC_A_COLS <= 512 ? 2 : 1;
+}
 __host__ __device__ inline int tmem_cols_for(int O, int stages) {
-    const int need = tmem_acc_cols(O) + stages * TC_A_COLS;
+    const int need = tmem_acc_bufs(O, stages) * tmem_acc_cols(O) + stages * TC_A_COLS;
     int n = 32;
     while (n < need) n <<= 1;
     return n;
@@ -163,8 +168,11 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + stages);
-    const uint32_t accum_bar = smem_u32(bars + 2 * stages);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 1);
+    // acc_full[b]: the MMAs of a segment using accumulator b are complete;
+    // acc_free[b]: all sampler warps have read accumulator b out
+    const uint32_t acc_full0 = smem_u32(bars + 2 * stages);
+    const uint32_t acc_free0 = smem_u32(bars + 2 * stages + 2);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 4);
 
     // the warp index, broadcast so that the compiler treats everything
     // derived from it as warp-uniform (uniform registers)
@@ -179,14 +187,19 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     const int u_begin = blockIdx.x * p.units_per_cta;
     const int u_end = min(u_begin + p.units_per_cta, total);
     const int tmem_cols = tmem_cols_for(p.O, stages);
-    const uint32_t a_col0 = tmem_acc_cols(p.O);
+    const int acc_bufs = tmem_acc_bufs(p.O, stages);
+    const uint32_t acc_cols = tmem_acc_cols(p.O);
+    const uint32_t a_col0 = acc_bufs * acc_cols;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(full0 + 8 * s, 1 + TC_TEAM_WARPS);
             mbar_init(empty0 + 8 * s, 1);
         }
-        mbar_init(accum_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full0 + 8 * b, 1);
+            mbar_init(acc_free0 + 8 * b, TC_SAMPLER_WARPS);
+        }
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -232,6 +245,12 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             int u = u_begin;
             bool live = true;
             while (live && next_segment(u, u_end, nkb, sg)) {
+                // segment segs accumulates in buffer b, its use n of that buffer;
+                // use n >= 1 waits until the samplers have read use n - 1 out
+                const int b = segs % acc_bufs, n = segs / acc_bufs;
+                if (n > 0 && !mbar_wait_sleep(acc_free0 + 8 * b, (n - 1) & 1, p.status, p.timeout_ns)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * acc_cols;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait_sleep(full0 + 8 * s, phase, p.status, p.timeout_ns)) { live = false; break; }
                     tc_fence_after_sync();
@@ -242,18 +261,22 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                         // K=16 steps: 8 TMEM columns of A, 32 bytes of the
                         // swizzled B rows; the segment's first MMA
                         // overwrites the accumulator
-                        mma_bf16_ts(tmem_base, a_tmem + ks * (TC_MMA_K / 2), bdesc + 2 * ks, idesc,
+                        mma_bf16_ts(d_tmem, a_tmem + ks * (TC_MMA_K / 2), bdesc + 2 * ks, idesc,
                                     (kb > sg.kb0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(empty0 + 8 * s);
                     if (++s == stages) { s = 0; phase ^= 1; }
                 }
                 // the segment's accumulator is complete once its MMAs are
-                mma_commit(accum_bar);
+                mma_commit(acc_full0 + 8 * b);
                 ++segs;
             }
             // the MMAs must be complete before TMEM is released
-            if (segs > 0) mbar_wait_sleep(accum_bar, (segs - 1) & 1, p.status, p.timeout_ns);
+            if (segs > 0) {
+                const int last = segs - 1;
+                mbar_wait_sleep(acc_full0 + 8 * (last % acc_bufs), (last / acc_bufs) & 1, p.status,
+                                p.timeout_ns);
+            }
         }
     } else {
         // ------------------------------------------------ samplers
@@ -288,11 +311,96 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         bool ok = true;
         int s = team;                   // this warp's stages: team, team + TC_TEAMS, ...
         uint32_t phase = 0;
-        int segs = 0;
 
-        Segment sg;
+        // Epilogue (S5) of segment e, the idx-th of this CTA: wait for its
+        // accumulator, read it out, then tell the MMA warp it is free.
+        auto epilogue = [&](const Segment &e, int idx) {
+            const int etb = e.tile / (tiles_x * tiles_y);
+            const int erem = e.tile - etb * tiles_x * tiles_y;
+            const int eth0 = (erem / tiles_x) * TC_TILE_H;
+            const int etw0 = (erem % tiles_x) * TC_TILE_W;
+            const uint32_t b = idx % acc_bufs;
+            if (ok) ok = mbar_wait_sleep(acc_full0 + 8 * b, (idx / acc_bufs) & 1, p.status, p.timeout_ns);
+            __syncwarp();
+            tc_fence_after_sync();
+                const int oh = eth0 + erow / TC_TILE_W;
+                const int ow = etw0 + erow % TC_TILE_W;
+                const bool pix_valid = oh < p.Ho && ow < p.Wo;
+                const size_t pix = (static_cast<size_t>(etb) * p.Ho + oh) * p.Wo + ow;
+                const uint32_t acc_lane = (static_cast<uint32_t>(q * 32) << 16) + b * acc_cols;
+                if (e.kb0 > 0) {
+                    // The tile's other K-blocks belong to the CTA before this one:
+                    // leave the fp32 partial for it and raise this CTA's flag.
+                    float *dst = p.partial + static_cast<size_t>(blockIdx.x) * part_floats;
+                    for (int ch = ch_begin; ch < ch_end; ++ch) {
+                        float vv[16];
+                        tmem_ld16(tmem_base + acc_lane + ch * 16, vv);
+                        float4 *d4 = reinterpret_cast<float4 *>(dst + (static_cast<size_t>(ch) * TC_BM + erow) * 16);
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            d4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
+                    }
+                    __threadfence();
+                    named_barrier_sync(1, 32 * TC_SAMPLER_WARPS);
+                    if (sw == 0 && lane == 0) st_release_u32(p.flags + blockIdx.x, p.epoch);
+                } else {
+                    // The tile's last K-blocks may belong to the next CTA: wait
+                    // (bounded) for its partial and add it.
+                    const bool merge = e.kb1 < nkb;
+                    const float *src = p.partial + static_cast<size_t>(blockIdx.x + 1) * part_floats;
+                    if (merge && ok) {
+                        const uint64_t t0ns = global_timer_ns();
+                        while (ld_acquire_u32(p.flags + blockIdx.x + 1) != p.epoch) {
+                            if (global_timer_ns() - t0ns > p.timeout_ns) {
+                                atomicOr(p.status, kStatusTimeout);
+                                ok = false;
+                                break;
+                            }
+                        }
+                    }
+                    __nv_bfloat16 *__restrict__ out = static_cast<__nv_bfloat16 *>(p.out);
+                    for (int ch = ch_begin; ch < ch_end; ++ch) {
+                        float vv[16];
+                        tmem_ld16(tmem_base + acc_lane + ch * 16, vv);
+                        if (merge && ok) {
+                            const float *sp = src + (static_cast<size_t>(ch) * TC_BM + erow) * 16;
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 a = ld_cg_f4(sp + 4 * e);
+                                vv[4 * e] += a.x; vv[4 * e + 1] += a.y; vv[4 * e + 2] += a.z; vv[4 * e + 3] += a.w;
+                            }
+                        }
+                        if (ok && pix_valid) {
+                            uint32_t pk[8];
+    #pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int o = ch * 16 + 2 * e;
+                                const float b0 = p.bias ? __ldg(p.bias + o) : 0.0f;
+                                const float b1 = p.bias ? __ldg(p.bias + o + 1) : 0.0f;
+                                pk[e] = pack_bf16x2(vv[2 * e] + b0, vv[2 * e + 1] + b1);
+                            }
+                            uint4 *dst = reinterpret_cast<uint4 *>(out + pix * p.O + ch * 16);
+                            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                        }
+                    }
+                }
+            // this warp's TMEM reads are complete: accumulator b is free
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_free0 + 8 * b);
+        };
+
+        // One pass per segment, plus one to finish: the pass for segment i
+        // samples it and then runs the epilogue of segment i (one
+        // accumulator) or of segment i - 1 (two: the MMA drain and the
+        // read-out then overlap with sampling).
+        const bool deferred = acc_bufs == 2;
+        Segment sg, prev;
         int u = u_begin;
-        while (next_segment(u, u_end, nkb, sg)) {
+        for (int seg_idx = 0;; ++seg_idx) {
+          const bool got = next_segment(u, u_end, nkb, sg);
+          if (got) {
             // ---- this segment's tile
             const int tb = sg.tile / (tiles_x * tiles_y);
             const int trem = sg.tile - tb * tiles_x * tiles_y;
@@ -407,7 +515,9 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 for (int kb = kb_first; ok && kb < sg.kb1; kb += TC_TEAMS) {
                     const bool has_next = kb + TC_TEAMS < sg.kb1;
                     int n_tap = tap, n_cb = cb + TC_TEAMS;
-                    while (n_cb >= ncb) { n_cb -= ncb; ++n_tap; }
+                    // (at most TC_TEAMS carries: cb < ncb)
+                    if (n_cb >= ncb) { n_cb -= ncb; ++n_tap; }
+                    if (TC_TEAMS == 2 && n_cb >= ncb) { n_cb -= ncb; ++n_tap; }
                     const int sq = seq_of(tap);
                     const uint32_t cur_slot = table_s + (sq & (TC_TABLE_SLOTS - 1)) * kBuf;
 
@@ -482,76 +592,11 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 }
             }
 
-            // ---- epilogue (S5) of the segment
-            if (ok) ok = mbar_wait_sleep(accum_bar, segs & 1, p.status, p.timeout_ns);
-            ++segs;
-            __syncwarp();
-            tc_fence_after_sync();
-            const int oh = th0 + erow / TC_TILE_W;
-            const int ow = tw0 + erow % TC_TILE_W;
-            const bool pix_valid = oh < p.Ho && ow < p.Wo;
-            const size_t pix = (static_cast<size_t>(tb) * p.Ho + oh) * p.Wo + ow;
-            const uint32_t acc_lane = static_cast<uint32_t>(q * 32) << 16;
-            if (sg.kb0 > 0) {
-                // The tile's other K-blocks belong to the CTA before this one:
-                // leave the fp32 partial for it and raise this CTA's flag.
-                float *dst = p.partial + static_cast<size_t>(blockIdx.x) * part_floats;
-                for (int ch = ch_begin; ch < ch_end; ++ch) {
-                    float vv[16];
-                    tmem_ld16(tmem_base + acc_lane + ch * 16, vv);
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + (static_cast<size_t>(ch) * TC_BM + erow) * 16);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        d4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
-                }
-                __threadfence();
-                named_barrier_sync(1, 32 * TC_SAMPLER_WARPS);
-                if (sw == 0 && lane == 0) st_release_u32(p.flags + blockIdx.x, p.epoch);
-            } else {
-                // The tile's last K-blocks may belong to the next CTA: wait
-                // (bounded) for its partial and add it.
-                const bool merge = sg.kb1 < nkb;
-                const float *src = p.partial + static_cast<size_t>(blockIdx.x + 1) * part_floats;
-                if (merge && ok) {
-                    const uint64_t t0ns = global_timer_ns();
-                    while (ld_acquire_u32(p.flags + blockIdx.x + 1) != p.epoch) {
-                        if (global_timer_ns() - t0ns > p.timeout_ns) {
-                            atomicOr(p.status, kStatusTimeout);
-                            ok = false;
-                            break;
-                        }
-                    }
-                }
-                __nv_bfloat16 *__restrict__ out = static_cast<__nv_bfloat16 *>(p.out);
-                for (int ch = ch_begin; ch < ch_end; ++ch) {
-                    float vv[16];
-                    tmem_ld16(tmem_base + acc_lane + ch * 16, vv);
-                    if (merge && ok) {
-                        const float *sp = src + (static_cast<size_t>(ch) * TC_BM + erow) * 16;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 a = ld_cg_f4(sp + 4 * e);
-                            vv[4 * e] += a.x; vv[4 * e + 1] += a.y; vv[4 * e + 2] += a.z; vv[4 * e + 3] += a.w;
-                        }
-                    }
-                    if (ok && pix_valid) {
-                        uint32_t pk[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int o = ch * 16 + 2 * e;
-                            const float b0 = p.bias ? __ldg(p.bias + o) : 0.0f;
-                            const float b1 = p.bias ? __ldg(p.bias + o + 1) : 0.0f;
-                            pk[e] = pack_bf16x2(vv[2 * e] + b0, vv[2 * e + 1] + b1);
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(out + pix * p.O + ch * 16);
-                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                    }
-                }
-            }
-            // TMEM reads of this segment finish before the next one's stages
-            // are handed to the MMA warp
-            tc_fence_before_sync();
+          }
+          if (deferred ? seg_idx > 0 : got)
+              epilogue(deferred ? prev : sg, deferred ? seg_idx - 1 : seg_idx);
+          if (!got) break;
+          prev = sg;
         }
     }
 

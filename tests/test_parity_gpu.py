@@ -84,6 +84,15 @@ TC_SHAPES = [
     Workload("tc_streamk_3x3", 3, 64, 64, 128, 64, 3, 3, 1, "bf16", 2.0, "sigmoid", 0.0, 0.1, 18),
     Workload("tc_streamk_c128", 2, 128, 64, 160, 32, 3, 3, 1, "bf16", 1.5, "sigmoid", 0.0, 0.1, 19),
     Workload("tc_streamk_5x5", 1, 64, 96, 208, 32, 5, 5, 2, "bf16", 4.0, "uniform_zero10", 0.0, 0.1, 20),
+    # one K-block per tile (1x1, C = 64) on the persistent schedule: every
+    # segment is one K-block, so one sampler team has nothing to sample in it
+    # and the accumulator's reuse rests on the "read out" barrier alone; with
+    # O = 64 two accumulators alternate, with O = 256 one is reused
+    Workload("tc_streamk_1x1", 2, 64, 64, 160, 64, 1, 1, 0, "bf16", 1.0, "sigmoid", 0.0, 0.1, 21),
+    Workload("tc_streamk_1x1_o256", 2, 64, 64, 160, 256, 1, 1, 0, "bf16", 1.0, "sigmoid", 0.0, 0.1, 22),
+    # 160 tiles x 9 K-blocks in runs of 10: the run of the ninth CTA starts on
+    # a tile's last K-block (a one-K-block tail segment)
+    Workload("tc_streamk_tail1", 2, 64, 64, 160, 64, 3, 3, 1, "bf16", 2.0, "uniform", 0.0, 0.1, 23),
 ]
 
 SIMT_SHAPES = [
@@ -92,6 +101,9 @@ SIMT_SHAPES = [
     Workload("simt_no_mask", 1, 33, 6, 5, 8, 2, 2, 0, "f32", 1.0, "none", 0.0, 0.0, 23),
     Workload("simt_bf16_odd", 2, 24, 10, 9, 40, 3, 3, 1, "bf16", 2.0, "sigmoid", 0.0, 0.1, 24),
     Workload("simt_pad_big", 1, 8, 4, 5, 9, 3, 3, 3, "f32", 1.0, "sigmoid", 0.0, 0.1, 25),
+    # a long packed weight row (7 * 7 * 272 fp32 = 53 KB), C not a multiple
+    # of the 16-channel step
+    Workload("simt_long_row", 1, 272, 7, 6, 8, 7, 7, 3, "f32", 1.5, "sigmoid", 0.0, 0.1, 26),
 ]
 
 
