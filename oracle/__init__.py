@@ -16,7 +16,10 @@ fp32 for the fp32 offsets).
 
 All arrays cross this boundary in logical NCHW order:
 x [B,C,H,W] fp32, offset [B,2k,Ho,Wo] fp32, mask [B,k,Ho,Wo] fp32 or None,
-weight [O,C,kh,kw] fp32, bias [O] fp32 or None; results are fp64.
+weight [O,C,kh,kw] fp32, bias [O] fp32 or None; results are fp64.  The
+general form (``forward_ex``) adds stride, per-axis padding, dilation,
+weight groups and offset groups (``ConvDesc``): offset
+[B,2*G*k,Ho,Wo], mask [B,G*k,Ho,Wo], weight [O,C/groups,kh,kw].
 """
 
 import ctypes
@@ -60,6 +63,10 @@ class Oracle:
         lib.oracle_dcn_forward.restype = i
         lib.oracle_dcn_forward_points.argtypes = [f, f, f, f, f, f, i, f] + [i] * 9
         lib.oracle_dcn_forward_points.restype = i
+        lib.oracle_dcn_forward_ex.argtypes = [f, f, f, f, f, f, f, i]
+        lib.oracle_dcn_forward_ex.restype = i
+        lib.oracle_dcn_forward_points_ex.argtypes = [f, f, f, f, f, f, i, f, f, i]
+        lib.oracle_dcn_forward_points_ex.restype = i
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i
         self._lib = lib
@@ -120,6 +127,78 @@ class Oracle:
         return out
 
 
+    # ---------------------------------------------------------- general form
+
+    def _prepare_ex(self, x, offset, mask, weight, bias, conv):
+        """conv: ConvDesc (or a dict with its fields)."""
+        c = conv if isinstance(conv, ConvDesc) else ConvDesc(**conv)
+        x, offset, mask, weight, bias = (self._f32(t) for t in (x, offset, mask, weight, bias))
+        B, C, H, W = x.shape
+        O, Cg, kh, kw = weight.shape
+        if c.groups <= 0 or C % c.groups or O % c.groups or Cg != C // c.groups:
+            raise ValueError("weight shape does not match x and groups")
+        if c.offset_groups <= 0 or C % c.offset_groups:
+            raise ValueError("offset_groups must divide C")
+        Ho, Wo = c.out_size(H, W, kh, kw)
+        if Ho <= 0 or Wo <= 0:
+            raise ValueError("empty output")
+        k, G = kh * kw, c.offset_groups
+        if offset.shape != (B, 2 * G * k, Ho, Wo):
+            raise ValueError(f"offset shape {offset.shape} != {(B, 2 * G * k, Ho, Wo)}")
+        if mask is not None and mask.shape != (B, G * k, Ho, Wo):
+            raise ValueError(f"mask shape {mask.shape} != {(B, G * k, Ho, Wo)}")
+        if bias is not None and bias.shape != (O,):
+            raise ValueError("bias must have shape [O]")
+        desc = np.array([B, C, H, W, O, kh, kw, c.stride[0], c.stride[1], c.padding[0],
+                         c.padding[1], c.dilation[0], c.dilation[1], c.groups, G], dtype=np.int32)
+        return (x, offset, mask, weight, bias), desc, (B, O, Ho, Wo)
+
+    def forward_ex(self, x, offset, mask, weight, bias, conv, nthreads=0):
+        """Whole output [B, O, Ho, Wo] in fp64 of the general problem."""
+        arrs, desc, (B, O, Ho, Wo) = self._prepare_ex(x, offset, mask, weight, bias, conv)
+        out = np.empty((B, O, Ho, Wo), dtype=np.float64)
+        rc = self._lib.oracle_dcn_forward_ex(*(self._ptr(a) for a in arrs), self._ptr(out),
+                                             self._ptr(desc), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_dcn_forward_ex rejected its arguments")
+        return out
+
+    def forward_points_ex(self, x, offset, mask, weight, bias, conv, points, nthreads=0):
+        """Selected pixels (b, h, w) of the general problem: [n, O] fp64."""
+        arrs, desc, (B, O, Ho, Wo) = self._prepare_ex(x, offset, mask, weight, bias, conv)
+        pts = np.ascontiguousarray(points, dtype=np.int32).reshape(-1, 3)
+        n = pts.shape[0]
+        out = np.empty((n, O), dtype=np.float64)
+        rc = self._lib.oracle_dcn_forward_points_ex(*(self._ptr(a) for a in arrs),
+                                                    self._ptr(pts), n, self._ptr(out),
+                                                    self._ptr(desc), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_dcn_forward_points_ex rejected its arguments")
+        return out
+
+
+class ConvDesc:
+    """Convolution parameters of the general problem: stride, padding and
+    dilation as (h, w) pairs (an int means both), weight groups and offset
+    (deformable) groups."""
+
+    def __init__(self, stride=1, padding=0, dilation=1, groups=1, offset_groups=1):
+        pair = lambda v: (int(v), int(v)) if np.isscalar(v) else (int(v[0]), int(v[1]))  # noqa: E731
+        self.stride, self.padding, self.dilation = pair(stride), pair(padding), pair(dilation)
+        self.groups, self.offset_groups = int(groups), int(offset_groups)
+
+    def out_size(self, H, W, kh, kw):
+        def one(n, k, s, p, d):
+            span = n + 2 * p - d * (k - 1) - 1
+            return span // s + 1 if span >= 0 else 0
+        return (one(H, kh, self.stride[0], self.padding[0], self.dilation[0]),
+                one(W, kw, self.stride[1], self.padding[1], self.dilation[1]))
+
+    def __repr__(self):
+        return (f"ConvDesc(stride={self.stride}, padding={self.padding}, dilation={self.dilation}, "
+                f"groups={self.groups}, offset_groups={self.offset_groups})")
+
+
 _default = None
 
 
@@ -137,3 +216,11 @@ def forward(*args, **kwargs):
 
 def forward_points(*args, **kwargs):
     return get().forward_points(*args, **kwargs)
+
+
+def forward_ex(*args, **kwargs):
+    return get().forward_ex(*args, **kwargs)
+
+
+def forward_points_ex(*args, **kwargs):
+    return get().forward_points_ex(*args, **kwargs)

@@ -15,7 +15,12 @@ raises AssertionError when the oracle disagrees with an independent fact:
   resample per tap, then the tap/channel contraction with einsum;
 * samples pushed out of the image: exactly the bias;
 * the mask: linearity, and mask 0 gives exactly the bias;
-* an affine input map: bilinear interpolation reproduces it exactly.
+* an affine input map: bilinear interpolation reproduces it exactly;
+* with stride, per-axis padding, dilation, weight groups and offset groups:
+  zero offsets against the library convolution with those parameters,
+  integer offsets against sliced shifted copies per offset group, fractional
+  offsets against the library resampler per offset group, and identical
+  offsets in every offset group against the one-group result.
 
 The rule being pinned is the one on the page "litert-community/Idol ...
 deform_conv.py" (module docstring and four-corner loop) and the page
@@ -283,5 +288,172 @@ def pin_affine_map(orc):
         assert float(diff.max()) <= 1e-12, f"affine map channel {c}: {float(diff.max()):.3e}"
 
 
+# ------------------------------------------------------------------ general
+# Stride, per-axis padding, dilation, weight groups and offset groups: the
+# convolution reading of torchvision deform_conv2d's parameters, which the
+# "deformops 3.0.1" page (section "Deformable convolution") names as the
+# operator, with a (C_out, C_in / groups, kH, kW) weight.
+
+GEN_SHAPES = [
+    dict(B=2, C=4, H=9, W=11, O=6, kh=3, kw=3, stride=(2, 1), padding=(1, 2), dilation=(1, 2),
+         groups=2, offset_groups=2),
+    dict(B=1, C=6, H=10, W=8, O=3, kh=3, kw=2, stride=(1, 3), padding=(2, 0), dilation=(2, 1),
+         groups=3, offset_groups=3),
+    dict(B=1, C=4, H=12, W=12, O=4, kh=3, kw=3, stride=2, padding=1, dilation=2,
+         groups=1, offset_groups=4),
+    # offset groups that straddle weight groups (C/groups = 3, C/offset_groups = 2)
+    dict(B=1, C=6, H=7, W=9, O=4, kh=2, kw=3, stride=1, padding=(0, 1), dilation=1,
+         groups=2, offset_groups=3),
+    dict(B=2, C=2, H=5, W=6, O=2, kh=1, kw=1, stride=2, padding=0, dilation=3,
+         groups=1, offset_groups=2),
+]
+
+
+def _conv_desc(s):
+    import oracle
+    return oracle.ConvDesc(stride=s["stride"], padding=s["padding"], dilation=s["dilation"],
+                           groups=s["groups"], offset_groups=s["offset_groups"])
+
+
+def _pair(v):
+    return (v, v) if isinstance(v, int) else tuple(v)
+
+
+def _rand_problem_ex(seed, s, off_std, mask=True, bias=True):
+    g = torch.Generator().manual_seed(seed)
+    B, C, H, W, O, kh, kw = (s[k] for k in ("B", "C", "H", "W", "O", "kh", "kw"))
+    Ho, Wo = _conv_desc(s).out_size(H, W, kh, kw)
+    k, G = kh * kw, s["offset_groups"]
+    x = torch.randn(B, C, H, W, generator=g)
+    off = torch.randn(B, 2 * G * k, Ho, Wo, generator=g) * off_std
+    m = torch.rand(B, G * k, Ho, Wo, generator=g) * 2 if mask else None
+    w = torch.randn(O, C // s["groups"], kh, kw, generator=g) * 0.3
+    b = torch.randn(O, generator=g) if bias else None
+    return x, off, m, w, b
+
+
+def _dense_tap_weight(w, groups, C, i, j):
+    """[O, C] weight of tap (i, j) with zeros outside each output's group."""
+    O, Cg = w.shape[0], w.shape[1]
+    Og = O // groups
+    Wd = torch.zeros(O, C, dtype=torch.float64)
+    for o in range(O):
+        g = o // Og
+        Wd[o, g * Cg:(g + 1) * Cg] = w[o, :, i, j].double()
+    return Wd
+
+
+def pin_general_direct_conv(orc):
+    """Zero offsets with mask 1 (or no mask) equal a library convolution with
+    the same stride, padding, dilation and groups."""
+    for n, s in enumerate(GEN_SHAPES):
+        x, off, m, w, b = _rand_problem_ex(110 + n, s, off_std=0.0)
+        off.zero_()
+        ref = F.conv2d(x.double(), w.double(), b.double(), stride=_pair(s["stride"]),
+                       padding=_pair(s["padding"]), dilation=_pair(s["dilation"]),
+                       groups=s["groups"])
+        for mask in (None, torch.ones_like(m)):
+            got = orc.forward_ex(x, off, mask, w, b, _conv_desc(s))
+            assert got.shape == tuple(ref.shape), f"{s}: shape {got.shape} != {tuple(ref.shape)}"
+            err = _rel_err(got, ref.numpy())
+            assert err <= 1e-13, f"general direct conv {s} mask={mask is not None}: {err:.3e}"
+
+
+def _strided_samples(x, s, i, j, dy, dx, Ho, Wo):
+    """x at (h*sh - ph + i*dh + dy, w*sw - pw + j*dw + dx) for integer dy,
+    dx, zero outside: padding and strided slicing."""
+    sh, sw = _pair(s["stride"])
+    ph, pw = _pair(s["padding"])
+    dh, dw = _pair(s["dilation"])
+    P = 40
+    xp = F.pad(x.double(), (P, P, P, P))
+    y0 = -ph + i * dh + dy + P
+    x0 = -pw + j * dw + dx + P
+    return xp[:, :, y0:y0 + sh * (Ho - 1) + 1:sh, x0:x0 + sw * (Wo - 1) + 1:sw]
+
+
+def pin_general_shifted_conv(orc):
+    """Integer offsets, one shift per (offset group, tap), equal a sum over
+    groups and taps of library-sliced shifted copies of x, contracted with
+    each group's weight."""
+    for n, s in enumerate(GEN_SHAPES):
+        x, off, m, w, b = _rand_problem_ex(120 + n, s, off_std=0.0)
+        B, C, H, W = x.shape
+        kh, kw, G = s["kh"], s["kw"], s["offset_groups"]
+        k_all, Cq = kh * kw, C // G
+        Ho, Wo = off.shape[2], off.shape[3]
+        gen = torch.Generator().manual_seed(1200 + n)
+        shifts = torch.randint(-3, 4, (G, k_all, 2), generator=gen)
+        for q in range(G):
+            for k in range(k_all):
+                off[:, 2 * (q * k_all + k)] = float(shifts[q, k, 0])
+                off[:, 2 * (q * k_all + k) + 1] = float(shifts[q, k, 1])
+        ref = b.double().view(1, -1, 1, 1).expand(B, -1, Ho, Wo).clone()
+        for q in range(G):
+            cs = slice(q * Cq, (q + 1) * Cq)
+            for i in range(kh):
+                for j in range(kw):
+                    k = i * kw + j
+                    samp = _strided_samples(x, s, i, j, int(shifts[q, k, 0]), int(shifts[q, k, 1]), Ho, Wo)
+                    Wd = _dense_tap_weight(w, s["groups"], C, i, j)
+                    ref += torch.einsum("oc,bchw->bohw", Wd[:, cs], samp[:, cs]) * \
+                        m[:, q * k_all + k:q * k_all + k + 1].double()
+        got = orc.forward_ex(x, off, m, w, b, _conv_desc(s))
+        err = _rel_err(got, ref.numpy())
+        assert err <= 1e-13, f"general shifted conv {s}: {err:.3e}"
+
+
+def pin_general_grid_sample(orc):
+    """Fractional offsets per offset group equal the library bilinear
+    resampler on that group's channels, then the grouped contraction."""
+    for n, s in enumerate(GEN_SHAPES):
+        x, off, m, w, b = _rand_problem_ex(130 + n, s, off_std=2.5)
+        B, C, H, W = x.shape
+        kh, kw, G = s["kh"], s["kw"], s["offset_groups"]
+        k_all, Cq = kh * kw, C // G
+        sh, sw = _pair(s["stride"])
+        ph, pw = _pair(s["padding"])
+        dh, dw = _pair(s["dilation"])
+        Ho, Wo = off.shape[2], off.shape[3]
+        hh = torch.arange(Ho, dtype=torch.float32).view(1, Ho, 1)
+        ww = torch.arange(Wo, dtype=torch.float32).view(1, 1, Wo)
+        ref = b.double().view(1, -1, 1, 1).expand(B, -1, Ho, Wo).clone()
+        for q in range(G):
+            cs = slice(q * Cq, (q + 1) * Cq)
+            for i in range(kh):
+                for j in range(kw):
+                    k = q * k_all + i * kw + j
+                    # fp32 coordinates, as the oracle forms them
+                    py = (hh * sh + float(i * dh - ph)) + off[:, 2 * k]
+                    px = (ww * sw + float(j * dw - pw)) + off[:, 2 * k + 1]
+                    grid = torch.stack([px.double() * (2.0 / (W - 1)) - 1.0,
+                                        py.double() * (2.0 / (H - 1)) - 1.0], dim=-1)
+                    samp = F.grid_sample(x[:, cs].double(), grid, mode="bilinear",
+                                         padding_mode="zeros", align_corners=True)
+                    Wd = _dense_tap_weight(w, s["groups"], C, i, j)
+                    ref += torch.einsum("oc,bchw->bohw", Wd[:, cs], samp) * m[:, k:k + 1].double()
+        got = orc.forward_ex(x, off, m, w, b, _conv_desc(s))
+        err = _rel_err(got, ref.numpy())
+        assert err <= 1e-10, f"general grid_sample {s}: {err:.3e}"
+
+
+def pin_offset_groups_collapse(orc):
+    """Offset groups that all carry the same offsets and mask give exactly
+    the one-group result."""
+    for n, s in enumerate(GEN_SHAPES):
+        if s["offset_groups"] == 1:
+            continue
+        x, off, m, w, b = _rand_problem_ex(140 + n, s, off_std=2.0)
+        G, k_all = s["offset_groups"], s["kh"] * s["kw"]
+        off1, m1 = off[:, :2 * k_all].clone(), m[:, :k_all].clone()
+        offG, mG = off1.repeat(1, G, 1, 1), m1.repeat(1, G, 1, 1)
+        s1 = dict(s, offset_groups=1)
+        got = orc.forward_ex(x, offG, mG, w, b, _conv_desc(s))
+        one = orc.forward_ex(x, off1, m1, w, b, _conv_desc(s1))
+        assert np.array_equal(got, one), f"offset groups collapse {s}"
+
+
 ALL_PINS = [pin_direct_conv, pin_shifted_conv, pin_integer_gather, pin_bilinear_golden,
-            pin_grid_sample, pin_outside_is_bias, pin_mask, pin_affine_map]
+            pin_grid_sample, pin_outside_is_bias, pin_mask, pin_affine_map,
+            pin_general_direct_conv, pin_general_shifted_conv, pin_general_grid_sample,
+            pin_offset_groups_collapse]

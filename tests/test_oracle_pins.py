@@ -40,3 +40,35 @@ def test_rejects_bad_shapes(orc):
         orc.forward(x, off[:, :4], m, w, b, 1)
     with pytest.raises(ValueError):
         orc.forward_points(x, off, m, w, b, 1, np.array([[0, 5, 0]]))
+
+
+def test_general_points_match_full(orc):
+    s = pins.GEN_SHAPES[0]
+    x, off, m, w, b = pins._rand_problem_ex(83, s, off_std=2.0)
+    desc = pins._conv_desc(s)
+    full = orc.forward_ex(x, off, m, w, b, desc)
+    B, O, Ho, Wo = full.shape
+    pts = np.array([[0, 0, 0], [1, Ho - 1, Wo - 1], [0, Ho // 2, 1], [1, 0, Wo - 1]])
+    got = orc.forward_points_ex(x, off, m, w, b, desc, pts)
+    for t, (bb, h, ww) in enumerate(pts):
+        assert np.array_equal(got[t], full[bb, :, h, ww])
+
+
+def test_general_form_reduces_to_page_form(orc):
+    """Stride 1, dilation 1, one group and one offset group: the general
+    entry point gives the page-1 entry point's bits."""
+    x, off, m, w, b = pins._rand_problem(84, B=2, C=3, H=8, W=7, O=4, kh=3, kw=5, pad=2, off_std=2.0)
+    page = orc.forward(x, off, m, w, b, 2)
+    general = orc.forward_ex(x, off, m, w, b, oracle.ConvDesc(padding=2))
+    assert np.array_equal(page, general)
+
+
+def test_general_rejects_bad_shapes(orc):
+    s = pins.GEN_SHAPES[0]
+    x, off, m, w, b = pins._rand_problem_ex(85, s, off_std=1.0)
+    desc = pins._conv_desc(s)
+    with pytest.raises(ValueError):          # offsets of one offset group only
+        orc.forward_ex(x, off[:, :off.shape[1] // 2], m, w, b, desc)
+    with pytest.raises(ValueError):          # groups that do not divide C
+        orc.forward_ex(x, off, m, w, b, oracle.ConvDesc(stride=2, padding=(1, 2), dilation=(1, 2),
+                                                        groups=3, offset_groups=2))
