@@ -1,17 +1,18 @@
 """GB300 (sm_103a) modulated deformable convolution, forward pass.
 
-torchvision ``deform_conv2d`` semantics with stride 1, dilation 1, one
-offset group and one weight group, computed by hand-written CUDA kernels
-behind the C ABI declared in ``include/dcn.h``.  This package is the thin
+torchvision ``deform_conv2d`` semantics -- stride, per-axis padding,
+dilation, weight groups and offset groups -- computed by hand-written CUDA
+kernels behind the C ABI declared in ``include/dcn.h``.  This package is the thin
 Python side: ``binding`` maps the C entry points one to one, and
 ``deform_conv2d`` below shapes PyTorch tensors into one call.
 """
 
 from . import binding
 from .binding import (DCN_BF16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
-                      DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, DcnError, dcn_create, dcn_destroy,
-                      dcn_forward, dcn_forward_host, dcn_forward_packed, dcn_last_path,
-                      dcn_pack_weight, dcn_selftest_timeout, dcn_set_path,
+                      DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, ConvDesc, DcnError, dcn_create,
+                      dcn_destroy, dcn_forward, dcn_forward_ex, dcn_forward_host,
+                      dcn_forward_packed, dcn_forward_packed_ex, dcn_last_path, dcn_out_size,
+                      dcn_pack_weight, dcn_pack_weight_ex, dcn_selftest_timeout, dcn_set_path,
                       dcn_set_sample_precision, dcn_status_string, dcn_sync_status)
 
 __all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF16",
@@ -19,7 +20,8 @@ __all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF1
            "DCN_SAMPLE_F32", "dcn_set_sample_precision", "dcn_create", "dcn_destroy",
            "dcn_forward", "dcn_forward_host", "dcn_forward_packed", "dcn_pack_weight",
            "dcn_set_path", "dcn_last_path", "dcn_sync_status", "dcn_selftest_timeout",
-           "dcn_status_string"]
+           "dcn_status_string", "ConvDesc", "dcn_forward_ex", "dcn_pack_weight_ex",
+           "dcn_forward_packed_ex", "dcn_out_size"]
 
 
 class Handle:
@@ -59,15 +61,32 @@ def _dtype_code(t):
     raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
 
 
-def deform_conv2d(x, offset, weight, bias=None, padding=0, mask=None, handle=None, out=None,
-                  stream=None):
-    """Modulated deformable convolution forward on CUDA tensors.
+def _pair(v, name):
+    if isinstance(v, int):
+        return (v, v)
+    v = tuple(int(t) for t in v)
+    if len(v) != 2:
+        raise ValueError(f"{name} must be an int or a pair")
+    return v
+
+
+def _out_size(n, k, s, p, d):
+    span = n + 2 * p - d * (k - 1) - 1
+    return span // s + 1 if span >= 0 else 0
+
+
+def deform_conv2d(x, offset, weight, bias=None, stride=1, padding=0, dilation=1, mask=None,
+                  handle=None, out=None, stream=None):
+    """Modulated deformable convolution forward on CUDA tensors, with
+    torchvision ``deform_conv2d``'s argument order.
 
     x       [B, C, H, W] float32/bfloat16, channels_last memory format
-    offset  [B, 2*kh*kw, Ho, Wo] float32, contiguous (dy, dx per tap)
-    weight  [O, C, kh, kw] same dtype as x, contiguous
+    offset  [B, 2*G*kh*kw, Ho, Wo] float32, contiguous ((dy, dx) per tap,
+            offset group after offset group); G = offset groups
+    weight  [O, C/groups, kh, kw] same dtype as x, contiguous; groups = C / its dim 1
     bias    [O] float32 or None
-    mask    [B, kh*kw, Ho, Wo] float32 or None
+    mask    [B, G*kh*kw, Ho, Wo] float32 or None
+    stride, padding, dilation: int or (h, w)
     Returns out [B, O, Ho, Wo] in x's dtype, channels_last memory format.
     Layouts are checked, never converted.
     """
@@ -85,23 +104,29 @@ def deform_conv2d(x, offset, weight, bias=None, padding=0, mask=None, handle=Non
     if weight.dtype != x.dtype:
         raise TypeError("weight must have x's dtype")
     B, C, H, W = x.shape
-    O, C2, kh, kw = weight.shape
-    if C2 != C:
-        raise ValueError("weight and x disagree on C")
-    pad = int(padding)
-    Ho, Wo = H + 2 * pad - kh + 1, W + 2 * pad - kw + 1
-    if tuple(offset.shape) != (B, 2 * kh * kw, Ho, Wo):
-        raise ValueError(f"offset must be {(B, 2 * kh * kw, Ho, Wo)}")
-    if mask is not None and tuple(mask.shape) != (B, kh * kw, Ho, Wo):
-        raise ValueError(f"mask must be {(B, kh * kw, Ho, Wo)}")
+    O, Cg, kh, kw = weight.shape
+    if Cg <= 0 or C % Cg != 0 or O % (C // Cg) != 0:
+        raise ValueError("weight's channel count must divide C, and the group count O")
+    groups = C // Cg
+    (sh, sw), (ph, pw), (dh, dw) = _pair(stride, "stride"), _pair(padding, "padding"), \
+        _pair(dilation, "dilation")
+    Ho, Wo = _out_size(H, kh, sh, ph, dh), _out_size(W, kw, sw, pw, dw)
+    k = kh * kw
+    if offset.dim() != 4 or offset.shape[1] % (2 * k) != 0:
+        raise ValueError("offset must be [B, 2*G*kh*kw, Ho, Wo]")
+    G = offset.shape[1] // (2 * k)
+    if G <= 0 or C % G != 0 or tuple(offset.shape) != (B, 2 * G * k, Ho, Wo):
+        raise ValueError(f"offset must be {(B, 2 * G * k, Ho, Wo)} with G dividing C")
+    if mask is not None and tuple(mask.shape) != (B, G * k, Ho, Wo):
+        raise ValueError(f"mask must be {(B, G * k, Ho, Wo)}")
     if out is None:
         out = torch.empty((B, O, Ho, Wo), dtype=x.dtype, device=x.device,
                           memory_format=torch.channels_last)
+    desc = ConvDesc(B, C, H, W, O, kh, kw, sh, sw, ph, pw, dh, dw, groups, G)
     own = handle is None
     h = Handle() if own else handle
     try:
-        dcn_forward(h.h, x, offset, mask, weight, bias, out, B, C, H, W, O, kh, kw, pad,
-                    _dtype_code(x), stream)
+        dcn_forward_ex(h.h, x, offset, mask, weight, bias, out, desc, _dtype_code(x), stream)
         if own:
             st = dcn_sync_status(h.h, stream)
             if st != 0:

@@ -22,7 +22,16 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_forward_packed",
            "dcn_forward_host", "dcn_set_path", "dcn_last_path", "dcn_sync_status",
            "dcn_selftest_timeout", "dcn_status_string", "dcn_forward_noalloc",
-           "dcn_set_sample_precision"]
+           "dcn_set_sample_precision", "dcn_out_size", "dcn_forward_ex", "dcn_pack_weight_ex",
+           "dcn_forward_packed_ex"]
+
+
+class ConvDesc(ctypes.Structure):
+    """``dcn_conv_desc_t``: the general problem (stride, per-axis padding,
+    dilation, weight groups, offset groups)."""
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "B", "C", "H", "W", "O", "kh", "kw", "stride_h", "stride_w", "pad_h", "pad_w",
+        "dil_h", "dil_w", "groups", "offset_groups")]
 
 
 class DcnError(RuntimeError):
@@ -58,6 +67,10 @@ def load():
         "dcn_selftest_timeout": ([P, LL, P], I),
         "dcn_status_string": ([I], ctypes.c_char_p),
         "dcn_forward_noalloc": ([P, P, P, P, P, P] + [I] * 9 + [P], I),
+        "dcn_out_size": ([I] * 5, I),
+        "dcn_forward_ex": ([P, P, P, P, P, P, P, ctypes.POINTER(ConvDesc), I, P], I),
+        "dcn_pack_weight_ex": ([P, P, ctypes.POINTER(ConvDesc), I, P], I),
+        "dcn_forward_packed_ex": ([P, P, P, P, P, P, ctypes.POINTER(ConvDesc), I, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -159,3 +172,24 @@ def dcn_forward_noalloc(x, offset, mask, weight, bias, out, B, C, H, W, O, kh, k
                                       _ptr(out), B, C, H, W, O, kh, kw, pad, dtype,
                                       _stream(stream)),
            "dcn_forward_noalloc")
+
+
+def dcn_out_size(n, k, stride, pad, dil):
+    return load().dcn_out_size(n, k, stride, pad, dil)
+
+
+def dcn_forward_ex(h, x, offset, mask, weight, bias, out, desc, dtype, stream=None):
+    _check(load().dcn_forward_ex(h, _ptr(x), _ptr(offset), _ptr(mask), _ptr(weight), _ptr(bias),
+                                 _ptr(out), ctypes.byref(desc), dtype, _stream(stream)),
+           "dcn_forward_ex")
+
+
+def dcn_pack_weight_ex(h, weight, desc, dtype, stream=None):
+    _check(load().dcn_pack_weight_ex(h, _ptr(weight), ctypes.byref(desc), dtype, _stream(stream)),
+           "dcn_pack_weight_ex")
+
+
+def dcn_forward_packed_ex(h, x, offset, mask, bias, out, desc, dtype, stream=None):
+    _check(load().dcn_forward_packed_ex(h, _ptr(x), _ptr(offset), _ptr(mask), _ptr(bias),
+                                        _ptr(out), ctypes.byref(desc), dtype, _stream(stream)),
+           "dcn_forward_packed_ex")

@@ -5,6 +5,7 @@
 // status code instead of throwing.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -21,10 +22,10 @@ struct dcn_handle_s {
     int last_path = -1;
     int sample = DCN_SAMPLE_INPUT_DTYPE;
 
-    // packed weight [O][kh*kw*C]
+    // packed weight [O][kh*kw*(C/groups)]; the key of the last pack
     void *wpack = nullptr;
     size_t wpack_cap = 0;
-    int pk_O = 0, pk_C = 0, pk_kh = 0, pk_kw = 0, pk_dtype = -1;
+    int pk_O = 0, pk_Cg = 0, pk_kh = 0, pk_kw = 0, pk_dtype = -1, pk_perm = 0;
 
     unsigned *status = nullptr;  // device status word
 
@@ -56,20 +57,65 @@ inline bool aligned(const void *p, size_t a) {
 
 inline size_t esize(int dtype) { return dtype == DCN_F32 ? 4 : 2; }
 
-dcn_status_t check_dims(int B, int C, int H, int W, int O, int kh, int kw, int pad, int dtype) {
+// A validated problem: the descriptor and its output size.
+struct Conv {
+    dcn_conv_desc_t d;
+    int Ho, Wo;
+    int taps() const { return d.kh * d.kw; }
+    int Cg() const { return d.C / d.groups; }
+    int Og() const { return d.O / d.groups; }
+    int Cq() const { return d.C / d.offset_groups; }
+};
+
+long long out_size_ll(long long n, long long k, long long stride, long long pad, long long dil) {
+    const long long span = n + 2 * pad - dil * (k - 1) - 1;
+    return span < 0 ? 0 : span / stride + 1;
+}
+
+dcn_status_t make_conv(const dcn_conv_desc_t &d, int dtype, Conv *c) {
     if (dtype != DCN_F32 && dtype != DCN_BF16) return DCN_ERR_INVALID_ARG;
-    if (B <= 0 || C <= 0 || H <= 0 || W <= 0 || O <= 0 || kh <= 0 || kw <= 0 || pad < 0)
+    if (d.B <= 0 || d.C <= 0 || d.H <= 0 || d.W <= 0 || d.O <= 0 || d.kh <= 0 || d.kw <= 0)
         return DCN_ERR_INVALID_ARG;
-    const long long Ho = static_cast<long long>(H) + 2ll * pad - kh + 1;
-    const long long Wo = static_cast<long long>(W) + 2ll * pad - kw + 1;
-    if (Ho <= 0 || Wo <= 0) return DCN_ERR_INVALID_ARG;
-    const long long taps = static_cast<long long>(kh) * kw;
+    if (d.stride_h <= 0 || d.stride_w <= 0 || d.dil_h <= 0 || d.dil_w <= 0 || d.pad_h < 0 || d.pad_w < 0)
+        return DCN_ERR_INVALID_ARG;
+    if (d.groups <= 0 || d.C % d.groups || d.O % d.groups) return DCN_ERR_INVALID_ARG;
+    if (d.offset_groups <= 0 || d.C % d.offset_groups) return DCN_ERR_INVALID_ARG;
+    const long long Ho = out_size_ll(d.H, d.kh, d.stride_h, d.pad_h, d.dil_h);
+    const long long Wo = out_size_ll(d.W, d.kw, d.stride_w, d.pad_w, d.dil_w);
+    if (Ho <= 0 || Wo <= 0 || Ho > kIndexLimit || Wo > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    const long long taps = static_cast<long long>(d.kh) * d.kw;
     if (taps > kIndexLimit) return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(B) * H * W * C > kIndexLimit) return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(B) * 2 * taps * Ho * Wo > kIndexLimit) return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(B) * Ho * Wo * O > kIndexLimit) return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(O) * C * taps > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(d.B) * d.H * d.W * d.C > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(d.B) * 2 * d.offset_groups * taps * Ho * Wo > kIndexLimit)
+        return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(d.B) * Ho * Wo * d.O > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(d.O) * (d.C / d.groups) * taps > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    c->d = d;
+    c->Ho = static_cast<int>(Ho);
+    c->Wo = static_cast<int>(Wo);
     return DCN_OK;
+}
+
+// The page form: stride 1, dilation 1, one padding, one group.
+dcn_conv_desc_t page_desc(int B, int C, int H, int W, int O, int kh, int kw, int pad) {
+    dcn_conv_desc_t d;
+    d.B = B; d.C = C; d.H = H; d.W = W; d.O = O; d.kh = kh; d.kw = kw;
+    d.stride_h = d.stride_w = 1;
+    d.pad_h = d.pad_w = pad;
+    d.dil_h = d.dil_w = 1;
+    d.groups = d.offset_groups = 1;
+    return d;
+}
+
+// Whether the tensor-core kernel runs this problem (one launch per weight
+// group and per 256 output channels; offset groups as virtual taps).
+bool tc_general_ok(const Conv &c) {
+    const int Cg = c.Cg(), Cq = c.Cq(), Og = c.Og();
+    if (Cg % 64 != 0 || Cq % 64 != 0 || Og % 16 != 0) return false;
+    if (Cg % Cq != 0 && Cq % Cg != 0) return false;
+    const int og_count = Cq >= Cg ? 1 : Cg / Cq;
+    if (static_cast<long long>(c.taps()) * og_count > dcn::tc_max_virtual_taps) return false;
+    return dcn::tc_supported(Cg, Og < 256 ? Og : 256);
 }
 
 // Grow a device buffer in stream order.
@@ -89,32 +135,57 @@ dcn_status_t ensure(void **buf, size_t *cap, size_t bytes, cudaStream_t s) {
     return DCN_OK;
 }
 
-dcn_status_t pack_impl(dcn_handle_t h, const void *weight, int O, int C, int kh, int kw,
-                       int dtype, cudaStream_t s) {
-    const size_t bytes = static_cast<size_t>(O) * C * kh * kw * esize(dtype);
+dcn_status_t pack_impl(dcn_handle_t h, const void *weight, const Conv &c, int dtype,
+                       cudaStream_t s) {
+    const int O = c.d.O, Cg = c.Cg(), kh = c.d.kh, kw = c.d.kw;
+    const size_t bytes = static_cast<size_t>(O) * Cg * kh * kw * esize(dtype);
     dcn_status_t st = ensure(&h->wpack, &h->wpack_cap, bytes, s);
     if (st != DCN_OK) return st;
-    const int perm = dcn::tc_pack_permuted(dtype, C, O) ? 1 : 0;
-    if (dcn::launch_pack_weight(weight, h->wpack, O, C, kh, kw, dtype, perm, s) != cudaSuccess)
+    const int perm = dcn::tc_pack_permuted(dtype, Cg) ? 1 : 0;
+    if (dcn::launch_pack_weight(weight, h->wpack, O, Cg, kh, kw, dtype, perm, s) != cudaSuccess)
         return DCN_ERR_CUDA;
-    h->pk_O = O; h->pk_C = C; h->pk_kh = kh; h->pk_kw = kw; h->pk_dtype = dtype;
+    h->pk_O = O; h->pk_Cg = Cg; h->pk_kh = kh; h->pk_kw = kw; h->pk_dtype = dtype;
+    h->pk_perm = perm;
+    return DCN_OK;
+}
+
+// The next flag value of the stream-K workspace (0 is never used).
+dcn_status_t next_epoch(dcn_handle_t h, cudaStream_t s, unsigned *epoch) {
+    if (++h->epoch == 0) {
+        // flag values wrapped: clear the flags and start again at 1
+        if (cudaMemsetAsync(h->flags, 0, h->flags_cap, s) != cudaSuccess) return DCN_ERR_CUDA;
+        h->epoch = 1;
+    }
+    *epoch = h->epoch;
     return DCN_OK;
 }
 
 dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *offset,
-                                 const float *mask, const float *bias, void *out,
-                                 int B, int C, int H, int W, int O, int kh, int kw, int pad,
+                                 const float *mask, const float *bias, void *out, const Conv &c,
                                  int dtype, cudaStream_t s) {
-    if (h->pk_O != O || h->pk_C != C || h->pk_kh != kh || h->pk_kw != kw || h->pk_dtype != dtype)
+    const dcn_conv_desc_t &d = c.d;
+    if (h->pk_O != d.O || h->pk_Cg != c.Cg() || h->pk_kh != d.kh || h->pk_kw != d.kw ||
+        h->pk_dtype != dtype)
         return DCN_ERR_INVALID_ARG;
+    const int taps = c.taps();
 
+    // the whole problem (the CUDA-core kernel's view)
     dcn::Params p;
     p.x = x; p.offset = offset; p.mask = mask; p.wpack = h->wpack; p.bias = bias; p.out = out;
-    p.B = B; p.C = C; p.H = H; p.W = W; p.O = O; p.kh = kh; p.kw = kw; p.pad = pad;
-    p.Ho = H + 2 * pad - kh + 1;
-    p.Wo = W + 2 * pad - kw + 1;
-    p.P = B * p.Ho * p.Wo;
-    p.K = kh * kw * C;
+    p.B = d.B; p.C = d.C; p.H = d.H; p.W = d.W; p.O = d.O; p.kh = d.kh; p.kw = d.kw;
+    p.sh = d.stride_h; p.sw = d.stride_w; p.ph = d.pad_h; p.pw = d.pad_w;
+    p.dh = d.dil_h; p.dw = d.dil_w;
+    p.groups = d.groups;
+    p.ogroups = d.offset_groups;
+    p.Ho = c.Ho;
+    p.Wo = c.Wo;
+    p.P = d.B * c.Ho * c.Wo;
+    p.K = taps * c.Cg();
+    p.x_cstride = d.C;
+    p.out_stride = d.O;
+    p.og_count = d.offset_groups;
+    p.off_bstride = 2 * taps * d.offset_groups;
+    p.mask_bstride = taps * d.offset_groups;
     p.status = h->status;
     p.timeout_ns = kWaitLimitNs;
     p.sample_f32 = h->sample == DCN_SAMPLE_F32 ? 1 : 0;
@@ -123,51 +194,75 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
     p.epoch = 0;
     p.sm_count = h->sm_count;
     p.units_per_cta = 0;
-    p.wperm = dcn::tc_pack_permuted(dtype, C, O) ? 1 : 0;   // as pack_impl packed it
+    p.wperm = h->pk_perm;
 
-    const bool tc_ok = dtype == DCN_BF16 && dcn::tc_supported(C, O) &&
+    const bool tc_ok = dtype == DCN_BF16 && tc_general_ok(c) && h->pk_perm &&
                        aligned(x, 32) && aligned(out, 16) && aligned(h->wpack, 16);
     int path = h->path;
     if (path == DCN_PATH_AUTO) path = tc_ok ? DCN_PATH_TC : DCN_PATH_SIMT;
     if (path == DCN_PATH_TC && !tc_ok) return DCN_ERR_UNSUPPORTED;
 
-    cudaError_t e;
-    if (path == DCN_PATH_TC) {
-        CUtensorMap map;
-        std::memset(&map, 0, sizeof(map));
-        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(O)};
-        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p.K) * 2};
-        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(O)};
-        const cuuint32_t estride[2] = {1, 1};
-        CUresult r = h->encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->wpack, gdim,
-                                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return DCN_ERR_CUDA;
-        // stream-K workspace: a [O/16][128][16] fp32 tile per SM, plus flags
-        const size_t part_bytes = static_cast<size_t>(h->sm_count) * 128 * O * sizeof(float);
-        const size_t flag_bytes = static_cast<size_t>(h->sm_count + 1) * sizeof(unsigned);
-        dcn_status_t st = ensure(&h->partial, &h->partial_cap, part_bytes, s);
-        if (st != DCN_OK) return st;
-        if (h->flags_cap < flag_bytes || !h->flags) {
-            st = ensure(&h->flags, &h->flags_cap, flag_bytes, s);
-            if (st != DCN_OK) return st;
-            if (cudaMemsetAsync(h->flags, 0, h->flags_cap, s) != cudaSuccess) return DCN_ERR_CUDA;
-            h->epoch = 0;
-        }
-        if (++h->epoch == 0) {
-            // flag values wrapped: clear the flags and start again at 1
-            if (cudaMemsetAsync(h->flags, 0, h->flags_cap, s) != cudaSuccess) return DCN_ERR_CUDA;
-            h->epoch = 1;
-        }
-        p.partial = static_cast<float *>(h->partial);
-        p.flags = static_cast<unsigned *>(h->flags);
-        p.epoch = h->epoch;
-        e = dcn::launch_tc(p, map, s);
-    } else {
-        e = dcn::launch_simt(p, dtype, s);
+    if (path == DCN_PATH_SIMT) {
+        if (dcn::launch_simt(p, dtype, s) != cudaSuccess) return DCN_ERR_CUDA;
+        h->last_path = path;
+        return DCN_OK;
     }
-    if (e != cudaSuccess) return DCN_ERR_CUDA;
+
+    // tensor cores: one launch per weight group and per 256 of its outputs
+    const int Cg = c.Cg(), Og = c.Og(), Cq = c.Cq();
+    const int chunk_max = Og < 256 ? Og : 256;
+    const size_t part_bytes = static_cast<size_t>(h->sm_count) * 128 * chunk_max * sizeof(float);
+    const size_t flag_bytes = static_cast<size_t>(h->sm_count + 1) * sizeof(unsigned);
+    dcn_status_t st = ensure(&h->partial, &h->partial_cap, part_bytes, s);
+    if (st != DCN_OK) return st;
+    if (h->flags_cap < flag_bytes || !h->flags) {
+        st = ensure(&h->flags, &h->flags_cap, flag_bytes, s);
+        if (st != DCN_OK) return st;
+        if (cudaMemsetAsync(h->flags, 0, h->flags_cap, s) != cudaSuccess) return DCN_ERR_CUDA;
+        h->epoch = 0;
+    }
+    const size_t HoWo = static_cast<size_t>(c.Ho) * c.Wo;
+    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    const __nv_bfloat16 *wb = static_cast<const __nv_bfloat16 *>(h->wpack);
+    __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(out);
+    for (int g = 0; g < d.groups; ++g) {
+        // the offset groups of this weight group's channels
+        const int og_base = g * Cg / Cq;
+        const int og_count = Cq >= Cg ? 1 : Cg / Cq;
+        for (int o0 = 0; o0 < Og; o0 += 256) {
+            const int n = Og - o0 < 256 ? Og - o0 : 256;
+            const size_t row0 = static_cast<size_t>(g) * Og + o0;
+            dcn::Params q = p;
+            q.x = xb + static_cast<size_t>(g) * Cg;
+            q.C = Cg;
+            q.O = n;
+            q.groups = 1;
+            q.ogroups = og_count;
+            q.og_count = og_count;
+            q.offset = offset + static_cast<size_t>(og_base) * 2 * taps * HoWo;
+            q.mask = mask ? mask + static_cast<size_t>(og_base) * taps * HoWo : nullptr;
+            q.wpack = wb + row0 * p.K;
+            q.bias = bias ? bias + row0 : nullptr;
+            q.out = ob + row0;
+            CUtensorMap map;
+            std::memset(&map, 0, sizeof(map));
+            const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(n)};
+            const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p.K) * 2};
+            const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(n)};
+            const cuuint32_t estride[2] = {1, 1};
+            CUresult r = h->encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                         const_cast<void *>(q.wpack), gdim, gstride, box, estride,
+                                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return DCN_ERR_CUDA;
+            q.partial = static_cast<float *>(h->partial);
+            q.flags = static_cast<unsigned *>(h->flags);
+            st = next_epoch(h, s, &q.epoch);
+            if (st != DCN_OK) return st;
+            if (dcn::launch_tc(q, map, s) != cudaSuccess) return DCN_ERR_CUDA;
+        }
+    }
     h->last_path = path;
     return DCN_OK;
 }
@@ -252,7 +347,20 @@ dcn_status_t dcn_pack_weight(dcn_handle_t h, const void *weight, int O, int C, i
     if (O <= 0 || C <= 0 || kh <= 0 || kw <= 0) return DCN_ERR_INVALID_ARG;
     if (static_cast<long long>(O) * C * kh * kw > kIndexLimit) return DCN_ERR_INVALID_ARG;
     if (!aligned(weight, esize(dtype))) return DCN_ERR_INVALID_ARG;
-    return pack_impl(h, weight, O, C, kh, kw, dtype, as_stream(stream));
+    Conv c;
+    c.d = page_desc(1, C, 1, 1, O, kh, kw, 0);   // only (O, C, kh, kw) key the pack
+    c.Ho = c.Wo = 1;
+    return pack_impl(h, weight, c, dtype, as_stream(stream));
+}
+
+dcn_status_t dcn_pack_weight_ex(dcn_handle_t h, const void *weight, const dcn_conv_desc_t *desc,
+                                int dtype, void *stream) {
+    if (!h || !weight || !desc) return DCN_ERR_INVALID_ARG;
+    Conv c;
+    dcn_status_t st = make_conv(*desc, dtype, &c);
+    if (st != DCN_OK) return st;
+    if (!aligned(weight, esize(dtype))) return DCN_ERR_INVALID_ARG;
+    return pack_impl(h, weight, c, dtype, as_stream(stream));
 }
 
 dcn_status_t dcn_forward_packed(dcn_handle_t h, const void *x, const float *offset,
@@ -260,12 +368,39 @@ dcn_status_t dcn_forward_packed(dcn_handle_t h, const void *x, const float *offs
                                 int B, int C, int H, int W, int O, int kh, int kw, int pad,
                                 int dtype, void *stream) {
     if (!h) return DCN_ERR_INVALID_ARG;
-    dcn_status_t st = check_dims(B, C, H, W, O, kh, kw, pad, dtype);
+    Conv c;
+    dcn_status_t st = make_conv(page_desc(B, C, H, W, O, kh, kw, pad), dtype, &c);
     if (st != DCN_OK) return st;
     st = check_forward_ptrs(x, offset, mask, nullptr, bias, out, dtype, false);
     if (st != DCN_OK) return st;
-    return forward_packed_impl(h, x, offset, mask, bias, out, B, C, H, W, O, kh, kw, pad, dtype,
-                               as_stream(stream));
+    return forward_packed_impl(h, x, offset, mask, bias, out, c, dtype, as_stream(stream));
+}
+
+dcn_status_t dcn_forward_packed_ex(dcn_handle_t h, const void *x, const float *offset,
+                                   const float *mask, const float *bias, void *out,
+                                   const dcn_conv_desc_t *desc, int dtype, void *stream) {
+    if (!h || !desc) return DCN_ERR_INVALID_ARG;
+    Conv c;
+    dcn_status_t st = make_conv(*desc, dtype, &c);
+    if (st != DCN_OK) return st;
+    st = check_forward_ptrs(x, offset, mask, nullptr, bias, out, dtype, false);
+    if (st != DCN_OK) return st;
+    return forward_packed_impl(h, x, offset, mask, bias, out, c, dtype, as_stream(stream));
+}
+
+static dcn_status_t forward_general(dcn_handle_t h, const void *x, const float *offset, const float *mask,
+                             const void *weight, const float *bias, void *out, const Conv &c,
+                             int dtype, void *stream) {
+    dcn_status_t st = check_forward_ptrs(x, offset, mask, weight, bias, out, dtype, true);
+    if (st != DCN_OK) return st;
+    // a forced tensor-core path that cannot run this shape launches nothing
+    if (h->path == DCN_PATH_TC &&
+        !(dtype == DCN_BF16 && tc_general_ok(c) && aligned(x, 32) && aligned(out, 16)))
+        return DCN_ERR_UNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    st = pack_impl(h, weight, c, dtype, s);
+    if (st != DCN_OK) return st;
+    return forward_packed_impl(h, x, offset, mask, bias, out, c, dtype, s);
 }
 
 dcn_status_t dcn_forward(dcn_handle_t h, const void *x, const float *offset, const float *mask,
@@ -273,18 +408,26 @@ dcn_status_t dcn_forward(dcn_handle_t h, const void *x, const float *offset, con
                          int B, int C, int H, int W, int O, int kh, int kw, int pad,
                          int dtype, void *stream) {
     if (!h) return DCN_ERR_INVALID_ARG;
-    dcn_status_t st = check_dims(B, C, H, W, O, kh, kw, pad, dtype);
+    Conv c;
+    dcn_status_t st = make_conv(page_desc(B, C, H, W, O, kh, kw, pad), dtype, &c);
     if (st != DCN_OK) return st;
-    st = check_forward_ptrs(x, offset, mask, weight, bias, out, dtype, true);
+    return forward_general(h, x, offset, mask, weight, bias, out, c, dtype, stream);
+}
+
+dcn_status_t dcn_forward_ex(dcn_handle_t h, const void *x, const float *offset, const float *mask,
+                            const void *weight, const float *bias, void *out,
+                            const dcn_conv_desc_t *desc, int dtype, void *stream) {
+    if (!h || !desc) return DCN_ERR_INVALID_ARG;
+    Conv c;
+    dcn_status_t st = make_conv(*desc, dtype, &c);
     if (st != DCN_OK) return st;
-    // a forced tensor-core path that cannot run this shape launches nothing
-    if (h->path == DCN_PATH_TC &&
-        !(dtype == DCN_BF16 && dcn::tc_supported(C, O) && aligned(x, 32) && aligned(out, 16)))
-        return DCN_ERR_UNSUPPORTED;
-    cudaStream_t s = as_stream(stream);
-    st = pack_impl(h, weight, O, C, kh, kw, dtype, s);
-    if (st != DCN_OK) return st;
-    return forward_packed_impl(h, x, offset, mask, bias, out, B, C, H, W, O, kh, kw, pad, dtype, s);
+    return forward_general(h, x, offset, mask, weight, bias, out, c, dtype, stream);
+}
+
+int dcn_out_size(int n, int k, int stride, int pad, int dil) {
+    if (n <= 0 || k <= 0 || stride <= 0 || pad < 0 || dil <= 0) return 0;
+    const long long r = out_size_ll(n, k, stride, pad, dil);
+    return r > kIndexLimit ? 0 : static_cast<int>(r);
 }
 
 dcn_status_t dcn_sync_status(dcn_handle_t h, void *stream) {
@@ -308,7 +451,8 @@ dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset
                               int B, int C, int H, int W, int O, int kh, int kw, int pad,
                               int dtype, void *stream) {
     if (!h) return DCN_ERR_INVALID_ARG;
-    dcn_status_t st = check_dims(B, C, H, W, O, kh, kw, pad, dtype);
+    Conv c;
+    dcn_status_t st = make_conv(page_desc(B, C, H, W, O, kh, kw, pad), dtype, &c);
     if (st != DCN_OK) return st;
     st = check_forward_ptrs(x, offset, mask, weight, bias, out, dtype, true);
     if (st != DCN_OK) return st;

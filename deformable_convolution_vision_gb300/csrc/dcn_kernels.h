@@ -7,16 +7,35 @@
 namespace dcn {
 
 // Everything a forward kernel needs, passed by value.  Device pointers.
+//
+// The CUDA-core kernel reads the whole problem.  A tensor-core launch sees
+// one weight group and one chunk of at most 256 of its output channels: C
+// is then the group's channel count, O the chunk's output count, and the
+// pointers are advanced to the group / chunk (x to its first channel,
+// offset and mask to its first offset group, wpack, bias and out to its
+// first output channel), with x_cstride and out_stride the full row
+// strides.
 struct Params {
-    const void *x;        // [B, H, W, C] channels-last
-    const float *offset;  // [B, 2*kh*kw, Ho, Wo]
-    const float *mask;    // [B, kh*kw, Ho, Wo] or nullptr
-    const void *wpack;    // [O][kh*kw*C], tap-major / channel-minor (see wperm)
+    const void *x;        // [B, H, W, x_cstride] channels-last
+    const float *offset;  // [B, 2*ogroups*kh*kw, Ho, Wo]
+    const float *mask;    // [B, ogroups*kh*kw, Ho, Wo] or nullptr
+    const void *wpack;    // [O][kh*kw*(C/groups)], tap-major / channel-minor (see wperm)
     const float *bias;    // [O] or nullptr
-    void *out;            // [B, Ho, Wo, O] channels-last
-    int B, C, H, W, O, kh, kw, pad, Ho, Wo;
+    void *out;            // [B, Ho, Wo, out_stride] channels-last
+    int B, C, H, W, O, kh, kw;
+    int sh, sw, ph, pw, dh, dw;  // stride, padding, dilation (h, w)
+    int groups;           // weight groups (CUDA-core kernel; 1 in a tensor-core launch)
+    int ogroups;          // offset groups (CUDA-core kernel)
+    int Ho, Wo;
     int P;                // B * Ho * Wo output pixels
-    int K;                // kh * kw * C
+    int K;                // kh * kw * (C / groups): packed weight row length
+    int x_cstride;        // elements between neighbouring pixels of x
+    int out_stride;       // elements between neighbouring pixels of out
+    // tensor-core launch view of the offset groups: og_count groups of
+    // C / og_count channels each, from the first one the pointers address;
+    // batch strides of offset and mask in planes (2*ogroups*kh*kw, ogroups*kh*kw)
+    int og_count;
+    int off_bstride, mask_bstride;
     unsigned *status;     // device status word (timeout bit)
     unsigned long long timeout_ns;  // bound of every barrier wait
     int sample_f32;       // tensor-core path: 1 = fp32 bilinear combine, 0 = bf16
@@ -41,19 +60,25 @@ __host__ __device__ constexpr int tc_channel_perm(int c) {
 
 enum Dtype { kF32 = 0, kBF16 = 1 };
 
-// S0: weight [O, C, kh, kw] -> packed [O][(i*kw + j)*C + c'], where
-// c' = c, or c' = tc_channel_perm(c) with perm != 0 (C % 64 == 0 only).
-cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int C, int kh, int kw,
+// S0: weight [O, Cg, kh, kw] -> packed [O][(i*kw + j)*Cg + c'], where
+// c' = c, or c' = tc_channel_perm(c) with perm != 0 (Cg % 64 == 0 only).
+cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int Cg, int kh, int kw,
                                int dtype, int perm, cudaStream_t stream);
 
 // CUDA-core fused sample + contraction + epilogue (fp32 or bf16 operands).
 cudaError_t launch_simt(const Params &p, int dtype, cudaStream_t stream);
 
-// tcgen05 fused implicit GEMM (bf16 operands).  `wmap` is a 2-D tensor map
-// over the packed bf16 weight, box {64, O}, 128-byte swizzle.
+// tcgen05 fused implicit GEMM (bf16 operands), one launch = one weight
+// group x one chunk of its output channels (see Params).  `wmap` is a 2-D
+// tensor map over the chunk's rows of the packed bf16 weight, box {64, O},
+// 128-byte swizzle.
+//   tc_supported: the channel and output counts of one launch;
+//   tc_max_virtual_taps: bound on kh*kw*og_count (a per-CTA table).
 bool tc_supported(int C, int O);
-// Whether a weight for this (dtype, C, O) is packed in tc_channel_perm order.
-inline bool tc_pack_permuted(int dtype, int C, int O) { return dtype == kBF16 && tc_supported(C, O); }
+constexpr int tc_max_virtual_taps = 512;
+// Whether a weight whose groups have Cg channels is packed in
+// tc_channel_perm order (bf16 and whole 64-channel blocks).
+inline bool tc_pack_permuted(int dtype, int Cg) { return dtype == kBF16 && Cg % 64 == 0; }
 cudaError_t launch_tc(const Params &p, const CUtensorMap &wmap, cudaStream_t stream);
 
 // One-thread kernel whose barrier wait runs out after timeout_ns.

@@ -112,17 +112,26 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     // the status word keeps the previous call's value: start this call at zero
     if (cudaMemsetAsync(s->status, 0, sizeof(unsigned), cs) != cudaSuccess) return DCN_ERR_CUDA;
-    const int perm = dcn::tc_pack_permuted(dtype, C, O) ? 1 : 0;
+    const int perm = dcn::tc_pack_permuted(dtype, C) ? 1 : 0;
     if (dcn::launch_pack_weight(weight, s->wpack, O, C, kh, kw, dtype, perm, cs) != cudaSuccess)
         return DCN_ERR_CUDA;
 
     dcn::Params p;
     p.x = x; p.offset = offset; p.mask = mask; p.wpack = s->wpack; p.bias = bias; p.out = out;
-    p.B = B; p.C = C; p.H = H; p.W = W; p.O = O; p.kh = kh; p.kw = kw; p.pad = pad;
+    p.B = B; p.C = C; p.H = H; p.W = W; p.O = O; p.kh = kh; p.kw = kw;
+    p.sh = p.sw = 1;
+    p.ph = p.pw = pad;
+    p.dh = p.dw = 1;
+    p.groups = p.ogroups = 1;
     p.Ho = static_cast<int>(Ho);
     p.Wo = static_cast<int>(Wo);
     p.P = B * p.Ho * p.Wo;
     p.K = kh * kw * C;
+    p.x_cstride = C;
+    p.out_stride = O;
+    p.og_count = 1;
+    p.off_bstride = 2 * kh * kw;
+    p.mask_bstride = kh * kw;
     p.status = s->status;
     p.timeout_ns = kWaitLimitNs;
     p.sample_f32 = 0;
@@ -133,8 +142,8 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.units_per_cta = 0;
     p.wperm = perm;
 
-    const bool tc = dtype == DCN_BF16 && dcn::tc_supported(C, O) && is_aligned(x, 32) &&
-                    is_aligned(out, 16);
+    const bool tc = dtype == DCN_BF16 && perm && dcn::tc_supported(C, O) && is_aligned(x, 32) &&
+                    is_aligned(out, 16) && kh * kw <= dcn::tc_max_virtual_taps;
     cudaError_t e;
     if (tc) {
         CUtensorMap map;

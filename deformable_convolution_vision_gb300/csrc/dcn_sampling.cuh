@@ -6,8 +6,11 @@
 //   py = (h - pad + i) + dy,  px = (w - pad + j) + dx       (fp32)
 // bilinearly from corners (y0 + a, x0 + e), y0 = floor(py), x0 = floor(px),
 // with weights (1-ly)(1-lx), (1-ly)lx, ly(1-lx), ly*lx, and every corner
-// outside the image contributes 0.  The mask scales the whole sample, so it
-// is folded into the four corner weights here.
+// outside the image contributes 0.  With stride, per-axis padding and
+// dilation (the convolution reading of torchvision deform_conv2d, which the
+// "deformops 3.0.1" page names) the integer part of the coordinate is
+// h*stride_h - pad_h + i*dil_h, likewise for w.  The mask scales the whole
+// sample, so it is folded into the four corner weights here.
 #pragma once
 
 #include <cstdint>
@@ -20,11 +23,12 @@ struct TapCorners {
                    // clamped inside the image so every load is in bounds
 };
 
-__device__ __forceinline__ void tap_corners(float dy, float dx, float m,
-                                            int h, int w, int i, int j, int pad,
-                                            int b, int H, int W, int C, TapCorners &t) {
-    float py = static_cast<float>(h - pad + i) + dy;
-    float px = static_cast<float>(w - pad + j) + dx;
+// y_base = h*stride_h - pad_h + i*dil_h, x_base likewise; cstride = the
+// element distance between neighbouring pixels of x.
+__device__ __forceinline__ void tap_corners(float dy, float dx, float m, int y_base, int x_base,
+                                            int b, int H, int W, int cstride, TapCorners &t) {
+    float py = static_cast<float>(y_base) + dy;
+    float px = static_cast<float>(x_base) + dx;
     // Coordinates below -1 or above H (W) leave every corner outside, so
     // clamping to [-2, H+1] changes no result; it keeps the integer
     // conversion in range for huge or non-finite offsets (NaN -> -2).
@@ -54,9 +58,9 @@ __device__ __forceinline__ void tap_corners(float dy, float dx, float m,
     // and one row that are 0 where the clamp folds both corners together
     const int yc0 = min(max(y0, 0), H - 1);
     const int xc0 = min(max(x0, 0), W - 1);
-    const int dxc = (x0 + 1 >= 1 && x0 + 1 <= W - 1) ? C : 0;      // xc1 - xc0, times C
-    const int dyc = (y0 + 1 >= 1 && y0 + 1 <= H - 1) ? W * C : 0;  // yc1 - yc0, times W*C
-    t.idx[0] = ((b * H + yc0) * W + xc0) * C;
+    const int dxc = (x0 + 1 >= 1 && x0 + 1 <= W - 1) ? cstride : 0;      // xc1 - xc0, in elements
+    const int dyc = (y0 + 1 >= 1 && y0 + 1 <= H - 1) ? W * cstride : 0;  // yc1 - yc0, in elements
+    t.idx[0] = ((b * H + yc0) * W + xc0) * cstride;
     t.idx[1] = t.idx[0] + dxc;
     t.idx[2] = t.idx[0] + dyc;
     t.idx[3] = t.idx[2] + dxc;

@@ -72,6 +72,13 @@ dcn_simt_kernel(Params p) {
     const int tx = tid % 16;   // channel group: outputs tx*4 .. tx*4+3
     const int HoWo = p.Ho * p.Wo;
     const int taps = p.kh * p.kw;
+    const int Cg = p.C / p.groups;     // input channels per weight group
+    const int Og = p.O / p.groups;     // output channels per weight group
+    const int Cq = p.C / p.ogroups;    // channels per offset group
+    // the channels this block's outputs contract over: their weight groups
+    const int o_last = min(o0 + SIMT_BN, p.O) - 1;
+    const int c_lo = (o0 / Og) * Cg;
+    const int c_hi = (o_last / Og + 1) * Cg;
 
     // the pixel whose corner weights this thread computes (tid < SIMT_BM)
     const int my_pix = pix0 + tid;
@@ -92,75 +99,86 @@ dcn_simt_kernel(Params p) {
     for (int tap = 0; tap < taps; ++tap) {
         const int i = tap / p.kw;
         const int j = tap - i * p.kw;
-        __syncthreads();  // the previous tap's corner table is no longer read
-        if (tid < SIMT_BM) {
-            TapCorners t;
-            if (my_pix < p.P) {
-                const size_t hw = static_cast<size_t>(my_h) * p.Wo + my_w;
-                const size_t ob = static_cast<size_t>(my_b) * 2 * taps * HoWo + hw;
-                const float dy = p.offset[ob + static_cast<size_t>(2 * tap) * HoWo];
-                const float dx = p.offset[ob + static_cast<size_t>(2 * tap + 1) * HoWo];
-                const float m = p.mask
-                    ? p.mask[(static_cast<size_t>(my_b) * taps + tap) * HoWo + hw] : 1.0f;
-                tap_corners(dy, dx, m, my_h, my_w, i, j, p.pad, my_b, p.H, p.W, p.C, t);
-            } else {
+        // the block's channels, one offset group at a time (each has its
+        // own offsets and mask, so its own corner table)
+        for (int q = c_lo / Cq; q * Cq < c_hi; ++q) {
+            const int cq_lo = max(c_lo, q * Cq);
+            const int cq_hi = min(c_hi, (q + 1) * Cq);
+            __syncthreads();  // the previous corner table is no longer read
+            if (tid < SIMT_BM) {
+                TapCorners t;
+                if (my_pix < p.P) {
+                    const size_t hw = static_cast<size_t>(my_h) * p.Wo + my_w;
+                    const size_t bq = static_cast<size_t>(my_b) * p.ogroups + q;
+                    const size_t ob = bq * 2 * taps * HoWo + hw;
+                    const float dy = p.offset[ob + static_cast<size_t>(2 * tap) * HoWo];
+                    const float dx = p.offset[ob + static_cast<size_t>(2 * tap + 1) * HoWo];
+                    const float m = p.mask ? p.mask[(bq * taps + tap) * HoWo + hw] : 1.0f;
+                    tap_corners(dy, dx, m, my_h * p.sh - p.ph + i * p.dh, my_w * p.sw - p.pw + j * p.dw,
+                                my_b, p.H, p.W, p.x_cstride, t);
+                } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) { t.w[q] = 0.0f; t.idx[q] = 0; }
+                    for (int e = 0; e < 4; ++e) { t.w[e] = 0.0f; t.idx[e] = 0; }
+                }
+                cw_s[tid] = make_float4(t.w[0], t.w[1], t.w[2], t.w[3]);
+                ci_s[tid] = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
             }
-            cw_s[tid] = make_float4(t.w[0], t.w[1], t.w[2], t.w[3]);
-            ci_s[tid] = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
-        }
-        __syncthreads();
+            __syncthreads();
 
-        for (int c0 = 0; c0 < p.C; c0 += SIMT_BK) {
-            // sampled operand: 16 channels x 64 pixels; consecutive threads
-            // take consecutive channels of one pixel (coalesced in NHWC)
+            for (int c0 = cq_lo; c0 < cq_hi; c0 += SIMT_BK) {
+                // sampled operand: 16 channels x 64 pixels; consecutive threads
+                // take consecutive channels of one pixel (coalesced in NHWC)
 #pragma unroll
-            for (int e = 0; e < (SIMT_BK * SIMT_BM) / SIMT_THREADS; ++e) {
-                const int idx = tid + e * SIMT_THREADS;
-                const int kk = idx % SIMT_BK;
-                const int pp = idx / SIMT_BK;
-                const int c = c0 + kk;
-                float v = 0.0f;
-                if (c < p.C) {
-                    const float4 cw = cw_s[pp];
-                    const int4 ci = ci_s[pp];
-                    if (cw.x != 0.0f) v += cw.x * to_f32<T>(x[ci.x + c]);
-                    if (cw.y != 0.0f) v += cw.y * to_f32<T>(x[ci.y + c]);
-                    if (cw.z != 0.0f) v += cw.z * to_f32<T>(x[ci.z + c]);
-                    if (cw.w != 0.0f) v += cw.w * to_f32<T>(x[ci.w + c]);
+                for (int e = 0; e < (SIMT_BK * SIMT_BM) / SIMT_THREADS; ++e) {
+                    const int idx = tid + e * SIMT_THREADS;
+                    const int kk = idx % SIMT_BK;
+                    const int pp = idx / SIMT_BK;
+                    const int c = c0 + kk;
+                    float v = 0.0f;
+                    if (c < cq_hi) {
+                        const float4 cw = cw_s[pp];
+                        const int4 ci = ci_s[pp];
+                        if (cw.x != 0.0f) v += cw.x * to_f32<T>(x[ci.x + c]);
+                        if (cw.y != 0.0f) v += cw.y * to_f32<T>(x[ci.y + c]);
+                        if (cw.z != 0.0f) v += cw.z * to_f32<T>(x[ci.z + c]);
+                        if (cw.w != 0.0f) v += cw.w * to_f32<T>(x[ci.w + c]);
+                    }
+                    As[kk][pp] = v;
                 }
-                As[kk][pp] = v;
-            }
-            // weight tile: 16 channels x 64 outputs, contiguous along K
+                // weight tile: 16 channels x 64 outputs; an output's weight is
+                // 0 for channels outside its group
 #pragma unroll
-            for (int e = 0; e < (SIMT_BK * SIMT_BN) / SIMT_THREADS; ++e) {
-                const int idx = tid + e * SIMT_THREADS;
-                const int kk = idx % SIMT_BK;
-                const int oo = idx / SIMT_BK;
-                const int c = c0 + kk;
-                const int o = o0 + oo;
-                float v = 0.0f;
-                if (c < p.C && o < p.O) {
-                    const int cp = p.wperm ? tc_channel_perm(c) : c;   // packed position of c
-                    v = to_f32<T>(wp[static_cast<size_t>(o) * p.K + static_cast<size_t>(tap) * p.C + cp]);
+                for (int e = 0; e < (SIMT_BK * SIMT_BN) / SIMT_THREADS; ++e) {
+                    const int idx = tid + e * SIMT_THREADS;
+                    const int kk = idx % SIMT_BK;
+                    const int oo = idx / SIMT_BK;
+                    const int c = c0 + kk;
+                    const int o = o0 + oo;
+                    float v = 0.0f;
+                    if (c < cq_hi && o < p.O) {
+                        const int cl = c - (o / Og) * Cg;   // channel within the output's group
+                        if (cl >= 0 && cl < Cg) {
+                            const int cp = p.wperm ? tc_channel_perm(cl) : cl;   // packed position
+                            v = to_f32<T>(wp[static_cast<size_t>(o) * p.K + static_cast<size_t>(tap) * Cg + cp]);
+                        }
+                    }
+                    Bs[kk][oo] = v;
                 }
-                Bs[kk][oo] = v;
+                __syncthreads();
+#pragma unroll
+                for (int kk = 0; kk < SIMT_BK; ++kk) {
+                    float a[4], b[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) a[r] = As[kk][ty * 4 + r];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) b[r] = Bs[kk][tx * 4 + r];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(a[r], b[s], acc[r][s]);
+                }
+                __syncthreads();
             }
-            __syncthreads();
-#pragma unroll
-            for (int kk = 0; kk < SIMT_BK; ++kk) {
-                float a[4], b[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) a[r] = As[kk][ty * 4 + r];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) b[r] = Bs[kk][tx * 4 + r];
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(a[r], b[s], acc[r][s]);
-            }
-            __syncthreads();
         }
     }
 
@@ -175,7 +193,7 @@ dcn_simt_kernel(Params p) {
             const int o = o0 + tx * 4 + s;
             if (o >= p.O) continue;
             const float bv = p.bias ? p.bias[o] : 0.0f;
-            out[static_cast<size_t>(pix) * p.O + o] = from_f32<T>(acc[r][s] + bv);
+            out[static_cast<size_t>(pix) * p.out_stride + o] = from_f32<T>(acc[r][s] + bv);
         }
     }
 }
@@ -184,6 +202,7 @@ dcn_simt_kernel(Params p) {
 
 cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int C, int kh, int kw,
                                int dtype, int perm, cudaStream_t stream) {
+    // C: the weight's channel count, C_in / groups
     if (perm && C % 64 != 0) return cudaErrorInvalidValue;
     const int K = kh * kw * C;
     const int threads = 256;

@@ -95,10 +95,11 @@ struct TcLayout {
     int bar_off;       // barriers after the stages
     int table_off;     // per-warp corner tables
     int raw_off;       // per-warp raw geometry inputs (dy, dx, mask) [3][32] fp32
+    int vt_off;        // virtual-tap table, int4 per (tap, offset group)
     int total;         // bytes used from the 1024-aligned base
 };
 
-__host__ __device__ inline TcLayout tc_layout(int O, int stages, bool f32) {
+__host__ __device__ inline TcLayout tc_layout(int O, int stages, bool f32, int vtaps) {
     TcLayout L;
     L.stages = stages;
     L.b_bytes = O * TC_BK * 2;
@@ -107,7 +108,8 @@ __host__ __device__ inline TcLayout tc_layout(int O, int stages, bool f32) {
     L.table_off = L.bar_off + (2 * stages + 5) * 8;
     L.table_off = (L.table_off + 15) & ~15;
     L.raw_off = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_SLOTS * table_buf_bytes(f32);
-    L.total = L.raw_off + TC_SAMPLER_WARPS * 3 * 32 * 4;
+    L.vt_off = L.raw_off + TC_SAMPLER_WARPS * 3 * 32 * 4;
+    L.total = L.vt_off + vtaps * 16;
     return L;
 }
 
@@ -164,7 +166,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const TcLayout L = tc_layout(p.O, stages, kSampleF32);
+    const TcLayout L = tc_layout(p.O, stages, kSampleF32, p.kh * p.kw * p.og_count);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + stages);
@@ -180,9 +182,14 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     const int lane = threadIdx.x % 32;
     const int tiles_x = (p.Wo + TC_TILE_W - 1) / TC_TILE_W;
     const int tiles_y = (p.Ho + TC_TILE_H - 1) / TC_TILE_H;
-    const int ncb = p.C / TC_BK;
+    const int ncb = p.C / TC_BK;                // channel blocks of the launch
     const int taps = p.kh * p.kw;
     const int nkb = taps * ncb;
+    // The K walk tap-major, channel-minor, seen as virtual taps: (tap,
+    // offset group) pairs, each with its own offsets and mask, of vncb
+    // channel blocks each.  K-block kb = vt * vncb + vcb.
+    const int vtaps = taps * p.og_count;
+    const int vncb = ncb / p.og_count;
     const int total = p.B * tiles_x * tiles_y * nkb;
     const int u_begin = blockIdx.x * p.units_per_cta;
     const int u_end = min(u_begin + p.units_per_cta, total);
@@ -191,6 +198,17 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     const uint32_t acc_cols = tmem_acc_cols(p.O);
     const uint32_t a_col0 = acc_bufs * acc_cols;
 
+    // virtual-tap table: {i*dil_h - pad_h, j*dil_w - pad_w, mask plane
+    // og*taps + tap of the launch's offset groups, channel offset of the
+    // offset group's first block}
+    int4 *vt_tab = reinterpret_cast<int4 *>(smem + L.vt_off);
+    for (int vt = threadIdx.x; vt < vtaps; vt += blockDim.x) {
+        const int tap = vt / p.og_count;
+        const int og = vt - tap * p.og_count;
+        const int i = tap / p.kw;
+        const int j = tap - i * p.kw;
+        vt_tab[vt] = make_int4(i * p.dh - p.ph, j * p.dw - p.pw, og * taps + tap, og * vncb * TC_BK);
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(full0 + 8 * s, 1 + TC_TEAM_WARPS);
@@ -300,7 +318,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         // the sequence of taps a warp visits: every tap, or with two teams
         // and one channel block per tap (alternate K-blocks = alternate
         // taps) every other one
-        const int tap_shift = (TC_TEAMS == 2 && ncb == 1) ? 1 : 0;
+        const int tap_shift = (TC_TEAMS == 2 && vncb == 1) ? 1 : 0;
         // epilogue: TMEM lane quarter, column part, A row of this thread
         const int part = sw >> 2;                        // 0 .. TC_EPI_PARTS - 1
         const int erow = q * 32 + lane;
@@ -379,7 +397,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                                 const float b1 = p.bias ? __ldg(p.bias + o + 1) : 0.0f;
                                 pk[e] = pack_bf16x2(vv[2 * e] + b0, vv[2 * e + 1] + b1);
                             }
-                            uint4 *dst = reinterpret_cast<uint4 *>(out + pix * p.O + ch * 16);
+                            uint4 *dst = reinterpret_cast<uint4 *>(out + pix * p.out_stride + ch * 16);
                             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                         }
@@ -415,7 +433,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 const int my_w = tw0 + my_px;
                 const bool my_valid = (my_h < p.Ho) && (my_w < p.Wo);
                 const int my_hw = my_valid ? my_h * p.Wo + my_w : 0;
-                const int t_first = kb_first / ncb;
+                const int t_first = kb_first / vncb;
                 const int tap_par = tap_shift ? (t_first & 1) : 0;
                 // position of a tap in the warp's sequence, and back
                 auto seq_of = [&](int tap) { return tap >> tap_shift; };
@@ -427,36 +445,34 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 // whole group ahead of their use into the warp's raw slot
                 // (asynchronously: no registers held while in flight)
                 auto load_raw = [&](int group_sq) {
-                    const int tap = tap_of(group_sq + my_g);
-                    const bool valid = my_valid && tap < taps;
+                    const int vt = tap_of(group_sq + my_g);
+                    const bool valid = my_valid && vt < vtaps;
+                    const int mc = valid ? vt_tab[vt].z : 0;   // mask plane; offsets 2*mc, 2*mc + 1
                     const float *o = valid
-                        ? p.offset + (static_cast<size_t>(tb) * 2 * taps + 2 * tap) * HoWo + my_hw
+                        ? p.offset + (static_cast<size_t>(tb) * p.off_bstride + 2 * mc) * HoWo + my_hw
                         : p.offset;
                     cp_async_4(raw_s, o, valid);
                     cp_async_4(raw_s + 128, valid ? o + HoWo : o, valid);
                     if (p.mask) {
                         const float *mp = valid
-                            ? p.mask + (static_cast<size_t>(tb) * taps + tap) * HoWo + my_hw
+                            ? p.mask + (static_cast<size_t>(tb) * p.mask_bstride + mc) * HoWo + my_hw
                             : p.mask;
                         cp_async_4(raw_s + 256, mp, valid);
                     }
                 };
-                // kernel row and column (ti, tj) of this lane's tap, advanced
-                // by a group per tabulation instead of divided out each time
-                const int step = TC_TAP_GROUP << tap_shift;
-                int ti = tap_of(g0 + my_g) / p.kw;
-                int tj = tap_of(g0 + my_g) - ti * p.kw;
-                // corner tables of the group's two taps (ring slot sq % 4)
+                // corner tables of the group's two virtual taps (ring slot sq % 4)
                 auto tabulate = [&](int group_sq) {
                     const int sq = group_sq + my_g;
-                    const int tap = tap_of(sq);
+                    const int vt = tap_of(sq);
                     TapCorners t;
                     cp_async_wait_all();
-                    if (my_valid && tap < taps) {
+                    if (my_valid && vt < vtaps) {
+                        const int4 e = vt_tab[vt];
                         const float dy = lds_f32(raw_s);
                         const float dx = lds_f32(raw_s + 128);
                         const float m = p.mask ? lds_f32(raw_s + 256) : 1.0f;
-                        tap_corners(dy, dx, m, my_h, my_w, ti, tj, p.pad, tb, p.H, p.W, p.C, t);
+                        tap_corners(dy, dx, m, my_h * p.sh + e.x, my_w * p.sw + e.y, tb, p.H, p.W,
+                                    p.x_cstride, t);
                     } else {
 #pragma unroll
                         for (int k = 0; k < 4; ++k) { t.w[k] = 0.0f; t.idx[k] = 0; }
@@ -473,8 +489,10 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                                        bf16x2_splat(t.w[3]));
                     }
                     *reinterpret_cast<int4 *>(slot + kIdx + rowb) = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
-                    tj += step;
-                    while (tj >= p.kw) { tj -= p.kw; ++ti; }
+                };
+                // the channel offset of virtual tap vt's block vcb in the launch
+                auto chan_off = [&](int vt, int vcb) {
+                    return (p.og_count == 1 ? 0 : vt_tab[vt].w) + vcb * TC_BK;
                 };
                 // the four 32-byte corner loads of one of this lane's two pixels
                 // from a table slot; corners outside the image read a clamped
@@ -495,29 +513,29 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 // finished reading them.
                 load_raw(g0);
                 tabulate(g0);
-                if (tap_of(g0 + TC_TAP_GROUP) < taps) load_raw(g0 + TC_TAP_GROUP);
-                if (sq0 != g0 && tap_of(g0 + TC_TAP_GROUP) < taps) {
+                if (tap_of(g0 + TC_TAP_GROUP) < vtaps) load_raw(g0 + TC_TAP_GROUP);
+                if (sq0 != g0 && tap_of(g0 + TC_TAP_GROUP) < vtaps) {
                     tabulate(g0 + TC_TAP_GROUP);
-                    if (tap_of(g0 + 2 * TC_TAP_GROUP) < taps) load_raw(g0 + 2 * TC_TAP_GROUP);
+                    if (tap_of(g0 + 2 * TC_TAP_GROUP) < vtaps) load_raw(g0 + 2 * TC_TAP_GROUP);
                 }
                 __syncwarp();
 
                 // Rolling pipeline: the corner loads of a pixel's next K-block
                 // go out as soon as its current ones are combined.
                 u32x8 v[8];
-                int tap = t_first, cb = kb_first - t_first * ncb;
+                int tap = t_first, cb = kb_first - t_first * vncb;   // virtual tap and its block
                 {
                     const uint32_t slot = table_s + (seq_of(tap) & (TC_TABLE_SLOTS - 1)) * kBuf;
-                    issue_px(0, slot, x + cb * TC_BK + quart * 16, v);
-                    issue_px(1, slot, x + cb * TC_BK + quart * 16, v);
+                    issue_px(0, slot, x + chan_off(tap, cb) + quart * 16, v);
+                    issue_px(1, slot, x + chan_off(tap, cb) + quart * 16, v);
                 }
 
                 for (int kb = kb_first; ok && kb < sg.kb1; kb += TC_TEAMS) {
                     const bool has_next = kb + TC_TEAMS < sg.kb1;
                     int n_tap = tap, n_cb = cb + TC_TEAMS;
                     // (at most TC_TEAMS carries: cb < ncb)
-                    if (n_cb >= ncb) { n_cb -= ncb; ++n_tap; }
-                    if (TC_TEAMS == 2 && n_cb >= ncb) { n_cb -= ncb; ++n_tap; }
+                    if (n_cb >= vncb) { n_cb -= vncb; ++n_tap; }
+                    if (TC_TEAMS == 2 && n_cb >= vncb) { n_cb -= vncb; ++n_tap; }
                     const int sq = seq_of(tap);
                     const uint32_t cur_slot = table_s + (sq & (TC_TABLE_SLOTS - 1)) * kBuf;
 
@@ -571,14 +589,14 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     // after.  The next K-block's tap is in the current group, so
                     // its slot is untouched.  Then the next K-block's loads.
                     if (has_next && n_tap != tap && (sq & (TC_TAP_GROUP - 1)) == 0 &&
-                        tap_of(sq + TC_TAP_GROUP) < taps) {
+                        tap_of(sq + TC_TAP_GROUP) < vtaps) {
                         tabulate(sq + TC_TAP_GROUP);
-                        if (tap_of(sq + 2 * TC_TAP_GROUP) < taps) load_raw(sq + 2 * TC_TAP_GROUP);
+                        if (tap_of(sq + 2 * TC_TAP_GROUP) < vtaps) load_raw(sq + 2 * TC_TAP_GROUP);
                     }
                     if (has_next) {
                         const uint32_t n_slot = table_s + (seq_of(n_tap) & (TC_TABLE_SLOTS - 1)) * kBuf;
-                        issue_px(0, n_slot, x + n_cb * TC_BK + quart * 16, v);
-                        issue_px(1, n_slot, x + n_cb * TC_BK + quart * 16, v);
+                        issue_px(0, n_slot, x + chan_off(n_tap, n_cb) + quart * 16, v);
+                        issue_px(1, n_slot, x + chan_off(n_tap, n_cb) + quart * 16, v);
                     }
                     tmem_wait_st();
                     tc_fence_before_sync();
@@ -648,14 +666,17 @@ cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t 
     const bool f32 = p.sample_f32 != 0;
     // A multiple of TC_TEAMS stages (with two teams each owns every other
     // one), as many as fit the budget and TMEM, at most 8.
-    auto smem_for = [&](int st) { return tc_layout(p.O, st, f32).total + 1024 + 1024; };
+    const int vtaps = p.kh * p.kw * p.og_count;
+    if (vtaps > tc_max_virtual_taps || p.og_count <= 0 || (p.C / TC_BK) % p.og_count != 0)
+        return cudaErrorInvalidValue;
+    auto smem_for = [&](int st) { return tc_layout(p.O, st, f32, vtaps).total + 1024 + 1024; };
     auto tmem_fits = [&](int st) { return tmem_acc_cols(p.O) + st * TC_A_COLS <= 512; };
     int stages = 2;
     for (int st = 8; st > 2; st -= TC_TEAMS) {
         if (tmem_fits(st) && smem_for(st) <= DCN_TC_SMEM_BUDGET) { stages = st; break; }
     }
     if (stages < 4 && tmem_fits(4) && smem_for(4) <= DCN_TC_SMEM_WIDE_BUDGET) stages = 4;
-    const TcLayout L = tc_layout(p.O, stages, f32);
+    const TcLayout L = tc_layout(p.O, stages, f32, vtaps);
     const int smem = L.total + 1024;  // slack for 1024-byte alignment
     auto kernel = f32 ? dcn_tc_kernel<true> : dcn_tc_kernel<false>;
     int &smem_set = f32 ? g_max_smem_set_f32 : g_max_smem_set;

@@ -122,3 +122,59 @@ def make_inputs(wl: Workload, seed=None):
         "weight": weight.to(dt),
         "bias": None if bias is None else bias.float().contiguous(),
     }
+
+
+@dataclass(frozen=True)
+class GeneralWorkload:
+    """A problem of the general form: stride, per-axis padding, dilation,
+    weight groups and offset groups.  Inputs follow make_inputs' recipe
+    (x ~ N(0,1), offsets ~ N(0, offset_std), sigmoid mask, weight std
+    1/sqrt(kh*kw*C/groups), bias ~ N(0, 0.1)); offsets and mask carry one
+    block of planes per offset group."""
+    name: str
+    B: int
+    C: int
+    H: int
+    W: int
+    O: int
+    kh: int
+    kw: int
+    stride: tuple = (1, 1)
+    padding: tuple = (0, 0)
+    dilation: tuple = (1, 1)
+    groups: int = 1
+    offset_groups: int = 1
+    dtype: str = "bf16"
+    offset_std: float = 2.0
+    mask: bool = True
+    seed: int = 0
+
+    def out_size(self):
+        def one(n, k, s, p, d):
+            span = n + 2 * p - d * (k - 1) - 1
+            return span // s + 1 if span >= 0 else 0
+        return (one(self.H, self.kh, self.stride[0], self.padding[0], self.dilation[0]),
+                one(self.W, self.kw, self.stride[1], self.padding[1], self.dilation[1]))
+
+
+def make_general_inputs(wl: GeneralWorkload):
+    """CPU tensors for a GeneralWorkload (layouts as make_inputs, with
+    weight [O, C/groups, kh, kw], offset [B, 2*G*kh*kw, Ho, Wo] and mask
+    [B, G*kh*kw, Ho, Wo], G = offset_groups)."""
+    g = torch.Generator().manual_seed(wl.seed)
+    Ho, Wo = wl.out_size()
+    k, G = wl.kh * wl.kw, wl.offset_groups
+    Cg = wl.C // wl.groups
+    x = torch.randn(wl.B, wl.C, wl.H, wl.W, generator=g)
+    offset = torch.randn(wl.B, 2 * G * k, Ho, Wo, generator=g) * wl.offset_std
+    mask = torch.sigmoid(torch.randn(wl.B, G * k, Ho, Wo, generator=g)) if wl.mask else None
+    weight = torch.randn(wl.O, Cg, wl.kh, wl.kw, generator=g) / (k * Cg) ** 0.5
+    bias = torch.randn(wl.O, generator=g) * 0.1
+    dt = TORCH_DTYPE[wl.dtype]
+    return {
+        "x": x.to(dt),
+        "offset": offset.contiguous(),
+        "mask": None if mask is None else mask.contiguous(),
+        "weight": weight.to(dt),
+        "bias": bias.contiguous(),
+    }

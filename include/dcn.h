@@ -81,7 +81,7 @@ typedef enum {
 /* Kernel selection for bf16.  AUTO takes the tcgen05 path when
  * C % 64 == 0, O % 16 == 0, 16 <= O <= 256, x is 32-byte aligned and out is
  * 16-byte aligned, and the CUDA-core path otherwise.  fp32 always takes the
- * CUDA-core path. */
+ * CUDA-core path.  (dcn_forward_ex states its own conditions.) */
 typedef enum {
     DCN_PATH_AUTO = 0,
     DCN_PATH_SIMT = 1,   /* CUDA-core fused sample + FFMA contraction */
@@ -206,6 +206,64 @@ DCN_API dcn_status_t dcn_forward_noalloc(const void *x, const float *offset, con
 
 /* Static, human-readable name of a status code. */
 DCN_API const char *dcn_status_string(dcn_status_t s);
+
+/* ------------------------------------------------------------------ general
+ * The general form: stride, per-axis padding, dilation, weight groups and
+ * offset (deformable) groups.  The pages fix stride 1, dilation 1, one
+ * padding and one group for their routine; the "deformops 3.0.1" page
+ * (section "Deformable convolution") names torchvision deform_conv2d, with
+ * a (C_out, C_in / groups, kH, kW) weight, as the operator, and these are
+ * the convolution reading of its parameters.  With G = offset_groups and
+ * Cq = C / G, output channel o in weight group g = o / (O / groups):
+ *
+ *   out[b,h,w,o] = bias[o] + sum_{i,j} sum_{c in group g}
+ *                  weight[o, c - g*C/groups, i, j] * m * S(b,c,py,px)
+ *   q  = c / Cq (the channel's offset group),
+ *   dy = offset[b, 2*kh*kw*q + 2k, h, w], dx = offset[b, 2*kh*kw*q + 2k+1, h, w],
+ *   m  = mask[b, kh*kw*q + k, h, w],
+ *   py = (h*stride_h - pad_h + i*dil_h) + dy,  px = (w*stride_w - pad_w + j*dil_w) + dx,
+ *   Ho = (H + 2*pad_h - dil_h*(kh-1) - 1) / stride_h + 1, likewise Wo.
+ *
+ * Layouts: x [B,H,W,C] and out [B,Ho,Wo,O] channels-last as above; offset
+ * [B, 2*G*kh*kw, Ho, Wo] and mask [B, G*kh*kw, Ho, Wo], each offset group's
+ * planes laid out like the one-group planes, one group after another;
+ * weight [O, C/groups, kh, kw]. */
+typedef struct {
+    int B, C, H, W;        /* input x [B, H, W, C] */
+    int O, kh, kw;         /* weight [O, C / groups, kh, kw] */
+    int stride_h, stride_w;  /* >= 1 */
+    int pad_h, pad_w;        /* >= 0, zero padding on both sides of each axis */
+    int dil_h, dil_w;        /* >= 1 */
+    int groups;              /* weight groups: divides C and O */
+    int offset_groups;       /* offset groups: divides C */
+} dcn_conv_desc_t;
+
+/* Output size of one axis: (n + 2*pad - dil*(k-1) - 1) / stride + 1, or 0
+ * if the kernel does not fit. */
+DCN_API int dcn_out_size(int n, int k, int stride, int pad, int dil);
+
+/* dcn_forward for the general form.  Argument rules as dcn_forward, plus
+ * the descriptor's (its fields as commented; every size product below
+ * 2^31).  AUTO takes the tcgen05 path for bf16 when, with Cg = C/groups,
+ * Og = O/groups, Cq = C/offset_groups: Cg % 64 == 0, Cq % 64 == 0, one of
+ * Cg and Cq divides the other, Og % 16 == 0, kh*kw*max(1, Cg/Cq) <= 512,
+ * x is 32-byte and out 16-byte aligned; it runs one launch per weight group
+ * and per 256 output channels.  Otherwise the CUDA-core path runs.  NULL
+ * desc: DCN_ERR_INVALID_ARG. */
+DCN_API dcn_status_t dcn_forward_ex(dcn_handle_t h,
+                            const void *x, const float *offset, const float *mask,
+                            const void *weight, const float *bias, void *out,
+                            const dcn_conv_desc_t *desc, int dtype, void *stream);
+
+/* The two halves of dcn_forward_ex: the pack keys on (O, C/groups, kh, kw,
+ * dtype) of desc; dcn_forward_packed_ex returns DCN_ERR_INVALID_ARG when
+ * they differ from the last pack on this handle. */
+DCN_API dcn_status_t dcn_pack_weight_ex(dcn_handle_t h, const void *weight,
+                                const dcn_conv_desc_t *desc, int dtype, void *stream);
+DCN_API dcn_status_t dcn_forward_packed_ex(dcn_handle_t h,
+                                   const void *x, const float *offset, const float *mask,
+                                   const float *bias, void *out,
+                                   const dcn_conv_desc_t *desc, int dtype, void *stream);
 
 #ifdef __cplusplus
 }

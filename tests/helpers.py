@@ -22,8 +22,8 @@ def to_device(inp, device="cuda"):
 def run_cuda(inp, pad, handle=None):
     import deformable_convolution_vision_gb300 as dcn
     d = to_device(inp)
-    out = dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], pad, d["mask"],
-                            handle=handle)
+    out = dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], padding=pad,
+                            mask=d["mask"], handle=handle)
     if handle is not None:
         st = dcn.dcn_sync_status(handle.h)
         assert st == 0, f"device status {dcn.dcn_status_string(st)}"

@@ -108,7 +108,8 @@ def test_host_entry_point_matches_device(handle, name):
     dcn.dcn_forward_host(handle.h, x, off, m, w, bias, out, wl.B, wl.C, wl.H, wl.W, wl.O,
                          wl.kh, wl.kw, wl.pad, code)
     d = to_device(inp)
-    ref = dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], wl.pad, d["mask"])
+    ref = dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], padding=wl.pad,
+                            mask=d["mask"])
     assert torch.equal(out, ref.permute(0, 2, 3, 1).cpu())
     assert compare_full(out.permute(0, 3, 1, 2), oracle_full(inp, wl.pad)) <= TOL[wl.dtype]
 
@@ -120,7 +121,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(handle):
     wl = WORKLOADS["tiny"]
     inp = make_inputs(wl)
     d = to_device(inp)
-    out = dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], wl.pad, d["mask"],
-                            handle=handle)
+    out = dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], padding=wl.pad,
+                            mask=d["mask"], handle=handle)
     assert dcn.dcn_sync_status(handle.h) == 0
     assert compare_full(out, oracle_full(inp, wl.pad)) <= TOL["f32"]
