@@ -8,14 +8,14 @@ Python side: ``binding`` maps the C entry points one to one, and
 """
 
 from . import binding
-from .binding import (DCN_BF16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
+from .binding import (DCN_BF16, DCN_F16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
                       DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, ConvDesc, DcnError, dcn_create,
                       dcn_destroy, dcn_forward, dcn_forward_ex, dcn_forward_host,
                       dcn_forward_packed, dcn_forward_packed_ex, dcn_last_path, dcn_out_size,
                       dcn_pack_weight, dcn_pack_weight_ex, dcn_selftest_timeout, dcn_set_path,
                       dcn_set_sample_precision, dcn_status_string, dcn_sync_status)
 
-__all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF16",
+__all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF16", "DCN_F16",
            "DCN_PATH_AUTO", "DCN_PATH_SIMT", "DCN_PATH_TC", "DCN_SAMPLE_INPUT_DTYPE",
            "DCN_SAMPLE_F32", "dcn_set_sample_precision", "dcn_create", "dcn_destroy",
            "dcn_forward", "dcn_forward_host", "dcn_forward_packed", "dcn_pack_weight",
@@ -58,7 +58,9 @@ def _dtype_code(t):
         return DCN_F32
     if t.dtype == torch.bfloat16:
         return DCN_BF16
-    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+    if t.dtype == torch.float16:
+        return DCN_F16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32, bfloat16 or float16")
 
 
 def _pair(v, name):
@@ -80,7 +82,7 @@ def deform_conv2d(x, offset, weight, bias=None, stride=1, padding=0, dilation=1,
     """Modulated deformable convolution forward on CUDA tensors, with
     torchvision ``deform_conv2d``'s argument order.
 
-    x       [B, C, H, W] float32/bfloat16, channels_last memory format
+    x       [B, C, H, W] float32/bfloat16/float16, channels_last memory format
     offset  [B, 2*G*kh*kw, Ho, Wo] float32, contiguous ((dy, dx) per tap,
             offset group after offset group); G = offset groups
     weight  [O, C/groups, kh, kw] same dtype as x, contiguous; groups = C / its dim 1

@@ -12,7 +12,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_HERE, "libdcn.so")
 
-DCN_F32, DCN_BF16 = 0, 1
+DCN_F32, DCN_BF16, DCN_F16 = 0, 1, 2
 DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC = 0, 1, 2
 DCN_SAMPLE_INPUT_DTYPE, DCN_SAMPLE_F32 = 0, 1
 STATUS = {0: "DCN_OK", 1: "DCN_ERR_INVALID_ARG", 2: "DCN_ERR_UNSUPPORTED", 3: "DCN_ERR_CUDA",

@@ -56,6 +56,9 @@ inline bool aligned(const void *p, size_t a) {
 }
 
 inline size_t esize(int dtype) { return dtype == DCN_F32 ? 4 : 2; }
+inline bool valid_dtype(int dtype) { return dtype == DCN_F32 || dtype == DCN_BF16 || dtype == DCN_F16; }
+// bf16 and fp16 run on the tensor cores where the shape allows
+inline bool tc_dtype(int dtype) { return dtype == DCN_BF16 || dtype == DCN_F16; }
 
 // A validated problem: the descriptor and its output size.
 struct Conv {
@@ -73,7 +76,7 @@ long long out_size_ll(long long n, long long k, long long stride, long long pad,
 }
 
 dcn_status_t make_conv(const dcn_conv_desc_t &d, int dtype, Conv *c) {
-    if (dtype != DCN_F32 && dtype != DCN_BF16) return DCN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
     if (d.B <= 0 || d.C <= 0 || d.H <= 0 || d.W <= 0 || d.O <= 0 || d.kh <= 0 || d.kw <= 0)
         return DCN_ERR_INVALID_ARG;
     if (d.stride_h <= 0 || d.stride_w <= 0 || d.dil_h <= 0 || d.dil_w <= 0 || d.pad_h < 0 || d.pad_w < 0)
@@ -189,6 +192,7 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
     p.status = h->status;
     p.timeout_ns = kWaitLimitNs;
     p.sample_f32 = h->sample == DCN_SAMPLE_F32 ? 1 : 0;
+    p.f16 = dtype == DCN_F16 ? 1 : 0;
     p.partial = nullptr;
     p.flags = nullptr;
     p.epoch = 0;
@@ -196,7 +200,7 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
     p.units_per_cta = 0;
     p.wperm = h->pk_perm;
 
-    const bool tc_ok = dtype == DCN_BF16 && tc_general_ok(c) && h->pk_perm &&
+    const bool tc_ok = tc_dtype(dtype) && tc_general_ok(c) && h->pk_perm &&
                        aligned(x, 32) && aligned(out, 16) && aligned(h->wpack, 16);
     int path = h->path;
     if (path == DCN_PATH_AUTO) path = tc_ok ? DCN_PATH_TC : DCN_PATH_SIMT;
@@ -222,9 +226,10 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
         h->epoch = 0;
     }
     const size_t HoWo = static_cast<size_t>(c.Ho) * c.Wo;
-    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
-    const __nv_bfloat16 *wb = static_cast<const __nv_bfloat16 *>(h->wpack);
-    __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(out);
+    // 16-bit elements (bf16 or fp16): pointer arithmetic only
+    const uint16_t *xb = static_cast<const uint16_t *>(x);
+    const uint16_t *wb = static_cast<const uint16_t *>(h->wpack);
+    uint16_t *ob = static_cast<uint16_t *>(out);
     for (int g = 0; g < d.groups; ++g) {
         // the offset groups of this weight group's channels
         const int og_base = g * Cg / Cq;
@@ -250,7 +255,9 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
             const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p.K) * 2};
             const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(n)};
             const cuuint32_t estride[2] = {1, 1};
-            CUresult r = h->encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            CUresult r = h->encode_tiled(&map,
+                                         dtype == DCN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                                          const_cast<void *>(q.wpack), gdim, gstride, box, estride,
                                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -343,7 +350,7 @@ dcn_status_t dcn_destroy(dcn_handle_t h) {
 dcn_status_t dcn_pack_weight(dcn_handle_t h, const void *weight, int O, int C, int kh, int kw,
                              int dtype, void *stream) {
     if (!h || !weight) return DCN_ERR_INVALID_ARG;
-    if (dtype != DCN_F32 && dtype != DCN_BF16) return DCN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
     if (O <= 0 || C <= 0 || kh <= 0 || kw <= 0) return DCN_ERR_INVALID_ARG;
     if (static_cast<long long>(O) * C * kh * kw > kIndexLimit) return DCN_ERR_INVALID_ARG;
     if (!aligned(weight, esize(dtype))) return DCN_ERR_INVALID_ARG;
@@ -395,7 +402,7 @@ static dcn_status_t forward_general(dcn_handle_t h, const void *x, const float *
     if (st != DCN_OK) return st;
     // a forced tensor-core path that cannot run this shape launches nothing
     if (h->path == DCN_PATH_TC &&
-        !(dtype == DCN_BF16 && tc_general_ok(c) && aligned(x, 32) && aligned(out, 16)))
+        !(tc_dtype(dtype) && tc_general_ok(c) && aligned(x, 32) && aligned(out, 16)))
         return DCN_ERR_UNSUPPORTED;
     cudaStream_t s = as_stream(stream);
     st = pack_impl(h, weight, c, dtype, s);

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace dcn {
 
@@ -217,9 +218,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
+// The same with fp16 A and B (format 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+    return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+__device__ __forceinline__ void mma_kind_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -230,9 +235,9 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.  A occupies TMEM
-// lanes 0..M-1 (row m in lane m) and K/2 columns from a_tmem, two bf16 per
+// lanes 0..M-1 (row m in lane m) and K/2 columns from a_tmem, two 16-bit values per
 // 32-bit column, the even k in the low half.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+__device__ __forceinline__ void mma_kind_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -315,6 +320,13 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t v) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
     return pack_bf16x2(lo, hi);
 }
+// The same rounding to an fp16x2 word.
+__device__ __forceinline__ uint32_t f2_to_f16x2(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
 
 // bf16x2 arithmetic on 32-bit words (low half = first element); each op
 // rounds once, to nearest even.
@@ -336,5 +348,55 @@ __device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t 
 // The two bf16 halves of a 32-bit word as fp32 (exact).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// fp16x2 counterparts (low half = first element; one rounding per op).
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint32_t f16x2_splat(float v) {
+    __half2 r = __float2half2_rn(v);
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// The 16-bit operand type of the tensor-core path: bf16 or fp16.  Both
+// feed tcgen05.mma kind::f16 (A and B of one type) with fp32 accumulation.
+template <bool kF16> struct Elem16;
+template <> struct Elem16<false> {   // bf16
+    __device__ static uint32_t splat(float v) { return bf16x2_splat(v); }
+    __device__ static uint32_t mul(uint32_t a, uint32_t b) { return bf16x2_mul(a, b); }
+    __device__ static uint32_t fma(uint32_t a, uint32_t b, uint32_t c) { return bf16x2_fma(a, b, c); }
+    __device__ static float lo(uint32_t w) { return bf16_lo(w); }
+    __device__ static float hi(uint32_t w) { return bf16_hi(w); }
+    __device__ static uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+    __device__ static uint32_t pack_f2(uint64_t v) { return f2_to_bf16x2(v); }
+    __host__ __device__ static constexpr uint32_t idesc(uint32_t M, uint32_t N) { return idesc_bf16_f32(M, N); }
+};
+template <> struct Elem16<true> {    // fp16
+    __device__ static uint32_t splat(float v) { return f16x2_splat(v); }
+    __device__ static uint32_t mul(uint32_t a, uint32_t b) { return f16x2_mul(a, b); }
+    __device__ static uint32_t fma(uint32_t a, uint32_t b, uint32_t c) { return f16x2_fma(a, b, c); }
+    __device__ static float lo(uint32_t w) { return f16_lo(w); }
+    __device__ static float hi(uint32_t w) { return f16_hi(w); }
+    __device__ static uint32_t pack(float lo, float hi) { return pack_f16x2(lo, hi); }
+    __device__ static uint32_t pack_f2(uint64_t v) { return f2_to_f16x2(v); }
+    __host__ __device__ static constexpr uint32_t idesc(uint32_t M, uint32_t N) { return idesc_f16_f32(M, N); }
+};
 
 }  // namespace dcn

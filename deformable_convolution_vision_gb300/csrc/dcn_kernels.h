@@ -38,7 +38,8 @@ struct Params {
     int off_bstride, mask_bstride;
     unsigned *status;     // device status word (timeout bit)
     unsigned long long timeout_ns;  // bound of every barrier wait
-    int sample_f32;       // tensor-core path: 1 = fp32 bilinear combine, 0 = bf16
+    int sample_f32;       // tensor-core path: 1 = fp32 bilinear combine, 0 = operand type
+    int f16;              // tensor-core path: 1 = fp16 operands, 0 = bf16
     // tensor-core path, stream-K scheduling (partial == nullptr: one tile per CTA)
     float *partial;       // fp32 partial tiles, one [O/16][128][16] slot per CTA
     unsigned *flags;      // one word per CTA: set to `epoch` once its partial is stored
@@ -58,27 +59,27 @@ __host__ __device__ constexpr int tc_channel_perm(int c) {
     return (c & ~0x3C) | ((c & 0x0C) << 2) | ((c & 0x30) >> 2);
 }
 
-enum Dtype { kF32 = 0, kBF16 = 1 };
+enum Dtype { kF32 = 0, kBF16 = 1, kF16 = 2 };
 
 // S0: weight [O, Cg, kh, kw] -> packed [O][(i*kw + j)*Cg + c'], where
 // c' = c, or c' = tc_channel_perm(c) with perm != 0 (Cg % 64 == 0 only).
 cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int Cg, int kh, int kw,
                                int dtype, int perm, cudaStream_t stream);
 
-// CUDA-core fused sample + contraction + epilogue (fp32 or bf16 operands).
+// CUDA-core fused sample + contraction + epilogue (fp32, bf16 or fp16 operands).
 cudaError_t launch_simt(const Params &p, int dtype, cudaStream_t stream);
 
-// tcgen05 fused implicit GEMM (bf16 operands), one launch = one weight
-// group x one chunk of its output channels (see Params).  `wmap` is a 2-D
-// tensor map over the chunk's rows of the packed bf16 weight, box {64, O},
-// 128-byte swizzle.
+// tcgen05 fused implicit GEMM (bf16 or fp16 operands, Params::f16), one
+// launch = one weight group x one chunk of its output channels (see
+// Params).  `wmap` is a 2-D tensor map over the chunk's rows of the packed
+// 16-bit weight, box {64, O}, 128-byte swizzle.
 //   tc_supported: the channel and output counts of one launch;
 //   tc_max_virtual_taps: bound on kh*kw*og_count (a per-CTA table).
 bool tc_supported(int C, int O);
 constexpr int tc_max_virtual_taps = 512;
 // Whether a weight whose groups have Cg channels is packed in
-// tc_channel_perm order (bf16 and whole 64-channel blocks).
-inline bool tc_pack_permuted(int dtype, int Cg) { return dtype == kBF16 && Cg % 64 == 0; }
+// tc_channel_perm order (a 16-bit type and whole 64-channel blocks).
+inline bool tc_pack_permuted(int dtype, int Cg) { return (dtype == kBF16 || dtype == kF16) && Cg % 64 == 0; }
 cudaError_t launch_tc(const Params &p, const CUtensorMap &wmap, cudaStream_t stream);
 
 // One-thread kernel whose barrier wait runs out after timeout_ns.

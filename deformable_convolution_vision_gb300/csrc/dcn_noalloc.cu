@@ -84,7 +84,7 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     const void *x, const float *offset, const float *mask, const void *weight, const float *bias,
     void *out, int B, int C, int H, int W, int O, int kh, int kw, int pad, int dtype, void *stream) {
     // the same argument rules as dcn_forward
-    if (dtype != DCN_F32 && dtype != DCN_BF16) return DCN_ERR_INVALID_ARG;
+    if (dtype != DCN_F32 && dtype != DCN_BF16 && dtype != DCN_F16) return DCN_ERR_INVALID_ARG;
     if (B <= 0 || C <= 0 || H <= 0 || W <= 0 || O <= 0 || kh <= 0 || kw <= 0 || pad < 0)
         return DCN_ERR_INVALID_ARG;
     const long long Ho = static_cast<long long>(H) + 2ll * pad - kh + 1;
@@ -135,6 +135,7 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.status = s->status;
     p.timeout_ns = kWaitLimitNs;
     p.sample_f32 = 0;
+    p.f16 = dtype == DCN_F16 ? 1 : 0;
     p.partial = nullptr;   // no stream-K workspace: one tile per CTA
     p.flags = nullptr;
     p.epoch = 0;
@@ -142,7 +143,7 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.units_per_cta = 0;
     p.wperm = perm;
 
-    const bool tc = dtype == DCN_BF16 && perm && dcn::tc_supported(C, O) && is_aligned(x, 32) &&
+    const bool tc = (dtype == DCN_BF16 || dtype == DCN_F16) && perm && dcn::tc_supported(C, O) && is_aligned(x, 32) &&
                     is_aligned(out, 16) && kh * kw <= dcn::tc_max_virtual_taps;
     cudaError_t e;
     if (tc) {
@@ -152,7 +153,9 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
         const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p.K) * 2};
         const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(O)};
         const cuuint32_t estride[2] = {1, 1};
-        if (s->encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s->wpack, gdim, gstride, box,
+        if (s->encode_tiled(&map,
+                            dtype == DCN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s->wpack, gdim, gstride, box,
                             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)

@@ -2,13 +2,14 @@
 //
 // The CUDA-core kernel is the path for fp32 operands (no TF32 anywhere: the
 // "deformops 3.0.1" page, section "Deformable convolution", keeps TF32 out
-// of the contraction) and for bf16 shapes outside the tensor-core kernel's
-// envelope.  It is an implicit GEMM on FFMA: per tap, the CTA computes the
+// of the contraction) and for bf16 / fp16 shapes outside the tensor-core
+// kernel's envelope.  It is an implicit GEMM on FFMA: per tap, the CTA computes the
 // four corner weights of its 64 pixels once, then for each chunk of 16
 // channels samples a [16 x 64] operand tile into shared memory, stages the
 // matching [16 x 64] weight tile, and accumulates a 4 x 4 register tile per
 // thread.  The sampled tile is never written to global memory.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "dcn_kernels.h"
 #include "dcn_sampling.cuh"
@@ -22,12 +23,14 @@ template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; 
 template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
     return __bfloat162float(v);
 }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
 
 template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
     return __float2bfloat16_rn(v);
 }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
 
 // S0: out[o][(i*kw + j)*C + c] = w[o][c'][i][j] with c' = c, or with
 // c' = tc_channel_perm(c) for the tensor-core operand order.  One thread
@@ -211,8 +214,9 @@ cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int C, in
         pack_weight_kernel<float><<<grid, threads, 0, stream>>>(
             static_cast<const float *>(weight), static_cast<float *>(wpack), O, C, kh, kw, perm);
     } else {
-        pack_weight_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(
-            static_cast<const __nv_bfloat16 *>(weight), static_cast<__nv_bfloat16 *>(wpack),
+        // bf16 and fp16: the permutation moves 16-bit words
+        pack_weight_kernel<uint16_t><<<grid, threads, 0, stream>>>(
+            static_cast<const uint16_t *>(weight), static_cast<uint16_t *>(wpack),
             O, C, kh, kw, perm);
     }
     return cudaGetLastError();
@@ -222,6 +226,8 @@ cudaError_t launch_simt(const Params &p, int dtype, cudaStream_t stream) {
     dim3 grid((p.P + SIMT_BM - 1) / SIMT_BM, (p.O + SIMT_BN - 1) / SIMT_BN);
     if (dtype == kF32)
         dcn_simt_kernel<float><<<grid, SIMT_THREADS, 0, stream>>>(p);
+    else if (dtype == kF16)
+        dcn_simt_kernel<__half><<<grid, SIMT_THREADS, 0, stream>>>(p);
     else
         dcn_simt_kernel<__nv_bfloat16><<<grid, SIMT_THREADS, 0, stream>>>(p);
     return cudaGetLastError();

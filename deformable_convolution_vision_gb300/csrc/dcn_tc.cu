@@ -1,5 +1,5 @@
-// tcgen05 fused implicit-GEMM forward kernel (bf16 operands, fp32 TMEM
-// accumulation) for sm_103a.
+// tcgen05 fused implicit-GEMM forward kernel (bf16 or fp16 operands, fp32
+// TMEM accumulation) for sm_103a.
 //
 // The contraction out[p, o] = sum_K A[p, K] * Wp[o, K] with K = (tap, c) is
 // a dense GEMM whose A operand is never materialised in memory: the im2col
@@ -25,12 +25,12 @@
 //               it computes the corner weights and addresses (S1, S2); per
 //               K-block each lane gathers 16 channels of two pixels: eight
 //               32-byte corner loads, the bilinear combine (by default in
-//               the input dtype, bf16, as packed bf16x2 FMAs; optionally in
-//               fp32 with packed f32x2 FMAs) and one 16x256b store of both
+//               the input dtype, as packed bf16x2 / fp16x2 FMAs; optionally
+//               in fp32 with packed f32x2 FMAs) and one 16x256b store of both
 //               pixels' rows into the stage's TMEM columns (S3).  After a
 //               tile's last K-block all sixteen run the epilogue (S5): TMEM
-//               -> registers, + bias in fp32, bf16 round, channels-last
-//               store.
+//               -> registers, + bias in fp32, rounding to the operand type,
+//               channels-last store.
 // K-blocks run tap-major with 64 channels each, so a tap's corner geometry
 // is computed once and reused for all of its channel blocks.  The geometry
 // of two taps at a time is computed by all 32 lanes of a warp into a ring
@@ -81,7 +81,7 @@ static_assert(TC_TABLE_SLOTS == 4, "ring index arithmetic assumes four slots");
 // Per-warp corner table of one tap: arrays of 16-byte rows, one row per
 // pixel of the warp's tile row (conflict-free writes, broadcast reads).
 // The fp32 combine keeps the weights as duplicated fp32 pairs
-// {w0,w0,w1,w1}, {w2,w2,w3,w3}; the bf16 combine as four bf16x2 pairs.
+// {w0,w0,w1,w1}, {w2,w2,w3,w3}; the 16-bit combine as four duplicated pairs.
 // Then the four corner indices.
 constexpr int TC_TABLE_ARRAY_BYTES = TC_TILE_W * 16;
 constexpr int TC_TABLE_W01 = 0;
@@ -158,9 +158,10 @@ __device__ __forceinline__ float4 ld_cg_f4(const float *p) {
     return __ldcg(reinterpret_cast<const float4 *>(p));
 }
 
-template <bool kSampleF32>
+template <bool kSampleF32, bool kF16>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
+    using E = Elem16<kF16>;   // the 16-bit operand type: its packed arithmetic and MMA format
     constexpr int kBuf = table_buf_bytes(kSampleF32);
     constexpr int kIdx = table_idx_off(kSampleF32);
     extern __shared__ uint8_t smem_raw[];
@@ -255,7 +256,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(TC_BM, p.O);
+            const uint32_t idesc = E::idesc(TC_BM, p.O);
             int s = 0;
             uint32_t phase = 0;
             int segs = 0;
@@ -279,7 +280,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                         // K=16 steps: 8 TMEM columns of A, 32 bytes of the
                         // swizzled B rows; the segment's first MMA
                         // overwrites the accumulator
-                        mma_bf16_ts(d_tmem, a_tmem + ks * (TC_MMA_K / 2), bdesc + 2 * ks, idesc,
+                        mma_kind_f16_ts(d_tmem, a_tmem + ks * (TC_MMA_K / 2), bdesc + 2 * ks, idesc,
                                     (kb > sg.kb0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(empty0 + 8 * s);
@@ -303,7 +304,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         const int q = warp & 3;                          // TMEM lane quarter this warp may access
         const int half = (sw % TC_TEAM_WARPS) / 4;       // which 16 lanes of the quarter
         const int trow = 2 * q + half;                   // its tile row = A rows 16 trow .. +15
-        const __nv_bfloat16 *__restrict__ x = static_cast<const __nv_bfloat16 *>(p.x);
+        const uint16_t *__restrict__ x = static_cast<const uint16_t *>(p.x);   // 16-bit elements
         uint8_t *table = smem + L.table_off + sw * TC_TABLE_SLOTS * kBuf;
         const uint32_t table_s = smem_u32(table);
         const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * 3 * 32 * 4) + lane * 4;
@@ -376,7 +377,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                             }
                         }
                     }
-                    __nv_bfloat16 *__restrict__ out = static_cast<__nv_bfloat16 *>(p.out);
+                    uint16_t *__restrict__ out = static_cast<uint16_t *>(p.out);
                     for (int ch = ch_begin; ch < ch_end; ++ch) {
                         float vv[16];
                         tmem_ld16(tmem_base + acc_lane + ch * 16, vv);
@@ -395,7 +396,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                                 const int o = ch * 16 + 2 * e;
                                 const float b0 = p.bias ? __ldg(p.bias + o) : 0.0f;
                                 const float b1 = p.bias ? __ldg(p.bias + o + 1) : 0.0f;
-                                pk[e] = pack_bf16x2(vv[2 * e] + b0, vv[2 * e + 1] + b1);
+                                pk[e] = E::pack(vv[2 * e] + b0, vv[2 * e + 1] + b1);
                             }
                             uint4 *dst = reinterpret_cast<uint4 *>(out + pix * p.out_stride + ch * 16);
                             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -483,10 +484,10 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                         *reinterpret_cast<float4 *>(slot + TC_TABLE_W01 + rowb) = make_float4(t.w[0], t.w[0], t.w[1], t.w[1]);
                         *reinterpret_cast<float4 *>(slot + TC_TABLE_W23 + rowb) = make_float4(t.w[2], t.w[2], t.w[3], t.w[3]);
                     } else {
-                        // the weights rounded to bf16, each duplicated into a bf16x2 pair
+                        // the weights rounded to the operand type, each duplicated into a pair
                         *reinterpret_cast<uint4 *>(slot + TC_TABLE_W01 + rowb) =
-                            make_uint4(bf16x2_splat(t.w[0]), bf16x2_splat(t.w[1]), bf16x2_splat(t.w[2]),
-                                       bf16x2_splat(t.w[3]));
+                            make_uint4(E::splat(t.w[0]), E::splat(t.w[1]), E::splat(t.w[2]),
+                                       E::splat(t.w[3]));
                     }
                     *reinterpret_cast<int4 *>(slot + kIdx + rowb) = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
                 };
@@ -497,7 +498,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 // the four 32-byte corner loads of one of this lane's two pixels
                 // from a table slot; corners outside the image read a clamped
                 // in-image address and carry weight 0
-                auto issue_px = [&](int px, uint32_t slot, const __nv_bfloat16 *xc, u32x8 (&v)[8]) {
+                auto issue_px = [&](int px, uint32_t slot, const uint16_t *xc, u32x8 (&v)[8]) {
                     const int4 ci = lds_v4_s32(slot + kIdx + (px ? r_off1 : r_off0));
                     v[4 * px + 0] = ldg_v8(xc + ci.x);
                     v[4 * px + 1] = ldg_v8(xc + ci.y);
@@ -561,22 +562,22 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
 #pragma unroll
                             for (int m = 0; m < 8; ++m) {
                                 // channels 2m, 2m+1: w0*x00 + w1*x01 + w2*x10 + w3*x11 in fp32
-                                uint64_t acc = f2_mul(c0, f2_make(bf16_lo(vp[0].w[m]), bf16_hi(vp[0].w[m])));
-                                acc = f2_fma(c1, f2_make(bf16_lo(vp[1].w[m]), bf16_hi(vp[1].w[m])), acc);
-                                acc = f2_fma(c2, f2_make(bf16_lo(vp[2].w[m]), bf16_hi(vp[2].w[m])), acc);
-                                acc = f2_fma(c3, f2_make(bf16_lo(vp[3].w[m]), bf16_hi(vp[3].w[m])), acc);
-                                w[4 * (m >> 1) + 2 * px + (m & 1)] = f2_to_bf16x2(acc);
+                                uint64_t acc = f2_mul(c0, f2_make(E::lo(vp[0].w[m]), E::hi(vp[0].w[m])));
+                                acc = f2_fma(c1, f2_make(E::lo(vp[1].w[m]), E::hi(vp[1].w[m])), acc);
+                                acc = f2_fma(c2, f2_make(E::lo(vp[2].w[m]), E::hi(vp[2].w[m])), acc);
+                                acc = f2_fma(c3, f2_make(E::lo(vp[3].w[m]), E::hi(vp[3].w[m])), acc);
+                                w[4 * (m >> 1) + 2 * px + (m & 1)] = E::pack_f2(acc);
                             }
                         } else {
-                            // the same sum in the input dtype: bf16 weights, one bf16
+                            // the same sum in the input dtype: 16-bit weights, one
                             // rounding per fused multiply-add, two channels per op
                             const int4 cw = lds_v4_s32(cur_slot + TC_TABLE_W01 + ro);
 #pragma unroll
                             for (int m = 0; m < 8; ++m) {
-                                uint32_t acc = bf16x2_mul(cw.x, vp[0].w[m]);
-                                acc = bf16x2_fma(cw.y, vp[1].w[m], acc);
-                                acc = bf16x2_fma(cw.z, vp[2].w[m], acc);
-                                acc = bf16x2_fma(cw.w, vp[3].w[m], acc);
+                                uint32_t acc = E::mul(cw.x, vp[0].w[m]);
+                                acc = E::fma(cw.y, vp[1].w[m], acc);
+                                acc = E::fma(cw.z, vp[2].w[m], acc);
+                                acc = E::fma(cw.w, vp[3].w[m], acc);
                                 w[4 * (m >> 1) + 2 * px + (m & 1)] = acc;
                             }
                         }
@@ -627,8 +628,9 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     }
 }
 
-int g_max_smem_set = 0;
-int g_max_smem_set_f32 = 0;
+// The dynamic shared-memory size last set on each instantiation
+// [fp32 combine][fp16 operands].
+int g_max_smem_set[2][2] = {{0, 0}, {0, 0}};
 
 // Carveout preference (percent of the 228 KB maximum) that selects the
 // smallest supported shared-memory size holding `needed` bytes; the driver
@@ -678,8 +680,10 @@ cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t 
     if (stages < 4 && tmem_fits(4) && smem_for(4) <= DCN_TC_SMEM_WIDE_BUDGET) stages = 4;
     const TcLayout L = tc_layout(p.O, stages, f32, vtaps);
     const int smem = L.total + 1024;  // slack for 1024-byte alignment
-    auto kernel = f32 ? dcn_tc_kernel<true> : dcn_tc_kernel<false>;
-    int &smem_set = f32 ? g_max_smem_set_f32 : g_max_smem_set;
+    const bool f16 = p.f16 != 0;
+    auto kernel = f32 ? (f16 ? dcn_tc_kernel<true, true> : dcn_tc_kernel<true, false>)
+                      : (f16 ? dcn_tc_kernel<false, true> : dcn_tc_kernel<false, false>);
+    int &smem_set = g_max_smem_set[f32 ? 1 : 0][f16 ? 1 : 0];
     if (smem != smem_set) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;

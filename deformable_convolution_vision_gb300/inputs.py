@@ -33,7 +33,7 @@ class Workload:
     kh: int
     kw: int
     pad: int
-    dtype: str            # "f32" or "bf16": dtype of x, weight and out
+    dtype: str            # "f32", "bf16" or "f16": dtype of x, weight and out
     offset_std: float
     mask: str             # "sigmoid", "uniform", "uniform_zero10", "uniform2", "none"
     weight_std: float     # 0 -> 1/sqrt(kh*kw*C)
@@ -83,7 +83,7 @@ WORKLOADS = {
 # The five measured workloads, in order.
 MAIN = ["tiny", "decoder3x3", "aspp7x7", "backbone3x3", "boundary5x5"]
 
-TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 def make_inputs(wl: Workload, seed=None):

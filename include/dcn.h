@@ -29,12 +29,13 @@
  * Numerics: sampling coordinates and corner weights are fp32.  The bilinear
  * combine of the four corners runs in the input dtype by default, as the
  * page's own gather decomposition does (its corner weights and sums are in
- * x.dtype): for bf16 the weights are rounded to bf16 and each fused
- * multiply-add rounds once to bf16; dcn_set_sample_precision selects an
- * fp32 combine instead.  The contraction accumulates in fp32 for both
- * dtypes (no TF32).  The bf16 path rounds each interpolated sample to bf16
- * before the tensor-core contraction and rounds the fp32 result (after
- * bias) to bf16 at the end.
+ * x.dtype): for bf16 (fp16) the weights are rounded to bf16 (fp16) and
+ * each fused multiply-add rounds once to that type; dcn_set_sample_precision
+ * selects an fp32 combine instead.  The contraction accumulates in fp32 for
+ * every dtype (no TF32).  The 16-bit paths round each interpolated sample to
+ * the operand type before the tensor-core contraction and round the fp32
+ * result (after bias) to it at the end.  fp16 has the narrower range: the
+ * caller keeps inputs, samples and outputs inside it (|v| < 65504).
  *
  * Ownership: the caller owns every tensor and the stream.  A handle owns a
  * small device workspace (the packed weight, a status word and, for
@@ -65,7 +66,8 @@ typedef struct dcn_handle_s *dcn_handle_t;
 /* Element type of x, weight and out. */
 typedef enum {
     DCN_F32 = 0,   /* fp32 operands, CUDA-core FFMA path */
-    DCN_BF16 = 1   /* bf16 operands, tcgen05 tensor-core path where the shape allows */
+    DCN_BF16 = 1,  /* bf16 operands, tcgen05 tensor-core path where the shape allows */
+    DCN_F16 = 2    /* fp16 operands, the same paths as bf16 (tcgen05 kind::f16 with fp16 A and B) */
 } dcn_dtype_t;
 
 typedef enum {
@@ -78,14 +80,14 @@ typedef enum {
     DCN_ERR_TIMEOUT = 6       /* a device-side bounded wait ran out (reported by dcn_sync_status) */
 } dcn_status_t;
 
-/* Kernel selection for bf16.  AUTO takes the tcgen05 path when
+/* Kernel selection for bf16 and fp16.  AUTO takes the tcgen05 path when
  * C % 64 == 0, O % 16 == 0, 16 <= O <= 256, x is 32-byte aligned and out is
  * 16-byte aligned, and the CUDA-core path otherwise.  fp32 always takes the
  * CUDA-core path.  (dcn_forward_ex states its own conditions.) */
 typedef enum {
     DCN_PATH_AUTO = 0,
     DCN_PATH_SIMT = 1,   /* CUDA-core fused sample + FFMA contraction */
-    DCN_PATH_TC = 2      /* tcgen05 fused implicit GEMM (bf16 only) */
+    DCN_PATH_TC = 2      /* tcgen05 fused implicit GEMM (bf16 or fp16) */
 } dcn_path_t;
 
 /* Create a handle on the current CUDA device.  Returns DCN_ERR_NO_DEVICE
@@ -112,8 +114,8 @@ DCN_API dcn_status_t dcn_forward(dcn_handle_t h,
 
 /* The two halves of dcn_forward, for callers that reuse one weight.
  * dcn_pack_weight reorders weight [O,C,kh,kw] into the handle's workspace
- * as [O][(i*kw + j)*C + c] (tap-major, channel-minor).  For bf16 shapes
- * the tensor-core kernel accepts, the channels inside each 64-channel
+ * as [O][(i*kw + j)*C + c] (tap-major, channel-minor).  For bf16 and fp16
+ * shapes the tensor-core kernel accepts, the channels inside each 64-channel
  * block are in that kernel's operand order instead; the workspace is
  * private to the handle and either kernel reads it correctly.
  * dcn_forward_packed then runs the fused kernel with that packed weight;
@@ -138,10 +140,10 @@ DCN_API dcn_status_t dcn_forward_host(dcn_handle_t h,
                               int B, int C, int H, int W, int O,
                               int kh, int kw, int pad, int dtype, void *stream);
 
-/* Precision of the bilinear combine on the bf16 tensor-core path. */
+/* Precision of the bilinear combine on the 16-bit tensor-core path. */
 typedef enum {
-    DCN_SAMPLE_INPUT_DTYPE = 0,  /* default: bf16 weights and bf16 fused multiply-adds */
-    DCN_SAMPLE_F32 = 1           /* fp32 weights and fp32 sums, then one bf16 rounding */
+    DCN_SAMPLE_INPUT_DTYPE = 0,  /* default: weights and fused multiply-adds in the operand type */
+    DCN_SAMPLE_F32 = 1           /* fp32 weights and fp32 sums, then one rounding to the operand type */
 } dcn_sample_t;
 
 /* Choose the combine precision (dcn_sample_t) for later calls on this
@@ -244,7 +246,7 @@ DCN_API int dcn_out_size(int n, int k, int stride, int pad, int dil);
 
 /* dcn_forward for the general form.  Argument rules as dcn_forward, plus
  * the descriptor's (its fields as commented; every size product below
- * 2^31).  AUTO takes the tcgen05 path for bf16 when, with Cg = C/groups,
+ * 2^31).  AUTO takes the tcgen05 path for bf16 and fp16 when, with Cg = C/groups,
  * Og = O/groups, Cq = C/offset_groups: Cg % 64 == 0, Cq % 64 == 0, one of
  * Cg and Cq divides the other, Og % 16 == 0, kh*kw*max(1, Cg/Cq) <= 512,
  * x is 32-byte and out 16-byte aligned; it runs one launch per weight group

@@ -5,7 +5,11 @@ err = max|gpu - ref| / max|ref| over the compared outputs."""
 import numpy as np
 import torch
 
-TOL = {"f32": 1e-4, "bf16": 2e-2}
+# fp32 and bf16: the spec bars.  fp16 keeps the bf16 bar's form but
+# scales it by the ratio of unit roundoffs, 2^-11 / 2^-8 = 1/8 (every
+# rounding on the path -- corner weights, combine, sample, output -- is one
+# unit roundoff of the operand type), with a factor 2 of margin: 2e-2 / 4.
+TOL = {"f32": 1e-4, "bf16": 2e-2, "f16": 5e-3}
 
 
 def to_device(inp, device="cuda"):
