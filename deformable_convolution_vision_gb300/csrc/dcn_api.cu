@@ -163,9 +163,11 @@ dcn_status_t next_epoch(dcn_handle_t h, cudaStream_t s, unsigned *epoch) {
     return DCN_OK;
 }
 
+// after_pack: this call's pack_impl launched the weight pack just before, on
+// the same stream (the first tensor-core launch then overlaps it).
 dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *offset,
                                  const float *mask, const float *bias, void *out, const Conv &c,
-                                 int dtype, cudaStream_t s) {
+                                 int dtype, cudaStream_t s, bool after_pack = false) {
     const dcn_conv_desc_t &d = c.d;
     if (h->pk_O != d.O || h->pk_Cg != c.Cg() || h->pk_kh != d.kh || h->pk_kw != d.kw ||
         h->pk_dtype != dtype)
@@ -217,9 +219,13 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
     const int chunk_max = Og < 256 ? Og : 256;
     const size_t part_bytes = static_cast<size_t>(h->sm_count) * 128 * chunk_max * sizeof(float);
     const size_t flag_bytes = static_cast<size_t>(h->sm_count + 1) * sizeof(unsigned);
+    // a workspace (re)allocation or clear puts stream work between the pack
+    // and the first launch, which then is an ordinary one
+    if (h->partial_cap < part_bytes || !h->partial) after_pack = false;
     dcn_status_t st = ensure(&h->partial, &h->partial_cap, part_bytes, s);
     if (st != DCN_OK) return st;
     if (h->flags_cap < flag_bytes || !h->flags) {
+        after_pack = false;
         st = ensure(&h->flags, &h->flags_cap, flag_bytes, s);
         if (st != DCN_OK) return st;
         if (cudaMemsetAsync(h->flags, 0, h->flags_cap, s) != cudaSuccess) return DCN_ERR_CUDA;
@@ -265,9 +271,12 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
             if (r != CUDA_SUCCESS) return DCN_ERR_CUDA;
             q.partial = static_cast<float *>(h->partial);
             q.flags = static_cast<unsigned *>(h->flags);
+            if (h->epoch + 1 == 0) after_pack = false;   // the wrap clears the flags first
             st = next_epoch(h, s, &q.epoch);
             if (st != DCN_OK) return st;
-            if (dcn::launch_tc(q, map, s) != cudaSuccess) return DCN_ERR_CUDA;
+            // only the first launch directly follows the pack
+            if (dcn::launch_tc(q, map, s, after_pack && g == 0 && o0 == 0) != cudaSuccess)
+                return DCN_ERR_CUDA;
         }
     }
     h->last_path = path;
@@ -407,7 +416,7 @@ static dcn_status_t forward_general(dcn_handle_t h, const void *x, const float *
     cudaStream_t s = as_stream(stream);
     st = pack_impl(h, weight, c, dtype, s);
     if (st != DCN_OK) return st;
-    return forward_packed_impl(h, x, offset, mask, bias, out, c, dtype, s);
+    return forward_packed_impl(h, x, offset, mask, bias, out, c, dtype, s, true);
 }
 
 dcn_status_t dcn_forward(dcn_handle_t h, const void *x, const float *offset, const float *mask,

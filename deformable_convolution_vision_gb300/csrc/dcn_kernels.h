@@ -80,7 +80,13 @@ constexpr int tc_max_virtual_taps = 512;
 // Whether a weight whose groups have Cg channels is packed in
 // tc_channel_perm order (a 16-bit type and whole 64-channel blocks).
 inline bool tc_pack_permuted(int dtype, int Cg) { return (dtype == kBF16 || dtype == kF16) && Cg % 64 == 0; }
-cudaError_t launch_tc(const Params &p, const CUtensorMap &wmap, cudaStream_t stream);
+// after_pack: the launch directly follows this call's launch_pack_weight on
+// the same stream.  It is then a programmatic dependent launch: the CTAs
+// start while the pack runs (the pack lets them launch at once) and only the
+// weight loads wait for the pack to finish (griddepcontrol.wait); x, offset
+// and mask were complete before the pack started.
+cudaError_t launch_tc(const Params &p, const CUtensorMap &wmap, cudaStream_t stream,
+                      bool after_pack = false);
 
 // One-thread kernel whose barrier wait runs out after timeout_ns.
 cudaError_t launch_selftest_timeout(unsigned *status, unsigned long long timeout_ns,

@@ -41,6 +41,9 @@ template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return
 template <typename T>
 __global__ void pack_weight_kernel(const T *__restrict__ w, T *__restrict__ wp,
                                    int O, int C, int kh, int kw, int perm) {
+    // a forward kernel launched as this one's programmatic dependent may
+    // start now; it waits for this grid's completion before it reads wp
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int K = kh * kw * C;
     const int kk = blockIdx.x * blockDim.x + threadIdx.x;
     if (kk >= K) return;

@@ -238,6 +238,10 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             int s = 0;
             uint32_t phase = 0;
             int kb = u_begin % nkb;
+            // The packed weight may still be in the making when this grid
+            // was launched as the pack's programmatic dependent: wait for
+            // that grid to complete (a no-op for an ordinary launch).
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int u = u_begin; u < u_end; ++u) {
                 if (!mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns)) break;
                 const uint32_t b_dst = smem_u32(smem + s * L.b_bytes);
@@ -654,13 +658,43 @@ int carveout_percent(int needed) {
 #define DCN_TC_SMEM_WIDE_BUDGET (164 * 1024)
 #endif
 
+// Launch with the cooperative attribute (all CTAs co-resident, for the
+// stream-K flags) and/or as a programmatic dependent of the previous kernel.
+template <typename Kernel>
+cudaError_t launch_ex(Kernel kernel, int grid, int smem, cudaStream_t stream, bool cooperative,
+                      bool dependent, const CUtensorMap &wmap, const Params &p, int stages) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    if (dependent) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, wmap, p, stages);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e;
+}
+
 }  // namespace
 
 bool tc_supported(int C, int O) {
     return C % TC_BK == 0 && O % 16 == 0 && O >= 16 && O <= 256;
 }
 
-cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t stream) {
+cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t stream,
+                      bool after_pack) {
     // One CTA per SM.  Its shared memory is kept small so that most of the
     // SM's L1/shared array stays L1 cache, which holds a good part of the
     // tile's corner footprint across taps.
@@ -704,17 +738,13 @@ cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t 
         const int units = static_cast<int>((total + p.sm_count - 1) / p.sm_count);
         p.units_per_cta = units;
         const int grid = static_cast<int>((total + units - 1) / units);
-        void *args[] = {const_cast<CUtensorMap *>(&wmap), &p, &stages};
-        const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kernel),
-                                                          dim3(grid), dim3(TC_THREADS), args, smem,
-                                                          stream);
+        const cudaError_t e = launch_ex(kernel, grid, smem, stream, true, after_pack, wmap, p, stages);
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         cudaGetLastError();   // not all CTAs could be resident: one tile per CTA instead
     }
     // one tile per CTA
     p.units_per_cta = nkb;
-    kernel<<<tiles, TC_THREADS, smem, stream>>>(wmap, p, stages);
-    return cudaGetLastError();
+    return launch_ex(kernel, tiles, smem, stream, false, after_pack, wmap, p, stages);
 }
 
 // ------------------------------------------------------------ self-test
