@@ -1,4 +1,5 @@
-"""Oracle for the modulated deformable convolution forward pass.
+"""Oracle for the modulated deformable convolution forward pass and its
+gradients.
 
 TEST INFRASTRUCTURE ONLY.  The plain C definition in ``dcn_oracle.c`` is
 what the CUDA path is checked against.  Only ``tests/``, the smoke check in
@@ -67,6 +68,8 @@ class Oracle:
         lib.oracle_dcn_forward_ex.restype = i
         lib.oracle_dcn_forward_points_ex.argtypes = [f, f, f, f, f, f, i, f, f, i]
         lib.oracle_dcn_forward_points_ex.restype = i
+        lib.oracle_dcn_backward_ex.argtypes = [f] * 10 + [f, i]
+        lib.oracle_dcn_backward_ex.restype = i
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i
         self._lib = lib
@@ -177,6 +180,39 @@ class Oracle:
         return out
 
 
+    # ----------------------------------------------------------- backward
+
+    def backward_ex(self, x, offset, mask, weight, grad_out, conv, nthreads=0):
+        """Gradients of the general problem's forward with respect to x,
+        offset, mask, weight and bias, given grad_out [B, O, Ho, Wo]: a dict
+        of fp64 arrays in the inputs' layouts (grad_mask None without a
+        mask)."""
+        arrs, desc, (B, O, Ho, Wo) = self._prepare_ex(x, offset, mask, weight, None, conv)
+        x, offset, mask, weight, _ = arrs
+        go = self._f32(grad_out)
+        if go.shape != (B, O, Ho, Wo):
+            raise ValueError(f"grad_out shape {go.shape} != {(B, O, Ho, Wo)}")
+        gx = np.empty(x.shape, dtype=np.float64)
+        goff = np.empty(offset.shape, dtype=np.float64)
+        gm = None if mask is None else np.empty(mask.shape, dtype=np.float64)
+        gw = np.empty(weight.shape, dtype=np.float64)
+        gb = np.empty((O,), dtype=np.float64)
+        rc = self._lib.oracle_dcn_backward_ex(
+            self._ptr(x), self._ptr(offset), self._ptr(mask), self._ptr(weight), self._ptr(go),
+            self._ptr(gx), self._ptr(goff), self._ptr(gm), self._ptr(gw), self._ptr(gb),
+            self._ptr(desc), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_dcn_backward_ex rejected its arguments")
+        return {"grad_x": gx, "grad_offset": goff, "grad_mask": gm, "grad_weight": gw,
+                "grad_bias": gb}
+
+    def backward(self, x, offset, mask, weight, grad_out, pad, nthreads=0):
+        """backward_ex for the page-1 problem (stride 1, dilation 1, one
+        padding, one weight group, one offset group)."""
+        return self.backward_ex(x, offset, mask, weight, grad_out, ConvDesc(padding=pad),
+                                nthreads)
+
+
 class ConvDesc:
     """Convolution parameters of the general problem: stride, padding and
     dilation as (h, w) pairs (an int means both), weight groups and offset
@@ -224,3 +260,11 @@ def forward_ex(*args, **kwargs):
 
 def forward_points_ex(*args, **kwargs):
     return get().forward_points_ex(*args, **kwargs)
+
+
+def backward(*args, **kwargs):
+    return get().backward(*args, **kwargs)
+
+
+def backward_ex(*args, **kwargs):
+    return get().backward_ex(*args, **kwargs)

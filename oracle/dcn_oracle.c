@@ -1,5 +1,6 @@
 /*
- * Oracle for the forward pass of modulated deformable convolution.
+ * Oracle for the forward pass of modulated deformable convolution and its
+ * gradients (the backward pass, at the end of this file).
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
  * CPU definition that the CUDA path is checked against.  Only the test suite,
@@ -64,6 +65,8 @@
  */
 #include <math.h>
 #include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -248,4 +251,156 @@ int oracle_max_threads(void)
 #else
     return 1;
 #endif
+}
+
+/* ------------------------------------------------------------------ backward
+ *
+ * The gradients of the forward above with respect to each of its inputs,
+ * given the cotangent grad_out [B, O, Ho, Wo] of its output: the chain rule
+ * applied to the forward's definition, term by term.  (The deformops page,
+ * section "Deformable convolution", has the backward keep fp32 accumulation
+ * and no TF32 so that rounding does not reach the offset gradients; the
+ * definition itself follows from the forward.)  For image b, output pixel
+ * (h, w), tap k = (i, j), offset group q and channel c of q, with m, py, px,
+ * y0, x0, ly, lx, wy, wx and S as in the forward, and
+ *
+ *   gA = sum over the outputs o of c's weight group of
+ *        grad_out[b,o,h,w] * weight[o, c - c0, i, j]     (column gradient)
+ *
+ * the contributions are
+ *
+ *   grad_bias[o]                 += grad_out[b,o,h,w]
+ *   grad_weight[o, c-c0, i, j]   += grad_out[b,o,h,w] * m * S
+ *   grad_mask[b, q*kk + k, h, w] += gA * S
+ *   grad_x[b, c, y0+a, x0+e]     += gA * m * wy_a * wx_e     (inside corners)
+ *   grad_offset[b, 2(q*kk+k), h, w]   += gA * m * dS/dpy
+ *   grad_offset[b, 2(q*kk+k)+1, h, w] += gA * m * dS/dpx
+ *
+ * with kk = kh*kw, dS/dpy = sum over inside corners of (2a-1) * wx_e * x,
+ * dS/dpx = sum over inside corners of (2e-1) * wy_a * x (d wy_1/d py = 1,
+ * d wy_0/d py = -1, likewise for x).  The corner weights are piecewise
+ * linear in the coordinate; at an integer coordinate the derivative is that
+ * of the cell [y0, y0+1) which floor selects (the right-hand derivative).
+ * A sample whose corners are all outside gives 0 to every gradient.
+ *
+ * All sums are fp64 in the fixed order b -> h -> w -> (i, j) -> q -> c ->
+ * o / corner.  Images are independent except for grad_weight and
+ * grad_bias, which are summed per image and then over images in order, so
+ * the result does not depend on the thread count.
+ *
+ * Layouts (host memory): x, offset, mask, weight as in the forward;
+ * grad_out [B, O, Ho, Wo] fp32; results fp64: grad_x [B, C, H, W],
+ * grad_offset like offset, grad_mask like mask (NULL: not computed),
+ * grad_weight like weight, grad_bias [O] (NULL: not computed).
+ */
+int oracle_dcn_backward_ex(const float *x, const float *offset, const float *mask,
+                           const float *weight, const float *grad_out,
+                           double *grad_x, double *grad_offset, double *grad_mask,
+                           double *grad_weight, double *grad_bias,
+                           const int *desc, int nthreads)
+{
+    if (!desc || !grad_out || !grad_x || !grad_offset || !grad_weight) return -1;
+    const oracle_problem p = oracle_make(x, offset, mask, weight, NULL, desc);
+    if (oracle_check(&p)) return -1;
+    const int k_total = p.kh * p.kw;
+    const int Cg = p.C / p.groups, Og = p.O / p.groups, Cq = p.C / p.ogroups;
+    const size_t plane_in = (size_t)p.H * p.W;
+    const size_t plane_out = (size_t)p.Ho * p.Wo;
+    const size_t n_w = (size_t)p.O * Cg * k_total;
+    const size_t per_image = n_w + (size_t)p.O;
+    double *part = (double *)calloc((size_t)p.B * per_image, sizeof(double));
+    if (!part) return -2;
+    memset(grad_x, 0, sizeof(double) * (size_t)p.B * p.C * plane_in);
+    memset(grad_offset, 0, sizeof(double) * (size_t)p.B * 2 * p.ogroups * k_total * plane_out);
+    if (grad_mask)
+        memset(grad_mask, 0, sizeof(double) * (size_t)p.B * p.ogroups * k_total * plane_out);
+    ORACLE_SET_THREADS(nthreads);
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < p.B; ++b) {
+        double *gw = part + (size_t)b * per_image;   /* this image's grad_weight */
+        double *gb = gw + n_w;                        /* and grad_bias */
+        for (int h = 0; h < p.Ho; ++h) {
+            for (int w = 0; w < p.Wo; ++w) {
+                const size_t pix = (size_t)h * p.Wo + w;
+                const float *go = grad_out + (size_t)b * p.O * plane_out + pix;
+                for (int o = 0; o < p.O; ++o) gb[o] += (double)go[o * plane_out];
+                for (int i = 0; i < p.kh; ++i) {
+                    for (int j = 0; j < p.kw; ++j) {
+                        const int k = i * p.kw + j;
+                        for (int q = 0; q < p.ogroups; ++q) {
+                            const size_t oq = (size_t)b * p.ogroups + q;
+                            const float dy = p.offset[(oq * 2 * k_total + 2 * k) * plane_out + pix];
+                            const float dx = p.offset[(oq * 2 * k_total + 2 * k + 1) * plane_out + pix];
+                            const double m = p.mask
+                                ? (double)p.mask[(oq * k_total + k) * plane_out + pix]
+                                : 1.0;
+                            const float py = (float)(h * p.sh - p.ph + i * p.dh) + dy;
+                            const float px = (float)(w * p.sw - p.pw + j * p.dw) + dx;
+                            const float fy0 = floorf(py);
+                            const float fx0 = floorf(px);
+                            const double ly = (double)py - (double)fy0;
+                            const double lx = (double)px - (double)fx0;
+                            const double wy[2] = {1.0 - ly, ly};
+                            const double wx[2] = {1.0 - lx, lx};
+                            double g_dy = 0.0, g_dx = 0.0, g_m = 0.0;
+                            for (int c = q * Cq; c < (q + 1) * Cq; ++c) {
+                                const int g = c / Cg;
+                                const int cl = c - g * Cg;
+                                const float *xc = p.x + ((size_t)b * p.C + c) * plane_in;
+                                double s = 0.0, s_y = 0.0, s_x = 0.0;
+                                for (int a = 0; a < 2; ++a) {
+                                    for (int e = 0; e < 2; ++e) {
+                                        const double yy = (double)fy0 + a;
+                                        const double xx = (double)fx0 + e;
+                                        if (yy >= 0.0 && yy <= p.H - 1 && xx >= 0.0 && xx <= p.W - 1) {
+                                            const double v = (double)xc[(size_t)yy * p.W + (size_t)xx];
+                                            s += wy[a] * wx[e] * v;
+                                            s_y += (a ? 1.0 : -1.0) * wx[e] * v;
+                                            s_x += (e ? 1.0 : -1.0) * wy[a] * v;
+                                        }
+                                    }
+                                }
+                                double ga = 0.0;
+                                for (int o = g * Og; o < (g + 1) * Og; ++o) {
+                                    const double gov = (double)go[o * plane_out];
+                                    const size_t wi = (((size_t)o * Cg + cl) * p.kh + i) * p.kw + j;
+                                    ga += gov * (double)p.weight[wi];
+                                    gw[wi] += gov * m * s;
+                                }
+                                g_m += ga * s;
+                                g_dy += ga * m * s_y;
+                                g_dx += ga * m * s_x;
+                                double *gxc = grad_x + ((size_t)b * p.C + c) * plane_in;
+                                for (int a = 0; a < 2; ++a) {
+                                    for (int e = 0; e < 2; ++e) {
+                                        const double yy = (double)fy0 + a;
+                                        const double xx = (double)fx0 + e;
+                                        if (yy >= 0.0 && yy <= p.H - 1 && xx >= 0.0 && xx <= p.W - 1)
+                                            gxc[(size_t)yy * p.W + (size_t)xx] += ga * m * wy[a] * wx[e];
+                                    }
+                                }
+                            }
+                            grad_offset[(oq * 2 * k_total + 2 * k) * plane_out + pix] = g_dy;
+                            grad_offset[(oq * 2 * k_total + 2 * k + 1) * plane_out + pix] = g_dx;
+                            if (grad_mask) grad_mask[(oq * k_total + k) * plane_out + pix] = g_m;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    for (size_t t = 0; t < n_w; ++t) {
+        double acc = 0.0;
+        for (int b = 0; b < p.B; ++b) acc += part[(size_t)b * per_image + t];
+        grad_weight[t] = acc;
+    }
+    if (grad_bias) {
+        for (int o = 0; o < p.O; ++o) {
+            double acc = 0.0;
+            for (int b = 0; b < p.B; ++b) acc += part[(size_t)b * per_image + n_w + o];
+            grad_bias[o] = acc;
+        }
+    }
+    free(part);
+    return 0;
 }
