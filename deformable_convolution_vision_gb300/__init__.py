@@ -1,16 +1,19 @@
-"""GB300 (sm_103a) modulated deformable convolution, forward pass.
+"""GB300 (sm_103a) modulated deformable convolution: forward and backward.
 
 torchvision ``deform_conv2d`` semantics -- stride, per-axis padding,
 dilation, weight groups and offset groups -- computed by hand-written CUDA
-kernels behind the C ABI declared in ``include/dcn.h``.  This package is the thin
-Python side: ``binding`` maps the C entry points one to one, and
-``deform_conv2d`` below shapes PyTorch tensors into one call.
+kernels behind the C ABI declared in ``include/dcn.h``.  This package is the
+thin Python side: ``binding`` maps the C entry points one to one,
+``deform_conv2d`` and ``deform_conv2d_backward`` below shape PyTorch tensors
+into one call each, and ``autograd.DeformConv2dFunction`` joins the two for
+torch's autograd.
 """
 
 from . import binding
 from .binding import (DCN_BF16, DCN_F16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
                       DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, ConvDesc, DcnError, dcn_create,
-                      dcn_destroy, dcn_forward, dcn_forward_ex, dcn_forward_host,
+                      dcn_backward, dcn_backward_ex, dcn_destroy, dcn_forward, dcn_forward_ex,
+                      dcn_forward_host,
                       dcn_forward_packed, dcn_forward_packed_ex, dcn_last_path, dcn_out_size,
                       dcn_pack_weight, dcn_pack_weight_ex, dcn_selftest_timeout, dcn_set_path,
                       dcn_set_sample_precision, dcn_status_string, dcn_sync_status)
@@ -21,7 +24,8 @@ __all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF1
            "dcn_forward", "dcn_forward_host", "dcn_forward_packed", "dcn_pack_weight",
            "dcn_set_path", "dcn_last_path", "dcn_sync_status", "dcn_selftest_timeout",
            "dcn_status_string", "ConvDesc", "dcn_forward_ex", "dcn_pack_weight_ex",
-           "dcn_forward_packed_ex", "dcn_out_size"]
+           "dcn_forward_packed_ex", "dcn_out_size", "dcn_backward", "dcn_backward_ex",
+           "deform_conv2d_backward"]
 
 
 class Handle:
@@ -77,32 +81,19 @@ def _out_size(n, k, s, p, d):
     return span // s + 1 if span >= 0 else 0
 
 
-def deform_conv2d(x, offset, weight, bias=None, stride=1, padding=0, dilation=1, mask=None,
-                  handle=None, out=None, stream=None):
-    """Modulated deformable convolution forward on CUDA tensors, with
-    torchvision ``deform_conv2d``'s argument order.
-
-    x       [B, C, H, W] float32/bfloat16/float16, channels_last memory format
-    offset  [B, 2*G*kh*kw, Ho, Wo] float32, contiguous ((dy, dx) per tap,
-            offset group after offset group); G = offset groups
-    weight  [O, C/groups, kh, kw] same dtype as x, contiguous; groups = C / its dim 1
-    bias    [O] float32 or None
-    mask    [B, G*kh*kw, Ho, Wo] float32 or None
-    stride, padding, dilation: int or (h, w)
-    Returns out [B, O, Ho, Wo] in x's dtype, channels_last memory format.
-    Layouts are checked, never converted.
-    """
+def _describe(x, offset, weight, stride, padding, dilation, mask):
+    """Check layouts and dtypes (never convert them); the problem's ConvDesc
+    and output size."""
     import torch
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor")
     if not x.is_contiguous(memory_format=torch.channels_last):
         raise ValueError("x must be channels_last contiguous")
-    for name, t in (("offset", offset), ("weight", weight), ("bias", bias), ("mask", mask)):
+    for name, t in (("offset", offset), ("weight", weight), ("mask", mask)):
         if t is not None and not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
-    if offset.dtype != torch.float32 or (mask is not None and mask.dtype != torch.float32) or \
-            (bias is not None and bias.dtype != torch.float32):
-        raise TypeError("offset, mask and bias must be float32")
+    if offset.dtype != torch.float32 or (mask is not None and mask.dtype != torch.float32):
+        raise TypeError("offset and mask must be float32")
     if weight.dtype != x.dtype:
         raise TypeError("weight must have x's dtype")
     B, C, H, W = x.shape
@@ -121,10 +112,31 @@ def deform_conv2d(x, offset, weight, bias=None, stride=1, padding=0, dilation=1,
         raise ValueError(f"offset must be {(B, 2 * G * k, Ho, Wo)} with G dividing C")
     if mask is not None and tuple(mask.shape) != (B, G * k, Ho, Wo):
         raise ValueError(f"mask must be {(B, G * k, Ho, Wo)}")
+    return ConvDesc(B, C, H, W, O, kh, kw, sh, sw, ph, pw, dh, dw, groups, G), Ho, Wo
+
+
+def deform_conv2d(x, offset, weight, bias=None, stride=1, padding=0, dilation=1, mask=None,
+                  handle=None, out=None, stream=None):
+    """Modulated deformable convolution forward on CUDA tensors, with
+    torchvision ``deform_conv2d``'s argument order.
+
+    x       [B, C, H, W] float32/bfloat16/float16, channels_last memory format
+    offset  [B, 2*G*kh*kw, Ho, Wo] float32, contiguous ((dy, dx) per tap,
+            offset group after offset group); G = offset groups
+    weight  [O, C/groups, kh, kw] same dtype as x, contiguous; groups = C / its dim 1
+    bias    [O] float32 or None
+    mask    [B, G*kh*kw, Ho, Wo] float32 or None
+    stride, padding, dilation: int or (h, w)
+    Returns out [B, O, Ho, Wo] in x's dtype, channels_last memory format.
+    Layouts are checked, never converted.
+    """
+    import torch
+    if bias is not None and (not bias.is_contiguous() or bias.dtype != torch.float32):
+        raise TypeError("bias must be contiguous float32")
+    desc, Ho, Wo = _describe(x, offset, weight, stride, padding, dilation, mask)
     if out is None:
-        out = torch.empty((B, O, Ho, Wo), dtype=x.dtype, device=x.device,
+        out = torch.empty((desc.B, desc.O, Ho, Wo), dtype=x.dtype, device=x.device,
                           memory_format=torch.channels_last)
-    desc = ConvDesc(B, C, H, W, O, kh, kw, sh, sw, ph, pw, dh, dw, groups, G)
     own = handle is None
     h = Handle() if own else handle
     try:
@@ -137,3 +149,33 @@ def deform_conv2d(x, offset, weight, bias=None, stride=1, padding=0, dilation=1,
         if own:
             h.close()
     return out
+
+
+def deform_conv2d_backward(grad_out, x, offset, weight, stride=1, padding=0, dilation=1,
+                           mask=None, bias=True, handle=None, stream=None):
+    """Gradients of ``deform_conv2d`` given ``grad_out`` [B, O, Ho, Wo]
+    (channels_last, x's dtype).  Returns a dict of fp32 CUDA tensors:
+    grad_x [B, C, H, W] (channels_last), grad_offset, grad_mask (None
+    without a mask), grad_weight [O, C/groups, kh, kw] and grad_bias [O]
+    (None when ``bias`` is False).  Layouts are checked, never converted."""
+    import torch
+    desc, Ho, Wo = _describe(x, offset, weight, stride, padding, dilation, mask)
+    if tuple(grad_out.shape) != (desc.B, desc.O, Ho, Wo) or grad_out.dtype != x.dtype or \
+            not grad_out.is_contiguous(memory_format=torch.channels_last):
+        raise ValueError(f"grad_out must be {(desc.B, desc.O, Ho, Wo)} channels_last in x's dtype")
+    f32 = dict(dtype=torch.float32, device=x.device)
+    gx = torch.empty(x.shape, memory_format=torch.channels_last, **f32)
+    goff = torch.empty(offset.shape, **f32)
+    gm = None if mask is None else torch.empty(mask.shape, **f32)
+    gw = torch.empty(weight.shape, **f32)
+    gb = torch.empty((desc.O,), **f32) if bias else None
+    own = handle is None
+    h = Handle() if own else handle
+    try:
+        dcn_backward_ex(h.h, x, offset, mask, weight, grad_out, gx, goff, gm, gw, gb, desc,
+                        _dtype_code(x), stream)
+    finally:
+        if own:
+            h.close()
+    return {"grad_x": gx, "grad_offset": goff, "grad_mask": gm, "grad_weight": gw,
+            "grad_bias": gb}

@@ -23,7 +23,7 @@ EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_f
            "dcn_forward_host", "dcn_set_path", "dcn_last_path", "dcn_sync_status",
            "dcn_selftest_timeout", "dcn_status_string", "dcn_forward_noalloc",
            "dcn_set_sample_precision", "dcn_out_size", "dcn_forward_ex", "dcn_pack_weight_ex",
-           "dcn_forward_packed_ex"]
+           "dcn_forward_packed_ex", "dcn_backward", "dcn_backward_ex"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -71,6 +71,8 @@ def load():
         "dcn_forward_ex": ([P, P, P, P, P, P, P, ctypes.POINTER(ConvDesc), I, P], I),
         "dcn_pack_weight_ex": ([P, P, ctypes.POINTER(ConvDesc), I, P], I),
         "dcn_forward_packed_ex": ([P, P, P, P, P, P, ctypes.POINTER(ConvDesc), I, P], I),
+        "dcn_backward": ([P] * 11 + [I] * 9 + [P], I),
+        "dcn_backward_ex": ([P] * 11 + [ctypes.POINTER(ConvDesc), I, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -193,3 +195,21 @@ def dcn_forward_packed_ex(h, x, offset, mask, bias, out, desc, dtype, stream=Non
     _check(load().dcn_forward_packed_ex(h, _ptr(x), _ptr(offset), _ptr(mask), _ptr(bias),
                                         _ptr(out), ctypes.byref(desc), dtype, _stream(stream)),
            "dcn_forward_packed_ex")
+
+
+def dcn_backward(h, x, offset, mask, weight, grad_out, grad_x, grad_offset, grad_mask,
+                 grad_weight, grad_bias, B, C, H, W, O, kh, kw, pad, dtype, stream=None):
+    _check(load().dcn_backward(h, _ptr(x), _ptr(offset), _ptr(mask), _ptr(weight), _ptr(grad_out),
+                               _ptr(grad_x), _ptr(grad_offset), _ptr(grad_mask), _ptr(grad_weight),
+                               _ptr(grad_bias), B, C, H, W, O, kh, kw, pad, dtype,
+                               _stream(stream)),
+           "dcn_backward")
+
+
+def dcn_backward_ex(h, x, offset, mask, weight, grad_out, grad_x, grad_offset, grad_mask,
+                    grad_weight, grad_bias, desc, dtype, stream=None):
+    _check(load().dcn_backward_ex(h, _ptr(x), _ptr(offset), _ptr(mask), _ptr(weight),
+                                  _ptr(grad_out), _ptr(grad_x), _ptr(grad_offset), _ptr(grad_mask),
+                                  _ptr(grad_weight), _ptr(grad_bias), ctypes.byref(desc), dtype,
+                                  _stream(stream)),
+           "dcn_backward_ex")

@@ -440,6 +440,82 @@ dcn_status_t dcn_forward_ex(dcn_handle_t h, const void *x, const float *offset, 
     return forward_general(h, x, offset, mask, weight, bias, out, c, dtype, stream);
 }
 
+static dcn_status_t backward_general(dcn_handle_t h, const void *x, const float *offset,
+                                     const float *mask, const void *weight, const void *grad_out,
+                                     float *grad_x, float *grad_offset, float *grad_mask,
+                                     float *grad_weight, float *grad_bias, const Conv &c,
+                                     int dtype, void *stream) {
+    if (!x || !offset || !weight || !grad_out || !grad_x || !grad_offset || !grad_weight)
+        return DCN_ERR_INVALID_ARG;
+    const size_t es = esize(dtype);
+    if (!aligned(x, es) || !aligned(weight, es) || !aligned(grad_out, es))
+        return DCN_ERR_INVALID_ARG;
+    const float *f32s[] = {offset, mask, grad_x, grad_offset, grad_mask, grad_weight, grad_bias};
+    for (const float *f : f32s)
+        if (f && !aligned(f, 4)) return DCN_ERR_INVALID_ARG;
+    const dcn_conv_desc_t &d = c.d;
+    const size_t taps = static_cast<size_t>(d.kh) * d.kw;
+    const size_t HoWo = static_cast<size_t>(c.Ho) * c.Wo;
+    // launch-grid limits of the weight-gradient kernel (taps and 64 x 64 tiles)
+    const long long tiles = static_cast<long long>(d.groups) * ((c.Og() + 63) / 64) * ((c.Cg() + 63) / 64);
+    if (taps > 65535 || tiles > 65535 || (d.C + 63) / 64 > 65535) return DCN_ERR_UNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    // the kernels add into the gradients: clear them first
+    const size_t bytes[5] = {
+        static_cast<size_t>(d.B) * d.H * d.W * d.C * 4,
+        static_cast<size_t>(d.B) * 2 * d.offset_groups * taps * HoWo * 4,
+        static_cast<size_t>(d.B) * d.offset_groups * taps * HoWo * 4,
+        static_cast<size_t>(d.O) * c.Cg() * taps * 4,
+        static_cast<size_t>(d.O) * 4,
+    };
+    float *bufs[5] = {grad_x, grad_offset, grad_mask, grad_weight, grad_bias};
+    for (int i = 0; i < 5; ++i)
+        if (bufs[i] && cudaMemsetAsync(bufs[i], 0, bytes[i], s) != cudaSuccess) return DCN_ERR_CUDA;
+    dcn::BwdParams p;
+    p.x = x; p.offset = offset; p.mask = mask; p.weight = weight; p.grad_out = grad_out;
+    p.grad_x = grad_x; p.grad_offset = grad_offset; p.grad_mask = grad_mask;
+    p.grad_weight = grad_weight; p.grad_bias = grad_bias;
+    p.B = d.B; p.C = d.C; p.H = d.H; p.W = d.W; p.O = d.O; p.kh = d.kh; p.kw = d.kw;
+    p.sh = d.stride_h; p.sw = d.stride_w; p.ph = d.pad_h; p.pw = d.pad_w;
+    p.dh = d.dil_h; p.dw = d.dil_w;
+    p.groups = d.groups;
+    p.ogroups = d.offset_groups;
+    p.Ho = c.Ho;
+    p.Wo = c.Wo;
+    p.P = d.B * c.Ho * c.Wo;
+    p.sm_count = h->sm_count;
+    p.gx_vec4 = (d.C % 4 == 0 && aligned(grad_x, 16)) ? 1 : 0;
+    p.pix_run = 0;
+    if (dcn::launch_backward(p, dtype, s) != cudaSuccess) return DCN_ERR_CUDA;
+    return DCN_OK;
+}
+
+dcn_status_t dcn_backward(dcn_handle_t h, const void *x, const float *offset, const float *mask,
+                          const void *weight, const void *grad_out, float *grad_x,
+                          float *grad_offset, float *grad_mask, float *grad_weight,
+                          float *grad_bias, int B, int C, int H, int W, int O, int kh, int kw,
+                          int pad, int dtype, void *stream) {
+    if (!h) return DCN_ERR_INVALID_ARG;
+    Conv c;
+    dcn_status_t st = make_conv(page_desc(B, C, H, W, O, kh, kw, pad), dtype, &c);
+    if (st != DCN_OK) return st;
+    return backward_general(h, x, offset, mask, weight, grad_out, grad_x, grad_offset, grad_mask,
+                            grad_weight, grad_bias, c, dtype, stream);
+}
+
+dcn_status_t dcn_backward_ex(dcn_handle_t h, const void *x, const float *offset,
+                             const float *mask, const void *weight, const void *grad_out,
+                             float *grad_x, float *grad_offset, float *grad_mask,
+                             float *grad_weight, float *grad_bias, const dcn_conv_desc_t *desc,
+                             int dtype, void *stream) {
+    if (!h || !desc) return DCN_ERR_INVALID_ARG;
+    Conv c;
+    dcn_status_t st = make_conv(*desc, dtype, &c);
+    if (st != DCN_OK) return st;
+    return backward_general(h, x, offset, mask, weight, grad_out, grad_x, grad_offset, grad_mask,
+                            grad_weight, grad_bias, c, dtype, stream);
+}
+
 int dcn_out_size(int n, int k, int stride, int pad, int dil) {
     if (n <= 0 || k <= 0 || stride <= 0 || pad < 0 || dil <= 0) return 0;
     const long long r = out_size_ll(n, k, stride, pad, dil);

@@ -88,6 +88,33 @@ inline bool tc_pack_permuted(int dtype, int Cg) { return (dtype == kBF16 || dtyp
 cudaError_t launch_tc(const Params &p, const CUtensorMap &wmap, cudaStream_t stream,
                       bool after_pack = false);
 
+// Everything the backward kernels need (device pointers).  x, weight and
+// grad_out are in the operand dtype; the gradients are fp32 and must be
+// zero on entry (the kernels add into them).
+struct BwdParams {
+    const void *x;          // [B, H, W, C] channels-last
+    const float *offset;    // [B, 2*ogroups*kh*kw, Ho, Wo]
+    const float *mask;      // [B, ogroups*kh*kw, Ho, Wo] or nullptr (all ones)
+    const void *weight;     // [O, C/groups, kh, kw]
+    const void *grad_out;   // [B, Ho, Wo, O] channels-last
+    float *grad_x;          // [B, H, W, C] channels-last
+    float *grad_offset;     // like offset
+    float *grad_mask;       // like mask, or nullptr (not wanted)
+    float *grad_weight;     // like weight
+    float *grad_bias;       // [O] or nullptr (not wanted)
+    int B, C, H, W, O, kh, kw;
+    int sh, sw, ph, pw, dh, dw;
+    int groups, ogroups;
+    int Ho, Wo, P;
+    int sm_count;
+    int gx_vec4;            // grad_x 16-byte aligned and C % 4 == 0
+    int pix_run;            // set by the launcher
+};
+
+// The backward pass: grad_x, grad_offset and grad_mask (one kernel),
+// grad_weight (one kernel), grad_bias (one kernel, when wanted).
+cudaError_t launch_backward(const BwdParams &p, int dtype, cudaStream_t stream);
+
 // One-thread kernel whose barrier wait runs out after timeout_ns.
 cudaError_t launch_selftest_timeout(unsigned *status, unsigned long long timeout_ns,
                                     cudaStream_t stream);

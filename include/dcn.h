@@ -267,6 +267,57 @@ DCN_API dcn_status_t dcn_forward_packed_ex(dcn_handle_t h,
                                    const float *bias, void *out,
                                    const dcn_conv_desc_t *desc, int dtype, void *stream);
 
+/* ------------------------------------------------------------ backward
+ *
+ * The gradients of the forward pass with respect to x, offset, mask, weight
+ * and bias, given grad_out (the cotangent of out).  They follow from the
+ * forward's definition by the chain rule; the page "deformops 3.0.1"
+ * (section "Deformable convolution") keeps fp32 accumulation and no TF32 in
+ * them.  With gA = sum over the outputs o of channel c's weight group of
+ * grad_out[p,o] * weight[o, c - c0, i, j], for each output pixel p, tap
+ * (i, j) and channel c:
+ *   grad_x at each inside corner    += gA * m * wy * wx
+ *   grad_offset (dy, dx)            += gA * m * (dS/dpy, dS/dpx)
+ *   grad_mask                       += gA * S
+ *   grad_weight[o, c - c0, i, j]    += grad_out[p,o] * m * S
+ *   grad_bias[o]                    += grad_out[p,o]
+ * where S is the bilinear sample and wy, wx its corner weights.  The
+ * corner weights are piecewise linear in the coordinate; at an integer
+ * coordinate the derivative is the one of the cell floor() selects.
+ *
+ * Layouts (device pointers, dense):
+ *   x        [B, H, W, C]          channels-last, `dtype`
+ *   offset   [B, 2*G*kh*kw, Ho, Wo] fp32     (G = offset groups)
+ *   mask     [B, G*kh*kw, Ho, Wo]  fp32, or NULL (all ones)
+ *   weight   [O, C/groups, kh, kw] `dtype`
+ *   grad_out [B, Ho, Wo, O]        channels-last, `dtype`
+ *   grad_x   [B, H, W, C]          fp32, channels-last
+ *   grad_offset like offset, fp32
+ *   grad_mask   like mask, fp32, or NULL (not computed; with mask NULL it is
+ *               the gradient at mask = 1)
+ *   grad_weight [O, C/groups, kh, kw] fp32
+ *   grad_bias   [O] fp32, or NULL (not computed)
+ * The gradients are overwritten (zeroed, then accumulated in fp32 with
+ * atomic reductions, so the order of the sums, and the last bits, vary from
+ * run to run).  Runs on CUDA cores; asynchronous on `stream`; allocates
+ * nothing.  Argument rules as dcn_forward / dcn_forward_ex (sizes, NULL
+ * inputs, alignment to the element size, 4 bytes for fp32 arrays);
+ * DCN_ERR_INVALID_ARG for a NULL x, offset, weight, grad_out, grad_x,
+ * grad_offset or grad_weight. */
+DCN_API dcn_status_t dcn_backward(dcn_handle_t h,
+                          const void *x, const float *offset, const float *mask,
+                          const void *weight, const void *grad_out,
+                          float *grad_x, float *grad_offset, float *grad_mask,
+                          float *grad_weight, float *grad_bias,
+                          int B, int C, int H, int W, int O,
+                          int kh, int kw, int pad, int dtype, void *stream);
+DCN_API dcn_status_t dcn_backward_ex(dcn_handle_t h,
+                             const void *x, const float *offset, const float *mask,
+                             const void *weight, const void *grad_out,
+                             float *grad_x, float *grad_offset, float *grad_mask,
+                             float *grad_weight, float *grad_bias,
+                             const dcn_conv_desc_t *desc, int dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
