@@ -229,6 +229,58 @@ def config_dict(wl, l2):
             "pad": wl.pad, "out_pixels": wl.pixels, "flops_per_step": wl.flops, "l2": l2}
 
 
+def fp32_fma_peak_tflops(sm_count, sm_mhz):
+    """fp32 CUDA-core peak: 128 FFMA lanes per SM, 2 FLOP each, per clock."""
+    return sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def time_backward(args, wl, dcn, torch, dev, stream, h, x, off, m, w, flush, code):
+    """The backward pass (all five gradients) on the same workload: CUDA
+    events around each dcn_backward call, L2 flushed before each."""
+    if args.no_backward:
+        return None
+    g = torch.Generator().manual_seed(7)
+    gout = torch.randn(wl.B, wl.O, wl.Ho, wl.Wo, generator=g).to(x.dtype).to(dev) \
+        .contiguous(memory_format=torch.channels_last)
+    f32 = dict(dtype=torch.float32, device=dev)
+    gx = torch.empty(x.shape, memory_format=torch.channels_last, **f32)
+    goff = torch.empty(off.shape, **f32)
+    gm = None if m is None else torch.empty(m.shape, **f32)
+    gw = torch.empty(w.shape, **f32)
+    gb = torch.empty((wl.O,), **f32)
+    dims = (wl.B, wl.C, wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad, code)
+
+    def call():
+        dcn.dcn_backward(h.h, x, off, m, w, gout, gx, goff, gm, gw, gb, *dims, stream)
+
+    for _ in range(max(3, min(args.warmup, 5))):
+        flush.fill_(2)
+        call()
+    n = max(3, min(args.steps, args.backward_steps))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for k in range(n):
+        flush.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dcn.dcn_sync_status(h.h, stream) != 0:
+        raise RuntimeError("device status set during the backward timing")
+    ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
+    flops = 2 * wl.flops   # the column-gradient and weight-gradient contractions
+    props = torch.cuda.get_device_properties(dev)
+    peak = fp32_fma_peak_tflops(props.multi_processor_count, 2070.0)
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"ms_per_call": ms, "value": achieved, "unit": "TFLOP/s",
+            "flops_per_call": flops, "calls": n,
+            "gradients": "x, offset, mask, weight, bias (fp32)",
+            "roofline": {"bound": "fma", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak,
+                         "peak_source": f"{props.multi_processor_count} SMs x 128 fp32 FMA lanes x 2 FLOP "
+                                        f"x 2070 MHz (the SM clock maximum)",
+                         "scope": "whole dcn_backward call"}}
+
+
 def run_ours(args, wl, rank, local_rank, world):
     import torch
     import deformable_convolution_vision_gb300 as dcn
@@ -327,6 +379,7 @@ def run_ours(args, wl, rank, local_rank, world):
         dcn.dcn_forward_host(h.h, hx, hoff, hm, hw, hb, hout, *dims, stream)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     e2e_max = reduce_max(e2e_s, world)
+    backward = time_backward(args, wl, dcn, torch, dev, stream, h, x, off, m, w, flush, code)
     h.close()
 
     if rank != 0:
@@ -362,6 +415,8 @@ def run_ours(args, wl, rank, local_rank, world):
         "gpu_launches": 2 * args.steps,   # per step: the weight pack and the fused kernel
         "wall_s_timed_region": wall,
     }
+    if backward is not None:
+        line["backward"] = backward
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -377,6 +432,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-step-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--backward-steps", type=int, default=50)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -70,6 +70,8 @@ class Oracle:
         lib.oracle_dcn_forward_points_ex.restype = i
         lib.oracle_dcn_backward_ex.argtypes = [f] * 10 + [f, i]
         lib.oracle_dcn_backward_ex.restype = i
+        lib.oracle_dcn_backward_points_ex.argtypes = [f] * 5 + [f, i, f, f, f, i]
+        lib.oracle_dcn_backward_points_ex.restype = i
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i
         self._lib = lib
@@ -206,6 +208,25 @@ class Oracle:
         return {"grad_x": gx, "grad_offset": goff, "grad_mask": gm, "grad_weight": gw,
                 "grad_bias": gb}
 
+    def backward_points_ex(self, x, offset, mask, weight, grad_out, conv, points, nthreads=0):
+        """grad_offset [n, 2*G*k] and grad_mask [n, G*k] (None without a
+        mask) at output pixels points [n, 3] of (b, h, w)."""
+        arrs, desc, (B, O, Ho, Wo) = self._prepare_ex(x, offset, mask, weight, None, conv)
+        x, offset, mask, weight, _ = arrs
+        go = self._f32(grad_out)
+        if go.shape != (B, O, Ho, Wo):
+            raise ValueError(f"grad_out shape {go.shape} != {(B, O, Ho, Wo)}")
+        pts = np.ascontiguousarray(points, dtype=np.int32).reshape(-1, 3)
+        n = pts.shape[0]
+        goff = np.empty((n, offset.shape[1]), dtype=np.float64)
+        gm = None if mask is None else np.empty((n, mask.shape[1]), dtype=np.float64)
+        rc = self._lib.oracle_dcn_backward_points_ex(
+            self._ptr(x), self._ptr(offset), self._ptr(mask), self._ptr(weight), self._ptr(go),
+            self._ptr(pts), n, self._ptr(goff), self._ptr(gm), self._ptr(desc), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_dcn_backward_points_ex rejected its arguments")
+        return goff, gm
+
     def backward(self, x, offset, mask, weight, grad_out, pad, nthreads=0):
         """backward_ex for the page-1 problem (stride 1, dilation 1, one
         padding, one weight group, one offset group)."""
@@ -268,3 +289,7 @@ def backward(*args, **kwargs):
 
 def backward_ex(*args, **kwargs):
     return get().backward_ex(*args, **kwargs)
+
+
+def backward_points_ex(*args, **kwargs):
+    return get().backward_points_ex(*args, **kwargs)

@@ -293,6 +293,89 @@ int oracle_max_threads(void)
  * grad_offset like offset, grad_mask like mask (NULL: not computed),
  * grad_weight like weight, grad_bias [O] (NULL: not computed).
  */
+/* One output pixel (b, h, w) of the backward pass.  gw and gb receive its
+ * weight and bias contributions (added), gx_b its scatter into image b's
+ * grad_x (added); each may be NULL (not wanted).  goff and gmask point at
+ * this pixel's first offset / mask gradient; consecutive channels of those
+ * arrays are `stride` apart; gmask may be NULL. */
+static void oracle_bwd_pixel(const oracle_problem *p, const float *grad_out, int b, int h, int w,
+                             double *gw, double *gb, double *gx_b,
+                             double *goff, double *gmask, ptrdiff_t stride)
+{
+    const int k_total = p->kh * p->kw;
+    const int Cg = p->C / p->groups, Og = p->O / p->groups, Cq = p->C / p->ogroups;
+    const size_t plane_in = (size_t)p->H * p->W;
+    const size_t plane_out = (size_t)p->Ho * p->Wo;
+    const size_t pix = (size_t)h * p->Wo + w;
+    const float *go = grad_out + (size_t)b * p->O * plane_out + pix;
+    if (gb)
+        for (int o = 0; o < p->O; ++o) gb[o] += (double)go[o * plane_out];
+    for (int i = 0; i < p->kh; ++i) {
+        for (int j = 0; j < p->kw; ++j) {
+            const int k = i * p->kw + j;
+            for (int q = 0; q < p->ogroups; ++q) {
+                const size_t oq = (size_t)b * p->ogroups + q;
+                const float dy = p->offset[(oq * 2 * k_total + 2 * k) * plane_out + pix];
+                const float dx = p->offset[(oq * 2 * k_total + 2 * k + 1) * plane_out + pix];
+                const double m = p->mask
+                    ? (double)p->mask[(oq * k_total + k) * plane_out + pix]
+                    : 1.0;
+                const float py = (float)(h * p->sh - p->ph + i * p->dh) + dy;
+                const float px = (float)(w * p->sw - p->pw + j * p->dw) + dx;
+                const float fy0 = floorf(py);
+                const float fx0 = floorf(px);
+                const double ly = (double)py - (double)fy0;
+                const double lx = (double)px - (double)fx0;
+                const double wy[2] = {1.0 - ly, ly};
+                const double wx[2] = {1.0 - lx, lx};
+                double g_dy = 0.0, g_dx = 0.0, g_m = 0.0;
+                for (int c = q * Cq; c < (q + 1) * Cq; ++c) {
+                    const int g = c / Cg;
+                    const int cl = c - g * Cg;
+                    const float *xc = p->x + ((size_t)b * p->C + c) * plane_in;
+                    double s = 0.0, s_y = 0.0, s_x = 0.0;
+                    for (int a = 0; a < 2; ++a) {
+                        for (int e = 0; e < 2; ++e) {
+                            const double yy = (double)fy0 + a;
+                            const double xx = (double)fx0 + e;
+                            if (yy >= 0.0 && yy <= p->H - 1 && xx >= 0.0 && xx <= p->W - 1) {
+                                const double v = (double)xc[(size_t)yy * p->W + (size_t)xx];
+                                s += wy[a] * wx[e] * v;
+                                s_y += (a ? 1.0 : -1.0) * wx[e] * v;
+                                s_x += (e ? 1.0 : -1.0) * wy[a] * v;
+                            }
+                        }
+                    }
+                    double ga = 0.0;
+                    for (int o = g * Og; o < (g + 1) * Og; ++o) {
+                        const double gov = (double)go[o * plane_out];
+                        const size_t wi = (((size_t)o * Cg + cl) * p->kh + i) * p->kw + j;
+                        ga += gov * (double)p->weight[wi];
+                        if (gw) gw[wi] += gov * m * s;
+                    }
+                    g_m += ga * s;
+                    g_dy += ga * m * s_y;
+                    g_dx += ga * m * s_x;
+                    if (gx_b) {
+                        double *gxc = gx_b + (size_t)c * plane_in;
+                        for (int a = 0; a < 2; ++a) {
+                            for (int e = 0; e < 2; ++e) {
+                                const double yy = (double)fy0 + a;
+                                const double xx = (double)fx0 + e;
+                                if (yy >= 0.0 && yy <= p->H - 1 && xx >= 0.0 && xx <= p->W - 1)
+                                    gxc[(size_t)yy * p->W + (size_t)xx] += ga * m * wy[a] * wx[e];
+                            }
+                        }
+                    }
+                }
+                goff[(ptrdiff_t)(q * 2 * k_total + 2 * k) * stride] = g_dy;
+                goff[(ptrdiff_t)(q * 2 * k_total + 2 * k + 1) * stride] = g_dx;
+                if (gmask) gmask[(ptrdiff_t)(q * k_total + k) * stride] = g_m;
+            }
+        }
+    }
+}
+
 int oracle_dcn_backward_ex(const float *x, const float *offset, const float *mask,
                            const float *weight, const float *grad_out,
                            double *grad_x, double *grad_offset, double *grad_mask,
@@ -303,7 +386,7 @@ int oracle_dcn_backward_ex(const float *x, const float *offset, const float *mas
     const oracle_problem p = oracle_make(x, offset, mask, weight, NULL, desc);
     if (oracle_check(&p)) return -1;
     const int k_total = p.kh * p.kw;
-    const int Cg = p.C / p.groups, Og = p.O / p.groups, Cq = p.C / p.ogroups;
+    const int Cg = p.C / p.groups;
     const size_t plane_in = (size_t)p.H * p.W;
     const size_t plane_out = (size_t)p.Ho * p.Wo;
     const size_t n_w = (size_t)p.O * Cg * k_total;
@@ -311,81 +394,19 @@ int oracle_dcn_backward_ex(const float *x, const float *offset, const float *mas
     double *part = (double *)calloc((size_t)p.B * per_image, sizeof(double));
     if (!part) return -2;
     memset(grad_x, 0, sizeof(double) * (size_t)p.B * p.C * plane_in);
-    memset(grad_offset, 0, sizeof(double) * (size_t)p.B * 2 * p.ogroups * k_total * plane_out);
-    if (grad_mask)
-        memset(grad_mask, 0, sizeof(double) * (size_t)p.B * p.ogroups * k_total * plane_out);
     ORACLE_SET_THREADS(nthreads);
     #pragma omp parallel for schedule(dynamic, 1)
     for (int b = 0; b < p.B; ++b) {
         double *gw = part + (size_t)b * per_image;   /* this image's grad_weight */
         double *gb = gw + n_w;                        /* and grad_bias */
+        double *gx_b = grad_x + (size_t)b * p.C * plane_in;
+        double *goff_b = grad_offset + (size_t)b * 2 * p.ogroups * k_total * plane_out;
+        double *gm_b = grad_mask ? grad_mask + (size_t)b * p.ogroups * k_total * plane_out : NULL;
         for (int h = 0; h < p.Ho; ++h) {
             for (int w = 0; w < p.Wo; ++w) {
                 const size_t pix = (size_t)h * p.Wo + w;
-                const float *go = grad_out + (size_t)b * p.O * plane_out + pix;
-                for (int o = 0; o < p.O; ++o) gb[o] += (double)go[o * plane_out];
-                for (int i = 0; i < p.kh; ++i) {
-                    for (int j = 0; j < p.kw; ++j) {
-                        const int k = i * p.kw + j;
-                        for (int q = 0; q < p.ogroups; ++q) {
-                            const size_t oq = (size_t)b * p.ogroups + q;
-                            const float dy = p.offset[(oq * 2 * k_total + 2 * k) * plane_out + pix];
-                            const float dx = p.offset[(oq * 2 * k_total + 2 * k + 1) * plane_out + pix];
-                            const double m = p.mask
-                                ? (double)p.mask[(oq * k_total + k) * plane_out + pix]
-                                : 1.0;
-                            const float py = (float)(h * p.sh - p.ph + i * p.dh) + dy;
-                            const float px = (float)(w * p.sw - p.pw + j * p.dw) + dx;
-                            const float fy0 = floorf(py);
-                            const float fx0 = floorf(px);
-                            const double ly = (double)py - (double)fy0;
-                            const double lx = (double)px - (double)fx0;
-                            const double wy[2] = {1.0 - ly, ly};
-                            const double wx[2] = {1.0 - lx, lx};
-                            double g_dy = 0.0, g_dx = 0.0, g_m = 0.0;
-                            for (int c = q * Cq; c < (q + 1) * Cq; ++c) {
-                                const int g = c / Cg;
-                                const int cl = c - g * Cg;
-                                const float *xc = p.x + ((size_t)b * p.C + c) * plane_in;
-                                double s = 0.0, s_y = 0.0, s_x = 0.0;
-                                for (int a = 0; a < 2; ++a) {
-                                    for (int e = 0; e < 2; ++e) {
-                                        const double yy = (double)fy0 + a;
-                                        const double xx = (double)fx0 + e;
-                                        if (yy >= 0.0 && yy <= p.H - 1 && xx >= 0.0 && xx <= p.W - 1) {
-                                            const double v = (double)xc[(size_t)yy * p.W + (size_t)xx];
-                                            s += wy[a] * wx[e] * v;
-                                            s_y += (a ? 1.0 : -1.0) * wx[e] * v;
-                                            s_x += (e ? 1.0 : -1.0) * wy[a] * v;
-                                        }
-                                    }
-                                }
-                                double ga = 0.0;
-                                for (int o = g * Og; o < (g + 1) * Og; ++o) {
-                                    const double gov = (double)go[o * plane_out];
-                                    const size_t wi = (((size_t)o * Cg + cl) * p.kh + i) * p.kw + j;
-                                    ga += gov * (double)p.weight[wi];
-                                    gw[wi] += gov * m * s;
-                                }
-                                g_m += ga * s;
-                                g_dy += ga * m * s_y;
-                                g_dx += ga * m * s_x;
-                                double *gxc = grad_x + ((size_t)b * p.C + c) * plane_in;
-                                for (int a = 0; a < 2; ++a) {
-                                    for (int e = 0; e < 2; ++e) {
-                                        const double yy = (double)fy0 + a;
-                                        const double xx = (double)fx0 + e;
-                                        if (yy >= 0.0 && yy <= p.H - 1 && xx >= 0.0 && xx <= p.W - 1)
-                                            gxc[(size_t)yy * p.W + (size_t)xx] += ga * m * wy[a] * wx[e];
-                                    }
-                                }
-                            }
-                            grad_offset[(oq * 2 * k_total + 2 * k) * plane_out + pix] = g_dy;
-                            grad_offset[(oq * 2 * k_total + 2 * k + 1) * plane_out + pix] = g_dx;
-                            if (grad_mask) grad_mask[(oq * k_total + k) * plane_out + pix] = g_m;
-                        }
-                    }
-                }
+                oracle_bwd_pixel(&p, grad_out, b, h, w, gw, gb, gx_b, goff_b + pix,
+                                 gm_b ? gm_b + pix : NULL, (ptrdiff_t)plane_out);
             }
         }
     }
@@ -402,5 +423,32 @@ int oracle_dcn_backward_ex(const float *x, const float *offset, const float *mas
         }
     }
     free(part);
+    return 0;
+}
+
+/* The offset and mask gradients of selected output pixels only (they
+ * depend on that pixel alone): pts holds n triples (b, h, w); goff receives
+ * n rows of 2*G*kh*kw values, gmask (may be NULL) n rows of G*kh*kw.  Same
+ * body as the full version. */
+int oracle_dcn_backward_points_ex(const float *x, const float *offset, const float *mask,
+                                  const float *weight, const float *grad_out,
+                                  const int *pts, int n, double *goff, double *gmask,
+                                  const int *desc, int nthreads)
+{
+    if (!desc || !grad_out || !goff || n < 0 || (n > 0 && !pts)) return -1;
+    const oracle_problem p = oracle_make(x, offset, mask, weight, NULL, desc);
+    if (oracle_check(&p)) return -1;
+    for (int t = 0; t < n; ++t) {
+        const int b = pts[3 * t], h = pts[3 * t + 1], w = pts[3 * t + 2];
+        if (b < 0 || b >= p.B || h < 0 || h >= p.Ho || w < 0 || w >= p.Wo) return -1;
+    }
+    const int k_total = p.kh * p.kw;
+    ORACLE_SET_THREADS(nthreads);
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int t = 0; t < n; ++t) {
+        oracle_bwd_pixel(&p, grad_out, pts[3 * t], pts[3 * t + 1], pts[3 * t + 2], NULL, NULL, NULL,
+                         goff + (size_t)t * 2 * p.ogroups * k_total,
+                         gmask ? gmask + (size_t)t * p.ogroups * k_total : NULL, 1);
+    }
     return 0;
 }

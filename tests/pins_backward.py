@@ -189,3 +189,19 @@ def pin_bwd_outside(orc):
 
 ALL_BACKWARD_PINS = [pin_bwd_autograd, pin_bwd_adjoint, pin_bwd_finite_diff_offsets,
                      pin_bwd_direct_conv, pin_bwd_outside]
+
+
+def check_points_match_full(orc):
+    """The per-pixel variant returns the full backward's offset and mask
+    gradients at the chosen pixels (the same body; a consistency check)."""
+    s = CASES[-2]
+    x, off, m, w, gout = _problem(420, s)
+    conv = _conv_desc(s)
+    full = orc.backward_ex(x, off, m, w, gout, conv)
+    B, _, Ho, Wo = off.shape
+    pts = np.array([[b, h, ww] for b in range(B) for h in range(0, Ho, 2) for ww in range(0, Wo, 3)],
+                   dtype=np.int32)
+    goff, gm = orc.backward_points_ex(x, off, m, w, gout, conv, pts)
+    for t, (b, h, ww) in enumerate(pts):
+        assert np.array_equal(goff[t], full["grad_offset"][b, :, h, ww])
+        assert np.array_equal(gm[t], full["grad_mask"][b, :, h, ww])

@@ -17,19 +17,19 @@ MUTANTS = {
     "dsdy_uses_wy": [("s_y += (a ? 1.0 : -1.0) * wx[e] * v;", "s_y += (a ? 1.0 : -1.0) * wy[a] * v;")],
     "dsdx_uses_wx": [("s_x += (e ? 1.0 : -1.0) * wy[a] * v;", "s_x += (e ? 1.0 : -1.0) * wx[e] * v;")],
     "offset_channels_swapped": [
-        ("grad_offset[(oq * 2 * k_total + 2 * k) * plane_out + pix] = g_dy;",
-         "grad_offset[(oq * 2 * k_total + 2 * k) * plane_out + pix] = g_dx;"),
-        ("grad_offset[(oq * 2 * k_total + 2 * k + 1) * plane_out + pix] = g_dx;",
-         "grad_offset[(oq * 2 * k_total + 2 * k + 1) * plane_out + pix] = g_dy;")],
+        ("goff[(ptrdiff_t)(q * 2 * k_total + 2 * k) * stride] = g_dy;",
+         "goff[(ptrdiff_t)(q * 2 * k_total + 2 * k) * stride] = g_dx;"),
+        ("goff[(ptrdiff_t)(q * 2 * k_total + 2 * k + 1) * stride] = g_dx;",
+         "goff[(ptrdiff_t)(q * 2 * k_total + 2 * k + 1) * stride] = g_dy;")],
     "grad_x_mask_dropped": [("+= ga * m * wy[a] * wx[e];", "+= ga * wy[a] * wx[e];")],
     "grad_weight_mask_dropped": [("gw[wi] += gov * m * s;", "gw[wi] += gov * s;")],
     "grad_mask_times_mask": [("g_m += ga * s;", "g_m += ga * m * s;")],
     "grad_offset_mask_dropped": [("g_dy += ga * m * s_y;", "g_dy += ga * s_y;"),
                                  ("g_dx += ga * m * s_x;", "g_dx += ga * s_x;")],
     "column_grad_wrong_outputs": [("for (int o = g * Og; o < (g + 1) * Og; ++o) {\n"
-                                   "                                    const double gov",
+                                   "                        const double gov",
                                    "for (int o = 0; o < Og; ++o) {\n"
-                                   "                                    const double gov")],
+                                   "                        const double gov")],
     "grad_x_corner_transposed": [("+= ga * m * wy[a] * wx[e];", "+= ga * m * wy[e] * wx[a];")],
     "weight_sum_last_image": [("for (int b = 0; b < p.B; ++b) acc += part[(size_t)b * per_image + t];",
                                "acc = part[(size_t)(p.B - 1) * per_image + t];")],
