@@ -37,6 +37,10 @@ struct dcn_handle_s {
     size_t flags_cap = 0;
     unsigned epoch = 0;
 
+    // backward on tensor cores: the weight packed as [kh*kw*C][O]
+    void *wpack_bwd = nullptr;
+    size_t wpack_bwd_cap = 0;
+
     // device staging for dcn_forward_host: x, offset, mask, weight, bias, out
     void *stage[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     size_t stage_cap[6] = {0, 0, 0, 0, 0, 0};
@@ -349,6 +353,7 @@ dcn_status_t dcn_destroy(dcn_handle_t h) {
     if (h->wpack) cudaFree(h->wpack);
     if (h->partial) cudaFree(h->partial);
     if (h->flags) cudaFree(h->flags);
+    if (h->wpack_bwd) cudaFree(h->wpack_bwd);
     if (h->status) cudaFree(h->status);
     for (int i = 0; i < 6; ++i)
         if (h->stage[i]) cudaFree(h->stage[i]);
@@ -486,7 +491,62 @@ static dcn_status_t backward_general(dcn_handle_t h, const void *x, const float 
     p.sm_count = h->sm_count;
     p.gx_vec4 = (d.C % 4 == 0 && aligned(grad_x, 16)) ? 1 : 0;
     p.pix_run = 0;
-    if (dcn::launch_backward(p, dtype, s) != cudaSuccess) return DCN_ERR_CUDA;
+    p.status = h->status;
+    p.timeout_ns = kWaitLimitNs;
+    p.f16 = dtype == DCN_F16 ? 1 : 0;
+
+    // the column gradient on tensor cores where the shape allows it
+    const bool tc_ok = tc_dtype(dtype) &&
+                       dcn::bwd_tc_supported(d.C, d.O, d.groups, d.offset_groups) &&
+                       aligned(x, 32) && aligned(grad_out, 16) && aligned(grad_x, 16);
+    int path = h->path;
+    if (path == DCN_PATH_AUTO) path = tc_ok ? DCN_PATH_TC : DCN_PATH_SIMT;
+    if (path == DCN_PATH_TC && !tc_ok) return DCN_ERR_UNSUPPORTED;
+    if (path == DCN_PATH_SIMT) {
+        if (dcn::launch_backward(p, dtype, s) != cudaSuccess) return DCN_ERR_CUDA;
+        h->last_path = path;
+        return DCN_OK;
+    }
+    const size_t wt_bytes = taps * d.C * d.O * 2;
+    dcn_status_t st = ensure(&h->wpack_bwd, &h->wpack_bwd_cap, wt_bytes, s);
+    if (st != DCN_OK) return st;
+    if (dcn::launch_pack_weight_bwd(weight, h->wpack_bwd, d.O, d.C, d.kh, d.kw, s) != cudaSuccess)
+        return DCN_ERR_CUDA;
+    const CUtensorMapDataType tdt = dtype == DCN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap gmap, wmap;
+    std::memset(&gmap, 0, sizeof(gmap));
+    std::memset(&wmap, 0, sizeof(wmap));
+    {
+        // grad_out [B][Ho][Wo][O]; box = 64 outputs x one 8 x 16 pixel tile
+        const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(d.O), static_cast<cuuint64_t>(c.Wo),
+                                    static_cast<cuuint64_t>(c.Ho), static_cast<cuuint64_t>(d.B)};
+        const cuuint64_t gstride[3] = {static_cast<cuuint64_t>(d.O) * 2,
+                                       static_cast<cuuint64_t>(c.Wo) * d.O * 2,
+                                       static_cast<cuuint64_t>(c.Ho) * c.Wo * d.O * 2};
+        const cuuint32_t box[4] = {64, 16, 8, 1};
+        const cuuint32_t estride[4] = {1, 1, 1, 1};
+        if (h->encode_tiled(&gmap, tdt, 4, const_cast<void *>(grad_out), gdim, gstride, box, estride,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DCN_ERR_CUDA;
+    }
+    {
+        // packed weight [kh*kw*C][O]; box = 64 outputs x 64 channel rows
+        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d.O), static_cast<cuuint64_t>(taps * d.C)};
+        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(d.O) * 2};
+        const cuuint32_t box[2] = {64, 64};
+        const cuuint32_t estride[2] = {1, 1};
+        if (h->encode_tiled(&wmap, tdt, 2, h->wpack_bwd, gdim, gstride, box, estride,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DCN_ERR_CUDA;
+    }
+    if (dcn::launch_bwd_data_tc(p, gmap, wmap, s) != cudaSuccess) return DCN_ERR_CUDA;
+    if (dcn::launch_backward_weight(p, dtype, s) != cudaSuccess) return DCN_ERR_CUDA;
+    h->last_path = path;
     return DCN_OK;
 }
 

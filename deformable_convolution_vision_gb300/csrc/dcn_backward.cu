@@ -386,13 +386,9 @@ __global__ void dcn_bwd_bias_kernel(BwdParams p) {
 }
 
 template <typename T>
-cudaError_t launch_backward_t(const BwdParams &p_in, cudaStream_t stream) {
+cudaError_t launch_backward_weight_t(const BwdParams &p_in, cudaStream_t stream) {
     BwdParams p = p_in;
     const int Cg = p.C / p.groups, Og = p.O / p.groups;
-    {
-        const dim3 grid((p.P + BWD_BM - 1) / BWD_BM, (p.C + BWD_BN - 1) / BWD_BN);
-        dcn_bwd_data_kernel<T><<<grid, BWD_THREADS, 0, stream>>>(p);
-    }
     {
         // runs of pixels: enough blocks for several waves on the device
         const int taps = p.kh * p.kw;
@@ -416,12 +412,27 @@ cudaError_t launch_backward_t(const BwdParams &p_in, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_backward_t(const BwdParams &p, cudaStream_t stream) {
+    const dim3 grid((p.P + BWD_BM - 1) / BWD_BM, (p.C + BWD_BN - 1) / BWD_BN);
+    dcn_bwd_data_kernel<T><<<grid, BWD_THREADS, 0, stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_backward_weight_t<T>(p, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_backward(const BwdParams &p, int dtype, cudaStream_t stream) {
     if (dtype == kF32) return launch_backward_t<float>(p, stream);
     if (dtype == kF16) return launch_backward_t<__half>(p, stream);
     return launch_backward_t<__nv_bfloat16>(p, stream);
+}
+
+cudaError_t launch_backward_weight(const BwdParams &p, int dtype, cudaStream_t stream) {
+    if (dtype == kF32) return launch_backward_weight_t<float>(p, stream);
+    if (dtype == kF16) return launch_backward_weight_t<__half>(p, stream);
+    return launch_backward_weight_t<__nv_bfloat16>(p, stream);
 }
 
 }  // namespace dcn

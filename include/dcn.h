@@ -299,11 +299,20 @@ DCN_API dcn_status_t dcn_forward_packed_ex(dcn_handle_t h,
  *   grad_bias   [O] fp32, or NULL (not computed)
  * The gradients are overwritten (zeroed, then accumulated in fp32 with
  * atomic reductions, so the order of the sums, and the last bits, vary from
- * run to run).  Runs on CUDA cores; asynchronous on `stream`; allocates
- * nothing.  Argument rules as dcn_forward / dcn_forward_ex (sizes, NULL
- * inputs, alignment to the element size, 4 bytes for fp32 arrays);
- * DCN_ERR_INVALID_ARG for a NULL x, offset, weight, grad_out, grad_x,
- * grad_offset or grad_weight. */
+ * run to run).  Asynchronous on `stream`.
+ * Kernels: with bf16/fp16 operands, one weight group, C and C/offset_groups
+ * multiples of 64, O a multiple of 64 up to 256, x 32-byte and grad_out and
+ * grad_x 16-byte aligned, the column gradient runs on tcgen05 tensor cores
+ * (fp32 accumulators in tensor memory, never written to memory) fused with
+ * the scatter into grad_x and the offset/mask sums; the handle then keeps a
+ * [kh*kw*C][O] copy of the weight in its workspace (grown on demand, in
+ * stream order).  Otherwise, and for fp32, CUDA cores run it and nothing is
+ * allocated.  dcn_set_path(DCN_PATH_SIMT) forces the CUDA-core kernels;
+ * DCN_PATH_TC returns DCN_ERR_UNSUPPORTED for shapes outside the envelope.
+ * The weight and bias gradients run on CUDA cores.  Argument rules as
+ * dcn_forward / dcn_forward_ex (sizes, NULL inputs, alignment to the
+ * element size, 4 bytes for fp32 arrays); DCN_ERR_INVALID_ARG for a NULL x,
+ * offset, weight, grad_out, grad_x, grad_offset or grad_weight. */
 DCN_API dcn_status_t dcn_backward(dcn_handle_t h,
                           const void *x, const float *offset, const float *mask,
                           const void *weight, const void *grad_out,

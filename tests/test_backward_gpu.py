@@ -37,21 +37,23 @@ def _cotangent(wl, dtype, seed):
     return torch.randn(wl.B, wl.O, Ho, Wo, generator=g).to(dtype)
 
 
-def run_backward(wl, inp, gout):
+def run_backward(wl, inp, gout, path=dcn.DCN_PATH_AUTO):
     d = to_device(inp)
     g = gout.cuda().contiguous(memory_format=torch.channels_last)
-    with dcn.Handle() as h:
+    with dcn.Handle(path) as h:
         r = dcn.deform_conv2d_backward(g, d["x"], d["offset"], d["weight"], stride=wl.stride,
                                        padding=wl.padding, dilation=wl.dilation, mask=d["mask"],
                                        handle=h)
         assert dcn.dcn_sync_status(h.h) == 0
+        if path != dcn.DCN_PATH_AUTO:
+            assert dcn.dcn_last_path(h.h) == path
     return r
 
 
-def check(wl):
+def check(wl, path=dcn.DCN_PATH_AUTO):
     inp = make_general_inputs(wl)
     gout = _cotangent(wl, inp["x"].dtype, wl.seed + 1000)
-    got = run_backward(wl, inp, gout)
+    got = run_backward(wl, inp, gout, path)
     conv = oracle.ConvDesc(stride=wl.stride, padding=wl.padding, dilation=wl.dilation,
                            groups=wl.groups, offset_groups=wl.offset_groups)
     ref = oracle.backward_ex(inp["x"], inp["offset"], inp["mask"], inp["weight"], gout, conv)
@@ -81,6 +83,25 @@ CASES = [
     GW("bwd_general_bf16", 2, 128, 12, 10, 64, 3, 3, (1, 2), (2, 1), (2, 1), 2, 2, "bf16", 2.5, True, 8),
     GW("bwd_1x1", 1, 64, 16, 16, 64, 1, 1, (1, 1), (0, 0), (1, 1), 1, 1, "bf16", 1.0, True, 9),
 ]
+
+# shapes the tensor-core column-gradient kernel takes (16-bit operands, one
+# weight group, C and the offset-group width multiples of 64, O a multiple
+# of 64 up to 256): ragged tiles, several tiles per CTA, several channel
+# blocks and output K-blocks, offset groups, stride and dilation, no mask
+TC_CASES = [
+    GW("bwdtc_ragged", 2, 64, 13, 21, 64, 3, 3, (1, 1), (1, 1), (1, 1), 1, 1, "bf16", 2.0, True, 31),
+    GW("bwdtc_many_tiles", 1, 64, 150, 150, 64, 3, 3, (1, 1), (1, 1), (1, 1), 1, 1, "bf16", 2.0, True, 32),
+    GW("bwdtc_c128_o128", 1, 128, 20, 24, 128, 3, 3, (1, 1), (1, 1), (1, 1), 1, 1, "bf16", 1.5, True, 33),
+    GW("bwdtc_o256", 1, 64, 12, 17, 256, 3, 3, (1, 1), (1, 1), (1, 1), 1, 1, "f16", 2.0, True, 34),
+    GW("bwdtc_og2", 1, 128, 14, 16, 64, 3, 3, (2, 1), (1, 1), (1, 2), 1, 2, "bf16", 2.0, True, 35),
+    GW("bwdtc_5x5_no_mask", 1, 64, 19, 23, 64, 5, 5, (1, 1), (2, 2), (1, 1), 1, 1, "f16", 4.0, False, 36),
+]
+
+
+@pytest.mark.parametrize("wl", TC_CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("path", [dcn.DCN_PATH_TC, dcn.DCN_PATH_SIMT])
+def test_backward_both_paths(wl, path):
+    check(wl, path=path)
 
 
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
