@@ -54,7 +54,7 @@ def test_mutant_is_caught(tmp_path, source, name):
     text = source
     for old, new in MUTANTS[name]:
         assert old in text, f"mutation anchor not found: {old!r}"
-        text = text.replace(old, new)
+        text = text.replace(old, new, 1)   # the first occurrence: the forward's code
     src = os.path.join(tmp_path, f"{name}.c")
     lib = os.path.join(tmp_path, f"{name}.so")
     with open(src, "w") as fh:
