@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
+
 #include "dcn_kernels.h"
 
 namespace dcn {
@@ -259,21 +261,70 @@ dcn_bwd_data_kernel(BwdParams p) {
     }
 }
 
+// Eight consecutive elements as fp32: one 16-byte load for 16-bit types
+// (two for fp32) when `vec`, else element by element with a bound.
+template <typename T>
+__device__ __forceinline__ void load8(const T *src, int n_valid, bool vec, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<float>(const float *src, int n_valid, bool vec, float (&v)[8]) {
+    if (vec && n_valid >= 8) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(src));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(src) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        return;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = e < n_valid ? __ldg(src + e) : 0.0f;
+}
+template <typename T>
+__device__ __forceinline__ void load8_16(const T *src, int n_valid, bool vec, float (&v)[8]) {
+    if (vec && n_valid >= 8) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4 *>(src));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            T lo, hi;
+            const uint16_t l16 = static_cast<uint16_t>(w[e] & 0xFFFFu), h16 = static_cast<uint16_t>(w[e] >> 16);
+            memcpy(&lo, &l16, 2);
+            memcpy(&hi, &h16, 2);
+            v[2 * e] = ld_f32(&lo);
+            v[2 * e + 1] = ld_f32(&hi);
+        }
+        return;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = e < n_valid ? ld_f32(src + e) : 0.0f;
+}
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *src, int n_valid, bool vec,
+                                                     float (&v)[8]) {
+    load8_16(src, n_valid, vec, v);
+}
+template <>
+__device__ __forceinline__ void load8<__half>(const __half *src, int n_valid, bool vec, float (&v)[8]) {
+    load8_16(src, n_valid, vec, v);
+}
+
+constexpr int WG_PX = 32;   // pixels per step of the weight-gradient kernel
+
 // grad_weight.  blockIdx.x: a run of p.pix_run pixels; blockIdx.y: the tap;
 // blockIdx.z: (weight group, 64-output chunk, 64-channel chunk).  Thread
 // (ty, tx) accumulates outputs 4 ty .. +3 x channels 4 tx .. +3 of the tile
-// over the run, then adds them to grad_weight.
+// over the run, 32 pixels per step, then adds them to grad_weight.  Staging
+// thread (tid / 8, tid % 8) loads 8 consecutive outputs (channels) of one
+// pixel.
 template <typename T>
 __global__ void __launch_bounds__(BWD_THREADS)
 dcn_bwd_weight_kernel(BwdParams p) {
-    __shared__ float Gs[BWD_BK][BWD_BM + 4];   // grad_out chunk [pixel][output]
-    __shared__ float As[BWD_BK][BWD_BN + 4];   // sampled chunk [pixel][channel]: m * S
-    __shared__ float4 geo_f[BWD_BK];
-    __shared__ int4 geo_i[BWD_BK];
+    __shared__ __align__(16) float Gs[WG_PX][BWD_BM];   // grad_out step [pixel][output]
+    __shared__ __align__(16) float As[WG_PX][BWD_BN];   // sampled step [pixel][channel]: m * S
+    __shared__ float4 geo_f[WG_PX];
+    __shared__ int4 geo_i[WG_PX];
 
     const T *__restrict__ x = static_cast<const T *>(p.x);
     const T *__restrict__ go = static_cast<const T *>(p.grad_out);
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+    const int sp = tid / 8, s8 = (tid % 8) * 8;          // staging pixel, first of 8 columns
     const int HoWo = p.Ho * p.Wo;
     const int Cg = p.C / p.groups, Og = p.O / p.groups, Cq = p.C / p.ogroups;
     const int o_chunks = (Og + BWD_BM - 1) / BWD_BM;
@@ -288,6 +339,11 @@ dcn_bwd_weight_kernel(BwdParams p) {
     const int i = tap / p.kw, j = tap - (tap / p.kw) * p.kw;
     const int px_lo = blockIdx.x * p.pix_run;
     const int px_hi = min(p.P, px_lo + p.pix_run);
+    // 16-byte staging loads: 8-element runs aligned in every row
+    const bool vec_o = (p.O % 8) == 0 && (o_lo % 8) == 0 &&
+                       (reinterpret_cast<uintptr_t>(go) & 15) == 0;
+    const bool vec_c = (p.C % 8) == 0 && (c_abs % 8) == 0 &&
+                       (reinterpret_cast<uintptr_t>(x) & 15) == 0;
 
     float acc[4][4];
 #pragma unroll
@@ -295,21 +351,25 @@ dcn_bwd_weight_kernel(BwdParams p) {
 #pragma unroll
         for (int s = 0; s < 4; ++s) acc[r][s] = 0.0f;
 
-    for (int p0 = px_lo; p0 < px_hi; p0 += BWD_BK) {
-        __syncthreads();   // the previous chunk is no longer read
+    for (int p0 = px_lo; p0 < px_hi; p0 += WG_PX) {
+        __syncthreads();   // the previous step is no longer read
+        {
+            const int pix = p0 + sp;
+            float v[8];
+            if (pix < px_hi) {
+                load8(go + static_cast<size_t>(pix) * p.O + o_lo + s8, o_n - s8, vec_o, v);
+            } else {
 #pragma unroll
-        for (int e = 0; e < (BWD_BK * BWD_BM) / BWD_THREADS; ++e) {
-            const int idx = tid + e * BWD_THREADS;
-            const int pp = idx / BWD_BM, oo = idx % BWD_BM;
-            const int pix = p0 + pp;
-            Gs[pp][oo] = (pix < px_hi && oo < o_n)
-                ? ld_f32(go + static_cast<size_t>(pix) * p.O + o_lo + oo) : 0.0f;
+                for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+            }
+            *reinterpret_cast<float4 *>(&Gs[sp][s8]) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4 *>(&Gs[sp][s8 + 4]) = make_float4(v[4], v[5], v[6], v[7]);
         }
         // the sampled operand, one offset group of the tile's channels at a time
         for (int q = c_abs / Cq; q * Cq < c_abs + cl_n; ++q) {
             const int cq_lo = max(c_abs, q * Cq), cq_hi = min(c_abs + cl_n, (q + 1) * Cq);
             __syncthreads();   // the previous group's geometry is no longer read
-            if (tid < BWD_BK) {
+            if (tid < WG_PX) {
                 const int pix = p0 + tid;
                 if (pix < px_hi) {
                     const int b = pix / HoWo;
@@ -324,38 +384,50 @@ dcn_bwd_weight_kernel(BwdParams p) {
                 }
             }
             __syncthreads();
+            const int c8 = c_abs + s8;            // this thread's 8 channels
+            if (c8 + 8 > cq_lo && c8 < cq_hi) {
+                const float4 f = geo_f[sp];
+                const int4 ci = geo_i[sp];
+                const int cor[4] = {ci.x, ci.y, ci.z, ci.w};
+                const float wq[4] = {(1.0f - f.x) * (1.0f - f.y), (1.0f - f.x) * f.y,
+                                     f.x * (1.0f - f.y), f.x * f.y};
+                // whole run of 8 inside this offset group: vector loads
+                const bool whole = c8 >= cq_lo && c8 + 8 <= cq_hi;
+                float sv[8];
 #pragma unroll
-            for (int e = 0; e < (BWD_BK * BWD_BN) / BWD_THREADS; ++e) {
-                const int idx = tid + e * BWD_THREADS;
-                const int pp = idx / BWD_BN, cc2 = idx % BWD_BN;
-                const int c = c_abs + cc2;
-                if (c >= cq_lo && c < cq_hi) {
-                    const float4 f = geo_f[pp];
-                    const int4 ci = geo_i[pp];
-                    const float v00 = ci.x >= 0 ? ld_f32(x + ci.x + c) : 0.0f;
-                    const float v01 = ci.y >= 0 ? ld_f32(x + ci.y + c) : 0.0f;
-                    const float v10 = ci.z >= 0 ? ld_f32(x + ci.z + c) : 0.0f;
-                    const float v11 = ci.w >= 0 ? ld_f32(x + ci.w + c) : 0.0f;
-                    const float S = (1.0f - f.x) * ((1.0f - f.y) * v00 + f.y * v01) +
-                                    f.x * ((1.0f - f.y) * v10 + f.y * v11);
-                    As[pp][cc2] = f.z * S;
-                } else if (cc2 >= cl_n) {
-                    As[pp][cc2] = 0.0f;
+                for (int e = 0; e < 8; ++e) sv[e] = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (cor[k] < 0) continue;
+                    float v[8];
+                    load8(x + cor[k] + c8, cq_hi - c8, vec_c && whole, v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) sv[e] = fmaf(wq[k], v[e], sv[e]);
                 }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = c8 + e;
+                    if (c >= cq_lo && c < cq_hi) As[sp][s8 + e] = f.z * sv[e];
+                }
+            }
+            if (s8 < BWD_BN) {
+                // channels past the tile's end stay zero
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (s8 + e >= cl_n) As[sp][s8 + e] = 0.0f;
             }
         }
         __syncthreads();
-#pragma unroll
-        for (int kk = 0; kk < BWD_BK; ++kk) {
-            float a[4], b[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) a[r] = Gs[kk][ty * 4 + r];
-#pragma unroll
-            for (int s = 0; s < 4; ++s) b[s] = As[kk][tx * 4 + s];
+#pragma unroll 8
+        for (int kk = 0; kk < WG_PX; ++kk) {
+            const float4 a = *reinterpret_cast<const float4 *>(&Gs[kk][ty * 4]);
+            const float4 bq = *reinterpret_cast<const float4 *>(&As[kk][tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+            const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(a[r], b[s], acc[r][s]);
+                for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(av[r], bv[s], acc[r][s]);
         }
     }
 #pragma unroll
@@ -398,7 +470,7 @@ cudaError_t launch_backward_weight_t(const BwdParams &p_in, cudaStream_t stream)
                          (static_cast<long long>(taps) * tiles);
         runs = runs < 1 ? 1 : runs;
         int run = static_cast<int>((p.P + runs - 1) / runs);
-        run = ((run + BWD_BK - 1) / BWD_BK) * BWD_BK;
+        run = ((run + WG_PX - 1) / WG_PX) * WG_PX;
         if (run < 256) run = 256;
         p.pix_run = run;
         const dim3 grid((p.P + run - 1) / run, taps, tiles);
