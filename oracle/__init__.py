@@ -38,16 +38,21 @@ LIBRARY = os.path.join(_HERE, "libdcn_oracle.so")
 CFLAGS = ["-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off"]
 
 
-def compile_oracle(source=SOURCE, output=LIBRARY):
-    """Compile the oracle's C source into a shared library (gcc)."""
-    cmd = ["gcc", *CFLAGS, source, "-o", output, "-lm"]
+MSDA_SOURCE = os.path.join(_HERE, "msda_oracle.c")
+
+
+def compile_oracle(source=SOURCE, output=LIBRARY, extra=(MSDA_SOURCE,)):
+    """Compile the oracle's C sources into a shared library (gcc)."""
+    cmd = ["gcc", *CFLAGS, source, *extra, "-o", output, "-lm"]
     subprocess.run(cmd, check=True)
     return output
 
 
 def _stale(source, output):
-    return (not os.path.exists(output)
-            or os.path.getmtime(output) < os.path.getmtime(source))
+    if not os.path.exists(output):
+        return True
+    built = os.path.getmtime(output)
+    return any(os.path.getmtime(s) > built for s in (source, MSDA_SOURCE))
 
 
 class Oracle:
@@ -72,6 +77,9 @@ class Oracle:
         lib.oracle_dcn_backward_ex.restype = i
         lib.oracle_dcn_backward_points_ex.argtypes = [f] * 5 + [f, i, f, f, f, i]
         lib.oracle_dcn_backward_points_ex.restype = i
+        if hasattr(lib, "oracle_msda_forward"):
+            lib.oracle_msda_forward.argtypes = [f, f, f, i, f, f, i, f] + [i] * 7
+            lib.oracle_msda_forward.restype = i
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i
         self._lib = lib
@@ -234,6 +242,29 @@ class Oracle:
                                 nthreads)
 
 
+    # --------------------------------------------------------------- MSDA
+
+    def msda_forward(self, value, shapes, starts, locations, weights, softmax=False, nthreads=0):
+        """Multi-scale deformable attention: value [B, S, G, D], shapes [L, 2]
+        (H, W), starts [L], locations [B, Q, G, L, K, 2], weights
+        [B, Q, G, L*K]; returns out [B, Q, G, D] in fp64."""
+        value, locations, weights = (self._f32(t) for t in (value, locations, weights))
+        shapes = np.ascontiguousarray(np.asarray(shapes), dtype=np.int32).reshape(-1, 2)
+        starts = np.ascontiguousarray(np.asarray(starts), dtype=np.int32).reshape(-1)
+        B, S, G, D = value.shape
+        L = shapes.shape[0]
+        Bq, Q, G2, L2, K, two = locations.shape
+        if (Bq, G2, L2, two) != (B, G, L, 2) or weights.shape != (B, Q, G, L * K) or starts.shape != (L,):
+            raise ValueError("msda shapes do not match")
+        out = np.empty((B, Q, G, D), dtype=np.float64)
+        rc = self._lib.oracle_msda_forward(self._ptr(value), self._ptr(shapes), self._ptr(starts), L,
+                                           self._ptr(locations), self._ptr(weights), int(bool(softmax)),
+                                           self._ptr(out), B, S, G, D, Q, K, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_msda_forward rejected its arguments")
+        return out
+
+
 class ConvDesc:
     """Convolution parameters of the general problem: stride, padding and
     dilation as (h, w) pairs (an int means both), weight groups and offset
@@ -293,3 +324,7 @@ def backward_ex(*args, **kwargs):
 
 def backward_points_ex(*args, **kwargs):
     return get().backward_points_ex(*args, **kwargs)
+
+
+def msda_forward(*args, **kwargs):
+    return get().msda_forward(*args, **kwargs)
