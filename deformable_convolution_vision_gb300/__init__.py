@@ -13,6 +13,7 @@ from . import binding
 from .binding import (DCN_BF16, DCN_F16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
                       DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, ConvDesc, DcnError, dcn_create,
                       dcn_backward, dcn_backward_ex, dcn_destroy, dcn_forward, dcn_forward_ex,
+                      dcn_msda_forward,
                       dcn_forward_host,
                       dcn_forward_packed, dcn_forward_packed_ex, dcn_last_path, dcn_out_size,
                       dcn_pack_weight, dcn_pack_weight_ex, dcn_selftest_timeout, dcn_set_path,
@@ -25,7 +26,7 @@ __all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF1
            "dcn_set_path", "dcn_last_path", "dcn_sync_status", "dcn_selftest_timeout",
            "dcn_status_string", "ConvDesc", "dcn_forward_ex", "dcn_pack_weight_ex",
            "dcn_forward_packed_ex", "dcn_out_size", "dcn_backward", "dcn_backward_ex",
-           "deform_conv2d_backward"]
+           "deform_conv2d_backward", "dcn_msda_forward", "msda"]
 
 
 class Handle:
@@ -179,3 +180,34 @@ def deform_conv2d_backward(grad_out, x, offset, weight, stride=1, padding=0, dil
             h.close()
     return {"grad_x": gx, "grad_offset": goff, "grad_mask": gm, "grad_weight": gw,
             "grad_bias": gb}
+
+
+def msda(value, shapes, starts, locations, weights, method=None, out=None, stream=None):
+    """Multi-scale deformable attention forward (the deformops functional
+    form): value [B, S, G, D] (float32/bfloat16/float16, contiguous),
+    shapes [L, 2] of (H, W) and starts [L] (any sequence or tensor; read on
+    the host), locations [B, Q, G, L, K, 2] float32 normalized (x, y),
+    weights [B, Q, G, L*K] float32, method None (weights as given) or
+    "softmax".  Returns out [B, Q, G, D] in value's dtype.  Layouts are
+    checked, never converted."""
+    import torch
+    if method not in (None, "softmax"):
+        raise ValueError("method must be None or 'softmax'")
+    shapes = [tuple(int(v) for v in hw) for hw in (shapes.tolist() if hasattr(shapes, "tolist") else shapes)]
+    starts = [int(v) for v in (starts.tolist() if hasattr(starts, "tolist") else starts)]
+    if len(shapes) != len(starts):
+        raise ValueError("shapes and starts must describe the same levels")
+    for name, t in (("value", value), ("locations", locations), ("weights", weights)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if locations.dtype != torch.float32 or weights.dtype != torch.float32:
+        raise TypeError("locations and weights must be float32")
+    B, S, G, D = value.shape
+    Bq, Q, G2, L, K, two = locations.shape
+    if (Bq, G2, L, two) != (B, G, len(shapes), 2) or tuple(weights.shape) != (B, Q, G, L * K):
+        raise ValueError("locations must be [B, Q, G, L, K, 2] and weights [B, Q, G, L*K]")
+    if out is None:
+        out = torch.empty((B, Q, G, D), dtype=value.dtype, device=value.device)
+    dcn_msda_forward(value, shapes, starts, locations, weights, out, B, S, G, D, Q, K,
+                     method == "softmax", _dtype_code(value), stream)
+    return out

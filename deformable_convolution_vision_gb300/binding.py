@@ -23,7 +23,7 @@ EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_f
            "dcn_forward_host", "dcn_set_path", "dcn_last_path", "dcn_sync_status",
            "dcn_selftest_timeout", "dcn_status_string", "dcn_forward_noalloc",
            "dcn_set_sample_precision", "dcn_out_size", "dcn_forward_ex", "dcn_pack_weight_ex",
-           "dcn_forward_packed_ex", "dcn_backward", "dcn_backward_ex"]
+           "dcn_forward_packed_ex", "dcn_backward", "dcn_backward_ex", "dcn_msda_forward"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -73,6 +73,7 @@ def load():
         "dcn_forward_packed_ex": ([P, P, P, P, P, P, ctypes.POINTER(ConvDesc), I, P], I),
         "dcn_backward": ([P] * 11 + [I] * 9 + [P], I),
         "dcn_backward_ex": ([P] * 11 + [ctypes.POINTER(ConvDesc), I, P], I),
+        "dcn_msda_forward": ([P, P, P, I, P, P, P] + [I] * 8 + [P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -213,3 +214,14 @@ def dcn_backward_ex(h, x, offset, mask, weight, grad_out, grad_x, grad_offset, g
                                   _ptr(grad_weight), _ptr(grad_bias), ctypes.byref(desc), dtype,
                                   _stream(stream)),
            "dcn_backward_ex")
+
+
+def dcn_msda_forward(value, shapes, starts, locations, weights, out, B, S, G, D, Q, K, softmax,
+                     dtype, stream=None):
+    """shapes: host sequence of (H, W) pairs; starts: host sequence of row offsets."""
+    L = len(starts)
+    sh = (ctypes.c_int * (2 * L))(*[int(v) for hw in shapes for v in hw])
+    st = (ctypes.c_int * L)(*[int(v) for v in starts])
+    _check(load().dcn_msda_forward(_ptr(value), sh, st, L, _ptr(locations), _ptr(weights), _ptr(out),
+                                   B, S, G, D, Q, K, int(bool(softmax)), dtype, _stream(stream)),
+           "dcn_msda_forward")

@@ -576,6 +576,40 @@ dcn_status_t dcn_backward_ex(dcn_handle_t h, const void *x, const float *offset,
                             grad_weight, grad_bias, c, dtype, stream);
 }
 
+dcn_status_t dcn_msda_forward(const void *value, const int *shapes, const int *starts, int L,
+                              const float *locations, const float *weights, void *out, int B,
+                              int S, int G, int D, int Q, int K, int softmax, int dtype,
+                              void *stream) {
+    if (!value || !shapes || !starts || !locations || !weights || !out) return DCN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
+    if (B <= 0 || S <= 0 || G <= 0 || D <= 0 || Q <= 0 || K <= 0) return DCN_ERR_INVALID_ARG;
+    if (L <= 0 || L > dcn::kMsdaMaxLevels) return DCN_ERR_UNSUPPORTED;
+    const long long LK = static_cast<long long>(L) * K;
+    if (static_cast<long long>(B) * S * G * D > kIndexLimit ||
+        static_cast<long long>(B) * Q * G * LK * 2 > kIndexLimit ||
+        static_cast<long long>(B) * Q * G * D > kIndexLimit)
+        return DCN_ERR_INVALID_ARG;
+    const size_t es = esize(dtype);
+    if (!aligned(value, es) || !aligned(out, es) || !aligned(locations, 8) || !aligned(weights, 4))
+        return DCN_ERR_INVALID_ARG;
+    dcn::MsdaParams p;
+    for (int l = 0; l < L; ++l) {
+        const int H = shapes[2 * l], W = shapes[2 * l + 1];
+        if (H <= 0 || W <= 0 || starts[l] < 0 ||
+            static_cast<long long>(starts[l]) + static_cast<long long>(H) * W > S)
+            return DCN_ERR_INVALID_ARG;
+        p.H[l] = H;
+        p.W[l] = W;
+        p.start[l] = starts[l];
+    }
+    p.value = value; p.locations = locations; p.weights = weights; p.out = out;
+    p.B = B; p.S = S; p.G = G; p.D = D; p.Q = Q; p.K = K; p.L = L;
+    p.softmax = softmax ? 1 : 0;
+    const bool vec = D % (dtype == DCN_F32 ? 4 : 8) == 0 && aligned(value, 16) && aligned(out, 16);
+    if (dcn::launch_msda(p, dtype, vec, as_stream(stream)) != cudaSuccess) return DCN_ERR_CUDA;
+    return DCN_OK;
+}
+
 int dcn_out_size(int n, int k, int stride, int pad, int dil) {
     if (n <= 0 || k <= 0 || stride <= 0 || pad < 0 || dil <= 0) return 0;
     const long long r = out_size_ll(n, k, stride, pad, dil);

@@ -149,6 +149,21 @@ cudaError_t launch_backward_weight(const BwdParams &p, int dtype, cudaStream_t s
 // grad_weight (one kernel), grad_bias (one kernel, when wanted).
 cudaError_t launch_backward(const BwdParams &p, int dtype, cudaStream_t stream);
 
+// Multi-scale deformable attention forward (device pointers; the level
+// table by value).
+constexpr int kMsdaMaxLevels = 8;
+struct MsdaParams {
+    const void *value;        // [B, S, G, D], the operand dtype
+    const float *locations;   // [B, Q, G, L, K, 2], normalized (x, y)
+    const float *weights;     // [B, Q, G, L*K]
+    void *out;                // [B, Q, G, D], the operand dtype
+    int B, S, G, D, Q, K, L;
+    int softmax;              // 1: normalize the weights over L*K
+    int H[kMsdaMaxLevels], W[kMsdaMaxLevels], start[kMsdaMaxLevels];
+};
+// vec: D a multiple of 8 (16-bit) or 4 (fp32) and value/out 16-byte aligned.
+cudaError_t launch_msda(const MsdaParams &p, int dtype, bool vec, cudaStream_t stream);
+
 // One-thread kernel whose barrier wait runs out after timeout_ns.
 cudaError_t launch_selftest_timeout(unsigned *status, unsigned long long timeout_ns,
                                     cudaStream_t stream);

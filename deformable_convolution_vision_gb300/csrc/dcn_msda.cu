@@ -1,0 +1,169 @@
+// Multi-scale deformable attention (MSDA), forward, on CUDA cores.
+//
+// The operator of page "deformops 3.0.1", section "Multi-scale deformable
+// attention" (functional form msda(value, shapes, starts, locations,
+// weights, method)): for batch b, query q, head g and channel d,
+//   out[b,q,g,d] = sum_{l,k} a[b,q,g,l,k] * bilinear(level l of value[b,:,g,d],
+//                                                   loc[b,q,g,l,k] * (W_l, H_l) - 0.5)
+// with zero padding, the weights a used as given or softmax-normalized over
+// the L*K entries of (b, q, g).  It shares the deformable convolution's
+// sampler rule (four corners, outside ones contribute nothing) but has no
+// contraction: the projections around it are dense layers outside the
+// operator, so the work is gathers and multiply-adds (CUDA cores), bound by
+// the L1/L2 traffic of the corner reads.
+//
+// One thread per CH consecutive channels of one (b, q, g): CH = 8 for
+// 16-bit values and 4 for fp32 (one 16-byte load per corner), or 1.  The
+// D / CH threads of a (b, q, g) are neighbours in the warp; with D = 32 and
+// G = 8 (16-bit) a warp is one query.  Each thread reads its (b, q, g)'s
+// logits and locations (the same addresses for the D / CH threads: one
+// broadcast request), computes the softmax in fp32, then for every sample
+// the corners and their weights, and accumulates CH fp32 sums.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstring>
+
+#include "dcn_kernels.h"
+
+namespace dcn {
+
+namespace {
+
+// CH elements as fp32 from a 16-byte (or one-element) load.
+template <typename T, int CH>
+__device__ __forceinline__ void msda_load(const T *p, float (&v)[CH]);
+
+template <>
+__device__ __forceinline__ void msda_load<float, 4>(const float *p, float (&v)[4]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+template <>
+__device__ __forceinline__ void msda_load<__nv_bfloat16, 8>(const __nv_bfloat16 *p, float (&v)[8]) {
+    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(w[e] << 16);
+        v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void msda_load<__half, 8>(const __half *p, float (&v)[8]) {
+    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        __half2 h;
+        memcpy(&h, &w[e], 4);
+        const float2 f = __half22float2(h);
+        v[2 * e] = f.x;
+        v[2 * e + 1] = f.y;
+    }
+}
+template <>
+__device__ __forceinline__ void msda_load<float, 1>(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
+template <>
+__device__ __forceinline__ void msda_load<__nv_bfloat16, 1>(const __nv_bfloat16 *p, float (&v)[1]) {
+    v[0] = __bfloat162float(*p);
+}
+template <>
+__device__ __forceinline__ void msda_load<__half, 1>(const __half *p, float (&v)[1]) {
+    v[0] = __half2float(*p);
+}
+
+template <typename T> __device__ __forceinline__ T msda_from_f32(float v);
+template <> __device__ __forceinline__ float msda_from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 msda_from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+template <> __device__ __forceinline__ __half msda_from_f32<__half>(float v) { return __float2half_rn(v); }
+
+template <typename T, int CH>
+__global__ void __launch_bounds__(256)
+msda_forward_kernel(MsdaParams p) {
+    const int per_row = p.D / CH;                        // threads per (b, q, g)
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long rows = static_cast<long long>(p.B) * p.Q * p.G;
+    if (t >= rows * per_row) return;
+    const long long row = t / per_row;                   // (b, q, g)
+    const int d0 = static_cast<int>(t - row * per_row) * CH;
+    const int g = static_cast<int>(row % p.G);
+    const int b = static_cast<int>(row / (static_cast<long long>(p.Q) * p.G));
+    const int LK = p.L * p.K;
+    const float *__restrict__ wrow = p.weights + row * LK;
+    const float *__restrict__ lrow = p.locations + row * LK * 2;
+    const T *__restrict__ value = static_cast<const T *>(p.value);
+
+    // attention weights: as given, or softmax over the L*K logits (fp32,
+    // largest logit subtracted first)
+    float wmax = -INFINITY, wsum = 1.0f;
+    if (p.softmax) {
+        for (int i = 0; i < LK; ++i) wmax = fmaxf(wmax, __ldg(wrow + i));
+        wsum = 0.0f;
+        for (int i = 0; i < LK; ++i) wsum += expf(__ldg(wrow + i) - wmax);
+    }
+    const float inv = 1.0f / wsum;
+
+    float acc[CH];
+#pragma unroll
+    for (int e = 0; e < CH; ++e) acc[e] = 0.0f;
+    for (int l = 0; l < p.L; ++l) {
+        const int H = p.H[l], W = p.W[l];
+        const size_t level0 = static_cast<size_t>(b) * p.S + p.start[l];
+        for (int k = 0; k < p.K; ++k) {
+            const int i = l * p.K + k;
+            const float lw = __ldg(wrow + i);
+            const float a = p.softmax ? expf(lw - wmax) * inv : lw;
+            const float2 loc = __ldg(reinterpret_cast<const float2 *>(lrow) + i);
+            // pixel coordinates, rounded as two separate fp32 operations
+            float px = __fsub_rn(__fmul_rn(loc.x, static_cast<float>(W)), 0.5f);
+            float py = __fsub_rn(__fmul_rn(loc.y, static_cast<float>(H)), 0.5f);
+            // beyond [-2, size+1] every corner is outside: clamping keeps the
+            // conversion in range (NaN -> -2) and changes no result
+            px = fminf(fmaxf(px, -2.0f), static_cast<float>(W + 1));
+            py = fminf(fmaxf(py, -2.0f), static_cast<float>(H + 1));
+            const float fx = floorf(px), fy = floorf(py);
+            const float lx = px - fx, ly = py - fy;
+            const int x0 = static_cast<int>(fx), y0 = static_cast<int>(fy);
+            const float cw[4] = {(1.0f - ly) * (1.0f - lx) * a, (1.0f - ly) * lx * a,
+                                 ly * (1.0f - lx) * a, ly * lx * a};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int yy = y0 + (c >> 1), xx = x0 + (c & 1);
+                if (static_cast<unsigned>(yy) >= static_cast<unsigned>(H) ||
+                    static_cast<unsigned>(xx) >= static_cast<unsigned>(W))
+                    continue;
+                float v[CH];
+                msda_load<T, CH>(value + ((level0 + static_cast<size_t>(yy) * W + xx) * p.G + g) * p.D + d0, v);
+#pragma unroll
+                for (int e = 0; e < CH; ++e) acc[e] = fmaf(cw[c], v[e], acc[e]);
+            }
+        }
+    }
+    T *__restrict__ out = static_cast<T *>(p.out) + row * p.D + d0;
+#pragma unroll
+    for (int e = 0; e < CH; ++e) out[e] = msda_from_f32<T>(acc[e]);
+}
+
+template <typename T, int CH>
+cudaError_t launch_msda_t(const MsdaParams &p, cudaStream_t stream) {
+    const long long threads = static_cast<long long>(p.B) * p.Q * p.G * (p.D / CH);
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 2147483647ll) return cudaErrorInvalidValue;
+    msda_forward_kernel<T, CH><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_msda(const MsdaParams &p, int dtype, bool vec, cudaStream_t stream) {
+    if (dtype == kF32)
+        return vec ? launch_msda_t<float, 4>(p, stream) : launch_msda_t<float, 1>(p, stream);
+    if (dtype == kF16)
+        return vec ? launch_msda_t<__half, 8>(p, stream) : launch_msda_t<__half, 1>(p, stream);
+    return vec ? launch_msda_t<__nv_bfloat16, 8>(p, stream) : launch_msda_t<__nv_bfloat16, 1>(p, stream);
+}
+
+}  // namespace dcn

@@ -178,3 +178,63 @@ def make_general_inputs(wl: GeneralWorkload):
         "weight": weight.to(dt),
         "bias": bias.contiguous(),
     }
+
+
+@dataclass(frozen=True)
+class MsdaWorkload:
+    """Multi-scale deformable attention (the deformops page's functional
+    form): value [B, S, G, D] ~ N(0, 1) in the compute dtype, locations
+    [B, Q, G, L, K, 2] ~ U(lo, hi) (normalized; beyond [0, 1] some corners
+    fall outside), weights [B, Q, G, L*K] ~ U(0, 1) raw logits (softmax
+    applied in the operator when `softmax`)."""
+    name: str
+    B: int
+    G: int
+    D: int
+    shapes: tuple          # ((H, W), ...) per level
+    Q: int
+    K: int
+    dtype: str = "bf16"
+    softmax: bool = True
+    loc_lo: float = 0.0
+    loc_hi: float = 1.0
+    seed: int = 0
+
+    @property
+    def starts(self):
+        out, s = [], 0
+        for h, w in self.shapes:
+            out.append(s)
+            s += h * w
+        return out
+
+    @property
+    def S(self):
+        return sum(h * w for h, w in self.shapes)
+
+    @property
+    def L(self):
+        return len(self.shapes)
+
+
+def make_msda_inputs(wl: MsdaWorkload):
+    g = torch.Generator().manual_seed(wl.seed)
+    value = torch.randn(wl.B, wl.S, wl.G, wl.D, generator=g)
+    loc = torch.rand(wl.B, wl.Q, wl.G, wl.L, wl.K, 2, generator=g) * (wl.loc_hi - wl.loc_lo) + wl.loc_lo
+    weights = torch.rand(wl.B, wl.Q, wl.G, wl.L * wl.K, generator=g)
+    return {"value": value.to(TORCH_DTYPE[wl.dtype]), "locations": loc.contiguous(),
+            "weights": weights.contiguous()}
+
+
+_PAGE_LEVELS = ((64, 64), (32, 32), (16, 16), (8, 8))
+MSDA_WORKLOADS = {
+    w.name: w for w in [
+        # the page's layer example: 300 queries over four levels
+        MsdaWorkload("msda_page", 1, 8, 32, _PAGE_LEVELS, 300, 4, seed=60),
+        # encoder scale: every pixel of the four levels is a query (5440)
+        MsdaWorkload("msda_encoder", 1, 8, 32, _PAGE_LEVELS, 5440, 4, seed=61),
+        # the upper end of the page's 5k-22k queries per call
+        MsdaWorkload("msda_encoder_22k", 1, 8, 32, ((128, 128), (64, 64), (32, 32), (16, 16)),
+                     21760, 4, seed=62),
+    ]
+}

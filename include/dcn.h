@@ -327,6 +327,38 @@ DCN_API dcn_status_t dcn_backward_ex(dcn_handle_t h,
                              float *grad_weight, float *grad_bias,
                              const dcn_conv_desc_t *desc, int dtype, void *stream);
 
+/* ------------------------------------------------ multi-scale deformable attention
+ *
+ * The forward pass of the operator of page "deformops 3.0.1", section
+ * "Multi-scale deformable attention" (its functional form msda(value,
+ * shapes, starts, locations, weights, method)), which shares the
+ * deformable convolution's bilinear sampler.  B batch, G heads, D channels
+ * per head, Q queries, L levels, K points per level:
+ *
+ *   out[b,q,g,d] = sum_{l,k} a[b,q,g,l,k] * S_l(b, g, d, py, px),
+ *   px = loc[b,q,g,l,k,0] * W_l - 0.5,  py = loc[b,q,g,l,k,1] * H_l - 0.5,
+ *
+ * S_l the bilinear sample of level l (corners outside it contribute 0), a
+ * the weights as given or, with softmax != 0, softmax-normalized over the
+ * L*K entries of each (b, q, g).  The pages fix neither the coordinate axis
+ * order nor the normalization; these are the Deformable DETR convention
+ * ((x, y), pixel centres at (i + 0.5) / size).
+ *
+ * Layouts (device pointers, dense):
+ *   value     [B, S, G, D]          `dtype`; level l occupies rows
+ *                                   starts[l] .. + H_l*W_l (row y*W_l + x)
+ *   locations [B, Q, G, L, K, 2]    fp32, 8-byte aligned
+ *   weights   [B, Q, G, L*K]        fp32
+ *   out       [B, Q, G, D]          `dtype`
+ *   shapes    HOST int[L][2] = (H_l, W_l);  starts  HOST int[L]
+ * Arithmetic in fp32 (coordinates, weights, softmax, sums), one rounding to
+ * `dtype` at the end.  1 <= L <= 8 (else DCN_ERR_UNSUPPORTED); every level
+ * inside [0, S).  Asynchronous on `stream`; allocates nothing; no handle. */
+DCN_API dcn_status_t dcn_msda_forward(const void *value, const int *shapes, const int *starts,
+                              int L, const float *locations, const float *weights, void *out,
+                              int B, int S, int G, int D, int Q, int K, int softmax,
+                              int dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -59,3 +59,36 @@ def test_create_without_device_reports_no_device(lib):
     h = ctypes.c_void_p()
     assert lib.dcn_create(ctypes.byref(h)) == binding.STATUS_CODE["DCN_ERR_NO_DEVICE"]
     assert h.value is None
+
+
+def test_python_wrappers_marshal_every_argument(lib):
+    """Each binding wrapper passes exactly the arguments its C function
+    takes; NULL pointers come back as DCN_ERR_INVALID_ARG before any launch
+    (no device is touched)."""
+    bad = binding.STATUS_CODE["DCN_ERR_INVALID_ARG"]
+    h = ctypes.c_void_p()   # NULL handle
+    desc = binding.ConvDesc(1, 64, 8, 8, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1)
+    calls = [
+        lambda: binding.dcn_forward(h, None, None, None, None, None, None, 1, 64, 8, 8, 64, 3, 3, 1,
+                                    1, 0),
+        lambda: binding.dcn_forward_packed(h, None, None, None, None, None, 1, 64, 8, 8, 64, 3, 3, 1,
+                                           1, 0),
+        lambda: binding.dcn_pack_weight(h, None, 64, 64, 3, 3, 1, 0),
+        lambda: binding.dcn_forward_host(h, None, None, None, None, None, None, 1, 64, 8, 8, 64, 3, 3,
+                                         1, 1, 0),
+        lambda: binding.dcn_forward_ex(h, None, None, None, None, None, None, desc, 1, 0),
+        lambda: binding.dcn_pack_weight_ex(h, None, desc, 1, 0),
+        lambda: binding.dcn_forward_packed_ex(h, None, None, None, None, None, desc, 1, 0),
+        lambda: binding.dcn_forward_noalloc(None, None, None, None, None, None, 1, 64, 8, 8, 64, 3,
+                                            3, 1, 1, 0),
+        lambda: binding.dcn_backward(h, None, None, None, None, None, None, None, None, None, None,
+                                     1, 64, 8, 8, 64, 3, 3, 1, 1, 0),
+        lambda: binding.dcn_backward_ex(h, None, None, None, None, None, None, None, None, None,
+                                        None, desc, 1, 0),
+        lambda: binding.dcn_msda_forward(None, [(8, 8)], [0], None, None, None, 1, 64, 8, 32, 10,
+                                         4, True, 1, 0),
+    ]
+    for call in calls:
+        with pytest.raises(binding.DcnError) as e:
+            call()
+        assert e.value.status == bad
