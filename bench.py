@@ -281,6 +281,56 @@ def time_backward(args, wl, dcn, torch, dev, stream, h, x, off, m, w, flush, cod
                          "scope": "whole dcn_backward call"}}
 
 
+def msda_bytes(m, es):
+    """Algorithmic HBM bytes of one MSDA call: value, locations, weights and
+    out, each moved once."""
+    return (m.B * m.S * m.G * m.D * es + m.B * m.Q * m.G * m.L * m.K * 2 * 4
+            + m.B * m.Q * m.G * m.L * m.K * 4 + m.B * m.Q * m.G * m.D * es)
+
+
+def time_msda(args, dcn, torch, dev, stream, flush, pk):
+    """Multi-scale deformable attention forward on the encoder-scale
+    workloads: CUDA events around each call, L2 flushed before each."""
+    if args.no_msda:
+        return None
+    from deformable_convolution_vision_gb300.inputs import MSDA_WORKLOADS, make_msda_inputs
+    res = {}
+    for name in ("msda_encoder", "msda_encoder_22k"):
+        m = MSDA_WORKLOADS[name]
+        inp = make_msda_inputs(m)
+        v = inp["value"].to(dev)
+        loc = inp["locations"].to(dev)
+        w = inp["weights"].to(dev)
+        out = torch.empty((m.B, m.Q, m.G, m.D), dtype=v.dtype, device=dev)
+        call = lambda: dcn.msda(v, m.shapes, m.starts, loc, w, method="softmax", out=out, stream=stream)
+        for _ in range(5):
+            flush.fill_(3)
+            call()
+        n = max(3, min(args.steps, 200))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for k in range(n):
+            flush.fill_(k & 0xFF)
+            ev[k][0].record(stream)
+            call()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        us = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+        es = v.element_size()
+        nbytes = msda_bytes(m, es)
+        samples = m.B * m.Q * m.G * m.L * m.K
+        achieved = nbytes / (us * 1e-6) / 1e9
+        res[name] = {
+            "config": f"B={m.B} G={m.G} D={m.D} levels={list(m.shapes)} Q={m.Q} K={m.K} "
+                      f"{m.dtype} softmax",
+            "us_per_call": us, "queries_per_s": m.B * m.Q / (us * 1e-6),
+            "samples_per_s": samples / (us * 1e-6), "calls": n,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm_gbs"], "algorithmic_bytes": nbytes,
+                         "corner_bytes_on_chip": samples * 4 * m.D * es,
+                         "scope": "whole dcn_msda_forward call (one kernel)"}}
+    return res
+
+
 def run_ours(args, wl, rank, local_rank, world):
     import torch
     import deformable_convolution_vision_gb300 as dcn
@@ -380,6 +430,7 @@ def run_ours(args, wl, rank, local_rank, world):
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     e2e_max = reduce_max(e2e_s, world)
     backward = time_backward(args, wl, dcn, torch, dev, stream, h, x, off, m, w, flush, code)
+    msda = time_msda(args, dcn, torch, dev, stream, flush, peaks()[0])
     h.close()
 
     if rank != 0:
@@ -417,6 +468,8 @@ def run_ours(args, wl, rank, local_rank, world):
     }
     if backward is not None:
         line["backward"] = backward
+    if msda is not None:
+        line["msda"] = msda
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -434,6 +487,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--backward-steps", type=int, default=50)
+    ap.add_argument("--no-msda", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -17,8 +17,10 @@
 // D / CH threads of a (b, q, g) are neighbours in the warp; with D = 32 and
 // G = 8 (16-bit) a warp is one query.  Each thread reads its (b, q, g)'s
 // logits and locations (the same addresses for the D / CH threads: one
-// broadcast request), computes the softmax in fp32, then for every sample
-// the corners and their weights, and accumulates CH fp32 sums.
+// broadcast request), computes the softmax in fp32, then per level the
+// corners and weights of all its points (unrolled for 4 and 8 points, so
+// that every corner load of a level is in flight at once) and accumulates
+// CH fp32 sums.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -80,7 +82,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 msda_from_f32<__nv_bfloat16
 }
 template <> __device__ __forceinline__ __half msda_from_f32<__half>(float v) { return __float2half_rn(v); }
 
-template <typename T, int CH>
+template <typename T, int CH, int KP>
 __global__ void __launch_bounds__(256)
 msda_forward_kernel(MsdaParams p) {
     const int per_row = p.D / CH;                        // threads per (b, q, g)
@@ -91,7 +93,8 @@ msda_forward_kernel(MsdaParams p) {
     const int d0 = static_cast<int>(t - row * per_row) * CH;
     const int g = static_cast<int>(row % p.G);
     const int b = static_cast<int>(row / (static_cast<long long>(p.Q) * p.G));
-    const int LK = p.L * p.K;
+    const int K = KP > 0 ? KP : p.K;                     // points per level
+    const int LK = p.L * K;
     const float *__restrict__ wrow = p.weights + row * LK;
     const float *__restrict__ lrow = p.locations + row * LK * 2;
     const T *__restrict__ value = static_cast<const T *>(p.value);
@@ -112,33 +115,49 @@ msda_forward_kernel(MsdaParams p) {
     for (int l = 0; l < p.L; ++l) {
         const int H = p.H[l], W = p.W[l];
         const size_t level0 = static_cast<size_t>(b) * p.S + p.start[l];
-        for (int k = 0; k < p.K; ++k) {
-            const int i = l * p.K + k;
-            const float lw = __ldg(wrow + i);
-            const float a = p.softmax ? expf(lw - wmax) * inv : lw;
-            const float2 loc = __ldg(reinterpret_cast<const float2 *>(lrow) + i);
-            // pixel coordinates, rounded as two separate fp32 operations
-            float px = __fsub_rn(__fmul_rn(loc.x, static_cast<float>(W)), 0.5f);
-            float py = __fsub_rn(__fmul_rn(loc.y, static_cast<float>(H)), 0.5f);
-            // beyond [-2, size+1] every corner is outside: clamping keeps the
-            // conversion in range (NaN -> -2) and changes no result
-            px = fminf(fmaxf(px, -2.0f), static_cast<float>(W + 1));
-            py = fminf(fmaxf(py, -2.0f), static_cast<float>(H + 1));
-            const float fx = floorf(px), fy = floorf(py);
-            const float lx = px - fx, ly = py - fy;
-            const int x0 = static_cast<int>(fx), y0 = static_cast<int>(fy);
-            const float cw[4] = {(1.0f - ly) * (1.0f - lx) * a, (1.0f - ly) * lx * a,
-                                 ly * (1.0f - lx) * a, ly * lx * a};
+        // With a compile-time point count every point of the level is set
+        // up first and all its corner loads go out together.
+        constexpr int KU = KP > 0 ? KP : 1;
+        for (int k0 = 0; k0 < K; k0 += KU) {
+            float cw[KU][4];
+            int off[KU][4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int yy = y0 + (c >> 1), xx = x0 + (c & 1);
-                if (static_cast<unsigned>(yy) >= static_cast<unsigned>(H) ||
-                    static_cast<unsigned>(xx) >= static_cast<unsigned>(W))
-                    continue;
-                float v[CH];
-                msda_load<T, CH>(value + ((level0 + static_cast<size_t>(yy) * W + xx) * p.G + g) * p.D + d0, v);
+            for (int u = 0; u < KU; ++u) {
+                const int i = l * K + k0 + u;
+                const float lw = __ldg(wrow + i);
+                const float a = p.softmax ? expf(lw - wmax) * inv : lw;
+                const float2 loc = __ldg(reinterpret_cast<const float2 *>(lrow) + i);
+                // pixel coordinates, rounded as two separate fp32 operations
+                float px = __fsub_rn(__fmul_rn(loc.x, static_cast<float>(W)), 0.5f);
+                float py = __fsub_rn(__fmul_rn(loc.y, static_cast<float>(H)), 0.5f);
+                // beyond [-2, size+1] every corner is outside: clamping keeps
+                // the conversion in range (NaN -> -2) and changes no result
+                px = fminf(fmaxf(px, -2.0f), static_cast<float>(W + 1));
+                py = fminf(fmaxf(py, -2.0f), static_cast<float>(H + 1));
+                const float fx = floorf(px), fy = floorf(py);
+                const float lx = px - fx, ly = py - fy;
+                const int x0 = static_cast<int>(fx), y0 = static_cast<int>(fy);
+                const float wq[4] = {(1.0f - ly) * (1.0f - lx) * a, (1.0f - ly) * lx * a,
+                                     ly * (1.0f - lx) * a, ly * lx * a};
 #pragma unroll
-                for (int e = 0; e < CH; ++e) acc[e] = fmaf(cw[c], v[e], acc[e]);
+                for (int c = 0; c < 4; ++c) {
+                    const int yy = y0 + (c >> 1), xx = x0 + (c & 1);
+                    const bool in = static_cast<unsigned>(yy) < static_cast<unsigned>(H) &&
+                                    static_cast<unsigned>(xx) < static_cast<unsigned>(W);
+                    // an outside corner reads the level's first row with weight 0
+                    cw[u][c] = in ? wq[c] : 0.0f;
+                    off[u][c] = in ? yy * W + xx : 0;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < KU; ++u) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[CH];
+                    msda_load<T, CH>(value + ((level0 + off[u][c]) * p.G + g) * p.D + d0, v);
+#pragma unroll
+                    for (int e = 0; e < CH; ++e) acc[e] = fmaf(cw[u][c], v[e], acc[e]);
+                }
             }
         }
     }
@@ -147,12 +166,125 @@ msda_forward_kernel(MsdaParams p) {
     for (int e = 0; e < CH; ++e) out[e] = msda_from_f32<T>(acc[e]);
 }
 
+// The same for a row group of GRP lanes (GRP = D / CH, a power of two that
+// divides the warp) and KP <= GRP points per level: the lanes of a
+// (b, q, g) share the per-point work instead of repeating it.  Lane r of
+// the group takes logits r, r + GRP, ... for the softmax (group reductions
+// by shuffles) and computes point r's corner weights and offsets, which the
+// other lanes read by shuffles.  Every lane of the warp takes part in the
+// shuffles; lanes past the last row compute on a clamped row and store
+// nothing.
+template <typename T, int CH, int KP, int GRP>
+__global__ void __launch_bounds__(256)
+msda_forward_group_kernel(MsdaParams p) {
+    static_assert(KP <= GRP && (GRP & (GRP - 1)) == 0 && GRP <= 32, "row group");
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long rows = static_cast<long long>(p.B) * p.Q * p.G;
+    const bool live = t < rows * GRP;
+    const long long row = live ? t / GRP : rows - 1;     // (b, q, g)
+    const int r = static_cast<int>(t % GRP);             // lane within the row group
+    const int lane = threadIdx.x % 32;
+    const int base = lane - r;                           // the group's first lane
+    const int d0 = r * CH;
+    const int g = static_cast<int>(row % p.G);
+    const int b = static_cast<int>(row / (static_cast<long long>(p.Q) * p.G));
+    const int LK = p.L * KP;
+    const float *__restrict__ wrow = p.weights + row * LK;
+    const float *__restrict__ lrow = p.locations + row * LK * 2;
+    const T *__restrict__ value = static_cast<const T *>(p.value);
+    const int GD = p.G * p.D;
+
+    float wmax = -INFINITY, wsum = 1.0f;
+    if (p.softmax) {
+        for (int i = r; i < LK; i += GRP) wmax = fmaxf(wmax, __ldg(wrow + i));
+#pragma unroll
+        for (int m = GRP / 2; m >= 1; m >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, m));
+        wsum = 0.0f;
+        for (int i = r; i < LK; i += GRP) wsum += expf(__ldg(wrow + i) - wmax);
+#pragma unroll
+        for (int m = GRP / 2; m >= 1; m >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, m);
+    }
+    const float inv = 1.0f / wsum;
+
+    float acc[CH];
+#pragma unroll
+    for (int e = 0; e < CH; ++e) acc[e] = 0.0f;
+    for (int l = 0; l < p.L; ++l) {
+        const int H = p.H[l], W = p.W[l];
+        const T *vbase = value + (static_cast<size_t>(b) * p.S + p.start[l]) * GD + g * p.D + d0;
+        // this lane's point (lanes r >= KP repeat point r % KP)
+        float wq[4];
+        int oq[4];
+        {
+            const int i = l * KP + (r % KP);
+            const float lw = __ldg(wrow + i);
+            const float a = p.softmax ? expf(lw - wmax) * inv : lw;
+            const float2 loc = __ldg(reinterpret_cast<const float2 *>(lrow) + i);
+            float px = __fsub_rn(__fmul_rn(loc.x, static_cast<float>(W)), 0.5f);
+            float py = __fsub_rn(__fmul_rn(loc.y, static_cast<float>(H)), 0.5f);
+            px = fminf(fmaxf(px, -2.0f), static_cast<float>(W + 1));
+            py = fminf(fmaxf(py, -2.0f), static_cast<float>(H + 1));
+            const float fx = floorf(px), fy = floorf(py);
+            const float lx = px - fx, ly = py - fy;
+            const int x0 = static_cast<int>(fx), y0 = static_cast<int>(fy);
+            const float w4[4] = {(1.0f - ly) * (1.0f - lx) * a, (1.0f - ly) * lx * a,
+                                 ly * (1.0f - lx) * a, ly * lx * a};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int yy = y0 + (c >> 1), xx = x0 + (c & 1);
+                const bool in = static_cast<unsigned>(yy) < static_cast<unsigned>(H) &&
+                                static_cast<unsigned>(xx) < static_cast<unsigned>(W);
+                // an outside corner reads the level's first row with weight 0
+                wq[c] = in ? w4[c] : 0.0f;
+                oq[c] = in ? (yy * W + xx) * GD : 0;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < KP; ++u) {
+            float cw[4];
+            int off[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                cw[c] = __shfl_sync(0xffffffffu, wq[c], base + u);
+                off[c] = __shfl_sync(0xffffffffu, oq[c], base + u);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[CH];
+                msda_load<T, CH>(vbase + off[c], v);
+#pragma unroll
+                for (int e = 0; e < CH; ++e) acc[e] = fmaf(cw[c], v[e], acc[e]);
+            }
+        }
+    }
+    if (live) {
+        T *__restrict__ out = static_cast<T *>(p.out) + row * p.D + d0;
+#pragma unroll
+        for (int e = 0; e < CH; ++e) out[e] = msda_from_f32<T>(acc[e]);
+    }
+}
+
 template <typename T, int CH>
 cudaError_t launch_msda_t(const MsdaParams &p, cudaStream_t stream) {
     const long long threads = static_cast<long long>(p.B) * p.Q * p.G * (p.D / CH);
     const long long blocks = (threads + 255) / 256;
     if (blocks > 2147483647ll) return cudaErrorInvalidValue;
-    msda_forward_kernel<T, CH><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    const unsigned nb = static_cast<unsigned>(blocks);
+    // the page's CUDA backend takes 4 or 8 points per level: those unrolled,
+    // and shared across the lanes of a (b, q, g) where its lanes are 4 or 8
+    const int per_row = p.D / CH;
+    if (CH > 1 && per_row == 4 && p.K == 4)
+        msda_forward_group_kernel<T, CH, 4, 4><<<nb, 256, 0, stream>>>(p);
+    else if (CH > 1 && per_row == 8 && p.K == 4)
+        msda_forward_group_kernel<T, CH, 4, 8><<<nb, 256, 0, stream>>>(p);
+    else if (CH > 1 && per_row == 8 && p.K == 8)
+        msda_forward_group_kernel<T, CH, 8, 8><<<nb, 256, 0, stream>>>(p);
+    else if (p.K == 4)
+        msda_forward_kernel<T, CH, 4><<<nb, 256, 0, stream>>>(p);
+    else if (p.K == 8)
+        msda_forward_kernel<T, CH, 8><<<nb, 256, 0, stream>>>(p);
+    else
+        msda_forward_kernel<T, CH, 0><<<nb, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -44,6 +44,10 @@ CASES = [
     # D not a multiple of 8 / 4: one channel per thread
     MsdaWorkload("msda_d_odd", 2, 3, 6, ((7, 5), (3, 3)), 21, 2, "bf16", True, -0.1, 1.1, 73),
     MsdaWorkload("msda_d_odd_f32", 1, 2, 5, ((6, 6),), 11, 3, "f32", False, -0.1, 1.1, 74),
+    # eight lanes per (query, head) sharing eight points; a last warp that the
+    # rows fill only in part (15 rows x 4 lanes)
+    MsdaWorkload("msda_d64_k8", 1, 4, 64, ((12, 10), (6, 5)), 23, 8, "bf16", True, -0.1, 1.1, 76),
+    MsdaWorkload("msda_partial_warp", 1, 3, 32, ((8, 8), (4, 4)), 5, 4, "bf16", True, -0.1, 1.1, 77),
     # five levels, eight points, many samples outside
     MsdaWorkload("msda_5lvl", 1, 4, 32, ((20, 24), (10, 12), (5, 6), (3, 3), (1, 2)), 64, 8, "bf16",
                  True, -0.5, 1.5, 75),
