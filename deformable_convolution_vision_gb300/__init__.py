@@ -13,7 +13,7 @@ from . import binding
 from .binding import (DCN_BF16, DCN_F16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
                       DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, ConvDesc, DcnError, dcn_create,
                       dcn_backward, dcn_backward_ex, dcn_destroy, dcn_forward, dcn_forward_ex,
-                      dcn_msda_forward,
+                      dcn_msda_forward, dcn_nchw_to_nhwc, dcn_nhwc_to_nchw,
                       dcn_forward_host,
                       dcn_forward_packed, dcn_forward_packed_ex, dcn_last_path, dcn_out_size,
                       dcn_pack_weight, dcn_pack_weight_ex, dcn_selftest_timeout, dcn_set_path,
@@ -26,7 +26,8 @@ __all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF1
            "dcn_set_path", "dcn_last_path", "dcn_sync_status", "dcn_selftest_timeout",
            "dcn_status_string", "ConvDesc", "dcn_forward_ex", "dcn_pack_weight_ex",
            "dcn_forward_packed_ex", "dcn_out_size", "dcn_backward", "dcn_backward_ex",
-           "deform_conv2d_backward", "dcn_msda_forward", "msda"]
+           "deform_conv2d_backward", "dcn_msda_forward", "msda", "dcn_nchw_to_nhwc",
+           "dcn_nhwc_to_nchw", "deform_conv2d_nchw"]
 
 
 class Handle:
@@ -210,4 +211,26 @@ def msda(value, shapes, starts, locations, weights, method=None, out=None, strea
         out = torch.empty((B, Q, G, D), dtype=value.dtype, device=value.device)
     dcn_msda_forward(value, shapes, starts, locations, weights, out, B, S, G, D, Q, K,
                      method == "softmax", _dtype_code(value), stream)
+    return out
+
+
+def deform_conv2d_nchw(input, offset, weight, bias=None, stride=1, padding=0, dilation=1,
+                       mask=None, handle=None, stream=None):
+    """torchvision's argument order and layouts: input [B, C, H, W] and the
+    result in plain (contiguous) NCHW.  The library's layout kernels copy
+    input to channels-last and the result back; offset, mask and bias stay
+    float32 and contiguous as for ``deform_conv2d``."""
+    import torch
+    if not input.is_cuda or not input.is_contiguous():
+        raise ValueError("input must be a contiguous (NCHW) CUDA tensor")
+    B, C, H, W = input.shape
+    code = _dtype_code(input)
+    x = torch.empty((B, C, H, W), dtype=input.dtype, device=input.device,
+                    memory_format=torch.channels_last)
+    dcn_nchw_to_nhwc(input, x, B, C, H, W, code, stream)
+    out_cl = deform_conv2d(x, offset, weight, bias, stride=stride, padding=padding,
+                           dilation=dilation, mask=mask, handle=handle, stream=stream)
+    Bo, O, Ho, Wo = out_cl.shape
+    out = torch.empty((Bo, O, Ho, Wo), dtype=out_cl.dtype, device=out_cl.device)
+    dcn_nhwc_to_nchw(out_cl, out, Bo, O, Ho, Wo, code, stream)
     return out

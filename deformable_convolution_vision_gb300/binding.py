@@ -23,7 +23,8 @@ EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_f
            "dcn_forward_host", "dcn_set_path", "dcn_last_path", "dcn_sync_status",
            "dcn_selftest_timeout", "dcn_status_string", "dcn_forward_noalloc",
            "dcn_set_sample_precision", "dcn_out_size", "dcn_forward_ex", "dcn_pack_weight_ex",
-           "dcn_forward_packed_ex", "dcn_backward", "dcn_backward_ex", "dcn_msda_forward"]
+           "dcn_forward_packed_ex", "dcn_backward", "dcn_backward_ex", "dcn_msda_forward",
+           "dcn_nchw_to_nhwc", "dcn_nhwc_to_nchw"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -74,6 +75,8 @@ def load():
         "dcn_backward": ([P] * 11 + [I] * 9 + [P], I),
         "dcn_backward_ex": ([P] * 11 + [ctypes.POINTER(ConvDesc), I, P], I),
         "dcn_msda_forward": ([P, P, P, I, P, P, P] + [I] * 8 + [P], I),
+        "dcn_nchw_to_nhwc": ([P, P] + [I] * 5 + [P], I),
+        "dcn_nhwc_to_nchw": ([P, P] + [I] * 5 + [P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -225,3 +228,13 @@ def dcn_msda_forward(value, shapes, starts, locations, weights, out, B, S, G, D,
     _check(load().dcn_msda_forward(_ptr(value), sh, st, L, _ptr(locations), _ptr(weights), _ptr(out),
                                    B, S, G, D, Q, K, int(bool(softmax)), dtype, _stream(stream)),
            "dcn_msda_forward")
+
+
+def dcn_nchw_to_nhwc(src, dst, B, C, H, W, dtype, stream=None):
+    _check(load().dcn_nchw_to_nhwc(_ptr(src), _ptr(dst), B, C, H, W, dtype, _stream(stream)),
+           "dcn_nchw_to_nhwc")
+
+
+def dcn_nhwc_to_nchw(src, dst, B, C, H, W, dtype, stream=None):
+    _check(load().dcn_nhwc_to_nchw(_ptr(src), _ptr(dst), B, C, H, W, dtype, _stream(stream)),
+           "dcn_nhwc_to_nchw")

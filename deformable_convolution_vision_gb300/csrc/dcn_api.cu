@@ -610,6 +610,31 @@ dcn_status_t dcn_msda_forward(const void *value, const int *shapes, const int *s
     return DCN_OK;
 }
 
+static dcn_status_t layout_copy(const void *src, void *dst, int B, int R, int S, int dtype,
+                                void *stream) {
+    if (!src || !dst || src == dst) return DCN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || B <= 0 || R <= 0 || S <= 0) return DCN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * R * S > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    const size_t es = esize(dtype);
+    if (!aligned(src, es) || !aligned(dst, es)) return DCN_ERR_INVALID_ARG;
+    if (B > 65535 || (R + 31) / 32 > 65535) return DCN_ERR_UNSUPPORTED;
+    if (dcn::launch_transpose(src, dst, B, R, S, static_cast<int>(es), as_stream(stream)) != cudaSuccess)
+        return DCN_ERR_CUDA;
+    return DCN_OK;
+}
+
+dcn_status_t dcn_nchw_to_nhwc(const void *src, void *dst, int B, int C, int H, int W, int dtype,
+                              void *stream) {
+    if (H <= 0 || W <= 0 || static_cast<long long>(H) * W > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    return layout_copy(src, dst, B, C, H * W, dtype, stream);
+}
+
+dcn_status_t dcn_nhwc_to_nchw(const void *src, void *dst, int B, int C, int H, int W, int dtype,
+                              void *stream) {
+    if (H <= 0 || W <= 0 || static_cast<long long>(H) * W > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    return layout_copy(src, dst, B, H * W, C, dtype, stream);
+}
+
 int dcn_out_size(int n, int k, int stride, int pad, int dil) {
     if (n <= 0 || k <= 0 || stride <= 0 || pad < 0 || dil <= 0) return 0;
     const long long r = out_size_ll(n, k, stride, pad, dil);

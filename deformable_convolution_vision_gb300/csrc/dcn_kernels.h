@@ -164,6 +164,10 @@ struct MsdaParams {
 // vec: D a multiple of 8 (16-bit) or 4 (fp32) and value/out 16-byte aligned.
 cudaError_t launch_msda(const MsdaParams &p, int dtype, bool vec, cudaStream_t stream);
 
+// Batched 2-D transpose [B][R][S] -> [B][S][R] of 2- or 4-byte elements.
+cudaError_t launch_transpose(const void *src, void *dst, int B, int R, int S, int esize,
+                             cudaStream_t stream);
+
 // One-thread kernel whose barrier wait runs out after timeout_ns.
 cudaError_t launch_selftest_timeout(unsigned *status, unsigned long long timeout_ns,
                                     cudaStream_t stream);

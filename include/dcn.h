@@ -327,6 +327,21 @@ DCN_API dcn_status_t dcn_backward_ex(dcn_handle_t h,
                              float *grad_weight, float *grad_bias,
                              const dcn_conv_desc_t *desc, int dtype, void *stream);
 
+/* ------------------------------------------------------------ layouts
+ *
+ * For callers with NCHW tensors (the torchvision layout that page
+ * "deformops 3.0.1", section "torchvision drop-in", keeps for its drop-in
+ * function): device-side layout copies between [B, C, H, W] and
+ * [B, H, W, C] (the layout of x and out above), in `dtype`'s element size.
+ * src and dst must not overlap.  Asynchronous on `stream`; allocates
+ * nothing.  DCN_ERR_INVALID_ARG for NULL or equal pointers, non-positive or
+ * oversized dimensions (B*C*H*W < 2^31), misalignment;
+ * DCN_ERR_UNSUPPORTED for B > 65535. */
+DCN_API dcn_status_t dcn_nchw_to_nhwc(const void *src, void *dst, int B, int C, int H, int W,
+                              int dtype, void *stream);
+DCN_API dcn_status_t dcn_nhwc_to_nchw(const void *src, void *dst, int B, int C, int H, int W,
+                              int dtype, void *stream);
+
 /* ------------------------------------------------ multi-scale deformable attention
  *
  * The forward pass of the operator of page "deformops 3.0.1", section
