@@ -55,7 +55,7 @@ def build(verbose=False, extra=()):
             sys.stderr.write(log)
     objs = [o for o, _ in results]
     tmp = LIBRARY + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -263,6 +263,12 @@ dcn_bwd_data_kernel(BwdParams p) {
 
 // Eight consecutive elements as fp32: one 16-byte load for 16-bit types
 // (two for fp32) when `vec`, else element by element with a bound.
+template <typename T> __device__ __forceinline__ T from_f32_t(float v);
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32_t<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+template <> __device__ __forceinline__ __half from_f32_t<__half>(float v) { return __float2half_rn(v); }
+
 template <typename T>
 __device__ __forceinline__ void load8(const T *src, int n_valid, bool vec, float (&v)[8]);
 template <>
@@ -484,6 +490,60 @@ cudaError_t launch_backward_weight_t(const BwdParams &p_in, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+// The sampled operand of the weight gradient, for pixels [pix0, pix0 +
+// npix): cols[pl][g][tap][cl] = m * S(pixel pix0 + pl, tap, channel
+// g * Cg + cl), rounded to the operand type T (the rounding the forward's
+// tensor-core contraction applies to the same operand).  One thread per 8
+// channels of a (pixel, tap): 16-byte corner loads and one 16-byte store.
+// Requires C, C/groups and C/offset_groups multiples of 8 and x 16-byte
+// aligned.
+template <typename T>
+__global__ void __launch_bounds__(256)
+dcn_bwd_columns_kernel(BwdParams p, T *__restrict__ cols, int pix0, int npix) {
+    const T *__restrict__ x = static_cast<const T *>(p.x);
+    const int C8 = p.C / 8;
+    const int taps = p.kh * p.kw;
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= static_cast<long long>(npix) * taps * C8) return;
+    const int c = static_cast<int>(t % C8) * 8;
+    const long long rest = t / C8;
+    const int tap = static_cast<int>(rest % taps);
+    const int pl = static_cast<int>(rest / taps);
+    const int pix = pix0 + pl;
+    const int Cg = p.C / p.groups, Cq = p.C / p.ogroups;
+    const int g = c / Cg, cl = c - g * Cg, q = c / Cq;
+    const int HoWo = p.Ho * p.Wo;
+    const int b = pix / HoWo;
+    const int hw = pix - b * HoWo;
+    const int h = hw / p.Wo, w = hw - (hw / p.Wo) * p.Wo;
+    const int i = tap / p.kw, j = tap - (tap / p.kw) * p.kw;
+    const Geo gg = geometry(p, b, h, w, i, j, q, tap);
+    const float wq[4] = {(1.0f - gg.ly) * (1.0f - gg.lx), (1.0f - gg.ly) * gg.lx,
+                         gg.ly * (1.0f - gg.lx), gg.ly * gg.lx};
+    float sv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sv[e] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (gg.idx[k] < 0) continue;
+        float v[8];
+        load8(x + gg.idx[k] + c, 8, true, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sv[e] = fmaf(wq[k], v[e], sv[e]);
+    }
+    uint32_t pk[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        T lo = from_f32_t<T>(gg.m * sv[2 * e]), hi = from_f32_t<T>(gg.m * sv[2 * e + 1]);
+        uint16_t l16, h16;
+        memcpy(&l16, &lo, 2);
+        memcpy(&h16, &hi, 2);
+        pk[e] = static_cast<uint32_t>(l16) | (static_cast<uint32_t>(h16) << 16);
+    }
+    *reinterpret_cast<uint4 *>(cols + ((static_cast<size_t>(pl) * p.groups + g) * taps + tap) * Cg + cl) =
+        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+}
+
 template <typename T>
 cudaError_t launch_backward_t(const BwdParams &p, cudaStream_t stream) {
     const dim3 grid((p.P + BWD_BM - 1) / BWD_BM, (p.C + BWD_BN - 1) / BWD_BN);
@@ -499,6 +559,35 @@ cudaError_t launch_backward(const BwdParams &p, int dtype, cudaStream_t stream) 
     if (dtype == kF32) return launch_backward_t<float>(p, stream);
     if (dtype == kF16) return launch_backward_t<__half>(p, stream);
     return launch_backward_t<__nv_bfloat16>(p, stream);
+}
+
+cudaError_t launch_bwd_columns(const BwdParams &p, int dtype, void *cols, int pix0, int npix,
+                               cudaStream_t stream) {
+    const long long threads = static_cast<long long>(npix) * p.kh * p.kw * (p.C / 8);
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 2147483647ll || p.C % 8) return cudaErrorInvalidValue;
+    if (dtype == kF16)
+        dcn_bwd_columns_kernel<__half><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            p, static_cast<__half *>(cols), pix0, npix);
+    else if (dtype == kBF16)
+        dcn_bwd_columns_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            p, static_cast<__nv_bfloat16 *>(cols), pix0, npix);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_bias(const BwdParams &p_in, int dtype, cudaStream_t stream) {
+    BwdParams p = p_in;
+    p.pix_run = 1024;
+    const dim3 grid((p.P + 1023) / 1024, (p.O + 255) / 256);
+    if (dtype == kF32)
+        dcn_bwd_bias_kernel<float><<<grid, 256, 0, stream>>>(p);
+    else if (dtype == kF16)
+        dcn_bwd_bias_kernel<__half><<<grid, 256, 0, stream>>>(p);
+    else
+        dcn_bwd_bias_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_backward_weight(const BwdParams &p, int dtype, cudaStream_t stream) {

@@ -4,8 +4,10 @@ Every gradient (x, offset, mask, weight, bias) is compared element by
 element with the oracle on the same seeded inputs and the same cotangent.
 The kernels compute in fp32 from the operands' exact values for every
 operand dtype (the oracle reads the same values and computes in fp64), so
-the bar is the fp32 one for all of them: max|gpu - ref| / max|ref| <= 1e-4
-per gradient.  Shapes cover ragged pixel counts, several output and
+the bar is the fp32 one, max|gpu - ref| / max|ref| <= 1e-4 per gradient --
+except the weight gradient of 16-bit operands on the tensor-core path, whose
+sampled operand is rounded to the operand type before its GEMM (the
+forward's rounding), which takes that dtype's bar.  Shapes cover ragged pixel counts, several output and
 channel chunks, C not a multiple of 4 (scalar reductions), offset groups
 narrower than four channels, stride, dilation and groups.
 """
@@ -17,7 +19,7 @@ import torch
 import oracle
 import deformable_convolution_vision_gb300 as dcn
 from deformable_convolution_vision_gb300.inputs import GeneralWorkload as GW, make_general_inputs
-from tests.helpers import to_device
+from tests.helpers import TOL, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +37,16 @@ def _cotangent(wl, dtype, seed):
     Ho, Wo = wl.out_size()
     g = torch.Generator().manual_seed(seed)
     return torch.randn(wl.B, wl.O, Ho, Wo, generator=g).to(dtype)
+
+
+def _bar(wl, key, path):
+    """The fp32 bar, except for the weight gradient of 16-bit operands on the
+    tensor-core path: its sampled operand is rounded to the operand type
+    before the contraction (as the forward's is), so it takes that type's
+    bar from TOL."""
+    if key == "grad_weight" and wl.dtype != "f32" and path != dcn.DCN_PATH_SIMT:
+        return TOL[wl.dtype]
+    return BAR
 
 
 def run_backward(wl, inp, gout, path=dcn.DCN_PATH_AUTO):
@@ -65,7 +77,8 @@ def check(wl, path=dcn.DCN_PATH_AUTO):
         g = got[k].cpu().numpy()
         assert np.isfinite(g).all(), k
         errs[k] = _rel(g, ref[k])
-        assert errs[k] <= BAR, f"{wl.name} {k}: rel err {errs[k]:.3e}"
+        bar = _bar(wl, k, path)
+        assert errs[k] <= bar, f"{wl.name} {k}: rel err {errs[k]:.3e} > {bar}"
     return errs
 
 
