@@ -51,3 +51,25 @@ def test_calls_on_one_handle_see_their_own_weight(wl):
         assert torch.equal(out, ref)
         cpu = dict(inp, weight=w.cpu())
         assert compare_full(out, oracle_full(cpu, wl.pad)) <= TOL[wl.dtype]
+
+
+@pytest.mark.parametrize("name", ["aspp7x7", "boundary5x5"])
+def test_full_size_in_the_bench_configuration(name):
+    """The benchmark's launch configuration: one handle, repeated
+    dcn_forward calls (so every call after the first overlaps its weight
+    pack), the persistent stream-K launch.  The third call's output is
+    compared with the oracle on sampled pixels."""
+    import oracle
+    from tests.helpers import compare_points, sample_points
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    d = to_device(inp)
+    with Handle() as h:
+        outs = [_call(h, d, wl, d["weight"]) for _ in range(3)]
+        assert dcn.dcn_sync_status(h.h) == 0
+        assert dcn.dcn_last_path(h.h) == DCN_PATH_TC
+    assert torch.equal(outs[0], outs[2])
+    pts = sample_points(wl.B, wl.Ho, wl.Wo, 256, seed=wl.seed + 9)
+    ref = oracle.forward_points(inp["x"], inp["offset"], inp["mask"], inp["weight"], inp["bias"],
+                                wl.pad, pts)
+    assert compare_points(outs[2], ref, pts) <= TOL[wl.dtype]
