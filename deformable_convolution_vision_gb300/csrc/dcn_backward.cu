@@ -494,7 +494,8 @@ cudaError_t launch_backward_weight_t(const BwdParams &p_in, cudaStream_t stream)
 // npix): cols[pl][g][tap][cl] = m * S(pixel pix0 + pl, tap, channel
 // g * Cg + cl), rounded to the operand type T (the rounding the forward's
 // tensor-core contraction applies to the same operand).  One thread per 8
-// channels of a (pixel, tap): 16-byte corner loads and one 16-byte store.
+// channels of a (pixel, tap), taps outermost: 16-byte corner loads and one
+// 16-byte store.
 // Requires C, C/groups and C/offset_groups multiples of 8 and x 16-byte
 // aligned.
 template <typename T>
@@ -505,10 +506,12 @@ dcn_bwd_columns_kernel(BwdParams p, T *__restrict__ cols, int pix0, int npix) {
     const int taps = p.kh * p.kw;
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (t >= static_cast<long long>(npix) * taps * C8) return;
+    // tap-major over the chunk's pixels: the threads of a block take one tap
+    // of neighbouring pixels, whose corner rows overlap (L1 hits)
     const int c = static_cast<int>(t % C8) * 8;
     const long long rest = t / C8;
-    const int tap = static_cast<int>(rest % taps);
-    const int pl = static_cast<int>(rest / taps);
+    const int pl = static_cast<int>(rest % npix);
+    const int tap = static_cast<int>(rest / npix);
     const int pix = pix0 + pl;
     const int Cg = p.C / p.groups, Cq = p.C / p.ogroups;
     const int g = c / Cg, cl = c - g * Cg, q = c / Cq;
