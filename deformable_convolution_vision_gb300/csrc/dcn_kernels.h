@@ -26,7 +26,11 @@ struct Params {
     int sh, sw, ph, pw, dh, dw;  // stride, padding, dilation (h, w)
     int groups;           // weight groups (CUDA-core kernel; 1 in a tensor-core launch)
     int ogroups;          // offset groups (CUDA-core kernel)
-    int Ho, Wo;
+    int Ho, Wo;           // output rows and columns of this launch
+    int h0;               // absolute output row of the launch's first row (its
+                          // sampling coordinates use h0 + row); 0 for a whole image
+    int plane;            // elements between consecutive offset/mask planes:
+                          // Ho * Wo, or the whole image's for a band of rows
     int P;                // B * Ho * Wo output pixels
     int K;                // kh * kw * (C / groups): packed weight row length
     int x_cstride;        // elements between neighbouring pixels of x

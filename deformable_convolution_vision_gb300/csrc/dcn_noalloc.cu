@@ -125,6 +125,8 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.groups = p.ogroups = 1;
     p.Ho = static_cast<int>(Ho);
     p.Wo = static_cast<int>(Wo);
+    p.h0 = 0;
+    p.plane = p.Ho * p.Wo;
     p.P = B * p.Ho * p.Wo;
     p.K = kh * kw * C;
     p.x_cstride = C;

@@ -116,11 +116,12 @@ dcn_simt_kernel(Params p) {
                 if (my_pix < p.P) {
                     const size_t hw = static_cast<size_t>(my_h) * p.Wo + my_w;
                     const size_t bq = static_cast<size_t>(my_b) * p.ogroups + q;
-                    const size_t ob = bq * 2 * taps * HoWo + hw;
-                    const float dy = p.offset[ob + static_cast<size_t>(2 * tap) * HoWo];
-                    const float dx = p.offset[ob + static_cast<size_t>(2 * tap + 1) * HoWo];
-                    const float m = p.mask ? p.mask[(bq * taps + tap) * HoWo + hw] : 1.0f;
-                    tap_corners(dy, dx, m, my_h * p.sh - p.ph + i * p.dh, my_w * p.sw - p.pw + j * p.dw,
+                    const size_t plane = static_cast<size_t>(p.plane);
+                    const size_t ob = bq * 2 * taps * plane + hw;
+                    const float dy = p.offset[ob + static_cast<size_t>(2 * tap) * plane];
+                    const float dx = p.offset[ob + static_cast<size_t>(2 * tap + 1) * plane];
+                    const float m = p.mask ? p.mask[(bq * taps + tap) * plane + hw] : 1.0f;
+                    tap_corners(dy, dx, m, (p.h0 + my_h) * p.sh - p.ph + i * p.dh, my_w * p.sw - p.pw + j * p.dw,
                                 my_b, p.H, p.W, p.x_cstride, t);
                 } else {
 #pragma unroll

@@ -313,7 +313,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         const uint32_t table_s = smem_u32(table);
         const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * 3 * 32 * 4) + lane * 4;
         const uint32_t a_lane = static_cast<uint32_t>(16 * trow) << 16;
-        const int HoWo = p.Ho * p.Wo;
+        const int plane = p.plane;                       // offset / mask plane stride
         const int my_g = lane >> 4;     // geometry: tap of the group
         const int my_px = lane & 15;    // geometry: pixel (tile column)
         const int quart = lane & 3;     // gather: 16 channels of the 64-channel K-block
@@ -454,13 +454,13 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     const bool valid = my_valid && vt < vtaps;
                     const int mc = valid ? vt_tab[vt].z : 0;   // mask plane; offsets 2*mc, 2*mc + 1
                     const float *o = valid
-                        ? p.offset + (static_cast<size_t>(tb) * p.off_bstride + 2 * mc) * HoWo + my_hw
+                        ? p.offset + (static_cast<size_t>(tb) * p.off_bstride + 2 * mc) * plane + my_hw
                         : p.offset;
                     cp_async_4(raw_s, o, valid);
-                    cp_async_4(raw_s + 128, valid ? o + HoWo : o, valid);
+                    cp_async_4(raw_s + 128, valid ? o + plane : o, valid);
                     if (p.mask) {
                         const float *mp = valid
-                            ? p.mask + (static_cast<size_t>(tb) * p.mask_bstride + mc) * HoWo + my_hw
+                            ? p.mask + (static_cast<size_t>(tb) * p.mask_bstride + mc) * plane + my_hw
                             : p.mask;
                         cp_async_4(raw_s + 256, mp, valid);
                     }
@@ -476,7 +476,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                         const float dy = lds_f32(raw_s);
                         const float dx = lds_f32(raw_s + 128);
                         const float m = p.mask ? lds_f32(raw_s + 256) : 1.0f;
-                        tap_corners(dy, dx, m, my_h * p.sh + e.x, my_w * p.sw + e.y, tb, p.H, p.W,
+                        tap_corners(dy, dx, m, (p.h0 + my_h) * p.sh + e.x, my_w * p.sw + e.y, tb, p.H, p.W,
                                     p.x_cstride, t);
                     } else {
 #pragma unroll

@@ -131,7 +131,10 @@ DCN_API dcn_status_t dcn_forward_packed(dcn_handle_t h,
 
 /* dcn_forward with HOST buffers (same layouts): copies every input to
  * device staging buffers owned by the handle, runs the forward pass,
- * copies out back and synchronises `stream`.  Pinned host memory gives
+ * copies out back and synchronises `stream`.  It runs as a pipeline over
+ * bands of output rows: uploads on `stream`, each band's kernel on a
+ * handle-owned stream, downloads on another, so later uploads overlap
+ * earlier bands' work; the call returns when all of it is done.  Pinned host memory gives
  * asynchronous copies; pageable memory works but is slower.  Returns the
  * device status as dcn_sync_status would. */
 DCN_API dcn_status_t dcn_forward_host(dcn_handle_t h,

@@ -125,3 +125,48 @@ def test_bounded_wait_reports_timeout_and_context_survives(handle):
                             mask=d["mask"], handle=handle)
     assert dcn.dcn_sync_status(handle.h) == 0
     assert compare_full(out, oracle_full(inp, wl.pad)) <= TOL["f32"]
+
+
+def _host_call(handle, wl, inp, code):
+    x = inp["x"].permute(0, 2, 3, 1).contiguous().pin_memory()
+    off = inp["offset"].pin_memory()
+    m = None if inp["mask"] is None else inp["mask"].pin_memory()
+    w = inp["weight"].contiguous().pin_memory()
+    bias = None if inp["bias"] is None else inp["bias"].pin_memory()
+    out = torch.empty((wl.B, wl.Ho, wl.Wo, wl.O), dtype=x.dtype).pin_memory()
+    dcn.dcn_forward_host(handle.h, x, off, m, w, bias, out, wl.B, wl.C, wl.H, wl.W, wl.O,
+                         wl.kh, wl.kw, wl.pad, code)
+    return out.permute(0, 3, 1, 2)
+
+
+@pytest.mark.parametrize("wl", [
+    # four bands of 64 rows (the benchmark's end-to-end call)
+    WORKLOADS["aspp7x7"],
+    # two images, two bands each, the last one ragged (Ho = 43)
+    WORKLOADS["decoder3x3"].with_(B=2, H=43, W=50, seed=81),
+    # five images: one band per image; no mask, no bias
+    WORKLOADS["decoder3x3"].with_(B=5, H=20, W=24, mask="none", bias_std=0.0, seed=82),
+    # fp16, and fp32 on the CUDA-core kernel, banded
+    WORKLOADS["decoder3x3"].with_(H=70, W=33, dtype="f16", seed=83),
+    WORKLOADS["decoder3x3"].with_(C=16, O=24, H=66, W=30, dtype="f32", seed=84),
+], ids=["aspp7x7", "b2_ragged", "b5_nomask", "f16", "f32"])
+def test_host_entry_point_bands(handle, wl):
+    """The host-buffer entry runs as a pipeline over bands of output rows
+    (uploads, kernels and downloads on separate streams); every band's
+    result must match the oracle."""
+    import oracle
+    from tests.helpers import compare_points, sample_points
+    inp = make_inputs(wl)
+    code = {"f32": dcn.DCN_F32, "bf16": dcn.DCN_BF16, "f16": dcn.DCN_F16}[wl.dtype]
+    out = _host_call(handle, wl, inp, code)
+    assert dcn.dcn_sync_status(handle.h) == 0
+    if wl.pixels * wl.O * wl.taps * wl.C <= 1e9:
+        assert compare_full(out, oracle_full(inp, wl.pad)) <= TOL[wl.dtype]
+    else:
+        pts = sample_points(wl.B, wl.Ho, wl.Wo, 256, seed=wl.seed)
+        ref = oracle.forward_points(inp["x"], inp["offset"], inp["mask"], inp["weight"],
+                                    inp["bias"], wl.pad, pts)
+        assert compare_points(out, ref, pts) <= TOL[wl.dtype]
+    # a second call on the same handle (streams and events reused) agrees
+    again = _host_call(handle, wl, inp, code)
+    assert torch.equal(out, again)
