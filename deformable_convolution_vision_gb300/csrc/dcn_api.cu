@@ -133,12 +133,16 @@ dcn_conv_desc_t page_desc(int B, int C, int H, int W, int O, int kh, int kw, int
 }
 
 // Whether the tensor-core kernel runs this problem (one launch per weight
-// group and per 256 output channels; offset groups as virtual taps).
+// group and per 256 output channels; offset groups as virtual taps).  A
+// group's channels go in whole 64-channel blocks, the last one completed
+// with zeros when Cg % 64 != 0; several offset groups inside one weight
+// group need whole blocks each.
 bool tc_general_ok(const Conv &c) {
     const int Cg = c.Cg(), Cq = c.Cq(), Og = c.Og();
-    if (Cg % 64 != 0 || Cq % 64 != 0 || Og % 16 != 0) return false;
+    if (Cg % 16 != 0 || Og % 16 != 0) return false;
     if (Cg % Cq != 0 && Cq % Cg != 0) return false;
     const int og_count = Cq >= Cg ? 1 : Cg / Cq;
+    if (og_count > 1 && Cq % 64 != 0) return false;
     if (static_cast<long long>(c.taps()) * og_count > dcn::tc_max_virtual_taps) return false;
     return dcn::tc_supported(Cg, Og < 256 ? Og : 256);
 }
@@ -163,10 +167,10 @@ dcn_status_t ensure(void **buf, size_t *cap, size_t bytes, cudaStream_t s) {
 dcn_status_t pack_impl(dcn_handle_t h, const void *weight, const Conv &c, int dtype,
                        cudaStream_t s) {
     const int O = c.d.O, Cg = c.Cg(), kh = c.d.kh, kw = c.d.kw;
-    const size_t bytes = static_cast<size_t>(O) * Cg * kh * kw * esize(dtype);
+    const int perm = dcn::tc_pack_permuted(dtype, Cg) ? 1 : 0;
+    const size_t bytes = static_cast<size_t>(O) * dcn::pack_kc(Cg, perm) * kh * kw * esize(dtype);
     dcn_status_t st = ensure(&h->wpack, &h->wpack_cap, bytes, s);
     if (st != DCN_OK) return st;
-    const int perm = dcn::tc_pack_permuted(dtype, Cg) ? 1 : 0;
     if (dcn::launch_pack_weight(weight, h->wpack, O, Cg, kh, kw, dtype, perm, s) != cudaSuccess)
         return DCN_ERR_CUDA;
     h->pk_O = O; h->pk_Cg = Cg; h->pk_kh = kh; h->pk_kw = kw; h->pk_dtype = dtype;
@@ -223,7 +227,8 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
         p.plane = band->plane;
         p.P = band->rows * c.Wo;
     }
-    p.K = taps * c.Cg();
+    p.kc = dcn::pack_kc(c.Cg(), h->pk_perm);
+    p.K = taps * p.kc;
     p.x_cstride = d.C;
     p.out_stride = d.O;
     p.og_count = d.offset_groups;

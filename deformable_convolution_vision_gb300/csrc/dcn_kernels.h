@@ -32,7 +32,9 @@ struct Params {
     int plane;            // elements between consecutive offset/mask planes:
                           // Ho * Wo, or the whole image's for a band of rows
     int P;                // B * Ho * Wo output pixels
-    int K;                // kh * kw * (C / groups): packed weight row length
+    int K;                // packed weight row length: kh * kw * kc
+    int kc;               // packed positions per tap: C / groups, or (tensor-core
+                          // order) C / groups rounded up to a multiple of 64
     int x_cstride;        // elements between neighbouring pixels of x
     int out_stride;       // elements between neighbouring pixels of out
     // tensor-core launch view of the offset groups: og_count groups of
@@ -65,10 +67,15 @@ __host__ __device__ constexpr int tc_channel_perm(int c) {
 
 enum Dtype { kF32 = 0, kBF16 = 1, kF16 = 2 };
 
-// S0: weight [O, Cg, kh, kw] -> packed [O][(i*kw + j)*Cg + c'], where
-// c' = c, or c' = tc_channel_perm(c) with perm != 0 (Cg % 64 == 0 only).
+// S0: weight [O, Cg, kh, kw] -> packed [O][(i*kw + j)*kc + pos].  perm == 0:
+// kc = Cg and position pos holds channel pos.  perm != 0 (the tensor-core
+// operand order, Cg % 16 == 0): kc = Cg rounded up to a multiple of 64,
+// position pos holds channel tc_channel_perm(pos), and zero where that is
+// >= Cg (the padding of a tap's last 64-channel block).
 cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int Cg, int kh, int kw,
                                int dtype, int perm, cudaStream_t stream);
+// Packed positions per tap for a pack of Cg channels.
+__host__ __device__ inline int pack_kc(int Cg, int perm) { return perm ? (Cg + 63) / 64 * 64 : Cg; }
 
 // CUDA-core fused sample + contraction + epilogue (fp32, bf16 or fp16 operands).
 cudaError_t launch_simt(const Params &p, int dtype, cudaStream_t stream);
@@ -82,8 +89,8 @@ cudaError_t launch_simt(const Params &p, int dtype, cudaStream_t stream);
 bool tc_supported(int C, int O);
 constexpr int tc_max_virtual_taps = 512;
 // Whether a weight whose groups have Cg channels is packed in
-// tc_channel_perm order (a 16-bit type and whole 64-channel blocks).
-inline bool tc_pack_permuted(int dtype, int Cg) { return (dtype == kBF16 || dtype == kF16) && Cg % 64 == 0; }
+// tc_channel_perm order (a 16-bit type, Cg a multiple of 16).
+inline bool tc_pack_permuted(int dtype, int Cg) { return (dtype == kBF16 || dtype == kF16) && Cg % 16 == 0; }
 // after_pack: the launch directly follows this call's launch_pack_weight on
 // the same stream.  It is then a programmatic dependent launch: the CTAs
 // start while the pack runs (the pack lets them launch at once) and only the

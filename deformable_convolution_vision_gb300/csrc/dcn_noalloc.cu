@@ -102,7 +102,9 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
         !is_aligned(offset, 4) || (mask && !is_aligned(mask, 4)) || (bias && !is_aligned(bias, 4)))
         return DCN_ERR_INVALID_ARG;
     // the packed weight must fit the fixed scratch array
-    if (static_cast<unsigned long long>(O) * C * taps * es > kScratchWeightBytes)
+    const int perm = dcn::tc_pack_permuted(dtype, C) ? 1 : 0;
+    const int kc = dcn::pack_kc(C, perm);
+    if (static_cast<unsigned long long>(O) * kc * taps * es > kScratchWeightBytes)
         return DCN_ERR_UNSUPPORTED;
 
     DeviceScratch *s = nullptr;
@@ -112,7 +114,6 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     // the status word keeps the previous call's value: start this call at zero
     if (cudaMemsetAsync(s->status, 0, sizeof(unsigned), cs) != cudaSuccess) return DCN_ERR_CUDA;
-    const int perm = dcn::tc_pack_permuted(dtype, C) ? 1 : 0;
     if (dcn::launch_pack_weight(weight, s->wpack, O, C, kh, kw, dtype, perm, cs) != cudaSuccess)
         return DCN_ERR_CUDA;
 
@@ -128,7 +129,8 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.h0 = 0;
     p.plane = p.Ho * p.Wo;
     p.P = B * p.Ho * p.Wo;
-    p.K = kh * kw * C;
+    p.kc = kc;
+    p.K = kh * kw * kc;
     p.x_cstride = C;
     p.out_stride = O;
     p.og_count = 1;

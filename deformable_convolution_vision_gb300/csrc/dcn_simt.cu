@@ -44,15 +44,16 @@ __global__ void pack_weight_kernel(const T *__restrict__ w, T *__restrict__ wp,
     // a forward kernel launched as this one's programmatic dependent may
     // start now; it waits for this grid's completion before it reads wp
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int K = kh * kw * C;
+    const int kc = pack_kc(C, perm);
+    const int K = kh * kw * kc;
     const int kk = blockIdx.x * blockDim.x + threadIdx.x;
     if (kk >= K) return;
-    const int tap = kk / C;
-    const int cp = kk - tap * C;
+    const int tap = kk / kc;
+    const int cp = kk - tap * kc;
     const int c = perm ? tc_channel_perm(cp) : cp;
     for (int o = blockIdx.y; o < O; o += gridDim.y) {
-        const size_t row = static_cast<size_t>(o) * K;
-        wp[row + kk] = w[row + static_cast<size_t>(c) * (kh * kw) + tap];
+        wp[static_cast<size_t>(o) * K + kk] =
+            c < C ? w[(static_cast<size_t>(o) * C + c) * (kh * kw) + tap] : T();
     }
 }
 
@@ -166,7 +167,7 @@ dcn_simt_kernel(Params p) {
                         const int cl = c - (o / Og) * Cg;   // channel within the output's group
                         if (cl >= 0 && cl < Cg) {
                             const int cp = p.wperm ? tc_channel_perm(cl) : cl;   // packed position
-                            v = to_f32<T>(wp[static_cast<size_t>(o) * p.K + static_cast<size_t>(tap) * Cg + cp]);
+                            v = to_f32<T>(wp[static_cast<size_t>(o) * p.K + static_cast<size_t>(tap) * p.kc + cp]);
                         }
                     }
                     Bs[kk][oo] = v;
@@ -210,8 +211,8 @@ dcn_simt_kernel(Params p) {
 cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int C, int kh, int kw,
                                int dtype, int perm, cudaStream_t stream) {
     // C: the weight's channel count, C_in / groups
-    if (perm && C % 64 != 0) return cudaErrorInvalidValue;
-    const int K = kh * kw * C;
+    if (perm && C % 16 != 0) return cudaErrorInvalidValue;
+    const int K = kh * kw * pack_kc(C, perm);
     const int threads = 256;
     const dim3 grid((K + threads - 1) / threads, O < 65535 ? O : 65535);
     if (dtype == kF32) {

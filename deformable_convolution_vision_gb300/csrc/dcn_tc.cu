@@ -183,7 +183,9 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     const int lane = threadIdx.x % 32;
     const int tiles_x = (p.Wo + TC_TILE_W - 1) / TC_TILE_W;
     const int tiles_y = (p.Ho + TC_TILE_H - 1) / TC_TILE_H;
-    const int ncb = p.C / TC_BK;                // channel blocks of the launch
+    // channel blocks of the launch; with C % 64 != 0 the last block of each
+    // tap is completed with zeros (the packed weight is zero there too)
+    const int ncb = (p.C + TC_BK - 1) / TC_BK;
     const int taps = p.kh * p.kw;
     const int nkb = taps * ncb;
     // The K walk tap-major, channel-minor, seen as virtual taps: (tap,
@@ -317,6 +319,11 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         const int my_g = lane >> 4;     // geometry: tap of the group
         const int my_px = lane & 15;    // geometry: pixel (tile column)
         const int quart = lane & 3;     // gather: 16 channels of the 64-channel K-block
+        // A lane whose 16 channels lie past the last one (C % 64 != 0, last
+        // block of a tap) reads the last 16 real channels instead: finite
+        // data in bounds, which the packed weight's zero rows cancel in the
+        // MMA.  No branch, one min per K-block.
+        const int chan_last = p.C - 16;
         const int rsub = lane >> 2;     // gather: pixels rsub and rsub + 8 of the row
         const uint32_t r_off0 = rsub * 16;
         const uint32_t r_off1 = (rsub + 8) * 16;
@@ -502,7 +509,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 // the four 32-byte corner loads of one of this lane's two pixels
                 // from a table slot; corners outside the image read a clamped
                 // in-image address and carry weight 0
-                auto issue_px = [&](int px, uint32_t slot, const uint16_t *xc, u32x8 (&v)[8]) {
+                auto issue_px = [&](int px, uint32_t slot, int cofs, u32x8 (&v)[8]) {
+                    const uint16_t *xc = x + min(cofs + quart * 16, chan_last);
                     const int4 ci = lds_v4_s32(slot + kIdx + (px ? r_off1 : r_off0));
                     v[4 * px + 0] = ldg_v8(xc + ci.x);
                     v[4 * px + 1] = ldg_v8(xc + ci.y);
@@ -531,8 +539,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 int tap = t_first, cb = kb_first - t_first * vncb;   // virtual tap and its block
                 {
                     const uint32_t slot = table_s + (seq_of(tap) & (TC_TABLE_SLOTS - 1)) * kBuf;
-                    issue_px(0, slot, x + chan_off(tap, cb) + quart * 16, v);
-                    issue_px(1, slot, x + chan_off(tap, cb) + quart * 16, v);
+                    issue_px(0, slot, chan_off(tap, cb), v);
+                    issue_px(1, slot, chan_off(tap, cb), v);
                 }
 
                 for (int kb = kb_first; ok && kb < sg.kb1; kb += TC_TEAMS) {
@@ -600,8 +608,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     }
                     if (has_next) {
                         const uint32_t n_slot = table_s + (seq_of(n_tap) & (TC_TABLE_SLOTS - 1)) * kBuf;
-                        issue_px(0, n_slot, x + chan_off(n_tap, n_cb) + quart * 16, v);
-                        issue_px(1, n_slot, x + chan_off(n_tap, n_cb) + quart * 16, v);
+                        issue_px(0, n_slot, chan_off(n_tap, n_cb), v);
+                        issue_px(1, n_slot, chan_off(n_tap, n_cb), v);
                     }
                     tmem_wait_st();
                     tc_fence_before_sync();
@@ -690,7 +698,7 @@ cudaError_t launch_ex(Kernel kernel, int grid, int smem, cudaStream_t stream, bo
 }  // namespace
 
 bool tc_supported(int C, int O) {
-    return C % TC_BK == 0 && O % 16 == 0 && O >= 16 && O <= 256;
+    return C % 16 == 0 && C > 0 && O % 16 == 0 && O >= 16 && O <= 256;
 }
 
 cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t stream,
@@ -702,8 +710,12 @@ cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t 
     const bool f32 = p.sample_f32 != 0;
     // A multiple of TC_TEAMS stages (with two teams each owns every other
     // one), as many as fit the budget and TMEM, at most 8.
+    // A channel count that is not a multiple of 64 (zero-completed last
+    // block) only with one offset group per launch.
     const int vtaps = p.kh * p.kw * p.og_count;
-    if (vtaps > tc_max_virtual_taps || p.og_count <= 0 || (p.C / TC_BK) % p.og_count != 0)
+    const int ncb = (p.C + TC_BK - 1) / TC_BK;
+    if (vtaps > tc_max_virtual_taps || p.og_count <= 0 || !tc_supported(p.C, p.O) ||
+        (p.og_count > 1 && (p.C % TC_BK != 0 || ncb % p.og_count != 0)) || p.K != p.kh * p.kw * ncb * TC_BK)
         return cudaErrorInvalidValue;
     auto smem_for = [&](int st) { return tc_layout(p.O, st, f32, vtaps).total + 1024 + 1024; };
     auto tmem_fits = [&](int st) { return tmem_acc_cols(p.O) + st * TC_A_COLS <= 512; };
@@ -729,7 +741,7 @@ cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t 
         smem_set = smem;
     }
     const int tiles = p.B * ((p.Ho + TC_TILE_H - 1) / TC_TILE_H) * ((p.Wo + TC_TILE_W - 1) / TC_TILE_W);
-    const int nkb = p.kh * p.kw * (p.C / TC_BK);
+    const int nkb = p.kh * p.kw * ncb;
     const long long total = static_cast<long long>(tiles) * nkb;
     if (p.partial && p.flags && tiles > p.sm_count && p.sm_count > 0) {
         // Stream-K: every CTA (one per SM, all resident) takes an equal run

@@ -81,8 +81,10 @@ typedef enum {
 } dcn_status_t;
 
 /* Kernel selection for bf16 and fp16.  AUTO takes the tcgen05 path when
- * C % 64 == 0, O % 16 == 0, 16 <= O <= 256, x is 32-byte aligned and out is
- * 16-byte aligned, and the CUDA-core path otherwise.  fp32 always takes the
+ * C % 16 == 0, O % 16 == 0, 16 <= O <= 256, x is 32-byte aligned and out is
+ * 16-byte aligned, and the CUDA-core path otherwise.  The tensor-core kernel
+ * contracts 64 channels at a time; when C % 64 != 0 it completes each
+ * tap's last block with zeros.  fp32 always takes the
  * CUDA-core path.  (dcn_forward_ex states its own conditions.) */
 typedef enum {
     DCN_PATH_AUTO = 0,
@@ -115,8 +117,9 @@ DCN_API dcn_status_t dcn_forward(dcn_handle_t h,
 /* The two halves of dcn_forward, for callers that reuse one weight.
  * dcn_pack_weight reorders weight [O,C,kh,kw] into the handle's workspace
  * as [O][(i*kw + j)*C + c] (tap-major, channel-minor).  For bf16 and fp16
- * shapes the tensor-core kernel accepts, the channels inside each 64-channel
- * block are in that kernel's operand order instead; the workspace is
+ * shapes with C % 16 == 0, the channels inside each 64-channel block are in
+ * the tensor-core kernel's operand order instead and each tap is padded
+ * with zeros to a whole number of blocks; the workspace is
  * private to the handle and either kernel reads it correctly.
  * dcn_forward_packed then runs the fused kernel with that packed weight;
  * it returns DCN_ERR_INVALID_ARG if (O, C, kh, kw, dtype) differ from the
@@ -174,8 +177,10 @@ DCN_API dcn_status_t dcn_sync_status(dcn_handle_t h, void *stream);
  * be in (0, 10^10]. */
 DCN_API dcn_status_t dcn_selftest_timeout(dcn_handle_t h, long long timeout_ns, void *stream);
 
-/* Largest packed weight (O*C*kh*kw elements times the element size, in
- * bytes) that dcn_forward_noalloc accepts: 8 MiB. */
+/* Largest packed weight that dcn_forward_noalloc accepts: 8 MiB.  The
+ * packed weight holds O*C'*kh*kw elements of the weight's type, where C' is
+ * C rounded up to a multiple of 64 for bf16/fp16 with C % 16 == 0 (the
+ * tensor-core operand order) and C otherwise. */
 #define DCN_NOALLOC_MAX_WEIGHT_BYTES 8388608ull
 
 /* dcn_forward without any device allocation.  The pages have no
@@ -250,8 +255,9 @@ DCN_API int dcn_out_size(int n, int k, int stride, int pad, int dil);
 /* dcn_forward for the general form.  Argument rules as dcn_forward, plus
  * the descriptor's (its fields as commented; every size product below
  * 2^31).  AUTO takes the tcgen05 path for bf16 and fp16 when, with Cg = C/groups,
- * Og = O/groups, Cq = C/offset_groups: Cg % 64 == 0, Cq % 64 == 0, one of
- * Cg and Cq divides the other, Og % 16 == 0, kh*kw*max(1, Cg/Cq) <= 512,
+ * Og = O/groups, Cq = C/offset_groups: Cg % 16 == 0, one of Cg and Cq
+ * divides the other, Cq % 64 == 0 when Cq < Cg (several offset groups in
+ * one weight group), Og % 16 == 0, kh*kw*max(1, Cg/Cq) <= 512,
  * x is 32-byte and out 16-byte aligned; it runs one launch per weight group
  * and per 256 output channels.  Otherwise the CUDA-core path runs.  NULL
  * desc: DCN_ERR_INVALID_ARG. */

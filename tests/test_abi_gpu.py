@@ -62,13 +62,13 @@ def test_forced_tc_path_rejects_unsupported_shapes(handle):
         dcn.dcn_forward(handle.h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"], out,
                         wl.B, wl.C, wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad, dcn.DCN_F32)
     assert e.value.status == E["DCN_ERR_UNSUPPORTED"]
-    wl2 = WORKLOADS["decoder3x3"].with_(C=48, H=16, W=16)  # C % 64 != 0
+    wl2 = WORKLOADS["decoder3x3"].with_(C=24, H=16, W=16)  # C % 16 != 0
     d2 = to_device(make_inputs(wl2))
     out2 = torch.empty((1, wl2.O, wl2.Ho, wl2.Wo), dtype=torch.bfloat16, device="cuda",
                        memory_format=torch.channels_last)
     with pytest.raises(dcn.DcnError) as e:
         dcn.dcn_forward(handle.h, d2["x"], d2["offset"], d2["mask"], d2["weight"], d2["bias"],
-                        out2, 1, 48, 16, 16, wl2.O, 3, 3, 1, dcn.DCN_BF16)
+                        out2, 1, 24, 16, 16, wl2.O, 3, 3, 1, dcn.DCN_BF16)
     assert e.value.status == E["DCN_ERR_UNSUPPORTED"]
     assert dcn.dcn_sync_status(handle.h) == 0
 

@@ -41,7 +41,7 @@ def test_both_f16_paths(path):
 
 
 def test_simt_odd_f16():
-    # C % 64 != 0: only the CUDA-core kernel takes it
+    # C % 16 != 0: only the CUDA-core kernel takes it
     wl = WORKLOADS["decoder3x3"].with_(dtype="f16", C=24, O=40, H=10, W=9, seed=42)
     check(wl, expect_path=DCN_PATH_SIMT)
 

@@ -45,7 +45,10 @@ def _noalloc(wl, d):
 
 
 def test_noalloc_matches_forward_on_two_calls_in_a_row():
-    cases = [WORKLOADS["decoder3x3"], WORKLOADS["tiny"]]  # tensor-core path, then CUDA-core path
+    # tensor-core path, CUDA-core path, then the tensor-core path with a
+    # zero-padded last channel block (C = 96)
+    cases = [WORKLOADS["decoder3x3"], WORKLOADS["tiny"],
+             WORKLOADS["decoder3x3"].with_(C=96, H=24, W=20, seed=95)]
     results = []
     for wl in cases:
         d = to_device(make_inputs(wl))
