@@ -10,6 +10,11 @@ timed with CUDA events on the stream the kernels run on; ms_per_step is
 the mean, the maximum over ranks when several run (weak scaling: every rank
 runs the same workload, no collective on the data path).
 
+Also reported, outside the headline value: the same call without the L2
+flush (warm_l2_mean), the host-buffer entry end to end (e2e), the backward
+pass, the MSDA forward, and the forward on the decoder 3x3, backbone 3x3
+and boundary 5x5 configurations (other_configs).
+
 Prints one JSON line.  --impl reference times the CPU oracle instead.
 """
 
@@ -331,6 +336,57 @@ def time_msda(args, dcn, torch, dev, stream, flush, pk):
     return res
 
 
+def time_other_configs(args, dcn, torch, dev, stream, flush, pk):
+    """The forward on the other synthetic configurations (decoder 3x3,
+    backbone 3x3, boundary 5x5): the public dcn_forward call, L2 flushed
+    before each, against the same roofline as the headline workload."""
+    if args.no_other_configs:
+        return None
+    from deformable_convolution_vision_gb300.inputs import WORKLOADS, make_inputs
+    res = {}
+    for name in ("decoder3x3", "backbone3x3", "boundary5x5"):
+        wl = WORKLOADS[name]
+        inp = make_inputs(wl)
+        x = inp["x"].to(dev).contiguous(memory_format=torch.channels_last)
+        off = inp["offset"].to(dev)
+        m = None if inp["mask"] is None else inp["mask"].to(dev)
+        w = inp["weight"].to(dev).contiguous()
+        b = None if inp["bias"] is None else inp["bias"].to(dev)
+        out = torch.empty((wl.B, wl.O, wl.Ho, wl.Wo), dtype=x.dtype, device=dev,
+                          memory_format=torch.channels_last)
+        dims = (wl.B, wl.C, wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad,
+                dcn.DCN_BF16 if wl.dtype == "bf16" else dcn.DCN_F32)
+        with dcn.Handle() as h:
+            call = lambda: dcn.dcn_forward(h.h, x, off, m, w, b, out, *dims, stream)
+            for _ in range(5):
+                flush.fill_(3)
+                call()
+            n = max(3, min(args.steps, 200))
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+            for k in range(n):
+                flush.fill_(k & 0xFF)
+                ev[k][0].record(stream)
+                call()
+                ev[k][1].record(stream)
+            torch.cuda.synchronize(dev)
+            if dcn.dcn_sync_status(h.h, stream) != 0:
+                raise RuntimeError(f"device status set on {name}")
+            path = dcn.dcn_last_path(h.h)
+        us = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+        t_tc = wl.flops / (pk["bf16_tflops"] * 1e12)
+        t_hbm = algorithmic_bytes(wl) / (pk["hbm_gbs"] * 1e9)
+        res[name] = {
+            "config": config_dict(wl, "flushed before every call")["workload"],
+            "us_per_call": us, "tflops": wl.flops / (us * 1e-6) / 1e12,
+            "out_pixels_per_s": wl.pixels / (us * 1e-6), "calls": n,
+            "path": "tensor cores" if path == dcn.DCN_PATH_TC else "CUDA cores",
+            "roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm",
+                         "frac": max(t_tc, t_hbm) / (us * 1e-6),
+                         "t_tensor_us": t_tc * 1e6, "t_hbm_us": t_hbm * 1e6,
+                         "scope": "whole dcn_forward call (weight pack + fused kernel)"}}
+    return res
+
+
 def run_ours(args, wl, rank, local_rank, world):
     import torch
     import deformable_convolution_vision_gb300 as dcn
@@ -409,6 +465,17 @@ def run_ours(args, wl, rank, local_rank, world):
     ms_max = reduce_max(ms, world)
     main_mean = statistics.fmean(main_ms)
 
+    # the same call with no flush between steps (inputs left in L2 by the
+    # previous step), reported apart and labelled as such
+    n_warm = min(args.steps, 500)
+    evw = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_warm)]
+    for k in range(n_warm):
+        evw[k][0].record(stream)
+        step()
+        evw[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    warm_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in evw)
+
     # end to end through the host-buffer entry point: pinned host inputs in,
     # pinned host output back, copies inside the timed region
     hx = inp["x"].permute(0, 2, 3, 1).contiguous().pin_memory()
@@ -431,6 +498,7 @@ def run_ours(args, wl, rank, local_rank, world):
     e2e_max = reduce_max(e2e_s, world)
     backward = time_backward(args, wl, dcn, torch, dev, stream, h, x, off, m, w, flush, code)
     msda = time_msda(args, dcn, torch, dev, stream, flush, peaks()[0])
+    others = time_other_configs(args, dcn, torch, dev, stream, flush, peaks()[0])
     h.close()
 
     if rank != 0:
@@ -451,7 +519,9 @@ def run_ours(args, wl, rank, local_rank, world):
         "roofline_frac_step": max(t_tc, t_hbm) / (ms_max * 1e-3),
         "step_ms": {"mean": ms, "min": min(step_ms), "median": statistics.median(step_ms),
                     "pack_mean": statistics.fmean(pack_ms), "main_mean": main_mean,
-                    "main_min": min(main_ms)},
+                    "main_min": min(main_ms),
+                    "warm_l2_mean": warm_ms,
+                    "warm_l2_note": "no flush between steps; not the reported value"},
         "roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "achieved": achieved,
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops"], "traffic": dram_traffic(wl.name),
@@ -470,6 +540,8 @@ def run_ours(args, wl, rank, local_rank, world):
         line["backward"] = backward
     if msda is not None:
         line["msda"] = msda
+    if others is not None:
+        line["other_configs"] = others
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -488,6 +560,7 @@ def main(argv=None):
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--backward-steps", type=int, default=50)
     ap.add_argument("--no-msda", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
