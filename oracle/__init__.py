@@ -80,6 +80,9 @@ class Oracle:
         if hasattr(lib, "oracle_msda_forward"):
             lib.oracle_msda_forward.argtypes = [f, f, f, i, f, f, i, f] + [i] * 7
             lib.oracle_msda_forward.restype = i
+        if hasattr(lib, "oracle_msda_backward"):
+            lib.oracle_msda_backward.argtypes = [f, f, f, i, f, f, i, f, f, f, f] + [i] * 7
+            lib.oracle_msda_backward.restype = i
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i
         self._lib = lib
@@ -264,6 +267,33 @@ class Oracle:
             raise ValueError("oracle_msda_forward rejected its arguments")
         return out
 
+    def msda_backward(self, value, shapes, starts, locations, weights, grad_out, softmax=False,
+                      nthreads=0):
+        """Gradients of msda_forward for the cotangent grad_out [B, Q, G, D]:
+        (grad_value [B, S, G, D], grad_locations [B, Q, G, L, K, 2],
+        grad_weights [B, Q, G, L*K]), fp64."""
+        value, locations, weights, grad_out = (self._f32(t) for t in
+                                               (value, locations, weights, grad_out))
+        shapes = np.ascontiguousarray(np.asarray(shapes), dtype=np.int32).reshape(-1, 2)
+        starts = np.ascontiguousarray(np.asarray(starts), dtype=np.int32).reshape(-1)
+        B, S, G, D = value.shape
+        L = shapes.shape[0]
+        Bq, Q, G2, L2, K, two = locations.shape
+        if ((Bq, G2, L2, two) != (B, G, L, 2) or weights.shape != (B, Q, G, L * K)
+                or starts.shape != (L,) or grad_out.shape != (B, Q, G, D)):
+            raise ValueError("msda shapes do not match")
+        gv = np.empty((B, S, G, D), dtype=np.float64)
+        gl = np.empty((B, Q, G, L, K, 2), dtype=np.float64)
+        gw = np.empty((B, Q, G, L * K), dtype=np.float64)
+        rc = self._lib.oracle_msda_backward(self._ptr(value), self._ptr(shapes), self._ptr(starts), L,
+                                            self._ptr(locations), self._ptr(weights),
+                                            int(bool(softmax)), self._ptr(grad_out), self._ptr(gv),
+                                            self._ptr(gl), self._ptr(gw), B, S, G, D, Q, K,
+                                            int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_msda_backward rejected its arguments")
+        return gv, gl, gw
+
 
 class ConvDesc:
     """Convolution parameters of the general problem: stride, padding and
@@ -328,3 +358,7 @@ def backward_points_ex(*args, **kwargs):
 
 def msda_forward(*args, **kwargs):
     return get().msda_forward(*args, **kwargs)
+
+
+def msda_backward(*args, **kwargs):
+    return get().msda_backward(*args, **kwargs)
