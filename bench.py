@@ -12,8 +12,8 @@ runs the same workload, no collective on the data path).
 
 Also reported, outside the headline value: the same call without the L2
 flush (warm_l2_mean), the host-buffer entry end to end (e2e), the backward
-pass, the MSDA forward, and the forward on the decoder 3x3, backbone 3x3
-and boundary 5x5 configurations (other_configs).
+pass, the MSDA forward and backward, and the forward on the decoder 3x3,
+backbone 3x3 and boundary 5x5 configurations (other_configs).
 
 Prints one JSON line.  --impl reference times the CPU oracle instead.
 """
@@ -387,6 +387,64 @@ def time_other_configs(args, dcn, torch, dev, stream, flush, pk):
     return res
 
 
+def msda_backward_bytes(m, es):
+    """Algorithmic HBM bytes of one MSDA backward call: value, grad_out,
+    locations and weights read once; the fp32 value gradient (zeroed, then
+    written), location and weight gradients written once."""
+    pts = m.B * m.Q * m.G * m.L * m.K
+    return (m.B * m.S * m.G * m.D * (es + 2 * 4) + m.B * m.Q * m.G * m.D * es
+            + pts * 2 * 4 * 2 + pts * 4 * 2)
+
+
+def time_msda_backward(args, dcn, torch, dev, stream, flush, pk):
+    """The MSDA backward on the encoder-scale workloads: whole
+    dcn_msda_backward calls (the zeroing of grad_value included), CUDA
+    events, L2 flushed before each."""
+    if args.no_msda:
+        return None
+    from deformable_convolution_vision_gb300.inputs import (MSDA_WORKLOADS, make_msda_grad_out,
+                                                            make_msda_inputs)
+    res = {}
+    for name in ("msda_encoder", "msda_encoder_22k"):
+        m = MSDA_WORKLOADS[name]
+        inp = make_msda_inputs(m)
+        v = inp["value"].to(dev)
+        loc = inp["locations"].to(dev)
+        w = inp["weights"].to(dev)
+        go = make_msda_grad_out(m).to(dev)
+        gv = torch.empty((m.B, m.S, m.G, m.D), dtype=torch.float32, device=dev)
+        gl = torch.empty((m.B, m.Q, m.G, m.L, m.K, 2), dtype=torch.float32, device=dev)
+        gw = torch.empty((m.B, m.Q, m.G, m.L * m.K), dtype=torch.float32, device=dev)
+        code = {torch.bfloat16: dcn.DCN_BF16, torch.float16: dcn.DCN_F16}.get(v.dtype, dcn.DCN_F32)
+        call = lambda: dcn.dcn_msda_backward(v, m.shapes, m.starts, loc, w, go, gv, gl, gw, m.B,
+                                             m.S, m.G, m.D, m.Q, m.K, True, code, stream)
+        for _ in range(5):
+            flush.fill_(3)
+            call()
+        n = max(3, min(args.steps, 200))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for k in range(n):
+            flush.fill_(k & 0xFF)
+            ev[k][0].record(stream)
+            call()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        us = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+        nbytes = msda_backward_bytes(m, v.element_size())
+        samples = m.B * m.Q * m.G * m.L * m.K
+        achieved = nbytes / (us * 1e-6) / 1e9
+        res[name] = {
+            "config": f"B={m.B} G={m.G} D={m.D} levels={list(m.shapes)} Q={m.Q} K={m.K} "
+                      f"{m.dtype} softmax",
+            "us_per_call": us, "queries_per_s": m.B * m.Q / (us * 1e-6), "calls": n,
+            "gradients": "value, locations, weights (fp32)",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm_gbs"], "algorithmic_bytes": nbytes,
+                         "fp32_reduction_bytes_on_chip": samples * 4 * m.D * 4,
+                         "scope": "whole dcn_msda_backward call (memset + one kernel)"}}
+    return res
+
+
 def run_ours(args, wl, rank, local_rank, world):
     import torch
     import deformable_convolution_vision_gb300 as dcn
@@ -498,6 +556,7 @@ def run_ours(args, wl, rank, local_rank, world):
     e2e_max = reduce_max(e2e_s, world)
     backward = time_backward(args, wl, dcn, torch, dev, stream, h, x, off, m, w, flush, code)
     msda = time_msda(args, dcn, torch, dev, stream, flush, peaks()[0])
+    msda_bwd = time_msda_backward(args, dcn, torch, dev, stream, flush, peaks()[0])
     others = time_other_configs(args, dcn, torch, dev, stream, flush, peaks()[0])
     h.close()
 
@@ -540,6 +599,8 @@ def run_ours(args, wl, rank, local_rank, world):
         line["backward"] = backward
     if msda is not None:
         line["msda"] = msda
+    if msda_bwd is not None:
+        line["msda_backward"] = msda_bwd
     if others is not None:
         line["other_configs"] = others
     if world == 1 and not args.no_cpu_baseline:

@@ -13,7 +13,7 @@ from . import binding
 from .binding import (DCN_BF16, DCN_F16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
                       DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, ConvDesc, DcnError, dcn_create,
                       dcn_backward, dcn_backward_ex, dcn_destroy, dcn_forward, dcn_forward_ex,
-                      dcn_msda_forward, dcn_nchw_to_nhwc, dcn_nhwc_to_nchw,
+                      dcn_msda_backward, dcn_msda_forward, dcn_nchw_to_nhwc, dcn_nhwc_to_nchw,
                       dcn_forward_host,
                       dcn_forward_packed, dcn_forward_packed_ex, dcn_last_path, dcn_out_size,
                       dcn_pack_weight, dcn_pack_weight_ex, dcn_selftest_timeout, dcn_set_path,
@@ -26,7 +26,8 @@ __all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF1
            "dcn_set_path", "dcn_last_path", "dcn_sync_status", "dcn_selftest_timeout",
            "dcn_status_string", "ConvDesc", "dcn_forward_ex", "dcn_pack_weight_ex",
            "dcn_forward_packed_ex", "dcn_out_size", "dcn_backward", "dcn_backward_ex",
-           "deform_conv2d_backward", "dcn_msda_forward", "msda", "dcn_nchw_to_nhwc",
+           "deform_conv2d_backward", "dcn_msda_forward", "msda", "dcn_msda_backward",
+           "msda_backward", "dcn_nchw_to_nhwc",
            "dcn_nhwc_to_nchw", "deform_conv2d_nchw"]
 
 
@@ -212,6 +213,41 @@ def msda(value, shapes, starts, locations, weights, method=None, out=None, strea
     dcn_msda_forward(value, shapes, starts, locations, weights, out, B, S, G, D, Q, K,
                      method == "softmax", _dtype_code(value), stream)
     return out
+
+
+def msda_backward(grad_out, value, shapes, starts, locations, weights, method=None, stream=None):
+    """Gradients of ``msda`` for the cotangent grad_out [B, Q, G, D] (value's
+    dtype, contiguous): returns (grad_value [B, S, G, D], grad_locations
+    [B, Q, G, L, K, 2], grad_weights [B, Q, G, L*K]), all float32 (the
+    kernel accumulates them in fp32).  Same argument rules as ``msda``."""
+    import torch
+    if method not in (None, "softmax"):
+        raise ValueError("method must be None or 'softmax'")
+    shapes = [tuple(int(v) for v in hw) for hw in (shapes.tolist() if hasattr(shapes, "tolist") else shapes)]
+    starts = [int(v) for v in (starts.tolist() if hasattr(starts, "tolist") else starts)]
+    if len(shapes) != len(starts):
+        raise ValueError("shapes and starts must describe the same levels")
+    for name, t in (("value", value), ("locations", locations), ("weights", weights),
+                    ("grad_out", grad_out)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if locations.dtype != torch.float32 or weights.dtype != torch.float32:
+        raise TypeError("locations and weights must be float32")
+    if grad_out.dtype != value.dtype:
+        raise TypeError("grad_out must have value's dtype")
+    B, S, G, D = value.shape
+    Bq, Q, G2, L, K, two = locations.shape
+    if (Bq, G2, L, two) != (B, G, len(shapes), 2) or tuple(weights.shape) != (B, Q, G, L * K):
+        raise ValueError("locations must be [B, Q, G, L, K, 2] and weights [B, Q, G, L*K]")
+    if tuple(grad_out.shape) != (B, Q, G, D):
+        raise ValueError("grad_out must be [B, Q, G, D]")
+    dev = value.device
+    gv = torch.empty((B, S, G, D), dtype=torch.float32, device=dev)
+    gl = torch.empty((B, Q, G, L, K, 2), dtype=torch.float32, device=dev)
+    gw = torch.empty((B, Q, G, L * K), dtype=torch.float32, device=dev)
+    dcn_msda_backward(value, shapes, starts, locations, weights, grad_out, gv, gl, gw,
+                      B, S, G, D, Q, K, method == "softmax", _dtype_code(value), stream)
+    return gv, gl, gw
 
 
 def deform_conv2d_nchw(input, offset, weight, bias=None, stride=1, padding=0, dilation=1,

@@ -4,7 +4,7 @@ in the library's kernels."""
 
 import torch
 
-from . import deform_conv2d, deform_conv2d_backward
+from . import deform_conv2d, deform_conv2d_backward, msda, msda_backward
 
 
 class DeformConv2dFunction(torch.autograd.Function):
@@ -38,3 +38,28 @@ def deform_conv2d_autograd(x, offset, weight, bias=None, stride=1, padding=0, di
                            mask=None):
     """deform_conv2d that records the graph for torch.autograd."""
     return DeformConv2dFunction.apply(x, offset, mask, weight, bias, stride, padding, dilation)
+
+
+class MsdaFunction(torch.autograd.Function):
+    """out = msda(value, shapes, starts, locations, weights, method);
+    gradients for value (in its dtype), locations and weights (float32)."""
+
+    @staticmethod
+    def forward(ctx, value, locations, weights, shapes, starts, method=None):
+        out = msda(value, shapes, starts, locations, weights, method=method)
+        ctx.save_for_backward(value, locations, weights)
+        ctx.meta = (shapes, starts, method)
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        value, locations, weights = ctx.saved_tensors
+        shapes, starts, method = ctx.meta
+        gv, gl, gw = msda_backward(grad_out.to(value.dtype).contiguous(), value, shapes, starts,
+                                   locations, weights, method=method)
+        return gv.to(value.dtype), gl, gw, None, None, None
+
+
+def msda_autograd(value, shapes, starts, locations, weights, method=None):
+    """msda that records the graph for torch.autograd."""
+    return MsdaFunction.apply(value, locations, weights, shapes, starts, method)

@@ -24,7 +24,7 @@ EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_f
            "dcn_selftest_timeout", "dcn_status_string", "dcn_forward_noalloc",
            "dcn_set_sample_precision", "dcn_out_size", "dcn_forward_ex", "dcn_pack_weight_ex",
            "dcn_forward_packed_ex", "dcn_backward", "dcn_backward_ex", "dcn_msda_forward",
-           "dcn_nchw_to_nhwc", "dcn_nhwc_to_nchw"]
+           "dcn_msda_backward", "dcn_nchw_to_nhwc", "dcn_nhwc_to_nchw"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -75,6 +75,7 @@ def load():
         "dcn_backward": ([P] * 11 + [I] * 9 + [P], I),
         "dcn_backward_ex": ([P] * 11 + [ctypes.POINTER(ConvDesc), I, P], I),
         "dcn_msda_forward": ([P, P, P, I, P, P, P] + [I] * 8 + [P], I),
+        "dcn_msda_backward": ([P, P, P, I, P, P, P, P, P, P] + [I] * 8 + [P], I),
         "dcn_nchw_to_nhwc": ([P, P] + [I] * 5 + [P], I),
         "dcn_nhwc_to_nchw": ([P, P] + [I] * 5 + [P], I),
     }
@@ -228,6 +229,19 @@ def dcn_msda_forward(value, shapes, starts, locations, weights, out, B, S, G, D,
     _check(load().dcn_msda_forward(_ptr(value), sh, st, L, _ptr(locations), _ptr(weights), _ptr(out),
                                    B, S, G, D, Q, K, int(bool(softmax)), dtype, _stream(stream)),
            "dcn_msda_forward")
+
+
+def dcn_msda_backward(value, shapes, starts, locations, weights, grad_out, grad_value,
+                      grad_locations, grad_weights, B, S, G, D, Q, K, softmax, dtype, stream=None):
+    """shapes: host sequence of (H, W) pairs; starts: host sequence of row offsets."""
+    L = len(starts)
+    sh = (ctypes.c_int * (2 * L))(*[int(v) for hw in shapes for v in hw])
+    st = (ctypes.c_int * L)(*[int(v) for v in starts])
+    _check(load().dcn_msda_backward(_ptr(value), sh, st, L, _ptr(locations), _ptr(weights),
+                                    _ptr(grad_out), _ptr(grad_value), _ptr(grad_locations),
+                                    _ptr(grad_weights), B, S, G, D, Q, K, int(bool(softmax)),
+                                    dtype, _stream(stream)),
+           "dcn_msda_backward")
 
 
 def dcn_nchw_to_nhwc(src, dst, B, C, H, W, dtype, stream=None):

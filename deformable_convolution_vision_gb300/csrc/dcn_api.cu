@@ -708,6 +708,52 @@ dcn_status_t dcn_msda_forward(const void *value, const int *shapes, const int *s
     return DCN_OK;
 }
 
+dcn_status_t dcn_msda_backward(const void *value, const int *shapes, const int *starts, int L,
+                               const float *locations, const float *weights, const void *grad_out,
+                               float *grad_value, float *grad_locations, float *grad_weights,
+                               int B, int S, int G, int D, int Q, int K, int softmax, int dtype,
+                               void *stream) {
+    if (!value || !shapes || !starts || !locations || !weights || !grad_out || !grad_value ||
+        !grad_locations || !grad_weights)
+        return DCN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
+    if (B <= 0 || S <= 0 || G <= 0 || D <= 0 || Q <= 0 || K <= 0) return DCN_ERR_INVALID_ARG;
+    if (L <= 0 || L > dcn::kMsdaMaxLevels) return DCN_ERR_UNSUPPORTED;
+    const long long LK = static_cast<long long>(L) * K;
+    if (static_cast<long long>(B) * S * G * D > kIndexLimit ||
+        static_cast<long long>(B) * Q * G * LK * 2 > kIndexLimit ||
+        static_cast<long long>(B) * Q * G * D > kIndexLimit)
+        return DCN_ERR_INVALID_ARG;
+    const size_t es = esize(dtype);
+    if (!aligned(value, es) || !aligned(grad_out, es) || !aligned(locations, 8) ||
+        !aligned(weights, 4) || !aligned(grad_value, 4) || !aligned(grad_locations, 8) ||
+        !aligned(grad_weights, 4))
+        return DCN_ERR_INVALID_ARG;
+    dcn::MsdaBwdParams p;
+    for (int l = 0; l < L; ++l) {
+        const int H = shapes[2 * l], W = shapes[2 * l + 1];
+        if (H <= 0 || W <= 0 || starts[l] < 0 ||
+            static_cast<long long>(starts[l]) + static_cast<long long>(H) * W > S)
+            return DCN_ERR_INVALID_ARG;
+        p.H[l] = H;
+        p.W[l] = W;
+        p.start[l] = starts[l];
+    }
+    p.value = value; p.locations = locations; p.weights = weights; p.grad_out = grad_out;
+    p.grad_value = grad_value; p.grad_locations = grad_locations; p.grad_weights = grad_weights;
+    p.B = B; p.S = S; p.G = G; p.D = D; p.Q = Q; p.K = K; p.L = L;
+    p.softmax = softmax ? 1 : 0;
+    cudaStream_t s = as_stream(stream);
+    // the value gradient is a sum of reductions: start it at zero
+    if (cudaMemsetAsync(grad_value, 0, static_cast<size_t>(B) * S * G * D * sizeof(float), s) !=
+        cudaSuccess)
+        return DCN_ERR_CUDA;
+    const bool vec = D % (dtype == DCN_F32 ? 4 : 8) == 0 && aligned(value, 16) &&
+                     aligned(grad_out, 16) && aligned(grad_value, 16);
+    if (dcn::launch_msda_backward(p, dtype, vec, s) != cudaSuccess) return DCN_ERR_CUDA;
+    return DCN_OK;
+}
+
 static dcn_status_t layout_copy(const void *src, void *dst, int B, int R, int S, int dtype,
                                 void *stream) {
     if (!src || !dst || src == dst) return DCN_ERR_INVALID_ARG;

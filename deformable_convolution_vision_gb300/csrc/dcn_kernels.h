@@ -182,6 +182,24 @@ struct MsdaParams {
 // vec: D a multiple of 8 (16-bit) or 4 (fp32) and value/out 16-byte aligned.
 cudaError_t launch_msda(const MsdaParams &p, int dtype, bool vec, cudaStream_t stream);
 
+// MSDA backward: the forward's operands plus the cotangent, fp32 gradients.
+// grad_value must be zero on entry (the kernel accumulates into it).
+struct MsdaBwdParams {
+    const void *value;        // [B, S, G, D], the operand dtype
+    const float *locations;   // [B, Q, G, L, K, 2]
+    const float *weights;     // [B, Q, G, L*K]
+    const void *grad_out;     // [B, Q, G, D], the operand dtype
+    float *grad_value;        // [B, S, G, D]
+    float *grad_locations;    // [B, Q, G, L, K, 2]
+    float *grad_weights;      // [B, Q, G, L*K]
+    int B, S, G, D, Q, K, L;
+    int softmax;
+    int H[kMsdaMaxLevels], W[kMsdaMaxLevels], start[kMsdaMaxLevels];
+};
+// vec: D a multiple of 8 (16-bit) or 4 (fp32); value, grad_out and
+// grad_value 16-byte aligned.
+cudaError_t launch_msda_backward(const MsdaBwdParams &p, int dtype, bool vec, cudaStream_t stream);
+
 // Batched 2-D transpose [B][R][S] -> [B][S][R] of 2- or 4-byte elements.
 cudaError_t launch_transpose(const void *src, void *dst, int B, int R, int S, int esize,
                              cudaStream_t stream);

@@ -1,0 +1,236 @@
+// Multi-scale deformable attention (MSDA), backward, on CUDA cores.
+//
+// The gradients of the forward in dcn_msda.cu (page "deformops 3.0.1",
+// section "Multi-scale deformable attention") for a cotangent go =
+// grad_out[b,q,g,:], the chain rule term by term.  Per (b, q, g) and point
+// t = (l, k), with the bilinear weights wy, wx of the forward and only the
+// corners c inside level l:
+//
+//   grad_a[t]        = sum_c wy wx <go, v_c>
+//   grad_value[c]   += a[t] wy wx go                  (fp32 reductions)
+//   grad_loc[t]      = a[t] (W_l sum_c wy sx <go, v_c>,  H_l sum_c sy wx <go, v_c>)
+//   grad_weights[t]  = grad_a[t], or with softmax a[t] (grad_a[t] - sum_s a[s] grad_a[s])
+//
+// sx, sy = -1 for the left/top corner, +1 for the right/bottom one (the
+// derivative of the cell picked by floor(), i.e. the right-hand one at an
+// integer coordinate).  The page's backward writes the value gradient with
+// no intermediate sampling buffer (section "DeformOps", "Zero-buffer
+// kernels"); so does this one, with fp32 reductions straight into
+// grad_value -- the page's float32-accumulator mode (section "Backend
+// selection"), which is exact where native half-precision atomics would
+// round every partial sum.
+//
+// Layout of the work: a group of GRP lanes per (b, q, g); lane r takes the
+// CH-channel chunks r, r + GRP, ... of the head (CH = 8 for 16-bit values,
+// 4 for fp32, one 16-byte load per corner; or 1).  Every lane computes each
+// point's corners and weights itself (the same addresses and arithmetic
+// in the whole group), loads its chunks of the four corner rows and of go,
+// accumulates its partial dot products, and reduces the three per-point
+// sums across the group with shuffles.  The lane t % GRP writes point t's
+// location gradient and its raw grad_a into grad_weights; with softmax the
+// same lane later reads that entry back and replaces it.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstring>
+
+#include "dcn_kernels.h"
+
+namespace dcn {
+
+namespace {
+
+template <typename T, int CH>
+__device__ __forceinline__ void bwd_load(const T *p, float (&v)[CH]);
+
+template <>
+__device__ __forceinline__ void bwd_load<float, 4>(const float *p, float (&v)[4]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+template <>
+__device__ __forceinline__ void bwd_load<__nv_bfloat16, 8>(const __nv_bfloat16 *p, float (&v)[8]) {
+    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(w[e] << 16);
+        v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void bwd_load<__half, 8>(const __half *p, float (&v)[8]) {
+    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        __half2 h;
+        memcpy(&h, &w[e], 4);
+        const float2 f = __half22float2(h);
+        v[2 * e] = f.x;
+        v[2 * e + 1] = f.y;
+    }
+}
+template <>
+__device__ __forceinline__ void bwd_load<float, 1>(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
+template <>
+__device__ __forceinline__ void bwd_load<__nv_bfloat16, 1>(const __nv_bfloat16 *p, float (&v)[1]) {
+    v[0] = __bfloat162float(*p);
+}
+template <>
+__device__ __forceinline__ void bwd_load<__half, 1>(const __half *p, float (&v)[1]) {
+    v[0] = __half2float(*p);
+}
+
+// grad_value[p .. p + CH) += s * g[0 .. CH): fp32 reductions (16 bytes each
+// for CH a multiple of 4; p is then 16-byte aligned)
+template <int CH>
+__device__ __forceinline__ void red_scaled(float *p, float s, const float (&g)[CH]) {
+    if constexpr (CH % 4 == 0) {
+#pragma unroll
+        for (int e = 0; e < CH; e += 4)
+            asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                         :: "l"(p + e), "f"(s * g[e]), "f"(s * g[e + 1]), "f"(s * g[e + 2]),
+                            "f"(s * g[e + 3]) : "memory");
+    } else {
+#pragma unroll
+        for (int e = 0; e < CH; ++e) atomicAdd(p + e, s * g[e]);
+    }
+}
+
+template <int GRP>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int m = GRP / 2; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+template <typename T, int CH, int GRP>
+__global__ void __launch_bounds__(256)
+msda_backward_kernel(MsdaBwdParams p) {
+    static_assert((GRP & (GRP - 1)) == 0 && GRP <= 32, "row group");
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long rows = static_cast<long long>(p.B) * p.Q * p.G;
+    // lanes past the last row work on the last row (for the shuffles) and
+    // write nothing
+    const bool live = t < rows * GRP;
+    const long long row = live ? t / GRP : rows - 1;     // (b, q, g)
+    const int r = static_cast<int>(t % GRP);             // lane within the row group
+    const int g = static_cast<int>(row % p.G);
+    const int b = static_cast<int>(row / (static_cast<long long>(p.Q) * p.G));
+    const int LK = p.L * p.K;
+    const int nch = p.D / CH;                            // chunks of the head
+    const float *__restrict__ wrow = p.weights + row * LK;
+    const float *__restrict__ lrow = p.locations + row * LK * 2;
+    const T *__restrict__ value = static_cast<const T *>(p.value);
+    const T *__restrict__ go_row = static_cast<const T *>(p.grad_out) + row * p.D;
+    float *__restrict__ gl_row = p.grad_locations + row * LK * 2;
+    float *__restrict__ gw_row = p.grad_weights + row * LK;
+    const int GD = p.G * p.D;
+
+    // the forward's attention weights (fp32 softmax, largest logit first)
+    float wmax = -INFINITY, wsum = 1.0f;
+    if (p.softmax) {
+        for (int i = r; i < LK; i += GRP) wmax = fmaxf(wmax, __ldg(wrow + i));
+#pragma unroll
+        for (int m = GRP / 2; m >= 1; m >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, m));
+        wsum = 0.0f;
+        for (int i = r; i < LK; i += GRP) wsum += expf(__ldg(wrow + i) - wmax);
+        wsum = group_sum<GRP>(wsum);
+    }
+    const float inv = 1.0f / wsum;
+
+    float s_ag = 0.0f;   // sum over points of a[t] * grad_a[t] (the same in every lane)
+    for (int l = 0; l < p.L; ++l) {
+        const int H = p.H[l], W = p.W[l];
+        const T *vlevel = value + (static_cast<size_t>(b) * p.S + p.start[l]) * GD + g * p.D;
+        float *glevel = p.grad_value + (static_cast<size_t>(b) * p.S + p.start[l]) * GD + g * p.D;
+        for (int k = 0; k < p.K; ++k) {
+            const int i = l * p.K + k;
+            const float lw = __ldg(wrow + i);
+            const float a = p.softmax ? expf(lw - wmax) * inv : lw;
+            const float2 loc = __ldg(reinterpret_cast<const float2 *>(lrow) + i);
+            // the forward's pixel coordinates, cell and weights
+            float px = __fsub_rn(__fmul_rn(loc.x, static_cast<float>(W)), 0.5f);
+            float py = __fsub_rn(__fmul_rn(loc.y, static_cast<float>(H)), 0.5f);
+            px = fminf(fmaxf(px, -2.0f), static_cast<float>(W + 1));
+            py = fminf(fmaxf(py, -2.0f), static_cast<float>(H + 1));
+            const float fx = floorf(px), fy = floorf(py);
+            const float lx = px - fx, ly = py - fy;
+            const int x0 = static_cast<int>(fx), y0 = static_cast<int>(fy);
+            const float wy[2] = {1.0f - ly, ly};
+            const float wx[2] = {1.0f - lx, lx};
+            float ga = 0.0f, gpx = 0.0f, gpy = 0.0f;     // this lane's partial sums
+            for (int c0 = r; c0 < nch; c0 += GRP) {
+                float go[CH];
+                bwd_load<T, CH>(go_row + c0 * CH, go);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int ay = c >> 1, ex = c & 1;
+                    const int yy = y0 + ay, xx = x0 + ex;
+                    if (static_cast<unsigned>(yy) >= static_cast<unsigned>(H) ||
+                        static_cast<unsigned>(xx) >= static_cast<unsigned>(W))
+                        continue;
+                    const size_t off = static_cast<size_t>(yy * W + xx) * GD + c0 * CH;
+                    float v[CH];
+                    bwd_load<T, CH>(vlevel + off, v);
+                    float dot = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < CH; ++e) dot = fmaf(go[e], v[e], dot);
+                    const float cw = wy[ay] * wx[ex];
+                    ga = fmaf(cw, dot, ga);
+                    gpx = fmaf(ex ? wy[ay] : -wy[ay], dot, gpx);
+                    gpy = fmaf(ay ? wx[ex] : -wx[ex], dot, gpy);
+                    if (live) red_scaled<CH>(glevel + off, a * cw, go);
+                }
+            }
+            ga = group_sum<GRP>(ga);
+            gpx = group_sum<GRP>(gpx);
+            gpy = group_sum<GRP>(gpy);
+            s_ag = fmaf(a, ga, s_ag);
+            if (live && r == i % GRP) {
+                *reinterpret_cast<float2 *>(gl_row + 2 * i) =
+                    make_float2(a * gpx * static_cast<float>(W), a * gpy * static_cast<float>(H));
+                gw_row[i] = ga;
+            }
+        }
+    }
+    if (p.softmax && live) {
+        // this lane's own entries, written above: grad_a -> a (grad_a - sum a grad_a)
+        for (int i = r; i < LK; i += GRP) {
+            const float a = expf(__ldg(wrow + i) - wmax) * inv;
+            gw_row[i] = a * (gw_row[i] - s_ag);
+        }
+    }
+}
+
+template <typename T, int CH>
+cudaError_t launch_t(const MsdaBwdParams &p, cudaStream_t stream) {
+    const int nch = p.D / CH;
+    // the largest power of two up to 32 that does not exceed the chunk count
+    int grp = 1;
+    while (grp * 2 <= nch && grp < 32) grp *= 2;
+    const long long threads = static_cast<long long>(p.B) * p.Q * p.G * grp;
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 2147483647ll) return cudaErrorInvalidValue;
+    const unsigned nb = static_cast<unsigned>(blocks);
+    switch (grp) {
+    case 1: msda_backward_kernel<T, CH, 1><<<nb, 256, 0, stream>>>(p); break;
+    case 2: msda_backward_kernel<T, CH, 2><<<nb, 256, 0, stream>>>(p); break;
+    case 4: msda_backward_kernel<T, CH, 4><<<nb, 256, 0, stream>>>(p); break;
+    case 8: msda_backward_kernel<T, CH, 8><<<nb, 256, 0, stream>>>(p); break;
+    case 16: msda_backward_kernel<T, CH, 16><<<nb, 256, 0, stream>>>(p); break;
+    default: msda_backward_kernel<T, CH, 32><<<nb, 256, 0, stream>>>(p); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_msda_backward(const MsdaBwdParams &p, int dtype, bool vec, cudaStream_t stream) {
+    if (dtype == kF32) return vec ? launch_t<float, 4>(p, stream) : launch_t<float, 1>(p, stream);
+    if (dtype == kF16) return vec ? launch_t<__half, 8>(p, stream) : launch_t<__half, 1>(p, stream);
+    return vec ? launch_t<__nv_bfloat16, 8>(p, stream) : launch_t<__nv_bfloat16, 1>(p, stream);
+}
+
+}  // namespace dcn

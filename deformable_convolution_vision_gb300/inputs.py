@@ -226,6 +226,13 @@ def make_msda_inputs(wl: MsdaWorkload):
             "weights": weights.contiguous()}
 
 
+def make_msda_grad_out(wl: MsdaWorkload):
+    """A cotangent for the backward: grad_out [B, Q, G, D] ~ N(0, 1) in the
+    compute dtype, from its own seed (the workload's + 1000)."""
+    g = torch.Generator().manual_seed(wl.seed + 1000)
+    return torch.randn(wl.B, wl.Q, wl.G, wl.D, generator=g).to(TORCH_DTYPE[wl.dtype])
+
+
 _PAGE_LEVELS = ((64, 64), (32, 32), (16, 16), (8, 8))
 MSDA_WORKLOADS = {
     w.name: w for w in [

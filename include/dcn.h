@@ -388,6 +388,39 @@ DCN_API dcn_status_t dcn_msda_forward(const void *value, const int *shapes, cons
                               int B, int S, int G, int D, int Q, int K, int softmax,
                               int dtype, void *stream);
 
+/* The backward of dcn_msda_forward: for the cotangent grad_out [B, Q, G, D]
+ * (`dtype`, like value), the gradients with respect to value, locations and
+ * weights, all fp32.  The chain rule applied to the definition above; with
+ * go = grad_out[b,q,g,:], per point t = (l, k) and inside corner c of its
+ * sample, bilinear weights wy, wx:
+ *
+ *   grad_value[c]     += a[t] wy wx go
+ *   grad_a[t]          = sum_c wy wx <go, v_c>
+ *   grad_locations[t]  = a[t] (W_l sum_c wy sx <go, v_c>, H_l sum_c sy wx <go, v_c>)
+ *   grad_weights[t]    = grad_a[t], or with softmax
+ *                        a[t] (grad_a[t] - sum_s a[s] grad_a[s])
+ *
+ * sx, sy = -1 for the left/top corner and +1 for the right/bottom one: at
+ * an integer coordinate the derivative of the cell floor() picks; a point
+ * whose corners are all outside has zero gradients.  The page's backward
+ * writes the value gradient with no intermediate sampling buffer, and its
+ * float32 accumulator is the exact choice (section "Backend selection");
+ * this one accumulates grad_value by fp32 reductions (so its last bits
+ * depend on the order of the additions).
+ *
+ * Layouts (device pointers, dense): value, locations, weights, shapes,
+ * starts as dcn_msda_forward; grad_out [B, Q, G, D] `dtype`; grad_value
+ * [B, S, G, D] fp32, overwritten (zeroed first, then accumulated);
+ * grad_locations [B, Q, G, L, K, 2] fp32, 8-byte aligned, overwritten;
+ * grad_weights [B, Q, G, L*K] fp32, overwritten.  Every pointer is
+ * required.  Arithmetic in fp32.  Errors as dcn_msda_forward.
+ * Asynchronous on `stream`; allocates nothing; no handle. */
+DCN_API dcn_status_t dcn_msda_backward(const void *value, const int *shapes, const int *starts,
+                               int L, const float *locations, const float *weights,
+                               const void *grad_out, float *grad_value, float *grad_locations,
+                               float *grad_weights, int B, int S, int G, int D, int Q, int K,
+                               int softmax, int dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

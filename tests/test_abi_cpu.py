@@ -87,6 +87,8 @@ def test_python_wrappers_marshal_every_argument(lib):
                                         None, desc, 1, 0),
         lambda: binding.dcn_msda_forward(None, [(8, 8)], [0], None, None, None, 1, 64, 8, 32, 10,
                                          4, True, 1, 0),
+        lambda: binding.dcn_msda_backward(None, [(8, 8)], [0], None, None, None, None, None, None,
+                                          1, 64, 8, 32, 10, 4, True, 1, 0),
         lambda: binding.dcn_nchw_to_nhwc(None, None, 1, 64, 8, 8, 1, 0),
         lambda: binding.dcn_nhwc_to_nchw(None, None, 1, 64, 8, 8, 1, 0),
     ]
