@@ -19,6 +19,8 @@ stay fp32.
 
 from dataclasses import dataclass, replace
 
+import math
+
 import torch
 
 
@@ -224,6 +226,30 @@ def make_msda_inputs(wl: MsdaWorkload):
     weights = torch.rand(wl.B, wl.Q, wl.G, wl.L * wl.K, generator=g)
     return {"value": value.to(TORCH_DTYPE[wl.dtype]), "locations": loc.contiguous(),
             "weights": weights.contiguous()}
+
+
+def make_device_inputs(wl: Workload, device="cuda", offset_bound=3.0):
+    """Inputs for problems too large to build on the host, drawn on the
+    device from a seeded device generator: x ~ N(0, 1) in the compute dtype
+    (channels-last), offsets ~ U(-offset_bound, offset_bound) (bounded, so
+    that the corners a pixel reaches lie within a small window of it),
+    sigmoid mask of N(0, 1), weight ~ N(0, 1/(kh*kw*C)), bias ~ N(0, 0.1),
+    all in the ABI layouts."""
+    g = torch.Generator(device=device).manual_seed(wl.seed)
+    dt = TORCH_DTYPE[wl.dtype]
+    x = torch.empty((wl.B, wl.C, wl.H, wl.W), dtype=dt, device=device,
+                    memory_format=torch.channels_last)
+    # fill in slabs of rows so that no fp32 temporary of x's size exists
+    for h0 in range(0, wl.H, 256):
+        h1 = min(wl.H, h0 + 256)
+        x[:, :, h0:h1] = torch.randn((wl.B, wl.C, h1 - h0, wl.W), generator=g, device=device).to(dt)
+    off = (torch.rand((wl.B, 2 * wl.taps, wl.Ho, wl.Wo), generator=g, device=device) * 2.0 - 1.0)
+    off.mul_(offset_bound)
+    mask = torch.sigmoid(torch.randn((wl.B, wl.taps, wl.Ho, wl.Wo), generator=g, device=device))
+    weight = (torch.randn((wl.O, wl.C, wl.kh, wl.kw), generator=g, device=device)
+              / math.sqrt(wl.taps * wl.C)).to(dt)
+    bias = torch.randn(wl.O, generator=g, device=device) * 0.1
+    return {"x": x, "offset": off, "mask": mask, "weight": weight, "bias": bias}
 
 
 def make_msda_grad_out(wl: MsdaWorkload):
