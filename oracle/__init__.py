@@ -39,9 +39,10 @@ CFLAGS = ["-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off"
 
 
 MSDA_SOURCE = os.path.join(_HERE, "msda_oracle.c")
+ATTN_SOURCE = os.path.join(_HERE, "attn_oracle.c")
 
 
-def compile_oracle(source=SOURCE, output=LIBRARY, extra=(MSDA_SOURCE,)):
+def compile_oracle(source=SOURCE, output=LIBRARY, extra=(MSDA_SOURCE, ATTN_SOURCE)):
     """Compile the oracle's C sources into a shared library (gcc)."""
     cmd = ["gcc", *CFLAGS, source, *extra, "-o", output, "-lm"]
     subprocess.run(cmd, check=True)
@@ -52,7 +53,7 @@ def _stale(source, output):
     if not os.path.exists(output):
         return True
     built = os.path.getmtime(output)
-    return any(os.path.getmtime(s) > built for s in (source, MSDA_SOURCE))
+    return any(os.path.getmtime(s) > built for s in (source, MSDA_SOURCE, ATTN_SOURCE))
 
 
 class Oracle:
@@ -80,6 +81,9 @@ class Oracle:
         if hasattr(lib, "oracle_msda_forward"):
             lib.oracle_msda_forward.argtypes = [f, f, f, i, f, f, i, f] + [i] * 7
             lib.oracle_msda_forward.restype = i
+        if hasattr(lib, "oracle_attn_forward"):
+            lib.oracle_attn_forward.argtypes = [f, f, f, i, f] + [i] * 14
+            lib.oracle_attn_forward.restype = i
         if hasattr(lib, "oracle_msda_backward"):
             lib.oracle_msda_backward.argtypes = [f, f, f, i, f, f, i, f, f, f, f] + [i] * 7
             lib.oracle_msda_backward.restype = i
@@ -267,6 +271,30 @@ class Oracle:
             raise ValueError("oracle_msda_forward rejected its arguments")
         return out
 
+    def attn_forward(self, value, offsets, weights, kernel_size, stride=1, padding=0, dilation=1,
+                     softmax=False, nthreads=0):
+        """Single-scale deformable sampling: value [B, H, W, G, D], offsets
+        [B, Ho, Wo, G, K, 2] as (dy, dx), weights [B, Ho, Wo, G, K]; returns
+        out [B, Ho, Wo, G, D] in fp64.  kernel_size, stride, padding and
+        dilation are ints or (h, w) pairs."""
+        pair = lambda v: (int(v), int(v)) if np.isscalar(v) else (int(v[0]), int(v[1]))  # noqa: E731
+        (kh, kw), (sh, sw), (ph, pw), (dh, dw) = (pair(v) for v in
+                                                  (kernel_size, stride, padding, dilation))
+        value, offsets, weights = (self._f32(t) for t in (value, offsets, weights))
+        B, H, W, G, D = value.shape
+        K = kh * kw
+        Ho = (H + 2 * ph - dh * (kh - 1) - 1) // sh + 1
+        Wo = (W + 2 * pw - dw * (kw - 1) - 1) // sw + 1
+        if offsets.shape != (B, Ho, Wo, G, K, 2) or weights.shape != (B, Ho, Wo, G, K):
+            raise ValueError("attn shapes do not match")
+        out = np.empty((B, Ho, Wo, G, D), dtype=np.float64)
+        rc = self._lib.oracle_attn_forward(self._ptr(value), self._ptr(offsets), self._ptr(weights),
+                                           int(bool(softmax)), self._ptr(out), B, H, W, G, D, kh, kw,
+                                           sh, sw, ph, pw, dh, dw, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_attn_forward rejected its arguments")
+        return out
+
     def msda_backward(self, value, shapes, starts, locations, weights, grad_out, softmax=False,
                       nthreads=0):
         """Gradients of msda_forward for the cotangent grad_out [B, Q, G, D]:
@@ -362,3 +390,7 @@ def msda_forward(*args, **kwargs):
 
 def msda_backward(*args, **kwargs):
     return get().msda_backward(*args, **kwargs)
+
+
+def attn_forward(*args, **kwargs):
+    return get().attn_forward(*args, **kwargs)

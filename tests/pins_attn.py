@@ -1,0 +1,159 @@
+"""Pins of the single-scale deformable sampling oracle: checks against what
+the mathematics, a library routine and the separately pinned convolution
+oracle fix, independently of this oracle's own code.
+
+- the operator is a depthwise deformable convolution with unit weights, G
+  offset groups and the aggregation weights as the mask: the convolution
+  oracle (pinned on its own) on those inputs;
+- the library bilinear resampler (torch grid_sample, zero padding, fp64)
+  per group and tap, then the weighted sum (softmax by torch in fp64);
+- integer offsets: every sample is one pixel of the map, exactly;
+- every corner outside: exactly 0;
+- a constant map sampled inside with softmax weights: the constant.
+"""
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+# (B, H, W, G, D, kernel, stride, padding, dilation)
+CASES = [
+    (2, 9, 11, 2, 3, (3, 3), (1, 1), (1, 1), (1, 1)),
+    (1, 12, 10, 3, 2, (3, 2), (2, 1), (1, 0), (1, 2)),
+    (1, 7, 8, 1, 4, (1, 1), (1, 1), (0, 0), (1, 1)),
+    (2, 10, 9, 4, 1, (5, 3), (2, 2), (2, 1), (2, 1)),
+]
+
+
+def _out_size(n, k, s, p, d):
+    return (n + 2 * p - d * (k - 1) - 1) // s + 1
+
+
+def _problem(seed, B, H, W, G, D, kernel, stride, padding, dilation, offset_std=1.5):
+    g = torch.Generator().manual_seed(seed)
+    kh, kw = kernel
+    Ho = _out_size(H, kh, stride[0], padding[0], dilation[0])
+    Wo = _out_size(W, kw, stride[1], padding[1], dilation[1])
+    K = kh * kw
+    value = torch.randn(B, H, W, G, D, generator=g)
+    off = torch.randn(B, Ho, Wo, G, K, 2, generator=g) * offset_std
+    w = torch.randn(B, Ho, Wo, G, K, generator=g)
+    return value, off, w, Ho, Wo
+
+
+def _rel(got, ref):
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-300))
+
+
+def pin_attn_depthwise_convolution(orc):
+    from oracle import ConvDesc
+    for n, (B, H, W, G, D, kernel, stride, padding, dilation) in enumerate(CASES):
+        value, off, w, Ho, Wo = _problem(700 + n, B, H, W, G, D, kernel, stride, padding, dilation)
+        kh, kw = kernel
+        K, C = kh * kw, G * D
+        x = value.reshape(B, H, W, C).permute(0, 3, 1, 2).contiguous()
+        # offset group q's planes: 2 (q K + k) = dy, 2 (q K + k) + 1 = dx
+        offset = off.permute(0, 3, 4, 5, 1, 2).reshape(B, 2 * G * K, Ho, Wo).contiguous()
+        weight = torch.ones(C, 1, kh, kw)
+        conv = ConvDesc(stride=stride, padding=padding, dilation=dilation, groups=C, offset_groups=G)
+        for softmax in (False, True):
+            a = torch.softmax(w.double(), dim=-1).float() if softmax else w
+            mask = a.permute(0, 3, 4, 1, 2).reshape(B, G * K, Ho, Wo).contiguous()
+            ref = orc.forward_ex(x, offset, mask, weight, None, conv)        # [B, C, Ho, Wo]
+            ref = ref.transpose(0, 2, 3, 1).reshape(B, Ho, Wo, G, D)
+            got = orc.attn_forward(value, off, a if softmax else w, kernel, stride, padding,
+                                   dilation, softmax=False)
+            err = _rel(got, ref)
+            assert err <= 1e-12, f"attn vs depthwise convolution, case {n}: {err:.3e}"
+            if softmax:
+                # the operator's own softmax against torch's, rounded to fp32
+                got_sm = orc.attn_forward(value, off, w, kernel, stride, padding, dilation,
+                                          softmax=True)
+                assert _rel(got_sm, ref) <= 1e-6, f"attn softmax, case {n}"
+
+
+def _grid_sample_reference(value, off, w, kernel, stride, padding, dilation, softmax):
+    B, H, W, G, D = value.shape
+    _, Ho, Wo, _, K, _ = off.shape
+    kh, kw = kernel
+    a = torch.softmax(w.double(), dim=-1) if softmax else w.double()
+    out = torch.zeros(B, Ho, Wo, G, D, dtype=torch.float64)
+    hs = torch.arange(Ho).view(Ho, 1) * stride[0] - padding[0]
+    ws = torch.arange(Wo).view(1, Wo) * stride[1] - padding[1]
+    for g in range(G):
+        inp = value[:, :, :, g, :].double().permute(0, 3, 1, 2)          # [B, D, H, W]
+        for k in range(K):
+            i, j = k // kw, k % kw
+            # the oracle's fp32 coordinates
+            py = ((hs + i * dilation[0]).float() + off[:, :, :, g, k, 0]).double()
+            px = ((ws + j * dilation[1]).float() + off[:, :, :, g, k, 1]).double()
+            grid = torch.stack([(2.0 * px + 1.0) / W - 1.0, (2.0 * py + 1.0) / H - 1.0], dim=-1)
+            samp = F.grid_sample(inp, grid, mode="bilinear", padding_mode="zeros",
+                                 align_corners=False)                     # [B, D, Ho, Wo]
+            out[:, :, :, g, :] += samp.permute(0, 2, 3, 1) * a[:, :, :, g, k].unsqueeze(-1)
+    return out.numpy()
+
+
+def pin_attn_grid_sample(orc):
+    for n, (B, H, W, G, D, kernel, stride, padding, dilation) in enumerate(CASES):
+        value, off, w, _, _ = _problem(720 + n, B, H, W, G, D, kernel, stride, padding, dilation)
+        for softmax in (False, True):
+            got = orc.attn_forward(value, off, w, kernel, stride, padding, dilation, softmax)
+            ref = _grid_sample_reference(value, off, w, kernel, stride, padding, dilation, softmax)
+            err = _rel(got, ref)
+            assert err <= 1e-10, f"attn grid_sample case {n} softmax={softmax}: {err:.3e}"
+
+
+def pin_attn_integer_offsets(orc):
+    B, H, W, G, D, kernel, stride, padding, dilation = CASES[1]
+    value, off, w, Ho, Wo = _problem(740, B, H, W, G, D, kernel, stride, padding, dilation)
+    off = torch.round(off * 2.0)
+    got = orc.attn_forward(value, off, w, kernel, stride, padding, dilation, False)
+    kh, kw = kernel
+    v = value.double().numpy()
+    exp = np.zeros_like(got)
+    for b in range(B):
+        for ho in range(Ho):
+            for wo in range(Wo):
+                for g in range(G):
+                    for k in range(kh * kw):
+                        i, j = k // kw, k % kw
+                        y = ho * stride[0] - padding[0] + i * dilation[0] + int(off[b, ho, wo, g, k, 0])
+                        x = wo * stride[1] - padding[1] + j * dilation[1] + int(off[b, ho, wo, g, k, 1])
+                        if 0 <= y < H and 0 <= x < W:
+                            exp[b, ho, wo, g] += float(w[b, ho, wo, g, k]) * v[b, y, x, g]
+    assert _rel(got, exp) <= 1e-13
+
+
+def pin_attn_outside(orc):
+    B, H, W, G, D, kernel, stride, padding, dilation = CASES[0]
+    value, off, w, _, _ = _problem(750, B, H, W, G, D, kernel, stride, padding, dilation)
+    off[..., 1] = torch.where(torch.rand(off[..., 1].shape) < 0.5, -float(W + 3), float(2 * W + 3))
+    for softmax in (False, True):
+        got = orc.attn_forward(value, off, w, kernel, stride, padding, dilation, softmax)
+        assert not np.any(got)
+
+
+def pin_attn_constant(orc):
+    B, H, W, G, D, kernel, stride, padding, dilation = (1, 12, 14, 3, 4, (3, 3), (1, 1), (1, 1), (1, 1))
+    value, off, w, Ho, Wo = _problem(760, B, H, W, G, D, kernel, stride, padding, dilation)
+    const = torch.randn(G, D)
+    value = const.view(1, 1, 1, G, D).expand_as(value).contiguous()
+    # positions within half a pixel of the tap, clamped into [0, H-1] x [0, W-1]:
+    # every corner with a nonzero weight is inside, so the softmax-weighted
+    # sum is the constant
+    kh, kw = kernel
+    for k in range(kh * kw):
+        i, j = k // kw, k % kw
+        by = (torch.arange(Ho) * stride[0] - padding[0] + i * dilation[0]).view(1, Ho, 1, 1).float()
+        bx = (torch.arange(Wo) * stride[1] - padding[1] + j * dilation[1]).view(1, 1, Wo, 1).float()
+        r = torch.rand(B, Ho, Wo, G, 2) - 0.5
+        off[..., k, 0] = (by + r[..., 0]).clamp(0.0, H - 1.0) - by
+        off[..., k, 1] = (bx + r[..., 1]).clamp(0.0, W - 1.0) - bx
+    got = orc.attn_forward(value, off, w, kernel, stride, padding, dilation, True)
+    exp = const.double().numpy()[None, None, None].repeat(Ho, 1).repeat(Wo, 2)
+    assert np.abs(got - exp).max() <= 1e-12 * np.abs(exp).max()
+
+
+ALL_ATTN_PINS = [pin_attn_depthwise_convolution, pin_attn_grid_sample, pin_attn_integer_offsets,
+                 pin_attn_outside, pin_attn_constant]
