@@ -754,6 +754,38 @@ dcn_status_t dcn_msda_backward(const void *value, const int *shapes, const int *
     return DCN_OK;
 }
 
+dcn_status_t dcn_attn_forward(const void *value, const float *offsets, const float *weights,
+                              void *out, int B, int H, int W, int G, int D, int kh, int kw,
+                              int stride_h, int stride_w, int pad_h, int pad_w, int dil_h,
+                              int dil_w, int softmax, int dtype, void *stream) {
+    if (!value || !offsets || !weights || !out) return DCN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || W <= 0 || G <= 0 || D <= 0 || kh <= 0 || kw <= 0 || stride_h <= 0 ||
+        stride_w <= 0 || pad_h < 0 || pad_w < 0 || dil_h <= 0 || dil_w <= 0)
+        return DCN_ERR_INVALID_ARG;
+    const long long Ho = out_size_ll(H, kh, stride_h, pad_h, dil_h);
+    const long long Wo = out_size_ll(W, kw, stride_w, pad_w, dil_w);
+    if (Ho <= 0 || Wo <= 0) return DCN_ERR_INVALID_ARG;
+    const long long K = static_cast<long long>(kh) * kw;
+    const long long GD = static_cast<long long>(G) * D;
+    if (K > kIndexLimit || static_cast<long long>(B) * H * W * GD > kIndexLimit ||
+        B * Ho * Wo * G * K * 2 > kIndexLimit || B * Ho * Wo * GD > kIndexLimit)
+        return DCN_ERR_INVALID_ARG;
+    const size_t es = esize(dtype);
+    if (!aligned(value, es) || !aligned(out, es) || !aligned(offsets, 8) || !aligned(weights, 4))
+        return DCN_ERR_INVALID_ARG;
+    dcn::AttnParams p;
+    p.value = value; p.offsets = offsets; p.weights = weights; p.out = out;
+    p.B = B; p.H = H; p.W = W; p.G = G; p.D = D;
+    p.Ho = static_cast<int>(Ho); p.Wo = static_cast<int>(Wo);
+    p.kh = kh; p.kw = kw; p.sh = stride_h; p.sw = stride_w; p.ph = pad_h; p.pw = pad_w;
+    p.dh = dil_h; p.dw = dil_w;
+    p.softmax = softmax ? 1 : 0;
+    const bool vec = D % (dtype == DCN_F32 ? 4 : 8) == 0 && aligned(value, 16) && aligned(out, 16);
+    if (dcn::launch_attn(p, dtype, vec, as_stream(stream)) != cudaSuccess) return DCN_ERR_CUDA;
+    return DCN_OK;
+}
+
 static dcn_status_t layout_copy(const void *src, void *dst, int B, int R, int S, int dtype,
                                 void *stream) {
     if (!src || !dst || src == dst) return DCN_ERR_INVALID_ARG;

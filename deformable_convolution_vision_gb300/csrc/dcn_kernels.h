@@ -200,6 +200,19 @@ struct MsdaBwdParams {
 // grad_value 16-byte aligned.
 cudaError_t launch_msda_backward(const MsdaBwdParams &p, int dtype, bool vec, cudaStream_t stream);
 
+// Single-scale deformable sampling (DCNv3), forward.
+struct AttnParams {
+    const void *value;        // [B, H, W, G, D], the operand dtype
+    const float *offsets;     // [B, Ho, Wo, G, K, 2], (dy, dx), 8-byte aligned
+    const float *weights;     // [B, Ho, Wo, G, K]
+    void *out;                // [B, Ho, Wo, G, D], the operand dtype
+    int B, H, W, G, D, Ho, Wo;
+    int kh, kw, sh, sw, ph, pw, dh, dw;
+    int softmax;              // 1: normalize the weights over the K taps
+};
+// vec: D a multiple of 8 (16-bit) or 4 (fp32) and value/out 16-byte aligned.
+cudaError_t launch_attn(const AttnParams &p, int dtype, bool vec, cudaStream_t stream);
+
 // Batched 2-D transpose [B][R][S] -> [B][S][R] of 2- or 4-byte elements.
 cudaError_t launch_transpose(const void *src, void *dst, int B, int R, int S, int esize,
                              cudaStream_t stream);

@@ -259,6 +259,62 @@ def make_msda_grad_out(wl: MsdaWorkload):
     return torch.randn(wl.B, wl.Q, wl.G, wl.D, generator=g).to(TORCH_DTYPE[wl.dtype])
 
 
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Single-scale deformable sampling (the deformops page's attn, the DCNv3
+    operator): value [B, H, W, G, D] ~ N(0, 1) in the compute dtype,
+    offsets [B, Ho, Wo, G, K, 2] ~ N(0, offset_std) pixels (dy, dx), weights
+    [B, Ho, Wo, G, K] ~ U(0, 1) raw logits (softmax applied in the operator
+    when `softmax`)."""
+    name: str
+    B: int
+    H: int
+    W: int
+    G: int
+    D: int
+    kernel: tuple = (3, 3)
+    stride: tuple = (1, 1)
+    padding: tuple = (1, 1)
+    dilation: tuple = (1, 1)
+    dtype: str = "bf16"
+    softmax: bool = True
+    offset_std: float = 2.0
+    seed: int = 0
+
+    def out_size(self):
+        def one(n, k, s, p, d):
+            return (n + 2 * p - d * (k - 1) - 1) // s + 1
+        return (one(self.H, self.kernel[0], self.stride[0], self.padding[0], self.dilation[0]),
+                one(self.W, self.kernel[1], self.stride[1], self.padding[1], self.dilation[1]))
+
+    @property
+    def K(self):
+        return self.kernel[0] * self.kernel[1]
+
+
+def make_attn_inputs(wl: AttnWorkload):
+    g = torch.Generator().manual_seed(wl.seed)
+    Ho, Wo = wl.out_size()
+    value = torch.randn(wl.B, wl.H, wl.W, wl.G, wl.D, generator=g)
+    off = torch.randn(wl.B, Ho, Wo, wl.G, wl.K, 2, generator=g) * wl.offset_std
+    weights = torch.rand(wl.B, Ho, Wo, wl.G, wl.K, generator=g)
+    return {"value": value.to(TORCH_DTYPE[wl.dtype]), "offsets": off.contiguous(),
+            "weights": weights.contiguous()}
+
+
+ATTN_WORKLOADS = {
+    w.name: w for w in [
+        # the page's layer example: DeformSample2d(dim=64, kernel_size=3,
+        # groups=4) on a 32 x 32 map
+        AttnWorkload("attn_page", 1, 32, 32, 4, 16, seed=90),
+        # a DCNv3 layer at the first stage of an InternImage-scale backbone on
+        # a 1024 x 1024 image (256 x 256 map, 112 channels in 7 groups of 16),
+        # two images
+        AttnWorkload("attn_stage1_1024", 2, 256, 256, 7, 16, seed=91),
+    ]
+}
+
+
 _PAGE_LEVELS = ((64, 64), (32, 32), (16, 16), (8, 8))
 MSDA_WORKLOADS = {
     w.name: w for w in [

@@ -421,6 +421,42 @@ DCN_API dcn_status_t dcn_msda_backward(const void *value, const int *shapes, con
                                float *grad_weights, int B, int S, int G, int D, int Q, int K,
                                int softmax, int dtype, void *stream);
 
+/* ------------------------------------------------ single-scale deformable sampling
+ *
+ * The forward pass of the operator of page "deformops 3.0.1", section
+ * "Single-scale deformable sampling" (the layers DeformAttn2d and
+ * DeformSample2d, functional form attn; the DCNv3 operator of InternImage),
+ * which samples and aggregates without the spatial weight of deformable
+ * convolution.  B batch, G groups of D channels, a kh x kw tap grid (K
+ * taps, tap k = i*kw + j):
+ *
+ *   out[b,ho,wo,g,d] = sum_k a[b,ho,wo,g,k] * S(value[b,:,:,g,d], py, px),
+ *   py = ho*stride_h - pad_h + i*dil_h + dy,  px = wo*stride_w - pad_w + j*dil_w + dx,
+ *
+ * S the bilinear sample (corners outside the map contribute 0), (dy, dx)
+ * = offsets[b,ho,wo,g,k,:], a the weights as given or, with softmax != 0,
+ * softmax-normalized over the K taps of each (b, ho, wo, g).  The page
+ * fixes none of the coordinate details; these are the deformable
+ * convolution's own (its tap grid, stride, padding and dilation, (dy, dx)
+ * pixel offsets), so the operator equals a depthwise dcn_forward_ex with
+ * unit weights, G offset groups and the weights as the mask.
+ * Ho = (H + 2 pad_h - dil_h (kh-1) - 1) / stride_h + 1, Wo likewise.
+ *
+ * Layouts (device pointers, dense, channels-last):
+ *   value    [B, H, W, G, D]         `dtype`
+ *   offsets  [B, Ho, Wo, G, K, 2]    fp32 (dy, dx), 8-byte aligned
+ *   weights  [B, Ho, Wo, G, K]       fp32
+ *   out      [B, Ho, Wo, G, D]       `dtype`
+ * Arithmetic in fp32 (coordinates, weights, softmax, sums), one rounding to
+ * `dtype` at the end.  Every size positive (pads >= 0), Ho, Wo > 0, each
+ * tensor below 2^31 elements, else DCN_ERR_INVALID_ARG.  Asynchronous on
+ * `stream`; allocates nothing; no handle. */
+DCN_API dcn_status_t dcn_attn_forward(const void *value, const float *offsets,
+                              const float *weights, void *out, int B, int H, int W, int G,
+                              int D, int kh, int kw, int stride_h, int stride_w, int pad_h,
+                              int pad_w, int dil_h, int dil_w, int softmax, int dtype,
+                              void *stream);
+
 #ifdef __cplusplus
 }
 #endif
