@@ -21,6 +21,9 @@
 // values, 4 for fp32: one 16-byte load per corner; or 1).  Every lane
 // computes each tap's corners and weights itself; the softmax maximum and
 // sum are group reductions.  Sums in fp32, one rounding to the output type.
+// For a 3 x 3 grid (KT = 9) the taps are unrolled and every corner load is
+// unconditional (an outside corner reads the map's first pixel with weight
+// 0), so that the loads of many taps can be in flight together.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -87,7 +90,7 @@ __device__ __forceinline__ void attn_store(T *p, const float (&acc)[CH]) {
     for (int e = 0; e < CH; ++e) p[e] = attn_from_f32<T>(acc[e]);
 }
 
-template <typename T, int CH, int GRP>
+template <typename T, int CH, int GRP, int KT>
 __global__ void __launch_bounds__(256)
 attn_forward_kernel(AttnParams p) {
     static_assert((GRP & (GRP - 1)) == 0 && GRP <= 32, "row group");
@@ -103,7 +106,8 @@ attn_forward_kernel(AttnParams p) {
     const int wo = static_cast<int>(pix % p.Wo);
     const int ho = static_cast<int>((pix / p.Wo) % p.Ho);
     const int b = static_cast<int>(pix / (static_cast<long long>(p.Wo) * p.Ho));
-    const int K = p.kh * p.kw;
+    const int K = KT > 0 ? KT : p.kh * p.kw;
+    const int kw = KT == 9 ? 3 : p.kw;
     const int nch = p.D / CH;
     const int GD = p.G * p.D;
     const float *__restrict__ wrow = p.weights + row * K;
@@ -129,8 +133,9 @@ attn_forward_kernel(AttnParams p) {
         float acc[CH];
 #pragma unroll
         for (int e = 0; e < CH; ++e) acc[e] = 0.0f;
+#pragma unroll (KT > 0 ? KT : 1)
         for (int k = 0; k < K; ++k) {
-            const int i = k / p.kw, j = k - (k / p.kw) * p.kw;
+            const int i = k / kw, j = k - (k / kw) * kw;
             const float lw = __ldg(wrow + k);
             const float a = p.softmax ? expf(lw - wmax) * inv : lw;
             const float2 o = __ldg(orow + k);                // (dy, dx)
@@ -148,13 +153,16 @@ attn_forward_kernel(AttnParams p) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int yy = y0 + (c >> 1), xx = x0 + (c & 1);
-                if (static_cast<unsigned>(yy) >= static_cast<unsigned>(p.H) ||
-                    static_cast<unsigned>(xx) >= static_cast<unsigned>(p.W))
-                    continue;
+                const bool in = static_cast<unsigned>(yy) < static_cast<unsigned>(p.H) &&
+                                static_cast<unsigned>(xx) < static_cast<unsigned>(p.W);
+                if constexpr (KT == 0) {
+                    if (!in) continue;
+                }
                 float v[CH];
-                attn_load<T, CH>(vbase + static_cast<size_t>(yy * p.W + xx) * GD + c0 * CH, v);
+                attn_load<T, CH>(vbase + static_cast<size_t>(in ? yy * p.W + xx : 0) * GD + c0 * CH, v);
+                const float wc = in ? wq[c] : 0.0f;
 #pragma unroll
-                for (int e = 0; e < CH; ++e) acc[e] = fmaf(wq[c], v[e], acc[e]);
+                for (int e = 0; e < CH; ++e) acc[e] = fmaf(wc, v[e], acc[e]);
             }
         }
         if (live) attn_store<T, CH>(static_cast<T *>(p.out) + row * p.D + c0 * CH, acc);
@@ -170,14 +178,22 @@ cudaError_t launch_t(const AttnParams &p, cudaStream_t stream) {
     const long long blocks = (threads + 255) / 256;
     if (blocks > 2147483647ll) return cudaErrorInvalidValue;
     const unsigned nb = static_cast<unsigned>(blocks);
+    const bool k3 = p.kh == 3 && p.kw == 3;
+#define DCN_ATTN_CASE(G_)                                                               \
+    case G_:                                                                            \
+        if (k3) attn_forward_kernel<T, CH, G_, 9><<<nb, 256, 0, stream>>>(p);           \
+        else attn_forward_kernel<T, CH, G_, 0><<<nb, 256, 0, stream>>>(p);              \
+        break;
     switch (grp) {
-    case 1: attn_forward_kernel<T, CH, 1><<<nb, 256, 0, stream>>>(p); break;
-    case 2: attn_forward_kernel<T, CH, 2><<<nb, 256, 0, stream>>>(p); break;
-    case 4: attn_forward_kernel<T, CH, 4><<<nb, 256, 0, stream>>>(p); break;
-    case 8: attn_forward_kernel<T, CH, 8><<<nb, 256, 0, stream>>>(p); break;
-    case 16: attn_forward_kernel<T, CH, 16><<<nb, 256, 0, stream>>>(p); break;
-    default: attn_forward_kernel<T, CH, 32><<<nb, 256, 0, stream>>>(p); break;
+        DCN_ATTN_CASE(1)
+        DCN_ATTN_CASE(2)
+        DCN_ATTN_CASE(4)
+        DCN_ATTN_CASE(8)
+        DCN_ATTN_CASE(16)
+        default:
+        DCN_ATTN_CASE(32)
     }
+#undef DCN_ATTN_CASE
     return cudaGetLastError();
 }
 
