@@ -84,6 +84,9 @@ class Oracle:
         if hasattr(lib, "oracle_attn_forward"):
             lib.oracle_attn_forward.argtypes = [f, f, f, i, f] + [i] * 14
             lib.oracle_attn_forward.restype = i
+        if hasattr(lib, "oracle_attn_backward"):
+            lib.oracle_attn_backward.argtypes = [f, f, f, i, f, f, f, f] + [i] * 14
+            lib.oracle_attn_backward.restype = i
         if hasattr(lib, "oracle_msda_backward"):
             lib.oracle_msda_backward.argtypes = [f, f, f, i, f, f, i, f, f, f, f] + [i] * 7
             lib.oracle_msda_backward.restype = i
@@ -295,6 +298,34 @@ class Oracle:
             raise ValueError("oracle_attn_forward rejected its arguments")
         return out
 
+    def attn_backward(self, value, offsets, weights, grad_out, kernel_size, stride=1, padding=0,
+                      dilation=1, softmax=False, nthreads=0):
+        """Gradients of attn_forward for the cotangent grad_out [B, Ho, Wo,
+        G, D]: (grad_value [B, H, W, G, D], grad_offsets [B, Ho, Wo, G, K, 2]
+        as (dy, dx), grad_weights [B, Ho, Wo, G, K]), fp64."""
+        pair = lambda v: (int(v), int(v)) if np.isscalar(v) else (int(v[0]), int(v[1]))  # noqa: E731
+        (kh, kw), (sh, sw), (ph, pw), (dh, dw) = (pair(v) for v in
+                                                  (kernel_size, stride, padding, dilation))
+        value, offsets, weights, grad_out = (self._f32(t) for t in
+                                             (value, offsets, weights, grad_out))
+        B, H, W, G, D = value.shape
+        K = kh * kw
+        Ho = (H + 2 * ph - dh * (kh - 1) - 1) // sh + 1
+        Wo = (W + 2 * pw - dw * (kw - 1) - 1) // sw + 1
+        if (offsets.shape != (B, Ho, Wo, G, K, 2) or weights.shape != (B, Ho, Wo, G, K)
+                or grad_out.shape != (B, Ho, Wo, G, D)):
+            raise ValueError("attn shapes do not match")
+        gv = np.empty((B, H, W, G, D), dtype=np.float64)
+        go_ = np.empty((B, Ho, Wo, G, K, 2), dtype=np.float64)
+        gw = np.empty((B, Ho, Wo, G, K), dtype=np.float64)
+        rc = self._lib.oracle_attn_backward(self._ptr(value), self._ptr(offsets), self._ptr(weights),
+                                            int(bool(softmax)), self._ptr(grad_out), self._ptr(gv),
+                                            self._ptr(go_), self._ptr(gw), B, H, W, G, D, kh, kw,
+                                            sh, sw, ph, pw, dh, dw, int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_attn_backward rejected its arguments")
+        return gv, go_, gw
+
     def msda_backward(self, value, shapes, starts, locations, weights, grad_out, softmax=False,
                       nthreads=0):
         """Gradients of msda_forward for the cotangent grad_out [B, Q, G, D]:
@@ -394,3 +425,7 @@ def msda_backward(*args, **kwargs):
 
 def attn_forward(*args, **kwargs):
     return get().attn_forward(*args, **kwargs)
+
+
+def attn_backward(*args, **kwargs):
+    return get().attn_backward(*args, **kwargs)
