@@ -13,7 +13,7 @@ runs the same workload, no collective on the data path).
 Also reported, outside the headline value: the same call without the L2
 flush (warm_l2_mean), the host-buffer entry end to end (e2e), the backward
 pass, the MSDA forward and backward, single-scale deformable sampling
-(DCNv3), and the forward on the decoder 3x3, backbone 3x3 and boundary 5x5
+(DCNv3) forward and backward, and the forward on the decoder 3x3, backbone 3x3 and boundary 5x5
 configurations (other_configs).
 
 Prints one JSON line.  --impl reference times the CPU oracle instead.
@@ -498,6 +498,68 @@ def time_attn(args, dcn, torch, dev, stream, flush, pk):
     return res
 
 
+def attn_backward_bytes(a, es):
+    """Algorithmic HBM bytes of one single-scale backward call: value,
+    grad_out, offsets and weights read once; the fp32 value gradient
+    (zeroed, then written), offset and weight gradients written once."""
+    Ho, Wo = a.out_size()
+    rows = a.B * Ho * Wo * a.G
+    return (a.B * a.H * a.W * a.G * a.D * (es + 2 * 4) + rows * a.D * es
+            + rows * a.K * (2 * 4 + 4) * 2)
+
+
+def time_attn_backward(args, dcn, torch, dev, stream, flush, pk):
+    """The single-scale sampling backward: whole dcn_attn_backward calls
+    (the zeroing of grad_value included), CUDA events, L2 flushed before
+    each."""
+    if args.no_msda:
+        return None
+    from deformable_convolution_vision_gb300.inputs import (ATTN_WORKLOADS, make_attn_grad_out,
+                                                            make_attn_inputs)
+    res = {}
+    for name in ("attn_page", "attn_stage1_1024"):
+        a = ATTN_WORKLOADS[name]
+        inp = make_attn_inputs(a)
+        v = inp["value"].to(dev)
+        off = inp["offsets"].to(dev)
+        w = inp["weights"].to(dev)
+        go = make_attn_grad_out(a).to(dev)
+        Ho, Wo = a.out_size()
+        gv = torch.empty((a.B, a.H, a.W, a.G, a.D), dtype=torch.float32, device=dev)
+        gof = torch.empty((a.B, Ho, Wo, a.G, a.K, 2), dtype=torch.float32, device=dev)
+        gw = torch.empty((a.B, Ho, Wo, a.G, a.K), dtype=torch.float32, device=dev)
+        code = {torch.bfloat16: dcn.DCN_BF16, torch.float16: dcn.DCN_F16}.get(v.dtype, dcn.DCN_F32)
+        call = lambda: dcn.dcn_attn_backward(v, off, w, go, gv, gof, gw, a.B, a.H, a.W, a.G, a.D,
+                                             a.kernel[0], a.kernel[1], a.stride[0], a.stride[1],
+                                             a.padding[0], a.padding[1], a.dilation[0],
+                                             a.dilation[1], True, code, stream)
+        for _ in range(5):
+            flush.fill_(3)
+            call()
+        n = max(3, min(args.steps, 200))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for k in range(n):
+            flush.fill_(k & 0xFF)
+            ev[k][0].record(stream)
+            call()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        us = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+        nbytes = attn_backward_bytes(a, v.element_size())
+        samples = a.B * Ho * Wo * a.G * a.K
+        achieved = nbytes / (us * 1e-6) / 1e9
+        res[name] = {
+            "config": f"B={a.B} {a.H}x{a.W} G={a.G} D={a.D} {a.kernel[0]}x{a.kernel[1]} "
+                      f"pad={a.padding[0]} {a.dtype} softmax",
+            "us_per_call": us, "out_pixels_per_s": a.B * Ho * Wo / (us * 1e-6), "calls": n,
+            "gradients": "value, offsets, weights (fp32)",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm_gbs"], "algorithmic_bytes": nbytes,
+                         "fp32_reduction_bytes_on_chip": samples * 4 * a.D * 4,
+                         "scope": "whole dcn_attn_backward call (memset + one kernel)"}}
+    return res
+
+
 def run_ours(args, wl, rank, local_rank, world):
     import torch
     import deformable_convolution_vision_gb300 as dcn
@@ -611,6 +673,7 @@ def run_ours(args, wl, rank, local_rank, world):
     msda = time_msda(args, dcn, torch, dev, stream, flush, peaks()[0])
     msda_bwd = time_msda_backward(args, dcn, torch, dev, stream, flush, peaks()[0])
     attn = time_attn(args, dcn, torch, dev, stream, flush, peaks()[0])
+    attn_bwd = time_attn_backward(args, dcn, torch, dev, stream, flush, peaks()[0])
     others = time_other_configs(args, dcn, torch, dev, stream, flush, peaks()[0])
     h.close()
 
@@ -657,6 +720,8 @@ def run_ours(args, wl, rank, local_rank, world):
         line["msda_backward"] = msda_bwd
     if attn is not None:
         line["single_scale_sampling"] = attn
+    if attn_bwd is not None:
+        line["single_scale_sampling_backward"] = attn_bwd
     if others is not None:
         line["other_configs"] = others
     if world == 1 and not args.no_cpu_baseline:

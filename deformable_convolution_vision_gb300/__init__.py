@@ -13,7 +13,7 @@ from . import binding
 from .binding import (DCN_BF16, DCN_F16, DCN_F32, DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC,
                       DCN_SAMPLE_F32, DCN_SAMPLE_INPUT_DTYPE, ConvDesc, DcnError, dcn_create,
                       dcn_backward, dcn_backward_ex, dcn_destroy, dcn_forward, dcn_forward_ex,
-                      dcn_attn_forward, dcn_msda_backward, dcn_msda_forward, dcn_nchw_to_nhwc,
+                      dcn_attn_backward, dcn_attn_forward, dcn_msda_backward, dcn_msda_forward, dcn_nchw_to_nhwc,
                       dcn_nhwc_to_nchw,
                       dcn_forward_host,
                       dcn_forward_packed, dcn_forward_packed_ex, dcn_last_path, dcn_out_size,
@@ -28,7 +28,8 @@ __all__ = ["binding", "deform_conv2d", "Handle", "DcnError", "DCN_F32", "DCN_BF1
            "dcn_status_string", "ConvDesc", "dcn_forward_ex", "dcn_pack_weight_ex",
            "dcn_forward_packed_ex", "dcn_out_size", "dcn_backward", "dcn_backward_ex",
            "deform_conv2d_backward", "dcn_msda_forward", "msda", "dcn_msda_backward",
-           "msda_backward", "dcn_attn_forward", "attn", "dcn_nchw_to_nhwc",
+           "msda_backward", "dcn_attn_forward", "attn", "dcn_attn_backward",
+           "attn_backward", "dcn_nchw_to_nhwc",
            "dcn_nhwc_to_nchw", "deform_conv2d_nchw"]
 
 
@@ -282,6 +283,42 @@ def attn(value, offsets, weights, kernel_size, stride=1, padding=0, dilation=1, 
     dcn_attn_forward(value, offsets, weights, out, B, H, W, G, D, kh, kw, sh, sw, ph, pw, dh, dw,
                      method == "softmax", _dtype_code(value), stream)
     return out
+
+
+def attn_backward(grad_out, value, offsets, weights, kernel_size, stride=1, padding=0, dilation=1,
+                  method=None, stream=None):
+    """Gradients of ``attn`` for the cotangent grad_out [B, Ho, Wo, G, D]
+    (value's dtype, contiguous): returns (grad_value [B, H, W, G, D],
+    grad_offsets [B, Ho, Wo, G, K, 2], grad_weights [B, Ho, Wo, G, K]), all
+    float32.  Same argument rules as ``attn``."""
+    import torch
+    if method not in (None, "softmax"):
+        raise ValueError("method must be None or 'softmax'")
+    pair = lambda v: (int(v), int(v)) if isinstance(v, int) else (int(v[0]), int(v[1]))  # noqa: E731
+    (kh, kw), (sh, sw), (ph, pw), (dh, dw) = (pair(v) for v in (kernel_size, stride, padding, dilation))
+    for name, t in (("value", value), ("offsets", offsets), ("weights", weights),
+                    ("grad_out", grad_out)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if offsets.dtype != torch.float32 or weights.dtype != torch.float32:
+        raise TypeError("offsets and weights must be float32")
+    if grad_out.dtype != value.dtype:
+        raise TypeError("grad_out must have value's dtype")
+    B, H, W, G, D = value.shape
+    Ho = dcn_out_size(H, kh, sh, ph, dh)
+    Wo = dcn_out_size(W, kw, sw, pw, dw)
+    K = kh * kw
+    if tuple(offsets.shape) != (B, Ho, Wo, G, K, 2) or tuple(weights.shape) != (B, Ho, Wo, G, K):
+        raise ValueError("offsets must be [B, Ho, Wo, G, K, 2] and weights [B, Ho, Wo, G, K]")
+    if tuple(grad_out.shape) != (B, Ho, Wo, G, D):
+        raise ValueError("grad_out must be [B, Ho, Wo, G, D]")
+    dev = value.device
+    gv = torch.empty((B, H, W, G, D), dtype=torch.float32, device=dev)
+    go = torch.empty((B, Ho, Wo, G, K, 2), dtype=torch.float32, device=dev)
+    gw = torch.empty((B, Ho, Wo, G, K), dtype=torch.float32, device=dev)
+    dcn_attn_backward(value, offsets, weights, grad_out, gv, go, gw, B, H, W, G, D, kh, kw, sh, sw,
+                      ph, pw, dh, dw, method == "softmax", _dtype_code(value), stream)
+    return gv, go, gw
 
 
 def deform_conv2d_nchw(input, offset, weight, bias=None, stride=1, padding=0, dilation=1,

@@ -4,7 +4,7 @@ in the library's kernels."""
 
 import torch
 
-from . import deform_conv2d, deform_conv2d_backward, msda, msda_backward
+from . import attn, attn_backward, deform_conv2d, deform_conv2d_backward, msda, msda_backward
 
 
 class DeformConv2dFunction(torch.autograd.Function):
@@ -63,3 +63,32 @@ class MsdaFunction(torch.autograd.Function):
 def msda_autograd(value, shapes, starts, locations, weights, method=None):
     """msda that records the graph for torch.autograd."""
     return MsdaFunction.apply(value, locations, weights, shapes, starts, method)
+
+
+class AttnFunction(torch.autograd.Function):
+    """out = attn(value, offsets, weights, kernel_size, stride, padding,
+    dilation, method); gradients for value (in its dtype), offsets and
+    weights (float32)."""
+
+    @staticmethod
+    def forward(ctx, value, offsets, weights, kernel_size, stride=1, padding=0, dilation=1,
+                method=None):
+        out = attn(value, offsets, weights, kernel_size, stride, padding, dilation, method=method)
+        ctx.save_for_backward(value, offsets, weights)
+        ctx.meta = (kernel_size, stride, padding, dilation, method)
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        value, offsets, weights = ctx.saved_tensors
+        kernel_size, stride, padding, dilation, method = ctx.meta
+        gv, go, gw = attn_backward(grad_out.to(value.dtype).contiguous(), value, offsets, weights,
+                                   kernel_size, stride, padding, dilation, method=method)
+        return gv.to(value.dtype), go, gw, None, None, None, None, None
+
+
+def attn_autograd(value, offsets, weights, kernel_size, stride=1, padding=0, dilation=1,
+                  method=None):
+    """attn that records the graph for torch.autograd."""
+    return AttnFunction.apply(value, offsets, weights, kernel_size, stride, padding, dilation,
+                              method)

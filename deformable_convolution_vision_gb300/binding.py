@@ -24,7 +24,8 @@ EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_f
            "dcn_selftest_timeout", "dcn_status_string", "dcn_forward_noalloc",
            "dcn_set_sample_precision", "dcn_out_size", "dcn_forward_ex", "dcn_pack_weight_ex",
            "dcn_forward_packed_ex", "dcn_backward", "dcn_backward_ex", "dcn_msda_forward",
-           "dcn_msda_backward", "dcn_attn_forward", "dcn_nchw_to_nhwc", "dcn_nhwc_to_nchw"]
+           "dcn_msda_backward", "dcn_attn_forward", "dcn_attn_backward", "dcn_nchw_to_nhwc",
+           "dcn_nhwc_to_nchw"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -77,6 +78,7 @@ def load():
         "dcn_msda_forward": ([P, P, P, I, P, P, P] + [I] * 8 + [P], I),
         "dcn_msda_backward": ([P, P, P, I, P, P, P, P, P, P] + [I] * 8 + [P], I),
         "dcn_attn_forward": ([P, P, P, P] + [I] * 15 + [P], I),
+        "dcn_attn_backward": ([P] * 7 + [I] * 15 + [P], I),
         "dcn_nchw_to_nhwc": ([P, P] + [I] * 5 + [P], I),
         "dcn_nhwc_to_nchw": ([P, P] + [I] * 5 + [P], I),
     }
@@ -251,6 +253,16 @@ def dcn_attn_forward(value, offsets, weights, out, B, H, W, G, D, kh, kw, stride
                                    G, D, kh, kw, stride_h, stride_w, pad_h, pad_w, dil_h, dil_w,
                                    int(bool(softmax)), dtype, _stream(stream)),
            "dcn_attn_forward")
+
+
+def dcn_attn_backward(value, offsets, weights, grad_out, grad_value, grad_offsets, grad_weights,
+                      B, H, W, G, D, kh, kw, stride_h, stride_w, pad_h, pad_w, dil_h, dil_w,
+                      softmax, dtype, stream=None):
+    _check(load().dcn_attn_backward(_ptr(value), _ptr(offsets), _ptr(weights), _ptr(grad_out),
+                                    _ptr(grad_value), _ptr(grad_offsets), _ptr(grad_weights), B, H,
+                                    W, G, D, kh, kw, stride_h, stride_w, pad_h, pad_w, dil_h,
+                                    dil_w, int(bool(softmax)), dtype, _stream(stream)),
+           "dcn_attn_backward")
 
 
 def dcn_nchw_to_nhwc(src, dst, B, C, H, W, dtype, stream=None):

@@ -20,7 +20,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(HERE, "libdcn.so")
 
 SOURCES = ["dcn_api.cu", "dcn_simt.cu", "dcn_tc.cu", "dcn_noalloc.cu", "dcn_backward.cu",
-           "dcn_bwd_tc.cu", "dcn_msda.cu", "dcn_msda_bwd.cu", "dcn_attn.cu", "dcn_layout.cu"]
+           "dcn_bwd_tc.cu", "dcn_msda.cu", "dcn_msda_bwd.cu", "dcn_attn.cu", "dcn_attn_bwd.cu",
+           "dcn_layout.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -786,6 +786,50 @@ dcn_status_t dcn_attn_forward(const void *value, const float *offsets, const flo
     return DCN_OK;
 }
 
+dcn_status_t dcn_attn_backward(const void *value, const float *offsets, const float *weights,
+                               const void *grad_out, float *grad_value, float *grad_offsets,
+                               float *grad_weights, int B, int H, int W, int G, int D, int kh,
+                               int kw, int stride_h, int stride_w, int pad_h, int pad_w,
+                               int dil_h, int dil_w, int softmax, int dtype, void *stream) {
+    if (!value || !offsets || !weights || !grad_out || !grad_value || !grad_offsets ||
+        !grad_weights)
+        return DCN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || W <= 0 || G <= 0 || D <= 0 || kh <= 0 || kw <= 0 || stride_h <= 0 ||
+        stride_w <= 0 || pad_h < 0 || pad_w < 0 || dil_h <= 0 || dil_w <= 0)
+        return DCN_ERR_INVALID_ARG;
+    const long long Ho = out_size_ll(H, kh, stride_h, pad_h, dil_h);
+    const long long Wo = out_size_ll(W, kw, stride_w, pad_w, dil_w);
+    if (Ho <= 0 || Wo <= 0) return DCN_ERR_INVALID_ARG;
+    const long long K = static_cast<long long>(kh) * kw;
+    const long long GD = static_cast<long long>(G) * D;
+    if (K > kIndexLimit || static_cast<long long>(B) * H * W * GD > kIndexLimit ||
+        B * Ho * Wo * G * K * 2 > kIndexLimit || B * Ho * Wo * GD > kIndexLimit)
+        return DCN_ERR_INVALID_ARG;
+    const size_t es = esize(dtype);
+    if (!aligned(value, es) || !aligned(grad_out, es) || !aligned(offsets, 8) ||
+        !aligned(weights, 4) || !aligned(grad_value, 4) || !aligned(grad_offsets, 8) ||
+        !aligned(grad_weights, 4))
+        return DCN_ERR_INVALID_ARG;
+    dcn::AttnBwdParams p;
+    p.value = value; p.offsets = offsets; p.weights = weights; p.grad_out = grad_out;
+    p.grad_value = grad_value; p.grad_offsets = grad_offsets; p.grad_weights = grad_weights;
+    p.B = B; p.H = H; p.W = W; p.G = G; p.D = D;
+    p.Ho = static_cast<int>(Ho); p.Wo = static_cast<int>(Wo);
+    p.kh = kh; p.kw = kw; p.sh = stride_h; p.sw = stride_w; p.ph = pad_h; p.pw = pad_w;
+    p.dh = dil_h; p.dw = dil_w;
+    p.softmax = softmax ? 1 : 0;
+    cudaStream_t s = as_stream(stream);
+    // the value gradient is a sum of reductions: start it at zero
+    if (cudaMemsetAsync(grad_value, 0, static_cast<size_t>(B) * H * W * GD * sizeof(float), s) !=
+        cudaSuccess)
+        return DCN_ERR_CUDA;
+    const bool vec = D % (dtype == DCN_F32 ? 4 : 8) == 0 && aligned(value, 16) &&
+                     aligned(grad_out, 16) && aligned(grad_value, 16);
+    if (dcn::launch_attn_backward(p, dtype, vec, s) != cudaSuccess) return DCN_ERR_CUDA;
+    return DCN_OK;
+}
+
 static dcn_status_t layout_copy(const void *src, void *dst, int B, int R, int S, int dtype,
                                 void *stream) {
     if (!src || !dst || src == dst) return DCN_ERR_INVALID_ARG;

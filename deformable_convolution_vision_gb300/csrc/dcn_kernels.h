@@ -213,6 +213,23 @@ struct AttnParams {
 // vec: D a multiple of 8 (16-bit) or 4 (fp32) and value/out 16-byte aligned.
 cudaError_t launch_attn(const AttnParams &p, int dtype, bool vec, cudaStream_t stream);
 
+// Its backward: fp32 gradients; grad_value must be zero on entry.
+struct AttnBwdParams {
+    const void *value;        // [B, H, W, G, D], the operand dtype
+    const float *offsets;     // [B, Ho, Wo, G, K, 2]
+    const float *weights;     // [B, Ho, Wo, G, K]
+    const void *grad_out;     // [B, Ho, Wo, G, D], the operand dtype
+    float *grad_value;        // [B, H, W, G, D]
+    float *grad_offsets;      // [B, Ho, Wo, G, K, 2], 8-byte aligned
+    float *grad_weights;      // [B, Ho, Wo, G, K]
+    int B, H, W, G, D, Ho, Wo;
+    int kh, kw, sh, sw, ph, pw, dh, dw;
+    int softmax;
+};
+// vec: D a multiple of 8 (16-bit) or 4 (fp32); value, grad_out and
+// grad_value 16-byte aligned.
+cudaError_t launch_attn_backward(const AttnBwdParams &p, int dtype, bool vec, cudaStream_t stream);
+
 // Batched 2-D transpose [B][R][S] -> [B][S][R] of 2- or 4-byte elements.
 cudaError_t launch_transpose(const void *src, void *dst, int B, int R, int S, int esize,
                              cudaStream_t stream);

@@ -302,6 +302,14 @@ def make_attn_inputs(wl: AttnWorkload):
             "weights": weights.contiguous()}
 
 
+def make_attn_grad_out(wl: AttnWorkload):
+    """A cotangent for the backward: grad_out [B, Ho, Wo, G, D] ~ N(0, 1) in
+    the compute dtype, from its own seed (the workload's + 1000)."""
+    g = torch.Generator().manual_seed(wl.seed + 1000)
+    Ho, Wo = wl.out_size()
+    return torch.randn(wl.B, Ho, Wo, wl.G, wl.D, generator=g).to(TORCH_DTYPE[wl.dtype])
+
+
 ATTN_WORKLOADS = {
     w.name: w for w in [
         # the page's layer example: DeformSample2d(dim=64, kernel_size=3,

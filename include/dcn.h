@@ -457,6 +457,39 @@ DCN_API dcn_status_t dcn_attn_forward(const void *value, const float *offsets,
                               int pad_w, int dil_h, int dil_w, int softmax, int dtype,
                               void *stream);
 
+/* The backward of dcn_attn_forward: for the cotangent grad_out [B, Ho, Wo,
+ * G, D] (`dtype`, like value), the gradients with respect to value,
+ * offsets and weights, all fp32.  The chain rule applied to the definition
+ * above; with go = grad_out[b,ho,wo,g,:], per tap k and inside corner c of
+ * its sample, bilinear weights wy, wx:
+ *
+ *   grad_value[c]    += a[k] wy wx go
+ *   grad_a[k]         = sum_c wy wx <go, v_c>
+ *   grad_offsets[k]   = a[k] (sum_c sy wx <go, v_c>, sum_c wy sx <go, v_c>)   (dy, dx)
+ *   grad_weights[k]   = grad_a[k], or with softmax
+ *                       a[k] (grad_a[k] - sum_s a[s] grad_a[s])
+ *
+ * sx, sy = -1 for the left/top corner and +1 for the right/bottom one: at
+ * an integer coordinate the derivative of the cell floor() picks; a tap
+ * whose corners are all outside has zero gradients.  The value gradient is
+ * accumulated by fp32 reductions with no intermediate buffer (the page's
+ * float32-accumulator rule, which it gives single-scale sampling and MSDA
+ * alike), so its last bits depend on the order of the additions.
+ *
+ * Layouts (device pointers, dense, channels-last): value, offsets, weights
+ * as dcn_attn_forward; grad_out [B, Ho, Wo, G, D] `dtype`; grad_value
+ * [B, H, W, G, D] fp32, overwritten (zeroed first, then accumulated);
+ * grad_offsets [B, Ho, Wo, G, K, 2] fp32, 8-byte aligned, overwritten;
+ * grad_weights [B, Ho, Wo, G, K] fp32, overwritten.  Every pointer is
+ * required.  Arithmetic in fp32.  Errors as dcn_attn_forward.
+ * Asynchronous on `stream`; allocates nothing; no handle. */
+DCN_API dcn_status_t dcn_attn_backward(const void *value, const float *offsets,
+                               const float *weights, const void *grad_out, float *grad_value,
+                               float *grad_offsets, float *grad_weights, int B, int H, int W,
+                               int G, int D, int kh, int kw, int stride_h, int stride_w,
+                               int pad_h, int pad_w, int dil_h, int dil_w, int softmax,
+                               int dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -91,6 +91,8 @@ def test_python_wrappers_marshal_every_argument(lib):
                                           1, 64, 8, 32, 10, 4, True, 1, 0),
         lambda: binding.dcn_attn_forward(None, None, None, None, 1, 8, 8, 4, 16, 3, 3, 1, 1, 1, 1,
                                          1, 1, True, 1, 0),
+        lambda: binding.dcn_attn_backward(None, None, None, None, None, None, None, 1, 8, 8, 4, 16,
+                                          3, 3, 1, 1, 1, 1, 1, 1, True, 1, 0),
         lambda: binding.dcn_nchw_to_nhwc(None, None, 1, 64, 8, 8, 1, 0),
         lambda: binding.dcn_nhwc_to_nchw(None, None, 1, 64, 8, 8, 1, 0),
     ]
