@@ -15,6 +15,7 @@
 
 #include "dcn.h"
 #include "dcn_kernels.h"
+#include "dcn_sampling_ops.h"
 
 struct dcn_handle_s {
     int device = 0;

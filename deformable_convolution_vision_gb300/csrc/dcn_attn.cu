@@ -29,7 +29,7 @@
 
 #include <cstring>
 
-#include "dcn_kernels.h"
+#include "dcn_sampling_ops.h"
 
 namespace dcn {
 

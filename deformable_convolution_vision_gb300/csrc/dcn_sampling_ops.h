@@ -1,0 +1,75 @@
+// Declarations of the CUDA-core sampling operators that share the
+// deformable convolution's bilinear sampler: multi-scale deformable
+// attention and single-scale deformable sampling, forward and backward.
+// Kept apart from dcn_kernels.h (the convolution's kernels) so that the two
+// families build from separate declarations.
+#pragma once
+
+#include "dcn_kernels.h"
+
+namespace dcn {
+
+// Multi-scale deformable attention forward (device pointers; the level
+// table by value).
+constexpr int kMsdaMaxLevels = 8;
+struct MsdaParams {
+    const void *value;        // [B, S, G, D], the operand dtype
+    const float *locations;   // [B, Q, G, L, K, 2], normalized (x, y)
+    const float *weights;     // [B, Q, G, L*K]
+    void *out;                // [B, Q, G, D], the operand dtype
+    int B, S, G, D, Q, K, L;
+    int softmax;              // 1: normalize the weights over L*K
+    int H[kMsdaMaxLevels], W[kMsdaMaxLevels], start[kMsdaMaxLevels];
+};
+// vec: D a multiple of 8 (16-bit) or 4 (fp32) and value/out 16-byte aligned.
+cudaError_t launch_msda(const MsdaParams &p, int dtype, bool vec, cudaStream_t stream);
+
+// MSDA backward: the forward's operands plus the cotangent, fp32 gradients.
+// grad_value must be zero on entry (the kernel accumulates into it).
+struct MsdaBwdParams {
+    const void *value;        // [B, S, G, D], the operand dtype
+    const float *locations;   // [B, Q, G, L, K, 2]
+    const float *weights;     // [B, Q, G, L*K]
+    const void *grad_out;     // [B, Q, G, D], the operand dtype
+    float *grad_value;        // [B, S, G, D]
+    float *grad_locations;    // [B, Q, G, L, K, 2]
+    float *grad_weights;      // [B, Q, G, L*K]
+    int B, S, G, D, Q, K, L;
+    int softmax;
+    int H[kMsdaMaxLevels], W[kMsdaMaxLevels], start[kMsdaMaxLevels];
+};
+// vec: D a multiple of 8 (16-bit) or 4 (fp32); value, grad_out and
+// grad_value 16-byte aligned.
+cudaError_t launch_msda_backward(const MsdaBwdParams &p, int dtype, bool vec, cudaStream_t stream);
+
+// Single-scale deformable sampling (DCNv3), forward.
+struct AttnParams {
+    const void *value;        // [B, H, W, G, D], the operand dtype
+    const float *offsets;     // [B, Ho, Wo, G, K, 2], (dy, dx), 8-byte aligned
+    const float *weights;     // [B, Ho, Wo, G, K]
+    void *out;                // [B, Ho, Wo, G, D], the operand dtype
+    int B, H, W, G, D, Ho, Wo;
+    int kh, kw, sh, sw, ph, pw, dh, dw;
+    int softmax;              // 1: normalize the weights over the K taps
+};
+// vec: D a multiple of 8 (16-bit) or 4 (fp32) and value/out 16-byte aligned.
+cudaError_t launch_attn(const AttnParams &p, int dtype, bool vec, cudaStream_t stream);
+
+// Its backward: fp32 gradients; grad_value must be zero on entry.
+struct AttnBwdParams {
+    const void *value;        // [B, H, W, G, D], the operand dtype
+    const float *offsets;     // [B, Ho, Wo, G, K, 2]
+    const float *weights;     // [B, Ho, Wo, G, K]
+    const void *grad_out;     // [B, Ho, Wo, G, D], the operand dtype
+    float *grad_value;        // [B, H, W, G, D]
+    float *grad_offsets;      // [B, Ho, Wo, G, K, 2], 8-byte aligned
+    float *grad_weights;      // [B, Ho, Wo, G, K]
+    int B, H, W, G, D, Ho, Wo;
+    int kh, kw, sh, sw, ph, pw, dh, dw;
+    int softmax;
+};
+// vec: D a multiple of 8 (16-bit) or 4 (fp32); value, grad_out and
+// grad_value 16-byte aligned.
+cudaError_t launch_attn_backward(const AttnBwdParams &p, int dtype, bool vec, cudaStream_t stream);
+
+}  // namespace dcn
