@@ -16,7 +16,7 @@ DCN_F32, DCN_BF16, DCN_F16 = 0, 1, 2
 DCN_PATH_AUTO, DCN_PATH_SIMT, DCN_PATH_TC = 0, 1, 2
 DCN_SAMPLE_INPUT_DTYPE, DCN_SAMPLE_F32 = 0, 1
 STATUS = {0: "DCN_OK", 1: "DCN_ERR_INVALID_ARG", 2: "DCN_ERR_UNSUPPORTED", 3: "DCN_ERR_CUDA",
-          4: "DCN_ERR_NO_DEVICE", 5: "DCN_ERR_OOM", 6: "DCN_ERR_TIMEOUT"}
+          4: "DCN_ERR_NO_DEVICE", 5: "DCN_ERR_OOM", 6: "DCN_ERR_TIMEOUT", 7: "DCN_ERR_BOUNDS"}
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 EXPORTS = ["dcn_create", "dcn_destroy", "dcn_forward", "dcn_pack_weight", "dcn_forward_packed",

@@ -14,6 +14,7 @@
 #include <new>
 
 #include "dcn.h"
+#include "dcn_device.cuh"
 #include "dcn_kernels.h"
 #include "dcn_sampling_ops.h"
 
@@ -190,6 +191,7 @@ dcn_status_t next_epoch(dcn_handle_t h, cudaStream_t s, unsigned *epoch) {
     return DCN_OK;
 }
 
+
 // A band of output rows [h0, h0 + rows) of a one-image problem; the
 // offset, mask and out pointers then address the band's first row, and
 // offset/mask planes stay `plane` elements apart (the whole image's).
@@ -237,6 +239,9 @@ dcn_status_t forward_packed_impl(dcn_handle_t h, const void *x, const float *off
     p.mask_bstride = taps * d.offset_groups;
     p.status = h->status;
     p.timeout_ns = kWaitLimitNs;
+#ifdef DCN_CHECK_BOUNDS
+    dcn::set_bounds(p, esize(dtype));
+#endif
     p.sample_f32 = h->sample == DCN_SAMPLE_F32 ? 1 : 0;
     p.f16 = dtype == DCN_F16 ? 1 : 0;
     p.partial = nullptr;
@@ -873,7 +878,7 @@ dcn_status_t dcn_sync_status(dcn_handle_t h, void *stream) {
     if (word != 0) {
         if (cudaMemsetAsync(h->status, 0, sizeof(unsigned), s) != cudaSuccess) return DCN_ERR_CUDA;
         if (cudaStreamSynchronize(s) != cudaSuccess) return DCN_ERR_CUDA;
-        return DCN_ERR_TIMEOUT;
+        return (word & dcn::kStatusBounds) ? DCN_ERR_BOUNDS : DCN_ERR_TIMEOUT;
     }
     return DCN_OK;
 }
@@ -1011,6 +1016,7 @@ const char *dcn_status_string(dcn_status_t s) {
         case DCN_ERR_NO_DEVICE: return "DCN_ERR_NO_DEVICE";
         case DCN_ERR_OOM: return "DCN_ERR_OOM";
         case DCN_ERR_TIMEOUT: return "DCN_ERR_TIMEOUT";
+        case DCN_ERR_BOUNDS: return "DCN_ERR_BOUNDS";
     }
     return "DCN_ERR_UNKNOWN";
 }

@@ -11,6 +11,21 @@ namespace dcn {
 
 // Bits of the handle's device status word.
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBounds = 2u;   // bounds-checked builds only
+
+#ifdef DCN_CHECK_BOUNDS
+// Bounds-checked builds (compiled with DCN_CHECK_BOUNDS): whether the bytes
+// [p, p + bytes) lie inside [lo, hi).  An access outside sets kStatusBounds
+// in *status and the caller skips it (or reads a safe address instead);
+// nothing traps.
+__device__ __forceinline__ bool in_bounds(const void *p, size_t bytes, const void *lo,
+                                          const void *hi, unsigned *status) {
+    const char *c = static_cast<const char *>(p);
+    const bool ok = c >= static_cast<const char *>(lo) && c + bytes <= static_cast<const char *>(hi);
+    if (!ok) atomicOr(status, kStatusBounds);
+    return ok;
+}
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -44,6 +44,10 @@ struct Params {
     int off_bstride, mask_bstride;
     unsigned *status;     // device status word (timeout bit)
     unsigned long long timeout_ns;  // bound of every barrier wait
+#ifdef DCN_CHECK_BOUNDS
+    // bounds-checked builds: the byte ranges of the caller's tensors
+    const void *x_lo, *x_hi, *off_lo, *off_hi, *mask_lo, *mask_hi, *out_lo, *out_hi;
+#endif
     int sample_f32;       // tensor-core path: 1 = fp32 bilinear combine, 0 = operand type
     int f16;              // tensor-core path: 1 = fp16 operands, 0 = bf16
     // tensor-core path, stream-K scheduling (partial == nullptr: one tile per CTA)
@@ -74,6 +78,25 @@ enum Dtype { kF32 = 0, kBF16 = 1, kF16 = 2 };
 // >= Cg (the padding of a tap's last 64-channel block).
 cudaError_t launch_pack_weight(const void *weight, void *wpack, int O, int Cg, int kh, int kw,
                                int dtype, int perm, cudaStream_t stream);
+#ifdef DCN_CHECK_BOUNDS
+// Bounds-checked builds: the byte ranges of the tensors a forward launch
+// reads and writes, from its (possibly banded) view.
+inline void set_bounds(Params &p, size_t es) {
+    const char *x = static_cast<const char *>(p.x);
+    p.x_lo = x;
+    p.x_hi = x + static_cast<size_t>(p.B) * p.H * p.W * p.x_cstride * es;
+    const size_t img = static_cast<size_t>(p.Ho) * p.Wo;   // one plane's pixels in this view
+    const size_t plane = static_cast<size_t>(p.plane);
+    p.off_lo = p.offset;
+    p.off_hi = p.offset + (static_cast<size_t>(p.B) * p.off_bstride - 1) * plane + img;
+    p.mask_lo = p.mask;
+    p.mask_hi = p.mask ? p.mask + (static_cast<size_t>(p.B) * p.mask_bstride - 1) * plane + img : nullptr;
+    char *out = static_cast<char *>(p.out);
+    p.out_lo = out;
+    p.out_hi = out + static_cast<size_t>(p.B) * img * p.out_stride * es;
+}
+#endif
+
 // Packed positions per tap for a pack of Cg channels.
 __host__ __device__ inline int pack_kc(int Cg, int perm) { return perm ? (Cg + 63) / 64 * 64 : Cg; }
 

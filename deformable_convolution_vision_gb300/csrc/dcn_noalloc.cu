@@ -138,6 +138,9 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     p.mask_bstride = kh * kw;
     p.status = s->status;
     p.timeout_ns = kWaitLimitNs;
+#ifdef DCN_CHECK_BOUNDS
+    dcn::set_bounds(p, es);
+#endif
     p.sample_f32 = 0;
     p.f16 = dtype == DCN_F16 ? 1 : 0;
     p.partial = nullptr;   // no stream-K workspace: one tile per CTA

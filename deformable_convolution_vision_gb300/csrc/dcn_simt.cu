@@ -13,6 +13,15 @@
 
 #include "dcn_kernels.h"
 #include "dcn_sampling.cuh"
+#ifdef DCN_CHECK_BOUNDS
+#include "dcn_device.cuh"
+// bounds-checked builds: a read outside its tensor gives 0 and sets the
+// status bit; a store outside is skipped
+#define DCN_READ(ptr, i, lo, hi) \
+    (in_bounds((ptr) + (i), sizeof(*(ptr)), (lo), (hi), p.status) ? (ptr)[i] : decltype(+(ptr)[i])(0))
+#else
+#define DCN_READ(ptr, i, lo, hi) ((ptr)[i])
+#endif
 
 namespace dcn {
 
@@ -119,9 +128,9 @@ dcn_simt_kernel(Params p) {
                     const size_t bq = static_cast<size_t>(my_b) * p.ogroups + q;
                     const size_t plane = static_cast<size_t>(p.plane);
                     const size_t ob = bq * 2 * taps * plane + hw;
-                    const float dy = p.offset[ob + static_cast<size_t>(2 * tap) * plane];
-                    const float dx = p.offset[ob + static_cast<size_t>(2 * tap + 1) * plane];
-                    const float m = p.mask ? p.mask[(bq * taps + tap) * plane + hw] : 1.0f;
+                    const float dy = DCN_READ(p.offset, ob + static_cast<size_t>(2 * tap) * plane, p.off_lo, p.off_hi);
+                    const float dx = DCN_READ(p.offset, ob + static_cast<size_t>(2 * tap + 1) * plane, p.off_lo, p.off_hi);
+                    const float m = p.mask ? DCN_READ(p.mask, (bq * taps + tap) * plane + hw, p.mask_lo, p.mask_hi) : 1.0f;
                     tap_corners(dy, dx, m, (p.h0 + my_h) * p.sh - p.ph + i * p.dh, my_w * p.sw - p.pw + j * p.dw,
                                 my_b, p.H, p.W, p.x_cstride, t);
                 } else {
@@ -146,10 +155,10 @@ dcn_simt_kernel(Params p) {
                     if (c < cq_hi) {
                         const float4 cw = cw_s[pp];
                         const int4 ci = ci_s[pp];
-                        if (cw.x != 0.0f) v += cw.x * to_f32<T>(x[ci.x + c]);
-                        if (cw.y != 0.0f) v += cw.y * to_f32<T>(x[ci.y + c]);
-                        if (cw.z != 0.0f) v += cw.z * to_f32<T>(x[ci.z + c]);
-                        if (cw.w != 0.0f) v += cw.w * to_f32<T>(x[ci.w + c]);
+                        if (cw.x != 0.0f) v += cw.x * to_f32<T>(DCN_READ(x, ci.x + c, p.x_lo, p.x_hi));
+                        if (cw.y != 0.0f) v += cw.y * to_f32<T>(DCN_READ(x, ci.y + c, p.x_lo, p.x_hi));
+                        if (cw.z != 0.0f) v += cw.z * to_f32<T>(DCN_READ(x, ci.z + c, p.x_lo, p.x_hi));
+                        if (cw.w != 0.0f) v += cw.w * to_f32<T>(DCN_READ(x, ci.w + c, p.x_lo, p.x_hi));
                     }
                     As[kk][pp] = v;
                 }
@@ -201,7 +210,11 @@ dcn_simt_kernel(Params p) {
             const int o = o0 + tx * 4 + s;
             if (o >= p.O) continue;
             const float bv = p.bias ? p.bias[o] : 0.0f;
-            out[static_cast<size_t>(pix) * p.out_stride + o] = from_f32<T>(acc[r][s] + bv);
+            T *dst = out + static_cast<size_t>(pix) * p.out_stride + o;
+#ifdef DCN_CHECK_BOUNDS
+            if (!in_bounds(dst, sizeof(T), p.out_lo, p.out_hi, p.status)) continue;
+#endif
+            *dst = from_f32<T>(acc[r][s] + bv);
         }
     }
 }

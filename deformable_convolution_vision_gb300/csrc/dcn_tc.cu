@@ -410,8 +410,13 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                                 pk[e] = E::pack(vv[2 * e] + b0, vv[2 * e + 1] + b1);
                             }
                             uint4 *dst = reinterpret_cast<uint4 *>(out + pix * p.out_stride + ch * 16);
-                            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#ifdef DCN_CHECK_BOUNDS
+                            if (in_bounds(dst, 32, p.out_lo, p.out_hi, p.status))
+#endif
+                            {
+                                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                            }
                         }
                     }
                 }
@@ -463,13 +468,26 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     const float *o = valid
                         ? p.offset + (static_cast<size_t>(tb) * p.off_bstride + 2 * mc) * plane + my_hw
                         : p.offset;
+#ifdef DCN_CHECK_BOUNDS
+                    // an offset or mask outside its tensor is not fetched (zero)
+                    const bool v_dy = valid && in_bounds(o, 4, p.off_lo, p.off_hi, p.status);
+                    const bool v_dx = valid && in_bounds(o + plane, 4, p.off_lo, p.off_hi, p.status);
+                    cp_async_4(raw_s, v_dy ? o : p.offset, v_dy);
+                    cp_async_4(raw_s + 128, v_dx ? o + plane : o, v_dx);
+#else
                     cp_async_4(raw_s, o, valid);
                     cp_async_4(raw_s + 128, valid ? o + plane : o, valid);
+#endif
                     if (p.mask) {
                         const float *mp = valid
                             ? p.mask + (static_cast<size_t>(tb) * p.mask_bstride + mc) * plane + my_hw
                             : p.mask;
+#ifdef DCN_CHECK_BOUNDS
+                        const bool v_m = valid && in_bounds(mp, 4, p.mask_lo, p.mask_hi, p.status);
+                        cp_async_4(raw_s + 256, v_m ? mp : p.mask, v_m);
+#else
                         cp_async_4(raw_s + 256, mp, valid);
+#endif
                     }
                 };
                 // corner tables of the group's two virtual taps (ring slot sq % 4)
@@ -512,10 +530,22 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 auto issue_px = [&](int px, uint32_t slot, int cofs, u32x8 (&v)[8]) {
                     const uint16_t *xc = x + min(cofs + quart * 16, chan_last);
                     const int4 ci = lds_v4_s32(slot + kIdx + (px ? r_off1 : r_off0));
+#ifdef DCN_CHECK_BOUNDS
+                    // a corner row outside x is read from x's first bytes instead
+                    auto chk = [&](const uint16_t *a) {
+                        return in_bounds(a, 32, p.x_lo, p.x_hi, p.status)
+                                   ? a : static_cast<const uint16_t *>(p.x_lo);
+                    };
+                    v[4 * px + 0] = ldg_v8(chk(xc + ci.x));
+                    v[4 * px + 1] = ldg_v8(chk(xc + ci.y));
+                    v[4 * px + 2] = ldg_v8(chk(xc + ci.z));
+                    v[4 * px + 3] = ldg_v8(chk(xc + ci.w));
+#else
                     v[4 * px + 0] = ldg_v8(xc + ci.x);
                     v[4 * px + 1] = ldg_v8(xc + ci.y);
                     v[4 * px + 2] = ldg_v8(xc + ci.z);
                     v[4 * px + 3] = ldg_v8(xc + ci.w);
+#endif
                 };
 
                 // Tables of the first two groups.  (The group after a group

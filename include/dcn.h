@@ -77,7 +77,10 @@ typedef enum {
     DCN_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     DCN_ERR_NO_DEVICE = 4,    /* no CUDA device is visible */
     DCN_ERR_OOM = 5,          /* workspace allocation failed */
-    DCN_ERR_TIMEOUT = 6       /* a device-side bounded wait ran out (reported by dcn_sync_status) */
+    DCN_ERR_TIMEOUT = 6,      /* a device-side bounded wait ran out (reported by dcn_sync_status) */
+    DCN_ERR_BOUNDS = 7        /* a bounds-checked build (compiled with DCN_CHECK_BOUNDS) skipped a
+                                 forward read or write outside the caller's tensors (reported by
+                                 dcn_sync_status); the ordinary build never reports it */
 } dcn_status_t;
 
 /* Kernel selection for bf16 and fp16.  AUTO takes the tcgen05 path when
@@ -167,7 +170,10 @@ DCN_API int dcn_last_path(dcn_handle_t h);
 
 /* Synchronise `stream` and report the handle's device status word:
  * DCN_OK, DCN_ERR_TIMEOUT if a kernel's bounded wait ran out (the word is
- * cleared after it is read), or DCN_ERR_CUDA if the synchronisation failed. */
+ * cleared after it is read), DCN_ERR_BOUNDS if a bounds-checked build
+ * skipped an access outside the caller's tensors (this takes precedence;
+ * the word is cleared likewise), or DCN_ERR_CUDA if the synchronisation
+ * failed. */
 DCN_API dcn_status_t dcn_sync_status(dcn_handle_t h, void *stream);
 
 /* Launch a one-thread kernel that waits on a barrier nothing arrives on,
