@@ -58,6 +58,7 @@ struct dcn_handle_s {
 
     // device staging for dcn_forward_host: x, offset, mask, weight, bias, out
     void *stage[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    unsigned *host_status = nullptr;   // pinned copy of the status word (host-buffer entry)
     size_t stage_cap[6] = {0, 0, 0, 0, 0, 0};
 
     PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;
@@ -405,6 +406,7 @@ dcn_status_t dcn_destroy(dcn_handle_t h) {
     if (h->status) cudaFree(h->status);
     for (int i = 0; i < 6; ++i)
         if (h->stage[i]) cudaFree(h->stage[i]);
+    if (h->host_status) cudaFreeHost(h->host_status);
     if (h->s_kernel) cudaStreamDestroy(h->s_kernel);
     if (h->s_down) cudaStreamDestroy(h->s_down);
     cudaEvent_t evs[3] = {h->ev_in, h->ev_k, h->ev_done};
@@ -916,7 +918,9 @@ dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset
             cudaStreamCreateWithFlags(&h->s_down, cudaStreamNonBlocking) != cudaSuccess ||
             cudaEventCreateWithFlags(&h->ev_in, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&h->ev_k, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) != cudaSuccess)
+            cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) != cudaSuccess ||
+            cudaHostAlloc(reinterpret_cast<void **>(&h->host_status), sizeof(unsigned),
+                          cudaHostAllocDefault) != cudaSuccess)
             return DCN_ERR_CUDA;
     }
     // The host link is the slow part (the copies take longer than the
@@ -982,7 +986,14 @@ dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset
     if (cudaEventRecord(h->ev_done, h->s_down) != cudaSuccess ||
         cudaStreamWaitEvent(s, h->ev_done, 0) != cudaSuccess)
         return DCN_ERR_CUDA;
-    return dcn_sync_status(h, stream);
+    // the status word comes back behind the last download: one
+    // synchronisation for both (the word is cleared only when it is set)
+    if (cudaMemcpyAsync(h->host_status, h->status, sizeof(unsigned), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return DCN_ERR_CUDA;
+    if (*h->host_status != 0) return dcn_sync_status(h, stream);
+    return DCN_OK;
 }
 
 dcn_status_t dcn_set_path(dcn_handle_t h, int path) {
