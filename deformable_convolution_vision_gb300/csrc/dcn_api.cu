@@ -67,9 +67,15 @@ struct dcn_handle_s {
 namespace {
 
 // Bands of output rows per dcn_forward_host call (whole images when there
-// are at least this many): measured on the 7x7 workload, 2, 3, 4, 6 and 8
-// bands took 371, 359, 352, 373 and 428 us per call.
-constexpr int kHostBands = 4;
+// are at least this many), the last one a quarter of the image: measured on
+// the 7x7 workload, three bands of 96, 96 and 64 rows took 334 us per call,
+// four of 64 rows 343 us, four of 80, 80, 64 and 32 rows 346 us and five
+// bands 356-359 us (earlier, with uniform bands: 2, 3, 4, 6 and 8 bands
+// 371, 359, 352, 373 and 428 us).  A band's kernel takes about as long
+// whatever its height (each tile runs all its taps in sequence), so more
+// bands cost more than the shorter tail after the last upload saves.
+constexpr int kHostBands = 3;
+constexpr int kHostLastDiv = 4;
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
 constexpr long long kIndexLimit = (1ll << 31) - 1;
@@ -942,6 +948,14 @@ dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset
     int rows = static_cast<int>((Ho + per_image - 1) / per_image);
     rows = (rows + 7) & ~7;   // whole 8-row tiles
     if (rows < 8) rows = 8;
+    int last_rows = 0;        // 0: every band `rows` tall
+    if (per_image > 1) {
+        last_rows = ((static_cast<int>(Ho) / kHostLastDiv) + 7) & ~7;
+        if (last_rows < 8) last_rows = 8;
+        const int rest = static_cast<int>(Ho) - last_rows;
+        rows = ((rest + per_image - 2) / (per_image - 1) + 7) & ~7;
+        if (rows < 8) rows = 8;
+    }
     Conv c1 = c;
     c1.d.B = 1;
     const size_t img_x = static_cast<size_t>(H) * W * C * es;
@@ -954,8 +968,11 @@ dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset
     for (int b = 0; b < B; ++b) {
         if (cudaMemcpyAsync(sx + b * img_x, hx + b * img_x, img_x, cudaMemcpyHostToDevice, s) != cudaSuccess)
             return DCN_ERR_CUDA;
-        for (int h0 = 0; h0 < static_cast<int>(Ho); h0 += rows) {
-            const int r = static_cast<int>(Ho) - h0 < rows ? static_cast<int>(Ho) - h0 : rows;
+        for (int h0 = 0; h0 < static_cast<int>(Ho);) {
+            int r = static_cast<int>(Ho) - h0 < rows ? static_cast<int>(Ho) - h0 : rows;
+            // the last band (at most last_rows) ends the call sooner
+            if (last_rows > 0 && static_cast<int>(Ho) - h0 - r < last_rows && static_cast<int>(Ho) - h0 > last_rows)
+                r = static_cast<int>(Ho) - h0 - last_rows;
             // this band's rows of every offset and mask plane of image b
             const size_t first = static_cast<size_t>(h0) * Wo;
             const size_t off0 = static_cast<size_t>(b) * 2 * taps * plane + first;
@@ -981,6 +998,7 @@ dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset
             if (cudaMemcpyAsync(static_cast<uint8_t *>(out) + out0, sout + out0, r * Wo * O * es,
                                 cudaMemcpyDeviceToHost, h->s_down) != cudaSuccess)
                 return DCN_ERR_CUDA;
+            h0 += r;
         }
     }
     if (cudaEventRecord(h->ev_done, h->s_down) != cudaSuccess ||

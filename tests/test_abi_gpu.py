@@ -140,9 +140,9 @@ def _host_call(handle, wl, inp, code):
 
 
 @pytest.mark.parametrize("wl", [
-    # four bands of 64 rows (the benchmark's end-to-end call)
+    # three bands of 96, 96 and 64 rows (the benchmark's end-to-end call)
     WORKLOADS["aspp7x7"],
-    # two images, two bands each, the last one ragged (Ho = 43)
+    # two images, two bands each, both ragged (27 and 16 rows of Ho = 43)
     WORKLOADS["decoder3x3"].with_(B=2, H=43, W=50, seed=81),
     # five images: one band per image; no mask, no bias
     WORKLOADS["decoder3x3"].with_(B=5, H=20, W=24, mask="none", bias_std=0.0, seed=82),
