@@ -7,9 +7,10 @@
   as nothing reaches the subnormal range: so bf16 and fp32, whose exponent
   range is fp32's, and not fp16, whose small corner-weight products would.
 - Batch splitting: a batch gives the same output as its images one by
-  one.  With every tile computed by one CTA (fewer tiles than SMs) the
-  order of every sum is the same, so the bits are equal; when the
-  persistent schedule splits tiles between CTAs at other places, the
+  one.  With every tile computed by one CTA (no more (tile, K-block)
+  units than SMs, so no split schedule) the order of every sum is the
+  same, so the bits are equal; when the persistent schedule splits tiles
+  between CTAs at other places, the
   partial sums meet in another order: the fp32 sum moves by a few units
   of fp32 roundoff of the sum of its terms' magnitudes, which the output
   rounding can turn into one unit in the last place of the output type,
@@ -48,8 +49,9 @@ def test_mask_linearity_is_exact(path, dtype):
 
 
 @pytest.mark.parametrize("wl", [
-    # 3 x 4 x 4 = 48 tiles: one CTA per tile, the same sums in the same order
-    Workload("inv_batch_small", 3, 64, 30, 60, 64, 3, 3, 1, "bf16", 2.0, "sigmoid", 0.0, 0.1, 131),
+    # 3 x 2 x 2 = 12 tiles x 9 K-blocks: one CTA per tile, the same sums in
+    # the same order
+    Workload("inv_batch_small", 3, 64, 16, 30, 64, 3, 3, 1, "bf16", 2.0, "sigmoid", 0.0, 0.1, 131),
     # 2 x 16 x 10 = 320 tiles: the persistent schedule splits tiles
     Workload("inv_batch_streamk", 2, 128, 128, 160, 32, 5, 5, 2, "bf16", 3.0, "sigmoid", 0.0, 0.1, 132),
 ], ids=lambda w: w.name)
@@ -65,7 +67,8 @@ def test_batch_split(wl):
         parts.append(_forward(db, wl.with_(B=1), DCN_PATH_TC, bias=d["bias"]))
     split = torch.cat(parts, 0)
     tiles = wl.B * ((wl.Ho + 7) // 8) * ((wl.Wo + 15) // 16)
-    if tiles <= torch.cuda.get_device_properties(0).multi_processor_count:
+    units = tiles * wl.taps * ((wl.C + 63) // 64)
+    if units <= torch.cuda.get_device_properties(0).multi_processor_count:
         assert torch.equal(whole, split)
     else:
         a, b = whole.float(), split.float()
