@@ -1,8 +1,11 @@
 /*
- * dcn.h -- C ABI of the GB300 (sm_103a) modulated deformable convolution
- * forward pass.
+ * dcn.h -- C ABI of the GB300 (sm_103a) deformable sampling library: the
+ * modulated deformable convolution forward pass (below; its general form,
+ * dcn_forward_ex, further down), its backward, multi-scale deformable
+ * attention and single-scale deformable sampling (forward and backward),
+ * and NCHW/NHWC layout copies.  Each function states its own operation.
  *
- * The operation (page "litert-community/Idol ... deform_conv.py", module
+ * The convolution (page "litert-community/Idol ... deform_conv.py", module
  * docstring and the four-corner loop of deform_conv2d_gather; page
  * "deformops 3.0.1", section "Deformable convolution"): torchvision
  * deform_conv2d with stride 1, dilation 1, one offset group and one weight
