@@ -170,3 +170,18 @@ def test_host_entry_point_bands(handle, wl):
     # a second call on the same handle (streams and events reused) agrees
     again = _host_call(handle, wl, inp, code)
     assert torch.equal(out, again)
+
+
+def test_host_entry_point_pageable_memory(handle):
+    """dcn_forward_host with pageable (not pinned) host buffers: slower,
+    the same result as with pinned ones."""
+    wl = WORKLOADS["decoder3x3"].with_(H=40, W=48, seed=85)
+    inp = make_inputs(wl)
+    pinned = _host_call(handle, wl, inp, dcn.DCN_BF16)
+    x = inp["x"].permute(0, 2, 3, 1).contiguous()
+    out = torch.empty((wl.B, wl.Ho, wl.Wo, wl.O), dtype=x.dtype)
+    dcn.dcn_forward_host(handle.h, x, inp["offset"].contiguous(), inp["mask"].contiguous(),
+                         inp["weight"].contiguous(), inp["bias"].contiguous(), out, wl.B, wl.C,
+                         wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad, dcn.DCN_BF16)
+    assert dcn.dcn_sync_status(handle.h) == 0
+    assert torch.equal(out.permute(0, 3, 1, 2), pinned)
