@@ -686,11 +686,15 @@ int carveout_percent(int needed) {
 }
 
 // Shared memory the CTA may use (weight stages + tables + alignment + the
-// 1 KB the system reserves).  The SM's L1/shared array is 256 KB; within
-// 100 KB the carveout leaves 156 KB of L1 for the corner gathers.  Wide
-// weights (large O) may take up to the second budget to keep four stages.
+// 1 KB the system reserves).  The SM's L1/shared array is 256 KB.  With
+// O = 64 a 140 KB budget gives eight stages (107 KB; the carveout then
+// leaves 124 KB of L1 for the corner gathers): measured against six stages
+// in 100 KB (156 KB of L1), the 7x7 workload 114.7 -> 112.6 us and the
+// boundary 5x5 157.7 -> 151.6 us; ten stages in the same L1 and twelve
+// with 92 KB of L1 were no better.  Wide weights (large O) may take up to
+// the second budget to keep four stages.
 #ifndef DCN_TC_SMEM_BUDGET
-#define DCN_TC_SMEM_BUDGET (100 * 1024)
+#define DCN_TC_SMEM_BUDGET (140 * 1024)
 #endif
 #ifndef DCN_TC_SMEM_WIDE_BUDGET
 #define DCN_TC_SMEM_WIDE_BUDGET (164 * 1024)
