@@ -29,65 +29,18 @@
 
 #include <cstring>
 
+#include "dcn_rowload.cuh"
 #include "dcn_sampling_ops.h"
 
 namespace dcn {
 
 namespace {
 
-template <typename T, int CH>
-__device__ __forceinline__ void attn_load(const T *p, float (&v)[CH]);
-
-template <>
-__device__ __forceinline__ void attn_load<float, 4>(const float *p, float (&v)[4]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-}
-template <>
-__device__ __forceinline__ void attn_load<__nv_bfloat16, 8>(const __nv_bfloat16 *p, float (&v)[8]) {
-    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        v[2 * e] = __uint_as_float(w[e] << 16);
-        v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-    }
-}
-template <>
-__device__ __forceinline__ void attn_load<__half, 8>(const __half *p, float (&v)[8]) {
-    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        __half2 h;
-        memcpy(&h, &w[e], 4);
-        const float2 f = __half22float2(h);
-        v[2 * e] = f.x;
-        v[2 * e + 1] = f.y;
-    }
-}
-template <>
-__device__ __forceinline__ void attn_load<float, 1>(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
-template <>
-__device__ __forceinline__ void attn_load<__nv_bfloat16, 1>(const __nv_bfloat16 *p, float (&v)[1]) {
-    v[0] = __bfloat162float(*p);
-}
-template <>
-__device__ __forceinline__ void attn_load<__half, 1>(const __half *p, float (&v)[1]) {
-    v[0] = __half2float(*p);
-}
-
-template <typename T> __device__ __forceinline__ T attn_from_f32(float v);
-template <> __device__ __forceinline__ float attn_from_f32<float>(float v) { return v; }
-template <> __device__ __forceinline__ __nv_bfloat16 attn_from_f32<__nv_bfloat16>(float v) {
-    return __float2bfloat16_rn(v);
-}
-template <> __device__ __forceinline__ __half attn_from_f32<__half>(float v) { return __float2half_rn(v); }
 
 template <typename T, int CH>
 __device__ __forceinline__ void attn_store(T *p, const float (&acc)[CH]) {
 #pragma unroll
-    for (int e = 0; e < CH; ++e) p[e] = attn_from_f32<T>(acc[e]);
+    for (int e = 0; e < CH; ++e) p[e] = round_to<T>(acc[e]);
 }
 
 template <typename T, int CH, int GRP, int KT>
@@ -159,7 +112,7 @@ attn_forward_kernel(AttnParams p) {
                     if (!in) continue;
                 }
                 float v[CH];
-                attn_load<T, CH>(vbase + static_cast<size_t>(in ? yy * p.W + xx : 0) * GD + c0 * CH, v);
+                row_load<T, CH>(vbase + static_cast<size_t>(in ? yy * p.W + xx : 0) * GD + c0 * CH, v);
                 const float wc = in ? wq[c] : 0.0f;
 #pragma unroll
                 for (int e = 0; e < CH; ++e) acc[e] = fmaf(wc, v[e], acc[e]);

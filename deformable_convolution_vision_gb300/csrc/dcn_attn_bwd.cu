@@ -33,74 +33,14 @@
 
 #include <cstring>
 
+#include "dcn_rowload.cuh"
 #include "dcn_sampling_ops.h"
 
 namespace dcn {
 
 namespace {
 
-template <typename T, int CH>
-__device__ __forceinline__ void ab_load(const T *p, float (&v)[CH]);
 
-template <>
-__device__ __forceinline__ void ab_load<float, 4>(const float *p, float (&v)[4]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-}
-template <>
-__device__ __forceinline__ void ab_load<__nv_bfloat16, 8>(const __nv_bfloat16 *p, float (&v)[8]) {
-    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        v[2 * e] = __uint_as_float(w[e] << 16);
-        v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-    }
-}
-template <>
-__device__ __forceinline__ void ab_load<__half, 8>(const __half *p, float (&v)[8]) {
-    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        __half2 h;
-        memcpy(&h, &w[e], 4);
-        const float2 f = __half22float2(h);
-        v[2 * e] = f.x;
-        v[2 * e + 1] = f.y;
-    }
-}
-template <>
-__device__ __forceinline__ void ab_load<float, 1>(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
-template <>
-__device__ __forceinline__ void ab_load<__nv_bfloat16, 1>(const __nv_bfloat16 *p, float (&v)[1]) {
-    v[0] = __bfloat162float(*p);
-}
-template <>
-__device__ __forceinline__ void ab_load<__half, 1>(const __half *p, float (&v)[1]) {
-    v[0] = __half2float(*p);
-}
-
-// Four 16-bit elements as fp32 from an 8-byte load.
-template <typename T>
-__device__ __forceinline__ void ab_load4(const T *p, float *v);
-template <>
-__device__ __forceinline__ void ab_load4<__nv_bfloat16>(const __nv_bfloat16 *p, float *v) {
-    const uint2 r = __ldg(reinterpret_cast<const uint2 *>(p));
-    v[0] = __uint_as_float(r.x << 16);
-    v[1] = __uint_as_float(r.x & 0xFFFF0000u);
-    v[2] = __uint_as_float(r.y << 16);
-    v[3] = __uint_as_float(r.y & 0xFFFF0000u);
-}
-template <>
-__device__ __forceinline__ void ab_load4<__half>(const __half *p, float *v) {
-    const uint2 r = __ldg(reinterpret_cast<const uint2 *>(p));
-    __half2 a, b;
-    memcpy(&a, &r.x, 4);
-    memcpy(&b, &r.y, 4);
-    const float2 fa = __half22float2(a), fb = __half22float2(b);
-    v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
-}
 
 // p[0 .. N) += s * g[0 .. N): fp32 reductions, 16 bytes each for N a
 // multiple of 4 (p is then 16-byte aligned)
@@ -171,10 +111,10 @@ attn_backward_kernel(AttnBwdParams p) {
     constexpr bool kSplit = kOneChunk && CH == 8;
     float go_d[CH], go_r[CH];
     if constexpr (kOneChunk) {
-        ab_load<T, CH>(go_row + r * CH, go_d);
+        row_load<T, CH>(go_row + r * CH, go_d);
         if constexpr (kSplit) {
-            ab_load4<T>(go_row + 4 * r, go_r);
-            ab_load4<T>(go_row + 4 * (r + GRP), go_r + 4);
+            row_load4<T>(go_row + 4 * r, go_r);
+            row_load4<T>(go_row + 4 * (r + GRP), go_r + 4);
         }
     }
 
@@ -200,7 +140,7 @@ attn_backward_kernel(AttnBwdParams p) {
 #pragma unroll
                 for (int e = 0; e < CH; ++e) go[e] = go_d[e];
             } else {
-                ab_load<T, CH>(go_row + c0 * CH, go);
+                row_load<T, CH>(go_row + c0 * CH, go);
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -211,7 +151,7 @@ attn_backward_kernel(AttnBwdParams p) {
                     continue;
                 const size_t at = static_cast<size_t>(yy * p.W + xx) * GD;
                 float v[CH];
-                ab_load<T, CH>(vbase + at + c0 * CH, v);
+                row_load<T, CH>(vbase + at + c0 * CH, v);
                 float dot = 0.0f;
 #pragma unroll
                 for (int e = 0; e < CH; ++e) dot = fmaf(go[e], v[e], dot);

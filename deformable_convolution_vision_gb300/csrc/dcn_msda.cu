@@ -26,61 +26,13 @@
 
 #include <cstring>
 
+#include "dcn_rowload.cuh"
 #include "dcn_sampling_ops.h"
 
 namespace dcn {
 
 namespace {
 
-// CH elements as fp32 from a 16-byte (or one-element) load.
-template <typename T, int CH>
-__device__ __forceinline__ void msda_load(const T *p, float (&v)[CH]);
-
-template <>
-__device__ __forceinline__ void msda_load<float, 4>(const float *p, float (&v)[4]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-}
-template <>
-__device__ __forceinline__ void msda_load<__nv_bfloat16, 8>(const __nv_bfloat16 *p, float (&v)[8]) {
-    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        v[2 * e] = __uint_as_float(w[e] << 16);
-        v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-    }
-}
-template <>
-__device__ __forceinline__ void msda_load<__half, 8>(const __half *p, float (&v)[8]) {
-    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        __half2 h;
-        memcpy(&h, &w[e], 4);
-        const float2 f = __half22float2(h);
-        v[2 * e] = f.x;
-        v[2 * e + 1] = f.y;
-    }
-}
-template <>
-__device__ __forceinline__ void msda_load<float, 1>(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
-template <>
-__device__ __forceinline__ void msda_load<__nv_bfloat16, 1>(const __nv_bfloat16 *p, float (&v)[1]) {
-    v[0] = __bfloat162float(*p);
-}
-template <>
-__device__ __forceinline__ void msda_load<__half, 1>(const __half *p, float (&v)[1]) {
-    v[0] = __half2float(*p);
-}
-
-template <typename T> __device__ __forceinline__ T msda_from_f32(float v);
-template <> __device__ __forceinline__ float msda_from_f32<float>(float v) { return v; }
-template <> __device__ __forceinline__ __nv_bfloat16 msda_from_f32<__nv_bfloat16>(float v) {
-    return __float2bfloat16_rn(v);
-}
-template <> __device__ __forceinline__ __half msda_from_f32<__half>(float v) { return __float2half_rn(v); }
 
 template <typename T, int CH, int KP>
 __global__ void __launch_bounds__(256)
@@ -154,7 +106,7 @@ msda_forward_kernel(MsdaParams p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float v[CH];
-                    msda_load<T, CH>(value + ((level0 + off[u][c]) * p.G + g) * p.D + d0, v);
+                    row_load<T, CH>(value + ((level0 + off[u][c]) * p.G + g) * p.D + d0, v);
 #pragma unroll
                     for (int e = 0; e < CH; ++e) acc[e] = fmaf(cw[u][c], v[e], acc[e]);
                 }
@@ -163,7 +115,7 @@ msda_forward_kernel(MsdaParams p) {
     }
     T *__restrict__ out = static_cast<T *>(p.out) + row * p.D + d0;
 #pragma unroll
-    for (int e = 0; e < CH; ++e) out[e] = msda_from_f32<T>(acc[e]);
+    for (int e = 0; e < CH; ++e) out[e] = round_to<T>(acc[e]);
 }
 
 // The same for a row group of GRP lanes (GRP = D / CH, a power of two that
@@ -251,7 +203,7 @@ msda_forward_group_kernel(MsdaParams p) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 float v[CH];
-                msda_load<T, CH>(vbase + off[c], v);
+                row_load<T, CH>(vbase + off[c], v);
 #pragma unroll
                 for (int e = 0; e < CH; ++e) acc[e] = fmaf(cw[c], v[e], acc[e]);
             }
@@ -260,7 +212,7 @@ msda_forward_group_kernel(MsdaParams p) {
     if (live) {
         T *__restrict__ out = static_cast<T *>(p.out) + row * p.D + d0;
 #pragma unroll
-        for (int e = 0; e < CH; ++e) out[e] = msda_from_f32<T>(acc[e]);
+        for (int e = 0; e < CH; ++e) out[e] = round_to<T>(acc[e]);
     }
 }
 
