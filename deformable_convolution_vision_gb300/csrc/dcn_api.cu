@@ -838,8 +838,11 @@ dcn_status_t dcn_attn_backward(const void *value, const float *offsets, const fl
     if (cudaMemsetAsync(grad_value, 0, static_cast<size_t>(B) * H * W * GD * sizeof(float), s) !=
         cudaSuccess)
         return DCN_ERR_CUDA;
-    const bool vec = D % (dtype == DCN_F32 ? 4 : 8) == 0 && aligned(value, 16) &&
-                     aligned(grad_out, 16) && aligned(grad_value, 16);
+    // four channels per lane: 8-byte (16-bit) or 16-byte (fp32) loads,
+    // 16-byte reductions
+    const size_t la = dtype == DCN_F32 ? 16 : 8;
+    const bool vec = D % 4 == 0 && aligned(value, la) && aligned(grad_out, la) &&
+                     aligned(grad_value, 16);
     if (dcn::launch_attn_backward(p, dtype, vec, s) != cudaSuccess) return DCN_ERR_CUDA;
     return DCN_OK;
 }

@@ -55,6 +55,24 @@ __device__ __forceinline__ void row_load<__half, 1>(const __half *p, float (&v)[
     v[0] = __half2float(*p);
 }
 
+template <>
+__device__ __forceinline__ void row_load<__nv_bfloat16, 4>(const __nv_bfloat16 *p, float (&v)[4]) {
+    const uint2 r = __ldg(reinterpret_cast<const uint2 *>(p));
+    v[0] = __uint_as_float(r.x << 16);
+    v[1] = __uint_as_float(r.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(r.y << 16);
+    v[3] = __uint_as_float(r.y & 0xFFFF0000u);
+}
+template <>
+__device__ __forceinline__ void row_load<__half, 4>(const __half *p, float (&v)[4]) {
+    const uint2 r = __ldg(reinterpret_cast<const uint2 *>(p));
+    __half2 a, b;
+    memcpy(&a, &r.x, 4);
+    memcpy(&b, &r.y, 4);
+    const float2 fa = __half22float2(a), fb = __half22float2(b);
+    v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+}
+
 // Four 16-bit elements as fp32 from an 8-byte load.
 template <typename T>
 __device__ __forceinline__ void row_load4(const T *p, float *v);

@@ -68,8 +68,8 @@ struct AttnBwdParams {
     int kh, kw, sh, sw, ph, pw, dh, dw;
     int softmax;
 };
-// vec: D a multiple of 8 (16-bit) or 4 (fp32); value, grad_out and
-// grad_value 16-byte aligned.
+// vec: D a multiple of 4; value and grad_out 8-byte (16-bit) or 16-byte
+// (fp32) aligned, grad_value 16-byte aligned.
 cudaError_t launch_attn_backward(const AttnBwdParams &p, int dtype, bool vec, cudaStream_t stream);
 
 }  // namespace dcn
