@@ -16,6 +16,7 @@
 #include "dcn.h"
 #include "dcn_device.cuh"
 #include "dcn_kernels.h"
+#include "dcn_limits.h"
 #include "dcn_sampling_ops.h"
 
 struct dcn_handle_s {
@@ -78,7 +79,8 @@ constexpr int kHostBands = 3;
 constexpr int kHostLastDiv = 4;
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
-constexpr long long kIndexLimit = (1ll << 31) - 1;
+using dcn::kIndexLimit;
+using dcn::within_index_limit;
 
 inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
@@ -117,13 +119,13 @@ dcn_status_t make_conv(const dcn_conv_desc_t &d, int dtype, Conv *c) {
     const long long Ho = out_size_ll(d.H, d.kh, d.stride_h, d.pad_h, d.dil_h);
     const long long Wo = out_size_ll(d.W, d.kw, d.stride_w, d.pad_w, d.dil_w);
     if (Ho <= 0 || Wo <= 0 || Ho > kIndexLimit || Wo > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (!within_index_limit({d.kh, d.kw})) return DCN_ERR_INVALID_ARG;
     const long long taps = static_cast<long long>(d.kh) * d.kw;
-    if (taps > kIndexLimit) return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(d.B) * d.H * d.W * d.C > kIndexLimit) return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(d.B) * 2 * d.offset_groups * taps * Ho * Wo > kIndexLimit)
+    if (!within_index_limit({d.B, d.H, d.W, d.C}) ||
+        !within_index_limit({d.B, 2, d.offset_groups, taps, Ho, Wo}) ||
+        !within_index_limit({d.B, Ho, Wo, d.O}) ||
+        !within_index_limit({d.O, d.C / d.groups, taps}))
         return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(d.B) * Ho * Wo * d.O > kIndexLimit) return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(d.O) * (d.C / d.groups) * taps > kIndexLimit) return DCN_ERR_INVALID_ARG;
     c->d = d;
     c->Ho = static_cast<int>(Ho);
     c->Wo = static_cast<int>(Wo);
@@ -427,7 +429,7 @@ dcn_status_t dcn_pack_weight(dcn_handle_t h, const void *weight, int O, int C, i
     if (!h || !weight) return DCN_ERR_INVALID_ARG;
     if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
     if (O <= 0 || C <= 0 || kh <= 0 || kw <= 0) return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(O) * C * kh * kw > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (!within_index_limit({O, C, kh, kw})) return DCN_ERR_INVALID_ARG;
     if (!aligned(weight, esize(dtype))) return DCN_ERR_INVALID_ARG;
     Conv c;
     c.d = page_desc(1, C, 1, 1, O, kh, kw, 0);   // only (O, C, kh, kw) key the pack
@@ -696,10 +698,8 @@ dcn_status_t dcn_msda_forward(const void *value, const int *shapes, const int *s
     if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
     if (B <= 0 || S <= 0 || G <= 0 || D <= 0 || Q <= 0 || K <= 0) return DCN_ERR_INVALID_ARG;
     if (L <= 0 || L > dcn::kMsdaMaxLevels) return DCN_ERR_UNSUPPORTED;
-    const long long LK = static_cast<long long>(L) * K;
-    if (static_cast<long long>(B) * S * G * D > kIndexLimit ||
-        static_cast<long long>(B) * Q * G * LK * 2 > kIndexLimit ||
-        static_cast<long long>(B) * Q * G * D > kIndexLimit)
+    if (!within_index_limit({B, S, G, D}) || !within_index_limit({B, Q, G, L, K, 2}) ||
+        !within_index_limit({B, Q, G, D}))
         return DCN_ERR_INVALID_ARG;
     const size_t es = esize(dtype);
     if (!aligned(value, es) || !aligned(out, es) || !aligned(locations, 8) || !aligned(weights, 4))
@@ -733,10 +733,8 @@ dcn_status_t dcn_msda_backward(const void *value, const int *shapes, const int *
     if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
     if (B <= 0 || S <= 0 || G <= 0 || D <= 0 || Q <= 0 || K <= 0) return DCN_ERR_INVALID_ARG;
     if (L <= 0 || L > dcn::kMsdaMaxLevels) return DCN_ERR_UNSUPPORTED;
-    const long long LK = static_cast<long long>(L) * K;
-    if (static_cast<long long>(B) * S * G * D > kIndexLimit ||
-        static_cast<long long>(B) * Q * G * LK * 2 > kIndexLimit ||
-        static_cast<long long>(B) * Q * G * D > kIndexLimit)
+    if (!within_index_limit({B, S, G, D}) || !within_index_limit({B, Q, G, L, K, 2}) ||
+        !within_index_limit({B, Q, G, D}))
         return DCN_ERR_INVALID_ARG;
     const size_t es = esize(dtype);
     if (!aligned(value, es) || !aligned(grad_out, es) || !aligned(locations, 8) ||
@@ -780,10 +778,8 @@ dcn_status_t dcn_attn_forward(const void *value, const float *offsets, const flo
     const long long Ho = out_size_ll(H, kh, stride_h, pad_h, dil_h);
     const long long Wo = out_size_ll(W, kw, stride_w, pad_w, dil_w);
     if (Ho <= 0 || Wo <= 0) return DCN_ERR_INVALID_ARG;
-    const long long K = static_cast<long long>(kh) * kw;
-    const long long GD = static_cast<long long>(G) * D;
-    if (K > kIndexLimit || static_cast<long long>(B) * H * W * GD > kIndexLimit ||
-        B * Ho * Wo * G * K * 2 > kIndexLimit || B * Ho * Wo * GD > kIndexLimit)
+    if (!within_index_limit({kh, kw}) || !within_index_limit({B, H, W, G, D}) ||
+        !within_index_limit({B, Ho, Wo, G, kh, kw, 2}) || !within_index_limit({B, Ho, Wo, G, D}))
         return DCN_ERR_INVALID_ARG;
     const size_t es = esize(dtype);
     if (!aligned(value, es) || !aligned(out, es) || !aligned(offsets, 8) || !aligned(weights, 4))
@@ -815,10 +811,8 @@ dcn_status_t dcn_attn_backward(const void *value, const float *offsets, const fl
     const long long Ho = out_size_ll(H, kh, stride_h, pad_h, dil_h);
     const long long Wo = out_size_ll(W, kw, stride_w, pad_w, dil_w);
     if (Ho <= 0 || Wo <= 0) return DCN_ERR_INVALID_ARG;
-    const long long K = static_cast<long long>(kh) * kw;
-    const long long GD = static_cast<long long>(G) * D;
-    if (K > kIndexLimit || static_cast<long long>(B) * H * W * GD > kIndexLimit ||
-        B * Ho * Wo * G * K * 2 > kIndexLimit || B * Ho * Wo * GD > kIndexLimit)
+    if (!within_index_limit({kh, kw}) || !within_index_limit({B, H, W, G, D}) ||
+        !within_index_limit({B, Ho, Wo, G, kh, kw, 2}) || !within_index_limit({B, Ho, Wo, G, D}))
         return DCN_ERR_INVALID_ARG;
     const size_t es = esize(dtype);
     if (!aligned(value, es) || !aligned(grad_out, es) || !aligned(offsets, 8) ||
@@ -835,7 +829,7 @@ dcn_status_t dcn_attn_backward(const void *value, const float *offsets, const fl
     p.softmax = softmax ? 1 : 0;
     cudaStream_t s = as_stream(stream);
     // the value gradient is a sum of reductions: start it at zero
-    if (cudaMemsetAsync(grad_value, 0, static_cast<size_t>(B) * H * W * GD * sizeof(float), s) !=
+    if (cudaMemsetAsync(grad_value, 0, static_cast<size_t>(B) * H * W * G * D * sizeof(float), s) !=
         cudaSuccess)
         return DCN_ERR_CUDA;
     // four channels per lane: 8-byte (16-bit) or 16-byte (fp32) loads,
@@ -851,7 +845,7 @@ static dcn_status_t layout_copy(const void *src, void *dst, int B, int R, int S,
                                 void *stream) {
     if (!src || !dst || src == dst) return DCN_ERR_INVALID_ARG;
     if (!valid_dtype(dtype) || B <= 0 || R <= 0 || S <= 0) return DCN_ERR_INVALID_ARG;
-    if (static_cast<long long>(B) * R * S > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (!within_index_limit({B, R, S})) return DCN_ERR_INVALID_ARG;
     const size_t es = esize(dtype);
     if (!aligned(src, es) || !aligned(dst, es)) return DCN_ERR_INVALID_ARG;
     if (B > 65535 || (R + 31) / 32 > 65535) return DCN_ERR_UNSUPPORTED;
@@ -862,13 +856,13 @@ static dcn_status_t layout_copy(const void *src, void *dst, int B, int R, int S,
 
 dcn_status_t dcn_nchw_to_nhwc(const void *src, void *dst, int B, int C, int H, int W, int dtype,
                               void *stream) {
-    if (H <= 0 || W <= 0 || static_cast<long long>(H) * W > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (H <= 0 || W <= 0 || !within_index_limit({H, W})) return DCN_ERR_INVALID_ARG;
     return layout_copy(src, dst, B, C, H * W, dtype, stream);
 }
 
 dcn_status_t dcn_nhwc_to_nchw(const void *src, void *dst, int B, int C, int H, int W, int dtype,
                               void *stream) {
-    if (H <= 0 || W <= 0 || static_cast<long long>(H) * W > kIndexLimit) return DCN_ERR_INVALID_ARG;
+    if (H <= 0 || W <= 0 || !within_index_limit({H, W})) return DCN_ERR_INVALID_ARG;
     return layout_copy(src, dst, B, H * W, C, dtype, stream);
 }
 

@@ -23,13 +23,13 @@
 
 #include "dcn.h"
 #include "dcn_kernels.h"
+#include "dcn_limits.h"
 
 namespace {
 
 constexpr size_t kScratchWeightBytes = DCN_NOALLOC_MAX_WEIGHT_BYTES;
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-constexpr long long kIndexLimit = (1ll << 31) - 1;
 
 // The packed weight [O][kh*kw*C] of the current call, shared by all calls.
 static __device__ __align__(256) unsigned char g_wpack_scratch[kScratchWeightBytes];
@@ -90,11 +90,10 @@ extern "C" DCN_API dcn_status_t dcn_forward_noalloc(
     const long long Ho = static_cast<long long>(H) + 2ll * pad - kh + 1;
     const long long Wo = static_cast<long long>(W) + 2ll * pad - kw + 1;
     if (Ho <= 0 || Wo <= 0) return DCN_ERR_INVALID_ARG;
+    if (!dcn::within_index_limit({kh, kw})) return DCN_ERR_INVALID_ARG;
     const long long taps = static_cast<long long>(kh) * kw;
-    if (taps > kIndexLimit || static_cast<long long>(B) * H * W * C > kIndexLimit ||
-        static_cast<long long>(B) * 2 * taps * Ho * Wo > kIndexLimit ||
-        static_cast<long long>(B) * Ho * Wo * O > kIndexLimit ||
-        static_cast<long long>(O) * C * taps > kIndexLimit)
+    if (!dcn::within_index_limit({B, H, W, C}) || !dcn::within_index_limit({B, 2, taps, Ho, Wo}) ||
+        !dcn::within_index_limit({B, Ho, Wo, O}) || !dcn::within_index_limit({O, C, taps}))
         return DCN_ERR_INVALID_ARG;
     if (!x || !offset || !weight || !out) return DCN_ERR_INVALID_ARG;
     const size_t es = dtype == DCN_F32 ? 4 : 2;

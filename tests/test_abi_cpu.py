@@ -100,3 +100,33 @@ def test_python_wrappers_marshal_every_argument(lib):
         with pytest.raises(binding.DcnError) as e:
             call()
         assert e.value.status == bad
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers: only where nothing can launch")
+def test_sizes_whose_product_wraps_are_rejected(lib):
+    """Every indexed tensor must hold fewer than 2^31 elements.  Dimensions
+    whose element count overflows a 64-bit product (and would wrap round
+    to a small one) must still be refused, before any launch.  The pointers
+    are fake and never dereferenced."""
+    bad = binding.STATUS_CODE["DCN_ERR_INVALID_ARG"]
+    src, dst, f32a, f32b, f32c = (ctypes.c_void_p(0x100000 * k) for k in range(1, 6))
+    # value 2^30 x 2^30 pixels of 16 channels: 2^64 elements; a 2^30 stride
+    # leaves a 1 x 1 output, so every other count is small
+    big, stride = 1 << 30, 1 << 30
+    assert lib.dcn_attn_forward(src, f32a, f32b, dst, 1, big, big, 1, 16, 1, 1, stride, stride,
+                                0, 0, 1, 1, 1, 1, None) == bad
+    assert lib.dcn_attn_backward(src, f32a, f32b, dst, f32a, f32b, f32c, 1, big, big, 1, 16, 1, 1,
+                                 stride, stride, 0, 0, 1, 1, 1, 1, None) == bad
+    # layout copies: 2^15 images of 2^20 channels x 2^14 x 2^15 pixels = 2^64
+    assert lib.dcn_nchw_to_nhwc(src, dst, 1 << 15, 1 << 20, 1 << 14, 1 << 15, 1, None) == bad
+    assert lib.dcn_nhwc_to_nchw(src, dst, 1 << 15, 1 << 20, 1 << 14, 1 << 15, 1, None) == bad
+    # plainly oversized problems on the other handle-free entries
+    shapes = (ctypes.c_int * 2)(8, 8)
+    starts = (ctypes.c_int * 1)(0)
+    assert lib.dcn_msda_forward(src, shapes, starts, 1, f32a, f32b, dst, 2, 1 << 30, 1, 2, 1, 1,
+                                1, 1, None) == bad
+    assert lib.dcn_msda_backward(src, shapes, starts, 1, f32a, f32b, dst, f32a, f32b, f32c, 2,
+                                 1 << 30, 1, 2, 1, 1, 1, 1, None) == bad
+    assert lib.dcn_forward_noalloc(src, f32a, f32b, dst, f32c, dst, 1, 1 << 16, 1 << 16, 1 << 16,
+                                   16, 1, 1, 0, 1, None) == bad
+    assert lib.dcn_out_size(1 << 30, 1, 1, 1 << 30, 1) == 0
