@@ -81,6 +81,27 @@ def _pair(v, name):
     return v
 
 
+def _check_devices(device, **named):
+    """Every given tensor (None is skipped) must live on ``device``: the
+    kernels take raw device pointers and cannot tell a host or another
+    GPU's pointer from their own."""
+    for name, t in named.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} must be on {device}, not {t.device}")
+
+
+def _check_out(out, shape, dtype, device, channels_last=False):
+    """A caller-supplied output must be exactly what the kernel writes: its
+    shape, dtype, device and dense layout (a smaller or strided buffer would
+    be written out of bounds)."""
+    import torch
+    fmt = torch.channels_last if channels_last else torch.contiguous_format
+    if tuple(out.shape) != tuple(shape) or out.dtype != dtype or out.device != device or \
+            not out.is_contiguous(memory_format=fmt):
+        layout = "channels_last" if channels_last else "contiguous"
+        raise ValueError(f"out must be {tuple(shape)} {dtype} on {device}, {layout}")
+
+
 def _out_size(n, k, s, p, d):
     span = n + 2 * p - d * (k - 1) - 1
     return span // s + 1 if span >= 0 else 0
@@ -92,6 +113,7 @@ def _describe(x, offset, weight, stride, padding, dilation, mask):
     import torch
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor")
+    _check_devices(x.device, offset=offset, weight=weight, mask=mask)
     if not x.is_contiguous(memory_format=torch.channels_last):
         raise ValueError("x must be channels_last contiguous")
     for name, t in (("offset", offset), ("weight", weight), ("mask", mask)):
@@ -139,9 +161,15 @@ def deform_conv2d(x, offset, weight, bias=None, stride=1, padding=0, dilation=1,
     if bias is not None and (not bias.is_contiguous() or bias.dtype != torch.float32):
         raise TypeError("bias must be contiguous float32")
     desc, Ho, Wo = _describe(x, offset, weight, stride, padding, dilation, mask)
+    if bias is not None:
+        _check_devices(x.device, bias=bias)
+        if tuple(bias.shape) != (desc.O,):
+            raise ValueError(f"bias must be {(desc.O,)}")
     if out is None:
         out = torch.empty((desc.B, desc.O, Ho, Wo), dtype=x.dtype, device=x.device,
                           memory_format=torch.channels_last)
+    else:
+        _check_out(out, (desc.B, desc.O, Ho, Wo), x.dtype, x.device, channels_last=True)
     own = handle is None
     h = Handle() if own else handle
     try:
@@ -165,6 +193,7 @@ def deform_conv2d_backward(grad_out, x, offset, weight, stride=1, padding=0, dil
     (None when ``bias`` is False).  Layouts are checked, never converted."""
     import torch
     desc, Ho, Wo = _describe(x, offset, weight, stride, padding, dilation, mask)
+    _check_devices(x.device, grad_out=grad_out)
     if tuple(grad_out.shape) != (desc.B, desc.O, Ho, Wo) or grad_out.dtype != x.dtype or \
             not grad_out.is_contiguous(memory_format=torch.channels_last):
         raise ValueError(f"grad_out must be {(desc.B, desc.O, Ho, Wo)} channels_last in x's dtype")
@@ -210,8 +239,11 @@ def msda(value, shapes, starts, locations, weights, method=None, out=None, strea
     Bq, Q, G2, L, K, two = locations.shape
     if (Bq, G2, L, two) != (B, G, len(shapes), 2) or tuple(weights.shape) != (B, Q, G, L * K):
         raise ValueError("locations must be [B, Q, G, L, K, 2] and weights [B, Q, G, L*K]")
+    _check_devices(value.device, locations=locations, weights=weights)
     if out is None:
         out = torch.empty((B, Q, G, D), dtype=value.dtype, device=value.device)
+    else:
+        _check_out(out, (B, Q, G, D), value.dtype, value.device)
     dcn_msda_forward(value, shapes, starts, locations, weights, out, B, S, G, D, Q, K,
                      method == "softmax", _dtype_code(value), stream)
     return out
@@ -243,6 +275,7 @@ def msda_backward(grad_out, value, shapes, starts, locations, weights, method=No
         raise ValueError("locations must be [B, Q, G, L, K, 2] and weights [B, Q, G, L*K]")
     if tuple(grad_out.shape) != (B, Q, G, D):
         raise ValueError("grad_out must be [B, Q, G, D]")
+    _check_devices(value.device, locations=locations, weights=weights, grad_out=grad_out)
     dev = value.device
     gv = torch.empty((B, S, G, D), dtype=torch.float32, device=dev)
     gl = torch.empty((B, Q, G, L, K, 2), dtype=torch.float32, device=dev)
@@ -278,8 +311,11 @@ def attn(value, offsets, weights, kernel_size, stride=1, padding=0, dilation=1, 
     K = kh * kw
     if tuple(offsets.shape) != (B, Ho, Wo, G, K, 2) or tuple(weights.shape) != (B, Ho, Wo, G, K):
         raise ValueError("offsets must be [B, Ho, Wo, G, K, 2] and weights [B, Ho, Wo, G, K]")
+    _check_devices(value.device, offsets=offsets, weights=weights)
     if out is None:
         out = torch.empty((B, Ho, Wo, G, D), dtype=value.dtype, device=value.device)
+    else:
+        _check_out(out, (B, Ho, Wo, G, D), value.dtype, value.device)
     dcn_attn_forward(value, offsets, weights, out, B, H, W, G, D, kh, kw, sh, sw, ph, pw, dh, dw,
                      method == "softmax", _dtype_code(value), stream)
     return out
@@ -312,6 +348,7 @@ def attn_backward(grad_out, value, offsets, weights, kernel_size, stride=1, padd
         raise ValueError("offsets must be [B, Ho, Wo, G, K, 2] and weights [B, Ho, Wo, G, K]")
     if tuple(grad_out.shape) != (B, Ho, Wo, G, D):
         raise ValueError("grad_out must be [B, Ho, Wo, G, D]")
+    _check_devices(value.device, offsets=offsets, weights=weights, grad_out=grad_out)
     dev = value.device
     gv = torch.empty((B, H, W, G, D), dtype=torch.float32, device=dev)
     go = torch.empty((B, Ho, Wo, G, K, 2), dtype=torch.float32, device=dev)

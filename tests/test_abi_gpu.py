@@ -185,3 +185,45 @@ def test_host_entry_point_pageable_memory(handle):
                          wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad, dcn.DCN_BF16)
     assert dcn.dcn_sync_status(handle.h) == 0
     assert torch.equal(out.permute(0, 3, 1, 2), pinned)
+
+
+def test_python_entries_refuse_wrong_buffers():
+    """``out`` of another dtype or layout, and a bias longer than O, are
+    refused before the library is called.  Every wrong buffer here is at
+    least as large as the right one, so nothing could be written out of
+    bounds even if a check were missing."""
+    from deformable_convolution_vision_gb300.inputs import (ATTN_WORKLOADS, MSDA_WORKLOADS,
+                                                            make_attn_inputs, make_msda_inputs)
+    wl = WORKLOADS["decoder3x3"].with_(H=24, W=40)
+    d = to_device(make_inputs(wl))
+    shape = (wl.B, wl.O, wl.Ho, wl.Wo)
+    wrong = {
+        "fp32 out": torch.empty(shape, device="cuda", memory_format=torch.channels_last),
+        "NCHW out": torch.empty(shape, dtype=torch.bfloat16, device="cuda"),
+    }
+    for name, out in wrong.items():
+        with pytest.raises(ValueError, match="out must be"):
+            dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], padding=wl.pad,
+                              mask=d["mask"], out=out)
+    long_bias = torch.zeros(wl.O + 1, device="cuda")
+    with pytest.raises(ValueError, match="bias must be"):
+        dcn.deform_conv2d(d["x"], d["offset"], d["weight"], long_bias, padding=wl.pad,
+                          mask=d["mask"])
+    ref = dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], padding=wl.pad,
+                            mask=d["mask"])
+    out = torch.empty_like(ref)
+    dcn.deform_conv2d(d["x"], d["offset"], d["weight"], d["bias"], padding=wl.pad,
+                      mask=d["mask"], out=out)
+    assert torch.equal(out, ref)
+
+    m = MSDA_WORKLOADS["msda_page"]
+    mi = {k: v.cuda() for k, v in make_msda_inputs(m).items()}
+    with pytest.raises(ValueError, match="out must be"):
+        dcn.msda(mi["value"], m.shapes, m.starts, mi["locations"], mi["weights"],
+                 out=torch.empty((m.B, m.Q, m.G, m.D), device="cuda"))
+    a = ATTN_WORKLOADS["attn_page"]
+    ai = {k: v.cuda() for k, v in make_attn_inputs(a).items()}
+    Ho, Wo = a.out_size()
+    with pytest.raises(ValueError, match="out must be"):
+        dcn.attn(ai["value"], ai["offsets"], ai["weights"], a.kernel, a.stride, a.padding,
+                 a.dilation, out=torch.empty((a.B, Ho, Wo, a.G, a.D), device="cuda"))
