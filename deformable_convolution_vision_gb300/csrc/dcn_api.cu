@@ -916,15 +916,31 @@ dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset
         st = ensure(&h->stage[i], &h->stage_cap[i], (bytes[i] + 255) & ~static_cast<size_t>(255), s);
         if (st != DCN_OK) return st;
     }
-    if (!h->s_kernel) {
-        if (cudaStreamCreateWithFlags(&h->s_kernel, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&h->s_down, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&h->ev_in, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&h->ev_k, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) != cudaSuccess ||
-            cudaHostAlloc(reinterpret_cast<void **>(&h->host_status), sizeof(unsigned),
-                          cudaHostAllocDefault) != cudaSuccess)
+    // Each pipeline resource is made on first use and stored only once made,
+    // so a failure part way leaves the others in place and this one null, to
+    // be retried by the next call (dcn_destroy frees whichever exist).
+    auto make_stream = [](cudaStream_t *out) {
+        cudaStream_t t = nullptr;
+        if (*out) return true;
+        if (cudaStreamCreateWithFlags(&t, cudaStreamNonBlocking) != cudaSuccess) return false;
+        *out = t;
+        return true;
+    };
+    auto make_event = [](cudaEvent_t *out) {
+        cudaEvent_t t = nullptr;
+        if (*out) return true;
+        if (cudaEventCreateWithFlags(&t, cudaEventDisableTiming) != cudaSuccess) return false;
+        *out = t;
+        return true;
+    };
+    if (!make_stream(&h->s_kernel) || !make_stream(&h->s_down) || !make_event(&h->ev_in) ||
+        !make_event(&h->ev_k) || !make_event(&h->ev_done))
+        return DCN_ERR_CUDA;
+    if (!h->host_status) {
+        void *t = nullptr;
+        if (cudaHostAlloc(&t, sizeof(unsigned), cudaHostAllocDefault) != cudaSuccess)
             return DCN_ERR_CUDA;
+        h->host_status = static_cast<unsigned *>(t);
     }
     // The host link is the slow part (the copies take longer than the
     // kernel), so the call is a pipeline over bands of output rows: the
