@@ -9,8 +9,12 @@ library routine fix, independently of the oracle's own code.
 - a constant value map sampled inside every level with softmax weights:
   the constant (the weights sum to one);
 - one-hot weights on one level of a map whose levels hold different
-  constants: that level's constant (catches level offsets and shapes).
+  constants: that level's constant (catches level offsets and shapes);
+- hand-derived samples and weighted sums on a two-level map
+  (tests/golden/msda_samples.txt), exact in binary.
 """
+
+import os
 
 import numpy as np
 import torch
@@ -141,5 +145,51 @@ def pin_msda_levels(orc):
         assert np.allclose(got, float(lv[l]), rtol=0, atol=1e-13), f"level {l}"
 
 
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "msda_samples.txt")
+
+
+def _golden():
+    levels, points, queries = [], [], []
+    with open(GOLDEN) as fh:
+        for line in fh:
+            f = line.split("#", 1)[0].split()
+            if not f:
+                continue
+            if f[0] == "level":
+                H, W = int(f[1]), int(f[2])
+                levels.append((H, W, [float(v) for v in f[3:]]))
+                assert len(levels[-1][2]) == H * W
+            elif f[0] == "point":
+                points.append((int(f[1]), int(f[2]), float(f[3]), float(f[4]), float(f[5])))
+            elif f[0] == "query":
+                queries.append(([float(v) for v in f[1:5]], f[5] == "softmax", float(f[6])))
+    return levels, points, queries
+
+
+def pin_msda_golden(orc):
+    """Hand-derived samples and weighted sums (tests/golden/msda_samples.txt),
+    exact in binary: each point alone (a one-hot weight) gives its sample,
+    and each query its weighted sum."""
+    levels, points, queries = _golden()
+    shapes = [[H, W] for H, W, _ in levels]
+    starts, S = _starts(shapes)
+    L, K = len(levels), 2
+    value = torch.tensor([v for _, _, vals in levels for v in vals], dtype=torch.float32)
+    value = value.view(1, S, 1, 1)
+    loc = torch.zeros(1, 1, 1, L, K, 2)
+    for l, k, x, y, _ in points:
+        loc[0, 0, 0, l, k, 0], loc[0, 0, 0, l, k, 1] = x, y
+    for l, k, x, y, sample in points:
+        w = torch.zeros(1, 1, 1, L * K)
+        w[..., l * K + k] = 1.0
+        got = float(orc.msda_forward(value, shapes, starts, loc, w, False)[0, 0, 0, 0])
+        assert got == sample, f"point (level {l}, k {k}) at ({x}, {y}): {got} != {sample}"
+    for weights, softmax, expected in queries:
+        w = torch.tensor(weights, dtype=torch.float32).view(1, 1, 1, L * K)
+        got = float(orc.msda_forward(value, shapes, starts, loc, w, softmax)[0, 0, 0, 0])
+        assert abs(got - expected) <= 1e-12 * max(1.0, abs(expected)), \
+            f"query {weights} softmax={softmax}: {got} != {expected}"
+
+
 ALL_MSDA_PINS = [pin_msda_grid_sample, pin_msda_pixel_centres, pin_msda_outside,
-                 pin_msda_constant, pin_msda_levels]
+                 pin_msda_constant, pin_msda_levels, pin_msda_golden]
