@@ -9,8 +9,12 @@ oracle fix, independently of this oracle's own code.
   per group and tap, then the weighted sum (softmax by torch in fp64);
 - integer offsets: every sample is one pixel of the map, exactly;
 - every corner outside: exactly 0;
-- a constant map sampled inside with softmax weights: the constant.
+- a constant map sampled inside with softmax weights: the constant;
+- hand-derived samples and weighted sums on a 2x3 map
+  (tests/golden/attn_samples.txt), exact in binary.
 """
+
+import os
 
 import numpy as np
 import torch
@@ -155,5 +159,50 @@ def pin_attn_constant(orc):
     assert np.abs(got - exp).max() <= 1e-12 * np.abs(exp).max()
 
 
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "attn_samples.txt")
+
+
+def _golden():
+    grid, taps, queries = None, [], []
+    with open(GOLDEN) as fh:
+        for line in fh:
+            f = line.split("#", 1)[0].split()
+            if not f:
+                continue
+            if f[0] == "map":
+                H, W = int(f[1]), int(f[2])
+                grid = (H, W, [float(v) for v in f[3:]])
+                assert len(grid[2]) == H * W
+            elif f[0] == "tap":
+                taps.append((int(f[1]), float(f[2]), float(f[3]), float(f[4])))
+            elif f[0] == "weights":
+                queries.append(([float(v) for v in f[1:10]], f[10] == "softmax", float(f[11])))
+    return grid, taps, queries
+
+
+def pin_attn_golden(orc):
+    """Hand-derived samples and weighted sums at output pixel (0, 0) of a
+    2x3 map, 3x3 taps, padding 1 (tests/golden/attn_samples.txt): each tap
+    alone (a one-hot weight) gives its sample, exactly, and each weight
+    vector its sum."""
+    (H, W, vals), taps, queries = _golden()
+    K = 9
+    value = torch.tensor(vals, dtype=torch.float32).view(1, H, W, 1, 1)
+    off = torch.zeros(1, H, W, 1, K, 2)          # 3x3, stride 1, padding 1: Ho, Wo = H, W
+    for k, dy, dx, _ in taps:
+        off[0, 0, 0, 0, k, 0], off[0, 0, 0, 0, k, 1] = dy, dx
+    for k, dy, dx, sample in taps:
+        w = torch.zeros(1, H, W, 1, K)
+        w[0, 0, 0, 0, k] = 1.0
+        got = float(orc.attn_forward(value, off, w, 3, 1, 1, 1, False)[0, 0, 0, 0, 0])
+        assert got == sample, f"tap {k} with offset ({dy}, {dx}): {got} != {sample}"
+    for weights, softmax, expected in queries:
+        w = torch.zeros(1, H, W, 1, K)
+        w[0, 0, 0, 0] = torch.tensor(weights)
+        got = float(orc.attn_forward(value, off, w, 3, 1, 1, 1, softmax)[0, 0, 0, 0, 0])
+        assert abs(got - expected) <= 1e-12 * max(1.0, abs(expected)), \
+            f"weights {weights} softmax={softmax}: {got} != {expected}"
+
+
 ALL_ATTN_PINS = [pin_attn_depthwise_convolution, pin_attn_grid_sample, pin_attn_integer_offsets,
-                 pin_attn_outside, pin_attn_constant]
+                 pin_attn_outside, pin_attn_constant, pin_attn_golden]
