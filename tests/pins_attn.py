@@ -10,7 +10,8 @@ oracle fix, independently of this oracle's own code.
 - integer offsets: every sample is one pixel of the map, exactly;
 - every corner outside: exactly 0;
 - a constant map sampled inside with softmax weights: the constant;
-- hand-derived samples and weighted sums on a 2x3 map
+- hand-derived samples and weighted sums on a 2x3 map, and on a
+  two-group 5x5 map with stride 2 and dilation 2
   (tests/golden/attn_samples.txt), exact in binary.
 """
 
@@ -163,45 +164,63 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "att
 
 
 def _golden():
-    grid, taps, queries = None, [], []
+    """The cases of the fixture: each a dict of the problem, the groups'
+    maps, the taps (k, dy, dx, samples per group) and the weight vectors
+    (weights, softmax, expected per group)."""
+    cases = []
     with open(GOLDEN) as fh:
         for line in fh:
             f = line.split("#", 1)[0].split()
             if not f:
                 continue
-            if f[0] == "map":
-                H, W = int(f[1]), int(f[2])
-                grid = (H, W, [float(v) for v in f[3:]])
-                assert len(grid[2]) == H * W
+            if f[0] == "case":
+                H, W, G, sh, sw, ph, pw, dh, dw, h, w = (int(v) for v in f[1:12])
+                cases.append({"H": H, "W": W, "G": G, "stride": (sh, sw), "padding": (ph, pw),
+                              "dilation": (dh, dw), "pixel": (h, w), "maps": {}, "taps": [],
+                              "weights": []})
+            elif f[0] == "map":
+                c = cases[-1]
+                c["maps"][int(f[1])] = [float(v) for v in f[2:]]
+                assert len(c["maps"][int(f[1])]) == c["H"] * c["W"]
             elif f[0] == "tap":
-                taps.append((int(f[1]), float(f[2]), float(f[3]), float(f[4])))
+                cases[-1]["taps"].append((int(f[1]), float(f[2]), float(f[3]),
+                                          [float(v) for v in f[4:]]))
             elif f[0] == "weights":
-                queries.append(([float(v) for v in f[1:10]], f[10] == "softmax", float(f[11])))
-    return grid, taps, queries
+                cases[-1]["weights"].append(([float(v) for v in f[1:10]], f[10] == "softmax",
+                                             [float(v) for v in f[11:]]))
+    return cases
 
 
 def pin_attn_golden(orc):
-    """Hand-derived samples and weighted sums at output pixel (0, 0) of a
-    2x3 map, 3x3 taps, padding 1 (tests/golden/attn_samples.txt): each tap
-    alone (a one-hot weight) gives its sample, exactly, and each weight
-    vector its sum."""
-    (H, W, vals), taps, queries = _golden()
-    K = 9
-    value = torch.tensor(vals, dtype=torch.float32).view(1, H, W, 1, 1)
-    off = torch.zeros(1, H, W, 1, K, 2)          # 3x3, stride 1, padding 1: Ho, Wo = H, W
-    for k, dy, dx, _ in taps:
-        off[0, 0, 0, 0, k, 0], off[0, 0, 0, 0, k, 1] = dy, dx
-    for k, dy, dx, sample in taps:
-        w = torch.zeros(1, H, W, 1, K)
-        w[0, 0, 0, 0, k] = 1.0
-        got = float(orc.attn_forward(value, off, w, 3, 1, 1, 1, False)[0, 0, 0, 0, 0])
-        assert got == sample, f"tap {k} with offset ({dy}, {dx}): {got} != {sample}"
-    for weights, softmax, expected in queries:
-        w = torch.zeros(1, H, W, 1, K)
-        w[0, 0, 0, 0] = torch.tensor(weights)
-        got = float(orc.attn_forward(value, off, w, 3, 1, 1, 1, softmax)[0, 0, 0, 0, 0])
-        assert abs(got - expected) <= 1e-12 * max(1.0, abs(expected)), \
-            f"weights {weights} softmax={softmax}: {got} != {expected}"
+    """Hand-derived samples and weighted sums at one output pixel per case
+    (tests/golden/attn_samples.txt): each tap alone (a one-hot weight) gives
+    its sample in every group, exactly, and each weight vector its sum."""
+    for n, c in enumerate(_golden()):
+        H, W, G, K = c["H"], c["W"], c["G"], 9
+        kernel, stride, padding, dilation = (3, 3), c["stride"], c["padding"], c["dilation"]
+        Ho = _out_size(H, 3, stride[0], padding[0], dilation[0])
+        Wo = _out_size(W, 3, stride[1], padding[1], dilation[1])
+        h, w = c["pixel"]
+        value = torch.stack([torch.tensor(c["maps"][g], dtype=torch.float32).view(H, W)
+                             for g in range(G)], dim=-1).view(1, H, W, G, 1)
+        off = torch.zeros(1, Ho, Wo, G, K, 2)
+        for k, dy, dx, _ in c["taps"]:
+            off[0, h, w, :, k, 0], off[0, h, w, :, k, 1] = dy, dx
+        for k, dy, dx, samples in c["taps"]:
+            a = torch.zeros(1, Ho, Wo, G, K)
+            a[0, h, w, :, k] = 1.0
+            got = orc.attn_forward(value, off, a, kernel, stride, padding, dilation, False)
+            for g in range(G):
+                v = float(got[0, h, w, g, 0])
+                assert v == samples[g], f"case {n + 1} tap {k} group {g}: {v} != {samples[g]}"
+        for weights, softmax, expected in c["weights"]:
+            a = torch.zeros(1, Ho, Wo, G, K)
+            a[0, h, w, :] = torch.tensor(weights)
+            got = orc.attn_forward(value, off, a, kernel, stride, padding, dilation, softmax)
+            for g in range(G):
+                v = float(got[0, h, w, g, 0])
+                assert abs(v - expected[g]) <= 1e-12 * max(1.0, abs(expected[g])), \
+                    f"case {n + 1} weights {weights} softmax={softmax} group {g}: {v} != {expected[g]}"
 
 
 ALL_ATTN_PINS = [pin_attn_depthwise_convolution, pin_attn_grid_sample, pin_attn_integer_offsets,
