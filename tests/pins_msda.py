@@ -10,7 +10,7 @@ library routine fix, independently of the oracle's own code.
   the constant (the weights sum to one);
 - one-hot weights on one level of a map whose levels hold different
   constants: that level's constant (catches level offsets and shapes);
-- hand-derived samples and weighted sums on a two-level map
+- hand-derived samples and weighted sums on a two-level map of two heads
   (tests/golden/msda_samples.txt), exact in binary.
 """
 
@@ -169,26 +169,32 @@ def _golden():
 def pin_msda_golden(orc):
     """Hand-derived samples and weighted sums (tests/golden/msda_samples.txt),
     exact in binary: each point alone (a one-hot weight) gives its sample,
-    and each query its weighted sum."""
+    and each query its weighted sum; head 1 holds ten times head 0's values
+    and gives ten times its results."""
     levels, points, queries = _golden()
     shapes = [[H, W] for H, W, _ in levels]
     starts, S = _starts(shapes)
-    L, K = len(levels), 2
-    value = torch.tensor([v for _, _, vals in levels for v in vals], dtype=torch.float32)
-    value = value.view(1, S, 1, 1)
-    loc = torch.zeros(1, 1, 1, L, K, 2)
+    L, K, G = len(levels), 2, 2
+    head0 = torch.tensor([v for _, _, vals in levels for v in vals], dtype=torch.float32)
+    value = torch.stack([head0, 10.0 * head0], dim=-1).view(1, S, G, 1)
+    loc = torch.zeros(1, 1, G, L, K, 2)
     for l, k, x, y, _ in points:
-        loc[0, 0, 0, l, k, 0], loc[0, 0, 0, l, k, 1] = x, y
+        loc[0, 0, :, l, k, 0], loc[0, 0, :, l, k, 1] = x, y
     for l, k, x, y, sample in points:
-        w = torch.zeros(1, 1, 1, L * K)
+        w = torch.zeros(1, 1, G, L * K)
         w[..., l * K + k] = 1.0
-        got = float(orc.msda_forward(value, shapes, starts, loc, w, False)[0, 0, 0, 0])
-        assert got == sample, f"point (level {l}, k {k}) at ({x}, {y}): {got} != {sample}"
+        got = orc.msda_forward(value, shapes, starts, loc, w, False)[0, 0, :, 0]
+        for g in range(G):
+            want = sample * 10.0 ** g
+            assert float(got[g]) == want, \
+                f"point (level {l}, k {k}) at ({x}, {y}) head {g}: {float(got[g])} != {want}"
     for weights, softmax, expected in queries:
-        w = torch.tensor(weights, dtype=torch.float32).view(1, 1, 1, L * K)
-        got = float(orc.msda_forward(value, shapes, starts, loc, w, softmax)[0, 0, 0, 0])
-        assert abs(got - expected) <= 1e-12 * max(1.0, abs(expected)), \
-            f"query {weights} softmax={softmax}: {got} != {expected}"
+        w = torch.tensor(weights, dtype=torch.float32).view(1, 1, 1, L * K).repeat(1, 1, G, 1)
+        got = orc.msda_forward(value, shapes, starts, loc, w, softmax)[0, 0, :, 0]
+        for g in range(G):
+            want = expected * 10.0 ** g
+            assert abs(float(got[g]) - want) <= 1e-12 * max(1.0, abs(want)), \
+                f"query {weights} softmax={softmax} head {g}: {float(got[g])} != {want}"
 
 
 ALL_MSDA_PINS = [pin_msda_grid_sample, pin_msda_pixel_centres, pin_msda_outside,
