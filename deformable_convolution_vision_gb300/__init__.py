@@ -81,6 +81,30 @@ def _pair(v, name):
     return v
 
 
+def _on_device_of(name):
+    """Run the wrapped entry point with the device of its tensor argument
+    ``name`` current: the C library launches on the current device, takes
+    the current device's stream by default and refuses a handle made on
+    another device, so a tensor on cuda:1 while cuda:0 is current would
+    otherwise reach the wrong GPU."""
+    import functools
+    import inspect
+
+    def wrap(fn):
+        sig = inspect.signature(fn)
+
+        @functools.wraps(fn)
+        def run(*args, **kwargs):
+            import torch
+            t = sig.bind_partial(*args, **kwargs).arguments.get(name)
+            if isinstance(t, torch.Tensor) and t.is_cuda:
+                with torch.cuda.device(t.device):
+                    return fn(*args, **kwargs)
+            return fn(*args, **kwargs)
+        return run
+    return wrap
+
+
 def _check_devices(device, **named):
     """Every given tensor (None is skipped) must live on ``device``: the
     kernels take raw device pointers and cannot tell a host or another
@@ -142,6 +166,7 @@ def _describe(x, offset, weight, stride, padding, dilation, mask):
     return ConvDesc(B, C, H, W, O, kh, kw, sh, sw, ph, pw, dh, dw, groups, G), Ho, Wo
 
 
+@_on_device_of("x")
 def deform_conv2d(x, offset, weight, bias=None, stride=1, padding=0, dilation=1, mask=None,
                   handle=None, out=None, stream=None):
     """Modulated deformable convolution forward on CUDA tensors, with
@@ -184,6 +209,7 @@ def deform_conv2d(x, offset, weight, bias=None, stride=1, padding=0, dilation=1,
     return out
 
 
+@_on_device_of("x")
 def deform_conv2d_backward(grad_out, x, offset, weight, stride=1, padding=0, dilation=1,
                            mask=None, bias=True, handle=None, stream=None):
     """Gradients of ``deform_conv2d`` given ``grad_out`` [B, O, Ho, Wo]
@@ -215,6 +241,7 @@ def deform_conv2d_backward(grad_out, x, offset, weight, stride=1, padding=0, dil
             "grad_bias": gb}
 
 
+@_on_device_of("value")
 def msda(value, shapes, starts, locations, weights, method=None, out=None, stream=None):
     """Multi-scale deformable attention forward (the deformops functional
     form): value [B, S, G, D] (float32/bfloat16/float16, contiguous),
@@ -249,6 +276,7 @@ def msda(value, shapes, starts, locations, weights, method=None, out=None, strea
     return out
 
 
+@_on_device_of("value")
 def msda_backward(grad_out, value, shapes, starts, locations, weights, method=None, stream=None):
     """Gradients of ``msda`` for the cotangent grad_out [B, Q, G, D] (value's
     dtype, contiguous): returns (grad_value [B, S, G, D], grad_locations
@@ -285,6 +313,7 @@ def msda_backward(grad_out, value, shapes, starts, locations, weights, method=No
     return gv, gl, gw
 
 
+@_on_device_of("value")
 def attn(value, offsets, weights, kernel_size, stride=1, padding=0, dilation=1, method=None,
          out=None, stream=None):
     """Single-scale deformable sampling (the deformops functional form attn,
@@ -321,6 +350,7 @@ def attn(value, offsets, weights, kernel_size, stride=1, padding=0, dilation=1, 
     return out
 
 
+@_on_device_of("value")
 def attn_backward(grad_out, value, offsets, weights, kernel_size, stride=1, padding=0, dilation=1,
                   method=None, stream=None):
     """Gradients of ``attn`` for the cotangent grad_out [B, Ho, Wo, G, D]
@@ -358,6 +388,7 @@ def attn_backward(grad_out, value, offsets, weights, kernel_size, stride=1, padd
     return gv, go, gw
 
 
+@_on_device_of("input")
 def deform_conv2d_nchw(input, offset, weight, bias=None, stride=1, padding=0, dilation=1,
                        mask=None, handle=None, stream=None):
     """torchvision's argument order and layouts: input [B, C, H, W] and the

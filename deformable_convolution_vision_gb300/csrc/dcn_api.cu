@@ -84,6 +84,20 @@ using dcn::within_index_limit;
 
 inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
+// A handle's workspace, status word and packed weight live on the device
+// that was current at dcn_create; an entry point that launches work refuses
+// the handle when another device is current (its pointers would reach
+// another GPU's memory).
+inline bool bad_handle(dcn_handle_t h) {
+    if (!h) return true;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return dev != h->device;
+}
+
 inline bool aligned(const void *p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
@@ -426,7 +440,7 @@ dcn_status_t dcn_destroy(dcn_handle_t h) {
 
 dcn_status_t dcn_pack_weight(dcn_handle_t h, const void *weight, int O, int C, int kh, int kw,
                              int dtype, void *stream) {
-    if (!h || !weight) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h) || !weight) return DCN_ERR_INVALID_ARG;
     if (!valid_dtype(dtype)) return DCN_ERR_INVALID_ARG;
     if (O <= 0 || C <= 0 || kh <= 0 || kw <= 0) return DCN_ERR_INVALID_ARG;
     if (!within_index_limit({O, C, kh, kw})) return DCN_ERR_INVALID_ARG;
@@ -439,7 +453,7 @@ dcn_status_t dcn_pack_weight(dcn_handle_t h, const void *weight, int O, int C, i
 
 dcn_status_t dcn_pack_weight_ex(dcn_handle_t h, const void *weight, const dcn_conv_desc_t *desc,
                                 int dtype, void *stream) {
-    if (!h || !weight || !desc) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h) || !weight || !desc) return DCN_ERR_INVALID_ARG;
     Conv c;
     dcn_status_t st = make_conv(*desc, dtype, &c);
     if (st != DCN_OK) return st;
@@ -451,7 +465,7 @@ dcn_status_t dcn_forward_packed(dcn_handle_t h, const void *x, const float *offs
                                 const float *mask, const float *bias, void *out,
                                 int B, int C, int H, int W, int O, int kh, int kw, int pad,
                                 int dtype, void *stream) {
-    if (!h) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h)) return DCN_ERR_INVALID_ARG;
     Conv c;
     dcn_status_t st = make_conv(page_desc(B, C, H, W, O, kh, kw, pad), dtype, &c);
     if (st != DCN_OK) return st;
@@ -463,7 +477,7 @@ dcn_status_t dcn_forward_packed(dcn_handle_t h, const void *x, const float *offs
 dcn_status_t dcn_forward_packed_ex(dcn_handle_t h, const void *x, const float *offset,
                                    const float *mask, const float *bias, void *out,
                                    const dcn_conv_desc_t *desc, int dtype, void *stream) {
-    if (!h || !desc) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h) || !desc) return DCN_ERR_INVALID_ARG;
     Conv c;
     dcn_status_t st = make_conv(*desc, dtype, &c);
     if (st != DCN_OK) return st;
@@ -491,7 +505,7 @@ dcn_status_t dcn_forward(dcn_handle_t h, const void *x, const float *offset, con
                          const void *weight, const float *bias, void *out,
                          int B, int C, int H, int W, int O, int kh, int kw, int pad,
                          int dtype, void *stream) {
-    if (!h) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h)) return DCN_ERR_INVALID_ARG;
     Conv c;
     dcn_status_t st = make_conv(page_desc(B, C, H, W, O, kh, kw, pad), dtype, &c);
     if (st != DCN_OK) return st;
@@ -501,7 +515,7 @@ dcn_status_t dcn_forward(dcn_handle_t h, const void *x, const float *offset, con
 dcn_status_t dcn_forward_ex(dcn_handle_t h, const void *x, const float *offset, const float *mask,
                             const void *weight, const float *bias, void *out,
                             const dcn_conv_desc_t *desc, int dtype, void *stream) {
-    if (!h || !desc) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h) || !desc) return DCN_ERR_INVALID_ARG;
     Conv c;
     dcn_status_t st = make_conv(*desc, dtype, &c);
     if (st != DCN_OK) return st;
@@ -669,7 +683,7 @@ dcn_status_t dcn_backward(dcn_handle_t h, const void *x, const float *offset, co
                           float *grad_offset, float *grad_mask, float *grad_weight,
                           float *grad_bias, int B, int C, int H, int W, int O, int kh, int kw,
                           int pad, int dtype, void *stream) {
-    if (!h) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h)) return DCN_ERR_INVALID_ARG;
     Conv c;
     dcn_status_t st = make_conv(page_desc(B, C, H, W, O, kh, kw, pad), dtype, &c);
     if (st != DCN_OK) return st;
@@ -682,7 +696,7 @@ dcn_status_t dcn_backward_ex(dcn_handle_t h, const void *x, const float *offset,
                              float *grad_x, float *grad_offset, float *grad_mask,
                              float *grad_weight, float *grad_bias, const dcn_conv_desc_t *desc,
                              int dtype, void *stream) {
-    if (!h || !desc) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h) || !desc) return DCN_ERR_INVALID_ARG;
     Conv c;
     dcn_status_t st = make_conv(*desc, dtype, &c);
     if (st != DCN_OK) return st;
@@ -873,7 +887,7 @@ int dcn_out_size(int n, int k, int stride, int pad, int dil) {
 }
 
 dcn_status_t dcn_sync_status(dcn_handle_t h, void *stream) {
-    if (!h) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h)) return DCN_ERR_INVALID_ARG;
     cudaStream_t s = as_stream(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return DCN_ERR_CUDA;
     unsigned word = 0;
@@ -892,7 +906,7 @@ dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset
                               const float *mask, const void *weight, const float *bias, void *out,
                               int B, int C, int H, int W, int O, int kh, int kw, int pad,
                               int dtype, void *stream) {
-    if (!h) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h)) return DCN_ERR_INVALID_ARG;
     Conv c;
     dcn_status_t st = make_conv(page_desc(B, C, H, W, O, kh, kw, pad), dtype, &c);
     if (st != DCN_OK) return st;
@@ -978,41 +992,60 @@ dcn_status_t dcn_forward_host(dcn_handle_t h, const void *x, const float *offset
     float *smask = static_cast<float *>(h->stage[2]);
     uint8_t *sout = static_cast<uint8_t *>(h->stage[5]);
     const uint8_t *hx = static_cast<const uint8_t *>(x);
-    for (int b = 0; b < B; ++b) {
-        if (cudaMemcpyAsync(sx + b * img_x, hx + b * img_x, img_x, cudaMemcpyHostToDevice, s) != cudaSuccess)
-            return DCN_ERR_CUDA;
-        for (int h0 = 0; h0 < static_cast<int>(Ho);) {
-            int r = static_cast<int>(Ho) - h0 < rows ? static_cast<int>(Ho) - h0 : rows;
-            // the last band (at most last_rows) ends the call sooner
-            if (last_rows > 0 && static_cast<int>(Ho) - h0 - r < last_rows && static_cast<int>(Ho) - h0 > last_rows)
-                r = static_cast<int>(Ho) - h0 - last_rows;
-            // this band's rows of every offset and mask plane of image b
-            const size_t first = static_cast<size_t>(h0) * Wo;
-            const size_t off0 = static_cast<size_t>(b) * 2 * taps * plane + first;
-            if (cudaMemcpy2DAsync(soff + off0, plane * 4, offset + off0, plane * 4, r * Wo * 4, 2 * taps,
-                                  cudaMemcpyHostToDevice, s) != cudaSuccess)
+    bool queued = false;   // work sits on the pipeline streams
+    auto run_bands = [&]() -> dcn_status_t {
+        for (int b = 0; b < B; ++b) {
+            if (cudaMemcpyAsync(sx + b * img_x, hx + b * img_x, img_x, cudaMemcpyHostToDevice, s) != cudaSuccess)
                 return DCN_ERR_CUDA;
-            const size_t m0 = static_cast<size_t>(b) * taps * plane + first;
-            if (mask && cudaMemcpy2DAsync(smask + m0, plane * 4, mask + m0, plane * 4, r * Wo * 4, taps,
-                                          cudaMemcpyHostToDevice, s) != cudaSuccess)
-                return DCN_ERR_CUDA;
-            if (cudaEventRecord(h->ev_in, s) != cudaSuccess ||
-                cudaStreamWaitEvent(h->s_kernel, h->ev_in, 0) != cudaSuccess)
-                return DCN_ERR_CUDA;
-            const Band band = {h0, r, static_cast<int>(plane)};
-            const size_t out0 = (static_cast<size_t>(b) * Ho + h0) * Wo * O * es;
-            st = forward_packed_impl(h, sx + b * img_x, soff + off0, mask ? smask + m0 : nullptr,
-                                     bias ? static_cast<const float *>(h->stage[4]) : nullptr,
-                                     sout + out0, c1, dtype, h->s_kernel, false, &band);
-            if (st != DCN_OK) return st;
-            if (cudaEventRecord(h->ev_k, h->s_kernel) != cudaSuccess ||
-                cudaStreamWaitEvent(h->s_down, h->ev_k, 0) != cudaSuccess)
-                return DCN_ERR_CUDA;
-            if (cudaMemcpyAsync(static_cast<uint8_t *>(out) + out0, sout + out0, r * Wo * O * es,
-                                cudaMemcpyDeviceToHost, h->s_down) != cudaSuccess)
-                return DCN_ERR_CUDA;
-            h0 += r;
+            for (int h0 = 0; h0 < static_cast<int>(Ho);) {
+                int r = static_cast<int>(Ho) - h0 < rows ? static_cast<int>(Ho) - h0 : rows;
+                // the last band (at most last_rows) ends the call sooner
+                if (last_rows > 0 && static_cast<int>(Ho) - h0 - r < last_rows && static_cast<int>(Ho) - h0 > last_rows)
+                    r = static_cast<int>(Ho) - h0 - last_rows;
+                // this band's rows of every offset and mask plane of image b
+                const size_t first = static_cast<size_t>(h0) * Wo;
+                const size_t off0 = static_cast<size_t>(b) * 2 * taps * plane + first;
+                if (cudaMemcpy2DAsync(soff + off0, plane * 4, offset + off0, plane * 4, r * Wo * 4, 2 * taps,
+                                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+                    return DCN_ERR_CUDA;
+                const size_t m0 = static_cast<size_t>(b) * taps * plane + first;
+                if (mask && cudaMemcpy2DAsync(smask + m0, plane * 4, mask + m0, plane * 4, r * Wo * 4, taps,
+                                              cudaMemcpyHostToDevice, s) != cudaSuccess)
+                    return DCN_ERR_CUDA;
+                if (cudaEventRecord(h->ev_in, s) != cudaSuccess ||
+                    cudaStreamWaitEvent(h->s_kernel, h->ev_in, 0) != cudaSuccess)
+                    return DCN_ERR_CUDA;
+                const Band band = {h0, r, static_cast<int>(plane)};
+                const size_t out0 = (static_cast<size_t>(b) * Ho + h0) * Wo * O * es;
+                queued = true;
+                const dcn_status_t bs = forward_packed_impl(h, sx + b * img_x, soff + off0, mask ? smask + m0 : nullptr,
+                                         bias ? static_cast<const float *>(h->stage[4]) : nullptr,
+                                         sout + out0, c1, dtype, h->s_kernel, false, &band);
+                if (bs != DCN_OK) return bs;
+                if (cudaEventRecord(h->ev_k, h->s_kernel) != cudaSuccess ||
+                    cudaStreamWaitEvent(h->s_down, h->ev_k, 0) != cudaSuccess)
+                    return DCN_ERR_CUDA;
+                if (cudaMemcpyAsync(static_cast<uint8_t *>(out) + out0, sout + out0, r * Wo * O * es,
+                                    cudaMemcpyDeviceToHost, h->s_down) != cudaSuccess)
+                    return DCN_ERR_CUDA;
+                h0 += r;
+            }
         }
+        return DCN_OK;
+    };
+    st = run_bands();
+    if (st != DCN_OK) {
+        // An error part way: earlier bands' kernels and downloads may still
+        // be queued on the pipeline streams and read the staging buffers.
+        // Make `stream` wait for both, so the next call's uploads and any
+        // reallocation on `stream` come after them.
+        if (queued) {
+            if (cudaEventRecord(h->ev_k, h->s_kernel) == cudaSuccess)
+                cudaStreamWaitEvent(s, h->ev_k, 0);
+            if (cudaEventRecord(h->ev_done, h->s_down) == cudaSuccess)
+                cudaStreamWaitEvent(s, h->ev_done, 0);
+        }
+        return st;
     }
     if (cudaEventRecord(h->ev_done, h->s_down) != cudaSuccess ||
         cudaStreamWaitEvent(s, h->ev_done, 0) != cudaSuccess)
@@ -1042,7 +1075,7 @@ dcn_status_t dcn_set_sample_precision(dcn_handle_t h, int mode) {
 }
 
 dcn_status_t dcn_selftest_timeout(dcn_handle_t h, long long timeout_ns, void *stream) {
-    if (!h || timeout_ns <= 0 || timeout_ns > 10000000000ll) return DCN_ERR_INVALID_ARG;
+    if (bad_handle(h) || timeout_ns <= 0 || timeout_ns > 10000000000ll) return DCN_ERR_INVALID_ARG;
     if (dcn::launch_selftest_timeout(h->status, static_cast<unsigned long long>(timeout_ns),
                                      as_stream(stream)) != cudaSuccess)
         return DCN_ERR_CUDA;

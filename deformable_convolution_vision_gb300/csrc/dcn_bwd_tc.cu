@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "dcn_attr_cache.h"
 #include "dcn_device.cuh"
 #include "dcn_kernels.h"
 
@@ -355,7 +356,8 @@ __global__ void pack_weight_bwd_kernel(const uint16_t *__restrict__ w, uint16_t 
         wt[static_cast<size_t>(row) * O + o] = w[(static_cast<size_t>(o) * C + c) * taps + tap];
 }
 
-int g_bwd_smem_set[2] = {0, 0};
+// the dynamic shared-memory limit set on each device, per operand type
+PerDeviceValue<> g_bwd_smem_set[2];
 
 }  // namespace
 
@@ -381,12 +383,13 @@ cudaError_t launch_bwd_data_tc(const BwdParams &p, const CUtensorMap &gmap,
     const BtLayout L = bt_layout(p.O);
     const int smem = L.total + 1024;
     auto kernel = p.f16 ? dcn_bwd_data_tc_kernel<true> : dcn_bwd_data_tc_kernel<false>;
-    int &set = g_bwd_smem_set[p.f16 ? 1 : 0];
-    if (set != smem) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        set = smem;
-    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = static_cast<cudaError_t>(g_bwd_smem_set[p.f16 ? 1 : 0].ensure(dev, smem, [&] {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    }));
+    if (e != cudaSuccess) return e;
     const int tiles = p.B * ((p.Ho + BT_TILE_H - 1) / BT_TILE_H) * ((p.Wo + BT_TILE_W - 1) / BT_TILE_W);
     const int grid = tiles < p.sm_count ? tiles : p.sm_count;
     kernel<<<grid, BT_THREADS, smem, stream>>>(gmap, wmap, p);
