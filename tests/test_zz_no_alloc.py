@@ -6,8 +6,12 @@ budget, loops where cudaMalloc/cudaFree would stall other streams).  Its
 scratch lives in fixed device arrays shared by every call, so this test
 calls it twice in a row, on different workloads that take different
 kernels, and checks each result against dcn_forward's within the parity
-tolerance.  It is collected last so that, if it fails, a run that stops at
-the first failure has already run every other test.
+tolerance and against the oracle.  A second test checks the entry
+point's contract itself: once the first calls on the device have loaded
+the kernels and looked up the scratch arrays, further calls change neither
+the device's free memory nor the memory torch's allocator holds.  It is
+collected last so that, if it fails, a run that stops at the first failure
+has already run every other test.
 """
 
 import numpy as np
@@ -15,6 +19,7 @@ import pytest
 import torch
 
 import deformable_convolution_vision_gb300 as dcn
+import oracle
 from deformable_convolution_vision_gb300 import binding
 from deformable_convolution_vision_gb300.inputs import WORKLOADS, make_inputs
 from tests.helpers import TOL, rel_err, to_device
@@ -51,13 +56,49 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row():
              WORKLOADS["decoder3x3"].with_(C=96, H=24, W=20, seed=95)]
     results = []
     for wl in cases:
-        d = to_device(make_inputs(wl))
-        results.append((wl, _with_handle(wl, d), _noalloc(wl, d)))
-    for wl, ref, got in results:
+        inp = make_inputs(wl)
+        d = to_device(inp)
+        results.append((wl, inp, _with_handle(wl, d), _noalloc(wl, d)))
+    for wl, inp, ref, got in results:
         g = got.float().cpu().numpy()
         assert np.isfinite(g).all(), wl.name
         err = rel_err(g, ref.float().cpu().numpy())
-        assert err <= TOL[wl.dtype], f"{wl.name}: {err:.3e}"
+        assert err <= TOL[wl.dtype], f"{wl.name}: {err:.3e} against dcn_forward"
+        want = oracle.forward(inp["x"], inp["offset"], inp["mask"], inp["weight"], inp["bias"],
+                              wl.pad)
+        err = rel_err(g, want)
+        assert err <= TOL[wl.dtype], f"{wl.name}: {err:.3e} against the oracle"
+
+
+def test_noalloc_allocates_nothing():
+    # the tensor-core and CUDA-core paths, inputs and outputs made up front
+    cases = [WORKLOADS["decoder3x3"].with_(H=40, W=36, seed=96), WORKLOADS["tiny"]]
+    prepared = []
+    for wl in cases:
+        d = to_device(make_inputs(wl))
+        out = torch.empty((wl.B, wl.O, wl.Ho, wl.Wo), dtype=d["x"].dtype, device="cuda",
+                          memory_format=torch.channels_last)
+        prepared.append((wl, d, out))
+
+    def call_all():
+        for wl, d, out in prepared:
+            dcn.binding.dcn_forward_noalloc(d["x"], d["offset"], d["mask"], d["weight"], d["bias"],
+                                            out, wl.B, wl.C, wl.H, wl.W, wl.O, wl.kh, wl.kw, wl.pad,
+                                            dcn.DCN_BF16 if wl.dtype == "bf16" else dcn.DCN_F32)
+
+    # the first calls may load the kernels and map the scratch arrays
+    call_all()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    held0 = torch.cuda.memory_allocated()
+    reserved0 = torch.cuda.memory_reserved()
+    for _ in range(5):
+        call_all()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"device free memory moved by {free0 - free1} bytes"
+    assert torch.cuda.memory_allocated() == held0
+    assert torch.cuda.memory_reserved() == reserved0
 
 
 def test_noalloc_rejects_weights_beyond_the_scratch():
