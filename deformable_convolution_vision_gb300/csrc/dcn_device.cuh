@@ -146,6 +146,38 @@ __device__ __forceinline__ void sts_v4_b32(uint32_t addr, uint32_t a, uint32_t b
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                  :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
+// (with a memory clobber: kept in order with the warp barriers around
+// the per-warp tables they write and read)
+__device__ __forceinline__ void sts_b32(uint32_t addr, uint32_t a) {
+    asm volatile("st.shared.b32 [%0], %1;" :: "r"(addr), "r"(a) : "memory");
+}
+__device__ __forceinline__ void sts_v4_b32_m(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ int lds_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ int4 lds_v4_s32_m(uint32_t addr) {
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint2 lds_v2_u32(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 lds_v4_f32(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
+}
 
 // Asynchronous 4-byte global -> shared copy; with valid == false nothing
 // is read and the destination is zero-filled.  The thread's copies are
@@ -288,6 +320,15 @@ __device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_
         : "memory");
 }
 
+// One repeat of the same shape: 16 lanes x 8 columns, r[0], r[1] to lane
+// taddr.lane + t/4, columns 2(t%4) + {0, 1}, and r[2], r[3] to lane
+// taddr.lane + 8 + t/4, the same columns.
+__device__ __forceinline__ void tmem_st_16x256b_x1(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                                   uint32_t r3) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};"
+                 :: "r"(taddr), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
+
 // Load 16 lanes x 64 columns (shape 16x256b, eight repeats of 8 columns):
 // the layout of tmem_st_16x256b_x4 over twice the columns.  Thread t gets,
 // in repeat r, r[4r], r[4r+1] from lane taddr.lane + t/4, columns
@@ -398,6 +439,18 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
     asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// A 32-bit word with its low (high) 16-bit half in both halves.
+__device__ __forceinline__ uint32_t splat_lo(uint32_t w) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %1, 0x1010;" : "=r"(d) : "r"(w));
+    return d;
+}
+__device__ __forceinline__ uint32_t splat_hi(uint32_t w) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %1, 0x3232;" : "=r"(d) : "r"(w));
     return d;
 }
 

@@ -66,4 +66,56 @@ __device__ __forceinline__ void tap_corners(float dy, float dx, float m, int y_b
     t.idx[3] = t.idx[2] + dxc;
 }
 
+// The same sample read as a 2 x 2 block of pixels that always lies inside
+// the image: rows yb, yb + sy and columns xb, xb + sx with sy = (H > 1),
+// sx = (W > 1).  Each corner inside the image falls on one of the block's
+// four slots and carries its weight there; a slot that no inside corner
+// falls on has weight 0.  No slot receives two corners, so the slot weights
+// are the corner weights of tap_corners, each moved to the slot of its
+// pixel, and a weighted sum over the slots equals the one over the corners.
+// The block's fixed shape lets a reader form the four addresses from one
+// index and two per-launch steps.
+struct TapBlock {
+    float w[4];    // slots (0,0), (0,sx), (sy,0), (sy,sx); mask folded in
+    int idx;       // element offset of slot (0,0)'s channel row in x
+};
+
+// One axis: coordinate q in [-2, n+1] -> block start b in [0, max(n-2, 0)]
+// and the weights of slots b and b + 1 (slot b + 1 only when n > 1).
+__device__ __forceinline__ void axis_block(float q, int n, int &b, float &w0, float &w1) {
+    const float f = floorf(q);
+    const float l = q - f;
+    const int i0 = static_cast<int>(f);          // corners i0 (weight 1 - l) and i0 + 1 (weight l)
+    b = min(max(i0, 0), max(n - 2, 0));
+    // corner i0 lies on slot d = i0 - b: d == 0 puts both corners inside, on
+    // slots 0 and 1; d == -1 (i0 = -1) leaves corner i0 + 1 on slot 0;
+    // d == 1 (i0 = n - 1) leaves corner i0 on slot 1; otherwise both are outside
+    const int d = i0 - b;
+    const float u = 1.0f - l;
+    w0 = d == 0 ? u : (d == -1 ? l : 0.0f);
+    w1 = d == 0 ? l : (d == 1 ? u : 0.0f);
+    if (n == 1) w1 = 0.0f;                       // no second slot: corner i0 + 1 is outside
+}
+
+__device__ __forceinline__ void tap_block(float dy, float dx, float m, int y_base, int x_base,
+                                          int b, int H, int W, int cstride, TapBlock &t) {
+    float py = static_cast<float>(y_base) + dy;
+    float px = static_cast<float>(x_base) + dx;
+    // as in tap_corners: the clamp changes no result and keeps the integer
+    // conversion in range for huge or non-finite offsets
+    py = fminf(fmaxf(py, -2.0f), static_cast<float>(H + 1));
+    px = fminf(fmaxf(px, -2.0f), static_cast<float>(W + 1));
+    int yb, xb;
+    float wy0, wy1, wx0, wx1;
+    axis_block(py, H, yb, wy0, wy1);
+    axis_block(px, W, xb, wx0, wx1);
+    wy0 *= m;
+    wy1 *= m;
+    t.w[0] = wy0 * wx0;
+    t.w[1] = wy0 * wx1;
+    t.w[2] = wy1 * wx0;
+    t.w[3] = wy1 * wx1;
+    t.idx = ((b * H + yb) * W + xb) * cstride;
+}
+
 }  // namespace dcn

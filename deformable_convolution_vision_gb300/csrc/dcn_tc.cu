@@ -19,7 +19,7 @@
 //               K=16, A from TMEM, B from shared memory) x 4 per K-block,
 //               accumulating in TMEM, and commits each stage back to its
 //               "empty" barrier.
-//   warps 2..17 samplers, two teams of eight that take alternate K-blocks.
+//   warps 2..9  samplers, eight warps that each take every K-block.
 //               A sampler warp owns one tile row (16 pixels, TMEM lanes
 //               32q + 16h .. +15 of its lane quarter q).  Per (pixel, tap)
 //               it computes the corner weights and addresses (S1, S2); per
@@ -46,6 +46,7 @@
 // and the kernel winds down without trapping.
 #include <cuda_bf16.h>
 
+#include "dcn_attr_cache.h"
 #include "dcn_device.cuh"
 #include "dcn_kernels.h"
 #include "dcn_sampling.cuh"
@@ -59,9 +60,15 @@ constexpr int TC_BK = 64;                // channels per K-block
 constexpr int TC_MMA_K = 16;
 constexpr int TC_TILE_W = 16;                                 // tile = 8 x 16 output pixels
 constexpr int TC_TILE_H = TC_BM / TC_TILE_W;
-// Sampler teams: a team of eight warps covers the 128 rows of a K-block;
-// with two teams each takes every other K-block (more warps to hide
-// latency, fewer registers per thread).
+// Sampler teams: a team of eight warps covers the 128 rows of a K-block,
+// each warp one tile row of 16 pixels.  Two register budgets are built:
+//  - two teams (18 warps, at most 96 registers a thread) that take
+//    alternate K-blocks, each warp with the corner loads of its next
+//    K-block in flight while it waits for its stage;
+//  - one team (10 warps, 168 registers: three warps share a scheduler's
+//    16 K registers) whose warps take every K-block with the loads of the
+//    next two in flight, so every load has a whole K-block of the warp's
+//    own work to land in.
 #ifndef DCN_TC_TEAMS
 #define DCN_TC_TEAMS 2
 #endif
@@ -69,32 +76,35 @@ constexpr int TC_TEAMS = DCN_TC_TEAMS;
 static_assert(TC_TEAMS == 1 || TC_TEAMS == 2, "one or two sampler teams");
 constexpr int TC_TEAM_WARPS = 8;
 constexpr int TC_SAMPLER_WARPS = TC_TEAM_WARPS * TC_TEAMS;
+constexpr int TC_DEPTH = TC_TEAMS == 1 ? 2 : 1;               // K-blocks of loads in flight per warp
 constexpr int TC_EPI_PARTS = TC_SAMPLER_WARPS / 4;            // epilogue column parts per lane quarter
 constexpr int TC_CTRL_WARPS = 2;                              // TMA producer, MMA issuer
 constexpr int TC_THREADS = 32 * (TC_CTRL_WARPS + TC_SAMPLER_WARPS);
+constexpr int TC_MAX_REGS = TC_TEAMS == 1 ? 168 : 96;
 constexpr int TC_A_COLS = TC_BK / 2;                          // TMEM columns of one A stage
 constexpr int TC_TAP_GROUP = 32 / TC_TILE_W;                  // taps tabulated together (one per 16 lanes)
 constexpr int TC_TABLE_SLOTS = 2 * TC_TAP_GROUP;              // ring: one group in use, one ahead
 static_assert(TC_TEAM_WARPS * TC_TILE_W == TC_BM, "a team covers the tile");
-static_assert(TC_TABLE_SLOTS == 4, "ring index arithmetic assumes four slots");
+static_assert(TC_TABLE_SLOTS == 4 && TC_TAP_GROUP == 2, "ring index arithmetic assumes four slots");
 
-// Per-warp corner table of one tap: arrays of 16-byte rows, one row per
-// pixel of the warp's tile row (conflict-free writes, broadcast reads).
-// The fp32 combine keeps the weights as duplicated fp32 pairs
-// {w0,w0,w1,w1}, {w2,w2,w3,w3}; the 16-bit combine as four duplicated pairs.
-// Then the four corner indices.
-constexpr int TC_TABLE_ARRAY_BYTES = TC_TILE_W * 16;
-constexpr int TC_TABLE_W01 = 0;
-constexpr int TC_TABLE_W23 = TC_TABLE_ARRAY_BYTES;            // fp32 combine only
-__host__ __device__ constexpr int table_buf_bytes(bool f32) { return (f32 ? 3 : 2) * TC_TABLE_ARRAY_BYTES; }
-__host__ __device__ constexpr int table_idx_off(bool f32) { return (f32 ? 2 : 1) * TC_TABLE_ARRAY_BYTES; }
+// Per-warp sampling table of one tap: one 16-byte entry per pixel of the
+// warp's tile row in each of two arrays (conflict-free writes, broadcast
+// reads).  A sample is read as the clamped 2 x 2 block of tap_block: the
+// first array holds its four slot weights (mask folded in) -- for the
+// 16-bit combine each rounded to the operand type and duplicated into both
+// halves of a word, for the fp32 combine as fp32 -- and the second the
+// element index of its slot (0,0).
+constexpr int TC_ENTRY_ARRAY_BYTES = TC_TILE_W * 16;
+__host__ __device__ constexpr int table_buf_bytes(bool) { return 2 * TC_ENTRY_ARRAY_BYTES; }
+// raw geometry inputs of one lane: {dy, dx, m, -}
+constexpr int TC_RAW_WARP_BYTES = 32 * 16;
 
 struct TcLayout {
     int stages;
     int b_bytes;       // O * 128: one weight K-block
     int bar_off;       // barriers after the stages
     int table_off;     // per-warp corner tables
-    int raw_off;       // per-warp raw geometry inputs (dy, dx, mask) [3][32] fp32
+    int raw_off;       // per-warp raw geometry inputs, {dy, dx, mask, -} per lane
     int vt_off;        // virtual-tap table, int4 per (tap, offset group)
     int total;         // bytes used from the 1024-aligned base
 };
@@ -108,7 +118,7 @@ __host__ __device__ inline TcLayout tc_layout(int O, int stages, bool f32, int v
     L.table_off = L.bar_off + (2 * stages + 5) * 8;
     L.table_off = (L.table_off + 15) & ~15;
     L.raw_off = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_SLOTS * table_buf_bytes(f32);
-    L.vt_off = L.raw_off + TC_SAMPLER_WARPS * 3 * 32 * 4;
+    L.vt_off = L.raw_off + TC_SAMPLER_WARPS * TC_RAW_WARP_BYTES;
     L.total = L.vt_off + vtaps * 16;
     return L;
 }
@@ -158,12 +168,11 @@ __device__ __forceinline__ float4 ld_cg_f4(const float *p) {
     return __ldcg(reinterpret_cast<const float4 *>(p));
 }
 
-template <bool kSampleF32, bool kF16>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+template <bool kSampleF32, bool kF16, bool kOneBlock>
+__global__ void __maxnreg__(TC_MAX_REGS)
 dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     using E = Elem16<kF16>;   // the 16-bit operand type: its packed arithmetic and MMA format
     constexpr int kBuf = table_buf_bytes(kSampleF32);
-    constexpr int kIdx = table_idx_off(kSampleF32);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -306,14 +315,14 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     } else {
         // ------------------------------------------------ samplers
         const int sw = warp - TC_CTRL_WARPS;             // sampler warp 0 .. TC_SAMPLER_WARPS - 1
-        const int team = sw / TC_TEAM_WARPS;             // takes units u_begin + team + TC_TEAMS * i
         const int q = warp & 3;                          // TMEM lane quarter this warp may access
+        const int team = sw / TC_TEAM_WARPS;             // takes units u_begin + team + TC_TEAMS * i
         const int half = (sw % TC_TEAM_WARPS) / 4;       // which 16 lanes of the quarter
         const int trow = 2 * q + half;                   // its tile row = A rows 16 trow .. +15
         const uint16_t *__restrict__ x = static_cast<const uint16_t *>(p.x);   // 16-bit elements
-        uint8_t *table = smem + L.table_off + sw * TC_TABLE_SLOTS * kBuf;
-        const uint32_t table_s = smem_u32(table);
-        const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * 3 * 32 * 4) + lane * 4;
+        const uint32_t table_s = smem_u32(smem + L.table_off + sw * TC_TABLE_SLOTS * kBuf);
+        const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * TC_RAW_WARP_BYTES) + lane * 16;
+        const uint32_t vt_s = smem_u32(smem + L.vt_off);
         const uint32_t a_lane = static_cast<uint32_t>(16 * trow) << 16;
         const int plane = p.plane;                       // offset / mask plane stride
         const int my_g = lane >> 4;     // geometry: tap of the group
@@ -326,18 +335,12 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         const int chan_last = p.C - 16;
         const int rsub = lane >> 2;     // gather: pixels rsub and rsub + 8 of the row
         const uint32_t r_off0 = rsub * 16;
-        const uint32_t r_off1 = (rsub + 8) * 16;
-        // the sequence of taps a warp visits: every tap, or with two teams
-        // and one channel block per tap (alternate K-blocks = alternate
-        // taps) every other one
-        const int tap_shift = (TC_TEAMS == 2 && vncb == 1) ? 1 : 0;
-        // epilogue: TMEM lane quarter, column part, A row of this thread
-        const int part = sw >> 2;                        // 0 .. TC_EPI_PARTS - 1
-        const int erow = q * 32 + lane;
-        const int nch = p.O / 16;
-        const int ch_begin = part * nch / TC_EPI_PARTS;
-        const int ch_end = (part + 1) * nch / TC_EPI_PARTS;
-        const size_t part_floats = static_cast<size_t>(nch) * TC_BM * 16;   // one partial tile
+        constexpr uint32_t r_off1_rel = 8 * 16;                 // pixel rsub + 8's entry, after rsub's
+        // element steps from a sample block's slot (0,0) to slots (0,1) and (1,0)
+        const int step_x = p.W > 1 ? p.x_cstride : 0;
+        const int step_y = p.H > 1 ? p.W * p.x_cstride : 0;
+        // without a mask the lane's m word holds 1 for good (nothing copies over it)
+        if (p.mask == nullptr) sts_b32(raw_s + 8, __float_as_uint(1.0f));
         bool ok = true;
         int s = team;                   // this warp's stages: team, team + TC_TEAMS, ...
         uint32_t phase = 0;
@@ -345,6 +348,13 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         // Epilogue (S5) of segment e, the idx-th of this CTA: wait for its
         // accumulator, read it out, then tell the MMA warp it is free.
         auto epilogue = [&](const Segment &e, int idx) {
+            // TMEM lane quarter, column part, A row of this thread
+            const int part = sw >> 2;                        // 0 .. TC_EPI_PARTS - 1
+            const int erow = q * 32 + lane;
+            const int nch = p.O / 16;
+            const int ch_begin = part * nch / TC_EPI_PARTS;
+            const int ch_end = (part + 1) * nch / TC_EPI_PARTS;
+            const size_t part_floats = static_cast<size_t>(nch) * TC_BM * 16;   // one partial tile
             const int etb = e.tile / (tiles_x * tiles_y);
             const int erem = e.tile - etb * tiles_x * tiles_y;
             const int eth0 = (erem / tiles_x) * TC_TILE_H;
@@ -444,213 +454,290 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             // this warp's K-blocks: every TC_TEAMS-th from the first of its team
             const int seg_u0 = sg.tile * nkb + sg.kb0;
             const int kb_first = sg.kb0 + (team - (seg_u0 - u_begin) % TC_TEAMS + TC_TEAMS) % TC_TEAMS;
-
             if (kb_first < sg.kb1) {
                 const int my_h = th0 + trow;
                 const int my_w = tw0 + my_px;
                 const bool my_valid = (my_h < p.Ho) && (my_w < p.Wo);
                 const int my_hw = my_valid ? my_h * p.Wo + my_w : 0;
-                const int t_first = kb_first / vncb;
-                const int tap_par = tap_shift ? (t_first & 1) : 0;
-                // position of a tap in the warp's sequence, and back
-                auto seq_of = [&](int tap) { return tap >> tap_shift; };
-                auto tap_of = [&](int sq) { return (sq << tap_shift) + tap_par; };
-                const int sq0 = seq_of(t_first);
-                const int g0 = sq0 & ~(TC_TAP_GROUP - 1);    // its group of two
+                // the image's first offset and mask planes
+                const float *off_img = p.offset + static_cast<size_t>(tb) * p.off_bstride * plane;
+                const float *mask_img = p.mask ? p.mask + static_cast<size_t>(tb) * p.mask_bstride * plane
+                                               : p.offset;
+                const int y_base = (p.h0 + my_h) * p.sh;
+                const int x_base = my_w * p.sw;
+                const int n = (sg.kb1 - kb_first + TC_TEAMS - 1) / TC_TEAMS;   // this warp's K-blocks
+                const uint32_t tl = table_s + r_off0;           // this lane's first entry in slot 0
 
-                // raw inputs (dy, dx, mask) of this lane's next tap, copied a
-                // whole group ahead of their use into the warp's raw slot
-                // (asynchronously: no registers held while in flight)
-                auto load_raw = [&](int group_sq) {
-                    const int vt = tap_of(group_sq + my_g);
+                // Raw inputs (dy, dx, mask) of virtual tap vt for this lane's
+                // pixel, copied ahead of their use into the lane's raw slot
+                // (asynchronously: no registers held while in flight).
+                auto load_raw = [&](int vt) {
                     const bool valid = my_valid && vt < vtaps;
-                    const int mc = valid ? vt_tab[vt].z : 0;   // mask plane; offsets 2*mc, 2*mc + 1
-                    const float *o = valid
-                        ? p.offset + (static_cast<size_t>(tb) * p.off_bstride + 2 * mc) * plane + my_hw
-                        : p.offset;
+                    const int mc = valid ? lds_s32(vt_s + vt * 16 + 8) : 0;   // mask plane; offsets 2mc, 2mc + 1
+                    const float *o = off_img + (2 * mc * plane + my_hw);
 #ifdef DCN_CHECK_BOUNDS
                     // an offset or mask outside its tensor is not fetched (zero)
                     const bool v_dy = valid && in_bounds(o, 4, p.off_lo, p.off_hi, p.status);
                     const bool v_dx = valid && in_bounds(o + plane, 4, p.off_lo, p.off_hi, p.status);
                     cp_async_4(raw_s, v_dy ? o : p.offset, v_dy);
-                    cp_async_4(raw_s + 128, v_dx ? o + plane : o, v_dx);
+                    cp_async_4(raw_s + 4, v_dx ? o + plane : p.offset, v_dx);
+                    if (p.mask) {
+                        const float *mp = mask_img + (mc * plane + my_hw);
+                        const bool v_m = valid && in_bounds(mp, 4, p.mask_lo, p.mask_hi, p.status);
+                        cp_async_4(raw_s + 8, v_m ? mp : p.mask, v_m);
+                    }
 #else
                     cp_async_4(raw_s, o, valid);
-                    cp_async_4(raw_s + 128, valid ? o + plane : o, valid);
+                    cp_async_4(raw_s + 4, o + plane, valid);
+                    if (p.mask) cp_async_4(raw_s + 8, mask_img + (mc * plane + my_hw), valid);
 #endif
-                    if (p.mask) {
-                        const float *mp = valid
-                            ? p.mask + (static_cast<size_t>(tb) * p.mask_bstride + mc) * plane + my_hw
-                            : p.mask;
-#ifdef DCN_CHECK_BOUNDS
-                        const bool v_m = valid && in_bounds(mp, 4, p.mask_lo, p.mask_hi, p.status);
-                        cp_async_4(raw_s + 256, v_m ? mp : p.mask, v_m);
-#else
-                        cp_async_4(raw_s + 256, mp, valid);
-#endif
-                    }
                 };
-                // corner tables of the group's two virtual taps (ring slot sq % 4)
-                auto tabulate = [&](int group_sq) {
-                    const int sq = group_sq + my_g;
-                    const int vt = tap_of(sq);
-                    TapCorners t;
+                // The table entry of virtual tap vt for this lane's pixel, in
+                // ring slot `slot`, from the raw inputs loaded for it.  A tap
+                // past the last one gets an entry that is never read.
+                auto tabulate = [&](int vt, int slot) {
                     cp_async_wait_all();
-                    if (my_valid && vt < vtaps) {
-                        const int4 e = vt_tab[vt];
-                        const float dy = lds_f32(raw_s);
-                        const float dx = lds_f32(raw_s + 128);
-                        const float m = p.mask ? lds_f32(raw_s + 256) : 1.0f;
-                        tap_corners(dy, dx, m, (p.h0 + my_h) * p.sh + e.x, my_w * p.sw + e.y, tb, p.H, p.W,
-                                    p.x_cstride, t);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) { t.w[k] = 0.0f; t.idx[k] = 0; }
-                    }
-                    uint8_t *slot = table + (sq & (TC_TABLE_SLOTS - 1)) * kBuf;
-                    const int rowb = my_px * 16;
+                    const float4 r = lds_v4_f32(raw_s);       // dy, dx, m
+                    const int4 e = lds_v4_s32_m(vt_s + min(vt, vtaps - 1) * 16);
+                    TapBlock t;
+                    tap_block(r.x, r.y, r.z, y_base + e.x, x_base + e.y, tb, p.H, p.W, p.x_cstride, t);
+                    const uint32_t ent = table_s + slot * kBuf + my_px * 16;
                     if constexpr (kSampleF32) {
-                        *reinterpret_cast<float4 *>(slot + TC_TABLE_W01 + rowb) = make_float4(t.w[0], t.w[0], t.w[1], t.w[1]);
-                        *reinterpret_cast<float4 *>(slot + TC_TABLE_W23 + rowb) = make_float4(t.w[2], t.w[2], t.w[3], t.w[3]);
+                        sts_v4_b32_m(ent, __float_as_uint(t.w[0]), __float_as_uint(t.w[1]),
+                                     __float_as_uint(t.w[2]), __float_as_uint(t.w[3]));
                     } else {
-                        // the weights rounded to the operand type, each duplicated into a pair
-                        *reinterpret_cast<uint4 *>(slot + TC_TABLE_W01 + rowb) =
-                            make_uint4(E::splat(t.w[0]), E::splat(t.w[1]), E::splat(t.w[2]),
-                                       E::splat(t.w[3]));
+                        sts_v4_b32_m(ent, E::splat(t.w[0]), E::splat(t.w[1]), E::splat(t.w[2]), E::splat(t.w[3]));
                     }
-                    *reinterpret_cast<int4 *>(slot + kIdx + rowb) = make_int4(t.idx[0], t.idx[1], t.idx[2], t.idx[3]);
+                    sts_b32(ent + TC_ENTRY_ARRAY_BYTES, static_cast<uint32_t>(t.idx + e.w));
                 };
-                // the channel offset of virtual tap vt's block vcb in the launch
-                auto chan_off = [&](int vt, int vcb) {
-                    return (p.og_count == 1 ? 0 : vt_tab[vt].w) + vcb * TC_BK;
-                };
-                // the four 32-byte corner loads of one of this lane's two pixels
-                // from a table slot; corners outside the image read a clamped
-                // in-image address and carry weight 0
-                auto issue_px = [&](int px, uint32_t slot, int cofs, u32x8 (&v)[8]) {
-                    const uint16_t *xc = x + min(cofs + quart * 16, chan_last);
-                    const int4 ci = lds_v4_s32(slot + kIdx + (px ? r_off1 : r_off0));
-#ifdef DCN_CHECK_BOUNDS
-                    // a corner row outside x is read from x's first bytes instead
-                    auto chk = [&](const uint16_t *a) {
-                        return in_bounds(a, 32, p.x_lo, p.x_hi, p.status)
-                                   ? a : static_cast<const uint16_t *>(p.x_lo);
-                    };
-                    v[4 * px + 0] = ldg_v8(chk(xc + ci.x));
-                    v[4 * px + 1] = ldg_v8(chk(xc + ci.y));
-                    v[4 * px + 2] = ldg_v8(chk(xc + ci.z));
-                    v[4 * px + 3] = ldg_v8(chk(xc + ci.w));
-#else
-                    v[4 * px + 0] = ldg_v8(xc + ci.x);
-                    v[4 * px + 1] = ldg_v8(xc + ci.y);
-                    v[4 * px + 2] = ldg_v8(xc + ci.z);
-                    v[4 * px + 3] = ldg_v8(xc + ci.w);
-#endif
-                };
-
-                // Tables of the first two groups.  (The group after a group
-                // whose first tap ends inside the segment is tabulated when
-                // that tap ends; a warp that starts on a group's second tap
-                // never sees the first end, so its next group is tabulated
-                // here.)  Slots of the previous segment are free: this warp
-                // finished reading them.
-                load_raw(g0);
-                tabulate(g0);
-                if (tap_of(g0 + TC_TAP_GROUP) < vtaps) load_raw(g0 + TC_TAP_GROUP);
-                if (sq0 != g0 && tap_of(g0 + TC_TAP_GROUP) < vtaps) {
-                    tabulate(g0 + TC_TAP_GROUP);
-                    if (tap_of(g0 + 2 * TC_TAP_GROUP) < vtaps) load_raw(g0 + 2 * TC_TAP_GROUP);
-                }
-                __syncwarp();
-
-                // Rolling pipeline: the corner loads of a pixel's next K-block
-                // go out as soon as its current ones are combined.
-                u32x8 v[8];
-                int tap = t_first, cb = kb_first - t_first * vncb;   // virtual tap and its block
-                {
-                    const uint32_t slot = table_s + (seq_of(tap) & (TC_TABLE_SLOTS - 1)) * kBuf;
-                    issue_px(0, slot, chan_off(tap, cb), v);
-                    issue_px(1, slot, chan_off(tap, cb), v);
-                }
-
-                for (int kb = kb_first; ok && kb < sg.kb1; kb += TC_TEAMS) {
-                    const bool has_next = kb + TC_TEAMS < sg.kb1;
-                    int n_tap = tap, n_cb = cb + TC_TEAMS;
-                    // (at most TC_TEAMS carries: cb < ncb)
-                    if (n_cb >= vncb) { n_cb -= vncb; ++n_tap; }
-                    if (TC_TEAMS == 2 && n_cb >= vncb) { n_cb -= vncb; ++n_tap; }
-                    const int sq = seq_of(tap);
-                    const uint32_t cur_slot = table_s + (sq & (TC_TABLE_SLOTS - 1)) * kBuf;
-
-                    // every lane waits; the warp leaves the loop together if any lane ran out
-                    const bool got = mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns, 2000u);
-                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                    // TMEM writes after the MMAs that read this stage
-                    tc_fence_after_sync();
-
-                    // The stage row of both pixels, 16 words in the order of one
-                    // 16x256b.x4 store: w[4k], w[4k+1] are words 2k, 2k+1 (channels
-                    // 4k .. 4k+3 of the lane's 16) of the first pixel, w[4k+2],
-                    // w[4k+3] those of the second.
-                    uint32_t w[16];
+                // The corner-row loads of both of this lane's pixels from the
+                // entries in ring slot `slot`: each sample block's four slots
+                // from the index of its slot (0,0), every one inside the image.
+                // xl is x advanced by the lane's channel offset.
+                auto issue = [&](const uint16_t *xl, int slot, u32x8 (&v)[8]) {
+                    const uint32_t ent = tl + slot * kBuf + TC_ENTRY_ARRAY_BYTES;
 #pragma unroll
                     for (int px = 0; px < 2; ++px) {
-                        const uint32_t ro = px ? r_off1 : r_off0;
-                        const u32x8 *vp = v + 4 * px;
-                        if constexpr (kSampleF32) {
-                            uint64_t c0, c1, c2, c3;   // {w_q, w_q} fp32 pairs
-                            lds_v2_u64(cur_slot + TC_TABLE_W01 + ro, c0, c1);
-                            lds_v2_u64(cur_slot + TC_TABLE_W23 + ro, c2, c3);
+                        const int e0 = lds_s32(ent + (px ? r_off1_rel : 0u));
+                        const int e1 = e0 + step_x;
+                        const int e2 = e0 + step_y;
+                        const int e3 = e2 + step_x;
+#ifdef DCN_CHECK_BOUNDS
+                        // a corner row outside x is read from x's first bytes instead
+                        auto chk = [&](const uint16_t *a) {
+                            return in_bounds(a, 32, p.x_lo, p.x_hi, p.status)
+                                       ? a : static_cast<const uint16_t *>(p.x_lo);
+                        };
+                        v[4 * px + 0] = ldg_v8(chk(xl + e0));
+                        v[4 * px + 1] = ldg_v8(chk(xl + e1));
+                        v[4 * px + 2] = ldg_v8(chk(xl + e2));
+                        v[4 * px + 3] = ldg_v8(chk(xl + e3));
+#else
+                        v[4 * px + 0] = ldg_v8(xl + e0);
+                        v[4 * px + 1] = ldg_v8(xl + e1);
+                        v[4 * px + 2] = ldg_v8(xl + e2);
+                        v[4 * px + 3] = ldg_v8(xl + e3);
+#endif
+                    }
+                };
+                // Wait for the current stage, combine the loaded corners with
+                // the weights in ring slot `slot` and store the stage row of
+                // both pixels (S3), 16 words in the order of one 16x256b.x4
+                // store: w[4k], w[4k+1] are words 2k, 2k+1 (channels 4k .. 4k+3
+                // of the lane's 16) of the first pixel, w[4k+2], w[4k+3] those
+                // of the second.
+                auto combine_store = [&](int slot, const u32x8 (&v)[8]) -> bool {
+                    // every lane waits; the warp leaves together if any lane ran out
+                    const bool got = mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns, 2000u);
+                    if (!__all_sync(0xffffffffu, got)) return false;
+                    // TMEM writes after the MMAs that read this stage
+                    tc_fence_after_sync();
+                    // the weights of both pixels
+                    const uint32_t taddr = tmem_base + a_lane + a_col0 + s * TC_A_COLS;
+                    if constexpr (kSampleF32) {
+                        uint64_t c[2][4];
 #pragma unroll
-                            for (int m = 0; m < 8; ++m) {
-                                // channels 2m, 2m+1: w0*x00 + w1*x01 + w2*x10 + w3*x11 in fp32
-                                uint64_t acc = f2_mul(c0, f2_make(E::lo(vp[0].w[m]), E::hi(vp[0].w[m])));
-                                acc = f2_fma(c1, f2_make(E::lo(vp[1].w[m]), E::hi(vp[1].w[m])), acc);
-                                acc = f2_fma(c2, f2_make(E::lo(vp[2].w[m]), E::hi(vp[2].w[m])), acc);
-                                acc = f2_fma(c3, f2_make(E::lo(vp[3].w[m]), E::hi(vp[3].w[m])), acc);
-                                w[4 * (m >> 1) + 2 * px + (m & 1)] = E::pack_f2(acc);
-                            }
-                        } else {
-                            // the same sum in the input dtype: 16-bit weights, one
-                            // rounding per fused multiply-add, two channels per op
-                            const int4 cw = lds_v4_s32(cur_slot + TC_TABLE_W01 + ro);
+                        for (int px = 0; px < 2; ++px) {
+                            const float4 cw = lds_v4_f32(tl + slot * kBuf + (px ? r_off1_rel : 0u));
+                            c[px][0] = f2_make(cw.x, cw.x); c[px][1] = f2_make(cw.y, cw.y);
+                            c[px][2] = f2_make(cw.z, cw.z); c[px][3] = f2_make(cw.w, cw.w);
+                        }
+                        // repeat k of the 16x256b store: words 2k, 2k+1 of both pixels
 #pragma unroll
-                            for (int m = 0; m < 8; ++m) {
-                                uint32_t acc = E::mul(cw.x, vp[0].w[m]);
-                                acc = E::fma(cw.y, vp[1].w[m], acc);
-                                acc = E::fma(cw.z, vp[2].w[m], acc);
-                                acc = E::fma(cw.w, vp[3].w[m], acc);
-                                w[4 * (m >> 1) + 2 * px + (m & 1)] = acc;
+                        for (int k = 0; k < 4; ++k) {
+                            uint32_t r[4];
+#pragma unroll
+                            for (int px = 0; px < 2; ++px) {
+                                const u32x8 *vp = v + 4 * px;
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const int m = 2 * k + h;
+                                    // channels 2m, 2m+1: the four slots' weighted sum in fp32
+                                    uint64_t acc = f2_mul(c[px][0], f2_make(E::lo(vp[0].w[m]), E::hi(vp[0].w[m])));
+                                    acc = f2_fma(c[px][1], f2_make(E::lo(vp[1].w[m]), E::hi(vp[1].w[m])), acc);
+                                    acc = f2_fma(c[px][2], f2_make(E::lo(vp[2].w[m]), E::hi(vp[2].w[m])), acc);
+                                    acc = f2_fma(c[px][3], f2_make(E::lo(vp[3].w[m]), E::hi(vp[3].w[m])), acc);
+                                    r[2 * px + h] = E::pack_f2(acc);
+                                }
                             }
+                            tmem_st_16x256b_x1(taddr + 8 * k, r[0], r[1], r[2], r[3]);
+                        }
+                    } else {
+                        const int4 cw0 = lds_v4_s32_m(tl + slot * kBuf);
+                        const int4 cw1 = lds_v4_s32_m(tl + slot * kBuf + r_off1_rel);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint32_t r[4];
+#pragma unroll
+                            for (int px = 0; px < 2; ++px) {
+                                const u32x8 *vp = v + 4 * px;
+                                const int4 cw = px ? cw1 : cw0;
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    // the same sum in the input dtype: 16-bit weights, one
+                                    // rounding per fused multiply-add, two channels per op
+                                    const int m = 2 * k + h;
+                                    uint32_t acc = E::mul(cw.x, vp[0].w[m]);
+                                    acc = E::fma(cw.y, vp[1].w[m], acc);
+                                    acc = E::fma(cw.z, vp[2].w[m], acc);
+                                    acc = E::fma(cw.w, vp[3].w[m], acc);
+                                    r[2 * px + h] = acc;
+                                }
+                            }
+                            tmem_st_16x256b_x1(taddr + 8 * k, r[0], r[1], r[2], r[3]);
                         }
                     }
-                    tmem_st_16x256b_x4(tmem_base + a_lane + a_col0 + s * TC_A_COLS, w);
-
-                    // The corner data is consumed.  If the first tap of a group
-                    // is done, the slots of the previous group are no longer
-                    // read: fill them with the next group and fetch the one
-                    // after.  The next K-block's tap is in the current group, so
-                    // its slot is untouched.  Then the next K-block's loads.
-                    if (has_next && n_tap != tap && (sq & (TC_TAP_GROUP - 1)) == 0 &&
-                        tap_of(sq + TC_TAP_GROUP) < vtaps) {
-                        tabulate(sq + TC_TAP_GROUP);
-                        if (tap_of(sq + 2 * TC_TAP_GROUP) < vtaps) load_raw(sq + 2 * TC_TAP_GROUP);
-                    }
-                    if (has_next) {
-                        const uint32_t n_slot = table_s + (seq_of(n_tap) & (TC_TABLE_SLOTS - 1)) * kBuf;
-                        issue_px(0, n_slot, chan_off(n_tap, n_cb), v);
-                        issue_px(1, n_slot, chan_off(n_tap, n_cb), v);
-                    }
+                    return true;
+                };
+                // This stage's row is written: release it to the MMA warp.
+                auto finish_stage = [&]() {
                     tmem_wait_st();
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(full0 + 8 * s);
-
-                    tap = n_tap;
-                    cb = n_cb;
                     s += TC_TEAMS;
                     if (s >= stages) { s -= stages; phase ^= 1; }
+                };
+                // The loads of this warp's next TC_DEPTH K-blocks are in flight
+                // while one is combined; with two in flight va and vb alternate.
+                u32x8 va[8], vb[8];   // (vb unused with one K-block in flight)
+                u32x8 (&v_odd)[8] = TC_DEPTH == 2 ? vb : va;
+
+                if constexpr (kOneBlock) {
+                    // One channel block per virtual tap: this warp's K-block jj
+                    // of the segment is virtual tap t0 + TC_TEAMS * jj, its table
+                    // in ring slot jj % 4.  Taps are tabulated in pairs of the
+                    // warp's sequence {2g, 2g + 1} (slots 2g % 4 and 2g % 4 + 1,
+                    // one per half-warp), so in a body unrolled by four K-blocks
+                    // every slot is a constant.  The lane's channel offset is
+                    // fixed.
+                    const int t0 = kb_first;
+                    const uint16_t *xl = x + min(quart * 16, chan_last);
+                    auto load_pair = [&](int g) { load_raw(t0 + TC_TEAMS * (2 * g + my_g)); };
+                    auto tab_pair = [&](int g) {
+                        tabulate(t0 + TC_TEAMS * (2 * g + my_g), (2 * g + my_g) & (TC_TABLE_SLOTS - 1));
+                    };
+                    load_pair(0);
+                    tab_pair(0);
+                    if (2 < n) { load_pair(1); tab_pair(1); }
+                    if (4 < n) load_pair(2);
+                    __syncwarp();
+                    issue(xl, 0, va);
+                    if constexpr (TC_DEPTH == 2) {
+                        if (n > 1) issue(xl, 1, vb);
+                    }
+                    // K-block jj = base + k in ring slot k; at an even k (past the
+                    // segment's first K-block) the pair after next is tabulated
+                    // into the slots the last pair used; then the loads of
+                    // K-block jj + TC_DEPTH.
+                    auto step = [&](int jj, int k, u32x8 (&v)[8]) -> bool {
+                        if (!combine_store(k, v)) return false;
+                        if ((k & 1) == 0 && jj > 0 && jj + 2 < n) {
+                            const int g = jj / 2 + 1;
+                            tab_pair(g);
+                            if (2 * g + 2 < n) load_pair(g + 1);
+                            __syncwarp();
+                        }
+                        if (jj + TC_DEPTH < n) issue(xl, (k + TC_DEPTH) & (TC_TABLE_SLOTS - 1), v);
+                        finish_stage();
+                        return true;
+                    };
+                    for (int jj = 0; jj < n; jj += 4) {
+                        if (!step(jj, 0, va)) { ok = false; break; }
+                        if (jj + 1 >= n) break;
+                        if (!step(jj + 1, 1, v_odd)) { ok = false; break; }
+                        if (jj + 2 >= n) break;
+                        if (!step(jj + 2, 2, va)) { ok = false; break; }
+                        if (jj + 3 >= n) break;
+                        if (!step(jj + 3, 3, v_odd)) { ok = false; break; }
+                    }
+                } else {
+                    // Several channel blocks per virtual tap (every warp visits
+                    // every tap): K-block (vt, cb), the table of vt in ring slot
+                    // vt % 4, taps tabulated in pairs {2G, 2G + 1} (slots 2G % 4,
+                    // 2G % 4 + 1).
+                    const int t_first = kb_first / vncb;
+                    auto load_group = [&](int g) { load_raw(g + my_g); };
+                    auto tab_group = [&](int g) { tabulate(g + my_g, (g + my_g) & (TC_TABLE_SLOTS - 1)); };
+                    const int g0 = t_first & ~(TC_TAP_GROUP - 1);
+                    load_group(g0);
+                    tab_group(g0);
+                    if (g0 + TC_TAP_GROUP < vtaps) {
+                        load_group(g0 + TC_TAP_GROUP);
+                        tab_group(g0 + TC_TAP_GROUP);
+                    }
+                    if (g0 + 2 * TC_TAP_GROUP < vtaps) load_group(g0 + 2 * TC_TAP_GROUP);
+                    __syncwarp();
+                    // advance a K-block (vt, cb) by TC_TEAMS blocks (at most
+                    // TC_TEAMS carries: cb < vncb)
+                    auto advance = [&](int &t, int &c) {
+                        c += TC_TEAMS;
+                        if (c >= vncb) { c -= vncb; ++t; }
+                        if (TC_TEAMS == 2 && c >= vncb) { c -= vncb; ++t; }
+                    };
+                    int vt = t_first, cb = kb_first - t_first * vncb;   // this warp's K-block jj
+                    int vtn = vt, cbn = cb;                             // K-block jj + TC_DEPTH
+                    for (int d = 0; d < TC_DEPTH; ++d) advance(vtn, cbn);
+                    int vt_prev = vt;
+                    // x advanced by the lane's channel offset in block c
+                    auto x_at = [&](int c) { return x + min(c * TC_BK + quart * 16, chan_last); };
+                    issue(x_at(cb), vt & (TC_TABLE_SLOTS - 1), va);
+                    if constexpr (TC_DEPTH == 2) {
+                        if (n > 1) {
+                            int vt1 = vt, cb1 = cb;
+                            advance(vt1, cb1);
+                            issue(x_at(cb1), vt1 & (TC_TABLE_SLOTS - 1), vb);
+                        }
+                    }
+                    auto step = [&](int jj, u32x8 (&v)[8]) -> bool {
+                        if (!combine_store(vt & (TC_TABLE_SLOTS - 1), v)) return false;
+                        // Entering an even virtual tap (other than at the
+                        // segment's start): the previous group's slots are no
+                        // longer read, so fill them with the next group and fetch
+                        // the one after.
+                        if (vt != vt_prev && (vt & (TC_TAP_GROUP - 1)) == 0 && vt + TC_TAP_GROUP < vtaps) {
+                            tab_group(vt + TC_TAP_GROUP);
+                            if (vt + 2 * TC_TAP_GROUP < vtaps) load_group(vt + 2 * TC_TAP_GROUP);
+                            __syncwarp();
+                        }
+                        // the corner data is consumed: the loads of K-block jj + TC_DEPTH
+                        if (jj + TC_DEPTH < n) issue(x_at(cbn), vtn & (TC_TABLE_SLOTS - 1), v);
+                        finish_stage();
+                        vt_prev = vt;
+                        advance(vt, cb);
+                        advance(vtn, cbn);
+                        return true;
+                    };
+                    for (int jj = 0; jj < n; jj += TC_DEPTH) {
+                        if (!step(jj, va)) { ok = false; break; }
+                        if constexpr (TC_DEPTH == 2) {
+                            if (jj + 1 < n && !step(jj + 1, vb)) { ok = false; break; }
+                        }
+                    }
                 }
+                // raw copies issued for taps past the segment's end must land
+                // before the next segment reuses the raw slot
+                cp_async_wait_all();
             }
 
           }
@@ -670,9 +757,9 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     }
 }
 
-// The dynamic shared-memory size last set on each instantiation
-// [fp32 combine][fp16 operands].
-int g_max_smem_set[2][2] = {{0, 0}, {0, 0}};
+// The dynamic shared-memory size last set on each device for each
+// instantiation [fp32 combine][fp16 operands][one channel block per tap].
+PerDeviceValue<> g_max_smem_set[2][2][2];
 
 // Carveout preference (percent of the 228 KB maximum) that selects the
 // smallest supported shared-memory size holding `needed` bytes; the driver
@@ -761,19 +848,27 @@ cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t 
     const TcLayout L = tc_layout(p.O, stages, f32, vtaps);
     const int smem = L.total + 1024;  // slack for 1024-byte alignment
     const bool f16 = p.f16 != 0;
-    auto kernel = f32 ? (f16 ? dcn_tc_kernel<true, true> : dcn_tc_kernel<true, false>)
-                      : (f16 ? dcn_tc_kernel<false, true> : dcn_tc_kernel<false, false>);
-    int &smem_set = g_max_smem_set[f32 ? 1 : 0][f16 ? 1 : 0];
-    if (smem != smem_set) {
+    // one channel block per virtual tap: the unrolled walk
+    const bool one = ncb / p.og_count == 1;
+    using KernelFn = void (*)(const CUtensorMap, Params, int);
+    static const KernelFn kKernels[2][2][2] = {
+        {{dcn_tc_kernel<false, false, false>, dcn_tc_kernel<false, false, true>},
+         {dcn_tc_kernel<false, true, false>, dcn_tc_kernel<false, true, true>}},
+        {{dcn_tc_kernel<true, false, false>, dcn_tc_kernel<true, false, true>},
+         {dcn_tc_kernel<true, true, false>, dcn_tc_kernel<true, true, true>}}};
+    const KernelFn kernel = kKernels[f32 ? 1 : 0][f16 ? 1 : 0][one ? 1 : 0];
+    int dev = 0;
+    cudaError_t ae = cudaGetDevice(&dev);
+    if (ae != cudaSuccess) return ae;
+    ae = static_cast<cudaError_t>(g_max_smem_set[f32 ? 1 : 0][f16 ? 1 : 0][one ? 1 : 0].ensure(dev, smem, [&] {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         // ask for just enough shared memory for the one resident CTA (plus
         // the 1 KB the system reserves per CTA); the rest stays L1
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 carveout_percent(smem + 1024));
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    carveout_percent(smem + 1024));
+    }));
+    if (ae != cudaSuccess) return ae;
     const int tiles = p.B * ((p.Ho + TC_TILE_H - 1) / TC_TILE_H) * ((p.Wo + TC_TILE_W - 1) / TC_TILE_W);
     const int nkb = p.kh * p.kw * ncb;
     const long long total = static_cast<long long>(tiles) * nkb;
