@@ -95,7 +95,7 @@ static_assert(TC_TABLE_SLOTS == 4 && TC_TAP_GROUP == 2, "ring index arithmetic a
 // halves of a word, for the fp32 combine as fp32 -- and the second the
 // element index of its slot (0,0).
 constexpr int TC_ENTRY_ARRAY_BYTES = TC_TILE_W * 16;
-__host__ __device__ constexpr int table_buf_bytes(bool) { return 2 * TC_ENTRY_ARRAY_BYTES; }
+__host__ __device__ constexpr int table_buf_bytes(bool f32) { return (f32 ? 2 : 1) * TC_ENTRY_ARRAY_BYTES; }
 // raw geometry inputs of one lane: {dy, dx, m, -}
 constexpr int TC_RAW_WARP_BYTES = 32 * 16;
 
@@ -505,17 +505,18 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     if constexpr (kSampleF32) {
                         sts_v4_b32_m(ent, __float_as_uint(t.w[0]), __float_as_uint(t.w[1]),
                                      __float_as_uint(t.w[2]), __float_as_uint(t.w[3]));
+                        sts_b32(ent + TC_ENTRY_ARRAY_BYTES, static_cast<uint32_t>(t.idx + e.w));
                     } else {
-                        sts_v4_b32_m(ent, E::splat(t.w[0]), E::splat(t.w[1]), E::splat(t.w[2]), E::splat(t.w[3]));
+                        sts_v4_b32_m(ent, E::pack(t.w[0], t.w[1]), E::pack(t.w[2], t.w[3]),
+                                     static_cast<uint32_t>(t.idx + e.w), 0u);
                     }
-                    sts_b32(ent + TC_ENTRY_ARRAY_BYTES, static_cast<uint32_t>(t.idx + e.w));
                 };
                 // The corner-row loads of both of this lane's pixels from the
                 // entries in ring slot `slot`: each sample block's four slots
                 // from the index of its slot (0,0), every one inside the image.
                 // xl is x advanced by the lane's channel offset.
                 auto issue = [&](const uint16_t *xl, int slot, u32x8 (&v)[8]) {
-                    const uint32_t ent = tl + slot * kBuf + TC_ENTRY_ARRAY_BYTES;
+                    const uint32_t ent = tl + slot * kBuf + (kSampleF32 ? TC_ENTRY_ARRAY_BYTES : 8);
 #pragma unroll
                     for (int px = 0; px < 2; ++px) {
                         const int e0 = lds_s32(ent + (px ? r_off1_rel : 0u));
@@ -546,7 +547,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 // store: w[4k], w[4k+1] are words 2k, 2k+1 (channels 4k .. 4k+3
                 // of the lane's 16) of the first pixel, w[4k+2], w[4k+3] those
                 // of the second.
-                auto combine_store = [&](int slot, const u32x8 (&v)[8]) -> bool {
+                auto combine_store = [&](int slot, const u32x8 (&v)[8], uint2 p0, uint2 p1) -> bool {
                     // every lane waits; the warp leaves together if any lane ran out
                     const bool got = mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns, 2000u);
                     if (!__all_sync(0xffffffffu, got)) return false;
@@ -583,8 +584,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                             tmem_st_16x256b_x1(taddr + 8 * k, r[0], r[1], r[2], r[3]);
                         }
                     } else {
-                        const int4 cw0 = lds_v4_s32_m(tl + slot * kBuf);
-                        const int4 cw1 = lds_v4_s32_m(tl + slot * kBuf + r_off1_rel);
+                        const int4 cw0 = make_int4(splat_lo(p0.x), splat_hi(p0.x), splat_lo(p0.y), splat_hi(p0.y));
+                        const int4 cw1 = make_int4(splat_lo(p1.x), splat_hi(p1.x), splat_lo(p1.y), splat_hi(p1.y));
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             uint32_t r[4];
@@ -651,7 +652,10 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     // into the slots the last pair used; then the loads of
                     // K-block jj + TC_DEPTH.
                     auto step = [&](int jj, int k, u32x8 (&v)[8]) -> bool {
-                        if (!combine_store(k, v)) return false;
+                        // this K-block's weights, read before the stage wait
+                        const uint2 p0 = lds_v2_u32(tl + k * kBuf);
+                        const uint2 p1 = lds_v2_u32(tl + k * kBuf + r_off1_rel);
+                        if (!combine_store(k, v, p0, p1)) return false;
                         if ((k & 1) == 0 && jj > 0 && jj + 2 < n) {
                             const int g = jj / 2 + 1;
                             tab_pair(g);
@@ -710,7 +714,10 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                         }
                     }
                     auto step = [&](int jj, u32x8 (&v)[8]) -> bool {
-                        if (!combine_store(vt & (TC_TABLE_SLOTS - 1), v)) return false;
+                        const uint32_t cs = tl + (vt & (TC_TABLE_SLOTS - 1)) * kBuf;
+                        const uint2 p0 = lds_v2_u32(cs);
+                        const uint2 p1 = lds_v2_u32(cs + r_off1_rel);
+                        if (!combine_store(vt & (TC_TABLE_SLOTS - 1), v, p0, p1)) return false;
                         // Entering an even virtual tap (other than at the
                         // segment's start): the previous group's slots are no
                         // longer read, so fill them with the next group and fetch
