@@ -43,10 +43,9 @@ PAD_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("sample", [DCN_SAMPLE_INPUT_DTYPE, DCN_SAMPLE_F32])
 @pytest.mark.parametrize("wl", PAD_SHAPES, ids=lambda w: w.name)
-def test_padded_blocks_on_tensor_cores(wl, sample):
-    check(wl, expect_path=DCN_PATH_TC, sample=sample)
+def test_padded_blocks_on_tensor_cores(wl):
+    check(wl, expect_path=DCN_PATH_TC, samples=(DCN_SAMPLE_INPUT_DTYPE, DCN_SAMPLE_F32))
 
 
 @pytest.mark.parametrize("idx", [0, 3, 4, 6])

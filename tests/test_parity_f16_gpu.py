@@ -24,14 +24,15 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("name", ["decoder3x3", "aspp7x7", "backbone3x3", "boundary5x5"])
 def test_workload_f16(name):
-    check(WORKLOADS[name].with_(dtype="f16"), expect_path=DCN_PATH_TC)
+    # full size, compared on the seam-aimed pixels (the bf16 runs compare whole)
+    check(WORKLOADS[name].with_(dtype="f16"), expect_path=DCN_PATH_TC, full_limit=4e9)
 
 
-@pytest.mark.parametrize("sample", [DCN_SAMPLE_INPUT_DTYPE, DCN_SAMPLE_F32])
 @pytest.mark.parametrize("idx", [0, 1, 4, 7, 10, 12])
-def test_tc_shapes_f16(idx, sample):
+def test_tc_shapes_f16(idx):
     wl = TC_SHAPES[idx]
-    check(wl.with_(dtype="f16", name=wl.name + "_f16"), expect_path=DCN_PATH_TC, sample=sample)
+    check(wl.with_(dtype="f16", name=wl.name + "_f16"), expect_path=DCN_PATH_TC,
+          samples=(DCN_SAMPLE_INPUT_DTYPE, DCN_SAMPLE_F32))
 
 
 @pytest.mark.parametrize("path", [DCN_PATH_SIMT, DCN_PATH_TC])

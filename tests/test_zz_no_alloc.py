@@ -14,6 +14,8 @@ collected last so that, if it fails, a run that stops at the first failure
 has already run every other test.
 """
 
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -89,12 +91,16 @@ def test_noalloc_allocates_nothing():
     # the first calls may load the kernels and map the scratch arrays
     call_all()
     torch.cuda.synchronize()
+    # tensors of earlier tests that the garbage collector frees in between
+    # would move torch's own count: collect them first
+    gc.collect()
     free0, _ = torch.cuda.mem_get_info()
     held0 = torch.cuda.memory_allocated()
     reserved0 = torch.cuda.memory_reserved()
     for _ in range(5):
         call_all()
     torch.cuda.synchronize()
+    gc.collect()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0, f"device free memory moved by {free0 - free1} bytes"
     assert torch.cuda.memory_allocated() == held0
