@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 METRIC = "deform-conv fwd effective TFLOP/s & out-pixels/s on 1 GB300; % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+L2_NOTE = f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write), outside the timed events"
 MAIN_KERNEL = "dcn_tc_kernel"
 TC_SOURCES = ["dcn_tc.cu", "dcn_device.cuh", "dcn_sampling.cuh", "dcn_kernels.h"]
 
@@ -217,7 +218,9 @@ def run_reference(args, wl, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(wl, "no GPU: host caches only"),
+        # the same workload description as the GPU arm (the oracle runs on
+        # the host; the flush note of the GPU arm does not apply to it)
+        "config": config_dict(wl, L2_NOTE),
         "out_pixels_per_s": px / el,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{px} random output pixels x all {wl.O} channels over "
@@ -634,6 +637,27 @@ def run_ours(args, wl, rank, local_rank, world):
         raise RuntimeError("device status set during the split timing")
     main_ms = [e[1].elapsed_time(e[2]) for e in ev3]
     pack_ms = [e[0].elapsed_time(e[1]) for e in ev3]
+
+    # The fused kernel with the fp32 bilinear combine (the sampled value
+    # summed in fp32 and rounded once to the operand type, instead of the
+    # input-dtype combine of the page's routine): same flush and events.
+    main_f32 = None
+    if code != dcn.DCN_F32:
+        with dcn.Handle(sample=dcn.DCN_SAMPLE_F32) as hf:
+            dcn.dcn_pack_weight(hf.h, w, wl.O, wl.C, wl.kh, wl.kw, code, stream)
+            for _ in range(3):
+                flush.fill_(3)
+                dcn.dcn_forward_packed(hf.h, x, off, m, b, out, *dims, stream)
+            evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_split)]
+            for k in range(n_split):
+                flush.fill_(k & 0xFF)
+                evf[k][0].record(stream)
+                dcn.dcn_forward_packed(hf.h, x, off, m, b, out, *dims, stream)
+                evf[k][1].record(stream)
+            torch.cuda.synchronize(dev)
+            if dcn.dcn_sync_status(hf.h, stream) != 0:
+                raise RuntimeError("device status set during the fp32-combine timing")
+            main_f32 = statistics.fmean(e[0].elapsed_time(e[1]) for e in evf)
     ms = statistics.fmean(step_ms)
     ms_max = reduce_max(ms, world)
     main_mean = statistics.fmean(main_ms)
@@ -689,13 +713,15 @@ def run_ours(args, wl, rank, local_rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic",
-        "config": config_dict(wl, f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write), "
-                                  f"outside the timed events"),
+        "config": config_dict(wl, L2_NOTE),
         "out_pixels_per_s": whole_job_rate(wl.pixels, world, ms_max * 1e-3),
         "roofline_frac_step": max(t_tc, t_hbm) / (ms_max * 1e-3),
         "step_ms": {"mean": ms, "min": min(step_ms), "median": statistics.median(step_ms),
                     "pack_mean": statistics.fmean(pack_ms), "main_mean": main_mean,
                     "main_min": min(main_ms),
+                    "main_mean_f32_combine": main_f32,
+                    "main_f32_combine_note": "the fused kernel alone with the fp32 bilinear combine "
+                                             "(DCN_SAMPLE_F32); the headline uses the input-dtype combine",
                     "warm_l2_mean": warm_ms,
                     "warm_l2_note": "no flush between steps; not the reported value"},
         "roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "achieved": achieved,
