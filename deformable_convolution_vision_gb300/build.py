@@ -21,7 +21,7 @@ LIBRARY = os.path.join(HERE, "libdcn.so")
 CHECKED_LIBRARY = os.path.join(HERE, "libdcn_checked.so")
 
 SOURCES = ["dcn_api.cu", "dcn_simt.cu", "dcn_tc.cu", "dcn_noalloc.cu", "dcn_backward.cu",
-           "dcn_bwd_tc.cu", "dcn_msda.cu", "dcn_msda_bwd.cu", "dcn_attn.cu", "dcn_attn_bwd.cu",
+           "dcn_bwd_tc.cu", "dcn_bwd_wgrad_tc.cu", "dcn_msda.cu", "dcn_msda_bwd.cu", "dcn_attn.cu", "dcn_attn_bwd.cu",
            "dcn_layout.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -63,7 +63,7 @@ def build(verbose=False, extra=(), checked=False):
             sys.stderr.write(log)
     objs = [o for o, _ in results]
     tmp = out_lib + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"]
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

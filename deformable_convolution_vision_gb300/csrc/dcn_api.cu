@@ -7,7 +7,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <cublas_v2.h>
 
 #include <cstdint>
 #include <cstring>
@@ -41,16 +40,9 @@ struct dcn_handle_s {
     size_t flags_cap = 0;
     unsigned epoch = 0;
 
-    // backward on tensor cores: the weight packed as [kh*kw*C][O]; the
-    // weight gradient's sampled columns (one chunk of pixels), its
-    // [O][kh*kw*C/groups] fp32 result and the cuBLAS handle of its GEMM
+    // backward on tensor cores: the weight packed as [kh*kw*C][O]
     void *wpack_bwd = nullptr;
     size_t wpack_bwd_cap = 0;
-    void *cols = nullptr;
-    size_t cols_cap = 0;
-    void *wgrad = nullptr;
-    size_t wgrad_cap = 0;
-    cublasHandle_t cublas = nullptr;
 
     // dcn_forward_host's pipeline: a kernel stream, a download stream and
     // the events between them (created on first use)
@@ -422,9 +414,6 @@ dcn_status_t dcn_destroy(dcn_handle_t h) {
     if (h->partial) cudaFree(h->partial);
     if (h->flags) cudaFree(h->flags);
     if (h->wpack_bwd) cudaFree(h->wpack_bwd);
-    if (h->cols) cudaFree(h->cols);
-    if (h->wgrad) cudaFree(h->wgrad);
-    if (h->cublas) cublasDestroy(h->cublas);
     if (h->status) cudaFree(h->status);
     for (int i = 0; i < 6; ++i)
         if (h->stage[i]) cudaFree(h->stage[i]);
@@ -623,56 +612,10 @@ static dcn_status_t backward_general(dcn_handle_t h, const void *x, const float 
     }
     if (dcn::launch_bwd_data_tc(p, gmap, wmap, s) != cudaSuccess) return DCN_ERR_CUDA;
 
-    // The weight gradient: grad_weight[o, (tap, cl)] = sum_p grad_out[p, o] *
-    // cols[p, (tap, cl)] is a plain GEMM once the sampled columns exist.  They
-    // are written in the operand type by the library's sampler (chunks of at
-    // most 512 MiB), contracted by a cuBLAS GEMM (16-bit inputs, fp32
-    // accumulation and output, no TF32), then permuted into the weight's
-    // [O][C/groups][kh][kw] layout by the layout kernel.
-    const int Cg = c.Cg(), Og = c.Og(), Cq = c.Cq();
-    if (!(d.C % 8 == 0 && Cg % 8 == 0 && Cq % 8 == 0 && aligned(x, 16))) {
-        if (dcn::launch_backward_weight(p, dtype, s) != cudaSuccess) return DCN_ERR_CUDA;
-        h->last_path = path;
-        return DCN_OK;
-    }
-    const size_t row_bytes = taps * d.C * 2;
-    const long long P = static_cast<long long>(d.B) * c.Ho * c.Wo;
-    long long chunk = static_cast<long long>((512ull << 20) / row_bytes);
-    if (chunk < 1) chunk = 1;
-    if (chunk > P) chunk = P;
-    st = ensure(&h->cols, &h->cols_cap, static_cast<size_t>(chunk) * row_bytes, s);
-    if (st != DCN_OK) return st;
-    const size_t kg = taps * Cg;   // the GEMM's rows per weight group
-    st = ensure(&h->wgrad, &h->wgrad_cap, static_cast<size_t>(d.O) * kg * 4, s);
-    if (st != DCN_OK) return st;
-    if (!h->cublas && cublasCreate(&h->cublas) != CUBLAS_STATUS_SUCCESS) {
-        h->cublas = nullptr;
-        return DCN_ERR_CUDA;
-    }
-    if (cublasSetStream(h->cublas, s) != CUBLAS_STATUS_SUCCESS) return DCN_ERR_CUDA;
-    const cudaDataType ct = dtype == DCN_F16 ? CUDA_R_16F : CUDA_R_16BF;
-    const float one = 1.0f, zero = 0.0f;
-    const uint16_t *cols = static_cast<const uint16_t *>(h->cols);
-    const uint16_t *go = static_cast<const uint16_t *>(grad_out);
-    float *wg = static_cast<float *>(h->wgrad);
-    for (long long pix0 = 0; pix0 < P; pix0 += chunk) {
-        const int npix = static_cast<int>(P - pix0 < chunk ? P - pix0 : chunk);
-        if (dcn::launch_bwd_columns(p, dtype, h->cols, static_cast<int>(pix0), npix, s) != cudaSuccess)
-            return DCN_ERR_CUDA;
-        for (int g = 0; g < d.groups; ++g) {
-            // column-major view: C[kg x Og] (+)= cols_g[kg x npix] * grad_out_g[Og x npix]^T
-            if (cublasGemmEx(h->cublas, CUBLAS_OP_N, CUBLAS_OP_T, static_cast<int>(kg), Og, npix,
-                             &one, cols + g * kg, ct, static_cast<int>(d.groups * kg),
-                             go + pix0 * d.O + static_cast<size_t>(g) * Og, ct, d.O,
-                             pix0 == 0 ? &zero : &one, wg + static_cast<size_t>(g) * Og * kg,
-                             CUDA_R_32F, static_cast<int>(kg), CUBLAS_COMPUTE_32F,
-                             CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-                return DCN_ERR_CUDA;
-        }
-    }
-    // [O][kh*kw][Cg] -> [O][Cg][kh*kw]
-    if (dcn::launch_transpose(wg, grad_weight, d.O, static_cast<int>(taps), Cg, 4, s) != cudaSuccess)
-        return DCN_ERR_CUDA;
+    // The weight gradient on tensor cores: the sampled operand m * S of
+    // each 128-pixel tile is contracted with the grad_out tile as soon as it
+    // is sampled, in shared memory; fp32 accumulation in tensor memory.
+    if (dcn::launch_bwd_wgrad_tc(p, gmap, s) != cudaSuccess) return DCN_ERR_CUDA;
     if (grad_bias && dcn::launch_bwd_bias(p, dtype, s) != cudaSuccess) return DCN_ERR_CUDA;
     h->last_path = path;
     return DCN_OK;

@@ -264,12 +264,6 @@ dcn_bwd_data_kernel(BwdParams p) {
 
 // Eight consecutive elements as fp32: one 16-byte load for 16-bit types
 // (two for fp32) when `vec`, else element by element with a bound.
-template <typename T> __device__ __forceinline__ T from_f32_t(float v);
-template <> __device__ __forceinline__ __nv_bfloat16 from_f32_t<__nv_bfloat16>(float v) {
-    return __float2bfloat16_rn(v);
-}
-template <> __device__ __forceinline__ __half from_f32_t<__half>(float v) { return __float2half_rn(v); }
-
 template <typename T>
 __device__ __forceinline__ void load8(const T *src, int n_valid, bool vec, float (&v)[8]);
 template <>
@@ -491,123 +485,6 @@ cudaError_t launch_backward_weight_t(const BwdParams &p_in, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-// The sampled operand of the weight gradient, for pixels [pix0, pix0 +
-// npix): cols[pl][g][tap][cl] = m * S(pixel pix0 + pl, tap, channel
-// g * Cg + cl), rounded to the operand type T (the rounding the forward's
-// tensor-core contraction applies to the same operand).  One thread per 8
-// channels of a (pixel, tap), taps outermost: 16-byte corner loads and one
-// 16-byte store.
-// Requires C, C/groups and C/offset_groups multiples of 8 and x 16-byte
-// aligned.
-template <typename T>
-__global__ void __launch_bounds__(256)
-dcn_bwd_columns_kernel(BwdParams p, T *__restrict__ cols, int pix0, int npix) {
-    const T *__restrict__ x = static_cast<const T *>(p.x);
-    const int C8 = p.C / 8;
-    const int taps = p.kh * p.kw;
-    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (t >= static_cast<long long>(npix) * taps * C8) return;
-    // tap-major over the chunk's pixels: the threads of a block take one tap
-    // of neighbouring pixels, whose corner rows overlap (L1 hits)
-    const int c = static_cast<int>(t % C8) * 8;
-    const long long rest = t / C8;
-    const int pl = static_cast<int>(rest % npix);
-    const int tap = static_cast<int>(rest / npix);
-    const int pix = pix0 + pl;
-    const int Cg = p.C / p.groups, Cq = p.C / p.ogroups;
-    const int g = c / Cg, cl = c - g * Cg, q = c / Cq;
-    const int HoWo = p.Ho * p.Wo;
-    const int b = pix / HoWo;
-    const int hw = pix - b * HoWo;
-    const int h = hw / p.Wo, w = hw - (hw / p.Wo) * p.Wo;
-    const int i = tap / p.kw, j = tap - (tap / p.kw) * p.kw;
-    const Geo gg = geometry(p, b, h, w, i, j, q, tap);
-    const float wq[4] = {(1.0f - gg.ly) * (1.0f - gg.lx), (1.0f - gg.ly) * gg.lx,
-                         gg.ly * (1.0f - gg.lx), gg.ly * gg.lx};
-    float sv[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sv[e] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (gg.idx[k] < 0) continue;
-        float v[8];
-        load8(x + gg.idx[k] + c, 8, true, v);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sv[e] = fmaf(wq[k], v[e], sv[e]);
-    }
-    uint32_t pk[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        T lo = from_f32_t<T>(gg.m * sv[2 * e]), hi = from_f32_t<T>(gg.m * sv[2 * e + 1]);
-        uint16_t l16, h16;
-        memcpy(&l16, &lo, 2);
-        memcpy(&h16, &hi, 2);
-        pk[e] = static_cast<uint32_t>(l16) | (static_cast<uint32_t>(h16) << 16);
-    }
-    *reinterpret_cast<uint4 *>(cols + ((static_cast<size_t>(pl) * p.groups + g) * taps + tap) * Cg + cl) =
-        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-}
-
-// The same for 16 channels per thread (16-bit operands; C, C/groups and
-// C/offset_groups multiples of 16, x 32-byte aligned): one 32-byte load per
-// corner, four threads per 64-channel corner row (one 128-byte line), and
-// half as many threads repeating each (pixel, tap)'s geometry.  Measured
-// against the 8-channel kernel: the whole backward call 1590 -> 1445 us on
-// the 7x7 workload, 679 -> 626 us on the backbone 3x3.
-template <typename T>
-__global__ void __launch_bounds__(256)
-dcn_bwd_columns16_kernel(BwdParams p, T *__restrict__ cols, int pix0, int npix) {
-    const T *__restrict__ x = static_cast<const T *>(p.x);
-    const int C16 = p.C / 16;
-    const int taps = p.kh * p.kw;
-    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (t >= static_cast<long long>(npix) * taps * C16) return;
-    const int c = static_cast<int>(t % C16) * 16;
-    const long long rest = t / C16;
-    const int pl = static_cast<int>(rest % npix);
-    const int tap = static_cast<int>(rest / npix);
-    const int pix = pix0 + pl;
-    const int Cg = p.C / p.groups, Cq = p.C / p.ogroups;
-    const int g = c / Cg, cl = c - g * Cg, q = c / Cq;
-    const int HoWo = p.Ho * p.Wo;
-    const int b = pix / HoWo;
-    const int hw = pix - b * HoWo;
-    const int h = hw / p.Wo, w = hw - (hw / p.Wo) * p.Wo;
-    const int i = tap / p.kw, j = tap - (tap / p.kw) * p.kw;
-    const Geo gg = geometry(p, b, h, w, i, j, q, tap);
-    const float wq[4] = {(1.0f - gg.ly) * (1.0f - gg.lx), (1.0f - gg.ly) * gg.lx,
-                         gg.ly * (1.0f - gg.lx), gg.ly * gg.lx};
-    float sv[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) sv[e] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (gg.idx[k] < 0) continue;
-        const u32x8 r = ldg_v8(x + gg.idx[k] + c);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            T lo, hi;
-            const uint16_t l16 = static_cast<uint16_t>(r.w[e] & 0xFFFFu), h16 = static_cast<uint16_t>(r.w[e] >> 16);
-            memcpy(&lo, &l16, 2);
-            memcpy(&hi, &h16, 2);
-            sv[2 * e] = fmaf(wq[k], ld_f32(&lo), sv[2 * e]);
-            sv[2 * e + 1] = fmaf(wq[k], ld_f32(&hi), sv[2 * e + 1]);
-        }
-    }
-    uint32_t pk[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        T lo = from_f32_t<T>(gg.m * sv[2 * e]), hi = from_f32_t<T>(gg.m * sv[2 * e + 1]);
-        uint16_t l16, h16;
-        memcpy(&l16, &lo, 2);
-        memcpy(&h16, &hi, 2);
-        pk[e] = static_cast<uint32_t>(l16) | (static_cast<uint32_t>(h16) << 16);
-    }
-    uint4 *dst = reinterpret_cast<uint4 *>(cols + ((static_cast<size_t>(pl) * p.groups + g) * taps + tap) * Cg + cl);
-    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-}
-
 template <typename T>
 cudaError_t launch_backward_t(const BwdParams &p, cudaStream_t stream) {
     const dim3 grid((p.P + BWD_BM - 1) / BWD_BM, (p.C + BWD_BN - 1) / BWD_BN);
@@ -623,37 +500,6 @@ cudaError_t launch_backward(const BwdParams &p, int dtype, cudaStream_t stream) 
     if (dtype == kF32) return launch_backward_t<float>(p, stream);
     if (dtype == kF16) return launch_backward_t<__half>(p, stream);
     return launch_backward_t<__nv_bfloat16>(p, stream);
-}
-
-cudaError_t launch_bwd_columns(const BwdParams &p, int dtype, void *cols, int pix0, int npix,
-                               cudaStream_t stream) {
-    const bool c16 = (dtype == kF16 || dtype == kBF16) && p.C % 16 == 0 &&
-                     (p.C / p.groups) % 16 == 0 && (p.C / p.ogroups) % 16 == 0 &&
-                     (reinterpret_cast<uintptr_t>(p.x) & 31) == 0;
-    if (c16) {
-        const long long threads16 = static_cast<long long>(npix) * p.kh * p.kw * (p.C / 16);
-        const long long blocks16 = (threads16 + 255) / 256;
-        if (blocks16 > 2147483647ll) return cudaErrorInvalidValue;
-        if (dtype == kF16)
-            dcn_bwd_columns16_kernel<__half><<<static_cast<unsigned>(blocks16), 256, 0, stream>>>(
-                p, static_cast<__half *>(cols), pix0, npix);
-        else
-            dcn_bwd_columns16_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks16), 256, 0, stream>>>(
-                p, static_cast<__nv_bfloat16 *>(cols), pix0, npix);
-        return cudaGetLastError();
-    }
-    const long long threads = static_cast<long long>(npix) * p.kh * p.kw * (p.C / 8);
-    const long long blocks = (threads + 255) / 256;
-    if (blocks > 2147483647ll || p.C % 8) return cudaErrorInvalidValue;
-    if (dtype == kF16)
-        dcn_bwd_columns_kernel<__half><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            p, static_cast<__half *>(cols), pix0, npix);
-    else if (dtype == kBF16)
-        dcn_bwd_columns_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            p, static_cast<__nv_bfloat16 *>(cols), pix0, npix);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_bias(const BwdParams &p_in, int dtype, cudaStream_t stream) {

@@ -178,11 +178,12 @@ cudaError_t launch_bwd_data_tc(const BwdParams &p, const CUtensorMap &gmap,
                                const CUtensorMap &wmap, cudaStream_t stream);
 // grad_weight and grad_bias on CUDA cores (the second half of launch_backward).
 cudaError_t launch_backward_weight(const BwdParams &p, int dtype, cudaStream_t stream);
-// The weight gradient's sampled operand for pixels [pix0, pix0 + npix):
-// cols [npix][groups][kh*kw][C/groups] in the 16-bit operand type
-// (C, C/groups, C/offset_groups multiples of 8; x 16-byte aligned).
-cudaError_t launch_bwd_columns(const BwdParams &p, int dtype, void *cols, int pix0, int npix,
-                               cudaStream_t stream);
+// grad_weight on tensor cores (16-bit operands, one weight group, C and
+// C/offset_groups multiples of 64, O a multiple of 64 up to 256): the
+// sampled operand of each 128-pixel tile contracted with the grad_out tile
+// (`gmap`, the column-gradient kernel's map) in shared memory, fp32 in
+// tensor memory, added into grad_weight (which must be zeroed first).
+cudaError_t launch_bwd_wgrad_tc(const BwdParams &p, const CUtensorMap &gmap, cudaStream_t stream);
 // grad_bias alone (column sums of grad_out).
 cudaError_t launch_bwd_bias(const BwdParams &p, int dtype, cudaStream_t stream);
 

@@ -327,12 +327,13 @@ DCN_API dcn_status_t dcn_forward_packed_ex(dcn_handle_t h,
  * stream order).  Otherwise, and for fp32, CUDA cores run it and nothing is
  * allocated.  dcn_set_path(DCN_PATH_SIMT) forces the CUDA-core kernels;
  * DCN_PATH_TC returns DCN_ERR_UNSUPPORTED for shapes outside the envelope.
- * The weight gradient of 16-bit operands (C, C/groups, C/offset_groups
- * multiples of 8, x 16-byte aligned) samples its operand into a column
- * buffer in the handle's workspace (rounded to the operand type, at most
- * 512 MiB at a time) and contracts it with grad_out by a cuBLAS GEMM (fp32
- * accumulation, no TF32); otherwise a CUDA-core kernel computes it in fp32.
- * The bias gradient runs on CUDA cores.  Argument rules as
+ * In the same envelope the weight gradient runs on tcgen05 too: each
+ * 128-pixel tile of the sampled operand m * S (summed in fp32, rounded once
+ * to the operand type) is contracted with the grad_out tile in shared
+ * memory as soon as it is sampled, fp32 accumulation in tensor memory, no
+ * TF32; the sampled operand is never written to memory.  Otherwise a
+ * CUDA-core kernel computes it in fp32.  The bias gradient runs on CUDA
+ * cores.  Argument rules as
  * dcn_forward / dcn_forward_ex (sizes, NULL inputs, alignment to the
  * element size, 4 bytes for fp32 arrays); DCN_ERR_INVALID_ARG for a NULL x,
  * offset, weight, grad_out, grad_x, grad_offset or grad_weight. */
