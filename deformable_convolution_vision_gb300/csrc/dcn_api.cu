@@ -674,6 +674,11 @@ dcn_status_t dcn_msda_forward(const void *value, const int *shapes, const int *s
     p.value = value; p.locations = locations; p.weights = weights; p.out = out;
     p.B = B; p.S = S; p.G = G; p.D = D; p.Q = Q; p.K = K; p.L = L;
     p.softmax = softmax ? 1 : 0;
+#ifdef DCN_CHECK_BOUNDS
+    p.v_lo = value;
+    p.v_hi = static_cast<const char *>(value) + static_cast<size_t>(B) * S * G * D * es;
+    p.gv_lo = p.gv_hi = nullptr;
+#endif
     const bool vec = D % (dtype == DCN_F32 ? 4 : 8) == 0 && aligned(value, 16) && aligned(out, 16);
     if (dcn::launch_msda(p, dtype, vec, as_stream(stream)) != cudaSuccess) return DCN_ERR_CUDA;
     return DCN_OK;
@@ -712,6 +717,12 @@ dcn_status_t dcn_msda_backward(const void *value, const int *shapes, const int *
     p.grad_value = grad_value; p.grad_locations = grad_locations; p.grad_weights = grad_weights;
     p.B = B; p.S = S; p.G = G; p.D = D; p.Q = Q; p.K = K; p.L = L;
     p.softmax = softmax ? 1 : 0;
+#ifdef DCN_CHECK_BOUNDS
+    p.v_lo = value;
+    p.v_hi = static_cast<const char *>(value) + static_cast<size_t>(B) * S * G * D * es;
+    p.gv_lo = grad_value;
+    p.gv_hi = grad_value + static_cast<size_t>(B) * S * G * D;
+#endif
     cudaStream_t s = as_stream(stream);
     // the value gradient is a sum of reductions: start it at zero
     if (cudaMemsetAsync(grad_value, 0, static_cast<size_t>(B) * S * G * D * sizeof(float), s) !=
@@ -748,6 +759,11 @@ dcn_status_t dcn_attn_forward(const void *value, const float *offsets, const flo
     p.kh = kh; p.kw = kw; p.sh = stride_h; p.sw = stride_w; p.ph = pad_h; p.pw = pad_w;
     p.dh = dil_h; p.dw = dil_w;
     p.softmax = softmax ? 1 : 0;
+#ifdef DCN_CHECK_BOUNDS
+    p.v_lo = value;
+    p.v_hi = static_cast<const char *>(value) + static_cast<size_t>(B) * H * W * G * D * es;
+    p.gv_lo = p.gv_hi = nullptr;
+#endif
     const bool vec = D % (dtype == DCN_F32 ? 4 : 8) == 0 && aligned(value, 16) && aligned(out, 16);
     if (dcn::launch_attn(p, dtype, vec, as_stream(stream)) != cudaSuccess) return DCN_ERR_CUDA;
     return DCN_OK;
@@ -784,6 +800,12 @@ dcn_status_t dcn_attn_backward(const void *value, const float *offsets, const fl
     p.kh = kh; p.kw = kw; p.sh = stride_h; p.sw = stride_w; p.ph = pad_h; p.pw = pad_w;
     p.dh = dil_h; p.dw = dil_w;
     p.softmax = softmax ? 1 : 0;
+#ifdef DCN_CHECK_BOUNDS
+    p.v_lo = value;
+    p.v_hi = static_cast<const char *>(value) + static_cast<size_t>(B) * H * W * G * D * es;
+    p.gv_lo = grad_value;
+    p.gv_hi = grad_value + static_cast<size_t>(B) * H * W * G * D;
+#endif
     cudaStream_t s = as_stream(stream);
     // the value gradient is a sum of reductions: start it at zero
     if (cudaMemsetAsync(grad_value, 0, static_cast<size_t>(B) * H * W * G * D * sizeof(float), s) !=

@@ -82,6 +82,7 @@ attn_forward_kernel(AttnParams p) {
     const int y_base = ho * p.sh - p.ph;
     const int x_base = wo * p.sw - p.pw;
 
+    DCN_BAD_DECL;
     for (int c0 = r; c0 < nch; c0 += GRP) {
         float acc[CH];
 #pragma unroll
@@ -112,12 +113,16 @@ attn_forward_kernel(AttnParams p) {
                     if (!in) continue;
                 }
                 float v[CH];
-                row_load<T, CH>(vbase + static_cast<size_t>(in ? yy * p.W + xx : 0) * GD + c0 * CH, v);
+                row_load<T, CH>(DCN_ROW(vbase + static_cast<size_t>(in ? yy * p.W + xx : 0) * GD + c0 * CH, CH), v);
                 const float wc = in ? wq[c] : 0.0f;
 #pragma unroll
                 for (int e = 0; e < CH; ++e) acc[e] = fmaf(wc, v[e], acc[e]);
             }
         }
+#ifdef DCN_CHECK_BOUNDS
+#pragma unroll
+        for (int e = 0; e < CH; ++e) acc[e] = DCN_POISON(acc[e]);
+#endif
         if (live) attn_store<T, CH>(static_cast<T *>(p.out) + row * p.D + c0 * CH, acc);
     }
 }

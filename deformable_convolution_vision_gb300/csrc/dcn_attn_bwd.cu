@@ -111,6 +111,7 @@ attn_backward_kernel(AttnBwdParams p) {
     float go_d[CH];
     if constexpr (kOneChunk) row_load<T, CH>(go_row + r * CH, go_d);
 
+    DCN_BAD_DECL;
     float s_ag = 0.0f;   // sum over taps of a[k] * grad_a[k] (the same in every lane)
     for (int k = 0; k < K; ++k) {
         const int i = k / p.kw, j = k - (k / p.kw) * p.kw;
@@ -144,7 +145,7 @@ attn_backward_kernel(AttnBwdParams p) {
                     continue;
                 const size_t at = static_cast<size_t>(yy * p.W + xx) * GD;
                 float v[CH];
-                row_load<T, CH>(vbase + at + c0 * CH, v);
+                row_load<T, CH>(DCN_ROW(vbase + at + c0 * CH, CH), v);
                 float dot = 0.0f;
 #pragma unroll
                 for (int e = 0; e < CH; ++e) dot = fmaf(go[e], v[e], dot);
@@ -152,23 +153,24 @@ attn_backward_kernel(AttnBwdParams p) {
                 ga = fmaf(cw, dot, ga);
                 gy = fmaf(ay ? wx[ex] : -wx[ex], dot, gy);
                 gx = fmaf(ex ? wy[ay] : -wy[ay], dot, gx);
-                if (live) ab_red<CH>(gvbase + at + c0 * CH, a * cw, go);
+                if (live && DCN_GROW_OK(gvbase + at + c0 * CH, CH)) ab_red<CH>(gvbase + at + c0 * CH, a * cw, go);
             }
         }
         ga = ab_sum<GRP>(ga);
         gy = ab_sum<GRP>(gy);
         gx = ab_sum<GRP>(gx);
         s_ag = fmaf(a, ga, s_ag);
+        DCN_BAD_SYNC;
         if (live && r == k % GRP) {
-            go_ofs[k] = make_float2(a * gy, a * gx);
-            gw_row[k] = ga;
+            go_ofs[k] = make_float2(DCN_POISON(a * gy), DCN_POISON(a * gx));
+            gw_row[k] = DCN_POISON(ga);
         }
     }
     if (p.softmax && live) {
         // this lane's own entries, written above: grad_a -> a (grad_a - sum a grad_a)
         for (int k = r; k < K; k += GRP) {
             const float a = expf(__ldg(wrow + k) - wmax) * inv;
-            gw_row[k] = a * (gw_row[k] - s_ag);
+            gw_row[k] = DCN_POISON(a * (gw_row[k] - s_ag));
         }
     }
 }

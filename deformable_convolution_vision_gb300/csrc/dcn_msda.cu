@@ -61,6 +61,7 @@ msda_forward_kernel(MsdaParams p) {
     }
     const float inv = 1.0f / wsum;
 
+    DCN_BAD_DECL;
     float acc[CH];
 #pragma unroll
     for (int e = 0; e < CH; ++e) acc[e] = 0.0f;
@@ -106,7 +107,7 @@ msda_forward_kernel(MsdaParams p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float v[CH];
-                    row_load<T, CH>(value + ((level0 + off[u][c]) * p.G + g) * p.D + d0, v);
+                    row_load<T, CH>(DCN_ROW(value + ((level0 + off[u][c]) * p.G + g) * p.D + d0, CH), v);
 #pragma unroll
                     for (int e = 0; e < CH; ++e) acc[e] = fmaf(cw[u][c], v[e], acc[e]);
                 }
@@ -115,7 +116,7 @@ msda_forward_kernel(MsdaParams p) {
     }
     T *__restrict__ out = static_cast<T *>(p.out) + row * p.D + d0;
 #pragma unroll
-    for (int e = 0; e < CH; ++e) out[e] = round_to<T>(acc[e]);
+    for (int e = 0; e < CH; ++e) out[e] = round_to<T>(DCN_POISON(acc[e]));
 }
 
 // The same for a row group of GRP lanes (GRP = D / CH, a power of two that
@@ -158,6 +159,7 @@ msda_forward_group_kernel(MsdaParams p) {
     }
     const float inv = 1.0f / wsum;
 
+    DCN_BAD_DECL;
     float acc[CH];
 #pragma unroll
     for (int e = 0; e < CH; ++e) acc[e] = 0.0f;
@@ -203,7 +205,7 @@ msda_forward_group_kernel(MsdaParams p) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 float v[CH];
-                row_load<T, CH>(vbase + off[c], v);
+                row_load<T, CH>(DCN_ROW(vbase + off[c], CH), v);
 #pragma unroll
                 for (int e = 0; e < CH; ++e) acc[e] = fmaf(cw[c], v[e], acc[e]);
             }
@@ -212,7 +214,7 @@ msda_forward_group_kernel(MsdaParams p) {
     if (live) {
         T *__restrict__ out = static_cast<T *>(p.out) + row * p.D + d0;
 #pragma unroll
-        for (int e = 0; e < CH; ++e) out[e] = round_to<T>(acc[e]);
+        for (int e = 0; e < CH; ++e) out[e] = round_to<T>(DCN_POISON(acc[e]));
     }
 }
 

@@ -110,6 +110,7 @@ msda_backward_kernel(MsdaBwdParams p) {
     }
     const float inv = 1.0f / wsum;
 
+    DCN_BAD_DECL;
     float s_ag = 0.0f;   // sum over points of a[t] * grad_a[t] (the same in every lane)
     // one chunk per lane: its cotangent once, in the load order (go_d, for
     // the dot products) and in the reduction order (go_r, see above)
@@ -160,7 +161,7 @@ msda_backward_kernel(MsdaBwdParams p) {
                     const size_t pix = static_cast<size_t>(yy * W + xx) * GD;
                     const size_t off = pix + c0 * CH;
                     float v[CH];
-                    row_load<T, CH>(vlevel + off, v);
+                    row_load<T, CH>(DCN_ROW(vlevel + off, CH), v);
                     float dot = 0.0f;
 #pragma unroll
                     for (int e = 0; e < CH; ++e) dot = fmaf(go[e], v[e], dot);
@@ -173,10 +174,11 @@ msda_backward_kernel(MsdaBwdParams p) {
                             const float sc = a * cw;
                             float lo[4] = {go_r[0], go_r[1], go_r[2], go_r[3]};
                             float hi[4] = {go_r[4], go_r[5], go_r[6], go_r[7]};
-                            red_scaled<4>(glevel + pix + 4 * r, sc, lo);
-                            red_scaled<4>(glevel + pix + 4 * (r + GRP), sc, hi);
+                            if (DCN_GROW_OK(glevel + pix + 4 * r, 4)) red_scaled<4>(glevel + pix + 4 * r, sc, lo);
+                            if (DCN_GROW_OK(glevel + pix + 4 * (r + GRP), 4))
+                                red_scaled<4>(glevel + pix + 4 * (r + GRP), sc, hi);
                         } else {
-                            red_scaled<CH>(glevel + off, a * cw, go);
+                            if (DCN_GROW_OK(glevel + off, CH)) red_scaled<CH>(glevel + off, a * cw, go);
                         }
                     }
                 }
@@ -185,10 +187,11 @@ msda_backward_kernel(MsdaBwdParams p) {
             gpx = group_sum<GRP>(gpx);
             gpy = group_sum<GRP>(gpy);
             s_ag = fmaf(a, ga, s_ag);
+            DCN_BAD_SYNC;
             if (live && r == i % GRP) {
                 *reinterpret_cast<float2 *>(gl_row + 2 * i) =
-                    make_float2(a * gpx * static_cast<float>(W), a * gpy * static_cast<float>(H));
-                gw_row[i] = ga;
+                    make_float2(DCN_POISON(a * gpx * static_cast<float>(W)), DCN_POISON(a * gpy * static_cast<float>(H)));
+                gw_row[i] = DCN_POISON(ga);
             }
         }
     }
@@ -196,7 +199,7 @@ msda_backward_kernel(MsdaBwdParams p) {
         // this lane's own entries, written above: grad_a -> a (grad_a - sum a grad_a)
         for (int i = r; i < LK; i += GRP) {
             const float a = expf(__ldg(wrow + i) - wmax) * inv;
-            gw_row[i] = a * (gw_row[i] - s_ag);
+            gw_row[i] = DCN_POISON(a * (gw_row[i] - s_ag));
         }
     }
 }

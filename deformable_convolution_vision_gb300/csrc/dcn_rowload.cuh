@@ -101,4 +101,40 @@ template <> __device__ __forceinline__ __nv_bfloat16 round_to<__nv_bfloat16>(flo
 }
 template <> __device__ __forceinline__ __half round_to<__half>(float v) { return __float2half_rn(v); }
 
+#ifdef DCN_CHECK_BOUNDS
+// Bounds-checked builds (compiled with DCN_CHECK_BOUNDS): the address `p`
+// of `n` elements if they lie inside [lo, hi), else `lo` (a safe address)
+// with `bad` set.  These kernels' entry points take no handle and so have
+// no status word: a thread that met an access outside its tensor writes
+// NaN into every output it owns instead, which the parity tests see.
+template <typename T>
+__device__ __forceinline__ T *checked_ptr(T *p, int n, const void *lo, const void *hi, bool &bad) {
+    const char *c = reinterpret_cast<const char *>(p);
+    if (c >= static_cast<const char *>(lo) && c + n * sizeof(T) <= static_cast<const char *>(hi))
+        return p;
+    bad = true;
+    return static_cast<T *>(const_cast<void *>(lo));
+}
+// Whether the `n` fp32 elements at `p` lie inside [lo, hi); `bad` is set
+// when they do not (the reduction is then skipped).
+__device__ __forceinline__ bool checked_ok(const float *p, int n, const void *lo, const void *hi, bool &bad) {
+    const char *c = reinterpret_cast<const char *>(p);
+    const bool ok = c >= static_cast<const char *>(lo) && c + n * sizeof(float) <= static_cast<const char *>(hi);
+    if (!ok) bad = true;
+    return ok;
+}
+#define DCN_ROW(ptr, n) checked_ptr((ptr), (n), p.v_lo, p.v_hi, bad)
+#define DCN_GROW_OK(ptr, n) checked_ok((ptr), (n), p.gv_lo, p.gv_hi, bad)
+#define DCN_BAD_DECL bool bad = false
+// every lane of the warp learns whether any lane met a bad access
+#define DCN_BAD_SYNC bad = __any_sync(0xffffffffu, bad)
+#define DCN_POISON(x) (bad ? __int_as_float(0x7fc00000) : (x))
+#else
+#define DCN_ROW(ptr, n) (ptr)
+#define DCN_GROW_OK(ptr, n) true
+#define DCN_BAD_DECL
+#define DCN_BAD_SYNC
+#define DCN_POISON(x) (x)
+#endif
+
 }  // namespace dcn

@@ -20,6 +20,12 @@ struct MsdaParams {
     int B, S, G, D, Q, K, L;
     int softmax;              // 1: normalize the weights over L*K
     int H[kMsdaMaxLevels], W[kMsdaMaxLevels], start[kMsdaMaxLevels];
+#ifdef DCN_CHECK_BOUNDS
+    // bounds-checked builds: the byte ranges of the tensors the corner rows
+    // are read from (and reduced into)
+    const void *v_lo, *v_hi;
+    const void *gv_lo, *gv_hi;
+#endif
 };
 // vec: D a multiple of 8 (16-bit) or 4 (fp32) and value/out 16-byte aligned.
 cudaError_t launch_msda(const MsdaParams &p, int dtype, bool vec, cudaStream_t stream);
@@ -37,6 +43,12 @@ struct MsdaBwdParams {
     int B, S, G, D, Q, K, L;
     int softmax;
     int H[kMsdaMaxLevels], W[kMsdaMaxLevels], start[kMsdaMaxLevels];
+#ifdef DCN_CHECK_BOUNDS
+    // bounds-checked builds: the byte ranges of the tensors the corner rows
+    // are read from (and reduced into)
+    const void *v_lo, *v_hi;
+    const void *gv_lo, *gv_hi;
+#endif
 };
 // vec: D a multiple of 8 (16-bit) or 4 (fp32); value, grad_out and
 // grad_value 16-byte aligned.
@@ -51,6 +63,12 @@ struct AttnParams {
     int B, H, W, G, D, Ho, Wo;
     int kh, kw, sh, sw, ph, pw, dh, dw;
     int softmax;              // 1: normalize the weights over the K taps
+#ifdef DCN_CHECK_BOUNDS
+    // bounds-checked builds: the byte ranges of the tensors the corner rows
+    // are read from (and reduced into)
+    const void *v_lo, *v_hi;
+    const void *gv_lo, *gv_hi;
+#endif
 };
 // vec: D a multiple of 8 (16-bit) or 4 (fp32) and value/out 16-byte aligned.
 cudaError_t launch_attn(const AttnParams &p, int dtype, bool vec, cudaStream_t stream);
@@ -67,6 +85,12 @@ struct AttnBwdParams {
     int B, H, W, G, D, Ho, Wo;
     int kh, kw, sh, sw, ph, pw, dh, dw;
     int softmax;
+#ifdef DCN_CHECK_BOUNDS
+    // bounds-checked builds: the byte ranges of the tensors the corner rows
+    // are read from (and reduced into)
+    const void *v_lo, *v_hi;
+    const void *gv_lo, *gv_hi;
+#endif
 };
 // vec: D a multiple of 4; value and grad_out 8-byte (16-bit) or 16-byte
 // (fp32) aligned, grad_value 16-byte aligned.

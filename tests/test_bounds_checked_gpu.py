@@ -1,14 +1,20 @@
-"""The forward parity suites against the bounds-checked build.
+"""The forward and sampling-operator parity suites against the
+bounds-checked build.
 
 compute-sanitizer is closed on this machine, so this stands in for its memory
 check on the hot path: libdcn_checked.so is the library compiled with
-DCN_CHECK_BOUNDS, in which the forward kernels (tensor-core and CUDA-core)
-check every corner load, offset and mask fetch, and output store against
-the byte ranges of the caller's tensors; an access outside is skipped and
-raises a status bit that dcn_sync_status reports as DCN_ERR_BOUNDS.  The
-parity suites of the forward run against that build in a child process:
-every case must still match the oracle and report a clean status, so no
-gather or store of theirs leaves its tensor.
+DCN_CHECK_BOUNDS.  In it the convolution's forward kernels (tensor-core and
+CUDA-core) check every corner load, offset and mask fetch, and output store
+against the byte ranges of the caller's tensors; an access outside is
+skipped and raises a status bit that dcn_sync_status reports as
+DCN_ERR_BOUNDS.  The multi-scale and single-scale sampling kernels,
+forward and backward, check every corner-row load of the value tensor and
+every reduction into the value gradient; their entry points take no handle,
+so a thread that meets an access outside writes NaN into every output it
+owns, which the suites' oracle comparisons reject.  The suites run against
+that build in a child process: every case must still match the oracle (and
+the convolution's report a clean status), so no gather, reduction or store
+of theirs leaves its tensor.
 """
 
 import os
@@ -22,7 +28,9 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_parity_gpu.py", "tests/test_parity_general_gpu.py",
           "tests/test_parity_channels_gpu.py", "tests/test_parity_f16_gpu.py",
-          "tests/test_abi_gpu.py", "tests/test_zz_no_alloc.py"]
+          "tests/test_abi_gpu.py", "tests/test_zz_no_alloc.py",
+          "tests/test_msda_gpu.py", "tests/test_msda_backward_gpu.py",
+          "tests/test_attn_gpu.py", "tests/test_attn_backward_gpu.py"]
 
 
 def test_forward_suites_pass_bounds_checked():
