@@ -58,7 +58,7 @@ constexpr int WG_BOX_BYTES = WG_BK * 128;      // one 64-output box of B
 // per sampler warp: the table of its 16 pixels for both units, fp32 weights
 // of the four slots then the slot (0,0) index (16 bytes each)
 constexpr int WG_TABLE_WARP_BYTES = 2 * 2 * WG_TILE_W * 16;
-constexpr int WG_RAW_WARP_BYTES = 32 * 16;     // {dy, dx, m, -} per lane
+constexpr int WG_RAW_WARP_BYTES = 3 * 32 * 4;  // dy, dx and m planes of 32 lanes
 
 struct WgLayout {
     int stages, b_bytes, stage_bytes, table_off, raw_off, bar_off, total;
@@ -208,7 +208,7 @@ dcn_bwd_wgrad_tc_kernel(const __grid_constant__ CUtensorMap gmap, BwdParams p, i
         const int my_g = lane >> 4;                      // geometry: unit
         const uint16_t *__restrict__ x = static_cast<const uint16_t *>(p.x);
         const uint32_t table_s = smem_u32(smem + L.table_off + sw * WG_TABLE_WARP_BYTES);
-        const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * WG_RAW_WARP_BYTES) + lane * 16;
+        const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * WG_RAW_WARP_BYTES) + lane * 4;
         const int HoWo = p.Ho * p.Wo;
         const int Cq = p.C / p.ogroups;
         // the unit this geometry lane tabulates: its tap, offset group and
@@ -225,7 +225,7 @@ dcn_bwd_wgrad_tc_kernel(const __grid_constant__ CUtensorMap gmap, BwdParams p, i
             const int u = min(2 * mt + g, units - 1);
             cbase[g] = (u - (u / ncb) * ncb) * WG_UNIT + 16 * quart;
         }
-        if (p.mask == nullptr) sts_b32(raw_s + 8, __float_as_uint(1.0f));
+        if (p.mask == nullptr) sts_b32(raw_s + 256, __float_as_uint(1.0f));
         const int step_x = p.W > 1 ? p.C : 0;
         const int step_y = p.H > 1 ? p.W * p.C : 0;
 
@@ -243,17 +243,17 @@ dcn_bwd_wgrad_tc_kernel(const __grid_constant__ CUtensorMap gmap, BwdParams p, i
             const size_t hw = valid ? static_cast<size_t>(oh) * p.Wo + ow : 0;
             const float *o = p.offset + (static_cast<size_t>(tb) * p.ogroups * taps * 2 + 2 * plane_g) * HoWo + hw;
             cp_async_4(raw_s, o, valid);
-            cp_async_4(raw_s + 4, o + HoWo, valid);
+            cp_async_4(raw_s + 128, o + HoWo, valid);
             if (p.mask)
-                cp_async_4(raw_s + 8, p.mask + (static_cast<size_t>(tb) * p.ogroups * taps + plane_g) * HoWo + hw, valid);
+                cp_async_4(raw_s + 256, p.mask + (static_cast<size_t>(tb) * p.ogroups * taps + plane_g) * HoWo + hw, valid);
         };
         auto tabulate = [&](int tile) {
             int tb, oh, ow;
             pixel_of(tile, tb, oh, ow);
             cp_async_wait_all();
-            const float4 r = lds_v4_f32(raw_s);         // dy, dx, m
+            const float dy = lds_f32(raw_s), dx = lds_f32(raw_s + 128), m = lds_f32(raw_s + 256);
             TapBlock t;
-            tap_block(r.x, r.y, r.z, oh * p.sh - p.ph + i_g * p.dh, ow * p.sw - p.pw + j_g * p.dw, tb,
+            tap_block(dy, dx, m, oh * p.sh - p.ph + i_g * p.dh, ow * p.sw - p.pw + j_g * p.dw, tb,
                       p.H, p.W, p.C, t);
             const uint32_t ent = table_s + my_g * 2 * WG_TILE_W * 16 + my_px * 16;
             sts_v4_b32_m(ent, __float_as_uint(t.w[0]), __float_as_uint(t.w[1]), __float_as_uint(t.w[2]),

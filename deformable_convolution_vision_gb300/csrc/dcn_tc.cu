@@ -96,15 +96,16 @@ static_assert(TC_TABLE_SLOTS == 4 && TC_TAP_GROUP == 2, "ring index arithmetic a
 // element index of its slot (0,0).
 constexpr int TC_ENTRY_ARRAY_BYTES = TC_TILE_W * 16;
 __host__ __device__ constexpr int table_buf_bytes(bool f32) { return (f32 ? 2 : 1) * TC_ENTRY_ARRAY_BYTES; }
-// raw geometry inputs of one lane: {dy, dx, m, -}
-constexpr int TC_RAW_WARP_BYTES = 32 * 16;
+// raw geometry inputs of a warp: dy, dx and m planes of 32 lanes each
+// (each cp.async of the warp writes 128 contiguous bytes: no bank conflicts)
+constexpr int TC_RAW_WARP_BYTES = 3 * 32 * 4;
 
 struct TcLayout {
     int stages;
     int b_bytes;       // O * 128: one weight K-block
     int bar_off;       // barriers after the stages
     int table_off;     // per-warp corner tables
-    int raw_off;       // per-warp raw geometry inputs, {dy, dx, mask, -} per lane
+    int raw_off;       // per-warp raw geometry inputs, dy, dx and mask planes
     int vt_off;        // virtual-tap table, int4 per (tap, offset group)
     int total;         // bytes used from the 1024-aligned base
 };
@@ -321,7 +322,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         const int trow = 2 * q + half;                   // its tile row = A rows 16 trow .. +15
         const uint16_t *__restrict__ x = static_cast<const uint16_t *>(p.x);   // 16-bit elements
         const uint32_t table_s = smem_u32(smem + L.table_off + sw * TC_TABLE_SLOTS * kBuf);
-        const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * TC_RAW_WARP_BYTES) + lane * 16;
+        const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * TC_RAW_WARP_BYTES) + lane * 4;
         const uint32_t vt_s = smem_u32(smem + L.vt_off);
         const uint32_t a_lane = static_cast<uint32_t>(16 * trow) << 16;
         const int plane = p.plane;                       // offset / mask plane stride
@@ -340,7 +341,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         const int step_x = p.W > 1 ? p.x_cstride : 0;
         const int step_y = p.H > 1 ? p.W * p.x_cstride : 0;
         // without a mask the lane's m word holds 1 for good (nothing copies over it)
-        if (p.mask == nullptr) sts_b32(raw_s + 8, __float_as_uint(1.0f));
+        if (p.mask == nullptr) sts_b32(raw_s + 256, __float_as_uint(1.0f));
         bool ok = true;
         int s = team;                   // this warp's stages: team, team + TC_TEAMS, ...
         uint32_t phase = 0;
@@ -480,16 +481,16 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     const bool v_dy = valid && in_bounds(o, 4, p.off_lo, p.off_hi, p.status);
                     const bool v_dx = valid && in_bounds(o + plane, 4, p.off_lo, p.off_hi, p.status);
                     cp_async_4(raw_s, v_dy ? o : p.offset, v_dy);
-                    cp_async_4(raw_s + 4, v_dx ? o + plane : p.offset, v_dx);
+                    cp_async_4(raw_s + 128, v_dx ? o + plane : p.offset, v_dx);
                     if (p.mask) {
                         const float *mp = mask_img + (mc * plane + my_hw);
                         const bool v_m = valid && in_bounds(mp, 4, p.mask_lo, p.mask_hi, p.status);
-                        cp_async_4(raw_s + 8, v_m ? mp : p.mask, v_m);
+                        cp_async_4(raw_s + 256, v_m ? mp : p.mask, v_m);
                     }
 #else
                     cp_async_4(raw_s, o, valid);
-                    cp_async_4(raw_s + 4, o + plane, valid);
-                    if (p.mask) cp_async_4(raw_s + 8, mask_img + (mc * plane + my_hw), valid);
+                    cp_async_4(raw_s + 128, o + plane, valid);
+                    if (p.mask) cp_async_4(raw_s + 256, mask_img + (mc * plane + my_hw), valid);
 #endif
                 };
                 // The table entry of virtual tap vt for this lane's pixel, in
@@ -497,10 +498,10 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 // past the last one gets an entry that is never read.
                 auto tabulate = [&](int vt, int slot) {
                     cp_async_wait_all();
-                    const float4 r = lds_v4_f32(raw_s);       // dy, dx, m
+                    const float dy = lds_f32(raw_s), dx = lds_f32(raw_s + 128), m = lds_f32(raw_s + 256);
                     const int4 e = lds_v4_s32_m(vt_s + min(vt, vtaps - 1) * 16);
                     TapBlock t;
-                    tap_block(r.x, r.y, r.z, y_base + e.x, x_base + e.y, tb, p.H, p.W, p.x_cstride, t);
+                    tap_block(dy, dx, m, y_base + e.x, x_base + e.y, tb, p.H, p.W, p.x_cstride, t);
                     const uint32_t ent = table_s + slot * kBuf + my_px * 16;
                     if constexpr (kSampleF32) {
                         sts_v4_b32_m(ent, __float_as_uint(t.w[0]), __float_as_uint(t.w[1]),
