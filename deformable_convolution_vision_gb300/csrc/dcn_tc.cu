@@ -31,12 +31,13 @@
 //               tile's last K-block all sixteen run the epilogue (S5): TMEM
 //               -> registers, + bias in fp32, rounding to the operand type,
 //               channels-last store.
-// K-blocks run tap-major with 64 channels each, so a tap's corner geometry
-// is computed once and reused for all of its channel blocks.  The geometry
-// of two taps at a time is computed by all 32 lanes of a warp into a ring
-// of four per-warp tables, with its inputs fetched a group ahead.  Each
-// lane issues the corner loads of its next K-block before it stores the
-// current one.
+// K-blocks of 64 channels run block-major: every tap of the first channel
+// block, then every tap of the next, so that the corner lines a tile
+// re-reads from tap to tap are one block's and stay in L1.  The geometry of
+// a warp's next two K-blocks is computed by all 32 lanes (one K-block per
+// half-warp) into a ring of four per-warp tables, with its inputs fetched a
+// pair ahead.  Each lane issues the corner loads of its next K-block before
+// it stores the current one.
 //
 // With more tiles than SMs the launch is persistent and stream-K: every
 // CTA takes an equal run of (tile, K-block) units; a tile split between two
@@ -87,13 +88,15 @@ constexpr int TC_TABLE_SLOTS = 2 * TC_TAP_GROUP;              // ring: one group
 static_assert(TC_TEAM_WARPS * TC_TILE_W == TC_BM, "a team covers the tile");
 static_assert(TC_TABLE_SLOTS == 4 && TC_TAP_GROUP == 2, "ring index arithmetic assumes four slots");
 
-// Per-warp sampling table of one tap: one 16-byte entry per pixel of the
-// warp's tile row in each of two arrays (conflict-free writes, broadcast
-// reads).  A sample is read as the clamped 2 x 2 block of tap_block: the
-// first array holds its four slot weights (mask folded in) -- for the
-// 16-bit combine each rounded to the operand type and duplicated into both
-// halves of a word, for the fp32 combine as fp32 -- and the second the
-// element index of its slot (0,0).
+// Per-warp sampling table of one K-block: one 16-byte entry per pixel of
+// the warp's tile row (conflict-free writes, broadcast reads).  A sample is
+// read as the clamped 2 x 2 block of tap_block.  An entry holds its four
+// slot weights (mask folded in), the element index of its slot (0,0) at
+// the K-block's first channel, and the limit of a lane's channel offset
+// within the K-block.  For the 16-bit combine the weights are rounded to
+// the operand type, two to a word, and all four fields share the entry;
+// for the fp32 combine the weights are fp32 and fill the entry, and the
+// index and limit sit in a second array.
 constexpr int TC_ENTRY_ARRAY_BYTES = TC_TILE_W * 16;
 __host__ __device__ constexpr int table_buf_bytes(bool f32) { return (f32 ? 2 : 1) * TC_ENTRY_ARRAY_BYTES; }
 // raw geometry inputs of a warp: dy, dx and m planes of 32 lanes each
@@ -169,7 +172,20 @@ __device__ __forceinline__ float4 ld_cg_f4(const float *p) {
     return __ldcg(reinterpret_cast<const float4 *>(p));
 }
 
-template <bool kSampleF32, bool kF16, bool kOneBlock>
+// Walk position j of a tile's K-blocks -> (channel block, virtual tap):
+// returns j / vtaps and sets vt = j % vtaps.  rcp is 1.0f / vtaps; for j
+// below 2^22 the float quotient is off by at most one, which the two
+// corrections take back.
+__device__ __forceinline__ int walk_split(int j, int vtaps, float rcp, int &vt) {
+    int q = __float2int_rz(__int2float_rn(j) * rcp);
+    int r = j - q * vtaps;
+    if (r < 0) { --q; r += vtaps; }
+    if (r >= vtaps) { ++q; r -= vtaps; }
+    vt = r;
+    return q;
+}
+
+template <bool kSampleF32, bool kF16>
 __global__ void __maxnreg__(TC_MAX_REGS)
 dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     using E = Elem16<kF16>;   // the 16-bit operand type: its packed arithmetic and MMA format
@@ -198,11 +214,16 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
     const int ncb = (p.C + TC_BK - 1) / TC_BK;
     const int taps = p.kh * p.kw;
     const int nkb = taps * ncb;
-    // The K walk tap-major, channel-minor, seen as virtual taps: (tap,
-    // offset group) pairs, each with its own offsets and mask, of vncb
-    // channel blocks each.  K-block kb = vt * vncb + vcb.
+    // Virtual taps: (tap, offset group) pairs, each with its own offsets and
+    // mask, of vncb channel blocks each; packed-weight K-block vt * vncb + cb.
+    // A tile walks its K-blocks block-major: position j = cb * vtaps + vt,
+    // every virtual tap of channel block 0, then of block 1, ...  Between
+    // two taps that read a corner pixel the L1 then holds one 128-byte line
+    // of it (its 64 channels of the block), not the vncb lines of all its
+    // channels.
     const int vtaps = taps * p.og_count;
     const int vncb = ncb / p.og_count;
+    const float vt_rcp = 1.0f / static_cast<float>(vtaps);
     const int total = p.B * tiles_x * tiles_y * nkb;
     const int u_begin = blockIdx.x * p.units_per_cta;
     const int u_end = min(u_begin + p.units_per_cta, total);
@@ -249,7 +270,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
             int issued = 0;
             int s = 0;
             uint32_t phase = 0;
-            int kb = u_begin % nkb;
+            // walk position u_begin % nkb as (virtual tap, channel block)
+            int vt, cb = walk_split(u_begin % nkb, vtaps, vt_rcp, vt);
             // The packed weight may still be in the making when this grid
             // was launched as the pack's programmatic dependent: wait for
             // that grid to complete (a no-op for an ordinary launch).
@@ -258,9 +280,12 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 if (!mbar_wait_sleep(empty0 + 8 * s, phase ^ 1, p.status, p.timeout_ns)) break;
                 const uint32_t b_dst = smem_u32(smem + s * L.b_bytes);
                 mbar_arrive_expect_tx(full0 + 8 * s, L.b_bytes);
-                tma_load_2d(b_dst, &wmap, full0 + 8 * s, kb * TC_BK, 0);
+                tma_load_2d(b_dst, &wmap, full0 + 8 * s, (vt * vncb + cb) * TC_BK, 0);
                 ++issued;
-                if (++kb == nkb) kb = 0;
+                if (++vt == vtaps) {
+                    vt = 0;
+                    if (++cb == vncb) cb = 0;
+                }
                 if (++s == stages) { s = 0; phase ^= 1; }
             }
             // Before the CTA can exit, every weight copy it started must
@@ -328,11 +353,10 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         const int plane = p.plane;                       // offset / mask plane stride
         const int my_g = lane >> 4;     // geometry: tap of the group
         const int my_px = lane & 15;    // geometry: pixel (tile column)
-        const int quart = lane & 3;     // gather: 16 channels of the 64-channel K-block
+        const int quart16 = (lane & 3) * 16;   // gather: the lane's 16 channels of the K-block
         // A lane whose 16 channels lie past the last one (C % 64 != 0, last
-        // block of a tap) reads the last 16 real channels instead: finite
-        // data in bounds, which the packed weight's zero rows cancel in the
-        // MMA.  No branch, one min per K-block.
+        // block) reads the last 16 real channels instead: finite data in
+        // bounds, which the packed weight's zero rows cancel in the MMA.
         const int chan_last = p.C - 16;
         const int rsub = lane >> 2;     // gather: pixels rsub and rsub + 8 of the row
         const uint32_t r_off0 = rsub * 16;
@@ -469,12 +493,25 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 const int n = (sg.kb1 - kb_first + TC_TEAMS - 1) / TC_TEAMS;   // this warp's K-blocks
                 const uint32_t tl = table_s + r_off0;           // this lane's first entry in slot 0
 
-                // Raw inputs (dy, dx, mask) of virtual tap vt for this lane's
-                // pixel, copied ahead of their use into the lane's raw slot
-                // (asynchronously: no registers held while in flight).
-                auto load_raw = [&](int vt) {
-                    const bool valid = my_valid && vt < vtaps;
-                    const int mc = valid ? lds_s32(vt_s + vt * 16 + 8) : 0;   // mask plane; offsets 2mc, 2mc + 1
+                // Walk position of the raw inputs this lane loaded last, as
+                // (virtual tap, channel block): the lane's loads are walk
+                // positions kb_first + TC_TEAMS * (2g + my_g), g = 0, 1, ...,
+                // each one 2 * TC_TEAMS after the one before.  A load and the
+                // tabulation of what it loaded alternate, so the table entry
+                // is always made from the most recent load.
+                int r_vt;
+                int r_cb = walk_split(kb_first + TC_TEAMS * my_g, vtaps, vt_rcp, r_vt);
+                // Raw inputs (dy, dx, mask) of the lane's next walk position
+                // (its first when `first`) for its pixel, copied ahead of their
+                // use into the lane's raw slot (asynchronously: no registers
+                // held while in flight).
+                auto load_raw = [&](bool first) {
+                    if (!first) {
+                        r_vt += 2 * TC_TEAMS;
+                        while (r_vt >= vtaps) { r_vt -= vtaps; ++r_cb; }
+                    }
+                    const bool valid = my_valid && r_cb < vncb;                  // j < nkb
+                    const int mc = lds_s32(vt_s + r_vt * 16 + 8);   // mask plane; offsets 2mc, 2mc + 1
                     const float *o = off_img + (2 * mc * plane + my_hw);
 #ifdef DCN_CHECK_BOUNDS
                     // an offset or mask outside its tensor is not fetched (zero)
@@ -493,34 +530,41 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     if (p.mask) cp_async_4(raw_s + 256, mask_img + (mc * plane + my_hw), valid);
 #endif
                 };
-                // The table entry of virtual tap vt for this lane's pixel, in
-                // ring slot `slot`, from the raw inputs loaded for it.  A tap
-                // past the last one gets an entry that is never read.
-                auto tabulate = [&](int vt, int slot) {
+                // The table entry of the last loaded walk position for this
+                // lane's pixel, in ring slot `slot`: the sample block's slot
+                // weights, the element index of its slot (0,0) at the
+                // K-block's first channel, and the limit of a lane's channel
+                // offset in the K-block (a lane past the last channel reads
+                // the last 16 instead).  A position past the last one gets an
+                // entry that is never read.
+                auto tabulate = [&](int slot) {
                     cp_async_wait_all();
                     const float dy = lds_f32(raw_s), dx = lds_f32(raw_s + 128), m = lds_f32(raw_s + 256);
-                    const int4 e = lds_v4_s32_m(vt_s + min(vt, vtaps - 1) * 16);
+                    const int4 e = lds_v4_s32_m(vt_s + r_vt * 16);
                     TapBlock t;
                     tap_block(dy, dx, m, y_base + e.x, x_base + e.y, tb, p.H, p.W, p.x_cstride, t);
+                    const int c0 = e.w + r_cb * TC_BK;
                     const uint32_t ent = table_s + slot * kBuf + my_px * 16;
                     if constexpr (kSampleF32) {
                         sts_v4_b32_m(ent, __float_as_uint(t.w[0]), __float_as_uint(t.w[1]),
                                      __float_as_uint(t.w[2]), __float_as_uint(t.w[3]));
-                        sts_b32(ent + TC_ENTRY_ARRAY_BYTES, static_cast<uint32_t>(t.idx + e.w));
+                        sts_v2_b32_m(ent + TC_ENTRY_ARRAY_BYTES, static_cast<uint32_t>(t.idx + c0),
+                                     static_cast<uint32_t>(chan_last - c0));
                     } else {
                         sts_v4_b32_m(ent, E::pack(t.w[0], t.w[1]), E::pack(t.w[2], t.w[3]),
-                                     static_cast<uint32_t>(t.idx + e.w), 0u);
+                                     static_cast<uint32_t>(t.idx + c0), static_cast<uint32_t>(chan_last - c0));
                     }
                 };
                 // The corner-row loads of both of this lane's pixels from the
                 // entries in ring slot `slot`: each sample block's four slots
-                // from the index of its slot (0,0), every one inside the image.
-                // xl is x advanced by the lane's channel offset.
-                auto issue = [&](const uint16_t *xl, int slot, u32x8 (&v)[8]) {
+                // from the index of its slot (0,0), every one inside the image,
+                // advanced by the lane's channel offset.
+                auto issue = [&](int slot, u32x8 (&v)[8]) {
                     const uint32_t ent = tl + slot * kBuf + (kSampleF32 ? TC_ENTRY_ARRAY_BYTES : 8);
 #pragma unroll
                     for (int px = 0; px < 2; ++px) {
-                        const int e0 = lds_s32(ent + (px ? r_off1_rel : 0u));
+                        const uint2 ei = lds_v2_u32(ent + (px ? r_off1_rel : 0u));
+                        const int e0 = static_cast<int>(ei.x) + min(quart16, static_cast<int>(ei.y));
                         const int e1 = e0 + step_x;
                         const int e2 = e0 + step_y;
                         const int e3 = e2 + step_x;
@@ -530,15 +574,15 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                             return in_bounds(a, 32, p.x_lo, p.x_hi, p.status)
                                        ? a : static_cast<const uint16_t *>(p.x_lo);
                         };
-                        v[4 * px + 0] = ldg_v8(chk(xl + e0));
-                        v[4 * px + 1] = ldg_v8(chk(xl + e1));
-                        v[4 * px + 2] = ldg_v8(chk(xl + e2));
-                        v[4 * px + 3] = ldg_v8(chk(xl + e3));
+                        v[4 * px + 0] = ldg_v8(chk(x + e0));
+                        v[4 * px + 1] = ldg_v8(chk(x + e1));
+                        v[4 * px + 2] = ldg_v8(chk(x + e2));
+                        v[4 * px + 3] = ldg_v8(chk(x + e3));
 #else
-                        v[4 * px + 0] = ldg_v8(xl + e0);
-                        v[4 * px + 1] = ldg_v8(xl + e1);
-                        v[4 * px + 2] = ldg_v8(xl + e2);
-                        v[4 * px + 3] = ldg_v8(xl + e3);
+                        v[4 * px + 0] = ldg_v8(x + e0);
+                        v[4 * px + 1] = ldg_v8(x + e1);
+                        v[4 * px + 2] = ldg_v8(x + e2);
+                        v[4 * px + 3] = ldg_v8(x + e3);
 #endif
                     }
                 };
@@ -625,123 +669,51 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 u32x8 va[8], vb[8];   // (vb unused with one K-block in flight)
                 u32x8 (&v_odd)[8] = TC_DEPTH == 2 ? vb : va;
 
-                if constexpr (kOneBlock) {
-                    // One channel block per virtual tap: this warp's K-block jj
-                    // of the segment is virtual tap t0 + TC_TEAMS * jj, its table
-                    // in ring slot jj % 4.  Taps are tabulated in pairs of the
-                    // warp's sequence {2g, 2g + 1} (slots 2g % 4 and 2g % 4 + 1,
-                    // one per half-warp), so in a body unrolled by four K-blocks
-                    // every slot is a constant.  The lane's channel offset is
-                    // fixed.
-                    const int t0 = kb_first;
-                    const uint16_t *xl = x + min(quart * 16, chan_last);
-                    auto load_pair = [&](int g) { load_raw(t0 + TC_TEAMS * (2 * g + my_g)); };
-                    auto tab_pair = [&](int g) {
-                        tabulate(t0 + TC_TEAMS * (2 * g + my_g), (2 * g + my_g) & (TC_TABLE_SLOTS - 1));
-                    };
-                    load_pair(0);
-                    tab_pair(0);
-                    if (2 < n) { load_pair(1); tab_pair(1); }
-                    if (4 < n) load_pair(2);
-                    __syncwarp();
-                    issue(xl, 0, va);
-                    if constexpr (TC_DEPTH == 2) {
-                        if (n > 1) issue(xl, 1, vb);
+                // This warp's K-block jj of the segment is walk position
+                // j = kb_first + TC_TEAMS * jj, its table in ring slot jj % 4.
+                // Tables are made in pairs of the warp's sequence {2g, 2g + 1}
+                // (slots 2g % 4 and 2g % 4 + 1, one per half-warp), so in a
+                // body unrolled by four K-blocks every slot is a constant.
+                auto load_pair = [&](int g) { load_raw(g == 0); };
+                auto tab_pair = [&](int g) { tabulate((2 * g + my_g) & (TC_TABLE_SLOTS - 1)); };
+                load_pair(0);
+                tab_pair(0);
+                if (2 < n) { load_pair(1); tab_pair(1); }
+                if (4 < n) load_pair(2);
+                __syncwarp();
+                issue(0, va);
+                if constexpr (TC_DEPTH == 2) {
+                    if (n > 1) issue(1, vb);
+                }
+                // K-block jj = base + k in ring slot k; at an even k (past the
+                // segment's first K-block) the pair after next is tabulated
+                // into the slots the last pair used; then the loads of
+                // K-block jj + TC_DEPTH.  (Issuing those loads before the
+                // tabulation was measured slower: the tabulation's shared
+                // reads then queue behind them.)
+                auto step = [&](int jj, int k, u32x8 (&v)[8]) -> bool {
+                    // this K-block's weights, read before the stage wait
+                    const uint2 p0 = lds_v2_u32(tl + k * kBuf);
+                    const uint2 p1 = lds_v2_u32(tl + k * kBuf + r_off1_rel);
+                    if (!combine_store(k, v, p0, p1)) return false;
+                    if ((k & 1) == 0 && jj > 0 && jj + 2 < n) {
+                        const int g = jj / 2 + 1;
+                        tab_pair(g);
+                        if (2 * g + 2 < n) load_pair(g + 1);
+                        __syncwarp();
                     }
-                    // K-block jj = base + k in ring slot k; at an even k (past the
-                    // segment's first K-block) the pair after next is tabulated
-                    // into the slots the last pair used; then the loads of
-                    // K-block jj + TC_DEPTH.
-                    auto step = [&](int jj, int k, u32x8 (&v)[8]) -> bool {
-                        // this K-block's weights, read before the stage wait
-                        const uint2 p0 = lds_v2_u32(tl + k * kBuf);
-                        const uint2 p1 = lds_v2_u32(tl + k * kBuf + r_off1_rel);
-                        if (!combine_store(k, v, p0, p1)) return false;
-                        if ((k & 1) == 0 && jj > 0 && jj + 2 < n) {
-                            const int g = jj / 2 + 1;
-                            tab_pair(g);
-                            if (2 * g + 2 < n) load_pair(g + 1);
-                            __syncwarp();
-                        }
-                        if (jj + TC_DEPTH < n) issue(xl, (k + TC_DEPTH) & (TC_TABLE_SLOTS - 1), v);
-                        finish_stage();
-                        return true;
-                    };
-                    for (int jj = 0; jj < n; jj += 4) {
-                        if (!step(jj, 0, va)) { ok = false; break; }
-                        if (jj + 1 >= n) break;
-                        if (!step(jj + 1, 1, v_odd)) { ok = false; break; }
-                        if (jj + 2 >= n) break;
-                        if (!step(jj + 2, 2, va)) { ok = false; break; }
-                        if (jj + 3 >= n) break;
-                        if (!step(jj + 3, 3, v_odd)) { ok = false; break; }
-                    }
-                } else {
-                    // Several channel blocks per virtual tap (every warp visits
-                    // every tap): K-block (vt, cb), the table of vt in ring slot
-                    // vt % 4, taps tabulated in pairs {2G, 2G + 1} (slots 2G % 4,
-                    // 2G % 4 + 1).
-                    const int t_first = kb_first / vncb;
-                    auto load_group = [&](int g) { load_raw(g + my_g); };
-                    auto tab_group = [&](int g) { tabulate(g + my_g, (g + my_g) & (TC_TABLE_SLOTS - 1)); };
-                    const int g0 = t_first & ~(TC_TAP_GROUP - 1);
-                    load_group(g0);
-                    tab_group(g0);
-                    if (g0 + TC_TAP_GROUP < vtaps) {
-                        load_group(g0 + TC_TAP_GROUP);
-                        tab_group(g0 + TC_TAP_GROUP);
-                    }
-                    if (g0 + 2 * TC_TAP_GROUP < vtaps) load_group(g0 + 2 * TC_TAP_GROUP);
-                    __syncwarp();
-                    // advance a K-block (vt, cb) by TC_TEAMS blocks (at most
-                    // TC_TEAMS carries: cb < vncb)
-                    auto advance = [&](int &t, int &c) {
-                        c += TC_TEAMS;
-                        if (c >= vncb) { c -= vncb; ++t; }
-                        if (TC_TEAMS == 2 && c >= vncb) { c -= vncb; ++t; }
-                    };
-                    int vt = t_first, cb = kb_first - t_first * vncb;   // this warp's K-block jj
-                    int vtn = vt, cbn = cb;                             // K-block jj + TC_DEPTH
-                    for (int d = 0; d < TC_DEPTH; ++d) advance(vtn, cbn);
-                    int vt_prev = vt;
-                    // x advanced by the lane's channel offset in block c
-                    auto x_at = [&](int c) { return x + min(c * TC_BK + quart * 16, chan_last); };
-                    issue(x_at(cb), vt & (TC_TABLE_SLOTS - 1), va);
-                    if constexpr (TC_DEPTH == 2) {
-                        if (n > 1) {
-                            int vt1 = vt, cb1 = cb;
-                            advance(vt1, cb1);
-                            issue(x_at(cb1), vt1 & (TC_TABLE_SLOTS - 1), vb);
-                        }
-                    }
-                    auto step = [&](int jj, u32x8 (&v)[8]) -> bool {
-                        const uint32_t cs = tl + (vt & (TC_TABLE_SLOTS - 1)) * kBuf;
-                        const uint2 p0 = lds_v2_u32(cs);
-                        const uint2 p1 = lds_v2_u32(cs + r_off1_rel);
-                        if (!combine_store(vt & (TC_TABLE_SLOTS - 1), v, p0, p1)) return false;
-                        // Entering an even virtual tap (other than at the
-                        // segment's start): the previous group's slots are no
-                        // longer read, so fill them with the next group and fetch
-                        // the one after.
-                        if (vt != vt_prev && (vt & (TC_TAP_GROUP - 1)) == 0 && vt + TC_TAP_GROUP < vtaps) {
-                            tab_group(vt + TC_TAP_GROUP);
-                            if (vt + 2 * TC_TAP_GROUP < vtaps) load_group(vt + 2 * TC_TAP_GROUP);
-                            __syncwarp();
-                        }
-                        // the corner data is consumed: the loads of K-block jj + TC_DEPTH
-                        if (jj + TC_DEPTH < n) issue(x_at(cbn), vtn & (TC_TABLE_SLOTS - 1), v);
-                        finish_stage();
-                        vt_prev = vt;
-                        advance(vt, cb);
-                        advance(vtn, cbn);
-                        return true;
-                    };
-                    for (int jj = 0; jj < n; jj += TC_DEPTH) {
-                        if (!step(jj, va)) { ok = false; break; }
-                        if constexpr (TC_DEPTH == 2) {
-                            if (jj + 1 < n && !step(jj + 1, vb)) { ok = false; break; }
-                        }
-                    }
+                    if (jj + TC_DEPTH < n) issue((k + TC_DEPTH) & (TC_TABLE_SLOTS - 1), v);
+                    finish_stage();
+                    return true;
+                };
+                for (int jj = 0; jj < n; jj += 4) {
+                    if (!step(jj, 0, va)) { ok = false; break; }
+                    if (jj + 1 >= n) break;
+                    if (!step(jj + 1, 1, v_odd)) { ok = false; break; }
+                    if (jj + 2 >= n) break;
+                    if (!step(jj + 2, 2, va)) { ok = false; break; }
+                    if (jj + 3 >= n) break;
+                    if (!step(jj + 3, 3, v_odd)) { ok = false; break; }
                 }
                 // raw copies issued for taps past the segment's end must land
                 // before the next segment reuses the raw slot
@@ -766,8 +738,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
 }
 
 // The dynamic shared-memory size last set on each device for each
-// instantiation [fp32 combine][fp16 operands][one channel block per tap].
-PerDeviceValue<> g_max_smem_set[2][2][2];
+// instantiation [fp32 combine][fp16 operands].
+PerDeviceValue<> g_max_smem_set[2][2];
 
 // Carveout preference (percent of the 228 KB maximum) that selects the
 // smallest supported shared-memory size holding `needed` bytes; the driver
@@ -856,19 +828,15 @@ cudaError_t launch_tc(const Params &p_in, const CUtensorMap &wmap, cudaStream_t 
     const TcLayout L = tc_layout(p.O, stages, f32, vtaps);
     const int smem = L.total + 1024;  // slack for 1024-byte alignment
     const bool f16 = p.f16 != 0;
-    // one channel block per virtual tap: the unrolled walk
-    const bool one = ncb / p.og_count == 1;
     using KernelFn = void (*)(const CUtensorMap, Params, int);
-    static const KernelFn kKernels[2][2][2] = {
-        {{dcn_tc_kernel<false, false, false>, dcn_tc_kernel<false, false, true>},
-         {dcn_tc_kernel<false, true, false>, dcn_tc_kernel<false, true, true>}},
-        {{dcn_tc_kernel<true, false, false>, dcn_tc_kernel<true, false, true>},
-         {dcn_tc_kernel<true, true, false>, dcn_tc_kernel<true, true, true>}}};
-    const KernelFn kernel = kKernels[f32 ? 1 : 0][f16 ? 1 : 0][one ? 1 : 0];
+    static const KernelFn kKernels[2][2] = {
+        {dcn_tc_kernel<false, false>, dcn_tc_kernel<false, true>},
+        {dcn_tc_kernel<true, false>, dcn_tc_kernel<true, true>}};
+    const KernelFn kernel = kKernels[f32 ? 1 : 0][f16 ? 1 : 0];
     int dev = 0;
     cudaError_t ae = cudaGetDevice(&dev);
     if (ae != cudaSuccess) return ae;
-    ae = static_cast<cudaError_t>(g_max_smem_set[f32 ? 1 : 0][f16 ? 1 : 0][one ? 1 : 0].ensure(dev, smem, [&] {
+    ae = static_cast<cudaError_t>(g_max_smem_set[f32 ? 1 : 0][f16 ? 1 : 0].ensure(dev, smem, [&] {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         // ask for just enough shared memory for the one resident CTA (plus
