@@ -110,6 +110,7 @@ struct TcLayout {
     int table_off;     // per-warp corner tables
     int raw_off;       // per-warp raw geometry inputs, dy, dx and mask planes
     int vt_off;        // virtual-tap table, int4 per (tap, offset group)
+    int bias_off;      // the bias, fp32 per output channel (zero without one)
     int total;         // bytes used from the 1024-aligned base
 };
 
@@ -123,7 +124,8 @@ __host__ __device__ inline TcLayout tc_layout(int O, int stages, bool f32, int v
     L.table_off = (L.table_off + 15) & ~15;
     L.raw_off = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_SLOTS * table_buf_bytes(f32);
     L.vt_off = L.raw_off + TC_SAMPLER_WARPS * TC_RAW_WARP_BYTES;
-    L.total = L.vt_off + vtaps * 16;
+    L.bias_off = L.vt_off + vtaps * 16;
+    L.total = L.bias_off + O * 4;
     return L;
 }
 
@@ -243,6 +245,8 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         const int j = tap - i * p.kw;
         vt_tab[vt] = make_int4(i * p.dh - p.ph, j * p.dw - p.pw, og * taps + tap, og * vncb * TC_BK);
     }
+    float *bias_tab = reinterpret_cast<float *>(smem + L.bias_off);
+    for (int o = threadIdx.x; o < p.O; o += blockDim.x) bias_tab[o] = p.bias ? __ldg(p.bias + o) : 0.0f;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(full0 + 8 * s, 1 + TC_TEAM_WARPS);
@@ -429,20 +433,22 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                         tmem_ld16(tmem_base + acc_lane + ch * 16, vv);
                         if (merge && ok) {
                             const float *sp = src + (static_cast<size_t>(ch) * TC_BM + erow) * 16;
-    #pragma unroll
+#pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float4 a = ld_cg_f4(sp + 4 * e);
                                 vv[4 * e] += a.x; vv[4 * e + 1] += a.y; vv[4 * e + 2] += a.z; vv[4 * e + 3] += a.w;
                             }
                         }
                         if (ok && pix_valid) {
+                            // + bias in fp32 (from its shared-memory copy), rounded
+                            // once to the operand type
+                            const uint32_t bs = smem_u32(smem + L.bias_off) + ch * 64;
                             uint32_t pk[8];
-    #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int o = ch * 16 + 2 * e;
-                                const float b0 = p.bias ? __ldg(p.bias + o) : 0.0f;
-                                const float b1 = p.bias ? __ldg(p.bias + o + 1) : 0.0f;
-                                pk[e] = E::pack(vv[2 * e] + b0, vv[2 * e + 1] + b1);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 bb = lds_v4_f32(bs + 16 * e);
+                                pk[2 * e] = E::pack(vv[4 * e] + bb.x, vv[4 * e + 1] + bb.y);
+                                pk[2 * e + 1] = E::pack(vv[4 * e + 2] + bb.z, vv[4 * e + 3] + bb.w);
                             }
                             uint4 *dst = reinterpret_cast<uint4 *>(out + pix * p.out_stride + ch * 16);
 #ifdef DCN_CHECK_BOUNDS
