@@ -108,6 +108,9 @@ TC_CASES = [
     GW("bwdtc_o256", 1, 64, 12, 17, 256, 3, 3, (1, 1), (1, 1), (1, 1), 1, 1, "f16", 2.0, True, 34),
     GW("bwdtc_og2", 1, 128, 14, 16, 64, 3, 3, (2, 1), (1, 1), (1, 2), 1, 2, "bf16", 2.0, True, 35),
     GW("bwdtc_5x5_no_mask", 1, 64, 19, 23, 64, 5, 5, (1, 1), (2, 2), (1, 1), 1, 1, "f16", 4.0, False, 36),
+    # offsets of std 8: many corners land outside the kernel's grad_x window
+    # around the tile (those go straight to grad_x), the rest inside it
+    GW("bwdtc_far_offsets", 2, 128, 40, 36, 64, 3, 3, (1, 1), (1, 1), (1, 1), 1, 1, "bf16", 8.0, True, 37),
 ]
 
 
