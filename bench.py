@@ -196,13 +196,22 @@ def cpu_baseline(wl, inp, seconds):
 
 # ------------------------------------------------------------------- arms
 
+def reference_step_seconds(args):
+    """Oracle seconds per reference step: each step is a sample of the
+    workload sized so that the whole run (warm-up steps at a quarter of a
+    step) stays within the budget -- at most reference_step_seconds a step,
+    less when there are many steps."""
+    return min(args.reference_step_seconds,
+               args.reference_budget_seconds / max(args.steps + 0.25 * args.warmup, 1.0))
+
+
 def run_reference(args, wl, rank, world):
     """The oracle, timed on the host cores: each step is a bounded sample."""
     if rank != 0:
         return
     from deformable_convolution_vision_gb300.inputs import make_inputs
     inp = make_inputs(wl)
-    per_step = args.reference_step_seconds
+    per_step = reference_step_seconds(args)
     for _ in range(args.warmup):
         time_oracle(wl, inp, per_step * 0.25)
     steps = []
@@ -224,7 +233,7 @@ def run_reference(args, wl, rank, world):
         "out_pixels_per_s": px / el,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{px} random output pixels x all {wl.O} channels over "
-                                   f"{args.steps} steps of ~{per_step} s"},
+                                   f"{args.steps} steps of ~{per_step:.3g} s"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -764,6 +773,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="aspp7x7")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-step-seconds", type=float, default=2.0)
+    ap.add_argument("--reference-budget-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--backward-steps", type=int, default=50)

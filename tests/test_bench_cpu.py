@@ -59,3 +59,18 @@ def test_single_scale_bytes():
         assert bench.attn_bytes(a, 2) == value + rows * K * 8 + rows * K * 4 + out, a.name
         assert bench.attn_backward_bytes(a, 2) == (value + 2 * a.B * a.H * a.W * a.G * a.D * 4
                                                    + out + 2 * (rows * K * 8 + rows * K * 4)), a.name
+
+
+def test_reference_arm_stays_within_its_budget():
+    """The reference arm (the oracle on the host cores) sizes its per-step
+    sample so that any --steps/--warmup finishes within the budget."""
+    import argparse
+    for steps, warmup in [(20, 3), (2000, 10), (1, 0), (100000, 100)]:
+        a = argparse.Namespace(steps=steps, warmup=warmup, reference_step_seconds=2.0,
+                               reference_budget_seconds=120.0)
+        per = bench.reference_step_seconds(a)
+        assert 0.0 < per <= 2.0
+        assert per * (steps + 0.25 * warmup) <= 120.0 + 1e-9
+    # few steps keep the full per-step sample
+    a = argparse.Namespace(steps=20, warmup=3, reference_step_seconds=2.0, reference_budget_seconds=120.0)
+    assert bench.reference_step_seconds(a) == 2.0
