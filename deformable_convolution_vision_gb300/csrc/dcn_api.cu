@@ -49,6 +49,11 @@ struct dcn_handle_s {
     cudaStream_t s_kernel = nullptr, s_down = nullptr;
     cudaEvent_t ev_in = nullptr, ev_k = nullptr, ev_done = nullptr;
 
+    // dcn_backward: the weight gradient's stream beside the data kernel and
+    // the fork / join events (created on first use)
+    cudaStream_t s_wgrad = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+
     // device staging for dcn_forward_host: x, offset, mask, weight, bias, out
     void *stage[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     unsigned *host_status = nullptr;   // pinned copy of the status word (host-buffer entry)
@@ -420,7 +425,8 @@ dcn_status_t dcn_destroy(dcn_handle_t h) {
     if (h->host_status) cudaFreeHost(h->host_status);
     if (h->s_kernel) cudaStreamDestroy(h->s_kernel);
     if (h->s_down) cudaStreamDestroy(h->s_down);
-    cudaEvent_t evs[3] = {h->ev_in, h->ev_k, h->ev_done};
+    if (h->s_wgrad) cudaStreamDestroy(h->s_wgrad);
+    cudaEvent_t evs[5] = {h->ev_in, h->ev_k, h->ev_done, h->ev_fork, h->ev_join};
     for (cudaEvent_t e : evs)
         if (e) cudaEventDestroy(e);
     delete h;
@@ -610,12 +616,43 @@ static dcn_status_t backward_general(dcn_handle_t h, const void *x, const float 
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return DCN_ERR_CUDA;
     }
-    if (dcn::launch_bwd_data_tc(p, gmap, wmap, s) != cudaSuccess) return DCN_ERR_CUDA;
-
     // The weight gradient on tensor cores: the sampled operand m * S of
     // each 128-pixel tile is contracted with the grad_out tile as soon as it
     // is sampled, in shared memory; fp32 accumulation in tensor memory.
-    if (dcn::launch_bwd_wgrad_tc(p, gmap, s) != cudaSuccess) return DCN_ERR_CUDA;
+    // The data kernel is bound by its reductions into grad_x in L2, not by
+    // its SMs (7x7 workload: 1.08 ms on 152 SMs, about the same on 127), so
+    // when the weight gradient's row blocks fit a quarter of the SMs it runs
+    // beside it, on a stream of its own, one CTA per row block on SMs the
+    // data kernel leaves free.  Measured: the backward call 1.21 -> 1.14 ms
+    // (7x7), 0.547 -> 0.473 ms (backbone 3x3); two CTAs per row block (fewer
+    // SMs for the data kernel) made the backbone slower again (0.590 ms).
+    const int wg_blocks = dcn::bwd_wgrad_row_blocks(p);
+    if (wg_blocks > 0 && wg_blocks * 4 <= h->sm_count) {
+        auto make_stream = [](cudaStream_t *out) {
+            return *out || cudaStreamCreateWithFlags(out, cudaStreamNonBlocking) == cudaSuccess;
+        };
+        auto make_event = [](cudaEvent_t *out) {
+            return *out || cudaEventCreateWithFlags(out, cudaEventDisableTiming) == cudaSuccess;
+        };
+        if (!make_stream(&h->s_wgrad) || !make_event(&h->ev_fork) || !make_event(&h->ev_join))
+            return DCN_ERR_CUDA;
+        if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
+            cudaStreamWaitEvent(h->s_wgrad, h->ev_fork, 0) != cudaSuccess)
+            return DCN_ERR_CUDA;
+        dcn::BwdParams pw = p;
+        pw.sm_count = wg_blocks;
+        dcn::BwdParams pd = p;
+        pd.sm_count = h->sm_count - wg_blocks;
+        const bool wg_ok = dcn::launch_bwd_wgrad_tc(pw, gmap, h->s_wgrad) == cudaSuccess;
+        const bool d_ok = dcn::launch_bwd_data_tc(pd, gmap, wmap, s) == cudaSuccess;
+        // the caller's stream waits for the weight gradient, whatever failed
+        const bool joined = cudaEventRecord(h->ev_join, h->s_wgrad) == cudaSuccess &&
+                            cudaStreamWaitEvent(s, h->ev_join, 0) == cudaSuccess;
+        if (!wg_ok || !d_ok || !joined) return DCN_ERR_CUDA;
+    } else {
+        if (dcn::launch_bwd_data_tc(p, gmap, wmap, s) != cudaSuccess) return DCN_ERR_CUDA;
+        if (dcn::launch_bwd_wgrad_tc(p, gmap, s) != cudaSuccess) return DCN_ERR_CUDA;
+    }
     if (grad_bias && dcn::launch_bwd_bias(p, dtype, s) != cudaSuccess) return DCN_ERR_CUDA;
     h->last_path = path;
     return DCN_OK;

@@ -362,6 +362,10 @@ PerDeviceValue<> g_wgrad_smem_set[2];
 
 }  // namespace
 
+int bwd_wgrad_row_blocks(const BwdParams &p) {
+    return (p.kh * p.kw * (p.C / WG_UNIT) + 1) / 2;
+}
+
 cudaError_t launch_bwd_wgrad_tc(const BwdParams &p, const CUtensorMap &gmap, cudaStream_t stream) {
     if (p.groups != 1 || p.C % WG_UNIT != 0 || p.O % 64 != 0 || p.O > 256 || p.O < 64 ||
         (p.C / p.ogroups) % WG_UNIT != 0)
@@ -379,9 +383,7 @@ cudaError_t launch_bwd_wgrad_tc(const BwdParams &p, const CUtensorMap &gmap, cud
         return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     }));
     if (e != cudaSuccess) return e;
-    const int taps = p.kh * p.kw;
-    const int units = taps * (p.C / WG_UNIT);
-    const int m_tiles = (units + 1) / 2;
+    const int m_tiles = bwd_wgrad_row_blocks(p);
     const int tiles = p.B * ((p.Ho + WG_TILE_H - 1) / WG_TILE_H) * ((p.Wo + WG_TILE_W - 1) / WG_TILE_W);
     // runs of tiles per row block: about one CTA per SM in all
     int splits = p.sm_count > m_tiles ? p.sm_count / m_tiles : 1;

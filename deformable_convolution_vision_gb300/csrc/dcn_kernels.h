@@ -183,7 +183,10 @@ cudaError_t launch_backward_weight(const BwdParams &p, int dtype, cudaStream_t s
 // sampled operand of each 128-pixel tile contracted with the grad_out tile
 // (`gmap`, the column-gradient kernel's map) in shared memory, fp32 in
 // tensor memory, added into grad_weight (which must be zeroed first).
+// The grid is (row blocks of 128 (tap, channel) rows) x (pixel ranges), the
+// ranges as many as p.sm_count allows (one at least).
 cudaError_t launch_bwd_wgrad_tc(const BwdParams &p, const CUtensorMap &gmap, cudaStream_t stream);
+int bwd_wgrad_row_blocks(const BwdParams &p);
 // grad_bias alone (column sums of grad_out).
 cudaError_t launch_bwd_bias(const BwdParams &p, int dtype, cudaStream_t stream);
 

@@ -331,7 +331,11 @@ DCN_API dcn_status_t dcn_forward_packed_ex(dcn_handle_t h,
  * 128-pixel tile of the sampled operand m * S (summed in fp32, rounded once
  * to the operand type) is contracted with the grad_out tile in shared
  * memory as soon as it is sampled, fp32 accumulation in tensor memory, no
- * TF32; the sampled operand is never written to memory.  Otherwise a
+ * TF32; the sampled operand is never written to memory.  When its blocks
+ * of 128 (tap, channel) rows number at most a quarter of the SMs it runs
+ * beside the column-gradient kernel, on a stream the handle owns that is
+ * forked from `stream` and joined back into it (the call stays ordered on
+ * `stream`; a handle is not used from two threads at once).  Otherwise a
  * CUDA-core kernel computes it in fp32.  The bias gradient runs on CUDA
  * cores.  Argument rules as
  * dcn_forward / dcn_forward_ex (sizes, NULL inputs, alignment to the
