@@ -111,6 +111,10 @@ TC_CASES = [
     # offsets of std 8: many corners land outside the kernel's grad_x window
     # around the tile (those go straight to grad_x), the rest inside it
     GW("bwdtc_far_offsets", 2, 128, 40, 36, 64, 3, 3, (1, 1), (1, 1), (1, 1), 1, 1, "bf16", 8.0, True, 37),
+    # 49 x 2 (tap, 64-channel) units: more weight-gradient row blocks than a
+    # quarter of the SMs, so the weight gradient runs after the data kernel
+    # instead of beside it (the cases above take the side-by-side path)
+    GW("bwdtc_7x7_c128", 1, 128, 21, 19, 64, 7, 7, (1, 1), (3, 3), (1, 1), 1, 1, "bf16", 2.0, True, 38),
 ]
 
 
