@@ -62,8 +62,8 @@ def run_backward(wl, inp, gout, path=dcn.DCN_PATH_AUTO):
     return r
 
 
-def check(wl, path=dcn.DCN_PATH_AUTO):
-    inp = make_general_inputs(wl)
+def check(wl, path=dcn.DCN_PATH_AUTO, inp=None):
+    inp = make_general_inputs(wl) if inp is None else inp
     gout = _cotangent(wl, inp["x"].dtype, wl.seed + 1000)
     got = run_backward(wl, inp, gout, path)
     conv = oracle.ConvDesc(stride=wl.stride, padding=wl.padding, dilation=wl.dilation,
@@ -127,6 +127,24 @@ def test_backward_both_paths(wl, path):
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
 def test_backward_matches_oracle(wl):
     check(wl)
+
+
+@pytest.mark.parametrize("path", [dcn.DCN_PATH_TC, dcn.DCN_PATH_SIMT])
+def test_backward_nonfinite_offsets(path):
+    """Offsets that are NaN, infinite or huge put the sampling coordinate
+    outside the image (the kernels clamp it, the oracle's corner tests
+    reject it): those taps add nothing to any gradient, nothing is read or
+    written out of bounds, and every gradient matches the oracle."""
+    wl = GW("bwd_nonfinite", 1, 64, 12, 14, 64, 3, 3, (1, 1), (1, 1), (1, 1), 1, 1, "bf16", 2.0,
+            True, 39)
+    inp = make_general_inputs(wl)
+    off = inp["offset"]
+    off[:, 0, :3] = float("nan")
+    off[:, 3, 3:6] = float("inf")
+    off[:, 5, 6:9] = -float("inf")
+    off[:, 7, 9:] = 3e38
+    off[:, 10, :, :4] = -1e30
+    check(wl, path=path, inp=inp)
 
 
 def test_backward_all_outside():
