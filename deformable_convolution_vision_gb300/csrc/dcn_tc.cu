@@ -99,16 +99,12 @@ static_assert(TC_TABLE_SLOTS == 4 && TC_TAP_GROUP == 2, "ring index arithmetic a
 // index and limit sit in a second array.
 constexpr int TC_ENTRY_ARRAY_BYTES = TC_TILE_W * 16;
 __host__ __device__ constexpr int table_buf_bytes(bool f32) { return (f32 ? 2 : 1) * TC_ENTRY_ARRAY_BYTES; }
-// raw geometry inputs of a warp: dy, dx and m planes of 32 lanes each
-// (each cp.async of the warp writes 128 contiguous bytes: no bank conflicts)
-constexpr int TC_RAW_WARP_BYTES = 3 * 32 * 4;
 
 struct TcLayout {
     int stages;
     int b_bytes;       // O * 128: one weight K-block
     int bar_off;       // barriers after the stages
     int table_off;     // per-warp corner tables
-    int raw_off;       // per-warp raw geometry inputs, dy, dx and mask planes
     int vt_off;        // virtual-tap table, int4 per (tap, offset group)
     int bias_off;      // the bias, fp32 per output channel (zero without one)
     int total;         // bytes used from the 1024-aligned base
@@ -122,8 +118,7 @@ __host__ __device__ inline TcLayout tc_layout(int O, int stages, bool f32, int v
     // full[stages], empty[stages], acc_full[2], acc_free[2], tmem slot (8 bytes each)
     L.table_off = L.bar_off + (2 * stages + 5) * 8;
     L.table_off = (L.table_off + 15) & ~15;
-    L.raw_off = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_SLOTS * table_buf_bytes(f32);
-    L.vt_off = L.raw_off + TC_SAMPLER_WARPS * TC_RAW_WARP_BYTES;
+    L.vt_off = L.table_off + TC_SAMPLER_WARPS * TC_TABLE_SLOTS * table_buf_bytes(f32);
     L.bias_off = L.vt_off + vtaps * 16;
     L.total = L.bias_off + O * 4;
     return L;
@@ -351,7 +346,6 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         const int trow = 2 * q + half;                   // its tile row = A rows 16 trow .. +15
         const uint16_t *__restrict__ x = static_cast<const uint16_t *>(p.x);   // 16-bit elements
         const uint32_t table_s = smem_u32(smem + L.table_off + sw * TC_TABLE_SLOTS * kBuf);
-        const uint32_t raw_s = smem_u32(smem + L.raw_off + sw * TC_RAW_WARP_BYTES) + lane * 4;
         const uint32_t vt_s = smem_u32(smem + L.vt_off);
         const uint32_t a_lane = static_cast<uint32_t>(16 * trow) << 16;
         const int plane = p.plane;                       // offset / mask plane stride
@@ -368,8 +362,6 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
         // element steps from a sample block's slot (0,0) to slots (0,1) and (1,0)
         const int step_x = p.W > 1 ? p.x_cstride : 0;
         const int step_y = p.H > 1 ? p.W * p.x_cstride : 0;
-        // without a mask the lane's m word holds 1 for good (nothing copies over it)
-        if (p.mask == nullptr) sts_b32(raw_s + 256, __float_as_uint(1.0f));
         bool ok = true;
         int s = team;                   // this warp's stages: team, team + TC_TEAMS, ...
         uint32_t phase = 0;
@@ -508,9 +500,9 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 int r_vt;
                 int r_cb = walk_split(kb_first + TC_TEAMS * my_g, vtaps, vt_rcp, r_vt);
                 // Raw inputs (dy, dx, mask) of the lane's next walk position
-                // (its first when `first`) for its pixel, copied ahead of their
-                // use into the lane's raw slot (asynchronously: no registers
-                // held while in flight).
+                // (its first when `first`) for its pixel, loaded into
+                // registers a pair ahead of their use.
+                float r_dy = 0.0f, r_dx = 0.0f, r_m = 0.0f;
                 auto load_raw = [&](bool first) {
                     if (!first) {
                         r_vt += 2 * TC_TEAMS;
@@ -519,21 +511,17 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     const bool valid = my_valid && r_cb < vncb;                  // j < nkb
                     const int mc = lds_s32(vt_s + r_vt * 16 + 8);   // mask plane; offsets 2mc, 2mc + 1
                     const float *o = off_img + (2 * mc * plane + my_hw);
+                    const float *mp = mask_img + (mc * plane + my_hw);
 #ifdef DCN_CHECK_BOUNDS
-                    // an offset or mask outside its tensor is not fetched (zero)
-                    const bool v_dy = valid && in_bounds(o, 4, p.off_lo, p.off_hi, p.status);
-                    const bool v_dx = valid && in_bounds(o + plane, 4, p.off_lo, p.off_hi, p.status);
-                    cp_async_4(raw_s, v_dy ? o : p.offset, v_dy);
-                    cp_async_4(raw_s + 128, v_dx ? o + plane : p.offset, v_dx);
-                    if (p.mask) {
-                        const float *mp = mask_img + (mc * plane + my_hw);
-                        const bool v_m = valid && in_bounds(mp, 4, p.mask_lo, p.mask_hi, p.status);
-                        cp_async_4(raw_s + 256, v_m ? mp : p.mask, v_m);
-                    }
+                    // an offset or mask outside its tensor is not read (zero)
+                    r_dy = valid && in_bounds(o, 4, p.off_lo, p.off_hi, p.status) ? __ldg(o) : 0.0f;
+                    r_dx = valid && in_bounds(o + plane, 4, p.off_lo, p.off_hi, p.status) ? __ldg(o + plane) : 0.0f;
+                    r_m = !p.mask ? 1.0f
+                          : (valid && in_bounds(mp, 4, p.mask_lo, p.mask_hi, p.status) ? __ldg(mp) : 0.0f);
 #else
-                    cp_async_4(raw_s, o, valid);
-                    cp_async_4(raw_s + 128, o + plane, valid);
-                    if (p.mask) cp_async_4(raw_s + 256, mask_img + (mc * plane + my_hw), valid);
+                    r_dy = valid ? __ldg(o) : 0.0f;
+                    r_dx = valid ? __ldg(o + plane) : 0.0f;
+                    r_m = !p.mask ? 1.0f : (valid ? __ldg(mp) : 0.0f);
 #endif
                 };
                 // The table entry of the last loaded walk position for this
@@ -544,8 +532,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 // the last 16 instead).  A position past the last one gets an
                 // entry that is never read.
                 auto tabulate = [&](int slot) {
-                    cp_async_wait_all();
-                    const float dy = lds_f32(raw_s), dx = lds_f32(raw_s + 128), m = lds_f32(raw_s + 256);
+                    const float dy = r_dy, dx = r_dx, m = r_m;
                     const int4 e = lds_v4_s32_m(vt_s + r_vt * 16);
                     TapBlock t;
                     tap_block(dy, dx, m, y_base + e.x, x_base + e.y, tb, p.H, p.W, p.x_cstride, t);
@@ -721,9 +708,6 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                     if (jj + 3 >= n) break;
                     if (!step(jj + 3, 3, v_odd)) { ok = false; break; }
                 }
-                // raw copies issued for taps past the segment's end must land
-                // before the next segment reuses the raw slot
-                cp_async_wait_all();
             }
 
           }
