@@ -503,13 +503,15 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 // (its first when `first`) for its pixel, loaded into
                 // registers a pair ahead of their use.
                 float r_dy = 0.0f, r_dx = 0.0f, r_m = 0.0f;
+                int4 r_e = make_int4(0, 0, 0, 0);   // the position's virtual-tap entry
                 auto load_raw = [&](bool first) {
                     if (!first) {
                         r_vt += 2 * TC_TEAMS;
                         while (r_vt >= vtaps) { r_vt -= vtaps; ++r_cb; }
                     }
                     const bool valid = my_valid && r_cb < vncb;                  // j < nkb
-                    const int mc = lds_s32(vt_s + r_vt * 16 + 8);   // mask plane; offsets 2mc, 2mc + 1
+                    r_e = lds_v4_s32_m(vt_s + r_vt * 16);
+                    const int mc = r_e.z;                            // mask plane; offsets 2mc, 2mc + 1
                     const float *o = off_img + (2 * mc * plane + my_hw);
                     const float *mp = mask_img + (mc * plane + my_hw);
 #ifdef DCN_CHECK_BOUNDS
@@ -533,7 +535,7 @@ dcn_tc_kernel(const __grid_constant__ CUtensorMap wmap, Params p, int stages) {
                 // entry that is never read.
                 auto tabulate = [&](int slot) {
                     const float dy = r_dy, dx = r_dx, m = r_m;
-                    const int4 e = lds_v4_s32_m(vt_s + r_vt * 16);
+                    const int4 e = r_e;
                     TapBlock t;
                     tap_block(dy, dx, m, y_base + e.x, x_base + e.y, tb, p.H, p.W, p.x_cstride, t);
                     const int c0 = e.w + r_cb * TC_BK;
