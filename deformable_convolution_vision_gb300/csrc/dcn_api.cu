@@ -566,6 +566,21 @@ static dcn_status_t backward_general(dcn_handle_t h, const void *x, const float 
     p.status = h->status;
     p.timeout_ns = kWaitLimitNs;
     p.f16 = dtype == DCN_F16 ? 1 : 0;
+#ifdef DCN_CHECK_BOUNDS
+    {
+        auto range = [](const void *base, size_t bytes, const void *&lo, const void *&hi) {
+            lo = base;
+            hi = base ? static_cast<const char *>(base) + bytes : nullptr;
+        };
+        range(x, static_cast<size_t>(d.B) * d.H * d.W * d.C * es, p.x_lo, p.x_hi);
+        range(offset, bytes[1], p.off_lo, p.off_hi);
+        range(mask, bytes[2], p.mask_lo, p.mask_hi);
+        range(grad_x, bytes[0], p.gx_lo, p.gx_hi);
+        range(grad_offset, bytes[1], p.goff_lo, p.goff_hi);
+        range(grad_mask, bytes[2], p.gmask_lo, p.gmask_hi);
+        range(grad_weight, bytes[3], p.gw_lo, p.gw_hi);
+    }
+#endif
 
     // the column gradient on tensor cores where the shape allows it
     const bool tc_ok = tc_dtype(dtype) &&

@@ -42,6 +42,15 @@ namespace dcn {
 
 namespace {
 
+// Bounds-checked builds check each global access of the kernels below
+// against its tensor's byte range (recording a miss in the status word and
+// skipping the access); other builds take every access as it is.
+#ifdef DCN_CHECK_BOUNDS
+#define BWD_IN(ptr, bytes, lo, hi) in_bounds((ptr), (bytes), (lo), (hi), p.status)
+#else
+#define BWD_IN(ptr, bytes, lo, hi) true
+#endif
+
 constexpr int BT_BM = 128;                  // pixels per tile (MMA M)
 constexpr int BT_BN = 64;                   // channels per unit (MMA N)
 constexpr int BT_BK = 64;                   // outputs per K-block
@@ -254,9 +263,12 @@ dcn_bwd_data_tc_kernel(const __grid_constant__ CUtensorMap gmap,
                     if (valid) {
                         hw = static_cast<size_t>(oh) * p.Wo + ow;
                         bq = static_cast<size_t>(tb) * p.ogroups + q_off;
-                        const float dy = __ldg(p.offset + (bq * 2 * taps + 2 * tap) * HoWo + hw);
-                        const float dx = __ldg(p.offset + (bq * 2 * taps + 2 * tap + 1) * HoWo + hw);
-                        m = p.mask ? __ldg(p.mask + (bq * taps + tap) * HoWo + hw) : 1.0f;
+                        const float *pdy = p.offset + (bq * 2 * taps + 2 * tap) * HoWo + hw;
+                        const float *pdx = pdy + HoWo;
+                        const float *pm = p.mask ? p.mask + (bq * taps + tap) * HoWo + hw : nullptr;
+                        const float dy = BWD_IN(pdy, 4, p.off_lo, p.off_hi) ? __ldg(pdy) : 0.0f;
+                        const float dx = BWD_IN(pdx, 4, p.off_lo, p.off_hi) ? __ldg(pdx) : 0.0f;
+                        m = !pm ? 1.0f : (BWD_IN(pm, 4, p.mask_lo, p.mask_hi) ? __ldg(pm) : 0.0f);
                         float py = static_cast<float>(oh * p.sh - p.ph + i * p.dh) + dy;
                         float pxf = static_cast<float>(ow * p.sw - p.pw + j * p.dw) + dx;
                         py = fminf(fmaxf(py, -2.0f), static_cast<float>(p.H + 1));
@@ -276,7 +288,7 @@ dcn_bwd_data_tc_kernel(const __grid_constant__ CUtensorMap gmap,
                             in[k] = static_cast<unsigned>(yy) < static_cast<unsigned>(p.H) &&
                                     static_cast<unsigned>(xx) < static_cast<unsigned>(p.W);
                             cidx[k] = in[k] ? (static_cast<size_t>((tb * p.H + yy) * p.W + xx)) * p.C + c0 : 0;
-                            if (in[k]) {
+                            if (in[k] && BWD_IN(x + cidx[k], 32, p.x_lo, p.x_hi)) {
                                 raw[k] = ldg_v8(x + cidx[k]);
                             } else {
 #pragma unroll
@@ -312,7 +324,7 @@ dcn_bwd_data_tc_kernel(const __grid_constant__ CUtensorMap gmap,
                             }
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                if (in[k])
+                                if (in[k] && BWD_IN(p.grad_x + cidx[k] + 4 * e4, 16, p.gx_lo, p.gx_hi))
                                     red_add_v4_f32(p.grad_x + cidx[k] + 4 * e4, sc[k][0], sc[k][1],
                                                    sc[k][2], sc[k][3]);
                         }
@@ -325,9 +337,14 @@ dcn_bwd_data_tc_kernel(const __grid_constant__ CUtensorMap gmap,
                     gdy += __shfl_xor_sync(0xffffffffu, gdy, 2);
                     gdx += __shfl_xor_sync(0xffffffffu, gdx, 2);
                     if (valid && quart == 0) {
-                        atomicAdd(p.grad_offset + (bq * 2 * taps + 2 * tap) * HoWo + hw, gdy * m);
-                        atomicAdd(p.grad_offset + (bq * 2 * taps + 2 * tap + 1) * HoWo + hw, gdx * m);
-                        if (p.grad_mask) atomicAdd(p.grad_mask + (bq * taps + tap) * HoWo + hw, gm);
+                        float *gdy_p = p.grad_offset + (bq * 2 * taps + 2 * tap) * HoWo + hw;
+                        float *gdx_p = gdy_p + HoWo;
+                        if (BWD_IN(gdy_p, 4, p.goff_lo, p.goff_hi)) atomicAdd(gdy_p, gdy * m);
+                        if (BWD_IN(gdx_p, 4, p.goff_lo, p.goff_hi)) atomicAdd(gdx_p, gdx * m);
+                        if (p.grad_mask) {
+                            float *gm_p = p.grad_mask + (bq * taps + tap) * HoWo + hw;
+                            if (BWD_IN(gm_p, 4, p.gmask_lo, p.gmask_hi)) atomicAdd(gm_p, gm);
+                        }
                     }
                 }
             }

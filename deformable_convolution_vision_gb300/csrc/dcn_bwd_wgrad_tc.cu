@@ -45,6 +45,16 @@ namespace dcn {
 
 namespace {
 
+// Bounds-checked builds check each global access of the kernel below
+// against its tensor's byte range (recording a miss in the status word and
+// skipping the access, or reading a safe address instead); other builds
+// take every access as it is.
+#ifdef DCN_CHECK_BOUNDS
+#define WG_IN(ptr, bytes, lo, hi) in_bounds((ptr), (bytes), (lo), (hi), p.status)
+#else
+#define WG_IN(ptr, bytes, lo, hi) true
+#endif
+
 constexpr int WG_UNIT = 64;                 // channels per unit (one 128-byte row)
 constexpr int WG_BM = 2 * WG_UNIT;          // (tap, channel) rows per CTA (MMA M)
 constexpr int WG_TILE_W = 16, WG_TILE_H = 8;
@@ -242,10 +252,16 @@ dcn_bwd_wgrad_tc_kernel(const __grid_constant__ CUtensorMap gmap, BwdParams p, i
             const bool valid = oh < p.Ho && ow < p.Wo && 2 * mt + my_g < units;
             const size_t hw = valid ? static_cast<size_t>(oh) * p.Wo + ow : 0;
             const float *o = p.offset + (static_cast<size_t>(tb) * p.ogroups * taps * 2 + 2 * plane_g) * HoWo + hw;
-            cp_async_4(raw_s, o, valid);
-            cp_async_4(raw_s + 128, o + HoWo, valid);
-            if (p.mask)
-                cp_async_4(raw_s + 256, p.mask + (static_cast<size_t>(tb) * p.ogroups * taps + plane_g) * HoWo + hw, valid);
+            // an offset or mask outside its tensor is not fetched (zero)
+            const bool v_dy = valid && WG_IN(o, 4, p.off_lo, p.off_hi);
+            const bool v_dx = valid && WG_IN(o + HoWo, 4, p.off_lo, p.off_hi);
+            cp_async_4(raw_s, v_dy ? o : p.offset, v_dy);
+            cp_async_4(raw_s + 128, v_dx ? o + HoWo : p.offset, v_dx);
+            if (p.mask) {
+                const float *mp = p.mask + (static_cast<size_t>(tb) * p.ogroups * taps + plane_g) * HoWo + hw;
+                const bool v_m = valid && WG_IN(mp, 4, p.mask_lo, p.mask_hi);
+                cp_async_4(raw_s + 256, v_m ? mp : p.mask, v_m);
+            }
         };
         auto tabulate = [&](int tile) {
             int tb, oh, ow;
@@ -284,10 +300,21 @@ dcn_bwd_wgrad_tc_kernel(const __grid_constant__ CUtensorMap gmap, BwdParams p, i
                     wgt[px] = lds_v4_f32(ent);
                     const int e0 = lds_s32(ent + WG_TILE_W * 16) + cbase[g];
                     const int e1 = e0 + step_x, e2 = e0 + step_y, e3 = e2 + step_x;
+#ifdef DCN_CHECK_BOUNDS
+                    // a corner row outside x is read from x's first bytes instead
+                    auto chk = [&](const uint16_t *a) {
+                        return WG_IN(a, 32, p.x_lo, p.x_hi) ? a : static_cast<const uint16_t *>(p.x_lo);
+                    };
+                    v[4 * px + 0] = ldg_v8(chk(x + e0));
+                    v[4 * px + 1] = ldg_v8(chk(x + e1));
+                    v[4 * px + 2] = ldg_v8(chk(x + e2));
+                    v[4 * px + 3] = ldg_v8(chk(x + e3));
+#else
                     v[4 * px + 0] = ldg_v8(x + e0);
                     v[4 * px + 1] = ldg_v8(x + e1);
                     v[4 * px + 2] = ldg_v8(x + e2);
                     v[4 * px + 3] = ldg_v8(x + e3);
+#endif
                 }
 #pragma unroll
                 for (int px = 0; px < 2; ++px) {
@@ -341,7 +368,8 @@ dcn_bwd_wgrad_tc_kernel(const __grid_constant__ CUtensorMap gmap, BwdParams p, i
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int o = ch * 16 + e;
-                        atomicAdd(p.grad_weight + (static_cast<size_t>(o) * p.C + c) * taps + tap, vv[e]);
+                        float *gw = p.grad_weight + (static_cast<size_t>(o) * p.C + c) * taps + tap;
+                        if (WG_IN(gw, 4, p.gw_lo, p.gw_hi)) atomicAdd(gw, vv[e]);
                     }
                 }
             }

@@ -147,6 +147,12 @@ struct BwdParams {
     unsigned *status;       // device status word (timeout bit)
     unsigned long long timeout_ns;
     int f16;                // 1: fp16 operands, 0: bf16
+#ifdef DCN_CHECK_BOUNDS
+    // bounds-checked builds: the byte ranges of the tensors the tensor-core
+    // backward kernels read and add into
+    const void *x_lo, *x_hi, *off_lo, *off_hi, *mask_lo, *mask_hi;
+    const void *gx_lo, *gx_hi, *goff_lo, *goff_hi, *gmask_lo, *gmask_hi, *gw_lo, *gw_hi;
+#endif
 };
 
 // Channel order of the tensor-core backward's weight operand inside each

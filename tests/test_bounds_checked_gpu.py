@@ -1,4 +1,4 @@
-"""The forward and sampling-operator parity suites against the
+"""The forward, backward and sampling-operator parity suites against the
 bounds-checked build.
 
 compute-sanitizer is closed on this machine, so this stands in for its memory
@@ -7,7 +7,11 @@ DCN_CHECK_BOUNDS.  In it the convolution's forward kernels (tensor-core and
 CUDA-core) check every corner load, offset and mask fetch, and output store
 against the byte ranges of the caller's tensors; an access outside is
 skipped and raises a status bit that dcn_sync_status reports as
-DCN_ERR_BOUNDS.  The multi-scale and single-scale sampling kernels,
+DCN_ERR_BOUNDS.  The convolution's tensor-core backward kernels (the column
+gradient with its scatter, and the weight gradient) check the same way
+every offset, mask and corner load and every reduction into grad_x,
+grad_offset, grad_mask and grad_weight; the CUDA-core backward kernels are
+not instrumented.  The multi-scale and single-scale sampling kernels,
 forward and backward, check every corner-row load of the value tensor and
 every reduction into the value gradient; their entry points take no handle,
 so a thread that meets an access outside writes NaN into every output it
@@ -29,6 +33,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_parity_gpu.py", "tests/test_parity_general_gpu.py",
           "tests/test_parity_channels_gpu.py", "tests/test_parity_f16_gpu.py",
           "tests/test_abi_gpu.py", "tests/test_zz_no_alloc.py",
+          "tests/test_backward_gpu.py", "tests/test_backward_full_gpu.py",
           "tests/test_msda_gpu.py", "tests/test_msda_backward_gpu.py",
           "tests/test_attn_gpu.py", "tests/test_attn_backward_gpu.py"]
 
