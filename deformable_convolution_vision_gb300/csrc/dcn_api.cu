@@ -14,6 +14,7 @@
 
 #include "dcn.h"
 #include "dcn_device.cuh"
+#include "dcn_backward.h"
 #include "dcn_kernels.h"
 #include "dcn_limits.h"
 #include "dcn_sampling_ops.h"

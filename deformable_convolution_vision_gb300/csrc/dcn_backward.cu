@@ -36,6 +36,7 @@
 #include <cstring>
 
 #include "dcn_device.cuh"
+#include "dcn_backward.h"
 #include "dcn_kernels.h"
 
 namespace dcn {

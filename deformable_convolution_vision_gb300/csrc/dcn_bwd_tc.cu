@@ -36,6 +36,7 @@
 
 #include "dcn_attr_cache.h"
 #include "dcn_device.cuh"
+#include "dcn_backward.h"
 #include "dcn_kernels.h"
 
 namespace dcn {

@@ -38,6 +38,7 @@
 
 #include "dcn_attr_cache.h"
 #include "dcn_device.cuh"
+#include "dcn_backward.h"
 #include "dcn_kernels.h"
 #include "dcn_sampling.cuh"
 
