@@ -74,3 +74,30 @@ def test_reference_arm_stays_within_its_budget():
     # few steps keep the full per-step sample
     a = argparse.Namespace(steps=20, warmup=3, reference_step_seconds=2.0, reference_budget_seconds=120.0)
     assert bench.reference_step_seconds(a) == 2.0
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line in the bench contract's form, on the same workload
+    description and metric as the GPU arm."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "decoder3x3",
+                        "--steps", "2", "--warmup", "3", "--reference-budget-seconds", "1"],
+                       cwd=root, capture_output=True, text=True, timeout=300,
+                       env={k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE")})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    wl = WORKLOADS["decoder3x3"]
+    assert d["config"] == bench.config_dict(wl, bench.L2_NOTE)
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
