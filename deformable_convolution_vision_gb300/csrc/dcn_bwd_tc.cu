@@ -323,9 +323,11 @@ dcn_bwd_data_tc_kernel(const __grid_constant__ CUtensorMap gmap,
                                 sc[2][t] = gmm * wy[1] * wx[0];
                                 sc[3][t] = gmm * wy[1] * wx[1];
                             }
+                            // (a tap whose mask is exactly 0 adds nothing to grad_x:
+                            // its reductions are skipped)
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                if (in[k] && BWD_IN(p.grad_x + cidx[k] + 4 * e4, 16, p.gx_lo, p.gx_hi))
+                                if (in[k] && m != 0.0f && BWD_IN(p.grad_x + cidx[k] + 4 * e4, 16, p.gx_lo, p.gx_hi))
                                     red_add_v4_f32(p.grad_x + cidx[k] + 4 * e4, sc[k][0], sc[k][1],
                                                    sc[k][2], sc[k][3]);
                         }
